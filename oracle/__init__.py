@@ -1,0 +1,218 @@
+"""fp64 CPU oracle of the tensor-parallel Transformer MLP block.
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline / reference leg import this package.  It shares no
+code with the CUDA path: the arithmetic lives in ``tpmlp_oracle.c`` (plain
+loops, double precision, inputs widened exactly from bfloat16) and this
+module only converts tensors and calls it.
+
+Definitions followed (see the C source for the formulas): "Megatron-LM:
+Tensor Model Parallel" (charles2530.github.io), section "MLP: Column
+Parallel first, then Row Parallel" (Figure 3a) and section "f / g Operators"
+(Figure 4); GeLU is the tanh approximation (the pages name GeLU without
+defining it).
+
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
+(brute force against float64 numpy matmul, GeLU closed forms and values,
+finite differences, the shard-partition invariant, special cases); the pages
+print no worked numeric example, so no value here is pinned to the pages'
+own numbers.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+from . import build as _build
+
+class Oracle:
+    """Calls into one build of the oracle library (the default one, or a
+    mutated copy that the tests compile to check that the pins bite)."""
+
+    def __init__(self, path: str | None = None):
+        L = ctypes.CDLL(path or _build.build())
+        dp = ctypes.POINTER(ctypes.c_double)
+        up = ctypes.POINTER(ctypes.c_uint16)
+        lp = ctypes.POINTER(ctypes.c_long)
+        cl = ctypes.c_long
+        L.orc_gelu.argtypes = [ctypes.c_double]
+        L.orc_gelu.restype = ctypes.c_double
+        L.orc_gelu_grad.argtypes = [ctypes.c_double]
+        L.orc_gelu_grad.restype = ctypes.c_double
+        L.orc_forward.argtypes = [dp] * 6 + [cl] * 4 + [dp] * 3
+        L.orc_backward.argtypes = [dp] * 5 + [cl] * 4 + [dp] * 5
+        L.orc_forward_rows_bf16.argtypes = [up] * 6 + [cl] * 4 + [lp, cl] + [dp] * 3
+        L.orc_backward_rows_bf16.argtypes = [up] * 5 + [cl] * 4 + [lp, cl, dp]
+        L.orc_backward_cols_bf16.argtypes = [up] * 5 + [cl] * 4 + [lp, cl] + [dp] * 3
+        L.orc_db2_bf16.argtypes = [up, cl, cl, dp]
+        for name in ("orc_forward", "orc_backward", "orc_forward_rows_bf16",
+                     "orc_backward_rows_bf16", "orc_backward_cols_bf16", "orc_db2_bf16",
+                     "orc_num_threads"):
+            getattr(L, name).restype = ctypes.c_int
+        self.L = L
+
+    def num_threads(self) -> int:
+        return int(self.L.orc_num_threads())
+
+    def gelu(self, x: float) -> float:
+        return float(self.L.orc_gelu(float(x)))
+
+    def gelu_grad(self, x: float) -> float:
+        return float(self.L.orc_gelu_grad(float(x)))
+
+    def forward(self, X, A, b1, B, b2, R, t: int):
+        """Y, Z, H (float64 numpy) of the block with t shards."""
+        X, A, b1, B, b2, R = (_f64(v) for v in (X, A, b1, B, b2, R))
+        T, h = X.shape
+        F = A.shape[1]
+        Y = np.zeros((T, h))
+        Z = np.zeros((T, F))
+        H = np.zeros((T, F))
+        _check(self.L.orc_forward(_dp(X), _dp(A), _dp(b1), _dp(B), _dp(b2), _dp(R), T, h, F, t,
+                                  _dp(Y), _dp(Z), _dp(H)), "forward")
+        return Y, Z, H
+
+    def backward(self, dY, X, A, b1, B, t: int):
+        """dX, dA, dB, db1, db2 (float64 numpy) of the block with t shards."""
+        dY, X, A, b1, B = (_f64(v) for v in (dY, X, A, b1, B))
+        T, h = X.shape
+        F = A.shape[1]
+        dX = np.zeros((T, h))
+        dA = np.zeros((h, F))
+        dB = np.zeros((F, h))
+        db1 = np.zeros(F)
+        db2 = np.zeros(h)
+        _check(self.L.orc_backward(_dp(dY), _dp(X), _dp(A), _dp(b1), _dp(B), T, h, F, t,
+                                   _dp(dX), _dp(dA), _dp(dB), _dp(db1), _dp(db2)), "backward")
+        return dX, dA, dB, db1, db2
+
+    def forward_rows(self, inp: dict, t: int, rows):
+        """Y, Z, H restricted to the given token rows, from bf16 CPU tensors."""
+        X, A, b1, B, b2, R = (_u16(inp[k]) for k in ("X", "A", "b1", "B", "b2", "residual"))
+        T, h = inp["X"].shape
+        F = inp["A"].shape[1]
+        rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        n = len(rows)
+        Y = np.zeros((n, h))
+        Z = np.zeros((n, F))
+        H = np.zeros((n, F))
+        _check(self.L.orc_forward_rows_bf16(_up(X), _up(A), _up(b1), _up(B), _up(b2), _up(R),
+                                            T, h, F, t, _lp(rows), n, _dp(Y), _dp(Z), _dp(H)),
+               "forward_rows")
+        return Y, Z, H
+
+    def backward_rows(self, inp: dict, t: int, rows):
+        """dX restricted to the given token rows, from bf16 CPU tensors."""
+        dY, X, A, b1, B = (_u16(inp[k]) for k in ("dY", "X", "A", "b1", "B"))
+        T, h = inp["X"].shape
+        F = inp["A"].shape[1]
+        rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        n = len(rows)
+        dX = np.zeros((n, h))
+        _check(self.L.orc_backward_rows_bf16(_up(dY), _up(X), _up(A), _up(b1), _up(B),
+                                             T, h, F, t, _lp(rows), n, _dp(dX)), "backward_rows")
+        return dX
+
+    def backward_cols(self, inp: dict, t: int, cols):
+        """dA[:, cols] ([h, n]), dB[cols, :] ([n, h]) and db1[cols] from bf16 CPU tensors."""
+        dY, X, A, b1, B = (_u16(inp[k]) for k in ("dY", "X", "A", "b1", "B"))
+        T, h = inp["X"].shape
+        F = inp["A"].shape[1]
+        cols = np.ascontiguousarray(np.asarray(cols, dtype=np.int64))
+        n = len(cols)
+        dA = np.zeros((h, n))
+        dB = np.zeros((n, h))
+        db1 = np.zeros(n)
+        _check(self.L.orc_backward_cols_bf16(_up(dY), _up(X), _up(A), _up(b1), _up(B),
+                                             T, h, F, t, _lp(cols), n, _dp(dA), _dp(dB),
+                                             _dp(db1)), "backward_cols")
+        return dA, dB, db1
+
+    def db2(self, dY) -> np.ndarray:
+        """Column sums of dY from a bf16 CPU tensor."""
+        T, h = dY.shape
+        d = _u16(dY)
+        out = np.zeros(h)
+        _check(self.L.orc_db2_bf16(_up(d), T, h, _dp(out)), "db2")
+        return out
+
+
+def _f64(x) -> np.ndarray:
+    """Exact widening to a contiguous float64 numpy array."""
+    if isinstance(x, torch.Tensor):
+        x = x.detach().to("cpu", torch.float64).numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _u16(x: torch.Tensor) -> np.ndarray:
+    """Raw bfloat16 bit patterns of a CPU tensor."""
+    assert x.dtype == torch.bfloat16
+    return np.ascontiguousarray(x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def _dp(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _up(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16))
+
+
+def _lp(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_long))
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise ValueError(f"oracle {what} failed with status {rc}")
+
+
+_default = None
+
+
+def default() -> Oracle:
+    """The oracle built from the committed source."""
+    global _default
+    if _default is None:
+        _default = Oracle()
+    return _default
+
+
+def gelu(x):
+    return default().gelu(x)
+
+
+def gelu_grad(x):
+    return default().gelu_grad(x)
+
+
+def forward(*a, **k):
+    return default().forward(*a, **k)
+
+
+def backward(*a, **k):
+    return default().backward(*a, **k)
+
+
+def forward_rows(*a, **k):
+    return default().forward_rows(*a, **k)
+
+
+def backward_rows(*a, **k):
+    return default().backward_rows(*a, **k)
+
+
+def backward_cols(*a, **k):
+    return default().backward_cols(*a, **k)
+
+
+def db2(dY):
+    return default().db2(dY)
+
+
+def num_threads() -> int:
+    return default().num_threads()

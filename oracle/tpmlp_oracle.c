@@ -1,0 +1,415 @@
+/*
+ * tpmlp_oracle.c -- plain, slow fp64 CPU oracle of the tensor-parallel
+ * Transformer MLP block, forward and backward.
+ *
+ * TEST INFRASTRUCTURE.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg load this library.  It shares no code, header
+ * or constant with the CUDA path, and the product path never calls it.
+ *
+ * What it computes (row-major matrices, T tokens, hidden h, FFN width F,
+ * t shards of width f = F / t):
+ *
+ *   shard i owns A_i = A[:, i f:(i+1) f], b1_i, B_i = B[i f:(i+1) f, :]
+ *   Z_i = X A_i + b1_i                 column-parallel first GEMM
+ *   H_i = GeLU(Z_i)                    local nonlinearity, no sync before it
+ *   Y   = sum_i H_i B_i + b2 + R       row-parallel partials, the g-operator
+ *                                      sum, then bias and residual
+ *
+ * following "Megatron-LM: Tensor Model Parallel" (charles2530.github.io),
+ * section "MLP: Column Parallel first, then Row Parallel" (Figure 3a) and
+ * section "f / g Operators" (Figure 4: g is a sum in the forward pass and the
+ * identity in the backward pass; f is the identity forward and a sum
+ * backward).  The backward pass is the chain rule of the same formula:
+ *
+ *   dH_i = dY B_i^T ;  dZ_i = dH_i * GeLU'(Z_i)
+ *   dB_i = H_i^T dY ;  dA_i = X^T dZ_i ;  db1_i = sum_rows dZ_i
+ *   dX   = sum_i dZ_i A_i^T            the f-operator sum
+ *   db2  = sum_rows dY                 (d residual = dY, not returned)
+ *
+ * Readings where the pages are silent:
+ *  - GeLU is named but never defined on the pages; the tanh approximation
+ *    0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))) is used.
+ *  - The pages' MLP has no biases.  b1 is split with A's columns (it must be
+ *    added before the local GeLU); b2 and the residual are added once, after
+ *    the shard sum.
+ *  - Nothing is rounded: inputs are widened exactly to double and every
+ *    intermediate stays double.  The oracle recomputes Z and H itself in the
+ *    backward pass.
+ *
+ * Each shard's partial product is formed on its own and then added to the
+ * running sum, exactly as the pages' per-rank computation followed by the
+ * all-reduce.  Loops are plain; OpenMP only splits independent output rows
+ * or columns across threads, never a sum.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_OK 0
+#define ORC_ERR_SHAPE 2
+#define ORC_ERR_ALLOC 8
+
+static double gelu_c(void) { return sqrt(2.0 / M_PI); }
+
+/* GeLU, tanh approximation (reading of the pages' unnamed "GeLU"). */
+double orc_gelu(double x) {
+    double u = gelu_c() * (x + 0.044715 * x * x * x);
+    return 0.5 * x * (1.0 + tanh(u));
+}
+
+/* d/dx of orc_gelu, written out by the product and chain rules. */
+double orc_gelu_grad(double x) {
+    double u = gelu_c() * (x + 0.044715 * x * x * x);
+    double th = tanh(u);
+    double du = gelu_c() * (1.0 + 3.0 * 0.044715 * x * x);
+    return 0.5 * (1.0 + th) + 0.5 * x * (1.0 - th * th) * du;
+}
+
+static int bad_shape(long T, long h, long F, long t) {
+    return T < 0 || h < 1 || F < 1 || t < 1 || F % t != 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Full computation on fp64 inputs (small problems).                       */
+/* ---------------------------------------------------------------------- */
+
+/* Column-parallel step for shard i: Z_i = X A_i + b1_i, H_i = GeLU(Z_i).
+ * Z and H are the full [T, F] arrays; shard i fills its column block. */
+static void shard_forward_first(const double* X, const double* A, const double* b1,
+                                long T, long h, long F, long f, long i,
+                                double* Z, double* H) {
+    long c0 = i * f;
+#pragma omp parallel for schedule(static)
+    for (long r = 0; r < T; ++r) {
+        for (long j = 0; j < f; ++j) {
+            double s = 0.0;
+            for (long k = 0; k < h; ++k) s += X[r * h + k] * A[k * F + c0 + j];
+            double z = s + b1[c0 + j];
+            Z[r * F + c0 + j] = z;
+            H[r * F + c0 + j] = orc_gelu(z);
+        }
+    }
+}
+
+/* Row-parallel partial for shard i: P_i = H_i B_i  ([T, h]). */
+static void shard_forward_second(const double* H, const double* B, long T, long h,
+                                 long F, long f, long i, double* P) {
+    long c0 = i * f;
+#pragma omp parallel for schedule(static)
+    for (long r = 0; r < T; ++r) {
+        for (long n = 0; n < h; ++n) {
+            double s = 0.0;
+            for (long j = 0; j < f; ++j) s += H[r * F + c0 + j] * B[(c0 + j) * h + n];
+            P[r * h + n] = s;
+        }
+    }
+}
+
+/* Forward pass.  Y [T,h]; Z, H [T,F] (may be NULL when not wanted). */
+int orc_forward(const double* X, const double* A, const double* b1, const double* B,
+                const double* b2, const double* R, long T, long h, long F, long t,
+                double* Y, double* Z, double* H) {
+    if (bad_shape(T, h, F, t)) return ORC_ERR_SHAPE;
+    long f = F / t;
+    double* Zw = Z ? Z : (double*)malloc(sizeof(double) * (size_t)(T * F + 1));
+    double* Hw = H ? H : (double*)malloc(sizeof(double) * (size_t)(T * F + 1));
+    double* P = (double*)malloc(sizeof(double) * (size_t)(T * h + 1));
+    if (!Zw || !Hw || !P) {
+        if (!Z) free(Zw);
+        if (!H) free(Hw);
+        free(P);
+        return ORC_ERR_ALLOC;
+    }
+    for (long e = 0; e < T * h; ++e) Y[e] = 0.0;
+    for (long i = 0; i < t; ++i) {
+        shard_forward_first(X, A, b1, T, h, F, f, i, Zw, Hw);
+        shard_forward_second(Hw, B, T, h, F, f, i, P);
+        for (long e = 0; e < T * h; ++e) Y[e] += P[e]; /* g: sum of partials */
+    }
+    for (long r = 0; r < T; ++r)
+        for (long n = 0; n < h; ++n) Y[r * h + n] += b2[n] + R[r * h + n];
+    if (!Z) free(Zw);
+    if (!H) free(Hw);
+    free(P);
+    return ORC_OK;
+}
+
+/* Backward pass given the upstream gradient dY [T,h].
+ * Outputs: dX [T,h], dA [h,F], dB [F,h], db1 [F], db2 [h]. */
+int orc_backward(const double* dY, const double* X, const double* A, const double* b1,
+                 const double* B, long T, long h, long F, long t, double* dX, double* dA,
+                 double* dB, double* db1, double* db2) {
+    if (bad_shape(T, h, F, t)) return ORC_ERR_SHAPE;
+    long f = F / t;
+    double* Z = (double*)malloc(sizeof(double) * (size_t)(T * F + 1));
+    double* H = (double*)malloc(sizeof(double) * (size_t)(T * F + 1));
+    double* dZ = (double*)malloc(sizeof(double) * (size_t)(T * F + 1));
+    double* dXi = (double*)malloc(sizeof(double) * (size_t)(T * h + 1));
+    if (!Z || !H || !dZ || !dXi) {
+        free(Z); free(H); free(dZ); free(dXi);
+        return ORC_ERR_ALLOC;
+    }
+    for (long e = 0; e < T * h; ++e) dX[e] = 0.0;
+    for (long i = 0; i < t; ++i) {
+        long c0 = i * f;
+        shard_forward_first(X, A, b1, T, h, F, f, i, Z, H);
+        /* dZ_i = (dY B_i^T) * GeLU'(Z_i) */
+#pragma omp parallel for schedule(static)
+        for (long r = 0; r < T; ++r) {
+            for (long j = 0; j < f; ++j) {
+                double s = 0.0;
+                for (long n = 0; n < h; ++n) s += dY[r * h + n] * B[(c0 + j) * h + n];
+                dZ[r * F + c0 + j] = s * orc_gelu_grad(Z[r * F + c0 + j]);
+            }
+        }
+        /* dB_i = H_i^T dY */
+#pragma omp parallel for schedule(static)
+        for (long j = 0; j < f; ++j) {
+            for (long n = 0; n < h; ++n) {
+                double s = 0.0;
+                for (long r = 0; r < T; ++r) s += H[r * F + c0 + j] * dY[r * h + n];
+                dB[(c0 + j) * h + n] = s;
+            }
+        }
+        /* dA_i = X^T dZ_i */
+#pragma omp parallel for schedule(static)
+        for (long k = 0; k < h; ++k) {
+            for (long j = 0; j < f; ++j) {
+                double s = 0.0;
+                for (long r = 0; r < T; ++r) s += X[r * h + k] * dZ[r * F + c0 + j];
+                dA[k * F + c0 + j] = s;
+            }
+        }
+        /* db1_i = column sums of dZ_i */
+        for (long j = 0; j < f; ++j) {
+            double s = 0.0;
+            for (long r = 0; r < T; ++r) s += dZ[r * F + c0 + j];
+            db1[c0 + j] = s;
+        }
+        /* dX_i = dZ_i A_i^T, then the f-operator sum over shards */
+#pragma omp parallel for schedule(static)
+        for (long r = 0; r < T; ++r) {
+            for (long k = 0; k < h; ++k) {
+                double s = 0.0;
+                for (long j = 0; j < f; ++j) s += dZ[r * F + c0 + j] * A[k * F + c0 + j];
+                dXi[r * h + k] = s;
+            }
+        }
+        for (long e = 0; e < T * h; ++e) dX[e] += dXi[e];
+    }
+    for (long n = 0; n < h; ++n) {
+        double s = 0.0;
+        for (long r = 0; r < T; ++r) s += dY[r * h + n];
+        db2[n] = s;
+    }
+    free(Z); free(H); free(dZ); free(dXi);
+    return ORC_OK;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Sampled computation on bf16 inputs (large problems).                     */
+/* Inputs are raw bfloat16 bit patterns, widened exactly to double on read. */
+/* Each sampled output is the same definition as above, evaluated alone.   */
+/* ---------------------------------------------------------------------- */
+
+static inline double w16(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float v;
+    memcpy(&v, &u, sizeof v);
+    return (double)v;
+}
+
+/* Z and H for a set of rows: Zr, Hr are [nrows, F]. */
+static void rows_first(const uint16_t* X, const uint16_t* A, const uint16_t* b1, long h,
+                       long F, const long* rows, long nrows, double* Zr, double* Hr) {
+    /* Each thread owns a block of columns and walks k in ascending order, so
+     * every Z entry is b1 + sum_k X[r,k] A[k,j] summed from k = 0 upwards. */
+#pragma omp parallel for schedule(static)
+    for (long j0 = 0; j0 < F; j0 += 256) {
+        long j1 = j0 + 256 < F ? j0 + 256 : F;
+        for (long q = 0; q < nrows; ++q)
+            for (long j = j0; j < j1; ++j) Zr[q * F + j] = 0.0;
+        for (long k = 0; k < h; ++k) {
+            const uint16_t* Ak = A + k * F;
+            for (long q = 0; q < nrows; ++q) {
+                double x = w16(X[rows[q] * h + k]);
+                double* z = Zr + q * F;
+                for (long j = j0; j < j1; ++j) z[j] += x * w16(Ak[j]);
+            }
+        }
+        for (long q = 0; q < nrows; ++q)
+            for (long j = j0; j < j1; ++j) {
+                double z = Zr[q * F + j] + w16(b1[j]);
+                Zr[q * F + j] = z;
+                Hr[q * F + j] = orc_gelu(z);
+            }
+    }
+}
+
+/* Y rows: Y[r,:] = sum_i H_i[r,:] B_i + b2 + R[r,:].  Yr is [nrows, h];
+ * Zr, Hr ([nrows, F]) receive the pre-activation and GeLU rows (may be NULL). */
+int orc_forward_rows_bf16(const uint16_t* X, const uint16_t* A, const uint16_t* b1,
+                          const uint16_t* B, const uint16_t* b2, const uint16_t* R,
+                          long T, long h, long F, long t, const long* rows, long nrows,
+                          double* Yr, double* Zr, double* Hr) {
+    if (bad_shape(T, h, F, t)) return ORC_ERR_SHAPE;
+    for (long q = 0; q < nrows; ++q)
+        if (rows[q] < 0 || rows[q] >= T) return ORC_ERR_SHAPE;
+    long f = F / t;
+    double* Z = Zr ? Zr : (double*)malloc(sizeof(double) * (size_t)(nrows * F + 1));
+    double* H = Hr ? Hr : (double*)malloc(sizeof(double) * (size_t)(nrows * F + 1));
+    if (!Z || !H) {
+        if (!Zr) free(Z);
+        if (!Hr) free(H);
+        return ORC_ERR_ALLOC;
+    }
+    rows_first(X, A, b1, h, F, rows, nrows, Z, H);
+#pragma omp parallel for schedule(static)
+    for (long n0 = 0; n0 < h; n0 += 64) {
+        long n1 = n0 + 64 < h ? n0 + 64 : h;
+        double part[64];
+        for (long q = 0; q < nrows; ++q) {
+            double* y = Yr + q * h;
+            for (long n = n0; n < n1; ++n) y[n] = 0.0;
+            for (long i = 0; i < t; ++i) {
+                for (long n = n0; n < n1; ++n) part[n - n0] = 0.0;
+                for (long j = i * f; j < (i + 1) * f; ++j) {
+                    double hv = H[q * F + j];
+                    const uint16_t* Bj = B + j * h;
+                    for (long n = n0; n < n1; ++n) part[n - n0] += hv * w16(Bj[n]);
+                }
+                for (long n = n0; n < n1; ++n) y[n] += part[n - n0]; /* g sum */
+            }
+            for (long n = n0; n < n1; ++n) y[n] += w16(b2[n]) + w16(R[rows[q] * h + n]);
+        }
+    }
+    if (!Zr) free(Z);
+    if (!Hr) free(H);
+    return ORC_OK;
+}
+
+/* dX rows: dX[r,:] = sum_i (dY[r,:] B_i^T * GeLU'(Z_i[r,:])) A_i^T.
+ * dXr is [nrows, h]. */
+int orc_backward_rows_bf16(const uint16_t* dY, const uint16_t* X, const uint16_t* A,
+                           const uint16_t* b1, const uint16_t* B, long T, long h, long F,
+                           long t, const long* rows, long nrows, double* dXr) {
+    if (bad_shape(T, h, F, t)) return ORC_ERR_SHAPE;
+    for (long q = 0; q < nrows; ++q)
+        if (rows[q] < 0 || rows[q] >= T) return ORC_ERR_SHAPE;
+    long f = F / t;
+    double* Z = (double*)malloc(sizeof(double) * (size_t)(nrows * F + 1));
+    double* H = (double*)malloc(sizeof(double) * (size_t)(nrows * F + 1));
+    double* dZ = (double*)malloc(sizeof(double) * (size_t)(nrows * F + 1));
+    if (!Z || !H || !dZ) {
+        free(Z); free(H); free(dZ);
+        return ORC_ERR_ALLOC;
+    }
+    rows_first(X, A, b1, h, F, rows, nrows, Z, H);
+    /* dZ[r, j] = (sum_n dY[r,n] B[j,n]) * GeLU'(Z[r,j]) */
+#pragma omp parallel for schedule(static)
+    for (long j = 0; j < F; ++j) {
+        const uint16_t* Bj = B + j * h;
+        for (long q = 0; q < nrows; ++q) {
+            const uint16_t* d = dY + rows[q] * h;
+            double s = 0.0;
+            for (long n = 0; n < h; ++n) s += w16(d[n]) * w16(Bj[n]);
+            dZ[q * F + j] = s * orc_gelu_grad(Z[q * F + j]);
+        }
+    }
+    /* dX[r, k] = sum_i sum_{j in shard i} dZ[r,j] A[k,j] */
+#pragma omp parallel for schedule(static)
+    for (long k = 0; k < h; ++k) {
+        const uint16_t* Ak = A + k * F;
+        for (long q = 0; q < nrows; ++q) {
+            double acc = 0.0;
+            for (long i = 0; i < t; ++i) {
+                double s = 0.0;
+                for (long j = i * f; j < (i + 1) * f; ++j) s += dZ[q * F + j] * w16(Ak[j]);
+                acc += s; /* f-operator sum */
+            }
+            dXr[q * h + k] = acc;
+        }
+    }
+    free(Z); free(H); free(dZ);
+    return ORC_OK;
+}
+
+/* Sampled FFN columns j (global index into F):
+ *   dA[:, j] ([h] per column) -> dAc is [h, ncols] (column q at dAc[k*ncols+q]);
+ *   dB[j, :] ([h] per column) -> dBr is [ncols, h];
+ *   db1[j]                    -> db1c is [ncols]. */
+int orc_backward_cols_bf16(const uint16_t* dY, const uint16_t* X, const uint16_t* A,
+                           const uint16_t* b1, const uint16_t* B, long T, long h, long F,
+                           long t, const long* cols, long ncols, double* dAc, double* dBr,
+                           double* db1c) {
+    if (bad_shape(T, h, F, t)) return ORC_ERR_SHAPE;
+    for (long q = 0; q < ncols; ++q)
+        if (cols[q] < 0 || cols[q] >= F) return ORC_ERR_SHAPE;
+    double* zc = (double*)malloc(sizeof(double) * (size_t)(T * ncols + 1));
+    double* hc = (double*)malloc(sizeof(double) * (size_t)(T * ncols + 1));
+    double* dzc = (double*)malloc(sizeof(double) * (size_t)(T * ncols + 1));
+    if (!zc || !hc || !dzc) {
+        free(zc); free(hc); free(dzc);
+        return ORC_ERR_ALLOC;
+    }
+    /* Z[:, j], H[:, j], dZ[:, j] for every sampled column (row-major [T, ncols]) */
+#pragma omp parallel for schedule(static)
+    for (long r = 0; r < T; ++r) {
+        const uint16_t* xr = X + r * h;
+        const uint16_t* dr = dY + r * h;
+        for (long q = 0; q < ncols; ++q) {
+            long j = cols[q];
+            double z = 0.0;
+            for (long k = 0; k < h; ++k) z += w16(xr[k]) * w16(A[k * F + j]);
+            z += w16(b1[j]);
+            double g = 0.0;
+            for (long n = 0; n < h; ++n) g += w16(dr[n]) * w16(B[j * h + n]);
+            zc[r * ncols + q] = z;
+            hc[r * ncols + q] = orc_gelu(z);
+            dzc[r * ncols + q] = g * orc_gelu_grad(z);
+        }
+    }
+    /* dA[k, j] = sum_r X[r,k] dZ[r,j] ; dB[j, n] = sum_r H[r,j] dY[r,n] */
+#pragma omp parallel for schedule(static)
+    for (long k = 0; k < h; ++k) {
+        for (long q = 0; q < ncols; ++q) {
+            double sa = 0.0, sb = 0.0;
+            for (long r = 0; r < T; ++r) {
+                sa += w16(X[r * h + k]) * dzc[r * ncols + q];
+                sb += hc[r * ncols + q] * w16(dY[r * h + k]);
+            }
+            dAc[k * ncols + q] = sa;
+            dBr[q * h + k] = sb;
+        }
+    }
+    for (long q = 0; q < ncols; ++q) {
+        double s = 0.0;
+        for (long r = 0; r < T; ++r) s += dzc[r * ncols + q];
+        db1c[q] = s;
+    }
+    free(zc); free(hc); free(dzc);
+    return ORC_OK;
+}
+
+/* db2 = column sums of dY (all h entries). */
+int orc_db2_bf16(const uint16_t* dY, long T, long h, double* db2) {
+    if (T < 0 || h < 1) return ORC_ERR_SHAPE;
+#pragma omp parallel for schedule(static)
+    for (long n = 0; n < h; ++n) {
+        double s = 0.0;
+        for (long r = 0; r < T; ++r) s += w16(dY[r * h + n]);
+        db2[n] = s;
+    }
+    return ORC_OK;
+}
+
+/* Threads the OpenMP runtime will use (1 without OpenMP). */
+int orc_num_threads(void) {
+#ifdef _OPENMP
+    extern int omp_get_max_threads(void);
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

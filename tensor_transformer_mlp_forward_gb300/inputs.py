@@ -1,0 +1,142 @@
+"""Seeded synthetic inputs for the tensor-parallel MLP block.
+
+This module only draws random tensors; it holds none of the block's
+arithmetic, so both the CUDA path and the fp64 oracle can take their inputs
+from it without sharing any computation.
+
+Workloads follow the layer shapes named on the source pages:
+
+* GPT-2-medium (355M): hidden 1024, seq 1024 -- "Megatron-LM: Tensor Model
+  Parallel" (charles2530.github.io), GPT-2 Training, Table 2.
+* Megatron 8.3B: hidden 3072, 72 layers, 8-way model parallel -- same page,
+  Scaling Study, Table 1; weights before the residual scaled by 1/sqrt(2N)
+  (same page, Training recipe table, "Initialization").
+* MT-NLG 530B: hidden 20480, seq 2048, TP 8 -- "MT-NLG 530B deep dive"
+  (zzszmyf.github.io), section 4.1 model configuration.
+
+The FFN width is 4h everywhere and T = batch * seq tokens.  Every tensor is
+drawn as float32 N(0, std) from a CPU ``torch.Generator`` in the fixed order
+X, A, b1, B, b2, residual, dY, then rounded to bfloat16 (round to nearest
+even).  A tensor whose std is 0 is all zeros and consumes no draws.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Dict, Optional
+
+import torch
+
+# Draws larger than this many elements are produced in row chunks so that the
+# float32 temporary stays small; the chunking is part of the definition of the
+# stream, so results are reproducible for a given seed.
+_CHUNK_ELEMS = 1 << 24
+
+DRAW_ORDER = ("X", "A", "b1", "B", "b2", "residual", "dY")
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One MLP-block problem: T tokens, hidden h, FFN width F, t shards."""
+
+    name: str
+    T: int
+    h: int
+    F: int
+    t: int
+    std: Dict[str, float]
+    seed: int
+
+    @property
+    def f(self) -> int:
+        return self.F // self.t
+
+    def flops_fwd_bwd(self) -> int:
+        """Algorithmic flops of forward + backward: six GEMMs of 2*T*h*F."""
+        return 12 * self.T * self.h * self.F
+
+    def shape(self, key: str):
+        T, h, F = self.T, self.h, self.F
+        return {
+            "X": (T, h),
+            "A": (h, F),
+            "b1": (F,),
+            "B": (F, h),
+            "b2": (h,),
+            "residual": (T, h),
+            "dY": (T, h),
+        }[key]
+
+    def with_shape(self, T: int, t: Optional[int] = None, name: Optional[str] = None):
+        return dataclasses.replace(
+            self, T=T, t=self.t if t is None else t, name=name or self.name
+        )
+
+
+def _std(x=1.0, a=0.02, b1=0.0, b=0.02, b2=0.0, res=1.0, dy=1.0):
+    return {"X": x, "A": a, "b1": b1, "B": b, "b2": b2, "residual": res, "dY": dy}
+
+
+# The five workload families.  The seed of family k is 1000 + k.
+TINY = Workload("tiny", 128, 256, 1024, 2, _std(b1=0.01, b2=0.01), 1000)
+GPT2_MEDIUM = Workload("gpt2-medium", 8192, 1024, 4096, 2, _std(), 1001)
+MEGATRON_8_3B = Workload(
+    "megatron-8.3b", 8192, 3072, 12288, 8, _std(b=0.02 / math.sqrt(2 * 72)), 1002
+)
+MTNLG_530B = Workload("mt-nlg-530b", 2048, 20480, 81920, 8, _std(a=0.006, b=0.006), 1003)
+SWEEP = Workload("sweep-h4096", 2048, 4096, 16384, 8, _std(), 1004)
+
+SWEEP_TOKENS = (512, 1024, 2048, 4096, 16384)
+SWEEP_SHARDS = (1, 2, 4, 8)
+
+WORKLOADS = {w.name: w for w in (TINY, GPT2_MEDIUM, MEGATRON_8_3B, MTNLG_530B, SWEEP)}
+
+
+def custom(T: int, h: int, F: int, t: int, seed: int, std=None, name="custom") -> Workload:
+    """A workload of arbitrary shape with the tiny family's distributions."""
+    return Workload(name, T, h, F, t, dict(std or TINY.std), seed)
+
+
+def _draw(gen: torch.Generator, shape, std: float) -> torch.Tensor:
+    if std == 0.0:
+        return torch.zeros(shape, dtype=torch.bfloat16)
+    n = math.prod(shape)
+    if n <= _CHUNK_ELEMS or len(shape) == 1:
+        return (torch.randn(shape, generator=gen, dtype=torch.float32) * std).to(torch.bfloat16)
+    rows, cols = shape
+    out = torch.empty(shape, dtype=torch.bfloat16)
+    step = max(1, _CHUNK_ELEMS // cols)
+    for r0 in range(0, rows, step):
+        r1 = min(rows, r0 + step)
+        chunk = torch.randn((r1 - r0, cols), generator=gen, dtype=torch.float32)
+        out[r0:r1] = (chunk * std).to(torch.bfloat16)
+    return out
+
+
+def make_inputs(w: Workload, keys=DRAW_ORDER) -> Dict[str, torch.Tensor]:
+    """Draw the workload's bf16 tensors on the CPU (contiguous, row-major).
+
+    ``keys`` may name a subset; tensors are still drawn in ``DRAW_ORDER`` so
+    a subset equals the same entries of the full draw.
+    """
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(w.seed)
+    out = {}
+    last = max(DRAW_ORDER.index(k) for k in keys)
+    for key in DRAW_ORDER[: last + 1]:
+        t = _draw(gen, w.shape(key), w.std[key])
+        if key in keys:
+            out[key] = t.contiguous()
+    return out
+
+
+def sample_indices(n: int, k: int, seed: int) -> torch.Tensor:
+    """k distinct sorted indices in [0, n) (always includes n-1, the tail)."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    k = min(k, n)
+    idx = torch.randperm(n, generator=gen)[:k]
+    if k and (n - 1) not in idx.tolist():
+        idx[-1] = n - 1
+    return torch.sort(idx).values.to(torch.int64)

@@ -1,0 +1,260 @@
+"""Checks that pin the fp64 oracle to facts outside itself.
+
+The pages print no worked numeric example of the MLP block, so the oracle is
+pinned by mathematics:
+
+* GeLU: exact identities of the tanh form (g(x) - g(-x) = x, g(0) = 0,
+  g'(0) = 1/2, g'(x) + g'(-x) = 1), its asymptotes, its distance to the
+  exact erf GeLU x Phi(x) (a different function whose maximum distance from
+  the tanh approximation is 4.73e-4, reached near |x| = 2.7), and the
+  derivative against central finite differences of the oracle's own GeLU.
+* Linear algebra: the oracle's loops against numpy float64 matmuls (a
+  library primitive), composed with the separately pinned GeLU.
+* Gradients: against central finite differences of L = <dY, Y>.
+* Partition invariant: every shard count t gives the unsharded block
+  ("Megatron-LM: Tensor Model Parallel", section "MLP: Column Parallel first,
+  then Row Parallel", Figure 3a; "f / g Operators", Figure 4).
+* Special cases: A = 0, B = 0, X = 0, linearity in residual and b2.
+* The sampled (bf16-input) entry points against the full computation.
+
+Each check returns True/False so that ``test_oracle_pins.py`` can run the same
+list against deliberately mutated copies of the oracle and show that every
+planted mistake fails at least one check.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+from tensor_transformer_mlp_forward_gb300 import inputs
+
+ERF_GAP = 4.74e-4  # max |tanh-GeLU - erf-GeLU| over the reals (measured on a fine grid)
+
+
+def _rel(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    den = np.max(np.abs(b)) if b.size else 0.0
+    if den == 0.0:
+        return float(np.max(np.abs(a - b))) if a.size else 0.0
+    return float(np.max(np.abs(a - b)) / den)
+
+
+def _rand_block(T, h, F, seed, scale_w=0.3):
+    rng = np.random.default_rng(seed)
+    return dict(
+        X=rng.standard_normal((T, h)),
+        A=rng.standard_normal((h, F)) * scale_w,
+        b1=rng.standard_normal(F) * 0.1,
+        B=rng.standard_normal((F, h)) * scale_w,
+        b2=rng.standard_normal(h) * 0.1,
+        R=rng.standard_normal((T, h)),
+        dY=rng.standard_normal((T, h)),
+    )
+
+
+# ----------------------------------------------------------------- GeLU pins
+
+def pin_gelu_identities(o) -> bool:
+    ok = o.gelu(0.0) == 0.0 and o.gelu_grad(0.0) == 0.5
+    for x in np.linspace(-6, 6, 241):
+        ok &= abs((o.gelu(x) - o.gelu(-x)) - x) <= 1e-14 * max(1.0, abs(x))
+        ok &= abs(o.gelu_grad(x) + o.gelu_grad(-x) - 1.0) <= 1e-14
+    return bool(ok)
+
+
+def pin_gelu_asymptotes(o) -> bool:
+    return (abs(o.gelu(12.0) - 12.0) < 1e-12 and abs(o.gelu(-12.0)) < 1e-12
+            and abs(o.gelu_grad(12.0) - 1.0) < 1e-12 and abs(o.gelu_grad(-12.0)) < 1e-12)
+
+
+def pin_gelu_vs_erf(o) -> bool:
+    worst = 0.0
+    for x in np.linspace(-8, 8, 3201):
+        exact = 0.5 * x * (1.0 + math.erf(x / math.sqrt(2.0)))
+        worst = max(worst, abs(o.gelu(x) - exact))
+    # the approximation is close to, but not equal to, the erf form
+    return 4.0e-4 < worst <= ERF_GAP
+
+
+def pin_gelu_known_values(o) -> bool:
+    # tanh-approximation GeLU at +-1 and 3, seven significant digits
+    return (abs(o.gelu(1.0) - 0.8411920) < 5e-8 and abs(o.gelu(-1.0) + 0.1588080) < 5e-8
+            and abs(o.gelu(3.0) - 2.9963626) < 5e-8)
+
+
+def pin_gelu_grad_fd(o) -> bool:
+    eps = 1e-5
+    for x in np.linspace(-5, 5, 101):
+        fd = (o.gelu(x + eps) - o.gelu(x - eps)) / (2 * eps)
+        if abs(fd - o.gelu_grad(x)) > 1e-8:
+            return False
+    return True
+
+
+# ------------------------------------------------------- linear algebra pins
+
+def _np_forward(o, p):
+    g = np.vectorize(o.gelu, otypes=[np.float64])
+    Z = p["X"] @ p["A"] + p["b1"]
+    H = g(Z)
+    return H @ p["B"] + p["b2"] + p["R"], Z, H
+
+
+def _np_backward(o, p):
+    g = np.vectorize(o.gelu, otypes=[np.float64])
+    gd = np.vectorize(o.gelu_grad, otypes=[np.float64])
+    Z = p["X"] @ p["A"] + p["b1"]
+    H = g(Z)
+    dZ = (p["dY"] @ p["B"].T) * gd(Z)
+    return dZ @ p["A"].T, p["X"].T @ dZ, H.T @ p["dY"], dZ.sum(0), p["dY"].sum(0)
+
+
+def pin_forward_vs_numpy(o) -> bool:
+    for (T, h, F, t, seed) in ((5, 6, 8, 1, 1), (7, 4, 12, 3, 2), (1, 3, 8, 4, 3), (0, 3, 4, 2, 4)):
+        p = _rand_block(T, h, F, seed)
+        Y, Z, H = o.forward(p["X"], p["A"], p["b1"], p["B"], p["b2"], p["R"], t)
+        Yn, Zn, Hn = _np_forward(o, p)
+        if T and (_rel(Y, Yn) > 1e-12 or _rel(Z, Zn) > 1e-12 or _rel(H, Hn) > 1e-12):
+            return False
+        if Y.shape != (T, h):
+            return False
+    return True
+
+
+def pin_backward_vs_numpy(o) -> bool:
+    for (T, h, F, t, seed) in ((5, 6, 8, 1, 5), (7, 4, 12, 3, 6), (2, 5, 8, 8, 7)):
+        p = _rand_block(T, h, F, seed)
+        got = o.backward(p["dY"], p["X"], p["A"], p["b1"], p["B"], t)
+        ref = _np_backward(o, p)
+        for a, b in zip(got, ref):
+            if _rel(a, b) > 1e-12:
+                return False
+    return True
+
+
+# ---------------------------------------------------------- gradient pins
+
+def pin_gradients_fd(o) -> bool:
+    """Every gradient against central differences of L = <dY, Y>."""
+    T, h, F, t = 3, 4, 8, 2
+    p = _rand_block(T, h, F, 11, scale_w=0.5)
+
+    def loss(q):
+        Y, _, _ = o.forward(q["X"], q["A"], q["b1"], q["B"], q["b2"], q["R"], t)
+        return float(np.sum(q["dY"] * Y))
+
+    dX, dA, dB, db1, db2 = o.backward(p["dY"], p["X"], p["A"], p["b1"], p["B"], t)
+    eps = 1e-6
+    for key, an in (("X", dX), ("A", dA), ("B", dB), ("b1", db1), ("b2", db2), ("R", p["dY"])):
+        fd = np.zeros_like(p[key])
+        it = np.nditer(p[key], flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            q = {k: v.copy() for k, v in p.items()}
+            q[key][idx] += eps
+            lp = loss(q)
+            q[key][idx] -= 2 * eps
+            lm = loss(q)
+            fd[idx] = (lp - lm) / (2 * eps)
+        if _rel(an, fd) > 1e-6:
+            return False
+    return True
+
+
+# ------------------------------------------------------ partition invariant
+
+def pin_partition_invariant(o) -> bool:
+    T, h, F = 6, 8, 64
+    p = _rand_block(T, h, F, 21)
+    base_f = o.forward(p["X"], p["A"], p["b1"], p["B"], p["b2"], p["R"], 1)
+    base_b = o.backward(p["dY"], p["X"], p["A"], p["b1"], p["B"], 1)
+    for t in (2, 4, 8):
+        f = o.forward(p["X"], p["A"], p["b1"], p["B"], p["b2"], p["R"], t)
+        b = o.backward(p["dY"], p["X"], p["A"], p["b1"], p["B"], t)
+        for a, c in zip(f + b, base_f + base_b):
+            if _rel(a, c) > 1e-12:
+                return False
+    return True
+
+
+# ------------------------------------------------------------ special cases
+
+def pin_special_cases(o) -> bool:
+    T, h, F, t = 4, 6, 16, 4
+    p = _rand_block(T, h, F, 31)
+    ok = True
+    # A = 0: Y = GeLU(b1) B + b2 + R in every row, dX = 0
+    q = dict(p, A=np.zeros_like(p["A"]))
+    Y, _, _ = o.forward(q["X"], q["A"], q["b1"], q["B"], q["b2"], q["R"], t)
+    row = np.array([o.gelu(v) for v in q["b1"]]) @ q["B"] + q["b2"]
+    ok &= _rel(Y - q["R"], np.tile(row, (T, 1))) < 1e-12
+    dX, *_ = o.backward(q["dY"], q["X"], q["A"], q["b1"], q["B"], t)
+    ok &= float(np.max(np.abs(dX))) == 0.0
+    # B = 0: Y = b2 + R, dA = 0, db1 = 0
+    q = dict(p, B=np.zeros_like(p["B"]))
+    Y, _, _ = o.forward(q["X"], q["A"], q["b1"], q["B"], q["b2"], q["R"], t)
+    ok &= _rel(Y, q["b2"] + q["R"]) < 1e-15
+    _, dA, _, db1, _ = o.backward(q["dY"], q["X"], q["A"], q["b1"], q["B"], t)
+    ok &= float(np.max(np.abs(dA))) == 0.0 and float(np.max(np.abs(db1))) == 0.0
+    # X = 0: dA = 0
+    q = dict(p, X=np.zeros_like(p["X"]))
+    _, dA, _, _, _ = o.backward(q["dY"], q["X"], q["A"], q["b1"], q["B"], t)
+    ok &= float(np.max(np.abs(dA))) == 0.0
+    # Y is affine in the residual and in b2 with unit slope
+    Y0, _, _ = o.forward(p["X"], p["A"], p["b1"], p["B"], p["b2"], p["R"], t)
+    Y1, _, _ = o.forward(p["X"], p["A"], p["b1"], p["B"], p["b2"] + 1.5, 2 * p["R"], t)
+    ok &= _rel(Y1 - Y0, p["R"] + 1.5) < 1e-12
+    # dY = 0: every gradient vanishes
+    g = o.backward(np.zeros_like(p["dY"]), p["X"], p["A"], p["b1"], p["B"], t)
+    ok &= all(float(np.max(np.abs(v))) == 0.0 for v in g)
+    return bool(ok)
+
+
+# --------------------------------------------------- sampled vs full (bf16)
+
+def pin_sampled_matches_full(o) -> bool:
+    w = inputs.custom(T=37, h=24, F=48, t=4, seed=77)
+    inp = inputs.make_inputs(w)
+    Y, Z, H = o.forward(inp["X"], inp["A"], inp["b1"], inp["B"], inp["b2"], inp["residual"], w.t)
+    dX, dA, dB, db1, db2 = o.backward(inp["dY"], inp["X"], inp["A"], inp["b1"], inp["B"], w.t)
+    rows = [0, 5, 36]
+    cols = [0, 11, 12, 47]
+    Yr, Zr, Hr = o.forward_rows(inp, w.t, rows)
+    dXr = o.backward_rows(inp, w.t, rows)
+    dAc, dBr, db1c = o.backward_cols(inp, w.t, cols)
+    d2 = o.db2(inp["dY"])
+    return (_rel(Yr, Y[rows]) < 1e-13 and _rel(Zr, Z[rows]) < 1e-13 and _rel(Hr, H[rows]) < 1e-13
+            and _rel(dXr, dX[rows]) < 1e-13 and _rel(dAc, dA[:, cols]) < 1e-13
+            and _rel(dBr, dB[cols]) < 1e-13 and _rel(db1c, db1[cols]) < 1e-13
+            and _rel(d2, db2) < 1e-13)
+
+
+ALL_PINS = [
+    pin_gelu_identities,
+    pin_gelu_asymptotes,
+    pin_gelu_vs_erf,
+    pin_gelu_known_values,
+    pin_gelu_grad_fd,
+    pin_forward_vs_numpy,
+    pin_backward_vs_numpy,
+    pin_gradients_fd,
+    pin_partition_invariant,
+    pin_special_cases,
+    pin_sampled_matches_full,
+]
+
+
+def failing_pins(o):
+    out = []
+    for pin in ALL_PINS:
+        try:
+            ok = pin(o)
+        except Exception:  # a mutant may also break an entry point outright
+            ok = False
+        if not ok:
+            out.append(pin.__name__)
+    return out

@@ -1,0 +1,67 @@
+"""The fp64 oracle against its pins, and the pins against planted mistakes."""
+
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from oracle import Oracle
+from tests import oracle_pins as P
+
+ORACLE_SRC = os.path.join(os.path.dirname(oracle.__file__), "tpmlp_oracle.c")
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.default()
+
+
+@pytest.mark.parametrize("pin", P.ALL_PINS, ids=lambda f: f.__name__)
+def test_pin(orc, pin):
+    assert pin(orc)
+
+
+# Plausible mistakes, each planted by a textual edit of the oracle's source:
+# a wrong constant, a wrong sign, a dropped term, a transposed or shifted
+# index, an operand swapped, a sum replaced by an overwrite.
+MUTANTS = {
+    "gelu_coefficient": ("0.5 * x * (1.0 + tanh(u));", "0.5 * x * (1.0 + tanh(1.05 * u));"),
+    "gelu_sign": ("return 0.5 * x * (1.0 + tanh(u));", "return 0.5 * x * (1.0 - tanh(u));"),
+    "gelu_grad_dropped_term": ("+ 0.5 * x * (1.0 - th * th) * du;", ";"),
+    "gelu_grad_cubic_factor": ("(1.0 + 3.0 * 0.044715 * x * x)", "(1.0 + 0.044715 * x * x)"),
+    "g_sum_overwrites": ("Y[e] += P[e]; /* g: sum of partials */", "Y[e] = P[e];"),
+    "first_gemm_transposed": ("s += X[r * h + k] * A[k * F + c0 + j];",
+                              "s += X[r * h + k] * A[(c0 + j) * h + k];"),
+    "b2_dropped": ("Y[r * h + n] += b2[n] + R[r * h + n];", "Y[r * h + n] += R[r * h + n];"),
+    "dB_uses_Z": ("s += H[r * F + c0 + j] * dY[r * h + n];", "s += Z[r * F + c0 + j] * dY[r * h + n];"),
+    "db1_shard_offset": ("for (long r = 0; r < T; ++r) s += dZ[r * F + c0 + j];",
+                         "for (long r = 0; r < T; ++r) s += dZ[r * F + j];"),
+    "f_sum_overwrites": ("for (long e = 0; e < T * h; ++e) dX[e] += dXi[e];",
+                         "for (long e = 0; e < T * h; ++e) dX[e] = dXi[e];"),
+    "dA_wrong_operand": ("s += X[r * h + k] * dZ[r * F + c0 + j];",
+                         "s += X[r * h + k] * H[r * F + c0 + j];"),
+    "rows_g_sum_overwrites": ("y[n] += part[n - n0]; /* g sum */", "y[n] = part[n - n0];"),
+    "rows_f_sum_overwrites": ("acc += s; /* f-operator sum */", "acc = s;"),
+    "cols_gelu_instead_of_grad": ("dzc[r * ncols + q] = g * orc_gelu_grad(z);",
+                                  "dzc[r * ncols + q] = g * orc_gelu(z);"),
+    "cols_dB_wrong_row": ("sb += hc[r * ncols + q] * w16(dY[r * h + k]);",
+                          "sb += hc[r * ncols + q] * w16(X[r * h + k]);"),
+    "db2_drops_last_row": ("for (long r = 0; r < T; ++r) s += w16(dY[r * h + n]);",
+                           "for (long r = 0; r + 1 < T; ++r) s += w16(dY[r * h + n]);"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(ORACLE_SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} must occur exactly once"
+    mut_c = tmp_path / "mutant.c"
+    mut_c.write_text(src.replace(old, new))
+    so = tmp_path / "mutant.so"
+    r = subprocess.run(["gcc", "-O1", "-std=c11", "-D_DEFAULT_SOURCE", "-fPIC", "-shared",
+                        str(mut_c), "-o", str(so), "-lm"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    failed = P.failing_pins(Oracle(str(so)))
+    assert failed, f"no pin caught the planted mistake {name}"
