@@ -1,0 +1,189 @@
+/*
+ * tpmlp.h -- C ABI of the GB300 (sm_103a) tensor-parallel Transformer MLP block.
+ *
+ * The block is the Megatron-LM MLP with the column-then-row split:
+ *
+ *     Y = GeLU(X A + b1) B + b2 + residual
+ *
+ * A [h, F] is split by columns into A_1..A_t, B [F, h] by rows into
+ * B_1..B_t, b1 [F] with A's columns ("Megatron-LM: Tensor Model Parallel",
+ * charles2530.github.io, section "MLP: Column Parallel first, then Row
+ * Parallel", Figure 3a).  Shard i computes GeLU(X A_i + b1_i) locally and
+ * contributes the partial product H_i B_i to the g-operator sum; the backward
+ * pass gathers dX through the f-operator sum (same page, section "f / g
+ * Operators", Figure 4).  All t shards run on the calling GPU: the g and f
+ * sums are fp32 accumulations inside the row-parallel GEMMs, not collectives.
+ * GeLU is the tanh approximation 0.5 x (1 + tanh(sqrt(2/pi)(x + 0.044715 x^3)))
+ * (the pages name GeLU without defining it).
+ *
+ * Conventions shared by every entry point:
+ *  - T tokens, hidden size h, FFN width F, shard count t, shard width
+ *    f = F / t.  Matrices are dense row-major with no padding.
+ *  - Tensors are bfloat16 (raw 16-bit patterns, type tpmlp_bf16) except the
+ *    bias gradients db1/db2 and the workspace, which are float32.
+ *    Products accumulate in float32; bf16 outputs are rounded to nearest even.
+ *  - Every pointer is a DEVICE pointer into memory the caller allocated and
+ *    owns, aligned to 16 bytes.  The library allocates nothing and keeps no
+ *    reference to any buffer after the call returns.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream).  Outputs must not alias inputs.
+ *  - Shape rules: T >= 0, h >= 8, F >= 8, 1 <= t <= TPMLP_MAX_SHARDS,
+ *    F % t == 0, h % 8 == 0 and f % 8 == 0 (16-byte row strides, the tensor
+ *    memory accelerator's rule), T, h, F < 2^31.  T == 0 is a valid empty
+ *    batch.
+ *  - Return value: TPMLP_OK, or an error code below; arguments are checked
+ *    before anything is launched, so a rejected call has no effect.  A launch
+ *    failure returns TPMLP_ERR_LAUNCH and tpmlp_last_cuda_error() holds the
+ *    CUDA error.  Device-side waits are bounded: a kernel whose wait gives up
+ *    records TPMLP_ERR_DEVICE_TIMEOUT in a device status word, which
+ *    tpmlp_device_status() reads (synchronously) and clears.
+ *  - Thread safety: entry points hold no mutable host state except a
+ *    once-per-process lookup of the driver's tensor-map encoder and a
+ *    once-per-device kernel attribute setup, both guarded.
+ */
+#ifndef TPMLP_H
+#define TPMLP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t tpmlp_bf16; /* raw bfloat16 bits */
+
+#define TPMLP_MAX_SHARDS 64
+
+enum tpmlp_status {
+    TPMLP_OK = 0,
+    TPMLP_ERR_NULL = 1,           /* a required pointer is NULL */
+    TPMLP_ERR_SHAPE = 2,          /* a shape rule above is violated */
+    TPMLP_ERR_ALIGN = 3,          /* a pointer is not 16-byte aligned */
+    TPMLP_ERR_WORKSPACE = 4,      /* workspace missing or too small */
+    TPMLP_ERR_LAUNCH = 5,         /* a CUDA call failed; see tpmlp_last_cuda_error */
+    TPMLP_ERR_DEVICE_TIMEOUT = 6, /* a bounded device wait gave up */
+    TPMLP_ERR_UNSUPPORTED = 7     /* the current device is not sm_103 */
+};
+
+/* ---------------------------------------------------------------------- */
+/* Whole block                                                             */
+/* ---------------------------------------------------------------------- */
+
+/* Forward pass (steps a2 + a3 below):
+ *   Z = X A + b1, H = GeLU(Z)         (all t column shards)
+ *   Y = sum_i H_i B_i + b2 + residual (g-operator sum of the row shards)
+ * In:  X [T,h], A [h,F], b1 [F], B [F,h], b2 [h], residual [T,h].
+ * Out: Y [T,h]; Z, H [T,F] are saved for the backward pass. */
+int tp_mlp_forward(const tpmlp_bf16* X, const tpmlp_bf16* A, const tpmlp_bf16* b1,
+                   const tpmlp_bf16* B, const tpmlp_bf16* b2, const tpmlp_bf16* residual,
+                   int T, int h, int F, int t, tpmlp_bf16* Y, tpmlp_bf16* Z, tpmlp_bf16* H,
+                   void* stream);
+
+/* Bytes of float32/bf16 scratch tp_mlp_backward needs for these sizes. */
+size_t tp_mlp_backward_workspace_bytes(int T, int h, int F, int t);
+
+/* Backward pass given dY = dL/dY (steps a4..a9 below):
+ *   db2 = sum_rows dY                      (g backward is the identity)
+ *   dZ_i = (dY B_i^T) * GeLU'(Z_i)         db1_i = sum_rows dZ_i
+ *   dX = sum_i dZ_i A_i^T                  (f-operator sum)
+ *   dA_i = X^T dZ_i ; dB_i = H_i^T dY
+ * In:  dY, X [T,h]; A [h,F]; B [F,h]; Z, H [T,F] from tp_mlp_forward.
+ * Out: dX [T,h], dA [h,F], dB [F,h] (bf16); db1 [F], db2 [h] (float32).
+ * d(residual) equals dY and is not written.  `workspace` must hold
+ * tp_mlp_backward_workspace_bytes(T,h,F,t) bytes (16-byte aligned); its
+ * contents on entry do not matter and on return are unspecified. */
+int tp_mlp_backward(const tpmlp_bf16* dY, const tpmlp_bf16* X, const tpmlp_bf16* A,
+                    const tpmlp_bf16* B, const tpmlp_bf16* Z, const tpmlp_bf16* H,
+                    int T, int h, int F, int t, tpmlp_bf16* dX, tpmlp_bf16* dA,
+                    tpmlp_bf16* dB, float* db1, float* db2, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------- */
+/* The steps of the hot path, one call each.  tp_mlp_forward and          */
+/* tp_mlp_backward are exactly these calls in this order.                  */
+/* ---------------------------------------------------------------------- */
+
+/* a2: column-parallel GEMM with fused bias and GeLU, all t shards in one
+ * launch: Z[:, i f:(i+1) f] = X A_i + b1_i, H = GeLU(Z).
+ * (Figure 3a of the page above: each shard applies GeLU to its own columns
+ * with no synchronisation before the nonlinearity.) */
+int tp_mlp_column_gelu(const tpmlp_bf16* X, const tpmlp_bf16* A, const tpmlp_bf16* b1,
+                       int T, int h, int F, int t, tpmlp_bf16* Z, tpmlp_bf16* H, void* stream);
+
+/* a3: row-parallel GEMM whose fp32 accumulator walks the shards in order,
+ * so the partials H_i B_i meet in the accumulator (the g-operator sum),
+ * with b2 and the residual fused into the epilogue:
+ * Y = sum_i H_i B_i + b2 + residual.  H [T,F], B [F,h] -> Y [T,h]. */
+int tp_mlp_row_sum(const tpmlp_bf16* H, const tpmlp_bf16* B, const tpmlp_bf16* b2,
+                   const tpmlp_bf16* residual, int T, int h, int F, int t, tpmlp_bf16* Y,
+                   void* stream);
+
+/* Float32 elements of partial-sum scratch tp_mlp_bias_grad needs. */
+size_t tp_mlp_bias_grad_workspace_floats(int T, int n);
+
+/* a4 (and the reduction of a6): column sums of a [T, n] bf16 matrix,
+ * db[j] = sum_r G[r, j], in float32, deterministic.  Used for db2 = sum_rows
+ * dY (the g operator is the identity backward, so dY reaches b2 whole).
+ * `partial` must hold tp_mlp_bias_grad_workspace_floats(T, n) floats. */
+int tp_mlp_bias_grad(const tpmlp_bf16* G, int T, int n, float* db, float* partial,
+                     void* stream);
+
+/* Float32 elements of the per-tile column partials tp_mlp_dgelu writes. */
+size_t tp_mlp_dgelu_partial_floats(int T, int F);
+
+/* a5 + a6: dZ_i = (dY B_i^T) * GeLU'(Z_i) for all shards in one launch, with
+ * the db1 column partial sums of each 128-row tile fused into the epilogue
+ * (written to `colsum_partial`, tp_mlp_dgelu_partial_floats(T,F) floats),
+ * then reduced into db1 [F] (float32).
+ * dY [T,h], B [F,h], Z [T,F] -> dZ [T,F] (bf16), db1 [F]. */
+int tp_mlp_dgelu(const tpmlp_bf16* dY, const tpmlp_bf16* B, const tpmlp_bf16* Z, int T, int h,
+                 int F, int t, tpmlp_bf16* dZ, float* db1, float* colsum_partial,
+                 void* stream);
+
+/* a7: dX = sum_i dZ_i A_i^T; the accumulator walks the shards in order, so
+ * the f-operator sum happens in fp32 inside the GEMM.
+ * dZ [T,F], A [h,F] -> dX [T,h]. */
+int tp_mlp_dx(const tpmlp_bf16* dZ, const tpmlp_bf16* A, int T, int h, int F, int t,
+              tpmlp_bf16* dX, void* stream);
+
+/* a8: dA_i = X^T dZ_i for every shard.  X [T,h], dZ [T,F] -> dA [h,F]. */
+int tp_mlp_dA(const tpmlp_bf16* X, const tpmlp_bf16* dZ, int T, int h, int F, int t,
+              tpmlp_bf16* dA, void* stream);
+
+/* a9: dB_i = H_i^T dY for every shard.  H [T,F], dY [T,h] -> dB [F,h]. */
+int tp_mlp_dB(const tpmlp_bf16* H, const tpmlp_bf16* dY, int T, int h, int F, int t,
+              tpmlp_bf16* dB, void* stream);
+
+/* ---------------------------------------------------------------------- */
+/* Status                                                                  */
+/* ---------------------------------------------------------------------- */
+
+/* Static text for a status code. */
+const char* tpmlp_status_string(int status);
+
+/* The CUDA error code (cudaError_t) behind the last TPMLP_ERR_LAUNCH on the
+ * calling thread, 0 if none. */
+int tpmlp_last_cuda_error(void);
+
+/* Reads and clears the device status word of the current device: TPMLP_OK,
+ * or TPMLP_ERR_DEVICE_TIMEOUT if a bounded wait in a kernel gave up since the
+ * last read.  Synchronises the device. Returns TPMLP_ERR_LAUNCH if the read
+ * itself fails. */
+int tpmlp_device_status(void);
+
+/* Number of kernels the last successful call on the calling thread
+ * launched (for launch accounting). */
+int tpmlp_last_launch_count(void);
+
+/* Self-test of the bounded device wait: launches one small kernel whose
+ * thread waits on a barrier that nothing ever completes, with a limit of
+ * `timeout_us` microseconds (1..1000000).  Returns TPMLP_OK after the launch;
+ * tpmlp_device_status() then reports TPMLP_ERR_DEVICE_TIMEOUT. */
+int tpmlp_selftest_bounded_wait(int timeout_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TPMLP_H */

@@ -1,0 +1,262 @@
+"""ctypes binding of ``libtpmlp.so`` (declared in include/tpmlp.h).
+
+Argument marshalling only: each function checks that the tensors are
+contiguous CUDA bfloat16 (or float32) tensors of the right shape, allocates
+the outputs the caller did not pass, and calls the C entry point of the same
+name on the current CUDA stream.  Every step of the computation runs in the
+library's kernels; there is no other code path.  A missing library raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libtpmlp.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "tpmlp.h")
+
+TPMLP_OK = 0
+TPMLP_ERR_NULL = 1
+TPMLP_ERR_SHAPE = 2
+TPMLP_ERR_ALIGN = 3
+TPMLP_ERR_WORKSPACE = 4
+TPMLP_ERR_LAUNCH = 5
+TPMLP_ERR_DEVICE_TIMEOUT = 6
+TPMLP_ERR_UNSUPPORTED = 7
+
+
+class TpMlpError(RuntimeError):
+    def __init__(self, fn: str, status: int, message: str):
+        super().__init__(f"{fn} failed: status {status} ({message})")
+        self.status = status
+
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_S = ctypes.c_size_t
+
+_SIGNATURES = {
+    "tp_mlp_forward": ([_P] * 6 + [_I] * 4 + [_P] * 3 + [_P], _I),
+    "tp_mlp_backward_workspace_bytes": ([_I] * 4, _S),
+    "tp_mlp_backward": ([_P] * 6 + [_I] * 4 + [_P] * 6 + [_S, _P], _I),
+    "tp_mlp_column_gelu": ([_P] * 3 + [_I] * 4 + [_P] * 2 + [_P], _I),
+    "tp_mlp_row_sum": ([_P] * 4 + [_I] * 4 + [_P] + [_P], _I),
+    "tp_mlp_bias_grad_workspace_floats": ([_I, _I], _S),
+    "tp_mlp_bias_grad": ([_P, _I, _I, _P, _P, _P], _I),
+    "tp_mlp_dgelu_partial_floats": ([_I, _I], _S),
+    "tp_mlp_dgelu": ([_P] * 3 + [_I] * 4 + [_P] * 3 + [_P], _I),
+    "tp_mlp_dx": ([_P] * 2 + [_I] * 4 + [_P] + [_P], _I),
+    "tp_mlp_dA": ([_P] * 2 + [_I] * 4 + [_P] + [_P], _I),
+    "tp_mlp_dB": ([_P] * 2 + [_I] * 4 + [_P] + [_P], _I),
+    "tpmlp_status_string": ([_I], ctypes.c_char_p),
+    "tpmlp_last_cuda_error": ([], _I),
+    "tpmlp_device_status": ([], _I),
+    "tpmlp_last_launch_count": ([], _I),
+    "tpmlp_selftest_bounded_wait": ([_I, _P], _I),
+}
+
+
+def declared_functions(header: str = HEADER):
+    """Names of the functions include/tpmlp.h declares."""
+    text = open(header).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\**(t\w+)\s*\(", text, flags=re.M)))
+
+
+def lib(path: str = LIB_PATH):
+    """The loaded library (loads on first use; raises if it was not built)."""
+    global _lib
+    if _lib is None or path != LIB_PATH:
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"CUDA library {path} is missing: build it first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        L = ctypes.CDLL(path)
+        for name, (args, res) in _SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        if path != LIB_PATH:
+            return L
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().tpmlp_status_string(status).decode()
+
+
+def _check(fn: str, status: int):
+    if status != TPMLP_OK:
+        msg = status_string(status)
+        if status == TPMLP_ERR_LAUNCH:
+            msg += f"; CUDA error {lib().tpmlp_last_cuda_error()}"
+        raise TpMlpError(fn, status, msg)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(x: Optional[torch.Tensor], name: str, shape=None, dtype=torch.bfloat16):
+    if x is None:
+        raise ValueError(f"{name} is required")
+    if not x.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if x.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {x.dtype}")
+    if not x.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(x.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(x.shape)}, expected {tuple(shape)}")
+    return x.data_ptr()
+
+
+def _out(x, shape, like: torch.Tensor, dtype=torch.bfloat16):
+    if x is None:
+        return torch.empty(shape, dtype=dtype, device=like.device)
+    return x
+
+
+def last_launch_count() -> int:
+    return int(lib().tpmlp_last_launch_count())
+
+
+def device_status() -> int:
+    return int(lib().tpmlp_device_status())
+
+
+def tp_mlp_column_gelu(X, A, b1, t: int, Z=None, H=None, stream=None):
+    T, h = X.shape
+    F = A.shape[1]
+    Z = _out(Z, (T, F), X)
+    H = _out(H, (T, F), X)
+    _check("tp_mlp_column_gelu", lib().tp_mlp_column_gelu(
+        _ptr(X, "X", (T, h)), _ptr(A, "A", (h, F)), _ptr(b1, "b1", (F,)), T, h, F, t,
+        _ptr(Z, "Z", (T, F)), _ptr(H, "H", (T, F)), _stream(stream)))
+    return Z, H
+
+
+def tp_mlp_row_sum(H, B, b2, residual, t: int, Y=None, stream=None):
+    T, F = H.shape
+    h = B.shape[1]
+    Y = _out(Y, (T, h), H)
+    _check("tp_mlp_row_sum", lib().tp_mlp_row_sum(
+        _ptr(H, "H", (T, F)), _ptr(B, "B", (F, h)), _ptr(b2, "b2", (h,)),
+        _ptr(residual, "residual", (T, h)), T, h, F, t, _ptr(Y, "Y", (T, h)), _stream(stream)))
+    return Y
+
+
+def tp_mlp_forward(X, A, b1, B, b2, residual, t: int, Y=None, Z=None, H=None, stream=None):
+    """Y, Z, H of the block (Z, H saved for the backward pass)."""
+    T, h = X.shape
+    F = A.shape[1]
+    Y = _out(Y, (T, h), X)
+    Z = _out(Z, (T, F), X)
+    H = _out(H, (T, F), X)
+    _check("tp_mlp_forward", lib().tp_mlp_forward(
+        _ptr(X, "X", (T, h)), _ptr(A, "A", (h, F)), _ptr(b1, "b1", (F,)), _ptr(B, "B", (F, h)),
+        _ptr(b2, "b2", (h,)), _ptr(residual, "residual", (T, h)), T, h, F, t,
+        _ptr(Y, "Y", (T, h)), _ptr(Z, "Z", (T, F)), _ptr(H, "H", (T, F)), _stream(stream)))
+    return Y, Z, H
+
+
+def tp_mlp_backward_workspace_bytes(T: int, h: int, F: int, t: int) -> int:
+    return int(lib().tp_mlp_backward_workspace_bytes(T, h, F, t))
+
+
+def tp_mlp_backward(dY, X, A, B, Z, H, t: int, dX=None, dA=None, dB=None, db1=None, db2=None,
+                    workspace=None, stream=None):
+    """dX, dA, dB (bf16) and db1, db2 (float32) of the block."""
+    T, h = X.shape
+    F = A.shape[1]
+    dX = _out(dX, (T, h), X)
+    dA = _out(dA, (h, F), X)
+    dB = _out(dB, (F, h), X)
+    db1 = _out(db1, (F,), X, torch.float32)
+    db2 = _out(db2, (h,), X, torch.float32)
+    need = tp_mlp_backward_workspace_bytes(T, h, F, t)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=X.device)
+    _check("tp_mlp_backward", lib().tp_mlp_backward(
+        _ptr(dY, "dY", (T, h)), _ptr(X, "X", (T, h)), _ptr(A, "A", (h, F)), _ptr(B, "B", (F, h)),
+        _ptr(Z, "Z", (T, F)), _ptr(H, "H", (T, F)), T, h, F, t,
+        _ptr(dX, "dX", (T, h)), _ptr(dA, "dA", (h, F)), _ptr(dB, "dB", (F, h)),
+        _ptr(db1, "db1", (F,), torch.float32), _ptr(db2, "db2", (h,), torch.float32),
+        _ptr(workspace, "workspace", None, torch.uint8), workspace.numel(), _stream(stream)))
+    return dX, dA, dB, db1, db2
+
+
+def tp_mlp_bias_grad(G, db=None, partial=None, stream=None):
+    T, n = G.shape
+    db = _out(db, (n,), G, torch.float32)
+    if partial is None:
+        partial = torch.empty(max(1, int(lib().tp_mlp_bias_grad_workspace_floats(T, n))),
+                              dtype=torch.float32, device=G.device)
+    _check("tp_mlp_bias_grad", lib().tp_mlp_bias_grad(
+        _ptr(G, "G", (T, n)), T, n, _ptr(db, "db", (n,), torch.float32),
+        _ptr(partial, "partial", None, torch.float32), _stream(stream)))
+    return db
+
+
+def tp_mlp_dgelu(dY, B, Z, t: int, dZ=None, db1=None, partial=None, stream=None):
+    T, h = dY.shape
+    F = B.shape[0]
+    dZ = _out(dZ, (T, F), dY)
+    db1 = _out(db1, (F,), dY, torch.float32)
+    if partial is None:
+        partial = torch.empty(max(1, int(lib().tp_mlp_dgelu_partial_floats(T, F))),
+                              dtype=torch.float32, device=dY.device)
+    _check("tp_mlp_dgelu", lib().tp_mlp_dgelu(
+        _ptr(dY, "dY", (T, h)), _ptr(B, "B", (F, h)), _ptr(Z, "Z", (T, F)), T, h, F, t,
+        _ptr(dZ, "dZ", (T, F)), _ptr(db1, "db1", (F,), torch.float32),
+        _ptr(partial, "partial", None, torch.float32), _stream(stream)))
+    return dZ, db1
+
+
+def tp_mlp_dx(dZ, A, t: int, dX=None, stream=None):
+    T, F = dZ.shape
+    h = A.shape[0]
+    dX = _out(dX, (T, h), dZ)
+    _check("tp_mlp_dx", lib().tp_mlp_dx(
+        _ptr(dZ, "dZ", (T, F)), _ptr(A, "A", (h, F)), T, h, F, t, _ptr(dX, "dX", (T, h)),
+        _stream(stream)))
+    return dX
+
+
+def tp_mlp_dA(X, dZ, t: int, dA=None, stream=None):
+    T, h = X.shape
+    F = dZ.shape[1]
+    dA = _out(dA, (h, F), X)
+    _check("tp_mlp_dA", lib().tp_mlp_dA(
+        _ptr(X, "X", (T, h)), _ptr(dZ, "dZ", (T, F)), T, h, F, t, _ptr(dA, "dA", (h, F)),
+        _stream(stream)))
+    return dA
+
+
+def tp_mlp_dB(H, dY, t: int, dB=None, stream=None):
+    T, F = H.shape
+    h = dY.shape[1]
+    dB = _out(dB, (F, h), H)
+    _check("tp_mlp_dB", lib().tp_mlp_dB(
+        _ptr(H, "H", (T, F)), _ptr(dY, "dY", (T, h)), T, h, F, t, _ptr(dB, "dB", (F, h)),
+        _stream(stream)))
+    return dB
+
+
+def selftest_bounded_wait(timeout_us: int, stream=None) -> int:
+    """Runs the bounded-wait self-test kernel and returns the device status."""
+    _check("tpmlp_selftest_bounded_wait",
+           lib().tpmlp_selftest_bounded_wait(timeout_us, _stream(stream)))
+    return device_status()

@@ -1,0 +1,672 @@
+// capi.cu -- the C ABI of the tensor-parallel MLP block (include/tpmlp.h):
+// argument checks, tensor-map construction, tile-space set-up and launches,
+// plus the column-sum (bias-gradient) kernels and the bounded-wait self-test.
+//
+// The block is the Megatron-LM MLP with the column-then-row split ("Megatron-
+// LM: Tensor Model Parallel", charles2530.github.io, section "MLP: Column
+// Parallel first, then Row Parallel", Figure 3a; "f / g Operators", Figure 4).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/tpmlp.h"
+#include "kernels.h"
+
+#define TPMLP_API extern "C" __attribute__((visibility("default")))
+
+namespace tpmlp {
+
+// Device status word: kernels write a nonzero code here when a bounded wait
+// gives up; tpmlp_device_status() reads and clears it.
+__device__ int g_status_word;
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+thread_local int t_last_launches = 0;
+
+// ------------------------------------------------------------- driver hooks
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encoder() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode != nullptr;
+}
+
+struct DeviceInfo {
+    int sms = 0;
+    int* status = nullptr;
+    bool ok = false;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+bool g_dev_ready[kMaxDevices] = {};
+std::mutex g_dev_mutex;
+
+int fail_cuda(cudaError_t e) {
+    t_last_cuda_error = static_cast<int>(e);
+    return TPMLP_ERR_LAUNCH;
+}
+
+// Once per device: SM count, compute capability 10.3, status-word address.
+int device_info(DeviceInfo& out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (dev < 0 || dev >= kMaxDevices) return TPMLP_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (!g_dev_ready[dev]) {
+        DeviceInfo d;
+        int major = 0, minor = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return fail_cuda(e);
+        d.ok = (major == 10 && minor == 3);
+        if (d.ok) {
+            e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status_word);
+            if (e != cudaSuccess) return fail_cuda(e);
+        }
+        g_dev[dev] = d;
+        g_dev_ready[dev] = true;
+    }
+    out = g_dev[dev];
+    return out.ok ? TPMLP_OK : TPMLP_ERR_UNSUPPORTED;
+}
+
+// --------------------------------------------------------- argument checks
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_dims(int T, int h, int F, int t) {
+    if (T < 0 || h < 8 || F < 8 || t < 1 || t > TPMLP_MAX_SHARDS) return TPMLP_ERR_SHAPE;
+    if (F % t != 0 || h % 8 != 0 || (F / t) % 8 != 0) return TPMLP_ERR_SHAPE;
+    return TPMLP_OK;
+}
+
+template <typename... P>
+bool any_null(P... p) {
+    return ((p == nullptr) || ...);
+}
+
+template <typename... P>
+bool all_aligned(P... p) {
+    return (aligned16(p) && ...);
+}
+
+long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
+
+// ------------------------------------------------------------- tensor maps
+
+// 3-D tensor map over a row-major bf16 matrix [rows, cols] whose shard index
+// (t shards) sits on the contiguous dimension (ON_CONTIG: dims {cols/t, t,
+// rows}), on the row dimension (ON_ROWS: dims {cols, rows/t, t}) or nowhere
+// (dims {cols, rows, 1}).  Box: 64 contiguous elements (128 bytes, the
+// swizzle width) by box_rows rows.
+int make_map(CUtensorMap* m, const void* ptr, long long rows, long long cols, int t, int on,
+             int box_rows) {
+    cuuint64_t dims[3], strides[2];
+    cuuint32_t box[3], estr[3] = {1, 1, 1};
+    const cuuint64_t row_bytes = static_cast<cuuint64_t>(cols) * 2;
+    if (on == ON_CONTIG) {
+        const long long cs = cols / t;
+        dims[0] = cs; dims[1] = t; dims[2] = rows;
+        strides[0] = static_cast<cuuint64_t>(cs) * 2; strides[1] = row_bytes;
+        box[0] = 64; box[1] = 1; box[2] = box_rows;
+    } else if (on == ON_ROWS) {
+        const long long rs = rows / t;
+        dims[0] = cols; dims[1] = rs; dims[2] = t;
+        strides[0] = row_bytes; strides[1] = static_cast<cuuint64_t>(rs) * row_bytes;
+        box[0] = 64; box[1] = box_rows; box[2] = 1;
+    } else {
+        dims[0] = cols; dims[1] = rows; dims[2] = 1;
+        strides[0] = row_bytes; strides[1] = static_cast<cuuint64_t>(rows) * row_bytes;
+        box[0] = 64; box[1] = box_rows; box[2] = 1;
+    }
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        t_last_cuda_error = static_cast<int>(r);
+        return TPMLP_ERR_LAUNCH;
+    }
+    return TPMLP_OK;
+}
+
+// One GEMM operand: a row-major [rows, cols] matrix, K-major or MN-major in
+// the product, with its shard placement.
+struct Operand {
+    const void* ptr;
+    long long rows, cols;
+    int on;
+    bool mn_major;
+};
+
+int operand_map(CUtensorMap* m, const Operand& o, int t, int tile_mn) {
+    return make_map(m, o.ptr, o.rows, o.cols, t, o.on, o.mn_major ? BK : tile_mn);
+}
+
+// Fills the tile space of a GEMM with output extent M x N per shard.
+void tile_space(GemmArgs& g, int M, int N, int K, int t, int mode, long long a_bytes,
+                long long b_bytes) {
+    g.M = M;
+    g.N = N;
+    g.shards = t;
+    g.shard_mode = mode;
+    g.m_tiles = static_cast<int>(cdiv(M, BM));
+    g.n_tiles = static_cast<int>(cdiv(N, BN));
+    g.mt_total = g.m_tiles * (mode == SHARD_M ? t : 1);
+    g.nt_total = g.n_tiles * (mode == SHARD_N ? t : 1);
+    g.k_blocks = static_cast<int>(cdiv(K, BK));
+    g.num_tiles = g.mt_total * g.nt_total;
+    // Keep the larger operand's panels read once: walk the other operand's
+    // tiles fastest so concurrent CTAs share the big panel through L2.
+    g.raster_m_fastest = b_bytes >= a_bytes ? 1 : 0;
+}
+
+typedef cudaError_t (*Launcher)(const CUtensorMap&, const CUtensorMap&, const GemmArgs&, int,
+                                cudaStream_t);
+
+int run_gemm(Launcher fn, const Operand& a, const Operand& b, GemmArgs& g, int t,
+             cudaStream_t st, const DeviceInfo& dev) {
+    if (g.num_tiles == 0) return TPMLP_OK;
+    alignas(64) CUtensorMap map_a, map_b;
+    int rc = operand_map(&map_a, a, t, BM);
+    if (rc) return rc;
+    rc = operand_map(&map_b, b, t, BN);
+    if (rc) return rc;
+    g.status = dev.status;
+    const int grid = std::min(g.num_tiles, dev.sms);
+    cudaError_t e = fn(map_a, map_b, g, grid, st);
+    if (e != cudaSuccess) return fail_cuda(e);
+    ++t_last_launches;
+    return TPMLP_OK;
+}
+
+GemmArgs blank_args() {
+    GemmArgs g;
+    std::memset(&g, 0, sizeof g);
+    return g;
+}
+
+const __nv_bfloat16* cb(const tpmlp_bf16* p) { return reinterpret_cast<const __nv_bfloat16*>(p); }
+__nv_bfloat16* mb(tpmlp_bf16* p) { return reinterpret_cast<__nv_bfloat16*>(p); }
+
+// ------------------------------------------------------------ the six GEMMs
+
+int column_gelu(const tpmlp_bf16* X, const tpmlp_bf16* A, const tpmlp_bf16* b1, int T, int h,
+                int F, int t, tpmlp_bf16* Z, tpmlp_bf16* H, cudaStream_t st, const DeviceInfo& d) {
+    const int f = F / t;
+    GemmArgs g = blank_args();
+    tile_space(g, T, f, h, t, SHARD_N, 1LL * T * h, 1LL * h * F);
+    g.a_on = ON_NONE;
+    g.b_on = ON_CONTIG;
+    g.out0 = mb(Z);
+    g.out1 = mb(H);
+    g.ld_out = F;
+    g.bias = cb(b1);
+    Operand a{X, T, h, ON_NONE, false};
+    Operand b{A, h, F, ON_CONTIG, true};
+    return run_gemm(launch_column_gelu, a, b, g, t, st, d);
+}
+
+int row_sum(const tpmlp_bf16* H, const tpmlp_bf16* B, const tpmlp_bf16* b2,
+            const tpmlp_bf16* R, int T, int h, int F, int t, tpmlp_bf16* Y, cudaStream_t st,
+            const DeviceInfo& d) {
+    const int f = F / t;
+    GemmArgs g = blank_args();
+    tile_space(g, T, h, f, t, SHARD_K, 1LL * T * F, 1LL * F * h);
+    g.a_on = ON_CONTIG;
+    g.b_on = ON_ROWS;
+    g.out0 = mb(Y);
+    g.ld_out = h;
+    g.bias = cb(b2);
+    g.aux = cb(R);
+    g.ld_aux = h;
+    Operand a{H, T, F, ON_CONTIG, false};
+    Operand b{B, F, h, ON_ROWS, true};
+    return run_gemm(launch_row_sum, a, b, g, t, st, d);
+}
+
+int dgelu_gemm(const tpmlp_bf16* dY, const tpmlp_bf16* B, const tpmlp_bf16* Z, int T, int h,
+               int F, int t, tpmlp_bf16* dZ, float* colsum, cudaStream_t st, const DeviceInfo& d) {
+    const int f = F / t;
+    GemmArgs g = blank_args();
+    tile_space(g, T, f, h, t, SHARD_N, 1LL * T * h, 1LL * F * h);
+    g.a_on = ON_NONE;
+    g.b_on = ON_ROWS;
+    g.out0 = mb(dZ);
+    g.ld_out = F;
+    g.aux = cb(Z);
+    g.ld_aux = F;
+    g.colsum = colsum;
+    g.ld_colsum = F;
+    Operand a{dY, T, h, ON_NONE, false};
+    Operand b{B, F, h, ON_ROWS, false};
+    return run_gemm(launch_dgelu, a, b, g, t, st, d);
+}
+
+int dx_gemm(const tpmlp_bf16* dZ, const tpmlp_bf16* A, int T, int h, int F, int t,
+            tpmlp_bf16* dX, cudaStream_t st, const DeviceInfo& d) {
+    const int f = F / t;
+    GemmArgs g = blank_args();
+    tile_space(g, T, h, f, t, SHARD_K, 1LL * T * F, 1LL * h * F);
+    g.a_on = ON_CONTIG;
+    g.b_on = ON_CONTIG;
+    g.out0 = mb(dX);
+    g.ld_out = h;
+    Operand a{dZ, T, F, ON_CONTIG, false};
+    Operand b{A, h, F, ON_CONTIG, false};
+    return run_gemm(launch_dx, a, b, g, t, st, d);
+}
+
+int dA_gemm(const tpmlp_bf16* X, const tpmlp_bf16* dZ, int T, int h, int F, int t,
+            tpmlp_bf16* dA, cudaStream_t st, const DeviceInfo& d) {
+    const int f = F / t;
+    GemmArgs g = blank_args();
+    tile_space(g, h, f, T, t, SHARD_N, 1LL * T * h, 1LL * T * F);
+    g.a_on = ON_NONE;
+    g.b_on = ON_CONTIG;
+    g.out0 = mb(dA);
+    g.ld_out = F;
+    Operand a{X, T, h, ON_NONE, true};
+    Operand b{dZ, T, F, ON_CONTIG, true};
+    return run_gemm(launch_weight_grad, a, b, g, t, st, d);
+}
+
+int dB_gemm(const tpmlp_bf16* H, const tpmlp_bf16* dY, int T, int h, int F, int t,
+            tpmlp_bf16* dB, cudaStream_t st, const DeviceInfo& d) {
+    const int f = F / t;
+    GemmArgs g = blank_args();
+    tile_space(g, f, h, T, t, SHARD_M, 1LL * T * F, 1LL * T * h);
+    g.a_on = ON_CONTIG;
+    g.b_on = ON_NONE;
+    g.out0 = mb(dB);
+    g.ld_out = h;
+    Operand a{H, T, F, ON_CONTIG, true};
+    Operand b{dY, T, h, ON_NONE, true};
+    return run_gemm(launch_weight_grad, a, b, g, t, st, d);
+}
+
+// -------------------------------------------------- column sums (bias grads)
+
+constexpr int kColBlock = 64;   // columns per CTA: 8 lanes x 8 bf16 (16 B each)
+constexpr int kSumThreads = 256;
+constexpr int kTargetCtas = 640;
+
+int colsum_chunks(int T, int n) {
+    const long long col_blocks = cdiv(n, kColBlock);
+    long long r = cdiv(kTargetCtas, col_blocks);
+    r = std::min<long long>(r, std::max<long long>(1, cdiv(T, 32)));
+    return static_cast<int>(std::max<long long>(1, r));
+}
+
+// Partial column sums of G [T, n] over one chunk of rows.  A warp covers
+// 64 columns and 4 rows per step (lanes 8j..8j+7 read row 4k+j, 16 B each);
+// the 4 row phases meet by warp shuffle, the 8 warps in shared memory, in a
+// fixed order.  Writes out[blockIdx.y * n + col].
+__global__ void __launch_bounds__(kSumThreads)
+    colsum_partial_kernel(const __nv_bfloat16* __restrict__ G, int T, int n, int rows_per_chunk,
+                          float* __restrict__ out) {
+    __shared__ float part[kSumThreads / 32][kColBlock];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int col0 = blockIdx.x * kColBlock + (lane & 7) * 8;
+    const int r0 = blockIdx.y * rows_per_chunk;
+    const int r1 = min(T, r0 + rows_per_chunk);
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    const bool full_vec = col0 + 8 <= n;
+    for (int r = r0 + warp * 4 + (lane >> 3); r < r1; r += 32) {
+        const __nv_bfloat16* row = G + static_cast<long long>(r) * n + col0;
+        if (full_vec) {
+            const uint4 u = __ldg(reinterpret_cast<const uint4*>(row));
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                acc[2 * j] += __uint_as_float(w[j] << 16);
+                acc[2 * j + 1] += __uint_as_float(w[j] & 0xFFFF0000u);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (col0 + i < n) acc[i] += __bfloat162float(row[i]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        acc[i] += __shfl_xor_sync(0xFFFFFFFFu, acc[i], 8);
+        acc[i] += __shfl_xor_sync(0xFFFFFFFFu, acc[i], 16);
+    }
+    if (lane < 8) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) part[warp][lane * 8 + i] = acc[i];
+    }
+    __syncthreads();
+    if (threadIdx.x < kColBlock) {
+        const int col = blockIdx.x * kColBlock + threadIdx.x;
+        float s = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kSumThreads / 32; ++w) s += part[w][threadIdx.x];
+        if (col < n) out[static_cast<long long>(blockIdx.y) * n + col] = s;
+    }
+}
+
+// out[j] = sum_{i < rows} P[i * n + j], summed in row order.
+__global__ void __launch_bounds__(256)
+    rowsum_kernel(const float* __restrict__ P, int rows, int n, float* __restrict__ out) {
+    const int j = blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= n) return;
+    float s = 0.0f;
+    for (int i = 0; i < rows; ++i) s += P[static_cast<long long>(i) * n + j];
+    out[j] = s;
+}
+
+int launch_rowsum(const float* P, int rows, int n, float* out, cudaStream_t st) {
+    rowsum_kernel<<<static_cast<unsigned>(cdiv(n, 256)), 256, 0, st>>>(P, rows, n, out);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail_cuda(e);
+    ++t_last_launches;
+    return TPMLP_OK;
+}
+
+int bias_grad(const tpmlp_bf16* G, int T, int n, float* db, float* partial, cudaStream_t st) {
+    if (T == 0) {
+        cudaError_t e = cudaMemsetAsync(db, 0, sizeof(float) * static_cast<size_t>(n), st);
+        return e == cudaSuccess ? TPMLP_OK : fail_cuda(e);
+    }
+    const int chunks = colsum_chunks(T, n);
+    const int rows_per_chunk = static_cast<int>(cdiv(T, chunks));
+    dim3 grid(static_cast<unsigned>(cdiv(n, kColBlock)), static_cast<unsigned>(chunks));
+    float* out = chunks == 1 ? db : partial;
+    colsum_partial_kernel<<<grid, kSumThreads, 0, st>>>(cb(G), T, n, rows_per_chunk, out);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail_cuda(e);
+    ++t_last_launches;
+    if (chunks == 1) return TPMLP_OK;
+    return launch_rowsum(partial, chunks, n, db, st);
+}
+
+// ------------------------------------------------------ bounded-wait check
+
+__global__ void wait_selftest_kernel(int* status, unsigned long long limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // Nothing ever arrives on `bar`: the wait must give up by itself.
+        const unsigned long long t0 = global_ns();
+        while (!mbar_try_wait(&bar, 0)) {
+            if (global_ns() - t0 > limit_ns) {
+                atomicExch(status, kStatusTimeout);
+                break;
+            }
+        }
+    }
+}
+
+size_t dgelu_partial_floats(int T, int F) {
+    return static_cast<size_t>(4 * cdiv(T, BM)) * static_cast<size_t>(F);
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct BackwardLayout {
+    size_t dz, colsum, db2, total;
+};
+
+BackwardLayout backward_layout(int T, int h, int F) {
+    BackwardLayout L;
+    L.dz = 0;
+    L.colsum = align256(L.dz + sizeof(uint16_t) * static_cast<size_t>(T) * F);
+    L.db2 = align256(L.colsum + sizeof(float) * dgelu_partial_floats(T, F));
+    const size_t db2_floats = static_cast<size_t>(colsum_chunks(T, h)) * h;
+    L.total = align256(L.db2 + sizeof(float) * db2_floats);
+    return L;
+}
+
+}  // namespace
+}  // namespace tpmlp
+
+using namespace tpmlp;
+
+// ======================================================================
+//                                 C ABI
+// ======================================================================
+
+#define TPMLP_PROLOGUE(dims_check)                 \
+    t_last_launches = 0;                           \
+    {                                              \
+        int rc_ = (dims_check);                    \
+        if (rc_) return rc_;                       \
+    }
+
+static int enter(DeviceInfo& d) {
+    if (!get_encoder()) return TPMLP_ERR_UNSUPPORTED;
+    return device_info(d);
+}
+
+TPMLP_API int tp_mlp_column_gelu(const tpmlp_bf16* X, const tpmlp_bf16* A, const tpmlp_bf16* b1,
+                                 int T, int h, int F, int t, tpmlp_bf16* Z, tpmlp_bf16* H,
+                                 void* stream) {
+    TPMLP_PROLOGUE(check_dims(T, h, F, t));
+    if (any_null(X, A, b1, Z, H)) return TPMLP_ERR_NULL;
+    if (!all_aligned(X, A, b1, Z, H)) return TPMLP_ERR_ALIGN;
+    if (T == 0) return TPMLP_OK;
+    DeviceInfo d;
+    if (int rc = enter(d)) return rc;
+    return column_gelu(X, A, b1, T, h, F, t, Z, H, static_cast<cudaStream_t>(stream), d);
+}
+
+TPMLP_API int tp_mlp_row_sum(const tpmlp_bf16* H, const tpmlp_bf16* B, const tpmlp_bf16* b2,
+                             const tpmlp_bf16* residual, int T, int h, int F, int t, tpmlp_bf16* Y,
+                             void* stream) {
+    TPMLP_PROLOGUE(check_dims(T, h, F, t));
+    if (any_null(H, B, b2, residual, Y)) return TPMLP_ERR_NULL;
+    if (!all_aligned(H, B, b2, residual, Y)) return TPMLP_ERR_ALIGN;
+    if (T == 0) return TPMLP_OK;
+    DeviceInfo d;
+    if (int rc = enter(d)) return rc;
+    return row_sum(H, B, b2, residual, T, h, F, t, Y, static_cast<cudaStream_t>(stream), d);
+}
+
+TPMLP_API int tp_mlp_forward(const tpmlp_bf16* X, const tpmlp_bf16* A, const tpmlp_bf16* b1,
+                             const tpmlp_bf16* B, const tpmlp_bf16* b2,
+                             const tpmlp_bf16* residual, int T, int h, int F, int t,
+                             tpmlp_bf16* Y, tpmlp_bf16* Z, tpmlp_bf16* H, void* stream) {
+    TPMLP_PROLOGUE(check_dims(T, h, F, t));
+    if (any_null(X, A, b1, B, b2, residual, Y, Z, H)) return TPMLP_ERR_NULL;
+    if (!all_aligned(X, A, b1, B, b2, residual, Y, Z, H)) return TPMLP_ERR_ALIGN;
+    if (T == 0) return TPMLP_OK;
+    DeviceInfo d;
+    if (int rc = enter(d)) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (int rc = column_gelu(X, A, b1, T, h, F, t, Z, H, st, d)) return rc;
+    return row_sum(H, B, b2, residual, T, h, F, t, Y, st, d);
+}
+
+TPMLP_API size_t tp_mlp_bias_grad_workspace_floats(int T, int n) {
+    if (T < 0 || n < 1) return 0;
+    return static_cast<size_t>(colsum_chunks(T, n)) * static_cast<size_t>(n);
+}
+
+TPMLP_API int tp_mlp_bias_grad(const tpmlp_bf16* G, int T, int n, float* db, float* partial,
+                               void* stream) {
+    t_last_launches = 0;
+    if (T < 0 || n < 8 || n % 8 != 0) return TPMLP_ERR_SHAPE;
+    if (any_null(G, db, partial)) return TPMLP_ERR_NULL;
+    if (!all_aligned(G, db, partial)) return TPMLP_ERR_ALIGN;
+    DeviceInfo d;
+    if (int rc = enter(d)) return rc;
+    return bias_grad(G, T, n, db, partial, static_cast<cudaStream_t>(stream));
+}
+
+TPMLP_API size_t tp_mlp_dgelu_partial_floats(int T, int F) {
+    if (T < 0 || F < 1) return 0;
+    return dgelu_partial_floats(T, F);
+}
+
+TPMLP_API int tp_mlp_dgelu(const tpmlp_bf16* dY, const tpmlp_bf16* B, const tpmlp_bf16* Z, int T,
+                           int h, int F, int t, tpmlp_bf16* dZ, float* db1,
+                           float* colsum_partial, void* stream) {
+    TPMLP_PROLOGUE(check_dims(T, h, F, t));
+    if (any_null(dY, B, Z, dZ, db1, colsum_partial)) return TPMLP_ERR_NULL;
+    if (!all_aligned(dY, B, Z, dZ, db1, colsum_partial)) return TPMLP_ERR_ALIGN;
+    DeviceInfo d;
+    if (int rc = enter(d)) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        cudaError_t e = cudaMemsetAsync(db1, 0, sizeof(float) * static_cast<size_t>(F), st);
+        return e == cudaSuccess ? TPMLP_OK : fail_cuda(e);
+    }
+    if (int rc = dgelu_gemm(dY, B, Z, T, h, F, t, dZ, colsum_partial, st, d)) return rc;
+    return launch_rowsum(colsum_partial, static_cast<int>(4 * cdiv(T, BM)), F, db1, st);
+}
+
+TPMLP_API int tp_mlp_dx(const tpmlp_bf16* dZ, const tpmlp_bf16* A, int T, int h, int F, int t,
+                        tpmlp_bf16* dX, void* stream) {
+    TPMLP_PROLOGUE(check_dims(T, h, F, t));
+    if (any_null(dZ, A, dX)) return TPMLP_ERR_NULL;
+    if (!all_aligned(dZ, A, dX)) return TPMLP_ERR_ALIGN;
+    if (T == 0) return TPMLP_OK;
+    DeviceInfo d;
+    if (int rc = enter(d)) return rc;
+    return dx_gemm(dZ, A, T, h, F, t, dX, static_cast<cudaStream_t>(stream), d);
+}
+
+TPMLP_API int tp_mlp_dA(const tpmlp_bf16* X, const tpmlp_bf16* dZ, int T, int h, int F, int t,
+                        tpmlp_bf16* dA, void* stream) {
+    TPMLP_PROLOGUE(check_dims(T, h, F, t));
+    if (any_null(X, dZ, dA)) return TPMLP_ERR_NULL;
+    if (!all_aligned(X, dZ, dA)) return TPMLP_ERR_ALIGN;
+    DeviceInfo d;
+    if (int rc = enter(d)) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        cudaError_t e = cudaMemsetAsync(dA, 0, sizeof(uint16_t) * static_cast<size_t>(h) * F, st);
+        return e == cudaSuccess ? TPMLP_OK : fail_cuda(e);
+    }
+    return dA_gemm(X, dZ, T, h, F, t, dA, st, d);
+}
+
+TPMLP_API int tp_mlp_dB(const tpmlp_bf16* H, const tpmlp_bf16* dY, int T, int h, int F, int t,
+                        tpmlp_bf16* dB, void* stream) {
+    TPMLP_PROLOGUE(check_dims(T, h, F, t));
+    if (any_null(H, dY, dB)) return TPMLP_ERR_NULL;
+    if (!all_aligned(H, dY, dB)) return TPMLP_ERR_ALIGN;
+    DeviceInfo d;
+    if (int rc = enter(d)) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        cudaError_t e = cudaMemsetAsync(dB, 0, sizeof(uint16_t) * static_cast<size_t>(F) * h, st);
+        return e == cudaSuccess ? TPMLP_OK : fail_cuda(e);
+    }
+    return dB_gemm(H, dY, T, h, F, t, dB, st, d);
+}
+
+TPMLP_API size_t tp_mlp_backward_workspace_bytes(int T, int h, int F, int t) {
+    if (check_dims(T, h, F, t)) return 0;
+    return backward_layout(T, h, F).total;
+}
+
+TPMLP_API int tp_mlp_backward(const tpmlp_bf16* dY, const tpmlp_bf16* X, const tpmlp_bf16* A,
+                              const tpmlp_bf16* B, const tpmlp_bf16* Z, const tpmlp_bf16* H,
+                              int T, int h, int F, int t, tpmlp_bf16* dX, tpmlp_bf16* dA,
+                              tpmlp_bf16* dB, float* db1, float* db2, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+    TPMLP_PROLOGUE(check_dims(T, h, F, t));
+    if (any_null(dY, X, A, B, Z, H, dX, dA, dB, db1, db2)) return TPMLP_ERR_NULL;
+    if (!all_aligned(dY, X, A, B, Z, H, dX, dA, dB, db1, db2)) return TPMLP_ERR_ALIGN;
+    const BackwardLayout L = backward_layout(T, h, F);
+    if (workspace == nullptr || workspace_bytes < L.total) return TPMLP_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return TPMLP_ERR_ALIGN;
+    DeviceInfo d;
+    if (int rc = enter(d)) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    tpmlp_bf16* dZ = reinterpret_cast<tpmlp_bf16*>(ws + L.dz);
+    float* colsum = reinterpret_cast<float*>(ws + L.colsum);
+    float* db2_part = reinterpret_cast<float*>(ws + L.db2);
+    // a4: db2 = sum_rows dY (the g operator passes dY to every shard unchanged)
+    if (int rc = bias_grad(dY, T, h, db2, db2_part, st)) return rc;
+    if (T == 0) {
+        cudaError_t e;
+        if ((e = cudaMemsetAsync(db1, 0, sizeof(float) * static_cast<size_t>(F), st)) != cudaSuccess ||
+            (e = cudaMemsetAsync(dA, 0, sizeof(uint16_t) * static_cast<size_t>(h) * F, st)) != cudaSuccess ||
+            (e = cudaMemsetAsync(dB, 0, sizeof(uint16_t) * static_cast<size_t>(F) * h, st)) != cudaSuccess)
+            return fail_cuda(e);
+        return TPMLP_OK;
+    }
+    // a5 + a6: dZ = (dY B_i^T) * GeLU'(Z_i), db1 partials fused, then reduced
+    if (int rc = dgelu_gemm(dY, B, Z, T, h, F, t, dZ, colsum, st, d)) return rc;
+    if (int rc = launch_rowsum(colsum, static_cast<int>(4 * cdiv(T, BM)), F, db1, st)) return rc;
+    // a7: dX = sum_i dZ_i A_i^T (the f-operator sum inside the accumulator)
+    if (int rc = dx_gemm(dZ, A, T, h, F, t, dX, st, d)) return rc;
+    // a8, a9: weight gradients of every shard
+    if (int rc = dA_gemm(X, dZ, T, h, F, t, dA, st, d)) return rc;
+    return dB_gemm(H, dY, T, h, F, t, dB, st, d);
+}
+
+TPMLP_API const char* tpmlp_status_string(int status) {
+    switch (status) {
+        case TPMLP_OK: return "ok";
+        case TPMLP_ERR_NULL: return "a required pointer is NULL";
+        case TPMLP_ERR_SHAPE: return "invalid shape (need h%8==0, (F/t)%8==0, F%t==0, h,F>=8, T>=0)";
+        case TPMLP_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+        case TPMLP_ERR_WORKSPACE: return "workspace missing or too small";
+        case TPMLP_ERR_LAUNCH: return "a CUDA call failed (see tpmlp_last_cuda_error)";
+        case TPMLP_ERR_DEVICE_TIMEOUT: return "a bounded device wait gave up";
+        case TPMLP_ERR_UNSUPPORTED: return "the current device is not sm_103 or the driver lacks TMA";
+        default: return "unknown status";
+    }
+}
+
+TPMLP_API int tpmlp_last_cuda_error(void) { return t_last_cuda_error; }
+
+TPMLP_API int tpmlp_last_launch_count(void) { return t_last_launches; }
+
+TPMLP_API int tpmlp_device_status(void) {
+    DeviceInfo d;
+    if (int rc = device_info(d)) return rc;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail_cuda(e);
+    int v = 0;
+    if ((e = cudaMemcpy(&v, d.status, sizeof v, cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return fail_cuda(e);
+    const int zero = 0;
+    if ((e = cudaMemcpy(d.status, &zero, sizeof zero, cudaMemcpyHostToDevice)) != cudaSuccess)
+        return fail_cuda(e);
+    return v;
+}
+
+TPMLP_API int tpmlp_selftest_bounded_wait(int timeout_us, void* stream) {
+    t_last_launches = 0;
+    if (timeout_us < 1 || timeout_us > 1000000) return TPMLP_ERR_SHAPE;
+    DeviceInfo d;
+    if (int rc = device_info(d)) return rc;
+    wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        d.status, 1000ull * static_cast<unsigned long long>(timeout_us));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail_cuda(e);
+    t_last_launches = 1;
+    return TPMLP_OK;
+}

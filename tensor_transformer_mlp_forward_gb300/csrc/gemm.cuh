@@ -1,0 +1,439 @@
+// gemm.cuh -- persistent tcgen05/TMEM bf16 GEMM for sm_103a with the MLP
+// block's fused epilogues.
+//
+//   D[m, n] = sum_k A[m, k] * B[n, k]        (fp32 accumulation in TMEM)
+//
+// A is the "rows" operand ([M, K] logically) and B the "columns" operand
+// ([N, K] logically); each is stored K-major (k contiguous) or MN-major
+// (m / n contiguous), chosen per GEMM so that every product of the block's
+// forward and backward pass reads the row-major tensors in place, with no
+// transpose kernel.
+//
+// Shards.  The block's t shards are index ranges of one tensor.  Each
+// operand is addressed through a 3-D tensor map whose middle or outer
+// dimension is the shard index, so a tile never crosses a shard boundary
+// and the tensor memory accelerator zero-fills each shard's ragged tail:
+//   SHARD_N  output columns split (column-parallel GEMM): tiles enumerate
+//            (shard, m tile, n tile inside the shard);
+//   SHARD_M  output rows split (the dB GEMM);
+//   SHARD_K  reduction split (row-parallel GEMM): each output tile walks
+//            shard 0's K range, then shard 1's, ..., accumulating into the
+//            same TMEM accumulator -- the in-device g / f operator sum.
+//
+// CTA layout (192 threads, one CTA per SM, persistent over tiles):
+//   warps 0-3  epilogue: TMEM -> registers -> fused math -> global memory,
+//              warp w owns accumulator rows 32w..32w+31;
+//   warp 4     TMA producer (one thread) feeding a STAGES-deep smem ring;
+//   warp 5     TMEM owner and MMA issuer (one thread).
+// Two 128x256 fp32 accumulators (all 512 TMEM columns) let the epilogue of
+// tile i overlap the mainloop of tile i+1.
+#pragma once
+
+#include "ptx.cuh"
+
+namespace tpmlp {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;  // 64 bf16 = one 128-byte swizzle row
+constexpr int STAGES = 4;
+constexpr int UMMA_K = 16;
+constexpr int A_STAGE_BYTES = BM * BK * 2;  // 16 KiB
+constexpr int B_STAGE_BYTES = BN * BK * 2;  // 32 KiB
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int MN_ATOM_BYTES = 64 * BK * 2;  // one 64-wide MN-major box: 8 KiB
+constexpr int NUM_THREADS = 192;
+constexpr int EPI_THREADS = 128;
+constexpr int TMEM_COLS = 512;
+constexpr int BAR_BYTES = 256;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+
+enum ShardMode { SHARD_NONE = 0, SHARD_N = 1, SHARD_M = 2, SHARD_K = 3 };
+// Where an operand's tensor map carries the shard index.
+enum ShardOn { ON_NONE = 0, ON_CONTIG = 1, ON_ROWS = 2 };
+enum Epilogue { EPI_BIAS_GELU = 0, EPI_BIAS_RESIDUAL = 1, EPI_DGELU = 2, EPI_STORE = 3 };
+
+struct GemmArgs {
+    int M, N;            // output extent of one shard (SHARD_M: M per shard; SHARD_N: N per shard)
+    int shards;          // t
+    int shard_mode;      // ShardMode
+    int a_on, b_on;      // ShardOn of each operand's tensor map
+    int m_tiles;         // m tiles per shard (SHARD_M) or in total
+    int n_tiles;         // n tiles per shard (SHARD_N) or in total
+    int mt_total, nt_total;
+    int k_blocks;        // BK blocks per shard (SHARD_K) or in total
+    int num_tiles;
+    int raster_m_fastest;
+    __nv_bfloat16* out0;  // primary output (Z, Y, dZ, dX, dA or dB)
+    __nv_bfloat16* out1;  // H for EPI_BIAS_GELU
+    long long ld_out;
+    const __nv_bfloat16* bias;  // b1 or b2, indexed by global output column
+    const __nv_bfloat16* aux;   // residual (EPI_BIAS_RESIDUAL) or Z (EPI_DGELU)
+    long long ld_aux;
+    float* colsum;  // EPI_DGELU: column sums per 32-row block, [4 * mt_total][ld_colsum]
+    long long ld_colsum;
+    int* status;    // device status word
+};
+
+struct TileCoord {
+    int m0, n0, s;
+};
+
+__device__ __forceinline__ TileCoord decode_tile(int tile, const GemmArgs& p) {
+    int mi, ni;
+    if (p.raster_m_fastest) {
+        mi = tile % p.mt_total;
+        ni = tile / p.mt_total;
+    } else {
+        ni = tile % p.nt_total;
+        mi = tile / p.nt_total;
+    }
+    TileCoord c;
+    c.s = 0;
+    if (p.shard_mode == SHARD_N) {
+        c.s = ni / p.n_tiles;
+        ni -= c.s * p.n_tiles;
+    } else if (p.shard_mode == SHARD_M) {
+        c.s = mi / p.m_tiles;
+        mi -= c.s * p.m_tiles;
+    }
+    c.m0 = mi * BM;
+    c.n0 = ni * BN;
+    return c;
+}
+
+// Tensor-map coordinates of an operand element given its contiguous and row
+// indices inside shard s.
+__device__ __forceinline__ void tma_coords(int on, int contig, int row, int s, int& c0, int& c1,
+                                           int& c2) {
+    if (on == ON_CONTIG) {
+        c0 = contig; c1 = s; c2 = row;
+    } else if (on == ON_ROWS) {
+        c0 = contig; c1 = row; c2 = s;
+    } else {
+        c0 = contig; c1 = row; c2 = 0;
+    }
+}
+
+// Loads one operand's [ROWS x BK] slice for k-block starting at k0.
+//  K-major:  one box of 64 (k) x ROWS (m or n), rows 128 B apart.
+//  MN-major: ROWS/64 boxes of 64 (m or n) x BK (k), each 8 KiB.
+template <bool MN, int ROWS>
+__device__ __forceinline__ void load_operand(const CUtensorMap* map, uint64_t* bar, uint8_t* dst,
+                                             int on, int mn0, int k0, int s) {
+    int c0, c1, c2;
+    if (!MN) {
+        tma_coords(on, k0, mn0, s, c0, c1, c2);
+        tma_load_3d(map, bar, dst, c0, c1, c2);
+    } else {
+#pragma unroll
+        for (int j = 0; j < ROWS / 64; ++j) {
+            tma_coords(on, mn0 + 64 * j, k0, s, c0, c1, c2);
+            tma_load_3d(map, bar, dst + j * MN_ATOM_BYTES, c0, c1, c2);
+        }
+    }
+}
+
+// Descriptor of the UMMA_K-deep slice `kk` of an operand stage buffer.
+//  K-major:  rows 128 B apart, 8-row groups 1024 B apart (SBO); the k slice
+//            starts 32 B further along the swizzled row.
+//  MN-major: 64-wide MN atoms MN_ATOM_BYTES apart (LBO), 8-deep k groups
+//            1024 B apart (SBO); the k slice starts 16 rows (2048 B) further.
+template <bool MN>
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
+    if (!MN) return smem_desc_sw128(base + kk * (UMMA_K * 2), 16, 1024);
+    return smem_desc_sw128(base + kk * (UMMA_K * 128), MN_ATOM_BYTES, 1024);
+}
+
+// ------------------------------------------------------------ epilogue math
+
+__device__ __forceinline__ float gelu_tanh(float x) {
+    const float c = 0.7978845608028654f;  // sqrt(2 / pi)
+    const float u = c * fmaf(0.044715f * x, x * x, x);
+    return 0.5f * x * (1.0f + tanh_approx(u));
+}
+
+__device__ __forceinline__ float gelu_tanh_grad(float x) {
+    const float c = 0.7978845608028654f;
+    const float x2 = x * x;
+    const float th = tanh_approx(c * fmaf(0.044715f * x, x2, x));
+    return 0.5f * (1.0f + th) + 0.5f * x * (1.0f - th * th) * c * fmaf(3.0f * 0.044715f, x2, 1.0f);
+}
+
+// 32 consecutive bf16 values -> float; entries at or beyond `valid` read 0.
+__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* p, int valid, float (&v)[32]) {
+    if (valid >= 32) {
+        const uint4* q = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint4 u = __ldg(q + i);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
+                v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = i < valid ? __bfloat162float(p[i]) : 0.0f;
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Stores 32 floats as bf16; only the first `valid` are written.
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* p, int valid, const float (&v)[32]) {
+    if (valid >= 32) {
+        uint4* q = reinterpret_cast<uint4*>(p);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint4 u;
+            u.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
+            u.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
+            u.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
+            u.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
+            q[i] = u;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < valid) p[i] = __float2bfloat16_rn(v[i]);
+    }
+}
+
+// Butterfly reduce-scatter over the warp: on return lane l holds the sum of
+// v[l] over all 32 lanes (31 shuffles for 32 columns).
+__device__ __forceinline__ float warp_column_sums(float (&v)[32], int lane) {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < off; ++i) {
+            const float send = upper ? v[i] : v[i + off];
+            const float keep = upper ? v[i + off] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, off);
+        }
+    }
+    return v[0];
+}
+
+// --------------------------------------------------------------- the kernel
+
+template <bool A_MN, bool B_MN, int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    tcgen05_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const GemmArgs p) {
+    extern __shared__ uint8_t smem_raw[];
+    // 128-byte swizzle atoms repeat every 1024 B: align the ring to 1 KiB.
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    uint8_t* ring_a = smem;
+    uint8_t* ring_b = smem + STAGES * A_STAGE_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint64_t* full = bars;                 // TMA landed      (STAGES)
+    uint64_t* empty = bars + STAGES;       // MMA drained     (STAGES)
+    uint64_t* acc_full = bars + 2 * STAGES;  // accumulator ready (2)
+    uint64_t* acc_empty = acc_full + 2;      // accumulator read  (2)
+    uint64_t* drain = acc_empty + 2;         // teardown          (1)
+    uint32_t* misc = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile uint32_t* abort_flag = misc + 1;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&acc_full[a], 1);
+            mbar_init(&acc_empty[a], 4);  // one arrival per epilogue warp
+        }
+        mbar_init(drain, 1);
+        misc[1] = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(&misc[0], TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == 4 && lane == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = misc[0];
+    const int total_kb = p.shard_mode == SHARD_K ? p.k_blocks * p.shards : p.k_blocks;
+
+    if (warp == 4) {
+        // ---------------------------------------------------- TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued = 0, issued_phase = 0;  // per-stage bits of the last issue
+            for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+                const TileCoord tc = decode_tile(tile, p);
+                bool ok = true;
+                for (int kb = 0; kb < total_kb; ++kb) {
+                    if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    int s = tc.s, k0 = kb * BK;
+                    if (p.shard_mode == SHARD_K) {
+                        s = kb / p.k_blocks;
+                        k0 = (kb - s * p.k_blocks) * BK;
+                    }
+                    mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+                    load_operand<A_MN, BM>(&tmA, &full[stage], ring_a + stage * A_STAGE_BYTES,
+                                           p.a_on, tc.m0, k0, s);
+                    load_operand<B_MN, BN>(&tmB, &full[stage], ring_b + stage * B_STAGE_BYTES,
+                                           p.b_on, tc.n0, k0, s);
+                    issued |= 1u << stage;
+                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+            }
+            // Every copy this thread started lands before the CTA may exit.
+            for (int s = 0; s < STAGES; ++s)
+                if (issued & (1u << s)) wait_drain(&full[s], (issued_phase >> s) & 1u, p.status);
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int count = 0;
+            for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++count) {
+                const int acc = count & 1;
+                const uint32_t acc_phase = (count >> 1) & 1;
+                if (!wait_bounded(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                bool ok = true;
+                for (int kb = 0; kb < total_kb; ++kb) {
+                    if (!wait_bounded(&full[stage], phase, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_base = smem_u32(ring_a + stage * A_STAGE_BYTES);
+                    const uint32_t b_base = smem_u32(ring_b + stage * B_STAGE_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                        tc_mma_f16(d_tmem, operand_desc<A_MN>(a_base, kk),
+                                   operand_desc<B_MN>(b_base, kk), idesc,
+                                   (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    tc_commit(&empty[stage]);  // frees the stage when these MMAs finish
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(&acc_full[acc]);
+            }
+            // No MMA may still be writing TMEM when it is released.
+            tc_commit(drain);
+            wait_drain(drain, 0, p.status);
+        }
+        __syncwarp();
+    } else {
+        // -------------------------------------------------------- epilogue
+        const int q = warp;  // TMEM lane quadrant == accumulator rows 32q..32q+31
+        int count = 0;
+        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++count) {
+            const TileCoord tc = decode_tile(tile, p);
+            const int acc = count & 1;
+            const uint32_t acc_phase = (count >> 1) & 1;
+            if (!wait_bounded(&acc_full[acc], acc_phase, abort_flag, p.status)) break;
+            tc_fence_after();
+
+            const int m = tc.m0 + q * 32 + lane;  // row inside the shard
+            const bool row_ok = m < p.M;
+            long long grow = m, gcol0 = tc.n0;
+            if (p.shard_mode == SHARD_N) gcol0 += static_cast<long long>(tc.s) * p.N;
+            if (p.shard_mode == SHARD_M) grow += static_cast<long long>(tc.s) * p.M;
+
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                const int n = tc.n0 + c * 32;
+                uint32_t r[32];
+                tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + c * 32, r);
+                tmem_wait_ld();
+                const int cvalid = min(32, p.N - n);  // columns inside the shard
+                const int valid = row_ok ? cvalid : 0;
+                const long long gcol = gcol0 + c * 32;
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+
+                if constexpr (EPI == EPI_BIAS_GELU) {
+                    if (valid > 0) {
+                        float b[32];
+                        load_bf16x32(p.bias + gcol, valid, b);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] += b[i];
+                        __nv_bfloat16* zrow = p.out0 + grow * p.ld_out + gcol;
+                        store_bf16x32(zrow, valid, v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+                        store_bf16x32(p.out1 + grow * p.ld_out + gcol, valid, v);
+                    }
+                } else if constexpr (EPI == EPI_BIAS_RESIDUAL) {
+                    if (valid > 0) {
+                        float b[32], res[32];
+                        load_bf16x32(p.bias + gcol, valid, b);
+                        load_bf16x32(p.aux + grow * p.ld_aux + gcol, valid, res);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] += b[i] + res[i];
+                        store_bf16x32(p.out0 + grow * p.ld_out + gcol, valid, v);
+                    }
+                } else if constexpr (EPI == EPI_DGELU) {
+                    float z[32];
+                    load_bf16x32(p.aux + grow * p.ld_aux + gcol, valid, z);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = i < valid ? v[i] * gelu_tanh_grad(z[i]) : 0.0f;
+                    if (valid > 0) store_bf16x32(p.out0 + grow * p.ld_out + gcol, valid, v);
+                    // db1 partial: lane l gets column n+l summed over this warp's 32 rows;
+                    // one partial row per (128-row tile, warp).
+                    const float cs = warp_column_sums(v, lane);
+                    if (lane < cvalid)
+                        p.colsum[(static_cast<long long>(tc.m0 / BM) * 4 + q) * p.ld_colsum + gcol +
+                                 lane] = cs;
+                } else {
+                    if (valid > 0) store_bf16x32(p.out0 + grow * p.ld_out + gcol, valid, v);
+                }
+            }
+            // TMEM of this accumulator may be overwritten from here on.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+
+        }
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+}  // namespace tpmlp

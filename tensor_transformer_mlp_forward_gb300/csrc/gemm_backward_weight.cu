@@ -1,0 +1,12 @@
+// gemm_backward_weight.cu -- the weight-gradient GEMMs dA = X^T dZ and
+// dB = H^T dY (both operands MN-major: the token dimension is the reduction).
+#include "kernels.h"
+
+namespace tpmlp {
+
+cudaError_t launch_weight_grad(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& g,
+                               int grid, cudaStream_t st) {
+    return launch_gemm<true, true, EPI_STORE>(a, b, g, grid, st);
+}
+
+}  // namespace tpmlp

@@ -1,0 +1,88 @@
+"""The C-ABI library on a host without a GPU: it builds, loads, exports every
+function include/tpmlp.h declares, and rejects bad arguments with the
+documented status codes before touching CUDA."""
+
+import ctypes
+
+import pytest
+
+from tensor_transformer_mlp_forward_gb300 import binding, build
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return binding.lib()
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = binding.declared_functions()
+    assert len(names) >= 15
+    for name in names:
+        assert hasattr(L, name), name
+    assert set(names) == set(binding._SIGNATURES)
+
+
+def test_status_strings(L):
+    for code in range(0, 8):
+        assert binding.status_string(code)
+    assert binding.status_string(99) == "unknown status"
+
+
+# fake device addresses: never dereferenced, because every check below fails
+# before the library calls into CUDA
+P = ctypes.c_void_p(0x10000)
+Q = ctypes.c_void_p(0x10008)  # 8-byte aligned only
+N = None
+
+
+def fwd(L, *, X=P, T=128, h=256, F=1024, t=2, Y=P):
+    return L.tp_mlp_forward(X, P, P, P, P, P, T, h, F, t, Y, P, P, N)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(t=0), dict(t=3), dict(h=12), dict(F=1000, t=8), dict(T=-1), dict(h=0), dict(F=4),
+    dict(t=65, F=65 * 8),
+])
+def test_shape_errors(L, kw):
+    assert fwd(L, **kw) == binding.TPMLP_ERR_SHAPE
+
+
+def test_null_and_alignment_errors(L):
+    assert fwd(L, X=N) == binding.TPMLP_ERR_NULL
+    assert fwd(L, Y=N) == binding.TPMLP_ERR_NULL
+    assert fwd(L, X=Q) == binding.TPMLP_ERR_ALIGN
+    assert L.tp_mlp_dx(P, Q, 128, 256, 1024, 2, P, N) == binding.TPMLP_ERR_ALIGN
+    assert L.tp_mlp_dA(P, P, 128, 256, 1024, 2, N, N) == binding.TPMLP_ERR_NULL
+    assert L.tp_mlp_bias_grad(P, 128, 12, P, P, N) == binding.TPMLP_ERR_SHAPE
+
+
+def test_workspace_errors(L):
+    T, h, F, t = 300, 200, 1536, 4
+    need = L.tp_mlp_backward_workspace_bytes(T, h, F, t)
+    # dZ (bf16) + db1 partials (4 rows per 128-token tile) + db2 partials
+    assert need >= 2 * T * F + 4 * 4 * 3 * F + 4 * h
+    args = [P] * 6 + [T, h, F, t] + [P] * 5
+    assert L.tp_mlp_backward(*args, N, need, N) == binding.TPMLP_ERR_WORKSPACE
+    assert L.tp_mlp_backward(*args, P, need - 1, N) == binding.TPMLP_ERR_WORKSPACE
+    assert L.tp_mlp_backward(*args, Q, need, N) == binding.TPMLP_ERR_ALIGN
+    assert L.tp_mlp_backward_workspace_bytes(T, h, 1000, 8) == 0
+
+
+def test_scratch_sizes(L):
+    assert L.tp_mlp_dgelu_partial_floats(300, 1536) == 4 * 3 * 1536
+    assert L.tp_mlp_dgelu_partial_floats(0, 1536) == 0
+    assert L.tp_mlp_bias_grad_workspace_floats(2048, 20480) >= 20480
+    assert L.tp_mlp_bias_grad_workspace_floats(8, 64) == 64
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="missing"):
+        binding.lib(str(tmp_path / "nope.so"))
+
+
+def test_no_cpu_fallback_in_binding():
+    src = open(binding.__file__).read()
+    assert "import oracle" not in src and "from oracle" not in src
+    for forbidden in ("torch.matmul", "torch.nn.functional", "torch.mm(", ".cpu()"):
+        assert forbidden not in src, forbidden

@@ -1,0 +1,153 @@
+"""CUDA path against the fp64 oracle, element by element, through the C ABI.
+
+Tolerances (fixed by the block's specification: bf16 inputs, fp32
+accumulation): max|gpu - ref| / max|ref| <= 1e-2 for the forward outputs
+(Y, and the saved Z and H) and <= 2e-2 for every gradient.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tensor_transformer_mlp_forward_gb300 import binding, inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL_FWD = 1e-2
+TOL_BWD = 2e-2
+
+
+def rel(got, ref) -> float:
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if ref.size == 0:
+        return 0.0
+    den = float(np.max(np.abs(ref)))
+    err = float(np.max(np.abs(got - ref)))
+    return err / den if den > 0 else err
+
+
+def np64(x: torch.Tensor) -> np.ndarray:
+    return x.detach().to("cpu", torch.float64).numpy()
+
+
+def run_gpu(inp_cpu, t):
+    g = {k: v.cuda() for k, v in inp_cpu.items()}
+    Y, Z, H = binding.tp_mlp_forward(g["X"], g["A"], g["b1"], g["B"], g["b2"], g["residual"], t)
+    dX, dA, dB, db1, db2 = binding.tp_mlp_backward(g["dY"], g["X"], g["A"], g["B"], Z, H, t)
+    torch.cuda.synchronize()
+    assert binding.device_status() == 0
+    return dict(Y=Y, Z=Z, H=H, dX=dX, dA=dA, dB=dB, db1=db1, db2=db2)
+
+
+def check_full(w: inputs.Workload):
+    cpu = inputs.make_inputs(w)
+    out = run_gpu(cpu, w.t)
+    Y, Z, H = oracle.forward(cpu["X"], cpu["A"], cpu["b1"], cpu["B"], cpu["b2"], cpu["residual"], w.t)
+    dX, dA, dB, db1, db2 = oracle.backward(cpu["dY"], cpu["X"], cpu["A"], cpu["b1"], cpu["B"], w.t)
+    errs = {}
+    for name, ref, tol in (("Y", Y, TOL_FWD), ("Z", Z, TOL_FWD), ("H", H, TOL_FWD),
+                           ("dX", dX, TOL_BWD), ("dA", dA, TOL_BWD), ("dB", dB, TOL_BWD),
+                           ("db1", db1, TOL_BWD), ("db2", db2, TOL_BWD)):
+        errs[name] = (rel(np64(out[name]), ref), tol)
+    bad = {k: v for k, v in errs.items() if not v[0] <= v[1]}
+    assert not bad, f"{w}: {errs}"
+    return out
+
+
+# Small problems the oracle finishes in seconds: several tiles in every
+# dimension, ragged tails against the 128 x 256 x 64 tiles, every t.
+SMALL = [
+    inputs.TINY,
+    inputs.custom(T=300, h=200, F=1536, t=1, seed=11),
+    inputs.custom(T=300, h=200, F=1536, t=2, seed=11),
+    inputs.custom(T=300, h=200, F=1536, t=4, seed=11),
+    inputs.custom(T=300, h=200, F=1536, t=8, seed=11),
+    inputs.custom(T=130, h=136, F=2560, t=5, seed=12),     # odd shard count, f = 512
+    inputs.custom(T=257, h=520, F=1600, t=8, seed=13),     # f = 200: ragged shard tail
+    inputs.custom(T=77, h=64, F=512, t=64, seed=14),       # f = 8: one sliver per shard
+    inputs.custom(T=1, h=8, F=8, t=1, seed=15),            # smallest legal block
+    inputs.custom(T=64, h=8, F=16, t=2, seed=16),          # boxes wider than the tensor
+]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: f"T{w.T}_h{w.h}_F{w.F}_t{w.t}")
+def test_small_against_oracle(w):
+    check_full(w)
+
+
+def test_empty_batch():
+    w = inputs.custom(T=0, h=64, F=256, t=2, seed=17)
+    cpu = inputs.make_inputs(w)
+    out = run_gpu(cpu, w.t)
+    for k in ("dA", "dB", "db1", "db2"):
+        assert float(out[k].abs().max()) == 0.0, k
+    for k in ("Y", "Z", "H", "dX"):
+        assert out[k].numel() == 0
+
+
+def test_deterministic():
+    w = inputs.custom(T=300, h=200, F=1536, t=4, seed=18)
+    cpu = inputs.make_inputs(w)
+    a = run_gpu(cpu, w.t)
+    b = run_gpu(cpu, w.t)
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_partition_invariant_on_gpu():
+    """With every shard width a multiple of the 64-deep k block, the shard
+    count changes only the tile boundaries, never a sum's order: all t give
+    bit-identical outputs."""
+    base = None
+    for t in (1, 2, 4, 8):
+        w = inputs.custom(T=300, h=200, F=2048, t=t, seed=19)
+        out = run_gpu(inputs.make_inputs(w), t)
+        if base is None:
+            base = out
+            continue
+        for k in base:
+            assert torch.equal(base[k], out[k]), (t, k)
+
+
+# ---------------------------------------------------------------- full sizes
+
+def check_sampled(w: inputs.Workload, nrows=8, ncols=16):
+    cpu = inputs.make_inputs(w)
+    out = run_gpu(cpu, w.t)
+    rows = inputs.sample_indices(w.T, nrows, w.seed + 1).numpy()
+    cols = inputs.sample_indices(w.F, ncols, w.seed + 2).numpy()
+    Yr, Zr, Hr = oracle.forward_rows(cpu, w.t, rows)
+    dXr = oracle.backward_rows(cpu, w.t, rows)
+    dAc, dBr, db1c = oracle.backward_cols(cpu, w.t, cols)
+    db2 = oracle.db2(cpu["dY"])
+    ri = torch.as_tensor(rows)
+    ci = torch.as_tensor(cols)
+    errs = {
+        "Y": (rel(np64(out["Y"].cpu()[ri]), Yr), TOL_FWD),
+        "Z": (rel(np64(out["Z"].cpu()[ri]), Zr), TOL_FWD),
+        "H": (rel(np64(out["H"].cpu()[ri]), Hr), TOL_FWD),
+        "dX": (rel(np64(out["dX"].cpu()[ri]), dXr), TOL_BWD),
+        "dA": (rel(np64(out["dA"].cpu()[:, ci]), dAc), TOL_BWD),
+        "dB": (rel(np64(out["dB"].cpu()[ci]), dBr), TOL_BWD),
+        "db1": (rel(np64(out["db1"].cpu()[ci]), db1c), TOL_BWD),
+        "db2": (rel(np64(out["db2"].cpu()), db2), TOL_BWD),
+    }
+    bad = {k: v for k, v in errs.items() if not v[0] <= v[1]}
+    assert not bad, f"{w.name} t={w.t}: {errs}"
+
+
+FULL = [
+    inputs.GPT2_MEDIUM.with_shape(T=8192, t=1),
+    inputs.GPT2_MEDIUM.with_shape(T=8192, t=2),
+    inputs.MEGATRON_8_3B,
+    inputs.MTNLG_530B,
+    inputs.SWEEP.with_shape(T=512, t=1),
+    inputs.SWEEP.with_shape(T=16384, t=8),
+]
+
+
+@pytest.mark.parametrize("w", FULL, ids=lambda w: f"{w.name}_T{w.T}_t{w.t}")
+def test_full_size_sampled(w):
+    check_sampled(w)
