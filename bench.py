@@ -1,0 +1,447 @@
+"""Throughput of the tensor-parallel MLP block, forward + backward, on GB300.
+
+One step = one pass of the whole hot path over one batch: the column-
+parallel GEMM with bias + GeLU, the row-parallel GEMM with the in-device
+g-operator sum + b2 + residual, the db2 column sums, the dZ GEMM with GeLU'
+and the fused db1 partials, the dX GEMM with the in-device f-operator sum,
+and the dA / dB weight-gradient GEMMs -- every one a call through the C ABI.
+
+Metric: TFLOPS of fwd+bwd = 12 T h F algorithmic flops per step / time,
+also given as % of the measured dense bf16 peak.
+
+    python bench.py [--gpus N --steps K --warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the fp64 CPU oracle, timed on host cores
+    python bench.py --sweep                 # one line per sweep point (not the headline)
+
+Under torchrun (N > 1) every rank runs an independent replica of the step on
+its own GPU (weak scaling, no collective on the data path); rank 0 prints
+the line with the max time over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "TFLOPS fwd+bwd of TP-sharded MLP block on 1 GB300; % of dense BF16 peak"
+UNIT = "TFLOPS"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_mtnlg_traffic.md")
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--workload", default="mt-nlg-530b")
+    p.add_argument("--tokens", type=int, default=None)
+    p.add_argument("--shards", type=int, default=None)
+    p.add_argument("--sweep", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args(argv)
+
+
+def workload(args):
+    from tensor_transformer_mlp_forward_gb300 import inputs
+
+    w = inputs.WORKLOADS[args.workload]
+    if args.tokens or args.shards:
+        w = w.with_shape(T=args.tokens or w.T, t=args.shards or w.t)
+    return w
+
+
+def describe(w, n_gpus):
+    seq = {"tiny": 64, "gpt2-medium": 1024, "megatron-8.3b": 1024, "mt-nlg-530b": 2048}.get(w.name)
+    cfg = {"workload": f"{w.name} MLP block (T={w.T}, h={w.h}, F={w.F}, t={w.t})",
+           "tokens": w.T, "hidden": w.h, "ffn": w.F, "shards": w.t}
+    if seq and w.T % seq == 0:
+        cfg["batch"], cfg["seq_len"] = w.T // seq, seq
+    big = 2 * w.h * w.F > 129e6
+    cfg["l2"] = ("inputs larger than L2; " if big else "") + "L2 flushed between timed steps (256 MiB write)"
+    cfg["parallelism"] = f"t={w.t} shards in-device; {n_gpus} replica(s)"
+    return cfg
+
+
+# ------------------------------------------------------------------ peaks
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as fh:
+            d = json.load(fh)
+        return float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, FALLBACK_BF16_TFLOPS_SUSTAINED, "fallback"
+
+
+def kernel_source_hash() -> str:
+    d = os.path.join(ROOT, "tensor_transformer_mlp_forward_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(f.encode())
+            h.update(open(os.path.join(d, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, wname: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    try:
+        text = open(TRAFFIC_FILE).read()
+    except OSError:
+        return None
+    src = kernel_source_hash()
+    for m in re.finditer(r"traffic: kernel=(\S+) workload=(\S+) src_sha=(\S+) bytes_per_launch=(\d+)", text):
+        if m.group(1) == kernel and m.group(2) == wname and m.group(3) == src:
+            return int(m.group(4))
+    return None
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.tmp = None
+
+    def __enter__(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.tmp is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.tmp.flush()
+        rows = []
+        with open(self.tmp.name) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+                except ValueError:
+                    continue
+        os.unlink(self.tmp.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for _, _, flags in rows for i, f in enumerate(flags)
+                          if f.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "samples": len(rows), "reasons": reasons}
+
+
+# -------------------------------------------------------------- our step
+
+STEP_CALLS = ("column_gelu", "row_sum", "db2", "dgelu", "dx", "dA", "dB")
+GEMM_CALLS = ("column_gelu", "row_sum", "dx", "dA", "dB")  # one kernel each
+
+
+class Step:
+    """All buffers of one replica, resident in HBM; run() issues one step."""
+
+    def __init__(self, w, device):
+        import torch
+
+        from tensor_transformer_mlp_forward_gb300 import binding, inputs
+
+        self.b = binding
+        self.w = w
+        T, h, F = w.T, w.h, w.F
+        self.cpu = inputs.make_inputs(w)
+        self.inp = {k: v.to(device) for k, v in self.cpu.items()}
+        e = lambda *s, dt=torch.bfloat16: torch.empty(s, dtype=dt, device=device)  # noqa: E731
+        self.Y, self.Z, self.H, self.dZ = e(T, h), e(T, F), e(T, F), e(T, F)
+        self.dX, self.dA, self.dB = e(T, h), e(h, F), e(F, h)
+        self.db1, self.db2 = e(F, dt=torch.float32), e(h, dt=torch.float32)
+        self.p_db1 = e(max(1, int(binding.lib().tp_mlp_dgelu_partial_floats(T, F))), dt=torch.float32)
+        self.p_db2 = e(max(1, int(binding.lib().tp_mlp_bias_grad_workspace_floats(T, h))), dt=torch.float32)
+        self.launches = 0
+
+    def run(self, events=None):
+        """One fwd+bwd step; if `events` (len 8) is given, records them
+        between the calls on the current stream."""
+        b, i, t = self.b, self.inp, self.w.t
+        calls = (
+            lambda: b.tp_mlp_column_gelu(i["X"], i["A"], i["b1"], t, Z=self.Z, H=self.H),
+            lambda: b.tp_mlp_row_sum(self.H, i["B"], i["b2"], i["residual"], t, Y=self.Y),
+            lambda: b.tp_mlp_bias_grad(i["dY"], db=self.db2, partial=self.p_db2),
+            lambda: b.tp_mlp_dgelu(i["dY"], i["B"], self.Z, t, dZ=self.dZ, db1=self.db1, partial=self.p_db1),
+            lambda: b.tp_mlp_dx(self.dZ, i["A"], t, dX=self.dX),
+            lambda: b.tp_mlp_dA(i["X"], self.dZ, t, dA=self.dA),
+            lambda: b.tp_mlp_dB(self.H, i["dY"], t, dB=self.dB),
+        )
+        if events is not None:
+            events[0].record()
+        for k, c in enumerate(calls):
+            c()
+            self.launches += b.last_launch_count()
+            if events is not None:
+                events[k + 1].record()
+
+
+def init_distributed(n_gpus):
+    import torch
+    import torch.distributed as dist
+
+    if n_gpus <= 1 or "RANK" not in os.environ:
+        return 0, 1, 0
+    rank = int(os.environ["RANK"])
+    world = int(os.environ["WORLD_SIZE"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    torch.cuda.set_device(local)
+    dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return rank, world, local
+
+
+def reduce_max_sum(elapsed_s: float, units: float):
+    """Max of the elapsed time and sum of the units over all ranks (host
+    bookkeeping only; identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return elapsed_s, units
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def time_ours(w, steps, warmup, local):
+    import torch
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    step = Step(w, dev)
+    for _ in range(warmup):
+        step.run()
+    torch.cuda.synchronize()
+    assert step.b.device_status() == 0, "device wait timed out during warm-up"
+    step.launches = 0
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STEP_CALLS) + 1)] for _ in range(steps)]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clocks:
+        t0 = time.perf_counter()
+        for k in range(steps):
+            flush.fill_(k & 0xFF)  # evict L2 between steps (outside the events)
+            step.run(evs[k])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    barrier()
+    assert step.b.device_status() == 0, "device wait timed out"
+    launches = step.launches
+    dev_ms = sum(evs[k][0].elapsed_time(evs[k][-1]) for k in range(steps))
+    per_call = {name: [evs[k][j].elapsed_time(evs[k][j + 1]) for k in range(steps)]
+                for j, name in enumerate(STEP_CALLS)}
+    return step, dev_ms / 1e3, wall, per_call, clocks.summary(), launches
+
+
+def time_e2e(step, steps, warmup):
+    """Same step through the public API with the batch tensors (X, residual,
+    dY) copied in from pinned host memory and the activation outputs (Y, dX)
+    copied back every step.  Weights and weight gradients stay resident."""
+    import torch
+
+    i = step.inp
+    host_in = {k: step.cpu[k].pin_memory() for k in ("X", "residual", "dY")}
+    host_out = {k: torch.empty_like(getattr(step, k), device="cpu").pin_memory() for k in ("Y", "dX")}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+    def one():
+        for k, v in host_in.items():
+            i[k].copy_(v, non_blocking=True)
+        step.run()
+        for k, v in host_out.items():
+            v.copy_(getattr(step, k), non_blocking=True)
+
+    for _ in range(max(1, warmup)):
+        one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / 1e3, h2d, d2h
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def oracle_sample(w, cpu, budget_s=20.0, max_rows=64, first=0):
+    """The fp64 oracle, as it stands, on whole token rows of forward +
+    backward (Y row and dX row); returns (flops, seconds, rows, threads)."""
+    import oracle
+    from tensor_transformer_mlp_forward_gb300 import inputs
+
+    rows_all = inputs.sample_indices(w.T, min(w.T, first + max_rows), w.seed + 7).tolist()[first:]
+    per_row = 10 * w.h * w.F  # Z row, Y row, dH row, recomputed Z row, dX row: 5 x 2hF
+    done, spent = 0, 0.0
+    while done < len(rows_all) and (done == 0 or spent < budget_s):
+        r = rows_all[done:done + 1]
+        t0 = time.perf_counter()
+        oracle.forward_rows(cpu, w.t, r)
+        oracle.backward_rows(cpu, w.t, r)
+        spent += time.perf_counter() - t0
+        done += 1
+    return per_row * done, spent, done, oracle.num_threads()
+
+
+def cpu_baseline(w, cpu, budget_s=20.0):
+    flops, secs, rows, threads = oracle_sample(w, cpu, budget_s)
+    return {"value": flops / secs / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{rows} token row(s) of Y and dX (forward + backward, 10*h*F flops each) "
+                      f"of the {w.name} block, fp64, {secs:.1f} s"}
+
+
+# ------------------------------------------------------------------ main
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from tensor_transformer_mlp_forward_gb300 import inputs
+
+    w = workload(args)
+    cpu = inputs.make_inputs(w)
+    total_flops, total_s, rows, threads = 0, 0.0, 0, 1
+    for k in range(args.warmup + args.steps):
+        f, s, r, threads = oracle_sample(w, cpu, budget_s=0.0, max_rows=1, first=k % w.T)
+        if k >= args.warmup:
+            total_flops += f
+            total_s += s
+            rows += r
+    value = total_flops / total_s / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": describe(w, args.gpus),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"each step: 1 token row of Y and dX (forward + backward) of the "
+                                   f"{w.name} block in fp64 ({rows} rows timed)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def run_ours(args, w):
+    import torch
+
+    rank, world, local = init_distributed(args.gpus)
+    step, dev_s, wall, per_call, clocks, launches = time_ours(w, args.steps, args.warmup, local)
+    flops = w.flops_fwd_bwd()
+    max_s, units = reduce_max_sum(dev_s, flops * args.steps)
+    value = units / max_s / 1e12
+
+    e2e = None
+    if not args.no_e2e:
+        e_s, h2d, d2h = time_e2e(step, args.steps, args.warmup)
+        e_max, e_units = reduce_max_sum(e_s, flops * args.steps)
+        e2e = {"value": e_units / e_max / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
+
+    burst, sustained, src = peaks()
+    gemm_flops = 2 * w.T * w.h * w.F
+    avg_ms = {k: statistics.mean(v) for k, v in per_call.items()}
+    dominant = max(GEMM_CALLS, key=lambda k: avg_ms[k])
+    achieved = gemm_flops / (avg_ms[dominant] / 1e3) / 1e12
+    roofline = {"bound": "tensor", "kernel": f"tcgen05_gemm ({dominant})", "achieved": achieved,
+                "peak": sustained, "unit": "TFLOP/s", "frac": achieved / sustained,
+                "peak_source": f"{src} bf16 sustained (MEASURED_PEAKS.json)" if src == "measured"
+                               else "fallback 1.7 PFLOP/s sustained",
+                "traffic": recorded_traffic(dominant, w.name)}
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * max_s / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": describe(w, world),
+        "pct_of_peak": {"burst": 100 * value / world / burst, "sustained": 100 * value / world / sustained,
+                        "source": src},
+        "per_call_ms": {k: round(v, 4) for k, v in avg_ms.items()},
+        "roofline": roofline,
+        "e2e": e2e,
+        "clocks": clocks,
+        "gpu_launches": launches,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(w, step.cpu)
+    print(json.dumps(line))
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.sweep:
+        from tensor_transformer_mlp_forward_gb300 import inputs
+
+        for T in inputs.SWEEP_TOKENS:
+            for t in inputs.SWEEP_SHARDS:
+                a = parse_args(["--workload", "sweep-h4096", "--tokens", str(T), "--shards", str(t),
+                                "--steps", str(args.steps), "--warmup", str(args.warmup),
+                                "--no-cpu-baseline", "--no-e2e"])
+                run_ours(a, workload(a))
+        return 0
+    return run_ours(args, workload(args))
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -24,7 +24,8 @@
  *    Products accumulate in float32; bf16 outputs are rounded to nearest even.
  *  - Every pointer is a DEVICE pointer into memory the caller allocated and
  *    owns, aligned to 16 bytes.  The library allocates nothing and keeps no
- *    reference to any buffer after the call returns.
+ *    reference to any buffer after the call returns.  A pointer to an array
+ *    with no elements (every [T, .] array when T == 0) may be NULL.
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *    default stream).  Outputs must not alias inputs.
  *  - Shape rules: T >= 0, h >= 8, F >= 8, 1 <= t <= TPMLP_MAX_SHARDS,

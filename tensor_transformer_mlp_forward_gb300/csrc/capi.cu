@@ -469,9 +469,9 @@ TPMLP_API int tp_mlp_column_gelu(const tpmlp_bf16* X, const tpmlp_bf16* A, const
                                  int T, int h, int F, int t, tpmlp_bf16* Z, tpmlp_bf16* H,
                                  void* stream) {
     TPMLP_PROLOGUE(check_dims(T, h, F, t));
+    if (T == 0) return TPMLP_OK;
     if (any_null(X, A, b1, Z, H)) return TPMLP_ERR_NULL;
     if (!all_aligned(X, A, b1, Z, H)) return TPMLP_ERR_ALIGN;
-    if (T == 0) return TPMLP_OK;
     DeviceInfo d;
     if (int rc = enter(d)) return rc;
     return column_gelu(X, A, b1, T, h, F, t, Z, H, static_cast<cudaStream_t>(stream), d);
@@ -481,9 +481,9 @@ TPMLP_API int tp_mlp_row_sum(const tpmlp_bf16* H, const tpmlp_bf16* B, const tpm
                              const tpmlp_bf16* residual, int T, int h, int F, int t, tpmlp_bf16* Y,
                              void* stream) {
     TPMLP_PROLOGUE(check_dims(T, h, F, t));
+    if (T == 0) return TPMLP_OK;
     if (any_null(H, B, b2, residual, Y)) return TPMLP_ERR_NULL;
     if (!all_aligned(H, B, b2, residual, Y)) return TPMLP_ERR_ALIGN;
-    if (T == 0) return TPMLP_OK;
     DeviceInfo d;
     if (int rc = enter(d)) return rc;
     return row_sum(H, B, b2, residual, T, h, F, t, Y, static_cast<cudaStream_t>(stream), d);
@@ -494,9 +494,9 @@ TPMLP_API int tp_mlp_forward(const tpmlp_bf16* X, const tpmlp_bf16* A, const tpm
                              const tpmlp_bf16* residual, int T, int h, int F, int t,
                              tpmlp_bf16* Y, tpmlp_bf16* Z, tpmlp_bf16* H, void* stream) {
     TPMLP_PROLOGUE(check_dims(T, h, F, t));
+    if (T == 0) return TPMLP_OK;
     if (any_null(X, A, b1, B, b2, residual, Y, Z, H)) return TPMLP_ERR_NULL;
     if (!all_aligned(X, A, b1, B, b2, residual, Y, Z, H)) return TPMLP_ERR_ALIGN;
-    if (T == 0) return TPMLP_OK;
     DeviceInfo d;
     if (int rc = enter(d)) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -513,7 +513,7 @@ TPMLP_API int tp_mlp_bias_grad(const tpmlp_bf16* G, int T, int n, float* db, flo
                                void* stream) {
     t_last_launches = 0;
     if (T < 0 || n < 8 || n % 8 != 0) return TPMLP_ERR_SHAPE;
-    if (any_null(G, db, partial)) return TPMLP_ERR_NULL;
+    if (any_null(db) || (T > 0 && any_null(G, partial))) return TPMLP_ERR_NULL;
     if (!all_aligned(G, db, partial)) return TPMLP_ERR_ALIGN;
     DeviceInfo d;
     if (int rc = enter(d)) return rc;
@@ -529,7 +529,7 @@ TPMLP_API int tp_mlp_dgelu(const tpmlp_bf16* dY, const tpmlp_bf16* B, const tpml
                            int h, int F, int t, tpmlp_bf16* dZ, float* db1,
                            float* colsum_partial, void* stream) {
     TPMLP_PROLOGUE(check_dims(T, h, F, t));
-    if (any_null(dY, B, Z, dZ, db1, colsum_partial)) return TPMLP_ERR_NULL;
+    if (any_null(db1) || (T > 0 && any_null(dY, B, Z, dZ, colsum_partial))) return TPMLP_ERR_NULL;
     if (!all_aligned(dY, B, Z, dZ, db1, colsum_partial)) return TPMLP_ERR_ALIGN;
     DeviceInfo d;
     if (int rc = enter(d)) return rc;
@@ -545,9 +545,9 @@ TPMLP_API int tp_mlp_dgelu(const tpmlp_bf16* dY, const tpmlp_bf16* B, const tpml
 TPMLP_API int tp_mlp_dx(const tpmlp_bf16* dZ, const tpmlp_bf16* A, int T, int h, int F, int t,
                         tpmlp_bf16* dX, void* stream) {
     TPMLP_PROLOGUE(check_dims(T, h, F, t));
+    if (T == 0) return TPMLP_OK;
     if (any_null(dZ, A, dX)) return TPMLP_ERR_NULL;
     if (!all_aligned(dZ, A, dX)) return TPMLP_ERR_ALIGN;
-    if (T == 0) return TPMLP_OK;
     DeviceInfo d;
     if (int rc = enter(d)) return rc;
     return dx_gemm(dZ, A, T, h, F, t, dX, static_cast<cudaStream_t>(stream), d);
@@ -556,7 +556,7 @@ TPMLP_API int tp_mlp_dx(const tpmlp_bf16* dZ, const tpmlp_bf16* A, int T, int h,
 TPMLP_API int tp_mlp_dA(const tpmlp_bf16* X, const tpmlp_bf16* dZ, int T, int h, int F, int t,
                         tpmlp_bf16* dA, void* stream) {
     TPMLP_PROLOGUE(check_dims(T, h, F, t));
-    if (any_null(X, dZ, dA)) return TPMLP_ERR_NULL;
+    if (any_null(dA) || (T > 0 && any_null(X, dZ))) return TPMLP_ERR_NULL;
     if (!all_aligned(X, dZ, dA)) return TPMLP_ERR_ALIGN;
     DeviceInfo d;
     if (int rc = enter(d)) return rc;
@@ -571,7 +571,7 @@ TPMLP_API int tp_mlp_dA(const tpmlp_bf16* X, const tpmlp_bf16* dZ, int T, int h,
 TPMLP_API int tp_mlp_dB(const tpmlp_bf16* H, const tpmlp_bf16* dY, int T, int h, int F, int t,
                         tpmlp_bf16* dB, void* stream) {
     TPMLP_PROLOGUE(check_dims(T, h, F, t));
-    if (any_null(H, dY, dB)) return TPMLP_ERR_NULL;
+    if (any_null(dB) || (T > 0 && any_null(H, dY))) return TPMLP_ERR_NULL;
     if (!all_aligned(H, dY, dB)) return TPMLP_ERR_ALIGN;
     DeviceInfo d;
     if (int rc = enter(d)) return rc;
@@ -594,10 +594,11 @@ TPMLP_API int tp_mlp_backward(const tpmlp_bf16* dY, const tpmlp_bf16* X, const t
                               tpmlp_bf16* dB, float* db1, float* db2, void* workspace,
                               size_t workspace_bytes, void* stream) {
     TPMLP_PROLOGUE(check_dims(T, h, F, t));
-    if (any_null(dY, X, A, B, Z, H, dX, dA, dB, db1, db2)) return TPMLP_ERR_NULL;
+    if (any_null(A, B, dA, dB, db1, db2) || (T > 0 && any_null(dY, X, Z, H, dX)))
+        return TPMLP_ERR_NULL;
     if (!all_aligned(dY, X, A, B, Z, H, dX, dA, dB, db1, db2)) return TPMLP_ERR_ALIGN;
     const BackwardLayout L = backward_layout(T, h, F);
-    if (workspace == nullptr || workspace_bytes < L.total) return TPMLP_ERR_WORKSPACE;
+    if (T > 0 && (workspace == nullptr || workspace_bytes < L.total)) return TPMLP_ERR_WORKSPACE;
     if (!aligned16(workspace)) return TPMLP_ERR_ALIGN;
     DeviceInfo d;
     if (int rc = enter(d)) return rc;

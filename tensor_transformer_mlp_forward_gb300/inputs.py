@@ -15,22 +15,27 @@ Workloads follow the layer shapes named on the source pages:
   (zzszmyf.github.io), section 4.1 model configuration.
 
 The FFN width is 4h everywhere and T = batch * seq tokens.  Every tensor is
-drawn as float32 N(0, std) from a CPU ``torch.Generator`` in the fixed order
-X, A, b1, B, b2, residual, dY, then rounded to bfloat16 (round to nearest
-even).  A tensor whose std is 0 is all zeros and consumes no draws.
+drawn as float32 N(0, std) on the CPU and rounded to bfloat16 (round to
+nearest even).  Tensor k of X, A, b1, B, b2, residual, dY (in that order)
+and row chunk c of it come from a ``torch.Generator`` seeded with
+(seed, k, c), so any subset of the tensors equals the same entries of the
+full draw.  A tensor whose std is 0 is all zeros.
 """
 
 from __future__ import annotations
 
+import concurrent.futures as cf
 import dataclasses
 import math
+import os
 from typing import Dict, Optional
 
 import torch
 
-# Draws larger than this many elements are produced in row chunks so that the
-# float32 temporary stays small; the chunking is part of the definition of the
-# stream, so results are reproducible for a given seed.
+# Matrices are drawn in row chunks of about this many elements, each chunk
+# from its own generator, so that chunks can be drawn in parallel threads and
+# the float32 temporaries stay small.  The chunking is part of the stream's
+# definition: results depend only on the seed.
 _CHUNK_ELEMS = 1 << 24
 
 DRAW_ORDER = ("X", "A", "b1", "B", "b2", "residual", "dY")
@@ -98,37 +103,38 @@ def custom(T: int, h: int, F: int, t: int, seed: int, std=None, name="custom") -
     return Workload(name, T, h, F, t, dict(std or TINY.std), seed)
 
 
-def _draw(gen: torch.Generator, shape, std: float) -> torch.Tensor:
+def _gen(seed: int, k: int, c: int) -> torch.Generator:
+    g = torch.Generator(device="cpu")
+    g.manual_seed((seed * 1_000_003 + k * 10_007 + c) & 0x7FFFFFFFFFFFFFFF)
+    return g
+
+
+def _draw(seed: int, k: int, shape, std: float) -> torch.Tensor:
     if std == 0.0:
         return torch.zeros(shape, dtype=torch.bfloat16)
-    n = math.prod(shape)
-    if n <= _CHUNK_ELEMS or len(shape) == 1:
-        return (torch.randn(shape, generator=gen, dtype=torch.float32) * std).to(torch.bfloat16)
+    if len(shape) == 1 or math.prod(shape) <= _CHUNK_ELEMS:
+        x = torch.randn(shape, generator=_gen(seed, k, 0), dtype=torch.float32)
+        return (x * std).to(torch.bfloat16)
     rows, cols = shape
     out = torch.empty(shape, dtype=torch.bfloat16)
     step = max(1, _CHUNK_ELEMS // cols)
-    for r0 in range(0, rows, step):
+
+    def chunk(c):
+        r0 = c * step
         r1 = min(rows, r0 + step)
-        chunk = torch.randn((r1 - r0, cols), generator=gen, dtype=torch.float32)
-        out[r0:r1] = (chunk * std).to(torch.bfloat16)
+        x = torch.randn((r1 - r0, cols), generator=_gen(seed, k, c), dtype=torch.float32)
+        out[r0:r1] = (x * std).to(torch.bfloat16)
+
+    n = (rows + step - 1) // step
+    with cf.ThreadPoolExecutor(max_workers=min(n, os.cpu_count() or 1)) as ex:
+        list(ex.map(chunk, range(n)))
     return out
 
 
 def make_inputs(w: Workload, keys=DRAW_ORDER) -> Dict[str, torch.Tensor]:
-    """Draw the workload's bf16 tensors on the CPU (contiguous, row-major).
-
-    ``keys`` may name a subset; tensors are still drawn in ``DRAW_ORDER`` so
-    a subset equals the same entries of the full draw.
-    """
-    gen = torch.Generator(device="cpu")
-    gen.manual_seed(w.seed)
-    out = {}
-    last = max(DRAW_ORDER.index(k) for k in keys)
-    for key in DRAW_ORDER[: last + 1]:
-        t = _draw(gen, w.shape(key), w.std[key])
-        if key in keys:
-            out[key] = t.contiguous()
-    return out
+    """Draw the workload's bf16 tensors on the CPU (contiguous, row-major)."""
+    return {key: _draw(w.seed, DRAW_ORDER.index(key), w.shape(key), w.std[key]).contiguous()
+            for key in DRAW_ORDER if key in keys}
 
 
 def sample_indices(n: int, k: int, seed: int) -> torch.Tensor:
@@ -140,3 +146,4 @@ def sample_indices(n: int, k: int, seed: int) -> torch.Tensor:
     if k and (n - 1) not in idx.tolist():
         idx[-1] = n - 1
     return torch.sort(idx).values.to(torch.int64)
+
