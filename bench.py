@@ -45,7 +45,7 @@ FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--steps", type=int, default=40)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--workload", default="mt-nlg-530b")
@@ -116,40 +116,60 @@ def recorded_traffic(kernel: str, wname: str):
 # ----------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    """nvidia-smi samples (every 100 ms) of SM clock and throttle reasons;
+    summary() keeps only the samples taken inside the marked window."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, device_index: int):
         self.dev = device_index
         self.proc = None
         self.tmp = None
+        self.window = None
 
     def __enter__(self):
         try:
             self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.tmp, stderr=subprocess.DEVNULL)
+            deadline = time.time() + 5.0  # let the sampler start before timing begins
+            while time.time() < deadline and os.path.getsize(self.tmp.name) == 0:
+                time.sleep(0.05)
         except Exception:
             self.proc = None
         return self
 
+    def mark(self, start: float, end: float):
+        self.window = (start, end)
+
     def __exit__(self, *exc):
         if self.proc is not None:
+            time.sleep(0.25)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
 
+    @staticmethod
+    def _when(stamp: str):
+        import datetime
+
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(stamp, fmt).timestamp()
+            except ValueError:
+                pass
+        return None
+
     def summary(self):
         if self.proc is None or self.tmp is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.tmp.flush()
         rows = []
         with open(self.tmp.name) as fh:
             for line in fh:
@@ -157,17 +177,22 @@ class ClockSampler:
                 if len(parts) < 8:
                     continue
                 try:
-                    rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+                    rows.append((self._when(parts[0]), float(parts[1]), float(parts[2]),
+                                 float(parts[3]), parts[4:8]))
                 except ValueError:
                     continue
         os.unlink(self.tmp.name)
+        if self.window and rows:
+            lo, hi = self.window
+            inside = [r for r in rows if r[0] is not None and lo - 0.05 <= r[0] <= hi + 0.05]
+            rows = inside or rows
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        reasons = sorted({names[i] for _, _, flags in rows for i, f in enumerate(flags)
+        reasons = sorted({self.NAMES[i] for r in rows for i, f in enumerate(r[4])
                           if f.lower() == "active"})
-        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "samples": len(rows), "reasons": reasons}
+        return {"sm_mhz": statistics.median(r[1] for r in rows), "sm_max_mhz": max(r[2] for r in rows),
+                "power_w_median": statistics.median(r[3] for r in rows), "samples": len(rows),
+                "reasons": reasons}
 
 
 # -------------------------------------------------------------- our step
@@ -274,11 +299,13 @@ def time_ours(w, steps, warmup, local):
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clocks:
         t0 = time.perf_counter()
+        w0 = time.time()
         for k in range(steps):
             flush.fill_(k & 0xFF)  # evict L2 between steps (outside the events)
             step.run(evs[k])
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
+        clocks.mark(w0, time.time())
     barrier()
     assert step.b.device_status() == 0, "device wait timed out"
     launches = step.launches
