@@ -130,6 +130,26 @@ size_t tp_mlp_bias_grad_workspace_floats(int T, int n);
 int tp_mlp_bias_grad(const tpmlp_bf16* G, int T, int n, float* db, float* partial,
                      void* stream);
 
+/* Column sums like tp_mlp_bias_grad, for callers that cannot allocate
+ * device memory (a framework that passes only the tensors it owns and
+ * reserves all other memory, or code that may not call an allocator after
+ * its set-up).  The source pages have no counterpart: this is a service of
+ * the library.  The partial sums go to a fixed 256 KiB array inside the
+ * library (tp_mlp_bias_grad_noalloc_max_floats() floats), so this call
+ * allocates nothing; every GPU that loads the library holds that array
+ * until the process exits.  Arguments as tp_mlp_bias_grad minus `partial`.
+ * Limit: the row-chunk partials, chunks(T, n) * n floats, must fit the
+ * array; every n <= 24576 fits at any T, larger shapes may return
+ * TPMLP_ERR_WORKSPACE (nothing launched).  The first call on each device
+ * looks up the array's device address: make it before any stream capture.
+ * All calls on a device share the array and every call overwrites the part
+ * it uses before reading it, so no clearing is needed; calls whose kernels
+ * overlap on the GPU (different streams, no ordering) race on it. */
+int tp_mlp_bias_grad_noalloc(const tpmlp_bf16* G, int T, int n, float* db, void* stream);
+
+/* Capacity, in floats, of the array tp_mlp_bias_grad_noalloc uses. */
+size_t tp_mlp_bias_grad_noalloc_max_floats(void);
+
 /* Float32 elements of the per-tile column partials tp_mlp_dgelu writes. */
 size_t tp_mlp_dgelu_partial_floats(int T, int F);
 

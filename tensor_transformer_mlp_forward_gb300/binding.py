@@ -50,6 +50,8 @@ _SIGNATURES = {
     "tp_mlp_row_sum": ([_P] * 4 + [_I] * 4 + [_P] + [_P], _I),
     "tp_mlp_bias_grad_workspace_floats": ([_I, _I], _S),
     "tp_mlp_bias_grad": ([_P, _I, _I, _P, _P, _P], _I),
+    "tp_mlp_bias_grad_noalloc": ([_P, _I, _I, _P, _P], _I),
+    "tp_mlp_bias_grad_noalloc_max_floats": ([], _S),
     "tp_mlp_dgelu_partial_floats": ([_I, _I], _S),
     "tp_mlp_dgelu": ([_P] * 3 + [_I] * 4 + [_P] * 3 + [_P], _I),
     "tp_mlp_dx": ([_P] * 2 + [_I] * 4 + [_P] + [_P], _I),
@@ -207,6 +209,18 @@ def tp_mlp_bias_grad(G, db=None, partial=None, stream=None):
     _check("tp_mlp_bias_grad", lib().tp_mlp_bias_grad(
         _ptr(G, "G", (T, n)), T, n, _ptr(db, "db", (n,), torch.float32),
         _ptr(partial, "partial", None, torch.float32), _stream(stream)))
+    return db
+
+
+def tp_mlp_bias_grad_noalloc(G, db=None, stream=None):
+    """Column sums of G [T, n] with the partial sums in the library's own
+    fixed device array, for callers that cannot allocate scratch memory
+    (only `db` is allocated here, and only when the caller did not pass it)."""
+    T, n = G.shape
+    db = _out(db, (n,), G, torch.float32)
+    _check("tp_mlp_bias_grad_noalloc", lib().tp_mlp_bias_grad_noalloc(
+        _ptr(G, "G", (T, n)) if T else None, T, n, _ptr(db, "db", (n,), torch.float32),
+        _stream(stream)))
     return db
 
 

@@ -520,6 +520,65 @@ TPMLP_API int tp_mlp_bias_grad(const tpmlp_bf16* G, int T, int n, float* db, flo
     return bias_grad(G, T, n, db, partial, static_cast<cudaStream_t>(stream));
 }
 
+// ----------------------------------------------------------------------
+// Column sums without any allocation.
+//
+// Some callers cannot allocate device memory at the point where they need
+// the bias gradient: a host framework that hands this library only the
+// tensors it already owns and keeps every other byte of device memory to
+// itself, or a plug-in that is forbidden to call cudaMalloc (or any
+// allocator) once its set-up is over.  For them the partial sums of
+// tp_mlp_bias_grad live in this fixed array instead of a caller buffer.  It
+// is part of the loaded module, so every GPU that loads the library holds
+// its 256 KiB until the process exits.
+constexpr int kNoAllocScratchFloats = 1 << 16;
+static __device__ __align__(256) float g_noalloc_colsum_scratch[kNoAllocScratchFloats];
+
+namespace {
+float* g_noalloc_scratch_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mutex;
+
+// Device address of the array on the current device.  In host code the
+// array's name stands for a host-side shadow, not for device memory, so the
+// address is looked up once per device (with that device current) and kept.
+int noalloc_scratch(float** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (dev < 0 || dev >= kMaxDevices) return TPMLP_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_scratch_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_colsum_scratch);
+        if (e != cudaSuccess) return fail_cuda(e);
+        g_noalloc_scratch_ptr[dev] = static_cast<float*>(p);
+    }
+    *out = g_noalloc_scratch_ptr[dev];
+    return TPMLP_OK;
+}
+}  // namespace
+
+TPMLP_API size_t tp_mlp_bias_grad_noalloc_max_floats(void) {
+    return static_cast<size_t>(kNoAllocScratchFloats);
+}
+
+TPMLP_API int tp_mlp_bias_grad_noalloc(const tpmlp_bf16* G, int T, int n, float* db,
+                                       void* stream) {
+    t_last_launches = 0;
+    if (T < 0 || n < 8 || n % 8 != 0) return TPMLP_ERR_SHAPE;
+    if (any_null(db) || (T > 0 && any_null(G))) return TPMLP_ERR_NULL;
+    if (!all_aligned(G, db)) return TPMLP_ERR_ALIGN;
+    // Same row chunks as tp_mlp_bias_grad; one chunk needs no partials.
+    const int chunks = T == 0 ? 1 : colsum_chunks(T, n);
+    if (chunks > 1 && static_cast<long long>(chunks) * n > kNoAllocScratchFloats)
+        return TPMLP_ERR_WORKSPACE;
+    DeviceInfo d;
+    if (int rc = enter(d)) return rc;
+    float* scratch = nullptr;
+    if (int rc = noalloc_scratch(&scratch)) return rc;
+    return bias_grad(G, T, n, db, scratch, static_cast<cudaStream_t>(stream));
+}
+
 TPMLP_API size_t tp_mlp_dgelu_partial_floats(int T, int F) {
     if (T < 0 || F < 1) return 0;
     return dgelu_partial_floats(T, F);
