@@ -180,6 +180,17 @@ int tp_mlp_dB(const tpmlp_bf16* H, const tpmlp_bf16* dY, int T, int h, int F, in
 /* Status                                                                  */
 /* ---------------------------------------------------------------------- */
 
+/* Which GEMM kernel the library launches (process-wide; returns the
+ * previous mode, or -1 for an invalid mode):
+ *   0  single-CTA kernel (128 x 256 output tiles, one SM each);
+ *   1  default: CTA pairs (cluster of 2, 256 x 256 tiles shared by two SMs
+ *      through tcgen05 cta_group::2) when the problem has at least as many
+ *      256 x 256 tiles as the GPU has SM pairs, else single CTAs;
+ *   2  CTA pairs always.
+ * Both kernels compute the same sums in the same order, so results are
+ * bitwise identical across modes. */
+int tpmlp_set_cta_pair_mode(int mode);
+
 /* Static text for a status code. */
 const char* tpmlp_status_string(int status);
 

@@ -62,6 +62,7 @@ _SIGNATURES = {
     "tpmlp_device_status": ([], _I),
     "tpmlp_last_launch_count": ([], _I),
     "tpmlp_selftest_bounded_wait": ([_I, _P], _I),
+    "tpmlp_set_cta_pair_mode": ([_I], _I),
 }
 
 
@@ -133,6 +134,15 @@ def _out(x, shape, like: torch.Tensor, dtype=torch.bfloat16):
 
 def last_launch_count() -> int:
     return int(lib().tpmlp_last_launch_count())
+
+
+def set_cta_pair_mode(mode: int) -> int:
+    """0 single-CTA GEMMs, 1 CTA pairs when the problem fills them (default),
+    2 CTA pairs always.  Returns the previous mode."""
+    prev = int(lib().tpmlp_set_cta_pair_mode(mode))
+    if prev < 0:
+        raise ValueError(f"invalid mode {mode}")
+    return prev
 
 
 def device_status() -> int:

@@ -10,6 +10,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -158,18 +159,21 @@ struct Operand {
     bool mn_major;
 };
 
-int operand_map(CUtensorMap* m, const Operand& o, int t, int tile_mn) {
-    return make_map(m, o.ptr, o.rows, o.cols, t, o.on, o.mn_major ? BK : tile_mn);
+int operand_map(CUtensorMap* m, const Operand& o, int t, int tile_rows) {
+    return make_map(m, o.ptr, o.rows, o.cols, t, o.on, o.mn_major ? BK : tile_rows);
 }
+
+// 0: single-CTA kernel only, 1: CTA pairs when the problem fills them, 2: pairs always.
+std::atomic<int> g_pair_mode{1};
 
 // Fills the tile space of a GEMM with output extent M x N per shard.
 void tile_space(GemmArgs& g, int M, int N, int K, int t, int mode, long long a_bytes,
-                long long b_bytes) {
+                long long b_bytes, int tile_m) {
     g.M = M;
     g.N = N;
     g.shards = t;
     g.shard_mode = mode;
-    g.m_tiles = static_cast<int>(cdiv(M, BM));
+    g.m_tiles = static_cast<int>(cdiv(M, tile_m));
     g.n_tiles = static_cast<int>(cdiv(N, BN));
     g.mt_total = g.m_tiles * (mode == SHARD_M ? t : 1);
     g.nt_total = g.n_tiles * (mode == SHARD_N ? t : 1);
@@ -180,20 +184,32 @@ void tile_space(GemmArgs& g, int M, int N, int K, int t, int mode, long long a_b
     g.raster_m_fastest = b_bytes >= a_bytes ? 1 : 0;
 }
 
-typedef cudaError_t (*Launcher)(const CUtensorMap&, const CUtensorMap&, const GemmArgs&, int,
+typedef cudaError_t (*Launcher)(const CUtensorMap&, const CUtensorMap&, const GemmArgs&, int, bool,
                                 cudaStream_t);
 
-int run_gemm(Launcher fn, const Operand& a, const Operand& b, GemmArgs& g, int t,
+// One GEMM: M x N output per shard, K reduction (per shard for SHARD_K).
+struct GemmShape {
+    int M, N, K, t, mode;
+    long long a_bytes, b_bytes;
+};
+
+int run_gemm(Launcher fn, const Operand& a, const Operand& b, GemmArgs& g, const GemmShape& sh,
              cudaStream_t st, const DeviceInfo& dev) {
+    const int pair_mode = g_pair_mode.load(std::memory_order_relaxed);
+    GemmArgs probe = g;
+    tile_space(probe, sh.M, sh.N, sh.K, sh.t, sh.mode, sh.a_bytes, sh.b_bytes, 2 * BM);
+    const bool pair = pair_mode == 2 || (pair_mode == 1 && probe.num_tiles >= dev.sms / 2);
+    tile_space(g, sh.M, sh.N, sh.K, sh.t, sh.mode, sh.a_bytes, sh.b_bytes, pair ? 2 * BM : BM);
     if (g.num_tiles == 0) return TPMLP_OK;
     alignas(64) CUtensorMap map_a, map_b;
-    int rc = operand_map(&map_a, a, t, BM);
+    int rc = operand_map(&map_a, a, sh.t, BM);
     if (rc) return rc;
-    rc = operand_map(&map_b, b, t, BN);
+    rc = operand_map(&map_b, b, sh.t, pair ? BN / 2 : BN);
     if (rc) return rc;
     g.status = dev.status;
-    const int grid = std::min(g.num_tiles, dev.sms);
-    cudaError_t e = fn(map_a, map_b, g, grid, st);
+    const int units = pair ? std::max(1, dev.sms / 2) : dev.sms;
+    const int grid = std::min(g.num_tiles, units);
+    cudaError_t e = fn(map_a, map_b, g, grid, pair, st);
     if (e != cudaSuccess) return fail_cuda(e);
     ++t_last_launches;
     return TPMLP_OK;
@@ -214,7 +230,7 @@ int column_gelu(const tpmlp_bf16* X, const tpmlp_bf16* A, const tpmlp_bf16* b1, 
                 int F, int t, tpmlp_bf16* Z, tpmlp_bf16* H, cudaStream_t st, const DeviceInfo& d) {
     const int f = F / t;
     GemmArgs g = blank_args();
-    tile_space(g, T, f, h, t, SHARD_N, 1LL * T * h, 1LL * h * F);
+    const GemmShape sh{T, f, h, t, SHARD_N, 1LL * T * h, 1LL * h * F};
     g.a_on = ON_NONE;
     g.b_on = ON_CONTIG;
     g.out0 = mb(Z);
@@ -223,7 +239,7 @@ int column_gelu(const tpmlp_bf16* X, const tpmlp_bf16* A, const tpmlp_bf16* b1, 
     g.bias = cb(b1);
     Operand a{X, T, h, ON_NONE, false};
     Operand b{A, h, F, ON_CONTIG, true};
-    return run_gemm(launch_column_gelu, a, b, g, t, st, d);
+    return run_gemm(launch_column_gelu, a, b, g, sh, st, d);
 }
 
 int row_sum(const tpmlp_bf16* H, const tpmlp_bf16* B, const tpmlp_bf16* b2,
@@ -231,7 +247,7 @@ int row_sum(const tpmlp_bf16* H, const tpmlp_bf16* B, const tpmlp_bf16* b2,
             const DeviceInfo& d) {
     const int f = F / t;
     GemmArgs g = blank_args();
-    tile_space(g, T, h, f, t, SHARD_K, 1LL * T * F, 1LL * F * h);
+    const GemmShape sh{T, h, f, t, SHARD_K, 1LL * T * F, 1LL * F * h};
     g.a_on = ON_CONTIG;
     g.b_on = ON_ROWS;
     g.out0 = mb(Y);
@@ -241,14 +257,14 @@ int row_sum(const tpmlp_bf16* H, const tpmlp_bf16* B, const tpmlp_bf16* b2,
     g.ld_aux = h;
     Operand a{H, T, F, ON_CONTIG, false};
     Operand b{B, F, h, ON_ROWS, true};
-    return run_gemm(launch_row_sum, a, b, g, t, st, d);
+    return run_gemm(launch_row_sum, a, b, g, sh, st, d);
 }
 
 int dgelu_gemm(const tpmlp_bf16* dY, const tpmlp_bf16* B, const tpmlp_bf16* Z, int T, int h,
                int F, int t, tpmlp_bf16* dZ, float* colsum, cudaStream_t st, const DeviceInfo& d) {
     const int f = F / t;
     GemmArgs g = blank_args();
-    tile_space(g, T, f, h, t, SHARD_N, 1LL * T * h, 1LL * F * h);
+    const GemmShape sh{T, f, h, t, SHARD_N, 1LL * T * h, 1LL * F * h};
     g.a_on = ON_NONE;
     g.b_on = ON_ROWS;
     g.out0 = mb(dZ);
@@ -259,49 +275,49 @@ int dgelu_gemm(const tpmlp_bf16* dY, const tpmlp_bf16* B, const tpmlp_bf16* Z, i
     g.ld_colsum = F;
     Operand a{dY, T, h, ON_NONE, false};
     Operand b{B, F, h, ON_ROWS, false};
-    return run_gemm(launch_dgelu, a, b, g, t, st, d);
+    return run_gemm(launch_dgelu, a, b, g, sh, st, d);
 }
 
 int dx_gemm(const tpmlp_bf16* dZ, const tpmlp_bf16* A, int T, int h, int F, int t,
             tpmlp_bf16* dX, cudaStream_t st, const DeviceInfo& d) {
     const int f = F / t;
     GemmArgs g = blank_args();
-    tile_space(g, T, h, f, t, SHARD_K, 1LL * T * F, 1LL * h * F);
+    const GemmShape sh{T, h, f, t, SHARD_K, 1LL * T * F, 1LL * h * F};
     g.a_on = ON_CONTIG;
     g.b_on = ON_CONTIG;
     g.out0 = mb(dX);
     g.ld_out = h;
     Operand a{dZ, T, F, ON_CONTIG, false};
     Operand b{A, h, F, ON_CONTIG, false};
-    return run_gemm(launch_dx, a, b, g, t, st, d);
+    return run_gemm(launch_dx, a, b, g, sh, st, d);
 }
 
 int dA_gemm(const tpmlp_bf16* X, const tpmlp_bf16* dZ, int T, int h, int F, int t,
             tpmlp_bf16* dA, cudaStream_t st, const DeviceInfo& d) {
     const int f = F / t;
     GemmArgs g = blank_args();
-    tile_space(g, h, f, T, t, SHARD_N, 1LL * T * h, 1LL * T * F);
+    const GemmShape sh{h, f, T, t, SHARD_N, 1LL * T * h, 1LL * T * F};
     g.a_on = ON_NONE;
     g.b_on = ON_CONTIG;
     g.out0 = mb(dA);
     g.ld_out = F;
     Operand a{X, T, h, ON_NONE, true};
     Operand b{dZ, T, F, ON_CONTIG, true};
-    return run_gemm(launch_weight_grad, a, b, g, t, st, d);
+    return run_gemm(launch_weight_grad, a, b, g, sh, st, d);
 }
 
 int dB_gemm(const tpmlp_bf16* H, const tpmlp_bf16* dY, int T, int h, int F, int t,
             tpmlp_bf16* dB, cudaStream_t st, const DeviceInfo& d) {
     const int f = F / t;
     GemmArgs g = blank_args();
-    tile_space(g, f, h, T, t, SHARD_M, 1LL * T * F, 1LL * T * h);
+    const GemmShape sh{f, h, T, t, SHARD_M, 1LL * T * F, 1LL * T * h};
     g.a_on = ON_CONTIG;
     g.b_on = ON_NONE;
     g.out0 = mb(dB);
     g.ld_out = h;
     Operand a{H, T, F, ON_CONTIG, true};
     Operand b{dY, T, h, ON_NONE, true};
-    return run_gemm(launch_weight_grad, a, b, g, t, st, d);
+    return run_gemm(launch_weight_grad, a, b, g, sh, st, d);
 }
 
 // -------------------------------------------------- column sums (bias grads)
@@ -698,6 +714,11 @@ TPMLP_API const char* tpmlp_status_string(int status) {
         case TPMLP_ERR_UNSUPPORTED: return "the current device is not sm_103 or the driver lacks TMA";
         default: return "unknown status";
     }
+}
+
+TPMLP_API int tpmlp_set_cta_pair_mode(int mode) {
+    if (mode < 0 || mode > 2) return -1;
+    return g_pair_mode.exchange(mode);
 }
 
 TPMLP_API int tpmlp_last_cuda_error(void) { return t_last_cuda_error; }

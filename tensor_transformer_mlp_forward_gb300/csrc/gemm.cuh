@@ -27,26 +27,42 @@
 //   warp 5     TMEM owner and MMA issuer (one thread).
 // Two 128x256 fp32 accumulators (all 512 TMEM columns) let the epilogue of
 // tile i overlap the mainloop of tile i+1.
+//
+// PAIR variant (cluster of 2 CTAs on neighbouring SMs, tcgen05 cta_group::2):
+// the pair computes a 256 x 256 tile.  Each CTA loads its own 128 rows of A
+// and 128 of the 256 B rows; the leader CTA's single thread issues
+// M=256 x N=256 MMAs that read both CTAs' shared memory and write 128
+// accumulator rows into each CTA's TMEM.  Per flop this halves the B traffic
+// into each SM (shared memory and L2), and leaves room for 6 stages.
 #pragma once
 
 #include "ptx.cuh"
 
 namespace tpmlp {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int BK = 64;  // 64 bf16 = one 128-byte swizzle row
-constexpr int STAGES = 4;
+constexpr int BM = 128;  // accumulator rows per CTA (TMEM lanes)
+constexpr int BN = 256;  // accumulator columns (one TMEM accumulator)
+constexpr int BK = 64;   // 64 bf16 = one 128-byte swizzle row
 constexpr int UMMA_K = 16;
-constexpr int A_STAGE_BYTES = BM * BK * 2;  // 16 KiB
-constexpr int B_STAGE_BYTES = BN * BK * 2;  // 32 KiB
-constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int MN_ATOM_BYTES = 64 * BK * 2;  // one 64-wide MN-major box: 8 KiB
 constexpr int NUM_THREADS = 192;
 constexpr int EPI_THREADS = 128;
 constexpr int TMEM_COLS = 512;
 constexpr int BAR_BYTES = 256;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+
+// Per-variant geometry.  Single CTA: a 128 x 256 tile, 4 stages of
+// A 128x64 + B 256x64.  CTA pair (cluster of 2, cta_group::2): a 256 x 256
+// tile, each CTA holding 128 rows of A and 128 rows of B per stage, 6 stages.
+template <bool PAIR>
+struct Geometry {
+    static constexpr int TILE_M = PAIR ? 2 * BM : BM;
+    static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // B rows in this CTA's smem
+    static constexpr int STAGES = PAIR ? 6 : 4;
+    static constexpr int A_STAGE_BYTES = BM * BK * 2;
+    static constexpr int B_STAGE_BYTES = B_ROWS * BK * 2;
+    static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+};
 
 enum ShardMode { SHARD_NONE = 0, SHARD_N = 1, SHARD_M = 2, SHARD_K = 3 };
 // Where an operand's tensor map carries the shard index.
@@ -58,7 +74,7 @@ struct GemmArgs {
     int shards;          // t
     int shard_mode;      // ShardMode
     int a_on, b_on;      // ShardOn of each operand's tensor map
-    int m_tiles;         // m tiles per shard (SHARD_M) or in total
+    int m_tiles;         // m tiles (TILE_M rows) per shard (SHARD_M) or in total
     int n_tiles;         // n tiles per shard (SHARD_N) or in total
     int mt_total, nt_total;
     int k_blocks;        // BK blocks per shard (SHARD_K) or in total
@@ -79,6 +95,7 @@ struct TileCoord {
     int m0, n0, s;
 };
 
+template <int TILE_M>
 __device__ __forceinline__ TileCoord decode_tile(int tile, const GemmArgs& p) {
     int mi, ni;
     if (p.raster_m_fastest) {
@@ -97,7 +114,7 @@ __device__ __forceinline__ TileCoord decode_tile(int tile, const GemmArgs& p) {
         c.s = mi / p.m_tiles;
         mi -= c.s * p.m_tiles;
     }
-    c.m0 = mi * BM;
+    c.m0 = mi * TILE_M;
     c.n0 = ni * BN;
     return c;
 }
@@ -115,22 +132,26 @@ __device__ __forceinline__ void tma_coords(int on, int contig, int row, int s, i
     }
 }
 
-// Loads one operand's [ROWS x BK] slice for k-block starting at k0.
+// Loads one operand's [ROWS x BK] slice for the k-block starting at k0.
 //  K-major:  one box of 64 (k) x ROWS (m or n), rows 128 B apart.
 //  MN-major: ROWS/64 boxes of 64 (m or n) x BK (k), each 8 KiB.
-template <bool MN, int ROWS>
-__device__ __forceinline__ void load_operand(const CUtensorMap* map, uint64_t* bar, uint8_t* dst,
-                                             int on, int mn0, int k0, int s) {
+// PAIR: completion is counted on the pair leader's barrier (`bar_cluster`,
+// a shared::cluster address); otherwise on this CTA's `bar`.
+template <bool MN, int ROWS, bool PAIR>
+__device__ __forceinline__ void load_operand(const CUtensorMap* map, uint64_t* bar,
+                                             uint32_t bar_cluster, uint8_t* dst, int on, int mn0,
+                                             int k0, int s) {
     int c0, c1, c2;
-    if (!MN) {
-        tma_coords(on, k0, mn0, s, c0, c1, c2);
-        tma_load_3d(map, bar, dst, c0, c1, c2);
-    } else {
 #pragma unroll
-        for (int j = 0; j < ROWS / 64; ++j) {
+    for (int j = 0; j < (MN ? ROWS / 64 : 1); ++j) {
+        if (!MN)
+            tma_coords(on, k0, mn0, s, c0, c1, c2);
+        else
             tma_coords(on, mn0 + 64 * j, k0, s, c0, c1, c2);
+        if constexpr (PAIR)
+            tma_load_3d_pair(map, bar_cluster, dst + j * MN_ATOM_BYTES, c0, c1, c2);
+        else
             tma_load_3d(map, bar, dst + j * MN_ATOM_BYTES, c0, c1, c2);
-        }
     }
 }
 
@@ -223,51 +244,65 @@ __device__ __forceinline__ float warp_column_sums(float (&v)[32], int lane) {
 
 // --------------------------------------------------------------- the kernel
 
-template <bool A_MN, bool B_MN, int EPI>
+template <bool A_MN, bool B_MN, int EPI, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tcgen05_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const GemmArgs p) {
+    using G = Geometry<PAIR>;
     extern __shared__ uint8_t smem_raw[];
     // 128-byte swizzle atoms repeat every 1024 B: align the ring to 1 KiB.
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     uint8_t* ring_a = smem;
-    uint8_t* ring_b = smem + STAGES * A_STAGE_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-    uint64_t* full = bars;                 // TMA landed      (STAGES)
-    uint64_t* empty = bars + STAGES;       // MMA drained     (STAGES)
-    uint64_t* acc_full = bars + 2 * STAGES;  // accumulator ready (2)
-    uint64_t* acc_empty = acc_full + 2;      // accumulator read  (2)
-    uint64_t* drain = acc_empty + 2;         // teardown          (1)
+    uint8_t* ring_b = smem + G::STAGES * G::A_STAGE_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + G::STAGES * G::STAGE_BYTES);
+    uint64_t* full = bars;                      // stage loaded  (STAGES)
+    uint64_t* empty = bars + G::STAGES;         // stage drained (STAGES)
+    uint64_t* acc_full = bars + 2 * G::STAGES;  // accumulator ready (2)
+    uint64_t* acc_empty = acc_full + 2;         // accumulator read  (2)
+    uint64_t* drain = acc_empty + 2;            // teardown          (1)
     uint32_t* misc = reinterpret_cast<uint32_t*>(drain + 1);
     volatile uint32_t* abort_flag = misc + 1;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // In a pair, CTA rank 0 (the leader) issues the MMAs for both; rank r
+    // holds accumulator rows 128r..128r+127 and B rows 128r..128r+127.
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < G::STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&acc_full[a], 1);
-            mbar_init(&acc_empty[a], 4);  // one arrival per epilogue warp
+            mbar_init(&acc_empty[a], PAIR ? 8 : 4);  // one arrival per epilogue warp
         }
         mbar_init(drain, 1);
         misc[1] = 0u;
         fence_mbar_init();
     }
     if (warp == 5) {
-        tmem_alloc(&misc[0], TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(&misc[0], TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(&misc[0], TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     if (warp == 4 && lane == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
     }
     tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR)
+        cluster_sync();  // the peer's barriers exist before anyone signals them
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = misc[0];
     const int total_kb = p.shard_mode == SHARD_K ? p.k_blocks * p.shards : p.k_blocks;
@@ -278,8 +313,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued = 0, issued_phase = 0;  // per-stage bits of the last issue
-            for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
-                const TileCoord tc = decode_tile(tile, p);
+            for (int tile = unit; tile < p.num_tiles; tile += units) {
+                const TileCoord tc = decode_tile<G::TILE_M>(tile, p);
                 bool ok = true;
                 for (int kb = 0; kb < total_kb; ++kb) {
                     if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
@@ -291,33 +326,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         s = kb / p.k_blocks;
                         k0 = (kb - s * p.k_blocks) * BK;
                     }
-                    mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-                    load_operand<A_MN, BM>(&tmA, &full[stage], ring_a + stage * A_STAGE_BYTES,
-                                           p.a_on, tc.m0, k0, s);
-                    load_operand<B_MN, BN>(&tmB, &full[stage], ring_b + stage * B_STAGE_BYTES,
-                                           p.b_on, tc.n0, k0, s);
+                    uint32_t bar_cluster = 0;
+                    if constexpr (PAIR) {
+                        // both CTAs' bytes complete the leader's barrier
+                        if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * G::STAGE_BYTES);
+                        bar_cluster = map_to_cta(smem_u32(&full[stage]), 0);
+                    } else {
+                        mbar_arrive_expect_tx(&full[stage], G::STAGE_BYTES);
+                    }
+                    load_operand<A_MN, BM, PAIR>(&tmA, &full[stage], bar_cluster,
+                                                 ring_a + stage * G::A_STAGE_BYTES, p.a_on,
+                                                 tc.m0 + static_cast<int>(rank) * BM, k0, s);
+                    load_operand<B_MN, G::B_ROWS, PAIR>(
+                        &tmB, &full[stage], bar_cluster, ring_b + stage * G::B_STAGE_BYTES, p.b_on,
+                        tc.n0 + static_cast<int>(rank) * G::B_ROWS, k0, s);
                     issued |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-                    if (++stage == STAGES) {
+                    if (++stage == G::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
             }
-            // Every copy this thread started lands before the CTA may exit.
-            for (int s = 0; s < STAGES; ++s)
-                if (issued & (1u << s)) wait_drain(&full[s], (issued_phase >> s) & 1u, p.status);
+            // Every copy this thread started lands before the CTA may exit.  A
+            // pair's copies complete on the leader's barriers, so there the
+            // stage's release by the MMA (which waited for them) is awaited.
+            for (int s = 0; s < G::STAGES; ++s) {
+                if (!(issued & (1u << s))) continue;
+                if constexpr (PAIR)
+                    wait_drain(&empty[s], (issued_phase >> s) & 1u, p.status);
+                else
+                    wait_drain(&full[s], (issued_phase >> s) & 1u, p.status);
+            }
         }
         __syncwarp();
     } else if (warp == 5) {
         // ------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+        if (lane == 0 && rank == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(G::TILE_M, BN, A_MN, B_MN);
             int stage = 0;
             uint32_t phase = 0;
             int count = 0;
-            for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++count) {
+            for (int tile = unit; tile < p.num_tiles; tile += units, ++count) {
                 const int acc = count & 1;
                 const uint32_t acc_phase = (count >> 1) & 1;
                 if (!wait_bounded(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
@@ -330,40 +381,57 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_base = smem_u32(ring_a + stage * A_STAGE_BYTES);
-                    const uint32_t b_base = smem_u32(ring_b + stage * B_STAGE_BYTES);
+                    const uint32_t a_base = smem_u32(ring_a + stage * G::A_STAGE_BYTES);
+                    const uint32_t b_base = smem_u32(ring_b + stage * G::B_STAGE_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        tc_mma_f16(d_tmem, operand_desc<A_MN>(a_base, kk),
-                                   operand_desc<B_MN>(b_base, kk), idesc,
-                                   (kb | kk) != 0 ? 1u : 0u);
+                        const uint64_t ad = operand_desc<A_MN>(a_base, kk);
+                        const uint64_t bd = operand_desc<B_MN>(b_base, kk);
+                        const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
+                        if constexpr (PAIR)
+                            tc_mma_f16_pair(d_tmem, ad, bd, idesc, accum);
+                        else
+                            tc_mma_f16(d_tmem, ad, bd, idesc, accum);
                     }
-                    tc_commit(&empty[stage]);  // frees the stage when these MMAs finish
-                    if (++stage == STAGES) {
+                    // frees the stage (in both CTAs of a pair) when these MMAs finish
+                    if constexpr (PAIR)
+                        tc_commit_pair_multicast(&empty[stage], 0x3);
+                    else
+                        tc_commit(&empty[stage]);
+                    if (++stage == G::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                tc_commit(&acc_full[acc]);
+                if constexpr (PAIR)
+                    tc_commit_pair_multicast(&acc_full[acc], 0x3);
+                else
+                    tc_commit(&acc_full[acc]);
             }
             // No MMA may still be writing TMEM when it is released.
-            tc_commit(drain);
+            if constexpr (PAIR)
+                tc_commit_pair(drain);
+            else
+                tc_commit(drain);
             wait_drain(drain, 0, p.status);
         }
         __syncwarp();
     } else {
         // -------------------------------------------------------- epilogue
         const int q = warp;  // TMEM lane quadrant == accumulator rows 32q..32q+31
+        const uint32_t release_bar =
+            PAIR ? map_to_cta(smem_u32(&acc_empty[0]), 0) : smem_u32(&acc_empty[0]);
         int count = 0;
-        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++count) {
-            const TileCoord tc = decode_tile(tile, p);
+        for (int tile = unit; tile < p.num_tiles; tile += units, ++count) {
+            const TileCoord tc = decode_tile<G::TILE_M>(tile, p);
             const int acc = count & 1;
             const uint32_t acc_phase = (count >> 1) & 1;
             if (!wait_bounded(&acc_full[acc], acc_phase, abort_flag, p.status)) break;
             tc_fence_after();
 
-            const int m = tc.m0 + q * 32 + lane;  // row inside the shard
+            const int m_cta = tc.m0 + static_cast<int>(rank) * BM;  // first row of this CTA
+            const int m = m_cta + q * 32 + lane;                       // row inside the shard
             const bool row_ok = m < p.M;
             long long grow = m, gcol0 = tc.n0;
             if (p.shard_mode == SHARD_N) gcol0 += static_cast<long long>(tc.s) * p.N;
@@ -388,8 +456,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         load_bf16x32(p.bias + gcol, valid, b);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] += b[i];
-                        __nv_bfloat16* zrow = p.out0 + grow * p.ld_out + gcol;
-                        store_bf16x32(zrow, valid, v);
+                        store_bf16x32(p.out0 + grow * p.ld_out + gcol, valid, v);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
                         store_bf16x32(p.out1 + grow * p.ld_out + gcol, valid, v);
@@ -410,10 +477,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int i = 0; i < 32; ++i) v[i] = i < valid ? v[i] * gelu_tanh_grad(z[i]) : 0.0f;
                     if (valid > 0) store_bf16x32(p.out0 + grow * p.ld_out + gcol, valid, v);
                     // db1 partial: lane l gets column n+l summed over this warp's 32 rows;
-                    // one partial row per (128-row tile, warp).
+                    // one partial row per 32-row block of the shard's rows.
                     const float cs = warp_column_sums(v, lane);
-                    if (lane < cvalid)
-                        p.colsum[(static_cast<long long>(tc.m0 / BM) * 4 + q) * p.ld_colsum + gcol +
+                    if (m_cta < p.M && lane < cvalid)
+                        p.colsum[(static_cast<long long>(m_cta / BM) * 4 + q) * p.ld_colsum + gcol +
                                  lane] = cs;
                 } else {
                     if (valid > 0) store_bf16x32(p.out0 + grow * p.ld_out + gcol, valid, v);
@@ -422,17 +489,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // TMEM of this accumulator may be overwritten from here on.
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[acc]);
-
+            if (lane == 0) {
+                if constexpr (PAIR)
+                    mbar_arrive_cluster(release_bar + acc * 8);
+                else
+                    mbar_arrive(&acc_empty[acc]);
+            }
         }
         __syncwarp();
     }
 
     tc_fence_before();
-    __syncthreads();
-    if (warp == 5) {
-        tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+    if constexpr (PAIR) {
+        cluster_sync();  // every remote arrive and multicast commit has landed
+        if (warp == 5) {
+            tc_fence_after();
+            tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        }
+        cluster_sync();
+    } else {
+        __syncthreads();
+        if (warp == 5) {
+            tc_fence_after();
+            tmem_dealloc(tmem_base, TMEM_COLS);
+        }
     }
 }
 

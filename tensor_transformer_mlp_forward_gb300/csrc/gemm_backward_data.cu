@@ -5,13 +5,15 @@
 namespace tpmlp {
 
 cudaError_t launch_dgelu(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& g, int grid,
-                         cudaStream_t st) {
-    return launch_gemm<false, false, EPI_DGELU>(a, b, g, grid, st);
+                        bool pair, cudaStream_t st) {
+    if (pair) return launch_gemm<false, false, EPI_DGELU, true>(a, b, g, grid, st);
+    return launch_gemm<false, false, EPI_DGELU, false>(a, b, g, grid, st);
 }
 
 cudaError_t launch_dx(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& g, int grid,
-                      cudaStream_t st) {
-    return launch_gemm<false, false, EPI_STORE>(a, b, g, grid, st);
+                        bool pair, cudaStream_t st) {
+    if (pair) return launch_gemm<false, false, EPI_STORE, true>(a, b, g, grid, st);
+    return launch_gemm<false, false, EPI_STORE, false>(a, b, g, grid, st);
 }
 
 }  // namespace tpmlp

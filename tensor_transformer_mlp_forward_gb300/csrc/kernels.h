@@ -9,28 +9,69 @@
 
 namespace tpmlp {
 
+// Each launcher runs the CTA-pair kernel when `pair` is set (grid even,
+// launched as clusters of 2), else the single-CTA kernel.
 // A K-major, B MN-major: the forward GEMMs.
 cudaError_t launch_column_gelu(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& g,
-                               int grid, cudaStream_t st);
+                               int grid, bool pair, cudaStream_t st);
 cudaError_t launch_row_sum(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& g,
-                           int grid, cudaStream_t st);
+                           int grid, bool pair, cudaStream_t st);
 // A K-major, B K-major: dZ and dX.
 cudaError_t launch_dgelu(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& g, int grid,
-                         cudaStream_t st);
+                         bool pair, cudaStream_t st);
 cudaError_t launch_dx(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& g, int grid,
-                      cudaStream_t st);
+                      bool pair, cudaStream_t st);
 // A MN-major, B MN-major: the weight gradients.
 cudaError_t launch_weight_grad(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& g,
-                               int grid, cudaStream_t st);
+                               int grid, bool pair, cudaStream_t st);
 
-template <bool A_MN, bool B_MN, int EPI>
+// `grid` is the number of work units wanted (CTAs, or CTA pairs when PAIR);
+// it is clipped to what can be resident at once, so the persistent loop never
+// waits for a second wave of CTAs.
+template <bool A_MN, bool B_MN, int EPI, bool PAIR>
 cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& g, int grid,
                         cudaStream_t st) {
-    auto kern = tcgen05_gemm_kernel<A_MN, B_MN, EPI>;
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    auto kern = tcgen05_gemm_kernel<A_MN, B_MN, EPI, PAIR>;
+    constexpr int smem = Geometry<PAIR>::SMEM_BYTES;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(a, b, g);
+    cudaLaunchConfig_t cfg = {};
+    if (PAIR) {
+        static int resident_clusters = 0;  // same for every device of this build's target
+        if (resident_clusters == 0) {
+            cudaLaunchConfig_t q = {};
+            q.gridDim = dim3(2 * static_cast<unsigned>(grid));
+            q.blockDim = dim3(NUM_THREADS);
+            q.dynamicSmemBytes = smem;
+            cudaLaunchAttribute qa[1];
+            qa[0].id = cudaLaunchAttributeClusterDimension;
+            qa[0].val.clusterDim.x = 2;
+            qa[0].val.clusterDim.y = 1;
+            qa[0].val.clusterDim.z = 1;
+            q.attrs = qa;
+            q.numAttrs = 1;
+            int n = 0;
+            e = cudaOccupancyMaxActiveClusters(&n, kern, &q);
+            if (e != cudaSuccess) return e;
+            resident_clusters = n > 0 ? n : 1;
+        }
+        grid = 2 * (grid < resident_clusters ? grid : resident_clusters);
+    }
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    if (PAIR) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    e = cudaLaunchKernelEx(&cfg, kern, a, b, g);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -72,9 +72,31 @@ SMALL = [
 ]
 
 
+@pytest.fixture(params=[0, 2], ids=["single_cta", "cta_pairs"])
+def pair_mode(request):
+    """Runs a test with the single-CTA GEMM kernel, then with CTA pairs."""
+    prev = binding.set_cta_pair_mode(request.param)
+    yield request.param
+    binding.set_cta_pair_mode(prev)
+
+
 @pytest.mark.parametrize("w", SMALL, ids=lambda w: f"T{w.T}_h{w.h}_F{w.F}_t{w.t}")
-def test_small_against_oracle(w):
+def test_small_against_oracle(w, pair_mode):
     check_full(w)
+
+
+def test_pairs_and_single_cta_agree_bitwise():
+    w = inputs.custom(T=600, h=520, F=2048, t=4, seed=20)
+    cpu = inputs.make_inputs(w)
+    prev = binding.set_cta_pair_mode(0)
+    try:
+        single = run_gpu(cpu, w.t)
+        binding.set_cta_pair_mode(2)
+        pairs = run_gpu(cpu, w.t)
+    finally:
+        binding.set_cta_pair_mode(prev)
+    for k in single:
+        assert torch.equal(single[k], pairs[k]), k
 
 
 def test_empty_batch():
