@@ -54,6 +54,8 @@ def parse_args(argv=None):
     p.add_argument("--sweep", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--pair-mode", type=int, default=None,
+                   help="GEMM kernel: 0 single CTA, 1 auto (default), 2 CTA pairs")
     return p.parse_args(argv)
 
 
@@ -409,6 +411,10 @@ def run_reference(args):
 def run_ours(args, w):
     import torch
 
+    from tensor_transformer_mlp_forward_gb300 import binding
+
+    if args.pair_mode is not None:
+        binding.set_cta_pair_mode(args.pair_mode)
     rank, world, local = init_distributed(args.gpus)
     step, dev_s, wall, per_call, clocks, launches = time_ours(w, args.steps, args.warmup, local)
     flops = w.flops_fwd_bwd()
@@ -446,6 +452,8 @@ def run_ours(args, w):
         "e2e": e2e,
         "clocks": clocks,
         "gpu_launches": launches,
+        "gemm_kernel": {0: "single CTA", 1: "auto", 2: "CTA pairs"}[
+            args.pair_mode if args.pair_mode is not None else 1],
     }
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(w, step.cpu)

@@ -199,12 +199,35 @@ int run_gemm(Launcher fn, const Operand& a, const Operand& b, GemmArgs& g, const
     GemmArgs probe = g;
     tile_space(probe, sh.M, sh.N, sh.K, sh.t, sh.mode, sh.a_bytes, sh.b_bytes, 2 * BM);
     const bool pair = pair_mode == 2 || (pair_mode == 1 && probe.num_tiles >= dev.sms / 2);
-    tile_space(g, sh.M, sh.N, sh.K, sh.t, sh.mode, sh.a_bytes, sh.b_bytes, pair ? 2 * BM : BM);
+    const int tile_m = pair ? 2 * BM : BM;
+    // When every shard boundary falls on a tile boundary (SHARD_N, SHARD_M)
+    // or a k-block boundary (SHARD_K), the shards are runs of whole tiles of
+    // the unsharded problem, visited in the same order: run it unsharded.
+    GemmShape f = sh;
+    Operand fa = a, fb = b;
+    if (sh.t > 1 && ((sh.mode == SHARD_K && sh.K % BK == 0) ||
+                     (sh.mode == SHARD_N && sh.N % BN == 0) ||
+                     (sh.mode == SHARD_M && sh.M % tile_m == 0))) {
+        if (sh.mode == SHARD_K) f.K = sh.K * sh.t;
+        if (sh.mode == SHARD_N) f.N = sh.N * sh.t;
+        if (sh.mode == SHARD_M) f.M = sh.M * sh.t;
+        f.t = 1;
+    }
+    if (f.t == 1) {
+        // One range: the tile loop needs no shard bookkeeping, and every map
+        // takes the form {cols, 1, rows} (rows as the outer dimension, which
+        // the tensor memory accelerator streams faster than {cols, rows, 1}).
+        f.mode = SHARD_NONE;
+        fa.on = fb.on = ON_CONTIG;
+    }
+    g.a_on = fa.on;
+    g.b_on = fb.on;
+    tile_space(g, f.M, f.N, f.K, f.t, f.mode, f.a_bytes, f.b_bytes, tile_m);
     if (g.num_tiles == 0) return TPMLP_OK;
     alignas(64) CUtensorMap map_a, map_b;
-    int rc = operand_map(&map_a, a, sh.t, BM);
+    int rc = operand_map(&map_a, fa, f.t, BM);
     if (rc) return rc;
-    rc = operand_map(&map_b, b, sh.t, pair ? BN / 2 : BN);
+    rc = operand_map(&map_b, fb, f.t, pair ? BN / 2 : BN);
     if (rc) return rc;
     g.status = dev.status;
     const int units = pair ? std::max(1, dev.sms / 2) : dev.sms;

@@ -33,7 +33,12 @@
 // and 128 of the 256 B rows; the leader CTA's single thread issues
 // M=256 x N=256 MMAs that read both CTAs' shared memory and write 128
 // accumulator rows into each CTA's TMEM.  Per flop this halves the B traffic
-// into each SM (shared memory and L2), and leaves room for 6 stages.
+// into each SM (shared memory and L2), and leaves room for 7 stages.
+//
+// The producer and MMA loops are single threads whose per-k-block latency
+// decides how much of the TMA latency the ring hides, so they carry no
+// divisions and no descriptor construction: shard and k advance by
+// counters, descriptors by adding offsets to precomputed bases.
 #pragma once
 
 #include "ptx.cuh"
@@ -52,12 +57,12 @@ constexpr int BAR_BYTES = 256;
 
 // Per-variant geometry.  Single CTA: a 128 x 256 tile, 4 stages of
 // A 128x64 + B 256x64.  CTA pair (cluster of 2, cta_group::2): a 256 x 256
-// tile, each CTA holding 128 rows of A and 128 rows of B per stage, 6 stages.
+// tile, each CTA holding 128 rows of A and 128 rows of B per stage, 7 stages.
 template <bool PAIR>
 struct Geometry {
     static constexpr int TILE_M = PAIR ? 2 * BM : BM;
     static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // B rows in this CTA's smem
-    static constexpr int STAGES = PAIR ? 6 : 4;
+    static constexpr int STAGES = PAIR ? 7 : 4;
     static constexpr int A_STAGE_BYTES = BM * BK * 2;
     static constexpr int B_STAGE_BYTES = B_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
@@ -132,15 +137,14 @@ __device__ __forceinline__ void tma_coords(int on, int contig, int row, int s, i
     }
 }
 
-// Loads one operand's [ROWS x BK] slice for the k-block starting at k0.
+// Loads one operand's [ROWS x BK] slice for the k-block starting at k0 into
+// shared address `dst`; completion counts on the mbarrier at `bar` (in a
+// pair: the leader's barrier, a shared::cluster address).
 //  K-major:  one box of 64 (k) x ROWS (m or n), rows 128 B apart.
 //  MN-major: ROWS/64 boxes of 64 (m or n) x BK (k), each 8 KiB.
-// PAIR: completion is counted on the pair leader's barrier (`bar_cluster`,
-// a shared::cluster address); otherwise on this CTA's `bar`.
 template <bool MN, int ROWS, bool PAIR>
-__device__ __forceinline__ void load_operand(const CUtensorMap* map, uint64_t* bar,
-                                             uint32_t bar_cluster, uint8_t* dst, int on, int mn0,
-                                             int k0, int s) {
+__device__ __forceinline__ void load_operand(const CUtensorMap* map, uint32_t bar, uint32_t dst,
+                                             int on, int mn0, int k0, int s) {
     int c0, c1, c2;
 #pragma unroll
     for (int j = 0; j < (MN ? ROWS / 64 : 1); ++j) {
@@ -149,21 +153,28 @@ __device__ __forceinline__ void load_operand(const CUtensorMap* map, uint64_t* b
         else
             tma_coords(on, mn0 + 64 * j, k0, s, c0, c1, c2);
         if constexpr (PAIR)
-            tma_load_3d_pair(map, bar_cluster, dst + j * MN_ATOM_BYTES, c0, c1, c2);
+            tma_load_3d_pair(map, bar, dst + j * MN_ATOM_BYTES, c0, c1, c2);
         else
             tma_load_3d(map, bar, dst + j * MN_ATOM_BYTES, c0, c1, c2);
     }
 }
 
-// Descriptor of the UMMA_K-deep slice `kk` of an operand stage buffer.
-//  K-major:  rows 128 B apart, 8-row groups 1024 B apart (SBO); the k slice
-//            starts 32 B further along the swizzled row.
+// Descriptor of an operand stage buffer starting at shared address `base`.
+//  K-major:  rows 128 B apart, 8-row groups 1024 B apart (SBO); LBO unused.
 //  MN-major: 64-wide MN atoms MN_ATOM_BYTES apart (LBO), 8-deep k groups
-//            1024 B apart (SBO); the k slice starts 16 rows (2048 B) further.
+//            1024 B apart (SBO).
 template <bool MN>
-__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
-    if (!MN) return smem_desc_sw128(base + kk * (UMMA_K * 2), 16, 1024);
-    return smem_desc_sw128(base + kk * (UMMA_K * 128), MN_ATOM_BYTES, 1024);
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base) {
+    if (!MN) return smem_desc_sw128(base, 16, 1024);
+    return smem_desc_sw128(base, MN_ATOM_BYTES, 1024);
+}
+
+// Start-address step (in the descriptor's 16-byte units) from one UMMA_K
+// slice to the next: 32 B along a swizzled K-major row, or 16 rows (2 KiB)
+// of an MN-major box.
+template <bool MN>
+constexpr uint64_t desc_k_step() {
+    return MN ? (UMMA_K * 128) >> 4 : (UMMA_K * 2) >> 4;
 }
 
 // ------------------------------------------------------------ epilogue math
@@ -313,35 +324,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued = 0, issued_phase = 0;  // per-stage bits of the last issue
+            const uint32_t ring_a_u = smem_u32(ring_a), ring_b_u = smem_u32(ring_b);
+            // stage barriers as seen by the TMA: the leader's in a pair
+            const uint32_t full_u = PAIR ? map_to_cta(smem_u32(full), 0) : smem_u32(full);
+            const bool split_k = p.shard_mode == SHARD_K;
             for (int tile = unit; tile < p.num_tiles; tile += units) {
                 const TileCoord tc = decode_tile<G::TILE_M>(tile, p);
+                const int a_row0 = tc.m0 + static_cast<int>(rank) * BM;
+                const int b_row0 = tc.n0 + static_cast<int>(rank) * G::B_ROWS;
+                int s = split_k ? 0 : tc.s;  // shard of the k range (SHARD_K walks them all)
+                int k0 = 0, kb_in_shard = 0;
                 bool ok = true;
                 for (int kb = 0; kb < total_kb; ++kb) {
                     if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
-                    int s = tc.s, k0 = kb * BK;
-                    if (p.shard_mode == SHARD_K) {
-                        s = kb / p.k_blocks;
-                        k0 = (kb - s * p.k_blocks) * BK;
-                    }
-                    uint32_t bar_cluster = 0;
-                    if constexpr (PAIR) {
-                        // both CTAs' bytes complete the leader's barrier
-                        if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * G::STAGE_BYTES);
-                        bar_cluster = map_to_cta(smem_u32(&full[stage]), 0);
-                    } else {
-                        mbar_arrive_expect_tx(&full[stage], G::STAGE_BYTES);
-                    }
-                    load_operand<A_MN, BM, PAIR>(&tmA, &full[stage], bar_cluster,
-                                                 ring_a + stage * G::A_STAGE_BYTES, p.a_on,
-                                                 tc.m0 + static_cast<int>(rank) * BM, k0, s);
-                    load_operand<B_MN, G::B_ROWS, PAIR>(
-                        &tmB, &full[stage], bar_cluster, ring_b + stage * G::B_STAGE_BYTES, p.b_on,
-                        tc.n0 + static_cast<int>(rank) * G::B_ROWS, k0, s);
+                    // in a pair both CTAs' bytes complete the leader's barrier
+                    if (!PAIR || rank == 0)
+                        mbar_arrive_expect_tx(&full[stage], PAIR ? 2 * G::STAGE_BYTES : G::STAGE_BYTES);
+                    const uint32_t bar = full_u + stage * 8;
+                    load_operand<A_MN, BM, PAIR>(&tmA, bar, ring_a_u + stage * G::A_STAGE_BYTES,
+                                                 p.a_on, a_row0, k0, s);
+                    load_operand<B_MN, G::B_ROWS, PAIR>(&tmB, bar, ring_b_u + stage * G::B_STAGE_BYTES,
+                                                        p.b_on, b_row0, k0, s);
                     issued |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    k0 += BK;
+                    if (++kb_in_shard == p.k_blocks) {  // next shard's k range
+                        kb_in_shard = 0;
+                        k0 = 0;
+                        ++s;
+                    }
                     if (++stage == G::STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -365,6 +379,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ------------------------------------------------------ MMA issuer
         if (lane == 0 && rank == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(G::TILE_M, BN, A_MN, B_MN);
+            const uint64_t a_desc0 = operand_desc<A_MN>(smem_u32(ring_a));
+            const uint64_t b_desc0 = operand_desc<B_MN>(smem_u32(ring_b));
             int stage = 0;
             uint32_t phase = 0;
             int count = 0;
@@ -381,17 +397,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_base = smem_u32(ring_a + stage * G::A_STAGE_BYTES);
-                    const uint32_t b_base = smem_u32(ring_b + stage * G::B_STAGE_BYTES);
+                    const uint64_t ad = a_desc0 + ((stage * G::A_STAGE_BYTES) >> 4);
+                    const uint64_t bd = b_desc0 + ((stage * G::B_STAGE_BYTES) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        const uint64_t ad = operand_desc<A_MN>(a_base, kk);
-                        const uint64_t bd = operand_desc<B_MN>(b_base, kk);
                         const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
                         if constexpr (PAIR)
-                            tc_mma_f16_pair(d_tmem, ad, bd, idesc, accum);
+                            tc_mma_f16_pair(d_tmem, ad + kk * desc_k_step<A_MN>(),
+                                            bd + kk * desc_k_step<B_MN>(), idesc, accum);
                         else
-                            tc_mma_f16(d_tmem, ad, bd, idesc, accum);
+                            tc_mma_f16(d_tmem, ad + kk * desc_k_step<A_MN>(),
+                                       bd + kk * desc_k_step<B_MN>(), idesc, accum);
                     }
                     // frees the stage (in both CTAs of a pair) when these MMAs finish
                     if constexpr (PAIR)

@@ -93,14 +93,15 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
 
-// 3-D tiled bulk tensor copy global -> shared, completion counted in bytes
-// on `bar`.  Coordinates are element indices (innermost first).
-__device__ __forceinline__ void tma_load_3d(const CUtensorMap* m, uint64_t* bar, void* dst,
+// 3-D tiled bulk tensor copy global -> shared (this CTA, address `dst`),
+// completion counted in bytes on the mbarrier at shared address `bar`.
+// Coordinates are element indices (innermost first).
+__device__ __forceinline__ void tma_load_3d(const CUtensorMap* m, uint32_t bar, uint32_t dst,
                                             int c0, int c1, int c2) {
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
 
@@ -243,10 +244,10 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
 // Tiled load into this CTA's shared memory whose completion is counted on an
 // mbarrier of either CTA of the pair (shared::cluster address).
 __device__ __forceinline__ void tma_load_3d_pair(const CUtensorMap* m, uint32_t bar_cluster,
-                                                 void* dst, int c0, int c1, int c2) {
+                                                 uint32_t dst, int c0, int c1, int c2) {
     asm volatile(
         "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
