@@ -184,8 +184,15 @@ void tile_space(GemmArgs& g, int M, int N, int K, int t, int mode, long long a_b
     g.raster_m_fastest = b_bytes >= a_bytes ? 1 : 0;
 }
 
-typedef cudaError_t (*Launcher)(const CUtensorMap&, const CUtensorMap&, const GemmArgs&, int, bool,
-                                cudaStream_t);
+typedef cudaError_t (*Launcher)(const GemmMaps&, const GemmArgs&, int, bool, cudaStream_t);
+
+// The output of one GEMM: row-major [rows, cols] over all shards; `ptr1` is
+// the second output of the bias + GeLU epilogue (H), else null.
+struct Output {
+    void* ptr0;
+    void* ptr1;
+    long long rows, cols;
+};
 
 // One GEMM: M x N output per shard, K reduction (per shard for SHARD_K).
 struct GemmShape {
@@ -193,8 +200,8 @@ struct GemmShape {
     long long a_bytes, b_bytes;
 };
 
-int run_gemm(Launcher fn, const Operand& a, const Operand& b, GemmArgs& g, const GemmShape& sh,
-             cudaStream_t st, const DeviceInfo& dev) {
+int run_gemm(Launcher fn, const Operand& a, const Operand& b, const Output& out, GemmArgs& g,
+             const GemmShape& sh, cudaStream_t st, const DeviceInfo& dev) {
     const int pair_mode = g_pair_mode.load(std::memory_order_relaxed);
     GemmArgs probe = g;
     tile_space(probe, sh.M, sh.N, sh.K, sh.t, sh.mode, sh.a_bytes, sh.b_bytes, 2 * BM);
@@ -222,17 +229,29 @@ int run_gemm(Launcher fn, const Operand& a, const Operand& b, GemmArgs& g, const
     }
     g.a_on = fa.on;
     g.b_on = fb.on;
+    // Output maps carry the shard index where the output is split, so that
+    // TMA stores clip each shard's ragged edge; 32-row x 64-column boxes.
+    int o_t = 1;
+    g.o_on = ON_CONTIG;
+    if (f.mode == SHARD_N || f.mode == SHARD_M) {
+        o_t = f.t;
+        g.o_on = f.mode == SHARD_N ? ON_CONTIG : ON_ROWS;
+    }
     tile_space(g, f.M, f.N, f.K, f.t, f.mode, f.a_bytes, f.b_bytes, tile_m);
     if (g.num_tiles == 0) return TPMLP_OK;
-    alignas(64) CUtensorMap map_a, map_b;
-    int rc = operand_map(&map_a, fa, f.t, BM);
+    alignas(64) GemmMaps maps;
+    int rc = operand_map(&maps.a, fa, f.t, BM);
     if (rc) return rc;
-    rc = operand_map(&map_b, fb, f.t, pair ? BN / 2 : BN);
+    rc = operand_map(&maps.b, fb, f.t, pair ? BN / 2 : BN);
+    if (rc) return rc;
+    rc = make_map(&maps.o0, out.ptr0, out.rows, out.cols, o_t, g.o_on, 32);
+    if (rc) return rc;
+    rc = make_map(&maps.o1, out.ptr1 ? out.ptr1 : out.ptr0, out.rows, out.cols, o_t, g.o_on, 32);
     if (rc) return rc;
     g.status = dev.status;
     const int units = pair ? std::max(1, dev.sms / 2) : dev.sms;
     const int grid = std::min(g.num_tiles, units);
-    cudaError_t e = fn(map_a, map_b, g, grid, pair, st);
+    cudaError_t e = fn(maps, g, grid, pair, st);
     if (e != cudaSuccess) return fail_cuda(e);
     ++t_last_launches;
     return TPMLP_OK;
@@ -245,7 +264,6 @@ GemmArgs blank_args() {
 }
 
 const __nv_bfloat16* cb(const tpmlp_bf16* p) { return reinterpret_cast<const __nv_bfloat16*>(p); }
-__nv_bfloat16* mb(tpmlp_bf16* p) { return reinterpret_cast<__nv_bfloat16*>(p); }
 
 // ------------------------------------------------------------ the six GEMMs
 
@@ -256,13 +274,11 @@ int column_gelu(const tpmlp_bf16* X, const tpmlp_bf16* A, const tpmlp_bf16* b1, 
     const GemmShape sh{T, f, h, t, SHARD_N, 1LL * T * h, 1LL * h * F};
     g.a_on = ON_NONE;
     g.b_on = ON_CONTIG;
-    g.out0 = mb(Z);
-    g.out1 = mb(H);
-    g.ld_out = F;
     g.bias = cb(b1);
     Operand a{X, T, h, ON_NONE, false};
     Operand b{A, h, F, ON_CONTIG, true};
-    return run_gemm(launch_column_gelu, a, b, g, sh, st, d);
+    Output o{Z, H, T, F};
+    return run_gemm(launch_column_gelu, a, b, o, g, sh, st, d);
 }
 
 int row_sum(const tpmlp_bf16* H, const tpmlp_bf16* B, const tpmlp_bf16* b2,
@@ -273,14 +289,13 @@ int row_sum(const tpmlp_bf16* H, const tpmlp_bf16* B, const tpmlp_bf16* b2,
     const GemmShape sh{T, h, f, t, SHARD_K, 1LL * T * F, 1LL * F * h};
     g.a_on = ON_CONTIG;
     g.b_on = ON_ROWS;
-    g.out0 = mb(Y);
-    g.ld_out = h;
     g.bias = cb(b2);
     g.aux = cb(R);
     g.ld_aux = h;
     Operand a{H, T, F, ON_CONTIG, false};
     Operand b{B, F, h, ON_ROWS, true};
-    return run_gemm(launch_row_sum, a, b, g, sh, st, d);
+    Output o{Y, nullptr, T, h};
+    return run_gemm(launch_row_sum, a, b, o, g, sh, st, d);
 }
 
 int dgelu_gemm(const tpmlp_bf16* dY, const tpmlp_bf16* B, const tpmlp_bf16* Z, int T, int h,
@@ -290,15 +305,14 @@ int dgelu_gemm(const tpmlp_bf16* dY, const tpmlp_bf16* B, const tpmlp_bf16* Z, i
     const GemmShape sh{T, f, h, t, SHARD_N, 1LL * T * h, 1LL * F * h};
     g.a_on = ON_NONE;
     g.b_on = ON_ROWS;
-    g.out0 = mb(dZ);
-    g.ld_out = F;
     g.aux = cb(Z);
     g.ld_aux = F;
     g.colsum = colsum;
     g.ld_colsum = F;
     Operand a{dY, T, h, ON_NONE, false};
     Operand b{B, F, h, ON_ROWS, false};
-    return run_gemm(launch_dgelu, a, b, g, sh, st, d);
+    Output o{dZ, nullptr, T, F};
+    return run_gemm(launch_dgelu, a, b, o, g, sh, st, d);
 }
 
 int dx_gemm(const tpmlp_bf16* dZ, const tpmlp_bf16* A, int T, int h, int F, int t,
@@ -308,11 +322,10 @@ int dx_gemm(const tpmlp_bf16* dZ, const tpmlp_bf16* A, int T, int h, int F, int 
     const GemmShape sh{T, h, f, t, SHARD_K, 1LL * T * F, 1LL * h * F};
     g.a_on = ON_CONTIG;
     g.b_on = ON_CONTIG;
-    g.out0 = mb(dX);
-    g.ld_out = h;
     Operand a{dZ, T, F, ON_CONTIG, false};
     Operand b{A, h, F, ON_CONTIG, false};
-    return run_gemm(launch_dx, a, b, g, sh, st, d);
+    Output o{dX, nullptr, T, h};
+    return run_gemm(launch_dx, a, b, o, g, sh, st, d);
 }
 
 int dA_gemm(const tpmlp_bf16* X, const tpmlp_bf16* dZ, int T, int h, int F, int t,
@@ -322,11 +335,10 @@ int dA_gemm(const tpmlp_bf16* X, const tpmlp_bf16* dZ, int T, int h, int F, int 
     const GemmShape sh{h, f, T, t, SHARD_N, 1LL * T * h, 1LL * T * F};
     g.a_on = ON_NONE;
     g.b_on = ON_CONTIG;
-    g.out0 = mb(dA);
-    g.ld_out = F;
     Operand a{X, T, h, ON_NONE, true};
     Operand b{dZ, T, F, ON_CONTIG, true};
-    return run_gemm(launch_weight_grad, a, b, g, sh, st, d);
+    Output o{dA, nullptr, h, F};
+    return run_gemm(launch_weight_grad, a, b, o, g, sh, st, d);
 }
 
 int dB_gemm(const tpmlp_bf16* H, const tpmlp_bf16* dY, int T, int h, int F, int t,
@@ -336,11 +348,10 @@ int dB_gemm(const tpmlp_bf16* H, const tpmlp_bf16* dY, int T, int h, int F, int 
     const GemmShape sh{f, h, T, t, SHARD_M, 1LL * T * F, 1LL * T * h};
     g.a_on = ON_CONTIG;
     g.b_on = ON_NONE;
-    g.out0 = mb(dB);
-    g.ld_out = h;
     Operand a{H, T, F, ON_CONTIG, true};
     Operand b{dY, T, h, ON_NONE, true};
-    return run_gemm(launch_weight_grad, a, b, g, sh, st, d);
+    Output o{dB, nullptr, F, h};
+    return run_gemm(launch_weight_grad, a, b, o, g, sh, st, d);
 }
 
 // -------------------------------------------------- column sums (bias grads)

@@ -54,6 +54,10 @@ constexpr int NUM_THREADS = 192;
 constexpr int EPI_THREADS = 128;
 constexpr int TMEM_COLS = 512;
 constexpr int BAR_BYTES = 256;
+// Epilogue staging: per epilogue warp two buffers, each a 32-row x 64-column
+// bf16 block (rows 128 B apart, 128-byte swizzle) stored by one TMA store.
+constexpr int EPI_BUF_BYTES = 32 * 128;
+constexpr int EPI_STAGING_BYTES = 4 * 2 * EPI_BUF_BYTES;
 
 // Per-variant geometry.  Single CTA: a 128 x 256 tile, 4 stages of
 // A 128x64 + B 256x64.  CTA pair (cluster of 2, cta_group::2): a 256 x 256
@@ -62,11 +66,11 @@ template <bool PAIR>
 struct Geometry {
     static constexpr int TILE_M = PAIR ? 2 * BM : BM;
     static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // B rows in this CTA's smem
-    static constexpr int STAGES = PAIR ? 7 : 4;
+    static constexpr int STAGES = PAIR ? 6 : 4;
     static constexpr int A_STAGE_BYTES = BM * BK * 2;
     static constexpr int B_STAGE_BYTES = B_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_STAGING_BYTES + BAR_BYTES;
 };
 
 enum ShardMode { SHARD_NONE = 0, SHARD_N = 1, SHARD_M = 2, SHARD_K = 3 };
@@ -85,9 +89,7 @@ struct GemmArgs {
     int k_blocks;        // BK blocks per shard (SHARD_K) or in total
     int num_tiles;
     int raster_m_fastest;
-    __nv_bfloat16* out0;  // primary output (Z, Y, dZ, dX, dA or dB)
-    __nv_bfloat16* out1;  // H for EPI_BIAS_GELU
-    long long ld_out;
+    int o_on;             // ShardOn of the output tensor maps (Z and H, Y, dZ, dX, dA or dB)
     const __nv_bfloat16* bias;  // b1 or b2, indexed by global output column
     const __nv_bfloat16* aux;   // residual (EPI_BIAS_RESIDUAL) or Z (EPI_DGELU)
     long long ld_aux;
@@ -217,23 +219,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Stores 32 floats as bf16; only the first `valid` are written.
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* p, int valid, const float (&v)[32]) {
-    if (valid >= 32) {
-        uint4* q = reinterpret_cast<uint4*>(p);
+// Writes 32 floats as bf16 into half `half` (bytes 64*half .. 64*half+63)
+// of this thread's 128-byte staging row at `row_addr`, in the 128-byte
+// swizzle: 16-byte piece c of row r sits at piece position c ^ (r % 8).
+__device__ __forceinline__ void stage_row(uint32_t row_addr, int half, uint32_t swz,
+                                          const float (&v)[32]) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            uint4 u;
-            u.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
-            u.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
-            u.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
-            u.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
-            q[i] = u;
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-            if (i < valid) p[i] = __float2bfloat16_rn(v[i]);
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t piece = static_cast<uint32_t>(half * 4 + j);
+        st_shared_v4(row_addr + ((piece ^ swz) << 4), pack_bf16x2(v[8 * j + 0], v[8 * j + 1]),
+                     pack_bf16x2(v[8 * j + 2], v[8 * j + 3]), pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
+                     pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
     }
 }
 
@@ -258,7 +254,10 @@ __device__ __forceinline__ float warp_column_sums(float (&v)[32], int lane) {
 template <bool A_MN, bool B_MN, int EPI, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tcgen05_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB, const GemmArgs p) {
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmO0,  // output (Z for EPI_BIAS_GELU)
+                        const __grid_constant__ CUtensorMap tmO1,  // H for EPI_BIAS_GELU
+                        const GemmArgs p) {
     using G = Geometry<PAIR>;
     extern __shared__ uint8_t smem_raw[];
     // 128-byte swizzle atoms repeat every 1024 B: align the ring to 1 KiB.
@@ -266,7 +265,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     uint8_t* ring_a = smem;
     uint8_t* ring_b = smem + G::STAGES * G::A_STAGE_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + G::STAGES * G::STAGE_BYTES);
+    uint8_t* staging = smem + G::STAGES * G::STAGE_BYTES;  // 1 KiB aligned
+    uint64_t* bars = reinterpret_cast<uint64_t*>(staging + EPI_STAGING_BYTES);
     uint64_t* full = bars;                      // stage loaded  (STAGES)
     uint64_t* empty = bars + G::STAGES;         // stage drained (STAGES)
     uint64_t* acc_full = bars + 2 * G::STAGES;  // accumulator ready (2)
@@ -308,6 +308,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 4 && lane == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
+        prefetch_tmap(&tmO0);
+        if (EPI == EPI_BIAS_GELU) prefetch_tmap(&tmO1);
     }
     tc_fence_before();
     if constexpr (PAIR)
@@ -435,9 +437,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
     } else {
         // -------------------------------------------------------- epilogue
-        const int q = warp;  // TMEM lane quadrant == accumulator rows 32q..32q+31
+        // Warp q owns accumulator rows 32q..32q+31 (its TMEM lane quadrant).
+        // Per 64-column block: TMEM -> registers -> fused math -> bf16 rows
+        // in a swizzled staging buffer -> one TMA store of the 32 x 64 block
+        // (full lines; the tensor map clips rows and columns outside the
+        // shard).  Two buffers per warp let a block be written while the
+        // previous one is still being stored.
+        const int q = warp;
         const uint32_t release_bar =
             PAIR ? map_to_cta(smem_u32(&acc_empty[0]), 0) : smem_u32(&acc_empty[0]);
+        const uint32_t buf_base = smem_u32(staging) + static_cast<uint32_t>(q) * 2u * EPI_BUF_BYTES;
+        const uint32_t my_row = static_cast<uint32_t>(lane) * 128u;
+        const uint32_t swz = static_cast<uint32_t>(lane & 7);
+        uint32_t seq = 0;  // stores committed so far: selects the buffer
         int count = 0;
         for (int tile = unit; tile < p.num_tiles; tile += units, ++count) {
             const TileCoord tc = decode_tile<G::TILE_M>(tile, p);
@@ -447,59 +459,94 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
 
             const int m_cta = tc.m0 + static_cast<int>(rank) * BM;  // first row of this CTA
-            const int m = m_cta + q * 32 + lane;                       // row inside the shard
+            const int row0 = m_cta + q * 32;                           // first row of this warp
+            const int m = row0 + lane;                                 // row inside the shard
             const bool row_ok = m < p.M;
             long long grow = m, gcol0 = tc.n0;
             if (p.shard_mode == SHARD_N) gcol0 += static_cast<long long>(tc.s) * p.N;
             if (p.shard_mode == SHARD_M) grow += static_cast<long long>(tc.s) * p.M;
 
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                const int n = tc.n0 + c * 32;
-                uint32_t r[32];
-                tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + c * 32, r);
-                tmem_wait_ld();
-                const int cvalid = min(32, p.N - n);  // columns inside the shard
-                const int valid = row_ok ? cvalid : 0;
-                const long long gcol = gcol0 + c * 32;
-                float v[32];
+            for (int c = 0; c < BN / 64; ++c) {
+                const int n64 = tc.n0 + c * 64;
+                uint32_t buf0, buf1;
+                if constexpr (EPI == EPI_BIAS_GELU) {  // Z and H: both buffers
+                    buf0 = buf_base;
+                    buf1 = buf_base + EPI_BUF_BYTES;
+                    if (lane == 0) bulk_wait_group_read<0>();
+                } else {
+                    buf0 = buf_base + (seq & 1u) * EPI_BUF_BYTES;
+                    buf1 = buf0;
+                    if (lane == 0) bulk_wait_group_read<1>();
+                }
+                __syncwarp();  // the buffer's previous store has read it
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+                for (int half = 0; half < 2; ++half) {
+                    const int n = n64 + half * 32;
+                    uint32_t r[32];
+                    tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + c * 64 +
+                                  half * 32,
+                              r);
+                    tmem_wait_ld();
+                    const int cvalid = min(32, p.N - n);  // columns inside the shard
+                    const int valid = row_ok ? cvalid : 0;
+                    const long long gcol = gcol0 + c * 64 + half * 32;
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 
-                if constexpr (EPI == EPI_BIAS_GELU) {
-                    if (valid > 0) {
-                        float b[32];
-                        load_bf16x32(p.bias + gcol, valid, b);
+                    if constexpr (EPI == EPI_BIAS_GELU) {
+                        if (valid > 0) {
+                            float b[32];
+                            load_bf16x32(p.bias + gcol, valid, b);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] += b[i];
-                        store_bf16x32(p.out0 + grow * p.ld_out + gcol, valid, v);
+                            for (int i = 0; i < 32; ++i) v[i] += b[i];
+                        }
+                        stage_row(buf0 + my_row, half, swz, v);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
-                        store_bf16x32(p.out1 + grow * p.ld_out + gcol, valid, v);
-                    }
-                } else if constexpr (EPI == EPI_BIAS_RESIDUAL) {
-                    if (valid > 0) {
-                        float b[32], res[32];
-                        load_bf16x32(p.bias + gcol, valid, b);
-                        load_bf16x32(p.aux + grow * p.ld_aux + gcol, valid, res);
+                        stage_row(buf1 + my_row, half, swz, v);
+                    } else if constexpr (EPI == EPI_BIAS_RESIDUAL) {
+                        if (valid > 0) {
+                            float b[32], res[32];
+                            load_bf16x32(p.bias + gcol, valid, b);
+                            load_bf16x32(p.aux + grow * p.ld_aux + gcol, valid, res);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] += b[i] + res[i];
-                        store_bf16x32(p.out0 + grow * p.ld_out + gcol, valid, v);
-                    }
-                } else if constexpr (EPI == EPI_DGELU) {
-                    float z[32];
-                    load_bf16x32(p.aux + grow * p.ld_aux + gcol, valid, z);
+                            for (int i = 0; i < 32; ++i) v[i] += b[i] + res[i];
+                        }
+                        stage_row(buf0 + my_row, half, swz, v);
+                    } else if constexpr (EPI == EPI_DGELU) {
+                        float z[32];
+                        load_bf16x32(p.aux + grow * p.ld_aux + gcol, valid, z);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = i < valid ? v[i] * gelu_tanh_grad(z[i]) : 0.0f;
-                    if (valid > 0) store_bf16x32(p.out0 + grow * p.ld_out + gcol, valid, v);
-                    // db1 partial: lane l gets column n+l summed over this warp's 32 rows;
-                    // one partial row per 32-row block of the shard's rows.
-                    const float cs = warp_column_sums(v, lane);
-                    if (m_cta < p.M && lane < cvalid)
-                        p.colsum[(static_cast<long long>(m_cta / BM) * 4 + q) * p.ld_colsum + gcol +
-                                 lane] = cs;
-                } else {
-                    if (valid > 0) store_bf16x32(p.out0 + grow * p.ld_out + gcol, valid, v);
+                        for (int i = 0; i < 32; ++i)
+                            v[i] = i < valid ? v[i] * gelu_tanh_grad(z[i]) : 0.0f;
+                        stage_row(buf0 + my_row, half, swz, v);
+                        // db1 partial: lane l gets column n+l summed over this warp's 32 rows;
+                        // one partial row per 32-row block of the shard's rows.
+                        const float cs = warp_column_sums(v, lane);
+                        if (m_cta < p.M && lane < cvalid)
+                            p.colsum[(static_cast<long long>(m_cta / BM) * 4 + q) * p.ld_colsum +
+                                     gcol + lane] = cs;
+                    } else {
+                        stage_row(buf0 + my_row, half, swz, v);
+                    }
+                }
+                fence_proxy_async_smem();  // staged rows visible to the TMA store
+                __syncwarp();
+                // Blocks wholly outside the shard are not stored.  Buffers
+                // alternate with the committed stores only, so the wait above
+                // (at most one store still reading) always covers the buffer.
+                const bool store = row0 < p.M && n64 < p.N;  // warp-uniform
+                if (store) {
+                    if (lane == 0) {
+                        int c0, c1, c2;
+                        tma_coords(p.o_on, n64, row0, tc.s, c0, c1, c2);
+                        tma_store_3d(&tmO0, buf0, c0, c1, c2);
+                        if constexpr (EPI == EPI_BIAS_GELU) tma_store_3d(&tmO1, buf1, c0, c1, c2);
+                        bulk_commit_group();
+                    }
+                    ++seq;
                 }
             }
             // TMEM of this accumulator may be overwritten from here on.
@@ -512,6 +559,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     mbar_arrive(&acc_empty[acc]);
             }
         }
+        if (lane == 0) bulk_wait_group<0>();  // every output store has completed
         __syncwarp();
     }
 

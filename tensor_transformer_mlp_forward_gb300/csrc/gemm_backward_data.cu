@@ -4,16 +4,16 @@
 
 namespace tpmlp {
 
-cudaError_t launch_dgelu(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& g, int grid,
+cudaError_t launch_dgelu(const GemmMaps& m, const GemmArgs& g, int grid,
                         bool pair, cudaStream_t st) {
-    if (pair) return launch_gemm<false, false, EPI_DGELU, true>(a, b, g, grid, st);
-    return launch_gemm<false, false, EPI_DGELU, false>(a, b, g, grid, st);
+    if (pair) return launch_gemm<false, false, EPI_DGELU, true>(m, g, grid, st);
+    return launch_gemm<false, false, EPI_DGELU, false>(m, g, grid, st);
 }
 
-cudaError_t launch_dx(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& g, int grid,
+cudaError_t launch_dx(const GemmMaps& m, const GemmArgs& g, int grid,
                         bool pair, cudaStream_t st) {
-    if (pair) return launch_gemm<false, false, EPI_STORE, true>(a, b, g, grid, st);
-    return launch_gemm<false, false, EPI_STORE, false>(a, b, g, grid, st);
+    if (pair) return launch_gemm<false, false, EPI_STORE, true>(m, g, grid, st);
+    return launch_gemm<false, false, EPI_STORE, false>(m, g, grid, st);
 }
 
 }  // namespace tpmlp

@@ -4,10 +4,10 @@
 
 namespace tpmlp {
 
-cudaError_t launch_weight_grad(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& g, int grid,
+cudaError_t launch_weight_grad(const GemmMaps& m, const GemmArgs& g, int grid,
                         bool pair, cudaStream_t st) {
-    if (pair) return launch_gemm<true, true, EPI_STORE, true>(a, b, g, grid, st);
-    return launch_gemm<true, true, EPI_STORE, false>(a, b, g, grid, st);
+    if (pair) return launch_gemm<true, true, EPI_STORE, true>(m, g, grid, st);
+    return launch_gemm<true, true, EPI_STORE, false>(m, g, grid, st);
 }
 
 }  // namespace tpmlp

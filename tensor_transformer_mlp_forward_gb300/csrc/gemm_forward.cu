@@ -4,16 +4,16 @@
 
 namespace tpmlp {
 
-cudaError_t launch_column_gelu(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& g, int grid,
+cudaError_t launch_column_gelu(const GemmMaps& m, const GemmArgs& g, int grid,
                         bool pair, cudaStream_t st) {
-    if (pair) return launch_gemm<false, true, EPI_BIAS_GELU, true>(a, b, g, grid, st);
-    return launch_gemm<false, true, EPI_BIAS_GELU, false>(a, b, g, grid, st);
+    if (pair) return launch_gemm<false, true, EPI_BIAS_GELU, true>(m, g, grid, st);
+    return launch_gemm<false, true, EPI_BIAS_GELU, false>(m, g, grid, st);
 }
 
-cudaError_t launch_row_sum(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& g, int grid,
+cudaError_t launch_row_sum(const GemmMaps& m, const GemmArgs& g, int grid,
                         bool pair, cudaStream_t st) {
-    if (pair) return launch_gemm<false, true, EPI_BIAS_RESIDUAL, true>(a, b, g, grid, st);
-    return launch_gemm<false, true, EPI_BIAS_RESIDUAL, false>(a, b, g, grid, st);
+    if (pair) return launch_gemm<false, true, EPI_BIAS_RESIDUAL, true>(m, g, grid, st);
+    return launch_gemm<false, true, EPI_BIAS_RESIDUAL, false>(m, g, grid, st);
 }
 
 }  // namespace tpmlp

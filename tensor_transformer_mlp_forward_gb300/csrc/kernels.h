@@ -9,27 +9,33 @@
 
 namespace tpmlp {
 
+// The four tensor maps of one GEMM: operands A and B, output o0 (and o1, the
+// second output of the bias + GeLU epilogue; a copy of o0 otherwise).
+struct GemmMaps {
+    CUtensorMap a, b, o0, o1;
+};
+
 // Each launcher runs the CTA-pair kernel when `pair` is set (grid even,
 // launched as clusters of 2), else the single-CTA kernel.
 // A K-major, B MN-major: the forward GEMMs.
-cudaError_t launch_column_gelu(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& g,
+cudaError_t launch_column_gelu(const GemmMaps& m, const GemmArgs& g,
                                int grid, bool pair, cudaStream_t st);
-cudaError_t launch_row_sum(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& g,
+cudaError_t launch_row_sum(const GemmMaps& m, const GemmArgs& g,
                            int grid, bool pair, cudaStream_t st);
 // A K-major, B K-major: dZ and dX.
-cudaError_t launch_dgelu(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& g, int grid,
+cudaError_t launch_dgelu(const GemmMaps& m, const GemmArgs& g, int grid,
                          bool pair, cudaStream_t st);
-cudaError_t launch_dx(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& g, int grid,
+cudaError_t launch_dx(const GemmMaps& m, const GemmArgs& g, int grid,
                       bool pair, cudaStream_t st);
 // A MN-major, B MN-major: the weight gradients.
-cudaError_t launch_weight_grad(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& g,
+cudaError_t launch_weight_grad(const GemmMaps& m, const GemmArgs& g,
                                int grid, bool pair, cudaStream_t st);
 
 // `grid` is the number of work units wanted (CTAs, or CTA pairs when PAIR);
 // it is clipped to what can be resident at once, so the persistent loop never
 // waits for a second wave of CTAs.
 template <bool A_MN, bool B_MN, int EPI, bool PAIR>
-cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& g, int grid,
+cudaError_t launch_gemm(const GemmMaps& m, const GemmArgs& g, int grid,
                         cudaStream_t st) {
     auto kern = tcgen05_gemm_kernel<A_MN, B_MN, EPI, PAIR>;
     constexpr int smem = Geometry<PAIR>::SMEM_BYTES;
@@ -70,7 +76,7 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmAr
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    e = cudaLaunchKernelEx(&cfg, kern, a, b, g);
+    e = cudaLaunchKernelEx(&cfg, kern, m.a, m.b, m.o0, m.o1, g);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
