@@ -166,6 +166,17 @@ int operand_map(CUtensorMap* m, const Operand& o, int t, int tile_rows) {
 // 0: single-CTA kernel only, 1: CTA pairs when the problem fills them, 2: pairs always.
 std::atomic<int> g_pair_mode{1};
 
+#ifndef TPMLP_BAND_BUDGET_MB
+#define TPMLP_BAND_BUDGET_MB 16
+#endif
+constexpr long long kBandBudgetBytes = TPMLP_BAND_BUDGET_MB * (1LL << 20);
+constexpr long long kBandMaxPanelBytes = 4LL << 20;
+
+// Reduction length of one output tile (all shards' k ranges for SHARD_K).
+long long K_total_of(const GemmArgs&, int K, int t, int mode) {
+    return mode == SHARD_K ? 1LL * K * t : K;
+}
+
 // Fills the tile space of a GEMM with output extent M x N per shard.
 void tile_space(GemmArgs& g, int M, int N, int K, int t, int mode, long long a_bytes,
                 long long b_bytes, int tile_m) {
@@ -182,6 +193,15 @@ void tile_space(GemmArgs& g, int M, int N, int K, int t, int mode, long long a_b
     // Keep the larger operand's panels read once: walk the other operand's
     // tiles fastest so concurrent CTAs share the big panel through L2.
     g.raster_m_fastest = b_bytes >= a_bytes ? 1 : 0;
+    // With a short reduction the panels are small and tiles finish quickly,
+    // so the fast dimension's panels are re-read across waves: band them to
+    // an L2-sized working set.  With a long reduction the concurrent tiles
+    // walk K together and share each k-slab, so one band spans everything.
+    const int fast_tiles = g.raster_m_fastest ? g.mt_total : g.nt_total;
+    const long long panel = 2LL * (g.raster_m_fastest ? tile_m : BN) * K_total_of(g, K, t, mode);
+    g.band = fast_tiles;
+    if (panel <= kBandMaxPanelBytes && panel * fast_tiles > kBandBudgetBytes)
+        g.band = static_cast<int>(std::max<long long>(1, kBandBudgetBytes / panel));
 }
 
 typedef cudaError_t (*Launcher)(const GemmMaps&, const GemmArgs&, int, bool, cudaStream_t);

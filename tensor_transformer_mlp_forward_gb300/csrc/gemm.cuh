@@ -89,6 +89,7 @@ struct GemmArgs {
     int k_blocks;        // BK blocks per shard (SHARD_K) or in total
     int num_tiles;
     int raster_m_fastest;
+    int band;            // tiles per band along the fast dimension (see decode_tile)
     int o_on;             // ShardOn of the output tensor maps (Z and H, Y, dZ, dX, dA or dB)
     const __nv_bfloat16* bias;  // b1 or b2, indexed by global output column
     const __nv_bfloat16* aux;   // residual (EPI_BIAS_RESIDUAL) or Z (EPI_DGELU)
@@ -104,13 +105,25 @@ struct TileCoord {
 
 template <int TILE_M>
 __device__ __forceinline__ TileCoord decode_tile(int tile, const GemmArgs& p) {
+    // Tiles are visited in bands of `band` tiles along the fast dimension:
+    // inside a band the fast index cycles over the band while the slow index
+    // advances, so the band's panels of the fast-dimension operand stay in L2
+    // while the other operand streams past them.
     int mi, ni;
     if (p.raster_m_fastest) {
-        mi = tile % p.mt_total;
-        ni = tile / p.mt_total;
+        const int per_band = p.band * p.nt_total;
+        const int b = tile / per_band;
+        const int in = tile - b * per_band;
+        const int width = min(p.band, p.mt_total - b * p.band);
+        mi = b * p.band + in % width;
+        ni = in / width;
     } else {
-        ni = tile % p.nt_total;
-        mi = tile / p.nt_total;
+        const int per_band = p.band * p.mt_total;
+        const int b = tile / per_band;
+        const int in = tile - b * per_band;
+        const int width = min(p.band, p.nt_total - b * p.band);
+        ni = b * p.band + in % width;
+        mi = in / width;
     }
     TileCoord c;
     c.s = 0;
