@@ -37,7 +37,7 @@ sys.path.insert(0, ROOT)
 METRIC = "TFLOPS fwd+bwd of TP-sharded MLP block on 1 GB300; % of dense BF16 peak"
 UNIT = "TFLOPS"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_mtnlg_traffic.md")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_mtnlg_full.md")
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
 
