@@ -222,6 +222,7 @@ class Step:
         self.db1, self.db2 = e(F, dt=torch.float32), e(h, dt=torch.float32)
         self.p_db1 = e(max(1, int(binding.lib().tp_mlp_dgelu_partial_floats(T, F))), dt=torch.float32)
         self.p_db2 = e(max(1, int(binding.lib().tp_mlp_bias_grad_workspace_floats(T, h))), dt=torch.float32)
+        self.ws_split = e(max(16, binding.split_workspace_bytes(T, h, F, w.t)), dt=torch.uint8)
         self.launches = 0
 
     def run(self, events=None):
@@ -230,10 +231,11 @@ class Step:
         b, i, t = self.b, self.inp, self.w.t
         calls = (
             lambda: b.tp_mlp_column_gelu(i["X"], i["A"], i["b1"], t, Z=self.Z, H=self.H),
-            lambda: b.tp_mlp_row_sum(self.H, i["B"], i["b2"], i["residual"], t, Y=self.Y),
+            lambda: b.tp_mlp_row_sum(self.H, i["B"], i["b2"], i["residual"], t, Y=self.Y,
+                                     workspace=self.ws_split),
             lambda: b.tp_mlp_bias_grad(i["dY"], db=self.db2, partial=self.p_db2),
             lambda: b.tp_mlp_dgelu(i["dY"], i["B"], self.Z, t, dZ=self.dZ, db1=self.db1, partial=self.p_db1),
-            lambda: b.tp_mlp_dx(self.dZ, i["A"], t, dX=self.dX),
+            lambda: b.tp_mlp_dx(self.dZ, i["A"], t, dX=self.dX, workspace=self.ws_split),
             lambda: b.tp_mlp_dA(i["X"], self.dZ, t, dA=self.dA),
             lambda: b.tp_mlp_dB(self.H, i["dY"], t, dB=self.dB),
         )

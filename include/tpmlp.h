@@ -71,15 +71,27 @@ enum tpmlp_status {
 /* Whole block                                                             */
 /* ---------------------------------------------------------------------- */
 
+/* Bytes of optional float32 scratch that lets the row-parallel GEMMs (a3,
+ * a7) split their reduction when their ceil(T/256) x ceil(h/256) output tiles
+ * cannot occupy the GPU (small T).  0 when these sizes never split. */
+size_t tp_mlp_split_workspace_bytes(int T, int h, int F, int t);
+
+/* Same value, named for tp_mlp_forward's `workspace`. */
+size_t tp_mlp_forward_workspace_bytes(int T, int h, int F, int t);
+
 /* Forward pass (steps a2 + a3 below):
  *   Z = X A + b1, H = GeLU(Z)         (all t column shards)
  *   Y = sum_i H_i B_i + b2 + residual (g-operator sum of the row shards)
  * In:  X [T,h], A [h,F], b1 [F], B [F,h], b2 [h], residual [T,h].
- * Out: Y [T,h]; Z, H [T,F] are saved for the backward pass. */
+ * Out: Y [T,h]; Z, H [T,F] are saved for the backward pass.
+ * `workspace` (16-byte aligned, may be NULL) of tp_mlp_forward_workspace_bytes
+ * bytes lets a3 split its reduction (see tp_mlp_row_sum); with NULL or fewer
+ * bytes it splits less or not at all -- the result is the same sum up to
+ * float32 rounding order. */
 int tp_mlp_forward(const tpmlp_bf16* X, const tpmlp_bf16* A, const tpmlp_bf16* b1,
                    const tpmlp_bf16* B, const tpmlp_bf16* b2, const tpmlp_bf16* residual,
                    int T, int h, int F, int t, tpmlp_bf16* Y, tpmlp_bf16* Z, tpmlp_bf16* H,
-                   void* stream);
+                   void* workspace, size_t workspace_bytes, void* stream);
 
 /* Bytes of float32/bf16 scratch tp_mlp_backward needs for these sizes. */
 size_t tp_mlp_backward_workspace_bytes(int T, int h, int F, int t);
@@ -115,10 +127,15 @@ int tp_mlp_column_gelu(const tpmlp_bf16* X, const tpmlp_bf16* A, const tpmlp_bf1
 /* a3: row-parallel GEMM whose fp32 accumulator walks the shards in order,
  * so the partials H_i B_i meet in the accumulator (the g-operator sum),
  * with b2 and the residual fused into the epilogue:
- * Y = sum_i H_i B_i + b2 + residual.  H [T,F], B [F,h] -> Y [T,h]. */
+ * Y = sum_i H_i B_i + b2 + residual.  H [T,F], B [F,h] -> Y [T,h].
+ * When the output tiles are too few for the GPU and `workspace` (16-byte
+ * aligned, tp_mlp_split_workspace_bytes bytes; may be NULL) allows, each
+ * tile's k range -- the shards in order -- is cut into contiguous runs whose
+ * fp32 partial sums go to the workspace, and a second kernel adds them in
+ * run order with b2 and the residual (two launches instead of one). */
 int tp_mlp_row_sum(const tpmlp_bf16* H, const tpmlp_bf16* B, const tpmlp_bf16* b2,
                    const tpmlp_bf16* residual, int T, int h, int F, int t, tpmlp_bf16* Y,
-                   void* stream);
+                   void* workspace, size_t workspace_bytes, void* stream);
 
 /* Float32 elements of partial-sum scratch tp_mlp_bias_grad needs. */
 size_t tp_mlp_bias_grad_workspace_floats(int T, int n);
@@ -164,9 +181,9 @@ int tp_mlp_dgelu(const tpmlp_bf16* dY, const tpmlp_bf16* B, const tpmlp_bf16* Z,
 
 /* a7: dX = sum_i dZ_i A_i^T; the accumulator walks the shards in order, so
  * the f-operator sum happens in fp32 inside the GEMM.
- * dZ [T,F], A [h,F] -> dX [T,h]. */
+ * dZ [T,F], A [h,F] -> dX [T,h].  `workspace` as for tp_mlp_row_sum. */
 int tp_mlp_dx(const tpmlp_bf16* dZ, const tpmlp_bf16* A, int T, int h, int F, int t,
-              tpmlp_bf16* dX, void* stream);
+              tpmlp_bf16* dX, void* workspace, size_t workspace_bytes, void* stream);
 
 /* a8: dA_i = X^T dZ_i for every shard.  X [T,h], dZ [T,F] -> dA [h,F]. */
 int tp_mlp_dA(const tpmlp_bf16* X, const tpmlp_bf16* dZ, int T, int h, int F, int t,
@@ -187,8 +204,9 @@ int tp_mlp_dB(const tpmlp_bf16* H, const tpmlp_bf16* dY, int T, int h, int F, in
  *      through tcgen05 cta_group::2) when the problem has at least as many
  *      256 x 256 tiles as the GPU has SM pairs, else single CTAs;
  *   2  CTA pairs always.
- * Both kernels compute the same sums in the same order, so results are
- * bitwise identical across modes. */
+ * Both kernels compute the same sums in the same order (the split of a
+ * reduction does not depend on the mode), so results are bitwise identical
+ * across modes. */
 int tpmlp_set_cta_pair_mode(int mode);
 
 /* Static text for a status code. */

@@ -43,18 +43,20 @@ _I = ctypes.c_int
 _S = ctypes.c_size_t
 
 _SIGNATURES = {
-    "tp_mlp_forward": ([_P] * 6 + [_I] * 4 + [_P] * 3 + [_P], _I),
+    "tp_mlp_split_workspace_bytes": ([_I] * 4, _S),
+    "tp_mlp_forward_workspace_bytes": ([_I] * 4, _S),
+    "tp_mlp_forward": ([_P] * 6 + [_I] * 4 + [_P] * 3 + [_P, _S, _P], _I),
     "tp_mlp_backward_workspace_bytes": ([_I] * 4, _S),
     "tp_mlp_backward": ([_P] * 6 + [_I] * 4 + [_P] * 6 + [_S, _P], _I),
     "tp_mlp_column_gelu": ([_P] * 3 + [_I] * 4 + [_P] * 2 + [_P], _I),
-    "tp_mlp_row_sum": ([_P] * 4 + [_I] * 4 + [_P] + [_P], _I),
+    "tp_mlp_row_sum": ([_P] * 4 + [_I] * 4 + [_P] + [_P, _S, _P], _I),
     "tp_mlp_bias_grad_workspace_floats": ([_I, _I], _S),
     "tp_mlp_bias_grad": ([_P, _I, _I, _P, _P, _P], _I),
     "tp_mlp_bias_grad_noalloc": ([_P, _I, _I, _P, _P], _I),
     "tp_mlp_bias_grad_noalloc_max_floats": ([], _S),
     "tp_mlp_dgelu_partial_floats": ([_I, _I], _S),
     "tp_mlp_dgelu": ([_P] * 3 + [_I] * 4 + [_P] * 3 + [_P], _I),
-    "tp_mlp_dx": ([_P] * 2 + [_I] * 4 + [_P] + [_P], _I),
+    "tp_mlp_dx": ([_P] * 2 + [_I] * 4 + [_P] + [_P, _S, _P], _I),
     "tp_mlp_dA": ([_P] * 2 + [_I] * 4 + [_P] + [_P], _I),
     "tp_mlp_dB": ([_P] * 2 + [_I] * 4 + [_P] + [_P], _I),
     "tpmlp_status_string": ([_I], ctypes.c_char_p),
@@ -160,27 +162,45 @@ def tp_mlp_column_gelu(X, A, b1, t: int, Z=None, H=None, stream=None):
     return Z, H
 
 
-def tp_mlp_row_sum(H, B, b2, residual, t: int, Y=None, stream=None):
+def split_workspace_bytes(T: int, h: int, F: int, t: int) -> int:
+    return int(lib().tp_mlp_split_workspace_bytes(T, h, F, t))
+
+
+def _workspace(ws, need: int, like: torch.Tensor):
+    """The caller's workspace, or a fresh one of `need` bytes (None if 0)."""
+    if ws is None and need > 0:
+        ws = torch.empty(need, dtype=torch.uint8, device=like.device)
+    if ws is None:
+        return None, 0
+    return _ptr(ws, "workspace", None, torch.uint8), ws.numel()
+
+
+def tp_mlp_row_sum(H, B, b2, residual, t: int, Y=None, workspace=None, stream=None):
     T, F = H.shape
     h = B.shape[1]
     Y = _out(Y, (T, h), H)
+    wp, wn = _workspace(workspace, split_workspace_bytes(T, h, F, t), H)
     _check("tp_mlp_row_sum", lib().tp_mlp_row_sum(
         _ptr(H, "H", (T, F)), _ptr(B, "B", (F, h)), _ptr(b2, "b2", (h,)),
-        _ptr(residual, "residual", (T, h)), T, h, F, t, _ptr(Y, "Y", (T, h)), _stream(stream)))
+        _ptr(residual, "residual", (T, h)), T, h, F, t, _ptr(Y, "Y", (T, h)), wp, wn,
+        _stream(stream)))
     return Y
 
 
-def tp_mlp_forward(X, A, b1, B, b2, residual, t: int, Y=None, Z=None, H=None, stream=None):
+def tp_mlp_forward(X, A, b1, B, b2, residual, t: int, Y=None, Z=None, H=None, workspace=None,
+                   stream=None):
     """Y, Z, H of the block (Z, H saved for the backward pass)."""
     T, h = X.shape
     F = A.shape[1]
     Y = _out(Y, (T, h), X)
     Z = _out(Z, (T, F), X)
     H = _out(H, (T, F), X)
+    wp, wn = _workspace(workspace, int(lib().tp_mlp_forward_workspace_bytes(T, h, F, t)), X)
     _check("tp_mlp_forward", lib().tp_mlp_forward(
         _ptr(X, "X", (T, h)), _ptr(A, "A", (h, F)), _ptr(b1, "b1", (F,)), _ptr(B, "B", (F, h)),
         _ptr(b2, "b2", (h,)), _ptr(residual, "residual", (T, h)), T, h, F, t,
-        _ptr(Y, "Y", (T, h)), _ptr(Z, "Z", (T, F)), _ptr(H, "H", (T, F)), _stream(stream)))
+        _ptr(Y, "Y", (T, h)), _ptr(Z, "Z", (T, F)), _ptr(H, "H", (T, F)), wp, wn,
+        _stream(stream)))
     return Y, Z, H
 
 
@@ -249,12 +269,13 @@ def tp_mlp_dgelu(dY, B, Z, t: int, dZ=None, db1=None, partial=None, stream=None)
     return dZ, db1
 
 
-def tp_mlp_dx(dZ, A, t: int, dX=None, stream=None):
+def tp_mlp_dx(dZ, A, t: int, dX=None, workspace=None, stream=None):
     T, F = dZ.shape
     h = A.shape[0]
     dX = _out(dX, (T, h), dZ)
+    wp, wn = _workspace(workspace, split_workspace_bytes(T, h, F, t), dZ)
     _check("tp_mlp_dx", lib().tp_mlp_dx(
-        _ptr(dZ, "dZ", (T, F)), _ptr(A, "A", (h, F)), T, h, F, t, _ptr(dX, "dX", (T, h)),
+        _ptr(dZ, "dZ", (T, F)), _ptr(A, "A", (h, F)), T, h, F, t, _ptr(dX, "dX", (T, h)), wp, wn,
         _stream(stream)))
     return dX
 

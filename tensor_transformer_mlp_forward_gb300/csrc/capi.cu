@@ -150,6 +150,24 @@ int make_map(CUtensorMap* m, const void* ptr, long long rows, long long cols, in
     return TPMLP_OK;
 }
 
+// fp32 map over a [splits, rows, cols] partial-sum workspace: dims {cols, rows,
+// splits}, 32 x 32 boxes (128-byte rows, 128-byte swizzle).
+int make_partial_map(CUtensorMap* m, void* ptr, long long rows, long long cols, int splits) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(splits)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 4,
+                             static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(cols) * 4};
+    cuuint32_t box[3] = {32, 32, 1}, estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        t_last_cuda_error = static_cast<int>(r);
+        return TPMLP_ERR_LAUNCH;
+    }
+    return TPMLP_OK;
+}
+
 // One GEMM operand: a row-major [rows, cols] matrix, K-major or MN-major in
 // the product, with its shard placement.
 struct Operand {
@@ -190,6 +208,8 @@ void tile_space(GemmArgs& g, int M, int N, int K, int t, int mode, long long a_b
     g.nt_total = g.n_tiles * (mode == SHARD_N ? t : 1);
     g.k_blocks = static_cast<int>(cdiv(K, BK));
     g.num_tiles = g.mt_total * g.nt_total;
+    g.base_tiles = g.num_tiles;
+    g.k_splits = 1;
     // Keep the larger operand's panels read once: walk the other operand's
     // tiles fastest so concurrent CTAs share the big panel through L2.
     g.raster_m_fastest = b_bytes >= a_bytes ? 1 : 0;
@@ -212,6 +232,7 @@ struct Output {
     void* ptr0;
     void* ptr1;
     long long rows, cols;
+    int k_splits;  // > 1: ptr0 is an fp32 [k_splits, rows, cols] partial-sum workspace
 };
 
 // One GEMM: M x N output per shard, K reduction (per shard for SHARD_K).
@@ -259,12 +280,19 @@ int run_gemm(Launcher fn, const Operand& a, const Operand& b, const Output& out,
     }
     tile_space(g, f.M, f.N, f.K, f.t, f.mode, f.a_bytes, f.b_bytes, tile_m);
     if (g.num_tiles == 0) return TPMLP_OK;
+    if (out.k_splits > 1) {
+        g.k_splits = out.k_splits;
+        g.num_tiles = g.base_tiles * out.k_splits;
+    }
     alignas(64) GemmMaps maps;
     int rc = operand_map(&maps.a, fa, f.t, BM);
     if (rc) return rc;
     rc = operand_map(&maps.b, fb, f.t, pair ? BN / 2 : BN);
     if (rc) return rc;
-    rc = make_map(&maps.o0, out.ptr0, out.rows, out.cols, o_t, g.o_on, 32);
+    if (out.k_splits > 1)
+        rc = make_partial_map(&maps.o0, out.ptr0, out.rows, out.cols, out.k_splits);
+    else
+        rc = make_map(&maps.o0, out.ptr0, out.rows, out.cols, o_t, g.o_on, 32);
     if (rc) return rc;
     rc = make_map(&maps.o1, out.ptr1 ? out.ptr1 : out.ptr0, out.rows, out.cols, o_t, g.o_on, 32);
     if (rc) return rc;
@@ -301,9 +329,97 @@ int column_gelu(const tpmlp_bf16* X, const tpmlp_bf16* A, const tpmlp_bf16* b1, 
     return run_gemm(launch_column_gelu, a, b, o, g, sh, st, d);
 }
 
+// ----------------------------------------------------- split reductions
+
+// The row-parallel GEMMs (a3, a7) have only ceil(T/256) x ceil(h/256) output
+// tiles.  When that leaves SM pairs idle, each tile's k range (the shards, in
+// order) is cut into `splits` contiguous runs computed by different CTA pairs
+// as fp32 partial sums -- the pages' per-rank partials -- and a second kernel
+// adds them in run order, then b2 and the residual.  `units` is the number of
+// CTA pairs.  Returns 1 (no split) unless splitting saves >= 20 % of the waves.
+int choose_splits(long long M, long long N, long long total_kb, int units) {
+    const long long tiles = cdiv(M, 2 * BM) * cdiv(N, BN);
+    if (units <= 0 || tiles <= 0) return 1;
+    const double base = static_cast<double>(cdiv(tiles, units));
+    double best = base;
+    int best_s = 1;
+    for (int sp = 2; sp <= 8 && total_kb / sp >= 8; ++sp) {
+        const double c = static_cast<double>(cdiv(tiles * sp, units)) / sp;
+        if (c < best - 1e-9) {
+            best = c;
+            best_s = sp;
+        }
+    }
+    return best <= 0.8 * base ? best_s : 1;
+}
+
+// CTA pairs the split heuristic assumes when sizing workspaces (GB300: 152 SMs).
+constexpr int kSizingPairs = 76;
+
+long long row_total_kb(int F, int t) { return cdiv(F / t, BK) * t; }
+
+// Floats of split-reduction workspace the row-parallel GEMMs of this shape use.
+size_t split_partial_floats(int T, int h, int F, int t) {
+    const int sp = choose_splits(T, h, row_total_kb(F, t), kSizingPairs);
+    return sp > 1 ? static_cast<size_t>(sp) * T * h : 0;
+}
+
+// out[i] = bf16(sum_s P[s][i] (+ bias[i % n] + res[i])), 8 elements a thread.
+__global__ void __launch_bounds__(256)
+    split_reduce_kernel(const float* __restrict__ P, int splits, long long count, int n,
+                        const __nv_bfloat16* __restrict__ bias, const __nv_bfloat16* __restrict__ res,
+                        __nv_bfloat16* __restrict__ out) {
+    const long long i = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
+    if (i >= count) return;
+    float a[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) a[j] = 0.0f;
+    for (int sp = 0; sp < splits; ++sp) {
+        const float4* q = reinterpret_cast<const float4*>(P + sp * count + i);
+        const float4 x = __ldg(q), y = __ldg(q + 1);
+        a[0] += x.x; a[1] += x.y; a[2] += x.z; a[3] += x.w;
+        a[4] += y.x; a[5] += y.y; a[6] += y.z; a[7] += y.w;
+    }
+    if (bias != nullptr) {
+        const uint4 b = __ldg(reinterpret_cast<const uint4*>(bias + i % n));
+        const uint4 r = __ldg(reinterpret_cast<const uint4*>(res + i));
+        const uint32_t bw[4] = {b.x, b.y, b.z, b.w}, rw[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            a[2 * j] += __uint_as_float(bw[j] << 16) + __uint_as_float(rw[j] << 16);
+            a[2 * j + 1] += __uint_as_float(bw[j] & 0xFFFF0000u) + __uint_as_float(rw[j] & 0xFFFF0000u);
+        }
+    }
+    uint4 o;
+    o.x = pack_bf16x2(a[0], a[1]);
+    o.y = pack_bf16x2(a[2], a[3]);
+    o.z = pack_bf16x2(a[4], a[5]);
+    o.w = pack_bf16x2(a[6], a[7]);
+    *reinterpret_cast<uint4*>(out + i) = o;
+}
+
+int launch_split_reduce(const float* P, int splits, int T, int h, const tpmlp_bf16* bias,
+                        const tpmlp_bf16* res, tpmlp_bf16* out, cudaStream_t st) {
+    const long long count = 1LL * T * h;
+    split_reduce_kernel<<<static_cast<unsigned>(cdiv(count / 8, 256)), 256, 0, st>>>(
+        P, splits, count, h, cb(bias), cb(res), reinterpret_cast<__nv_bfloat16*>(out));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail_cuda(e);
+    ++t_last_launches;
+    return TPMLP_OK;
+}
+
+// Splits to use for a row-parallel GEMM given the caller's workspace.
+int row_splits(int T, int h, int F, int t, size_t ws_bytes, const DeviceInfo& d) {
+    int sp = choose_splits(T, h, row_total_kb(F, t), d.sms / 2);
+    const size_t per = sizeof(float) * static_cast<size_t>(T) * h;
+    while (sp > 1 && static_cast<size_t>(sp) * per > ws_bytes) --sp;
+    return sp;
+}
+
 int row_sum(const tpmlp_bf16* H, const tpmlp_bf16* B, const tpmlp_bf16* b2,
-            const tpmlp_bf16* R, int T, int h, int F, int t, tpmlp_bf16* Y, cudaStream_t st,
-            const DeviceInfo& d) {
+            const tpmlp_bf16* R, int T, int h, int F, int t, tpmlp_bf16* Y, void* ws,
+            size_t ws_bytes, cudaStream_t st, const DeviceInfo& d) {
     const int f = F / t;
     GemmArgs g = blank_args();
     const GemmShape sh{T, h, f, t, SHARD_K, 1LL * T * F, 1LL * F * h};
@@ -314,8 +430,14 @@ int row_sum(const tpmlp_bf16* H, const tpmlp_bf16* B, const tpmlp_bf16* b2,
     g.ld_aux = h;
     Operand a{H, T, F, ON_CONTIG, false};
     Operand b{B, F, h, ON_ROWS, true};
-    Output o{Y, nullptr, T, h};
-    return run_gemm(launch_row_sum, a, b, o, g, sh, st, d);
+    const int sp = ws ? row_splits(T, h, F, t, ws_bytes, d) : 1;
+    if (sp == 1) {
+        Output o{Y, nullptr, T, h, 1};
+        return run_gemm(launch_row_sum, a, b, o, g, sh, st, d);
+    }
+    Output o{ws, nullptr, T, h, sp};
+    if (int rc = run_gemm(launch_row_partial, a, b, o, g, sh, st, d)) return rc;
+    return launch_split_reduce(static_cast<const float*>(ws), sp, T, h, b2, R, Y, st);
 }
 
 int dgelu_gemm(const tpmlp_bf16* dY, const tpmlp_bf16* B, const tpmlp_bf16* Z, int T, int h,
@@ -336,7 +458,7 @@ int dgelu_gemm(const tpmlp_bf16* dY, const tpmlp_bf16* B, const tpmlp_bf16* Z, i
 }
 
 int dx_gemm(const tpmlp_bf16* dZ, const tpmlp_bf16* A, int T, int h, int F, int t,
-            tpmlp_bf16* dX, cudaStream_t st, const DeviceInfo& d) {
+            tpmlp_bf16* dX, void* ws, size_t ws_bytes, cudaStream_t st, const DeviceInfo& d) {
     const int f = F / t;
     GemmArgs g = blank_args();
     const GemmShape sh{T, h, f, t, SHARD_K, 1LL * T * F, 1LL * h * F};
@@ -344,8 +466,14 @@ int dx_gemm(const tpmlp_bf16* dZ, const tpmlp_bf16* A, int T, int h, int F, int 
     g.b_on = ON_CONTIG;
     Operand a{dZ, T, F, ON_CONTIG, false};
     Operand b{A, h, F, ON_CONTIG, false};
-    Output o{dX, nullptr, T, h};
-    return run_gemm(launch_dx, a, b, o, g, sh, st, d);
+    const int sp = ws ? row_splits(T, h, F, t, ws_bytes, d) : 1;
+    if (sp == 1) {
+        Output o{dX, nullptr, T, h, 1};
+        return run_gemm(launch_dx, a, b, o, g, sh, st, d);
+    }
+    Output o{ws, nullptr, T, h, sp};
+    if (int rc = run_gemm(launch_dx_partial, a, b, o, g, sh, st, d)) return rc;
+    return launch_split_reduce(static_cast<const float*>(ws), sp, T, h, nullptr, nullptr, dX, st);
 }
 
 int dA_gemm(const tpmlp_bf16* X, const tpmlp_bf16* dZ, int T, int h, int F, int t,
@@ -501,16 +629,17 @@ size_t dgelu_partial_floats(int T, int F) {
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct BackwardLayout {
-    size_t dz, colsum, db2, total;
+    size_t dz, colsum, db2, split, total;
 };
 
-BackwardLayout backward_layout(int T, int h, int F) {
+BackwardLayout backward_layout(int T, int h, int F, int t) {
     BackwardLayout L;
     L.dz = 0;
     L.colsum = align256(L.dz + sizeof(uint16_t) * static_cast<size_t>(T) * F);
     L.db2 = align256(L.colsum + sizeof(float) * dgelu_partial_floats(T, F));
     const size_t db2_floats = static_cast<size_t>(colsum_chunks(T, h)) * h;
-    L.total = align256(L.db2 + sizeof(float) * db2_floats);
+    L.split = align256(L.db2 + sizeof(float) * db2_floats);
+    L.total = align256(L.split + sizeof(float) * split_partial_floats(T, h, F, t));
     return L;
 }
 
@@ -549,29 +678,32 @@ TPMLP_API int tp_mlp_column_gelu(const tpmlp_bf16* X, const tpmlp_bf16* A, const
 
 TPMLP_API int tp_mlp_row_sum(const tpmlp_bf16* H, const tpmlp_bf16* B, const tpmlp_bf16* b2,
                              const tpmlp_bf16* residual, int T, int h, int F, int t, tpmlp_bf16* Y,
-                             void* stream) {
+                             void* workspace, size_t workspace_bytes, void* stream) {
     TPMLP_PROLOGUE(check_dims(T, h, F, t));
     if (T == 0) return TPMLP_OK;
     if (any_null(H, B, b2, residual, Y)) return TPMLP_ERR_NULL;
-    if (!all_aligned(H, B, b2, residual, Y)) return TPMLP_ERR_ALIGN;
+    if (!all_aligned(H, B, b2, residual, Y, workspace)) return TPMLP_ERR_ALIGN;
     DeviceInfo d;
     if (int rc = enter(d)) return rc;
-    return row_sum(H, B, b2, residual, T, h, F, t, Y, static_cast<cudaStream_t>(stream), d);
+    return row_sum(H, B, b2, residual, T, h, F, t, Y, workspace, workspace_bytes,
+                   static_cast<cudaStream_t>(stream), d);
 }
 
 TPMLP_API int tp_mlp_forward(const tpmlp_bf16* X, const tpmlp_bf16* A, const tpmlp_bf16* b1,
                              const tpmlp_bf16* B, const tpmlp_bf16* b2,
                              const tpmlp_bf16* residual, int T, int h, int F, int t,
-                             tpmlp_bf16* Y, tpmlp_bf16* Z, tpmlp_bf16* H, void* stream) {
+                             tpmlp_bf16* Y, tpmlp_bf16* Z, tpmlp_bf16* H, void* workspace,
+                             size_t workspace_bytes, void* stream) {
     TPMLP_PROLOGUE(check_dims(T, h, F, t));
     if (T == 0) return TPMLP_OK;
     if (any_null(X, A, b1, B, b2, residual, Y, Z, H)) return TPMLP_ERR_NULL;
     if (!all_aligned(X, A, b1, B, b2, residual, Y, Z, H)) return TPMLP_ERR_ALIGN;
+    if (!aligned16(workspace)) return TPMLP_ERR_ALIGN;
     DeviceInfo d;
     if (int rc = enter(d)) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (int rc = column_gelu(X, A, b1, T, h, F, t, Z, H, st, d)) return rc;
-    return row_sum(H, B, b2, residual, T, h, F, t, Y, st, d);
+    return row_sum(H, B, b2, residual, T, h, F, t, Y, workspace, workspace_bytes, st, d);
 }
 
 TPMLP_API size_t tp_mlp_bias_grad_workspace_floats(int T, int n) {
@@ -672,14 +804,15 @@ TPMLP_API int tp_mlp_dgelu(const tpmlp_bf16* dY, const tpmlp_bf16* B, const tpml
 }
 
 TPMLP_API int tp_mlp_dx(const tpmlp_bf16* dZ, const tpmlp_bf16* A, int T, int h, int F, int t,
-                        tpmlp_bf16* dX, void* stream) {
+                        tpmlp_bf16* dX, void* workspace, size_t workspace_bytes, void* stream) {
     TPMLP_PROLOGUE(check_dims(T, h, F, t));
     if (T == 0) return TPMLP_OK;
     if (any_null(dZ, A, dX)) return TPMLP_ERR_NULL;
-    if (!all_aligned(dZ, A, dX)) return TPMLP_ERR_ALIGN;
+    if (!all_aligned(dZ, A, dX, workspace)) return TPMLP_ERR_ALIGN;
     DeviceInfo d;
     if (int rc = enter(d)) return rc;
-    return dx_gemm(dZ, A, T, h, F, t, dX, static_cast<cudaStream_t>(stream), d);
+    return dx_gemm(dZ, A, T, h, F, t, dX, workspace, workspace_bytes,
+                   static_cast<cudaStream_t>(stream), d);
 }
 
 TPMLP_API int tp_mlp_dA(const tpmlp_bf16* X, const tpmlp_bf16* dZ, int T, int h, int F, int t,
@@ -712,9 +845,18 @@ TPMLP_API int tp_mlp_dB(const tpmlp_bf16* H, const tpmlp_bf16* dY, int T, int h,
     return dB_gemm(H, dY, T, h, F, t, dB, st, d);
 }
 
+TPMLP_API size_t tp_mlp_split_workspace_bytes(int T, int h, int F, int t) {
+    if (check_dims(T, h, F, t) || T == 0) return 0;
+    return sizeof(float) * split_partial_floats(T, h, F, t);
+}
+
+TPMLP_API size_t tp_mlp_forward_workspace_bytes(int T, int h, int F, int t) {
+    return tp_mlp_split_workspace_bytes(T, h, F, t);
+}
+
 TPMLP_API size_t tp_mlp_backward_workspace_bytes(int T, int h, int F, int t) {
     if (check_dims(T, h, F, t)) return 0;
-    return backward_layout(T, h, F).total;
+    return backward_layout(T, h, F, t).total;
 }
 
 TPMLP_API int tp_mlp_backward(const tpmlp_bf16* dY, const tpmlp_bf16* X, const tpmlp_bf16* A,
@@ -726,7 +868,7 @@ TPMLP_API int tp_mlp_backward(const tpmlp_bf16* dY, const tpmlp_bf16* X, const t
     if (any_null(A, B, dA, dB, db1, db2) || (T > 0 && any_null(dY, X, Z, H, dX)))
         return TPMLP_ERR_NULL;
     if (!all_aligned(dY, X, A, B, Z, H, dX, dA, dB, db1, db2)) return TPMLP_ERR_ALIGN;
-    const BackwardLayout L = backward_layout(T, h, F);
+    const BackwardLayout L = backward_layout(T, h, F, t);
     if (T > 0 && (workspace == nullptr || workspace_bytes < L.total)) return TPMLP_ERR_WORKSPACE;
     if (!aligned16(workspace)) return TPMLP_ERR_ALIGN;
     DeviceInfo d;
@@ -750,7 +892,7 @@ TPMLP_API int tp_mlp_backward(const tpmlp_bf16* dY, const tpmlp_bf16* X, const t
     if (int rc = dgelu_gemm(dY, B, Z, T, h, F, t, dZ, colsum, st, d)) return rc;
     if (int rc = launch_rowsum(colsum, static_cast<int>(4 * cdiv(T, BM)), F, db1, st)) return rc;
     // a7: dX = sum_i dZ_i A_i^T (the f-operator sum inside the accumulator)
-    if (int rc = dx_gemm(dZ, A, T, h, F, t, dX, st, d)) return rc;
+    if (int rc = dx_gemm(dZ, A, T, h, F, t, dX, ws + L.split, L.total - L.split, st, d)) return rc;
     // a8, a9: weight gradients of every shard
     if (int rc = dA_gemm(X, dZ, T, h, F, t, dA, st, d)) return rc;
     return dB_gemm(H, dY, T, h, F, t, dB, st, d);

@@ -76,7 +76,9 @@ struct Geometry {
 enum ShardMode { SHARD_NONE = 0, SHARD_N = 1, SHARD_M = 2, SHARD_K = 3 };
 // Where an operand's tensor map carries the shard index.
 enum ShardOn { ON_NONE = 0, ON_CONTIG = 1, ON_ROWS = 2 };
-enum Epilogue { EPI_BIAS_GELU = 0, EPI_BIAS_RESIDUAL = 1, EPI_DGELU = 2, EPI_STORE = 3 };
+// EPI_PARTIAL: split reduction -- the fp32 accumulator of k-range split ks is
+// stored as is into plane ks of an fp32 [splits, M, N] workspace.
+enum Epilogue { EPI_BIAS_GELU = 0, EPI_BIAS_RESIDUAL = 1, EPI_DGELU = 2, EPI_STORE = 3, EPI_PARTIAL = 4 };
 
 struct GemmArgs {
     int M, N;            // output extent of one shard (SHARD_M: M per shard; SHARD_N: N per shard)
@@ -87,7 +89,9 @@ struct GemmArgs {
     int n_tiles;         // n tiles per shard (SHARD_N) or in total
     int mt_total, nt_total;
     int k_blocks;        // BK blocks per shard (SHARD_K) or in total
-    int num_tiles;
+    int num_tiles;       // work units: output tiles x k_splits
+    int base_tiles;      // output tiles (mt_total * nt_total)
+    int k_splits;        // contiguous k-block ranges per output tile (EPI_PARTIAL)
     int raster_m_fastest;
     int band;            // tiles per band along the fast dimension (see decode_tile)
     int o_on;             // ShardOn of the output tensor maps (Z and H, Y, dZ, dX, dA or dB)
@@ -101,10 +105,15 @@ struct GemmArgs {
 
 struct TileCoord {
     int m0, n0, s;
+    int ks;  // k-range split of this work unit (0 unless the reduction is split)
 };
 
 template <int TILE_M>
 __device__ __forceinline__ TileCoord decode_tile(int tile, const GemmArgs& p) {
+    // Work unit -> (split, output tile): the splits of one tile are
+    // base_tiles apart, so each split sweeps the tiles in the order below.
+    const int ks = tile / p.base_tiles;
+    tile -= ks * p.base_tiles;
     // Tiles are visited in bands of `band` tiles along the fast dimension:
     // inside a band the fast index cycles over the band while the slow index
     // advances, so the band's panels of the fast-dimension operand stay in L2
@@ -127,6 +136,7 @@ __device__ __forceinline__ TileCoord decode_tile(int tile, const GemmArgs& p) {
     }
     TileCoord c;
     c.s = 0;
+    c.ks = ks;
     if (p.shard_mode == SHARD_N) {
         c.s = ni / p.n_tiles;
         ni -= c.s * p.n_tiles;
@@ -347,10 +357,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const TileCoord tc = decode_tile<G::TILE_M>(tile, p);
                 const int a_row0 = tc.m0 + static_cast<int>(rank) * BM;
                 const int b_row0 = tc.n0 + static_cast<int>(rank) * G::B_ROWS;
-                int s = split_k ? 0 : tc.s;  // shard of the k range (SHARD_K walks them all)
-                int k0 = 0, kb_in_shard = 0;
+                // this unit's k-blocks [kb_begin, kb_end) and where they start
+                const int kb_begin = tc.ks * total_kb / p.k_splits;
+                const int kb_end = (tc.ks + 1) * total_kb / p.k_splits;
+                int s = tc.s, kb_in_shard = kb_begin;  // shard of the k range
+                if (split_k) {                          // SHARD_K walks the shards
+                    s = kb_begin / p.k_blocks;
+                    kb_in_shard = kb_begin - s * p.k_blocks;
+                }
+                int k0 = kb_in_shard * BK;
                 bool ok = true;
-                for (int kb = 0; kb < total_kb; ++kb) {
+                for (int kb = kb_begin; kb < kb_end; ++kb) {
                     if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
                         ok = false;
                         break;
@@ -405,8 +422,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (!wait_bounded(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
+                const int ks = p.k_splits > 1 ? tile / p.base_tiles : 0;
+                const int kb_begin = ks * total_kb / p.k_splits;
+                const int kb_end = (ks + 1) * total_kb / p.k_splits;
                 bool ok = true;
-                for (int kb = 0; kb < total_kb; ++kb) {
+                for (int kb = kb_begin; kb < kb_end; ++kb) {
                     if (!wait_bounded(&full[stage], phase, abort_flag, p.status)) {
                         ok = false;
                         break;
@@ -416,7 +436,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint64_t bd = b_desc0 + ((stage * G::B_STAGE_BYTES) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        const uint32_t accum = (kb | kk) != 0 ? 1u : 0u;
+                        const uint32_t accum = (kb != kb_begin || kk != 0) ? 1u : 0u;
                         if constexpr (PAIR)
                             tc_mma_f16_pair(d_tmem, ad + kk * desc_k_step<A_MN>(),
                                             bd + kk * desc_k_step<B_MN>(), idesc, accum);
@@ -479,6 +499,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (p.shard_mode == SHARD_N) gcol0 += static_cast<long long>(tc.s) * p.N;
             if (p.shard_mode == SHARD_M) grow += static_cast<long long>(tc.s) * p.M;
 
+            if constexpr (EPI == EPI_PARTIAL) {
+                // fp32 accumulator blocks of 32 rows x 32 columns (128 B rows)
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    const int n = tc.n0 + c * 32;
+                    const uint32_t buf = buf_base + (seq & 1u) * EPI_BUF_BYTES;
+                    if (lane == 0) bulk_wait_group_read<1>();
+                    __syncwarp();
+                    uint32_t r[32];
+                    tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + c * 32, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(buf + my_row + ((static_cast<uint32_t>(j) ^ swz) << 4), r[4 * j],
+                                     r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (row0 < p.M && n < p.N) {  // warp-uniform
+                        if (lane == 0) {
+                            tma_store_3d(&tmO0, buf, n, row0, tc.ks);
+                            bulk_commit_group();
+                        }
+                        ++seq;
+                    }
+                }
+            } else {
 #pragma unroll 1
             for (int c = 0; c < BN / 64; ++c) {
                 const int n64 = tc.n0 + c * 64;
@@ -561,6 +607,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     ++seq;
                 }
+            }
             }
             // TMEM of this accumulator may be overwritten from here on.
             tc_fence_before();

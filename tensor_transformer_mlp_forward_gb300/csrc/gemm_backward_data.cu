@@ -16,4 +16,10 @@ cudaError_t launch_dx(const GemmMaps& m, const GemmArgs& g, int grid,
     return launch_gemm<false, false, EPI_STORE, false>(m, g, grid, st);
 }
 
+cudaError_t launch_dx_partial(const GemmMaps& m, const GemmArgs& g, int grid, bool pair,
+                               cudaStream_t st) {
+    if (pair) return launch_gemm<false, false, EPI_PARTIAL, true>(m, g, grid, st);
+    return launch_gemm<false, false, EPI_PARTIAL, false>(m, g, grid, st);
+}
+
 }  // namespace tpmlp

@@ -22,11 +22,16 @@ cudaError_t launch_column_gelu(const GemmMaps& m, const GemmArgs& g,
                                int grid, bool pair, cudaStream_t st);
 cudaError_t launch_row_sum(const GemmMaps& m, const GemmArgs& g,
                            int grid, bool pair, cudaStream_t st);
+// The same two GEMMs with a split reduction: fp32 partials per k-range split.
+cudaError_t launch_row_partial(const GemmMaps& m, const GemmArgs& g, int grid, bool pair,
+                               cudaStream_t st);
 // A K-major, B K-major: dZ and dX.
 cudaError_t launch_dgelu(const GemmMaps& m, const GemmArgs& g, int grid,
                          bool pair, cudaStream_t st);
 cudaError_t launch_dx(const GemmMaps& m, const GemmArgs& g, int grid,
                       bool pair, cudaStream_t st);
+cudaError_t launch_dx_partial(const GemmMaps& m, const GemmArgs& g, int grid, bool pair,
+                              cudaStream_t st);
 // A MN-major, B MN-major: the weight gradients.
 cudaError_t launch_weight_grad(const GemmMaps& m, const GemmArgs& g,
                                int grid, bool pair, cudaStream_t st);

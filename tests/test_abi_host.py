@@ -37,7 +37,7 @@ N = None
 
 
 def fwd(L, *, X=P, T=128, h=256, F=1024, t=2, Y=P):
-    return L.tp_mlp_forward(X, P, P, P, P, P, T, h, F, t, Y, P, P, N)
+    return L.tp_mlp_forward(X, P, P, P, P, P, T, h, F, t, Y, P, P, N, 0, N)
 
 
 @pytest.mark.parametrize("kw", [
@@ -52,7 +52,9 @@ def test_null_and_alignment_errors(L):
     assert fwd(L, X=N) == binding.TPMLP_ERR_NULL
     assert fwd(L, Y=N) == binding.TPMLP_ERR_NULL
     assert fwd(L, X=Q) == binding.TPMLP_ERR_ALIGN
-    assert L.tp_mlp_dx(P, Q, 128, 256, 1024, 2, P, N) == binding.TPMLP_ERR_ALIGN
+    assert L.tp_mlp_dx(P, Q, 128, 256, 1024, 2, P, N, 0, N) == binding.TPMLP_ERR_ALIGN
+    assert L.tp_mlp_dx(P, P, 128, 256, 1024, 2, P, Q, 1 << 20, N) == binding.TPMLP_ERR_ALIGN
+    assert L.tp_mlp_row_sum(P, P, P, P, 128, 256, 1024, 2, P, Q, 1 << 20, N) == binding.TPMLP_ERR_ALIGN
     assert L.tp_mlp_dA(P, P, 128, 256, 1024, 2, N, N) == binding.TPMLP_ERR_NULL
     assert L.tp_mlp_bias_grad(P, 128, 12, P, P, N) == binding.TPMLP_ERR_SHAPE
 
@@ -67,6 +69,20 @@ def test_workspace_errors(L):
     assert L.tp_mlp_backward(*args, P, need - 1, N) == binding.TPMLP_ERR_WORKSPACE
     assert L.tp_mlp_backward(*args, Q, need, N) == binding.TPMLP_ERR_ALIGN
     assert L.tp_mlp_backward_workspace_bytes(T, h, 1000, 8) == 0
+
+
+def test_split_workspace_sizes(L):
+    # few output tiles (T=512, h=4096: 2 x 16 tiles of 256 x 256): the
+    # row-parallel GEMMs split their reduction, and the scratch covers it
+    n = L.tp_mlp_split_workspace_bytes(512, 4096, 16384, 8)
+    assert n > 0 and n % (4 * 512 * 4096) == 0
+    assert L.tp_mlp_forward_workspace_bytes(512, 4096, 16384, 8) == n
+    # many tiles (MT-NLG 530B): no split, no scratch
+    assert L.tp_mlp_split_workspace_bytes(2048, 20480, 81920, 8) == 0
+    assert L.tp_mlp_split_workspace_bytes(0, 4096, 16384, 8) == 0
+    # the backward workspace includes the dX split scratch
+    assert (L.tp_mlp_backward_workspace_bytes(512, 4096, 16384, 8)
+            >= n + 2 * 512 * 16384)
 
 
 def test_scratch_sizes(L):

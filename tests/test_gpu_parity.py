@@ -99,6 +99,28 @@ def test_pairs_and_single_cta_agree_bitwise():
         assert torch.equal(single[k], pairs[k]), k
 
 
+def test_split_reduction_matches_unsplit():
+    """The row-parallel GEMMs with and without a split reduction (few output
+    tiles: T=512, h=4096 gives 2 x 16 tiles) agree up to the bf16 rounding of
+    their outputs; the oracle comparison of the split path is
+    test_full_size_sampled[sweep-h4096_T512_t1]."""
+    w = inputs.SWEEP.with_shape(T=512, t=4)
+    cpu = inputs.make_inputs(w)
+    g = {k: v.cuda() for k, v in cpu.items()}
+    assert binding.split_workspace_bytes(w.T, w.h, w.F, w.t) > 0
+    H = torch.randn(w.T, w.F, device="cuda").mul_(0.5).to(torch.bfloat16)
+    y_split = binding.tp_mlp_row_sum(H, g["B"], g["b2"], g["residual"], w.t)
+    empty = torch.empty(0, dtype=torch.uint8, device="cuda")
+    y_one = binding.tp_mlp_row_sum(H, g["B"], g["b2"], g["residual"], w.t, workspace=empty)
+    dx_split = binding.tp_mlp_dx(H, g["A"], w.t)
+    dx_one = binding.tp_mlp_dx(H, g["A"], w.t, workspace=empty)
+    torch.cuda.synchronize()
+    assert binding.device_status() == 0
+    assert rel(np64(y_split), np64(y_one)) < TOL_FWD  # one bf16 ulp apart at most
+    assert rel(np64(dx_split), np64(dx_one)) < TOL_FWD
+    assert not torch.equal(dx_split, dx_one)  # the split path really ran
+
+
 def test_empty_batch():
     w = inputs.custom(T=0, h=64, F=256, t=2, seed=17)
     cpu = inputs.make_inputs(w)
