@@ -49,7 +49,9 @@ class Oracle:
         L.orc_backward_rows_bf16.argtypes = [up] * 5 + [cl] * 4 + [lp, cl, dp]
         L.orc_backward_cols_bf16.argtypes = [up] * 5 + [cl] * 4 + [lp, cl] + [dp] * 3
         L.orc_db2_bf16.argtypes = [up, cl, cl, dp]
-        for name in ("orc_forward", "orc_backward", "orc_forward_rows_bf16",
+        L.orc_ln_forward.argtypes = [dp] * 4 + [cl, cl, ctypes.c_double] + [dp] * 4
+        L.orc_ln_backward.argtypes = [dp] * 5 + [cl, cl, ctypes.c_double] + [dp] * 3
+        for name in ("orc_ln_forward", "orc_ln_backward", "orc_forward", "orc_backward", "orc_forward_rows_bf16",
                      "orc_backward_rows_bf16", "orc_backward_cols_bf16", "orc_db2_bf16",
                      "orc_num_threads"):
             getattr(L, name).restype = ctypes.c_int
@@ -132,6 +134,31 @@ class Oracle:
                                              _dp(db1)), "backward_cols")
         return dA, dB, db1
 
+    def ln_forward(self, a, r, gamma, beta, eps: float = 1e-5):
+        """X, s, mean, rstd of the residual add + LayerNorm (float64 numpy)."""
+        a, r, gamma, beta = (_f64(v) for v in (a, r, gamma, beta))
+        T, h = a.shape
+        X = np.zeros((T, h))
+        s = np.zeros((T, h))
+        mean = np.zeros(T)
+        rstd = np.zeros(T)
+        _check(self.L.orc_ln_forward(_dp(a), _dp(r), _dp(gamma), _dp(beta), T, h, eps, _dp(X),
+                                     _dp(s), _dp(mean), _dp(rstd)), "ln_forward")
+        return X, s, mean, rstd
+
+    def ln_backward(self, dX, dres, a, r, gamma, eps: float = 1e-5):
+        """ds, dgamma, dbeta of the residual add + LayerNorm (dres may be None)."""
+        dX, a, r, gamma = (_f64(v) for v in (dX, a, r, gamma))
+        T, h = a.shape
+        dr = None if dres is None else _f64(dres)
+        ds = np.zeros((T, h))
+        dg = np.zeros(h)
+        db = np.zeros(h)
+        _check(self.L.orc_ln_backward(_dp(dX), None if dr is None else _dp(dr), _dp(a), _dp(r),
+                                      _dp(gamma), T, h, eps, _dp(ds), _dp(dg), _dp(db)),
+               "ln_backward")
+        return ds, dg, db
+
     def db2(self, dY) -> np.ndarray:
         """Column sums of dY from a bf16 CPU tensor."""
         T, h = dY.shape
@@ -212,6 +239,14 @@ def backward_cols(*a, **k):
 
 def db2(dY):
     return default().db2(dY)
+
+
+def ln_forward(*a, **k):
+    return default().ln_forward(*a, **k)
+
+
+def ln_backward(*a, **k):
+    return default().ln_backward(*a, **k)
 
 
 def num_threads() -> int:

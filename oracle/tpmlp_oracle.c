@@ -413,3 +413,95 @@ int orc_num_threads(void) {
     return 1;
 #endif
 }
+
+/* ---------------------------------------------------------------------- */
+/* Residual add + LayerNorm feeding the block's input X.                   */
+/*                                                                         */
+/* "Megatron-DeepSpeed to ZeRO-3" (seekfood.cn), section 4.3, gives only   */
+/* the signature of a fused LayerNorm + residual kernel (output, input,    */
+/* residual, gamma, beta, n); "Megatron-LM: Tensor Model Parallel",        */
+/* Figure 2, places layer normalization and the residual connection around */
+/* the MLP.  Reading: per row of n = h values                              */
+/*   s = input + residual                (the residual stream)            */
+/*   mu = mean(s), var = mean((s - mu)^2)  (biased), rstd = 1/sqrt(var+eps)*/
+/*   X = (s - mu) * rstd * gamma + beta  (the MLP's input)                */
+/* and the backward pass of the same formula, where ds also receives      */
+/* dres, the gradient reaching s directly (the MLP's residual path):      */
+/*   xhat = (s - mu) rstd ; g = dX * gamma                                */
+/*   ds = rstd (g - mean(g) - xhat mean(g xhat)) + dres                   */
+/*   dgamma = sum_rows dX xhat ; dbeta = sum_rows dX ; dinput = dres_in = ds */
+/* ---------------------------------------------------------------------- */
+
+int orc_ln_forward(const double* a, const double* r, const double* gamma, const double* beta,
+                   long T, long h, double eps, double* X, double* s, double* mean, double* rstd) {
+    if (T < 0 || h < 1) return ORC_ERR_SHAPE;
+#pragma omp parallel for schedule(static)
+    for (long i = 0; i < T; ++i) {
+        const double* ai = a + i * h;
+        const double* ri = r + i * h;
+        double* si = s + i * h;
+        double sum = 0.0;
+        for (long j = 0; j < h; ++j) {
+            si[j] = ai[j] + ri[j];
+            sum += si[j];
+        }
+        double mu = sum / (double)h;
+        double sq = 0.0;
+        for (long j = 0; j < h; ++j) sq += (si[j] - mu) * (si[j] - mu);
+        double rs = 1.0 / sqrt(sq / (double)h + eps);
+        for (long j = 0; j < h; ++j) X[i * h + j] = (si[j] - mu) * rs * gamma[j] + beta[j];
+        mean[i] = mu;
+        rstd[i] = rs;
+    }
+    return ORC_OK;
+}
+
+/* dres may be NULL (no residual-path gradient). */
+int orc_ln_backward(const double* dX, const double* dres, const double* a, const double* r,
+                    const double* gamma, long T, long h, double eps, double* ds,
+                    double* dgamma, double* dbeta) {
+    if (T < 0 || h < 1) return ORC_ERR_SHAPE;
+    double* xhat = (double*)malloc(sizeof(double) * (size_t)(T * h + 1));
+    if (!xhat) return ORC_ERR_ALLOC;
+#pragma omp parallel for schedule(static)
+    for (long i = 0; i < T; ++i) {
+        const double* ai = a + i * h;
+        const double* ri = r + i * h;
+        double sum = 0.0;
+        for (long j = 0; j < h; ++j) sum += ai[j] + ri[j];
+        double mu = sum / (double)h;
+        double sq = 0.0;
+        for (long j = 0; j < h; ++j) {
+            double c = ai[j] + ri[j] - mu;
+            sq += c * c;
+        }
+        double rs = 1.0 / sqrt(sq / (double)h + eps);
+        double mg = 0.0, mgx = 0.0;
+        for (long j = 0; j < h; ++j) {
+            double xh = (ai[j] + ri[j] - mu) * rs;
+            double g = dX[i * h + j] * gamma[j];
+            xhat[i * h + j] = xh;
+            mg += g;
+            mgx += g * xh;
+        }
+        mg /= (double)h;
+        mgx /= (double)h;
+        for (long j = 0; j < h; ++j) {
+            double g = dX[i * h + j] * gamma[j];
+            double v = rs * (g - mg - xhat[i * h + j] * mgx);
+            ds[i * h + j] = v + (dres ? dres[i * h + j] : 0.0);
+        }
+    }
+#pragma omp parallel for schedule(static)
+    for (long j = 0; j < h; ++j) {
+        double sg = 0.0, sb = 0.0;
+        for (long i = 0; i < T; ++i) {
+            sg += dX[i * h + j] * xhat[i * h + j];
+            sb += dX[i * h + j];
+        }
+        dgamma[j] = sg;
+        dbeta[j] = sb;
+    }
+    free(xhat);
+    return ORC_OK;
+}

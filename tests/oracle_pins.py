@@ -16,6 +16,10 @@ pinned by mathematics:
   then Row Parallel", Figure 3a; "f / g Operators", Figure 4).
 * Special cases: A = 0, B = 0, X = 0, linearity in residual and b2.
 * The sampled (bf16-input) entry points against the full computation.
+* Residual add + LayerNorm: row statistics against numpy's mean and biased
+  variance (mean 0, mean square var/(var+eps)), affinity in gamma/beta,
+  invariance to a per-row shift and (as eps -> 0) to scale, and every
+  gradient against central differences.
 
 Each check returns True/False so that ``test_oracle_pins.py`` can run the same
 list against deliberately mutated copies of the oracle and show that every
@@ -233,6 +237,72 @@ def pin_sampled_matches_full(o) -> bool:
             and _rel(d2, db2) < 1e-13)
 
 
+# ------------------------------------------------- residual add + LayerNorm
+
+def _ln_inputs(T, h, seed):
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal((T, h)) * 1.5 + 0.3, rng.standard_normal((T, h)),
+            1.0 + 0.2 * rng.standard_normal(h), 0.1 * rng.standard_normal(h))
+
+
+def pin_ln_normalizes(o) -> bool:
+    """gamma = 1, beta = 0: every row of X has mean 0 and mean square
+    var / (var + eps) with the biased variance of s = input + residual."""
+    a, r, _, _ = _ln_inputs(5, 24, 41)
+    eps = 0.37  # large, so that its placement shows
+    X, s, mean, rstd = o.ln_forward(a, r, np.ones(24), np.zeros(24), eps)
+    su = a + r
+    var = su.var(axis=1)  # numpy's biased variance: a library primitive
+    return (_rel(s, su) == 0.0 and float(np.max(np.abs(X.mean(axis=1)))) < 1e-14
+            and _rel((X * X).mean(axis=1), var / (var + eps)) < 1e-13
+            and _rel(mean, su.mean(axis=1)) < 1e-14)
+
+
+def pin_ln_affine_and_invariant(o) -> bool:
+    a, r, g, b = _ln_inputs(4, 16, 42)
+    X0, _, _, _ = o.ln_forward(a, r, np.ones(16), np.zeros(16))
+    X1, _, _, _ = o.ln_forward(a, r, g, b)
+    ok = _rel(X1, X0 * g + b) < 1e-14
+    shift = np.arange(4.0)[:, None] * 3.0  # a per-row constant moves mu, not X
+    X2, _, _, _ = o.ln_forward(a + shift, r, g, b)
+    ok &= _rel(X2, X1) < 1e-12
+    Xs, _, _, _ = o.ln_forward(7.0 * a, 7.0 * r, g, b, 1e-14)  # scale-free as eps -> 0
+    Xt, _, _, _ = o.ln_forward(a, r, g, b, 1e-14)
+    return bool(ok and _rel(Xs, Xt) < 1e-9)
+
+
+def pin_ln_gradients_fd(o) -> bool:
+    """ds, dgamma, dbeta against central differences of
+    L = <dX, X> + <dres, s>; d(input) = d(residual) = ds."""
+    T, h, eps = 3, 6, 1e-3
+    a, r, g, b = _ln_inputs(T, h, 43)
+    rng = np.random.default_rng(44)
+    dX, dres = rng.standard_normal((T, h)), rng.standard_normal((T, h))
+    p = dict(a=a, r=r, g=g, b=b)
+
+    def loss(q):
+        X, s, _, _ = o.ln_forward(q["a"], q["r"], q["g"], q["b"], eps)
+        return float(np.sum(dX * X) + np.sum(dres * s))
+
+    ds, dg, db = o.ln_backward(dX, dres, a, r, g, eps)
+    step = 1e-6
+    for key, an in (("a", ds), ("r", ds), ("g", dg), ("b", db)):
+        fd = np.zeros_like(p[key])
+        it = np.nditer(p[key], flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            q = {k: v.copy() for k, v in p.items()}
+            q[key][idx] += step
+            lp = loss(q)
+            q[key][idx] -= 2 * step
+            fd[idx] = (lp - loss(q)) / (2 * step)
+        if _rel(an, fd) > 1e-6:
+            return False
+    # without the residual-path gradient each row of ds sums to zero
+    ds0, _, _ = o.ln_backward(dX, None, a, r, g, eps)
+    return float(np.max(np.abs(ds0.sum(axis=1)))) < 1e-12
+
+
 ALL_PINS = [
     pin_gelu_identities,
     pin_gelu_asymptotes,
@@ -245,6 +315,9 @@ ALL_PINS = [
     pin_partition_invariant,
     pin_special_cases,
     pin_sampled_matches_full,
+    pin_ln_normalizes,
+    pin_ln_affine_and_invariant,
+    pin_ln_gradients_fd,
 ]
 
 

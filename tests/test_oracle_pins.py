@@ -47,6 +47,15 @@ MUTANTS = {
                                   "dzc[r * ncols + q] = g * orc_gelu(z);"),
     "cols_dB_wrong_row": ("sb += hc[r * ncols + q] * w16(dY[r * h + k]);",
                           "sb += hc[r * ncols + q] * w16(X[r * h + k]);"),
+    "ln_unbiased_variance": ("double rs = 1.0 / sqrt(sq / (double)h + eps);\n        for (long j = 0; j < h; ++j) X[",
+                             "double rs = 1.0 / sqrt(sq / (double)(h - 1) + eps);\n        for (long j = 0; j < h; ++j) X["),
+    "ln_eps_outside_sqrt": ("double rs = 1.0 / sqrt(sq / (double)h + eps);\n        for (long j = 0; j < h; ++j) X[",
+                            "double rs = 1.0 / (sqrt(sq / (double)h) + eps);\n        for (long j = 0; j < h; ++j) X["),
+    "ln_bwd_drops_xhat_term": ("double v = rs * (g - mg - xhat[i * h + j] * mgx);",
+                               "double v = rs * (g - mg);"),
+    "ln_dgamma_uses_gamma": ("sg += dX[i * h + j] * xhat[i * h + j];",
+                             "sg += dX[i * h + j] * gamma[j] * xhat[i * h + j];"),
+    "ln_ds_drops_dres": ("ds[i * h + j] = v + (dres ? dres[i * h + j] : 0.0);", "ds[i * h + j] = v;"),
     "db2_drops_last_row": ("for (long r = 0; r < T; ++r) s += w16(dY[r * h + n]);",
                            "for (long r = 0; r + 1 < T; ++r) s += w16(dY[r * h + n]);"),
 }
