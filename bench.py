@@ -54,6 +54,8 @@ def parse_args(argv=None):
     p.add_argument("--sweep", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--layernorm", action="store_true",
+                   help="time the residual add + LayerNorm kernels instead (GB/s)")
     p.add_argument("--pair-mode", type=int, default=None,
                    help="GEMM kernel: 0 single CTA, 1 auto (default), 2 CTA pairs")
     return p.parse_args(argv)
@@ -463,8 +465,64 @@ def run_ours(args, w):
     return 0
 
 
+def run_layernorm(args, w):
+    """Residual add + LayerNorm on the workload's activations [T, h]: HBM GB/s
+    of the forward and backward calls against the measured copy bandwidth."""
+    import torch
+
+    from tensor_transformer_mlp_forward_gb300 import binding
+
+    dev = torch.device("cuda", 0)
+    T, h = w.T, w.h
+    gen = torch.Generator(device=dev).manual_seed(w.seed)
+    bf = lambda *sh: torch.randn(*sh, generator=gen, device=dev).to(torch.bfloat16)  # noqa: E731
+    a, r, dX, dres = bf(T, h), bf(T, h), bf(T, h), bf(T, h)
+    gam, bet = bf(h), bf(h)
+    X, s = torch.empty_like(a), torch.empty_like(a)
+    ds = torch.empty_like(a)
+    mean = torch.empty(T, device=dev)
+    rstd = torch.empty(T, device=dev)
+    dg, db = torch.empty(h, device=dev), torch.empty(h, device=dev)
+    part = torch.empty(max(1, int(binding.lib().tp_ln_residual_backward_workspace_floats(T, h))),
+                       device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    fwd = lambda: binding.tp_ln_residual_forward(a, r, gam, bet, 1e-5, X=X, s=s, mean=mean, rstd=rstd)  # noqa: E731
+    bwd = lambda: binding.tp_ln_residual_backward(dX, dres, a, r, gam, mean, rstd, ds=ds,  # noqa: E731
+                                                  dgamma=dg, dbeta=db, partial=part)
+    out = {}
+    for name, fn, algo in (("forward", fwd, 8 * T * h), ("backward", bwd, 10 * T * h)):
+        for _ in range(args.warmup):
+            fn()
+        ts = []
+        for _ in range(args.steps):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        ms = statistics.mean(ts)
+        out[name] = {"ms": round(ms, 4), "algorithmic_bytes": algo,
+                     "gbs": round(algo / (ms / 1e3) / 1e9, 1)}
+    try:
+        peak = float(json.load(open(PEAKS_FILE))["hbm_gbs"])
+        src = "measured"
+    except Exception:
+        peak, src = 6800.0, "fallback"
+    for v in out.values():
+        v["frac_of_hbm"] = round(v["gbs"] / peak, 3)
+    print(json.dumps({"metric": "GB/s of residual add + LayerNorm (fwd, bwd) on 1 GB300",
+                      "unit": "GB/s", "config": {"workload": f"{w.name} activations (T={w.T}, h={w.h})"},
+                      "hbm_peak_gbs": peak, "peak_source": src, "steps": args.steps,
+                      "l2": "L2 flushed between timed calls", **out}))
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.layernorm:
+        return run_layernorm(args, workload(args))
     if args.impl == "reference":
         return run_reference(args)
     if args.sweep:

@@ -194,6 +194,44 @@ int tp_mlp_dB(const tpmlp_bf16* H, const tpmlp_bf16* dY, int T, int h, int F, in
               tpmlp_bf16* dB, void* stream);
 
 /* ---------------------------------------------------------------------- */
+/* Residual add + LayerNorm feeding the block's input X                    */
+/* ---------------------------------------------------------------------- */
+
+/* The step in front of the MLP: "Megatron-DeepSpeed to ZeRO-3"
+ * (seekfood.cn), section 4.3, names a fused LayerNorm + residual kernel
+ * (output, input, residual, gamma, beta, n); "Megatron-LM: Tensor Model
+ * Parallel", Figure 2, places layer normalization and the residual
+ * connection around the MLP.  Per row of h values:
+ *   s = a + r ; mu = mean(s) ; var = mean((s - mu)^2) (biased)
+ *   X = (s - mu) / sqrt(var + eps) * gamma + beta
+ * X feeds tp_mlp_forward and s is its `residual`.
+ * In:  a, r [T,h] (sublayer output and incoming residual stream), gamma,
+ *      beta [h] (bf16), eps > 0.
+ * Out: X [T,h]; s [T,h] (may be NULL: not written); mean, rstd [T] float32
+ *      (rstd = 1/sqrt(var+eps)), saved for the backward pass.
+ * Rules: T >= 0, h % 8 == 0, 8 <= h <= 49152 (a row is staged in shared
+ * memory). */
+int tp_ln_residual_forward(const tpmlp_bf16* a, const tpmlp_bf16* r, const tpmlp_bf16* gamma,
+                           const tpmlp_bf16* beta, int T, int h, float eps, tpmlp_bf16* X,
+                           tpmlp_bf16* s, float* mean, float* rstd, void* stream);
+
+/* Float32 elements of partial-sum scratch tp_ln_residual_backward needs. */
+size_t tp_ln_residual_backward_workspace_floats(int T, int h);
+
+/* Backward pass of tp_ln_residual_forward.  dres (may be NULL) is the
+ * gradient reaching s directly -- for the MLP block, its dY:
+ *   xhat = (s - mu) rstd ; g = dX * gamma
+ *   ds = rstd (g - mean(g) - xhat mean(g xhat)) + dres    (= da = dr)
+ *   dgamma = sum_rows dX xhat ; dbeta = sum_rows dX      (float32, deterministic)
+ * In:  dX, dres, a, r [T,h]; gamma [h]; mean, rstd [T] from the forward pass.
+ * Out: ds [T,h] (bf16), dgamma, dbeta [h] (float32).  `partial` holds
+ * tp_ln_residual_backward_workspace_floats(T,h) floats. */
+int tp_ln_residual_backward(const tpmlp_bf16* dX, const tpmlp_bf16* dres, const tpmlp_bf16* a,
+                            const tpmlp_bf16* r, const tpmlp_bf16* gamma, const float* mean,
+                            const float* rstd, int T, int h, tpmlp_bf16* ds, float* dgamma,
+                            float* dbeta, float* partial, void* stream);
+
+/* ---------------------------------------------------------------------- */
 /* Status                                                                  */
 /* ---------------------------------------------------------------------- */
 

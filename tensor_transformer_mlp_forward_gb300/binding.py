@@ -59,6 +59,9 @@ _SIGNATURES = {
     "tp_mlp_dx": ([_P] * 2 + [_I] * 4 + [_P] + [_P, _S, _P], _I),
     "tp_mlp_dA": ([_P] * 2 + [_I] * 4 + [_P] + [_P], _I),
     "tp_mlp_dB": ([_P] * 2 + [_I] * 4 + [_P] + [_P], _I),
+    "tp_ln_residual_forward": ([_P] * 4 + [_I, _I, ctypes.c_float] + [_P] * 4 + [_P], _I),
+    "tp_ln_residual_backward_workspace_floats": ([_I, _I], _S),
+    "tp_ln_residual_backward": ([_P] * 7 + [_I, _I] + [_P] * 4 + [_P], _I),
     "tpmlp_status_string": ([_I], ctypes.c_char_p),
     "tpmlp_last_cuda_error": ([], _I),
     "tpmlp_device_status": ([], _I),
@@ -298,6 +301,43 @@ def tp_mlp_dB(H, dY, t: int, dB=None, stream=None):
         _ptr(H, "H", (T, F)), _ptr(dY, "dY", (T, h)), T, h, F, t, _ptr(dB, "dB", (F, h)),
         _stream(stream)))
     return dB
+
+
+def tp_ln_residual_forward(a, r, gamma, beta, eps: float = 1e-5, X=None, s=None, mean=None,
+                           rstd=None, want_s: bool = True, stream=None):
+    """X, s, mean, rstd of s = a + r, X = LayerNorm(s) * gamma + beta."""
+    T, h = a.shape
+    X = _out(X, (T, h), a)
+    if want_s:
+        s = _out(s, (T, h), a)
+    mean = _out(mean, (T,), a, torch.float32)
+    rstd = _out(rstd, (T,), a, torch.float32)
+    _check("tp_ln_residual_forward", lib().tp_ln_residual_forward(
+        _ptr(a, "a", (T, h)), _ptr(r, "r", (T, h)), _ptr(gamma, "gamma", (h,)),
+        _ptr(beta, "beta", (h,)), T, h, eps, _ptr(X, "X", (T, h)),
+        _ptr(s, "s", (T, h)) if s is not None else None, _ptr(mean, "mean", (T,), torch.float32),
+        _ptr(rstd, "rstd", (T,), torch.float32), _stream(stream)))
+    return X, s, mean, rstd
+
+
+def tp_ln_residual_backward(dX, dres, a, r, gamma, mean, rstd, ds=None, dgamma=None, dbeta=None,
+                            partial=None, stream=None):
+    """ds (= d a = d r), dgamma, dbeta of the residual add + LayerNorm."""
+    T, h = a.shape
+    ds = _out(ds, (T, h), a)
+    dgamma = _out(dgamma, (h,), a, torch.float32)
+    dbeta = _out(dbeta, (h,), a, torch.float32)
+    if partial is None:
+        partial = torch.empty(max(1, int(lib().tp_ln_residual_backward_workspace_floats(T, h))),
+                              dtype=torch.float32, device=a.device)
+    _check("tp_ln_residual_backward", lib().tp_ln_residual_backward(
+        _ptr(dX, "dX", (T, h)), _ptr(dres, "dres", (T, h)) if dres is not None else None,
+        _ptr(a, "a", (T, h)), _ptr(r, "r", (T, h)), _ptr(gamma, "gamma", (h,)),
+        _ptr(mean, "mean", (T,), torch.float32), _ptr(rstd, "rstd", (T,), torch.float32), T, h,
+        _ptr(ds, "ds", (T, h)), _ptr(dgamma, "dgamma", (h,), torch.float32),
+        _ptr(dbeta, "dbeta", (h,), torch.float32), _ptr(partial, "partial", None, torch.float32),
+        _stream(stream)))
+    return ds, dgamma, dbeta
 
 
 def selftest_bounded_wait(timeout_us: int, stream=None) -> int:

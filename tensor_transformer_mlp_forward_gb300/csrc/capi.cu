@@ -898,6 +898,64 @@ TPMLP_API int tp_mlp_backward(const tpmlp_bf16* dY, const tpmlp_bf16* X, const t
     return dB_gemm(H, dY, T, h, F, t, dB, st, d);
 }
 
+// ----------------------------------------------- residual add + LayerNorm
+
+// LayerNorm rows are staged in shared memory as fp32.
+constexpr int kLnMaxHidden = 49152;
+
+static int check_ln(int T, int h, float eps) {
+    if (T < 0 || h < 8 || h % 8 != 0 || h > kLnMaxHidden || !(eps > 0.0f)) return TPMLP_ERR_SHAPE;
+    return TPMLP_OK;
+}
+
+TPMLP_API int tp_ln_residual_forward(const tpmlp_bf16* a, const tpmlp_bf16* r,
+                                     const tpmlp_bf16* gamma, const tpmlp_bf16* beta, int T, int h,
+                                     float eps, tpmlp_bf16* X, tpmlp_bf16* s, float* mean,
+                                     float* rstd, void* stream) {
+    TPMLP_PROLOGUE(check_ln(T, h, eps));
+    if (any_null(gamma, beta) || (T > 0 && any_null(a, r, X, mean, rstd))) return TPMLP_ERR_NULL;
+    if (!all_aligned(a, r, gamma, beta, X, s)) return TPMLP_ERR_ALIGN;
+    if (T == 0) return TPMLP_OK;
+    DeviceInfo d;
+    if (int rc = enter(d)) return rc;
+    cudaError_t e = launch_ln_forward(cb(a), cb(r), cb(gamma), cb(beta), T, h, eps,
+                                      reinterpret_cast<__nv_bfloat16*>(X),
+                                      reinterpret_cast<__nv_bfloat16*>(s), mean, rstd,
+                                      static_cast<cudaStream_t>(stream), &t_last_launches);
+    return e == cudaSuccess ? TPMLP_OK : fail_cuda(e);
+}
+
+TPMLP_API size_t tp_ln_residual_backward_workspace_floats(int T, int h) {
+    if (check_ln(T, h, 1.0f)) return 0;
+    return 2 * static_cast<size_t>(ln_param_chunks(T, h)) * static_cast<size_t>(h);
+}
+
+TPMLP_API int tp_ln_residual_backward(const tpmlp_bf16* dX, const tpmlp_bf16* dres,
+                                      const tpmlp_bf16* a, const tpmlp_bf16* r,
+                                      const tpmlp_bf16* gamma, const float* mean, const float* rstd,
+                                      int T, int h, tpmlp_bf16* ds, float* dgamma, float* dbeta,
+                                      float* partial, void* stream) {
+    TPMLP_PROLOGUE(check_ln(T, h, 1.0f));
+    if (any_null(gamma, dgamma, dbeta) ||
+        (T > 0 && any_null(dX, a, r, mean, rstd, ds, partial)))
+        return TPMLP_ERR_NULL;
+    if (!all_aligned(dX, dres, a, r, gamma, ds, dgamma, dbeta, partial)) return TPMLP_ERR_ALIGN;
+    DeviceInfo d;
+    if (int rc = enter(d)) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        cudaError_t e;
+        if ((e = cudaMemsetAsync(dgamma, 0, sizeof(float) * static_cast<size_t>(h), st)) != cudaSuccess ||
+            (e = cudaMemsetAsync(dbeta, 0, sizeof(float) * static_cast<size_t>(h), st)) != cudaSuccess)
+            return fail_cuda(e);
+        return TPMLP_OK;
+    }
+    cudaError_t e = launch_ln_backward(cb(dX), cb(dres), cb(a), cb(r), cb(gamma), mean, rstd, T, h,
+                                       reinterpret_cast<__nv_bfloat16*>(ds), dgamma, dbeta, partial,
+                                       st, &t_last_launches);
+    return e == cudaSuccess ? TPMLP_OK : fail_cuda(e);
+}
+
 TPMLP_API const char* tpmlp_status_string(int status) {
     switch (status) {
         case TPMLP_OK: return "ok";

@@ -36,6 +36,20 @@ cudaError_t launch_dx_partial(const GemmMaps& m, const GemmArgs& g, int grid, bo
 cudaError_t launch_weight_grad(const GemmMaps& m, const GemmArgs& g,
                                int grid, bool pair, cudaStream_t st);
 
+// Residual add + LayerNorm (layernorm.cu).  `launches` is incremented per
+// kernel launched.
+cudaError_t launch_ln_forward(const __nv_bfloat16* a, const __nv_bfloat16* r,
+                              const __nv_bfloat16* gamma, const __nv_bfloat16* beta, int T, int h,
+                              float eps, __nv_bfloat16* X, __nv_bfloat16* s, float* mean,
+                              float* rstd, cudaStream_t st, int* launches);
+cudaError_t launch_ln_backward(const __nv_bfloat16* dX, const __nv_bfloat16* dres,
+                               const __nv_bfloat16* a, const __nv_bfloat16* r,
+                               const __nv_bfloat16* gamma, const float* mean, const float* rstd,
+                               int T, int h, __nv_bfloat16* ds, float* dgamma, float* dbeta,
+                               float* partial, cudaStream_t st, int* launches);
+// Row chunks of the dgamma / dbeta partial sums (partial = 2 * chunks * h floats).
+int ln_param_chunks(int T, int h);
+
 // `grid` is the number of work units wanted (CTAs, or CTA pairs when PAIR);
 // it is clipped to what can be resident at once, so the persistent loop never
 // waits for a second wave of CTAs.
