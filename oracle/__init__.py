@@ -51,6 +51,15 @@ class Oracle:
         L.orc_db2_bf16.argtypes = [up, cl, cl, dp]
         L.orc_ln_forward.argtypes = [dp] * 4 + [cl, cl, ctypes.c_double] + [dp] * 4
         L.orc_ln_backward.argtypes = [dp] * 5 + [cl, cl, ctypes.c_double] + [dp] * 3
+        u32p = ctypes.POINTER(ctypes.c_uint32)
+        u64 = ctypes.c_uint64
+        L.orc_philox4x32_10.argtypes = [u32p, u32p, u32p]
+        L.orc_philox4x32_10.restype = None
+        L.orc_dropout_mask.argtypes = [u64, u64, cl, ctypes.c_double, ctypes.POINTER(ctypes.c_uint8)]
+        L.orc_forward_dropout.argtypes = [dp] * 6 + [cl] * 4 + [ctypes.c_double, u64, u64] + [dp] * 3
+        L.orc_backward_dropout.argtypes = [dp] * 5 + [cl] * 4 + [ctypes.c_double, u64, u64] + [dp] * 5
+        for name in ("orc_dropout_mask", "orc_forward_dropout", "orc_backward_dropout"):
+            getattr(L, name).restype = ctypes.c_int
         for name in ("orc_ln_forward", "orc_ln_backward", "orc_forward", "orc_backward", "orc_forward_rows_bf16",
                      "orc_backward_rows_bf16", "orc_backward_cols_bf16", "orc_db2_bf16",
                      "orc_num_threads"):
@@ -159,6 +168,41 @@ class Oracle:
                "ln_backward")
         return ds, dg, db
 
+    def philox4x32_10(self, counter, key):
+        c = (ctypes.c_uint32 * 4)(*counter)
+        k = (ctypes.c_uint32 * 2)(*key)
+        out = (ctypes.c_uint32 * 4)()
+        self.L.orc_philox4x32_10(c, k, out)
+        return list(out)
+
+    def dropout_mask(self, seed: int, offset: int, n: int, p: float) -> np.ndarray:
+        keep = np.zeros(max(n, 1), dtype=np.uint8)
+        _check(self.L.orc_dropout_mask(seed, offset, n, p,
+                                       keep.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8))),
+               "dropout_mask")
+        return keep[:n]
+
+    def forward_dropout(self, X, A, b1, B, b2, R, t: int, p: float, seed: int, offset: int = 0):
+        X, A, b1, B, b2, R = (_f64(v) for v in (X, A, b1, B, b2, R))
+        T, h = X.shape
+        F = A.shape[1]
+        Y, Z, H = np.zeros((T, h)), np.zeros((T, F)), np.zeros((T, F))
+        _check(self.L.orc_forward_dropout(_dp(X), _dp(A), _dp(b1), _dp(B), _dp(b2), _dp(R), T, h,
+                                          F, t, p, seed, offset, _dp(Y), _dp(Z), _dp(H)),
+               "forward_dropout")
+        return Y, Z, H
+
+    def backward_dropout(self, dY, X, A, b1, B, t: int, p: float, seed: int, offset: int = 0):
+        dY, X, A, b1, B = (_f64(v) for v in (dY, X, A, b1, B))
+        T, h = X.shape
+        F = A.shape[1]
+        dX, dA, dB = np.zeros((T, h)), np.zeros((h, F)), np.zeros((F, h))
+        db1, db2 = np.zeros(F), np.zeros(h)
+        _check(self.L.orc_backward_dropout(_dp(dY), _dp(X), _dp(A), _dp(b1), _dp(B), T, h, F, t, p,
+                                           seed, offset, _dp(dX), _dp(dA), _dp(dB), _dp(db1),
+                                           _dp(db2)), "backward_dropout")
+        return dX, dA, dB, db1, db2
+
     def db2(self, dY) -> np.ndarray:
         """Column sums of dY from a bf16 CPU tensor."""
         T, h = dY.shape
@@ -239,6 +283,22 @@ def backward_cols(*a, **k):
 
 def db2(dY):
     return default().db2(dY)
+
+
+def philox4x32_10(counter, key):
+    return default().philox4x32_10(counter, key)
+
+
+def dropout_mask(*a, **k):
+    return default().dropout_mask(*a, **k)
+
+
+def forward_dropout(*a, **k):
+    return default().forward_dropout(*a, **k)
+
+
+def backward_dropout(*a, **k):
+    return default().backward_dropout(*a, **k)
 
 
 def ln_forward(*a, **k):

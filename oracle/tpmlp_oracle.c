@@ -505,3 +505,100 @@ int orc_ln_backward(const double* dX, const double* dres, const double* a, const
     free(xhat);
     return ORC_OK;
 }
+
+/* ---------------------------------------------------------------------- */
+/* Dropout before the residual add ("bias-dropout-add").                   */
+/*                                                                         */
+/* "Megatron-LM: Tensor Model Parallel", section "Hybrid MP + DP" (the     */
+/* random-number paragraph): the dropout in front of the residual lies     */
+/* outside the model-parallel region and uses the same pattern on every    */
+/* TP rank; the training-recipe table sets dropout 0.1.  Reading:          */
+/*   Y = R + keep * (sum_i H_i B_i + b2) / (1 - p)                         */
+/* with keep(e) for element e = row * h + col decided by a counter-based    */
+/* generator shared by every shard: Philox4x32 with 10 rounds (Salmon et   */
+/* al., "Parallel Random Numbers: As Easy as 1, 2, 3", SC'11).  Counter    */
+/* g = offset + e: word g % 4 of Philox(counter = (lo g/4, hi g/4, 0, 0),   */
+/* key = (lo seed, hi seed)); keep iff word >= floor(p * 2^32).            */
+/* ---------------------------------------------------------------------- */
+
+/* One Philox4x32-10 block: 10 rounds of the multiply-hi/lo bijection with
+ * multipliers 0xD2511F53 (word 0) and 0xCD9E8D57 (word 2), the key bumped by
+ * the Weyl constants 0x9E3779B9, 0xBB67AE85 between rounds. */
+void orc_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4]) {
+    uint32_t c[4] = {ctr_in[0], ctr_in[1], ctr_in[2], ctr_in[3]};
+    uint32_t k0 = key_in[0], k1 = key_in[1];
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        uint64_t p0 = (uint64_t)0xD2511F53u * c[0];
+        uint64_t p1 = (uint64_t)0xCD9E8D57u * c[2];
+        uint32_t n0 = (uint32_t)(p1 >> 32) ^ c[1] ^ k0;
+        uint32_t n1 = (uint32_t)p1;
+        uint32_t n2 = (uint32_t)(p0 >> 32) ^ c[3] ^ k1;
+        uint32_t n3 = (uint32_t)p0;
+        c[0] = n0; c[1] = n1; c[2] = n2; c[3] = n3;
+    }
+    out[0] = c[0]; out[1] = c[1]; out[2] = c[2]; out[3] = c[3];
+}
+
+/* keep[e] for the n elements e = 0 .. n-1 (1 = kept). */
+int orc_dropout_mask(uint64_t seed, uint64_t offset, long n, double p, uint8_t* keep) {
+    if (n < 0 || !(p >= 0.0 && p < 1.0)) return ORC_ERR_SHAPE;
+    uint32_t thr = (uint32_t)(p * 4294967296.0);
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+#pragma omp parallel for schedule(static)
+    for (long e = 0; e < n; ++e) {
+        uint64_t g = offset + (uint64_t)e;
+        uint64_t blk = g >> 2;
+        uint32_t ctr[4] = {(uint32_t)blk, (uint32_t)(blk >> 32), 0u, 0u};
+        uint32_t w[4];
+        orc_philox4x32_10(ctr, key, w);
+        keep[e] = w[g & 3] >= thr ? 1 : 0;
+    }
+    return ORC_OK;
+}
+
+/* Forward with dropout: Y = R + keep * (sum_i H_i B_i + b2) / (1 - p). */
+int orc_forward_dropout(const double* X, const double* A, const double* b1, const double* B,
+                        const double* b2, const double* R, long T, long h, long F, long t,
+                        double p, uint64_t seed, uint64_t offset, double* Y, double* Z,
+                        double* H) {
+    if (bad_shape(T, h, F, t)) return ORC_ERR_SHAPE;
+    double* zero = (double*)calloc((size_t)(T * h + 1), sizeof(double));
+    uint8_t* keep = (uint8_t*)malloc((size_t)(T * h + 1));
+    if (!zero || !keep) {
+        free(zero); free(keep);
+        return ORC_ERR_ALLOC;
+    }
+    /* the MLP's output before the residual: sum_i H_i B_i + b2 */
+    int rc = orc_forward(X, A, b1, B, b2, zero, T, h, F, t, Y, Z, H);
+    if (rc == ORC_OK) rc = orc_dropout_mask(seed, offset, T * h, p, keep);
+    if (rc == ORC_OK)
+        for (long e = 0; e < T * h; ++e) Y[e] = R[e] + (keep[e] ? Y[e] / (1.0 - p) : 0.0);
+    free(zero); free(keep);
+    return rc;
+}
+
+/* Backward with dropout: the MLP sees dP = keep * dY / (1 - p) (the residual
+ * still receives dY).  Outputs as orc_backward. */
+int orc_backward_dropout(const double* dY, const double* X, const double* A, const double* b1,
+                         const double* B, long T, long h, long F, long t, double p, uint64_t seed,
+                         uint64_t offset, double* dX, double* dA, double* dB, double* db1,
+                         double* db2) {
+    if (bad_shape(T, h, F, t)) return ORC_ERR_SHAPE;
+    double* dP = (double*)malloc(sizeof(double) * (size_t)(T * h + 1));
+    uint8_t* keep = (uint8_t*)malloc((size_t)(T * h + 1));
+    if (!dP || !keep) {
+        free(dP); free(keep);
+        return ORC_ERR_ALLOC;
+    }
+    int rc = orc_dropout_mask(seed, offset, T * h, p, keep);
+    if (rc == ORC_OK) {
+        for (long e = 0; e < T * h; ++e) dP[e] = keep[e] ? dY[e] / (1.0 - p) : 0.0;
+        rc = orc_backward(dP, X, A, b1, B, T, h, F, t, dX, dA, dB, db1, db2);
+    }
+    free(dP); free(keep);
+    return rc;
+}

@@ -20,6 +20,9 @@ pinned by mathematics:
   variance (mean 0, mean square var/(var+eps)), affinity in gamma/beta,
   invariance to a per-row shift and (as eps -> 0) to scale, and every
   gradient against central differences.
+* Dropout: the published Philox4x32-10 known-answer vectors, drop rates
+  within binomial bounds, the counter/seed semantics, p = 0 equal to the
+  plain block, and the gradients against central differences.
 
 Each check returns True/False so that ``test_oracle_pins.py`` can run the same
 list against deliberately mutated copies of the oracle and show that every
@@ -303,6 +306,81 @@ def pin_ln_gradients_fd(o) -> bool:
     return float(np.max(np.abs(ds0.sum(axis=1)))) < 1e-12
 
 
+# -------------------------------------------------------------- dropout
+
+def pin_philox_known_answers(o) -> bool:
+    """The published Philox4x32-10 known-answer vectors
+    (tests/golden/philox4x32_10_kat.txt)."""
+    import os
+
+    path = os.path.join(os.path.dirname(__file__), "golden", "philox4x32_10_kat.txt")
+    n = 0
+    for line in open(path):
+        if not line.strip() or line.startswith("#"):
+            continue
+        words = [int(x, 16) for x in line.split()]
+        if o.philox4x32_10(words[0:4], words[4:6]) != words[6:10]:
+            return False
+        n += 1
+    return n == 3
+
+
+def pin_dropout_mask(o) -> bool:
+    n = 200000
+    ok = True
+    for p in (0.1, 0.5):
+        keep = o.dropout_mask(99, 7, n, p)
+        drop = 1.0 - keep.mean()
+        ok &= abs(drop - p) < 6.0 * math.sqrt(p * (1 - p) / n)
+    ok &= bool(o.dropout_mask(99, 7, 1000, 0.0).all())
+    # seed 0, offset 0: element e reads word e of the first known-answer
+    # block (6627e8d5 e169c58d bc57ac4c 9b00dbd8); at p = 1/2 the first is
+    # below 2^31 (dropped), the other three above (kept)
+    ok &= o.dropout_mask(0, 0, 4, 0.5).tolist() == [0, 1, 1, 1]
+    a = o.dropout_mask(99, 0, 4096, 0.5)
+    ok &= bool((a[5:] == o.dropout_mask(99, 5, 4091, 0.5)).all())  # the counter is offset + e
+    ok &= bool((a != o.dropout_mask(100, 0, 4096, 0.5)).any())      # the seed matters
+    return bool(ok)
+
+
+def pin_dropout_forward(o) -> bool:
+    T, h, F, t, p = 6, 16, 32, 2, 0.25
+    q = _rand_block(T, h, F, 51)
+    Y0, _, _ = o.forward(q["X"], q["A"], q["b1"], q["B"], q["b2"], q["R"], t)
+    Yp0, _, _ = o.forward_dropout(q["X"], q["A"], q["b1"], q["B"], q["b2"], q["R"], t, 0.0, 5)
+    Yd, _, _ = o.forward_dropout(q["X"], q["A"], q["b1"], q["B"], q["b2"], q["R"], t, p, 5, 3)
+    keep = o.dropout_mask(5, 3, T * h, p).reshape(T, h)
+    expect = q["R"] + keep * (Y0 - q["R"]) / (1.0 - p)
+    return _rel(Yp0, Y0) < 1e-13 and _rel(Yd, expect) < 1e-12
+
+
+def pin_dropout_backward_fd(o) -> bool:
+    """Gradients with dropout against central differences of <dY, Y>; the
+    mask depends only on (seed, offset, position), so it stays fixed."""
+    T, h, F, t, p = 3, 4, 8, 2, 0.3
+    q = _rand_block(T, h, F, 52, scale_w=0.5)
+
+    def loss(v):
+        Y, _, _ = o.forward_dropout(v["X"], v["A"], v["b1"], v["B"], v["b2"], v["R"], t, p, 11)
+        return float(np.sum(q["dY"] * Y))
+
+    grads = o.backward_dropout(q["dY"], q["X"], q["A"], q["b1"], q["B"], t, p, 11)
+    eps = 1e-6
+    for key, an in zip(("X", "A", "B", "b1", "b2"), grads):
+        fd = np.zeros_like(q[key])
+        it = np.nditer(q[key], flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            v = {k: w.copy() for k, w in q.items()}
+            v[key][idx] += eps
+            lp = loss(v)
+            v[key][idx] -= 2 * eps
+            fd[idx] = (lp - loss(v)) / (2 * eps)
+        if _rel(an, fd) > 1e-6:
+            return False
+    return True
+
+
 ALL_PINS = [
     pin_gelu_identities,
     pin_gelu_asymptotes,
@@ -318,6 +396,10 @@ ALL_PINS = [
     pin_ln_normalizes,
     pin_ln_affine_and_invariant,
     pin_ln_gradients_fd,
+    pin_philox_known_answers,
+    pin_dropout_mask,
+    pin_dropout_forward,
+    pin_dropout_backward_fd,
 ]
 
 

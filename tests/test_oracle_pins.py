@@ -56,6 +56,11 @@ MUTANTS = {
     "ln_dgamma_uses_gamma": ("sg += dX[i * h + j] * xhat[i * h + j];",
                              "sg += dX[i * h + j] * gamma[j] * xhat[i * h + j];"),
     "ln_ds_drops_dres": ("ds[i * h + j] = v + (dres ? dres[i * h + j] : 0.0);", "ds[i * h + j] = v;"),
+    "philox_multiplier": ("uint64_t p0 = (uint64_t)0xD2511F53u * c[0];", "uint64_t p0 = (uint64_t)0xD2511F55u * c[0];"),
+    "philox_no_key_bump": ("k1 += 0xBB67AE85u;", "k1 += 0u;"),
+    "dropout_no_rescale": ("Y[e] = R[e] + (keep[e] ? Y[e] / (1.0 - p) : 0.0);", "Y[e] = R[e] + (keep[e] ? Y[e] : 0.0);"),
+    "dropout_bwd_ignores_mask": ("dP[e] = keep[e] ? dY[e] / (1.0 - p) : 0.0;", "dP[e] = dY[e] / (1.0 - p);"),
+    "dropout_counter_word": ("keep[e] = w[g & 3] >= thr ? 1 : 0;", "keep[e] = w[0] >= thr ? 1 : 0;"),
     "db2_drops_last_row": ("for (long r = 0; r < T; ++r) s += w16(dY[r * h + n]);",
                            "for (long r = 0; r + 1 < T; ++r) s += w16(dY[r * h + n]);"),
 }
