@@ -52,6 +52,8 @@ def parse_args(argv=None):
     p.add_argument("--tokens", type=int, default=None)
     p.add_argument("--shards", type=int, default=None)
     p.add_argument("--sweep", action="store_true")
+    p.add_argument("--dropout", type=float, default=0.0,
+                   help="dropout rate before the residual add (0: the block without dropout)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--layernorm", action="store_true",
@@ -208,7 +210,7 @@ GEMM_CALLS = ("column_gelu", "row_sum", "dx", "dA", "dB")  # one kernel each
 class Step:
     """All buffers of one replica, resident in HBM; run() issues one step."""
 
-    def __init__(self, w, device):
+    def __init__(self, w, device, p_drop=0.0, seed=0x5EED):
         import torch
 
         from tensor_transformer_mlp_forward_gb300 import binding, inputs
@@ -226,20 +228,39 @@ class Step:
         self.p_db2 = e(max(1, int(binding.lib().tp_mlp_bias_grad_workspace_floats(T, h))), dt=torch.float32)
         self.ws_split = e(max(16, binding.split_workspace_bytes(T, h, F, w.t)), dt=torch.uint8)
         self.launches = 0
+        # dropout before the residual add: a fresh pattern every step (the
+        # element counter advances by T*h, rounded up to a Philox block)
+        self.p_drop, self.seed, self.offset = p_drop, seed, 0
+        self.dP = e(T, h) if p_drop > 0 else None
+        self.names = STEP_CALLS if p_drop <= 0 else (
+            "column_gelu", "row_sum", "dropout_grad", "db2", "dgelu", "dx", "dA", "dB")
 
     def run(self, events=None):
         """One fwd+bwd step; if `events` (len 8) is given, records them
         between the calls on the current stream."""
         b, i, t = self.b, self.inp, self.w.t
-        calls = (
-            lambda: b.tp_mlp_column_gelu(i["X"], i["A"], i["b1"], t, Z=self.Z, H=self.H),
-            lambda: b.tp_mlp_row_sum(self.H, i["B"], i["b2"], i["residual"], t, Y=self.Y,
-                                     workspace=self.ws_split),
-            lambda: b.tp_mlp_bias_grad(i["dY"], db=self.db2, partial=self.p_db2),
-            lambda: b.tp_mlp_dgelu(i["dY"], i["B"], self.Z, t, dZ=self.dZ, db1=self.db1, partial=self.p_db1),
+        if self.p_drop <= 0:
+            dP = i["dY"]
+            calls = (
+                lambda: b.tp_mlp_column_gelu(i["X"], i["A"], i["b1"], t, Z=self.Z, H=self.H),
+                lambda: b.tp_mlp_row_sum(self.H, i["B"], i["b2"], i["residual"], t, Y=self.Y,
+                                         workspace=self.ws_split),
+            )
+        else:
+            dP, p, sd, off = self.dP, self.p_drop, self.seed, self.offset
+            self.offset += (self.w.T * self.w.h + 3) // 4 * 4
+            calls = (
+                lambda: b.tp_mlp_column_gelu(i["X"], i["A"], i["b1"], t, Z=self.Z, H=self.H),
+                lambda: b.tp_mlp_row_sum_dropout(self.H, i["B"], i["b2"], i["residual"], t, p, sd,
+                                                 off, Y=self.Y, workspace=self.ws_split),
+                lambda: b.tp_mlp_dropout_grad(i["dY"], p, sd, off, dP=dP),
+            )
+        calls = calls + (
+            lambda: b.tp_mlp_bias_grad(dP, db=self.db2, partial=self.p_db2),
+            lambda: b.tp_mlp_dgelu(dP, i["B"], self.Z, t, dZ=self.dZ, db1=self.db1, partial=self.p_db1),
             lambda: b.tp_mlp_dx(self.dZ, i["A"], t, dX=self.dX, workspace=self.ws_split),
             lambda: b.tp_mlp_dA(i["X"], self.dZ, t, dA=self.dA),
-            lambda: b.tp_mlp_dB(self.H, i["dY"], t, dB=self.dB),
+            lambda: b.tp_mlp_dB(self.H, dP, t, dB=self.dB),
         )
         if events is not None:
             events[0].record()
@@ -287,19 +308,19 @@ def barrier():
         dist.barrier()
 
 
-def time_ours(w, steps, warmup, local):
+def time_ours(w, steps, warmup, local, p_drop=0.0):
     import torch
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    step = Step(w, dev)
+    step = Step(w, dev, p_drop)
     for _ in range(warmup):
         step.run()
     torch.cuda.synchronize()
     assert step.b.device_status() == 0, "device wait timed out during warm-up"
     step.launches = 0
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STEP_CALLS) + 1)] for _ in range(steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(step.names) + 1)] for _ in range(steps)]
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     barrier()
     torch.cuda.synchronize()
@@ -317,7 +338,7 @@ def time_ours(w, steps, warmup, local):
     launches = step.launches
     dev_ms = sum(evs[k][0].elapsed_time(evs[k][-1]) for k in range(steps))
     per_call = {name: [evs[k][j].elapsed_time(evs[k][j + 1]) for k in range(steps)]
-                for j, name in enumerate(STEP_CALLS)}
+                for j, name in enumerate(step.names)}
     return step, dev_ms / 1e3, wall, per_call, clocks.summary(), launches
 
 
@@ -420,7 +441,8 @@ def run_ours(args, w):
     if args.pair_mode is not None:
         binding.set_cta_pair_mode(args.pair_mode)
     rank, world, local = init_distributed(args.gpus)
-    step, dev_s, wall, per_call, clocks, launches = time_ours(w, args.steps, args.warmup, local)
+    step, dev_s, wall, per_call, clocks, launches = time_ours(w, args.steps, args.warmup, local,
+                                                              args.dropout)
     flops = w.flops_fwd_bwd()
     max_s, units = reduce_max_sum(dev_s, flops * args.steps)
     value = units / max_s / 1e12
@@ -448,7 +470,7 @@ def run_ours(args, w):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * max_s / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": describe(w, world),
+        "config": dict(describe(w, world), **({"dropout": args.dropout} if args.dropout > 0 else {})),
         "pct_of_peak": {"burst": 100 * value / world / burst, "sustained": 100 * value / world / sustained,
                         "source": src},
         "per_call_ms": {k: round(v, 4) for k, v in avg_ms.items()},

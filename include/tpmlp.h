@@ -232,6 +232,64 @@ int tp_ln_residual_backward(const tpmlp_bf16* dX, const tpmlp_bf16* dres, const 
                             float* dbeta, float* partial, void* stream);
 
 /* ---------------------------------------------------------------------- */
+/* Dropout before the residual add                                         */
+/* ---------------------------------------------------------------------- */
+
+/* "Megatron-LM: Tensor Model Parallel", Figure 2 places dropout between the
+ * MLP's output and the residual add, and its training-recipe table (row
+ * "Stabilization") gives the rate 0.1.  The same page (section "Hybrid
+ * MP + DP", the paragraph on random numbers) puts this dropout outside the
+ * model-parallel region: every shard of a model instance must draw the same
+ * pattern.  Here the pattern is a pure function of (seed, element), so it
+ * cannot depend on the shard count or the GPU's schedule:
+ *   g    = offset + row * h + col            (element counter)
+ *   w    = Philox4x32-10(counter = (g/4 mod 2^32, g/4 >> 32, 0, 0),
+ *                        key = (seed mod 2^32, seed >> 32))[g mod 4]
+ *   keep = w >= floor(p * 2^32)              (exact integer comparison)
+ *   Y    = residual + keep * (sum_i H_i B_i + b2) / (1 - p)
+ * (Philox4x32 with 10 rounds: Salmon, Moraes, Dror, Shaw, "Parallel Random
+ * Numbers: As Easy as 1, 2, 3", SC'11.)  Rules beyond the block's: p is a
+ * double in [0, 1) -- p = 0 gives tp_mlp_forward's result exactly -- and
+ * offset is a multiple of 4 (a Philox block holds four element counters);
+ * otherwise TPMLP_ERR_SHAPE.  A caller advances offset by T*h (rounded up to
+ * a multiple of 4) per call to draw a fresh pattern with the same seed. */
+
+/* a3 with bias-dropout-add in its epilogue (and in the split reduction when
+ * the GEMM splits).  Arguments as tp_mlp_row_sum plus p, seed, offset. */
+int tp_mlp_row_sum_dropout(const tpmlp_bf16* H, const tpmlp_bf16* B, const tpmlp_bf16* b2,
+                           const tpmlp_bf16* residual, int T, int h, int F, int t, double p,
+                           uint64_t seed, uint64_t offset, tpmlp_bf16* Y, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/* tp_mlp_forward with the dropout above: a2, then tp_mlp_row_sum_dropout.
+ * Workspace as tp_mlp_forward's. */
+int tp_mlp_forward_dropout(const tpmlp_bf16* X, const tpmlp_bf16* A, const tpmlp_bf16* b1,
+                           const tpmlp_bf16* B, const tpmlp_bf16* b2, const tpmlp_bf16* residual,
+                           int T, int h, int F, int t, double p, uint64_t seed, uint64_t offset,
+                           tpmlp_bf16* Y, tpmlp_bf16* Z, tpmlp_bf16* H, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/* The gradient the dropout passes to the MLP's output:
+ * dP = keep * dY / (1 - p), bf16, keep drawn as above from (seed, offset).
+ * dY, dP [T,h]; rules T >= 0, h % 8 == 0, h >= 8. */
+int tp_mlp_dropout_grad(const tpmlp_bf16* dY, int T, int h, double p, uint64_t seed,
+                        uint64_t offset, tpmlp_bf16* dP, void* stream);
+
+/* Bytes of scratch tp_mlp_backward_dropout needs: tp_mlp_backward's plus
+ * the bf16 dP [T,h]. */
+size_t tp_mlp_backward_dropout_workspace_bytes(int T, int h, int F, int t);
+
+/* Backward pass of tp_mlp_forward_dropout: tp_mlp_dropout_grad into the
+ * workspace, then tp_mlp_backward's steps a4..a9 on dP (so db2 = sum_rows dP
+ * and dB_i = H_i^T dP).  The residual's gradient is dY itself, not written.
+ * Arguments as tp_mlp_backward plus p, seed, offset (the forward pass's). */
+int tp_mlp_backward_dropout(const tpmlp_bf16* dY, const tpmlp_bf16* X, const tpmlp_bf16* A,
+                            const tpmlp_bf16* B, const tpmlp_bf16* Z, const tpmlp_bf16* H, int T,
+                            int h, int F, int t, double p, uint64_t seed, uint64_t offset,
+                            tpmlp_bf16* dX, tpmlp_bf16* dA, tpmlp_bf16* dB, float* db1,
+                            float* db2, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------- */
 /* Status                                                                  */
 /* ---------------------------------------------------------------------- */
 

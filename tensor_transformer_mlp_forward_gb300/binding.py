@@ -41,6 +41,8 @@ _lib = None
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _S = ctypes.c_size_t
+_D = ctypes.c_double
+_U64 = ctypes.c_uint64
 
 _SIGNATURES = {
     "tp_mlp_split_workspace_bytes": ([_I] * 4, _S),
@@ -59,6 +61,13 @@ _SIGNATURES = {
     "tp_mlp_dx": ([_P] * 2 + [_I] * 4 + [_P] + [_P, _S, _P], _I),
     "tp_mlp_dA": ([_P] * 2 + [_I] * 4 + [_P] + [_P], _I),
     "tp_mlp_dB": ([_P] * 2 + [_I] * 4 + [_P] + [_P], _I),
+    "tp_mlp_row_sum_dropout": ([_P] * 4 + [_I] * 4 + [_D, _U64, _U64] + [_P] + [_P, _S, _P], _I),
+    "tp_mlp_forward_dropout": ([_P] * 6 + [_I] * 4 + [_D, _U64, _U64] + [_P] * 3 + [_P, _S, _P],
+                               _I),
+    "tp_mlp_dropout_grad": ([_P, _I, _I, _D, _U64, _U64, _P, _P], _I),
+    "tp_mlp_backward_dropout_workspace_bytes": ([_I] * 4, _S),
+    "tp_mlp_backward_dropout": ([_P] * 6 + [_I] * 4 + [_D, _U64, _U64] + [_P] * 6 + [_S, _P],
+                                _I),
     "tp_ln_residual_forward": ([_P] * 4 + [_I, _I, ctypes.c_float] + [_P] * 4 + [_P], _I),
     "tp_ln_residual_backward_workspace_floats": ([_I, _I], _S),
     "tp_ln_residual_backward": ([_P] * 7 + [_I, _I] + [_P] * 4 + [_P], _I),
@@ -228,6 +237,74 @@ def tp_mlp_backward(dY, X, A, B, Z, H, t: int, dX=None, dA=None, dB=None, db1=No
         _ptr(dY, "dY", (T, h)), _ptr(X, "X", (T, h)), _ptr(A, "A", (h, F)), _ptr(B, "B", (F, h)),
         _ptr(Z, "Z", (T, F)), _ptr(H, "H", (T, F)), T, h, F, t,
         _ptr(dX, "dX", (T, h)), _ptr(dA, "dA", (h, F)), _ptr(dB, "dB", (F, h)),
+        _ptr(db1, "db1", (F,), torch.float32), _ptr(db2, "db2", (h,), torch.float32),
+        _ptr(workspace, "workspace", None, torch.uint8), workspace.numel(), _stream(stream)))
+    return dX, dA, dB, db1, db2
+
+
+def tp_mlp_row_sum_dropout(H, B, b2, residual, t: int, p: float, seed: int, offset: int = 0,
+                           Y=None, workspace=None, stream=None):
+    """a3 with dropout before the residual add (keep drawn from seed, offset)."""
+    T, F = H.shape
+    h = B.shape[1]
+    Y = _out(Y, (T, h), H)
+    wp, wn = _workspace(workspace, split_workspace_bytes(T, h, F, t), H)
+    _check("tp_mlp_row_sum_dropout", lib().tp_mlp_row_sum_dropout(
+        _ptr(H, "H", (T, F)), _ptr(B, "B", (F, h)), _ptr(b2, "b2", (h,)),
+        _ptr(residual, "residual", (T, h)), T, h, F, t, float(p), int(seed), int(offset),
+        _ptr(Y, "Y", (T, h)), wp, wn, _stream(stream)))
+    return Y
+
+
+def tp_mlp_forward_dropout(X, A, b1, B, b2, residual, t: int, p: float, seed: int,
+                           offset: int = 0, Y=None, Z=None, H=None, workspace=None, stream=None):
+    """Y, Z, H of the block with dropout before the residual add."""
+    T, h = X.shape
+    F = A.shape[1]
+    Y = _out(Y, (T, h), X)
+    Z = _out(Z, (T, F), X)
+    H = _out(H, (T, F), X)
+    wp, wn = _workspace(workspace, int(lib().tp_mlp_forward_workspace_bytes(T, h, F, t)), X)
+    _check("tp_mlp_forward_dropout", lib().tp_mlp_forward_dropout(
+        _ptr(X, "X", (T, h)), _ptr(A, "A", (h, F)), _ptr(b1, "b1", (F,)), _ptr(B, "B", (F, h)),
+        _ptr(b2, "b2", (h,)), _ptr(residual, "residual", (T, h)), T, h, F, t, float(p),
+        int(seed), int(offset), _ptr(Y, "Y", (T, h)), _ptr(Z, "Z", (T, F)),
+        _ptr(H, "H", (T, F)), wp, wn, _stream(stream)))
+    return Y, Z, H
+
+
+def tp_mlp_dropout_grad(dY, p: float, seed: int, offset: int = 0, dP=None, stream=None):
+    """dP = keep * dY / (1 - p) (bf16)."""
+    T, h = dY.shape
+    dP = _out(dP, (T, h), dY)
+    _check("tp_mlp_dropout_grad", lib().tp_mlp_dropout_grad(
+        _ptr(dY, "dY", (T, h)), T, h, float(p), int(seed), int(offset), _ptr(dP, "dP", (T, h)),
+        _stream(stream)))
+    return dP
+
+
+def tp_mlp_backward_dropout_workspace_bytes(T: int, h: int, F: int, t: int) -> int:
+    return int(lib().tp_mlp_backward_dropout_workspace_bytes(T, h, F, t))
+
+
+def tp_mlp_backward_dropout(dY, X, A, B, Z, H, t: int, p: float, seed: int, offset: int = 0,
+                            dX=None, dA=None, dB=None, db1=None, db2=None, workspace=None,
+                            stream=None):
+    """dX, dA, dB (bf16) and db1, db2 (float32) of the block with dropout."""
+    T, h = X.shape
+    F = A.shape[1]
+    dX = _out(dX, (T, h), X)
+    dA = _out(dA, (h, F), X)
+    dB = _out(dB, (F, h), X)
+    db1 = _out(db1, (F,), X, torch.float32)
+    db2 = _out(db2, (h,), X, torch.float32)
+    need = tp_mlp_backward_dropout_workspace_bytes(T, h, F, t)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=X.device)
+    _check("tp_mlp_backward_dropout", lib().tp_mlp_backward_dropout(
+        _ptr(dY, "dY", (T, h)), _ptr(X, "X", (T, h)), _ptr(A, "A", (h, F)), _ptr(B, "B", (F, h)),
+        _ptr(Z, "Z", (T, F)), _ptr(H, "H", (T, F)), T, h, F, t, float(p), int(seed),
+        int(offset), _ptr(dX, "dX", (T, h)), _ptr(dA, "dA", (h, F)), _ptr(dB, "dB", (F, h)),
         _ptr(db1, "db1", (F,), torch.float32), _ptr(db2, "db2", (h,), torch.float32),
         _ptr(workspace, "workspace", None, torch.uint8), workspace.numel(), _stream(stream)))
     return dX, dA, dB, db1, db2

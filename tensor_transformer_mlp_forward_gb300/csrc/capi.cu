@@ -364,11 +364,12 @@ size_t split_partial_floats(int T, int h, int F, int t) {
     return sp > 1 ? static_cast<size_t>(sp) * T * h : 0;
 }
 
-// out[i] = bf16(sum_s P[s][i] (+ bias[i % n] + res[i])), 8 elements a thread.
+// out[i] = bf16(sum_s P[s][i] (+ bias[i % n] + res[i])), 8 elements a thread;
+// with dropout, out[i] = res[i] + keep(i) * (sum_s P[s][i] + bias[i % n]) * scale.
 __global__ void __launch_bounds__(256)
     split_reduce_kernel(const float* __restrict__ P, int splits, long long count, int n,
                         const __nv_bfloat16* __restrict__ bias, const __nv_bfloat16* __restrict__ res,
-                        __nv_bfloat16* __restrict__ out) {
+                        Dropout dr, __nv_bfloat16* __restrict__ out) {
     const long long i = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
     if (i >= count) return;
     float a[8];
@@ -384,10 +385,22 @@ __global__ void __launch_bounds__(256)
         const uint4 b = __ldg(reinterpret_cast<const uint4*>(bias + i % n));
         const uint4 r = __ldg(reinterpret_cast<const uint4*>(res + i));
         const uint32_t bw[4] = {b.x, b.y, b.z, b.w}, rw[4] = {r.x, r.y, r.z, r.w};
+        if (dr.threshold == 0u) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            a[2 * j] += __uint_as_float(bw[j] << 16) + __uint_as_float(rw[j] << 16);
-            a[2 * j + 1] += __uint_as_float(bw[j] & 0xFFFF0000u) + __uint_as_float(rw[j] & 0xFFFF0000u);
+            for (int j = 0; j < 4; ++j) {
+                a[2 * j] += __uint_as_float(bw[j] << 16) + __uint_as_float(rw[j] << 16);
+                a[2 * j + 1] += __uint_as_float(bw[j] & 0xFFFF0000u) + __uint_as_float(rw[j] & 0xFFFF0000u);
+            }
+        } else {
+            const uint32_t keep = dropout_keep4(dr.seed, dr.offset + i, dr.threshold) |
+                                  (dropout_keep4(dr.seed, dr.offset + i + 4, dr.threshold) << 4);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t bb = (j & 1) ? (bw[j >> 1] & 0xFFFF0000u) : (bw[j >> 1] << 16);
+                const uint32_t rr = (j & 1) ? (rw[j >> 1] & 0xFFFF0000u) : (rw[j >> 1] << 16);
+                a[j] = __uint_as_float(rr) +
+                       (((keep >> j) & 1u) ? (a[j] + __uint_as_float(bb)) * dr.scale : 0.0f);
+            }
         }
     }
     uint4 o;
@@ -399,10 +412,11 @@ __global__ void __launch_bounds__(256)
 }
 
 int launch_split_reduce(const float* P, int splits, int T, int h, const tpmlp_bf16* bias,
-                        const tpmlp_bf16* res, tpmlp_bf16* out, cudaStream_t st) {
+                        const tpmlp_bf16* res, const Dropout& dr, tpmlp_bf16* out,
+                        cudaStream_t st) {
     const long long count = 1LL * T * h;
     split_reduce_kernel<<<static_cast<unsigned>(cdiv(count / 8, 256)), 256, 0, st>>>(
-        P, splits, count, h, cb(bias), cb(res), reinterpret_cast<__nv_bfloat16*>(out));
+        P, splits, count, h, cb(bias), cb(res), dr, reinterpret_cast<__nv_bfloat16*>(out));
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail_cuda(e);
     ++t_last_launches;
@@ -419,7 +433,7 @@ int row_splits(int T, int h, int F, int t, size_t ws_bytes, const DeviceInfo& d)
 
 int row_sum(const tpmlp_bf16* H, const tpmlp_bf16* B, const tpmlp_bf16* b2,
             const tpmlp_bf16* R, int T, int h, int F, int t, tpmlp_bf16* Y, void* ws,
-            size_t ws_bytes, cudaStream_t st, const DeviceInfo& d) {
+            size_t ws_bytes, cudaStream_t st, const DeviceInfo& d, const Dropout& dr = Dropout{}) {
     const int f = F / t;
     GemmArgs g = blank_args();
     const GemmShape sh{T, h, f, t, SHARD_K, 1LL * T * F, 1LL * F * h};
@@ -428,6 +442,7 @@ int row_sum(const tpmlp_bf16* H, const tpmlp_bf16* B, const tpmlp_bf16* b2,
     g.bias = cb(b2);
     g.aux = cb(R);
     g.ld_aux = h;
+    g.drop = dr;
     Operand a{H, T, F, ON_CONTIG, false};
     Operand b{B, F, h, ON_ROWS, true};
     const int sp = ws ? row_splits(T, h, F, t, ws_bytes, d) : 1;
@@ -437,7 +452,57 @@ int row_sum(const tpmlp_bf16* H, const tpmlp_bf16* B, const tpmlp_bf16* b2,
     }
     Output o{ws, nullptr, T, h, sp};
     if (int rc = run_gemm(launch_row_partial, a, b, o, g, sh, st, d)) return rc;
-    return launch_split_reduce(static_cast<const float*>(ws), sp, T, h, b2, R, Y, st);
+    return launch_split_reduce(static_cast<const float*>(ws), sp, T, h, b2, R, dr, Y, st);
+}
+
+// dP = keep * dY * scale (bf16), 8 elements a thread: the gradient that
+// reaches the MLP's output through the dropout.
+__global__ void __launch_bounds__(256)
+    dropout_grad_kernel(const __nv_bfloat16* __restrict__ dY, long long count, Dropout dr,
+                        __nv_bfloat16* __restrict__ dP) {
+    const long long i = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
+    if (i >= count) return;
+    const uint4 g = __ldg(reinterpret_cast<const uint4*>(dY + i));
+    const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+    const uint32_t keep = dropout_keep4(dr.seed, dr.offset + i, dr.threshold) |
+                          (dropout_keep4(dr.seed, dr.offset + i + 4, dr.threshold) << 4);
+    float a[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t gg = (j & 1) ? (gw[j >> 1] & 0xFFFF0000u) : (gw[j >> 1] << 16);
+        a[j] = ((keep >> j) & 1u) ? __uint_as_float(gg) * dr.scale : 0.0f;
+    }
+    uint4 o;
+    o.x = pack_bf16x2(a[0], a[1]);
+    o.y = pack_bf16x2(a[2], a[3]);
+    o.z = pack_bf16x2(a[4], a[5]);
+    o.w = pack_bf16x2(a[6], a[7]);
+    *reinterpret_cast<uint4*>(dP + i) = o;
+}
+
+int dropout_grad(const tpmlp_bf16* dY, int T, int h, const Dropout& dr, tpmlp_bf16* dP,
+                 cudaStream_t st) {
+    const long long count = 1LL * T * h;
+    if (count == 0) return TPMLP_OK;
+    dropout_grad_kernel<<<static_cast<unsigned>(cdiv(count / 8, 256)), 256, 0, st>>>(
+        cb(dY), count, dr, reinterpret_cast<__nv_bfloat16*>(dP));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail_cuda(e);
+    ++t_last_launches;
+    return TPMLP_OK;
+}
+
+// Dropout parameters from the caller's rate p in [0, 1): keep iff the
+// element's Philox word >= floor(p * 2^32), survivors scaled by 1 / (1 - p).
+// The element counters advance four to a Philox block, so `offset` must be a
+// multiple of 4.
+int make_dropout(double p, uint64_t seed, uint64_t offset, Dropout& dr) {
+    if (!(p >= 0.0 && p < 1.0) || offset % 4 != 0) return TPMLP_ERR_SHAPE;
+    dr.threshold = static_cast<uint32_t>(p * 4294967296.0);
+    dr.scale = static_cast<float>(1.0 / (1.0 - p));
+    dr.seed = seed;
+    dr.offset = offset;
+    return TPMLP_OK;
 }
 
 int dgelu_gemm(const tpmlp_bf16* dY, const tpmlp_bf16* B, const tpmlp_bf16* Z, int T, int h,
@@ -473,7 +538,7 @@ int dx_gemm(const tpmlp_bf16* dZ, const tpmlp_bf16* A, int T, int h, int F, int 
     }
     Output o{ws, nullptr, T, h, sp};
     if (int rc = run_gemm(launch_dx_partial, a, b, o, g, sh, st, d)) return rc;
-    return launch_split_reduce(static_cast<const float*>(ws), sp, T, h, nullptr, nullptr, dX, st);
+    return launch_split_reduce(static_cast<const float*>(ws), sp, T, h, nullptr, nullptr, Dropout{}, dX, st);
 }
 
 int dA_gemm(const tpmlp_bf16* X, const tpmlp_bf16* dZ, int T, int h, int F, int t,
@@ -859,22 +924,13 @@ TPMLP_API size_t tp_mlp_backward_workspace_bytes(int T, int h, int F, int t) {
     return backward_layout(T, h, F, t).total;
 }
 
-TPMLP_API int tp_mlp_backward(const tpmlp_bf16* dY, const tpmlp_bf16* X, const tpmlp_bf16* A,
-                              const tpmlp_bf16* B, const tpmlp_bf16* Z, const tpmlp_bf16* H,
-                              int T, int h, int F, int t, tpmlp_bf16* dX, tpmlp_bf16* dA,
-                              tpmlp_bf16* dB, float* db1, float* db2, void* workspace,
-                              size_t workspace_bytes, void* stream) {
-    TPMLP_PROLOGUE(check_dims(T, h, F, t));
-    if (any_null(A, B, dA, dB, db1, db2) || (T > 0 && any_null(dY, X, Z, H, dX)))
-        return TPMLP_ERR_NULL;
-    if (!all_aligned(dY, X, A, B, Z, H, dX, dA, dB, db1, db2)) return TPMLP_ERR_ALIGN;
-    const BackwardLayout L = backward_layout(T, h, F, t);
-    if (T > 0 && (workspace == nullptr || workspace_bytes < L.total)) return TPMLP_ERR_WORKSPACE;
-    if (!aligned16(workspace)) return TPMLP_ERR_ALIGN;
-    DeviceInfo d;
-    if (int rc = enter(d)) return rc;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
+// Steps a4..a9 given the gradient dY at the MLP's output and a workspace laid
+// out by backward_layout (arguments already checked).
+static int backward_steps(const tpmlp_bf16* dY, const tpmlp_bf16* X, const tpmlp_bf16* A,
+                          const tpmlp_bf16* B, const tpmlp_bf16* Z, const tpmlp_bf16* H, int T,
+                          int h, int F, int t, tpmlp_bf16* dX, tpmlp_bf16* dA, tpmlp_bf16* dB,
+                          float* db1, float* db2, uint8_t* ws, const BackwardLayout& L,
+                          cudaStream_t st, const DeviceInfo& d) {
     tpmlp_bf16* dZ = reinterpret_cast<tpmlp_bf16*>(ws + L.dz);
     float* colsum = reinterpret_cast<float*>(ws + L.colsum);
     float* db2_part = reinterpret_cast<float*>(ws + L.db2);
@@ -896,6 +952,112 @@ TPMLP_API int tp_mlp_backward(const tpmlp_bf16* dY, const tpmlp_bf16* X, const t
     // a8, a9: weight gradients of every shard
     if (int rc = dA_gemm(X, dZ, T, h, F, t, dA, st, d)) return rc;
     return dB_gemm(H, dY, T, h, F, t, dB, st, d);
+}
+
+TPMLP_API int tp_mlp_backward(const tpmlp_bf16* dY, const tpmlp_bf16* X, const tpmlp_bf16* A,
+                              const tpmlp_bf16* B, const tpmlp_bf16* Z, const tpmlp_bf16* H,
+                              int T, int h, int F, int t, tpmlp_bf16* dX, tpmlp_bf16* dA,
+                              tpmlp_bf16* dB, float* db1, float* db2, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+    TPMLP_PROLOGUE(check_dims(T, h, F, t));
+    if (any_null(A, B, dA, dB, db1, db2) || (T > 0 && any_null(dY, X, Z, H, dX)))
+        return TPMLP_ERR_NULL;
+    if (!all_aligned(dY, X, A, B, Z, H, dX, dA, dB, db1, db2)) return TPMLP_ERR_ALIGN;
+    const BackwardLayout L = backward_layout(T, h, F, t);
+    if (T > 0 && (workspace == nullptr || workspace_bytes < L.total)) return TPMLP_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return TPMLP_ERR_ALIGN;
+    DeviceInfo d;
+    if (int rc = enter(d)) return rc;
+    return backward_steps(dY, X, A, B, Z, H, T, h, F, t, dX, dA, dB, db1, db2,
+                          static_cast<uint8_t*>(workspace), L, static_cast<cudaStream_t>(stream), d);
+}
+
+// ------------------------------------------------ dropout before the residual
+
+TPMLP_API int tp_mlp_row_sum_dropout(const tpmlp_bf16* H, const tpmlp_bf16* B,
+                                     const tpmlp_bf16* b2, const tpmlp_bf16* residual, int T,
+                                     int h, int F, int t, double p, uint64_t seed, uint64_t offset,
+                                     tpmlp_bf16* Y, void* workspace, size_t workspace_bytes,
+                                     void* stream) {
+    TPMLP_PROLOGUE(check_dims(T, h, F, t));
+    Dropout dr;
+    if (int rc = make_dropout(p, seed, offset, dr)) return rc;
+    if (T == 0) return TPMLP_OK;
+    if (any_null(H, B, b2, residual, Y)) return TPMLP_ERR_NULL;
+    if (!all_aligned(H, B, b2, residual, Y, workspace)) return TPMLP_ERR_ALIGN;
+    DeviceInfo d;
+    if (int rc = enter(d)) return rc;
+    return row_sum(H, B, b2, residual, T, h, F, t, Y, workspace, workspace_bytes,
+                   static_cast<cudaStream_t>(stream), d, dr);
+}
+
+TPMLP_API int tp_mlp_forward_dropout(const tpmlp_bf16* X, const tpmlp_bf16* A,
+                                     const tpmlp_bf16* b1, const tpmlp_bf16* B,
+                                     const tpmlp_bf16* b2, const tpmlp_bf16* residual, int T,
+                                     int h, int F, int t, double p, uint64_t seed, uint64_t offset,
+                                     tpmlp_bf16* Y, tpmlp_bf16* Z, tpmlp_bf16* H, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+    TPMLP_PROLOGUE(check_dims(T, h, F, t));
+    Dropout dr;
+    if (int rc = make_dropout(p, seed, offset, dr)) return rc;
+    if (T == 0) return TPMLP_OK;
+    if (any_null(X, A, b1, B, b2, residual, Y, Z, H)) return TPMLP_ERR_NULL;
+    if (!all_aligned(X, A, b1, B, b2, residual, Y, Z, H)) return TPMLP_ERR_ALIGN;
+    if (!aligned16(workspace)) return TPMLP_ERR_ALIGN;
+    DeviceInfo d;
+    if (int rc = enter(d)) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (int rc = column_gelu(X, A, b1, T, h, F, t, Z, H, st, d)) return rc;
+    return row_sum(H, B, b2, residual, T, h, F, t, Y, workspace, workspace_bytes, st, d, dr);
+}
+
+TPMLP_API int tp_mlp_dropout_grad(const tpmlp_bf16* dY, int T, int h, double p, uint64_t seed,
+                                  uint64_t offset, tpmlp_bf16* dP, void* stream) {
+    t_last_launches = 0;
+    if (T < 0 || h < 8 || h % 8 != 0) return TPMLP_ERR_SHAPE;
+    Dropout dr;
+    if (int rc = make_dropout(p, seed, offset, dr)) return rc;
+    if (T == 0) return TPMLP_OK;
+    if (any_null(dY, dP)) return TPMLP_ERR_NULL;
+    if (!all_aligned(dY, dP)) return TPMLP_ERR_ALIGN;
+    return dropout_grad(dY, T, h, dr, dP, static_cast<cudaStream_t>(stream));
+}
+
+// The dropout backward keeps dP = keep * dY / (1 - p) after the block's own
+// backward workspace.
+static size_t dropout_dp_offset(const BackwardLayout& L) { return align256(L.total); }
+
+TPMLP_API size_t tp_mlp_backward_dropout_workspace_bytes(int T, int h, int F, int t) {
+    if (check_dims(T, h, F, t)) return 0;
+    const BackwardLayout L = backward_layout(T, h, F, t);
+    return align256(dropout_dp_offset(L) + sizeof(uint16_t) * static_cast<size_t>(T) * h);
+}
+
+TPMLP_API int tp_mlp_backward_dropout(const tpmlp_bf16* dY, const tpmlp_bf16* X,
+                                      const tpmlp_bf16* A, const tpmlp_bf16* B,
+                                      const tpmlp_bf16* Z, const tpmlp_bf16* H, int T, int h,
+                                      int F, int t, double p, uint64_t seed, uint64_t offset,
+                                      tpmlp_bf16* dX, tpmlp_bf16* dA, tpmlp_bf16* dB, float* db1,
+                                      float* db2, void* workspace, size_t workspace_bytes,
+                                      void* stream) {
+    TPMLP_PROLOGUE(check_dims(T, h, F, t));
+    Dropout dr;
+    if (int rc = make_dropout(p, seed, offset, dr)) return rc;
+    if (any_null(A, B, dA, dB, db1, db2) || (T > 0 && any_null(dY, X, Z, H, dX)))
+        return TPMLP_ERR_NULL;
+    if (!all_aligned(dY, X, A, B, Z, H, dX, dA, dB, db1, db2)) return TPMLP_ERR_ALIGN;
+    const BackwardLayout L = backward_layout(T, h, F, t);
+    if (T > 0 && (workspace == nullptr ||
+                  workspace_bytes < tp_mlp_backward_dropout_workspace_bytes(T, h, F, t)))
+        return TPMLP_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return TPMLP_ERR_ALIGN;
+    DeviceInfo d;
+    if (int rc = enter(d)) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    tpmlp_bf16* dP = T > 0 ? reinterpret_cast<tpmlp_bf16*>(ws + dropout_dp_offset(L)) : nullptr;
+    if (int rc = dropout_grad(dY, T, h, dr, dP, st)) return rc;
+    return backward_steps(dP, X, A, B, Z, H, T, h, F, t, dX, dA, dB, db1, db2, ws, L, st, d);
 }
 
 // ----------------------------------------------- residual add + LayerNorm

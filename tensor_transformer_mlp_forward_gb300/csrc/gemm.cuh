@@ -41,6 +41,7 @@
 // counters, descriptors by adding offsets to precomputed bases.
 #pragma once
 
+#include "philox.cuh"
 #include "ptx.cuh"
 
 namespace tpmlp {
@@ -98,6 +99,7 @@ struct GemmArgs {
     const __nv_bfloat16* bias;  // b1 or b2, indexed by global output column
     const __nv_bfloat16* aux;   // residual (EPI_BIAS_RESIDUAL) or Z (EPI_DGELU)
     long long ld_aux;
+    Dropout drop;   // EPI_BIAS_RESIDUAL: bias-dropout-add (drop.threshold 0: none)
     float* colsum;  // EPI_DGELU: column sums per 32-row block, [4 * mt_total][ld_colsum]
     long long ld_colsum;
     int* status;    // device status word
@@ -570,8 +572,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             float b[32], res[32];
                             load_bf16x32(p.bias + gcol, valid, b);
                             load_bf16x32(p.aux + grow * p.ld_aux + gcol, valid, res);
+                            if (p.drop.threshold == 0u) {
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] += b[i] + res[i];
+                                for (int i = 0; i < 32; ++i) v[i] += b[i] + res[i];
+                            } else {
+                                // Y = residual + keep * (P + b2) / (1 - p); element
+                                // e = row * h + col, counters offset + e (4 per block)
+                                const uint64_t g0 = p.drop.offset +
+                                                    static_cast<uint64_t>(grow * p.ld_aux + gcol);
+#pragma unroll
+                                for (int q4 = 0; q4 < 8; ++q4) {
+                                    const uint32_t keep =
+                                        dropout_keep4(p.drop.seed, g0 + 4 * q4, p.drop.threshold);
+#pragma unroll
+                                    for (int j = 0; j < 4; ++j) {
+                                        const int i = 4 * q4 + j;
+                                        v[i] = res[i] + (((keep >> j) & 1u) ? (v[i] + b[i]) * p.drop.scale
+                                                                            : 0.0f);
+                                    }
+                                }
+                            }
                         }
                         stage_row(buf0 + my_row, half, swz, v);
                     } else if constexpr (EPI == EPI_DGELU) {

@@ -102,3 +102,29 @@ def test_no_cpu_fallback_in_binding():
     assert "import oracle" not in src and "from oracle" not in src
     for forbidden in ("torch.matmul", "torch.nn.functional", "torch.mm(", ".cpu()"):
         assert forbidden not in src, forbidden
+
+
+def test_dropout_argument_errors(L):
+    rs = lambda p, off, Y=P: L.tp_mlp_row_sum_dropout(P, P, P, P, 128, 256, 1024, 2, p, 7, off,
+                                                      Y, N, 0, N)
+    assert rs(1.0, 0) == binding.TPMLP_ERR_SHAPE   # p must be < 1
+    assert rs(-0.1, 0) == binding.TPMLP_ERR_SHAPE
+    assert rs(float("nan"), 0) == binding.TPMLP_ERR_SHAPE
+    assert rs(0.1, 6) == binding.TPMLP_ERR_SHAPE   # offset a multiple of 4
+    assert rs(0.1, 8, Y=N) == binding.TPMLP_ERR_NULL
+    assert L.tp_mlp_dropout_grad(P, 128, 12, 0.1, 7, 0, P, N) == binding.TPMLP_ERR_SHAPE
+    assert L.tp_mlp_dropout_grad(Q, 128, 256, 0.1, 7, 0, P, N) == binding.TPMLP_ERR_ALIGN
+    fd = [P] * 6 + [128, 256, 1024, 2, 0.1, 7, 0] + [P] * 3 + [N, 0, N]
+    assert L.tp_mlp_forward_dropout(*fd[:10], 0.1, 7, 2, *fd[13:]) == binding.TPMLP_ERR_SHAPE
+    # an empty batch is valid and launches nothing
+    assert L.tp_mlp_dropout_grad(N, 0, 256, 0.1, 7, 0, N, N) == binding.TPMLP_OK
+
+
+def test_dropout_backward_workspace(L):
+    T, h, F, t = 300, 200, 1536, 4
+    base = L.tp_mlp_backward_workspace_bytes(T, h, F, t)
+    need = L.tp_mlp_backward_dropout_workspace_bytes(T, h, F, t)
+    assert need >= base + 2 * T * h       # plus the bf16 dP
+    args = [P] * 6 + [T, h, F, t, 0.1, 7, 0] + [P] * 5
+    assert L.tp_mlp_backward_dropout(*args, P, need - 1, N) == binding.TPMLP_ERR_WORKSPACE
+    assert L.tp_mlp_backward_dropout(*args, N, need, N) == binding.TPMLP_ERR_WORKSPACE
