@@ -52,6 +52,8 @@ def parse_args(argv=None):
     p.add_argument("--tokens", type=int, default=None)
     p.add_argument("--shards", type=int, default=None)
     p.add_argument("--sweep", action="store_true")
+    p.add_argument("--recompute", action="store_true",
+                   help="activation recompute: save only X, rebuild Z and H in the backward pass")
     p.add_argument("--dropout", type=float, default=0.0,
                    help="dropout rate before the residual add (0: the block without dropout)")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -210,7 +212,7 @@ GEMM_CALLS = ("column_gelu", "row_sum", "dx", "dA", "dB")  # one kernel each
 class Step:
     """All buffers of one replica, resident in HBM; run() issues one step."""
 
-    def __init__(self, w, device, p_drop=0.0, seed=0x5EED):
+    def __init__(self, w, device, p_drop=0.0, seed=0x5EED, recompute=False):
         import torch
 
         from tensor_transformer_mlp_forward_gb300 import binding, inputs
@@ -232,29 +234,33 @@ class Step:
         # element counter advances by T*h, rounded up to a Philox block)
         self.p_drop, self.seed, self.offset = p_drop, seed, 0
         self.dP = e(T, h) if p_drop > 0 else None
-        self.names = STEP_CALLS if p_drop <= 0 else (
-            "column_gelu", "row_sum", "dropout_grad", "db2", "dgelu", "dx", "dA", "dB")
+        # activation recompute: the forward pass writes only H (transient),
+        # the backward pass rebuilds Z and H from X before a4
+        self.recompute = recompute
+        self.names = (("column_gelu", "row_sum") + (("dropout_grad",) if p_drop > 0 else ())
+                      + (("recompute",) if recompute else ()) + STEP_CALLS[2:])
 
     def run(self, events=None):
         """One fwd+bwd step; if `events` (len 8) is given, records them
         between the calls on the current stream."""
         b, i, t = self.b, self.inp, self.w.t
+        rec = self.recompute
+        calls = (lambda: b.tp_mlp_column_gelu(i["X"], i["A"], i["b1"], t, Z=None if rec else self.Z,
+                                              H=self.H, want_z=not rec),)
         if self.p_drop <= 0:
             dP = i["dY"]
-            calls = (
-                lambda: b.tp_mlp_column_gelu(i["X"], i["A"], i["b1"], t, Z=self.Z, H=self.H),
-                lambda: b.tp_mlp_row_sum(self.H, i["B"], i["b2"], i["residual"], t, Y=self.Y,
-                                         workspace=self.ws_split),
-            )
+            calls += (lambda: b.tp_mlp_row_sum(self.H, i["B"], i["b2"], i["residual"], t, Y=self.Y,
+                                               workspace=self.ws_split),)
         else:
             dP, p, sd, off = self.dP, self.p_drop, self.seed, self.offset
             self.offset += (self.w.T * self.w.h + 3) // 4 * 4
-            calls = (
-                lambda: b.tp_mlp_column_gelu(i["X"], i["A"], i["b1"], t, Z=self.Z, H=self.H),
+            calls += (
                 lambda: b.tp_mlp_row_sum_dropout(self.H, i["B"], i["b2"], i["residual"], t, p, sd,
                                                  off, Y=self.Y, workspace=self.ws_split),
                 lambda: b.tp_mlp_dropout_grad(i["dY"], p, sd, off, dP=dP),
             )
+        if rec:
+            calls += (lambda: b.tp_mlp_column_gelu(i["X"], i["A"], i["b1"], t, Z=self.Z, H=self.H),)
         calls = calls + (
             lambda: b.tp_mlp_bias_grad(dP, db=self.db2, partial=self.p_db2),
             lambda: b.tp_mlp_dgelu(dP, i["B"], self.Z, t, dZ=self.dZ, db1=self.db1, partial=self.p_db1),
@@ -308,12 +314,12 @@ def barrier():
         dist.barrier()
 
 
-def time_ours(w, steps, warmup, local, p_drop=0.0):
+def time_ours(w, steps, warmup, local, p_drop=0.0, recompute=False):
     import torch
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    step = Step(w, dev, p_drop)
+    step = Step(w, dev, p_drop, recompute=recompute)
     for _ in range(warmup):
         step.run()
     torch.cuda.synchronize()
@@ -442,7 +448,7 @@ def run_ours(args, w):
         binding.set_cta_pair_mode(args.pair_mode)
     rank, world, local = init_distributed(args.gpus)
     step, dev_s, wall, per_call, clocks, launches = time_ours(w, args.steps, args.warmup, local,
-                                                              args.dropout)
+                                                              args.dropout, args.recompute)
     flops = w.flops_fwd_bwd()
     max_s, units = reduce_max_sum(dev_s, flops * args.steps)
     value = units / max_s / 1e12
@@ -470,7 +476,9 @@ def run_ours(args, w):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * max_s / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(describe(w, world), **({"dropout": args.dropout} if args.dropout > 0 else {})),
+        "config": dict(describe(w, world), **({"dropout": args.dropout} if args.dropout > 0 else {}),
+                       **({"activation_recompute": "Z, H rebuilt by a2 in the backward pass; "
+                           "value counts the 12*T*h*F model flops only"} if args.recompute else {})),
         "pct_of_peak": {"burst": 100 * value / world / burst, "sustained": 100 * value / world / sustained,
                         "source": src},
         "per_call_ms": {k: round(v, 4) for k, v in avg_ms.items()},
@@ -481,6 +489,8 @@ def run_ours(args, w):
         "gemm_kernel": {0: "single CTA", 1: "auto", 2: "CTA pairs"}[
             args.pair_mode if args.pair_mode is not None else 1],
     }
+    if args.recompute:  # the rebuilt a2 is a seventh GEMM of 2*T*h*F flops
+        line["hardware_tflops"] = value * 14 / 12
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(w, step.cpu)
     print(json.dumps(line))

@@ -120,7 +120,9 @@ int tp_mlp_backward(const tpmlp_bf16* dY, const tpmlp_bf16* X, const tpmlp_bf16*
 /* a2: column-parallel GEMM with fused bias and GeLU, all t shards in one
  * launch: Z[:, i f:(i+1) f] = X A_i + b1_i, H = GeLU(Z).
  * (Figure 3a of the page above: each shard applies GeLU to its own columns
- * with no synchronisation before the nonlinearity.) */
+ * with no synchronisation before the nonlinearity.)  Z may be NULL: only H
+ * is written (the forward pass of activation recompute, which rebuilds Z in
+ * the backward pass). */
 int tp_mlp_column_gelu(const tpmlp_bf16* X, const tpmlp_bf16* A, const tpmlp_bf16* b1,
                        int T, int h, int F, int t, tpmlp_bf16* Z, tpmlp_bf16* H, void* stream);
 
@@ -230,6 +232,47 @@ int tp_ln_residual_backward(const tpmlp_bf16* dX, const tpmlp_bf16* dres, const 
                             const tpmlp_bf16* r, const tpmlp_bf16* gamma, const float* mean,
                             const float* rstd, int T, int h, tpmlp_bf16* ds, float* dgamma,
                             float* dbeta, float* partial, void* stream);
+
+/* ---------------------------------------------------------------------- */
+/* Activation recompute                                                    */
+/* ---------------------------------------------------------------------- */
+
+/* "MT-NLG 530B deep dive" (zzszmyf.github.io), section 2.2 (activation
+ * checkpointing): keep only each layer's input, and rerun the layer's
+ * forward computation when the backward pass needs its intermediate
+ * activations -- about a third more compute for much less activation
+ * memory; "Megatron-LM: Tensor Model Parallel", training-recipe table (row
+ * "Memory"), checkpoints after every Transformer layer.  For this block the
+ * saved activations shrink from Z and H (2 T F values) to X (T h, which the
+ * caller holds anyway); Z and H are rebuilt by a2 at the start of the
+ * backward pass. */
+
+/* Bytes of scratch tp_mlp_forward_recompute needs: H [T,F] bf16, live only
+ * during the call, plus a3's split-reduction scratch. */
+size_t tp_mlp_forward_recompute_workspace_bytes(int T, int h, int F, int t);
+
+/* Forward pass that saves nothing for the backward pass: a2 writes only H,
+ * into the workspace, and a3 reads it; Y as tp_mlp_forward.  The workspace
+ * (16-byte aligned, at least the H part; the split part is optional as for
+ * tp_mlp_forward) may be reused by other calls once this one completes. */
+int tp_mlp_forward_recompute(const tpmlp_bf16* X, const tpmlp_bf16* A, const tpmlp_bf16* b1,
+                             const tpmlp_bf16* B, const tpmlp_bf16* b2,
+                             const tpmlp_bf16* residual, int T, int h, int F, int t,
+                             tpmlp_bf16* Y, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/* Bytes of scratch tp_mlp_backward_recompute needs: the recomputed Z and H
+ * ([T,F] bf16 each) plus tp_mlp_backward's workspace. */
+size_t tp_mlp_backward_recompute_workspace_bytes(int T, int h, int F, int t);
+
+/* Backward pass from the layer input alone: a2 recomputes Z = X A + b1 and
+ * H = GeLU(Z) into the workspace (bitwise the values tp_mlp_forward saves),
+ * then steps a4..a9 run as in tp_mlp_backward.  In: dY, X [T,h]; A [h,F];
+ * b1 [F]; B [F,h].  Out as tp_mlp_backward. */
+int tp_mlp_backward_recompute(const tpmlp_bf16* dY, const tpmlp_bf16* X, const tpmlp_bf16* A,
+                              const tpmlp_bf16* b1, const tpmlp_bf16* B, int T, int h, int F,
+                              int t, tpmlp_bf16* dX, tpmlp_bf16* dA, tpmlp_bf16* dB, float* db1,
+                              float* db2, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------- */
 /* Dropout before the residual add                                         */

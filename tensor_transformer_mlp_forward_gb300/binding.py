@@ -61,6 +61,10 @@ _SIGNATURES = {
     "tp_mlp_dx": ([_P] * 2 + [_I] * 4 + [_P] + [_P, _S, _P], _I),
     "tp_mlp_dA": ([_P] * 2 + [_I] * 4 + [_P] + [_P], _I),
     "tp_mlp_dB": ([_P] * 2 + [_I] * 4 + [_P] + [_P], _I),
+    "tp_mlp_forward_recompute_workspace_bytes": ([_I] * 4, _S),
+    "tp_mlp_forward_recompute": ([_P] * 6 + [_I] * 4 + [_P] + [_P, _S, _P], _I),
+    "tp_mlp_backward_recompute_workspace_bytes": ([_I] * 4, _S),
+    "tp_mlp_backward_recompute": ([_P] * 5 + [_I] * 4 + [_P] * 6 + [_S, _P], _I),
     "tp_mlp_row_sum_dropout": ([_P] * 4 + [_I] * 4 + [_D, _U64, _U64] + [_P] + [_P, _S, _P], _I),
     "tp_mlp_forward_dropout": ([_P] * 6 + [_I] * 4 + [_D, _U64, _U64] + [_P] * 3 + [_P, _S, _P],
                                _I),
@@ -163,14 +167,15 @@ def device_status() -> int:
     return int(lib().tpmlp_device_status())
 
 
-def tp_mlp_column_gelu(X, A, b1, t: int, Z=None, H=None, stream=None):
+def tp_mlp_column_gelu(X, A, b1, t: int, Z=None, H=None, stream=None, want_z=True):
+    """Z, H of step a2; with want_z=False only H is written (Z is None)."""
     T, h = X.shape
     F = A.shape[1]
-    Z = _out(Z, (T, F), X)
+    Z = _out(Z, (T, F), X) if want_z else None
     H = _out(H, (T, F), X)
     _check("tp_mlp_column_gelu", lib().tp_mlp_column_gelu(
         _ptr(X, "X", (T, h)), _ptr(A, "A", (h, F)), _ptr(b1, "b1", (F,)), T, h, F, t,
-        _ptr(Z, "Z", (T, F)), _ptr(H, "H", (T, F)), _stream(stream)))
+        _ptr(Z, "Z", (T, F)) if want_z else None, _ptr(H, "H", (T, F)), _stream(stream)))
     return Z, H
 
 
@@ -236,6 +241,45 @@ def tp_mlp_backward(dY, X, A, B, Z, H, t: int, dX=None, dA=None, dB=None, db1=No
     _check("tp_mlp_backward", lib().tp_mlp_backward(
         _ptr(dY, "dY", (T, h)), _ptr(X, "X", (T, h)), _ptr(A, "A", (h, F)), _ptr(B, "B", (F, h)),
         _ptr(Z, "Z", (T, F)), _ptr(H, "H", (T, F)), T, h, F, t,
+        _ptr(dX, "dX", (T, h)), _ptr(dA, "dA", (h, F)), _ptr(dB, "dB", (F, h)),
+        _ptr(db1, "db1", (F,), torch.float32), _ptr(db2, "db2", (h,), torch.float32),
+        _ptr(workspace, "workspace", None, torch.uint8), workspace.numel(), _stream(stream)))
+    return dX, dA, dB, db1, db2
+
+
+def tp_mlp_forward_recompute(X, A, b1, B, b2, residual, t: int, Y=None, workspace=None,
+                             stream=None):
+    """Y of the block; nothing is saved for the backward pass but X."""
+    T, h = X.shape
+    F = A.shape[1]
+    Y = _out(Y, (T, h), X)
+    need = int(lib().tp_mlp_forward_recompute_workspace_bytes(T, h, F, t))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=X.device)
+    _check("tp_mlp_forward_recompute", lib().tp_mlp_forward_recompute(
+        _ptr(X, "X", (T, h)), _ptr(A, "A", (h, F)), _ptr(b1, "b1", (F,)), _ptr(B, "B", (F, h)),
+        _ptr(b2, "b2", (h,)), _ptr(residual, "residual", (T, h)), T, h, F, t,
+        _ptr(Y, "Y", (T, h)), _ptr(workspace, "workspace", None, torch.uint8),
+        workspace.numel(), _stream(stream)))
+    return Y
+
+
+def tp_mlp_backward_recompute(dY, X, A, b1, B, t: int, dX=None, dA=None, dB=None, db1=None,
+                              db2=None, workspace=None, stream=None):
+    """Gradients of the block from its input X (Z and H recomputed)."""
+    T, h = X.shape
+    F = A.shape[1]
+    dX = _out(dX, (T, h), X)
+    dA = _out(dA, (h, F), X)
+    dB = _out(dB, (F, h), X)
+    db1 = _out(db1, (F,), X, torch.float32)
+    db2 = _out(db2, (h,), X, torch.float32)
+    need = int(lib().tp_mlp_backward_recompute_workspace_bytes(T, h, F, t))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=X.device)
+    _check("tp_mlp_backward_recompute", lib().tp_mlp_backward_recompute(
+        _ptr(dY, "dY", (T, h)), _ptr(X, "X", (T, h)), _ptr(A, "A", (h, F)),
+        _ptr(b1, "b1", (F,)), _ptr(B, "B", (F, h)), T, h, F, t,
         _ptr(dX, "dX", (T, h)), _ptr(dA, "dA", (h, F)), _ptr(dB, "dB", (F, h)),
         _ptr(db1, "db1", (F,), torch.float32), _ptr(db2, "db2", (h,), torch.float32),
         _ptr(workspace, "workspace", None, torch.uint8), workspace.numel(), _stream(stream)))

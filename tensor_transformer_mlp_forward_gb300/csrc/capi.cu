@@ -325,7 +325,8 @@ int column_gelu(const tpmlp_bf16* X, const tpmlp_bf16* A, const tpmlp_bf16* b1, 
     g.bias = cb(b1);
     Operand a{X, T, h, ON_NONE, false};
     Operand b{A, h, F, ON_CONTIG, true};
-    Output o{Z, H, T, F};
+    g.skip_o0 = Z == nullptr;  // H only: Z is recomputed by the backward pass
+    Output o{Z ? Z : H, H, T, F};
     return run_gemm(launch_column_gelu, a, b, o, g, sh, st, d);
 }
 
@@ -734,7 +735,7 @@ TPMLP_API int tp_mlp_column_gelu(const tpmlp_bf16* X, const tpmlp_bf16* A, const
                                  void* stream) {
     TPMLP_PROLOGUE(check_dims(T, h, F, t));
     if (T == 0) return TPMLP_OK;
-    if (any_null(X, A, b1, Z, H)) return TPMLP_ERR_NULL;
+    if (any_null(X, A, b1, H)) return TPMLP_ERR_NULL;  // Z NULL: H only
     if (!all_aligned(X, A, b1, Z, H)) return TPMLP_ERR_ALIGN;
     DeviceInfo d;
     if (int rc = enter(d)) return rc;
@@ -970,6 +971,76 @@ TPMLP_API int tp_mlp_backward(const tpmlp_bf16* dY, const tpmlp_bf16* X, const t
     if (int rc = enter(d)) return rc;
     return backward_steps(dY, X, A, B, Z, H, T, h, F, t, dX, dA, dB, db1, db2,
                           static_cast<uint8_t*>(workspace), L, static_cast<cudaStream_t>(stream), d);
+}
+
+// ------------------------------------------------ activation recompute
+
+// Forward with recompute: H lives in the workspace only until a3 has read it;
+// the split-reduction scratch follows it.
+static size_t recompute_h_bytes(int T, int F) {
+    return align256(sizeof(uint16_t) * static_cast<size_t>(T) * F);
+}
+
+TPMLP_API size_t tp_mlp_forward_recompute_workspace_bytes(int T, int h, int F, int t) {
+    if (check_dims(T, h, F, t) || T == 0) return 0;
+    return recompute_h_bytes(T, F) + sizeof(float) * split_partial_floats(T, h, F, t);
+}
+
+TPMLP_API int tp_mlp_forward_recompute(const tpmlp_bf16* X, const tpmlp_bf16* A,
+                                       const tpmlp_bf16* b1, const tpmlp_bf16* B,
+                                       const tpmlp_bf16* b2, const tpmlp_bf16* residual, int T,
+                                       int h, int F, int t, tpmlp_bf16* Y, void* workspace,
+                                       size_t workspace_bytes, void* stream) {
+    TPMLP_PROLOGUE(check_dims(T, h, F, t));
+    if (T == 0) return TPMLP_OK;
+    if (any_null(X, A, b1, B, b2, residual, Y)) return TPMLP_ERR_NULL;
+    if (!all_aligned(X, A, b1, B, b2, residual, Y)) return TPMLP_ERR_ALIGN;
+    const size_t hb = recompute_h_bytes(T, F);
+    if (workspace == nullptr || workspace_bytes < hb) return TPMLP_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return TPMLP_ERR_ALIGN;
+    DeviceInfo d;
+    if (int rc = enter(d)) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    tpmlp_bf16* H = reinterpret_cast<tpmlp_bf16*>(ws);
+    if (int rc = column_gelu(X, A, b1, T, h, F, t, nullptr, H, st, d)) return rc;
+    return row_sum(H, B, b2, residual, T, h, F, t, Y, ws + hb, workspace_bytes - hb, st, d);
+}
+
+// Backward with recompute: Z and H are rebuilt in the workspace, followed by
+// the block's own backward workspace.
+TPMLP_API size_t tp_mlp_backward_recompute_workspace_bytes(int T, int h, int F, int t) {
+    if (check_dims(T, h, F, t)) return 0;
+    return 2 * recompute_h_bytes(T, F) + backward_layout(T, h, F, t).total;
+}
+
+TPMLP_API int tp_mlp_backward_recompute(const tpmlp_bf16* dY, const tpmlp_bf16* X,
+                                        const tpmlp_bf16* A, const tpmlp_bf16* b1,
+                                        const tpmlp_bf16* B, int T, int h, int F, int t,
+                                        tpmlp_bf16* dX, tpmlp_bf16* dA, tpmlp_bf16* dB,
+                                        float* db1, float* db2, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+    TPMLP_PROLOGUE(check_dims(T, h, F, t));
+    if (any_null(A, B, dA, dB, db1, db2) || (T > 0 && any_null(dY, X, b1, dX)))
+        return TPMLP_ERR_NULL;
+    if (!all_aligned(dY, X, A, b1, B, dX, dA, dB, db1, db2)) return TPMLP_ERR_ALIGN;
+    const BackwardLayout L = backward_layout(T, h, F, t);
+    if (T > 0 && (workspace == nullptr ||
+                  workspace_bytes < tp_mlp_backward_recompute_workspace_bytes(T, h, F, t)))
+        return TPMLP_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return TPMLP_ERR_ALIGN;
+    DeviceInfo d;
+    if (int rc = enter(d)) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const size_t hb = recompute_h_bytes(T, F);
+    tpmlp_bf16* Z = T > 0 ? reinterpret_cast<tpmlp_bf16*>(ws) : nullptr;
+    tpmlp_bf16* H = T > 0 ? reinterpret_cast<tpmlp_bf16*>(ws + hb) : nullptr;
+    // the recompute: a2 again, from the saved input X
+    if (T > 0)
+        if (int rc = column_gelu(X, A, b1, T, h, F, t, Z, H, st, d)) return rc;
+    return backward_steps(dY, X, A, B, Z, H, T, h, F, t, dX, dA, dB, db1, db2,
+                          ws == nullptr ? nullptr : ws + 2 * hb, L, st, d);
 }
 
 // ------------------------------------------------ dropout before the residual

@@ -99,6 +99,7 @@ struct GemmArgs {
     const __nv_bfloat16* bias;  // b1 or b2, indexed by global output column
     const __nv_bfloat16* aux;   // residual (EPI_BIAS_RESIDUAL) or Z (EPI_DGELU)
     long long ld_aux;
+    int skip_o0;    // EPI_BIAS_GELU: 1 = H only, Z is not stored (recomputed later)
     Dropout drop;   // EPI_BIAS_RESIDUAL: bias-dropout-add (drop.threshold 0: none)
     float* colsum;  // EPI_DGELU: column sums per 32-row block, [4 * mt_total][ld_colsum]
     long long ld_colsum;
@@ -563,7 +564,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                             for (int i = 0; i < 32; ++i) v[i] += b[i];
                         }
-                        stage_row(buf0 + my_row, half, swz, v);
+                        if (!p.skip_o0) stage_row(buf0 + my_row, half, swz, v);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
                         stage_row(buf1 + my_row, half, swz, v);
@@ -621,7 +622,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (lane == 0) {
                         int c0, c1, c2;
                         tma_coords(p.o_on, n64, row0, tc.s, c0, c1, c2);
-                        tma_store_3d(&tmO0, buf0, c0, c1, c2);
+                        if (EPI != EPI_BIAS_GELU || !p.skip_o0) tma_store_3d(&tmO0, buf0, c0, c1, c2);
                         if constexpr (EPI == EPI_BIAS_GELU) tma_store_3d(&tmO1, buf1, c0, c1, c2);
                         bulk_commit_group();
                     }

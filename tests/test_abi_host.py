@@ -128,3 +128,21 @@ def test_dropout_backward_workspace(L):
     args = [P] * 6 + [T, h, F, t, 0.1, 7, 0] + [P] * 5
     assert L.tp_mlp_backward_dropout(*args, P, need - 1, N) == binding.TPMLP_ERR_WORKSPACE
     assert L.tp_mlp_backward_dropout(*args, N, need, N) == binding.TPMLP_ERR_WORKSPACE
+
+
+def test_recompute_workspace(L):
+    T, h, F, t = 300, 200, 1536, 4
+    fwd_need = L.tp_mlp_forward_recompute_workspace_bytes(T, h, F, t)
+    assert fwd_need >= 2 * T * F                  # H lives in the workspace
+    bwd_need = L.tp_mlp_backward_recompute_workspace_bytes(T, h, F, t)
+    assert bwd_need >= 4 * T * F + L.tp_mlp_backward_workspace_bytes(T, h, F, t)
+    fargs = [P] * 6 + [T, h, F, t, P]
+    assert L.tp_mlp_forward_recompute(*fargs, N, fwd_need, N) == binding.TPMLP_ERR_WORKSPACE
+    assert L.tp_mlp_forward_recompute(*fargs, P, 2 * T * F - 1, N) == binding.TPMLP_ERR_WORKSPACE
+    assert L.tp_mlp_forward_recompute(*fargs, Q, fwd_need, N) == binding.TPMLP_ERR_ALIGN
+    bargs = [P] * 5 + [T, h, F, t] + [P] * 5
+    assert L.tp_mlp_backward_recompute(*bargs, P, bwd_need - 1, N) == binding.TPMLP_ERR_WORKSPACE
+    bargs_nob1 = [P] * 3 + [N, P] + [T, h, F, t] + [P] * 5
+    assert L.tp_mlp_backward_recompute(*bargs_nob1, P, bwd_need, N) == binding.TPMLP_ERR_NULL
+    # Z may be NULL in a2 (H only), H may not
+    assert L.tp_mlp_column_gelu(P, P, P, T, h, F, t, N, N, N) == binding.TPMLP_ERR_NULL
