@@ -1,0 +1,111 @@
+"""Run ONE entry point of the library a few times at a given shape, holding
+only that call's operands on the device -- the command a profiler wraps to
+capture a single kernel of the block at its full per-launch size:
+
+    python -m tensor_transformer_mlp_forward_gb300.profile_call dB \\
+        --T 2048 --h 20480 --F 81920 --t 8 --repeat 4
+
+Operands are seeded device-side normals (the profile depends on shapes, not
+values).  Prints one JSON line with the mean CUDA-event time per call.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import sys
+
+CALLS = ("column_gelu", "column_gelu_h_only", "row_sum", "row_sum_dropout", "dgelu", "dx", "dA",
+         "dB", "dropout_grad", "ln_forward", "ln_backward")
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    p.add_argument("call", choices=CALLS)
+    p.add_argument("--T", type=int, default=2048)
+    p.add_argument("--h", type=int, default=20480)
+    p.add_argument("--F", type=int, default=81920)
+    p.add_argument("--t", type=int, default=8)
+    p.add_argument("--repeat", type=int, default=4)
+    p.add_argument("--dropout", type=float, default=0.1)
+    return p.parse_args(argv)
+
+
+def main(argv=None) -> int:
+    import torch
+
+    from tensor_transformer_mlp_forward_gb300 import binding as b
+
+    a = parse_args(argv)
+    T, h, F, t = a.T, a.h, a.F, a.t
+    dev = torch.device("cuda", 0)
+    gen = torch.Generator(device=dev).manual_seed(1234)
+
+    def bf(*shape, std=1.0):
+        return (torch.randn(*shape, generator=gen, device=dev) * std).to(torch.bfloat16)
+
+    c = a.call
+    if c in ("column_gelu", "column_gelu_h_only"):
+        X, A, b1 = bf(T, h), bf(h, F, std=0.02), bf(F, std=0.02)
+        Z = None if c == "column_gelu_h_only" else bf(T, F)
+        H = bf(T, F)
+        fn = lambda: b.tp_mlp_column_gelu(X, A, b1, t, Z=Z, H=H, want_z=Z is not None)  # noqa: E731
+    elif c in ("row_sum", "row_sum_dropout"):
+        H, B, b2, R, Y = bf(T, F), bf(F, h, std=0.02), bf(h, std=0.02), bf(T, h), bf(T, h)
+        ws = torch.empty(max(16, b.split_workspace_bytes(T, h, F, t)), dtype=torch.uint8, device=dev)
+        if c == "row_sum":
+            fn = lambda: b.tp_mlp_row_sum(H, B, b2, R, t, Y=Y, workspace=ws)  # noqa: E731
+        else:
+            fn = lambda: b.tp_mlp_row_sum_dropout(H, B, b2, R, t, a.dropout, 7, 0, Y=Y,  # noqa: E731
+                                                  workspace=ws)
+    elif c == "dgelu":
+        dY, B, Z, dZ = bf(T, h), bf(F, h, std=0.02), bf(T, F), bf(T, F)
+        db1 = torch.empty(F, device=dev)
+        part = torch.empty(max(1, int(b.lib().tp_mlp_dgelu_partial_floats(T, F))), device=dev)
+        fn = lambda: b.tp_mlp_dgelu(dY, B, Z, t, dZ=dZ, db1=db1, partial=part)  # noqa: E731
+    elif c == "dx":
+        dZ, A, dX = bf(T, F), bf(h, F, std=0.02), bf(T, h)
+        ws = torch.empty(max(16, b.split_workspace_bytes(T, h, F, t)), dtype=torch.uint8, device=dev)
+        fn = lambda: b.tp_mlp_dx(dZ, A, t, dX=dX, workspace=ws)  # noqa: E731
+    elif c == "dA":
+        X, dZ, dA = bf(T, h), bf(T, F), bf(h, F)
+        fn = lambda: b.tp_mlp_dA(X, dZ, t, dA=dA)  # noqa: E731
+    elif c == "dB":
+        H, dY, dB = bf(T, F), bf(T, h), bf(F, h)
+        fn = lambda: b.tp_mlp_dB(H, dY, t, dB=dB)  # noqa: E731
+    elif c == "dropout_grad":
+        dY, dP = bf(T, h), bf(T, h)
+        fn = lambda: b.tp_mlp_dropout_grad(dY, a.dropout, 7, 0, dP=dP)  # noqa: E731
+    else:
+        x, r, gam, bet = bf(T, h), bf(T, h), bf(h, std=0.1), bf(h, std=0.1)
+        X, s = torch.empty_like(x), torch.empty_like(x)
+        mean, rstd = torch.empty(T, device=dev), torch.empty(T, device=dev)
+        b.tp_ln_residual_forward(x, r, gam, bet, 1e-5, X=X, s=s, mean=mean, rstd=rstd)
+        if c == "ln_forward":
+            fn = lambda: b.tp_ln_residual_forward(x, r, gam, bet, 1e-5, X=X, s=s,  # noqa: E731
+                                                  mean=mean, rstd=rstd)
+        else:
+            dX, dres, ds = bf(T, h), bf(T, h), torch.empty_like(x)
+            dg, dbt = torch.empty(h, device=dev), torch.empty(h, device=dev)
+            part = torch.empty(max(1, int(b.lib().tp_ln_residual_backward_workspace_floats(T, h))),
+                               device=dev)
+            fn = lambda: b.tp_ln_residual_backward(dX, dres, x, r, gam, mean, rstd, ds=ds,  # noqa: E731
+                                                   dgamma=dg, dbeta=dbt, partial=part)
+    ms = []
+    for _ in range(a.repeat):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    status = b.device_status()
+    print(json.dumps({"call": c, "T": T, "h": h, "F": F, "t": t, "repeat": a.repeat,
+                      "launches_per_call": b.last_launch_count(),
+                      "ms_mean_after_first": sum(ms[1:]) / max(1, len(ms) - 1), "ms": ms,
+                      "device_status": status}))
+    return 0 if status == 0 else 1
+
+
+if __name__ == "__main__":
+    sys.exit(main())
