@@ -207,17 +207,25 @@ constexpr uint64_t desc_k_step() {
 
 // ------------------------------------------------------------ epilogue math
 
+// tanh GeLU with u(x) = c x (1 + a x^2), c = sqrt(2/pi), a = 0.044715:
+//   GeLU(x)  = 0.5 x (1 + tanh u)
+//   GeLU'(x) = 0.5 (1 + th) + 0.5 x (1 - th^2) u'(x),  th = tanh u,
+// the latter rearranged as 0.5 + w + th (0.5 - w th) with w = 0.5 x u'(x),
+// u'(x) = c (1 + 3 a x^2), to keep the epilogue's instruction count low.
+constexpr float kGeluC = 0.7978845608028654f;
+constexpr float kGeluA = 0.044715f;
+
 __device__ __forceinline__ float gelu_tanh(float x) {
-    const float c = 0.7978845608028654f;  // sqrt(2 / pi)
-    const float u = c * fmaf(0.044715f * x, x * x, x);
-    return 0.5f * x * (1.0f + tanh_approx(u));
+    const float th = tanh_approx(x * fmaf(kGeluC * kGeluA, x * x, kGeluC));
+    const float hx = 0.5f * x;
+    return fmaf(hx, th, hx);
 }
 
 __device__ __forceinline__ float gelu_tanh_grad(float x) {
-    const float c = 0.7978845608028654f;
     const float x2 = x * x;
-    const float th = tanh_approx(c * fmaf(0.044715f * x, x2, x));
-    return 0.5f * (1.0f + th) + 0.5f * x * (1.0f - th * th) * c * fmaf(3.0f * 0.044715f, x2, 1.0f);
+    const float th = tanh_approx(x * fmaf(kGeluC * kGeluA, x2, kGeluC));
+    const float w = x * fmaf(1.5f * kGeluC * kGeluA, x2, 0.5f * kGeluC);
+    return fmaf(th, fmaf(-w, th, 0.5f), 0.5f + w);
 }
 
 // 32 consecutive bf16 values -> float; entries at or beyond `valid` read 0.
@@ -237,6 +245,39 @@ __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* p, int valid, 
     } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = i < valid ? __bfloat162float(p[i]) : 0.0f;
+    }
+}
+
+// Raw bf16 bits of 32 consecutive values (entries at or beyond `valid` are
+// 0), so that the loads can be issued well before the values are needed.
+__device__ __forceinline__ void load_raw32(const __nv_bfloat16* p, int valid, uint4 (&r)[4]) {
+    if (valid >= 32) {
+        const uint4* q = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) r[i] = __ldg(q + i);
+    } else {
+        const unsigned short* e = reinterpret_cast<const unsigned short*>(p);
+        uint32_t w[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const uint32_t lo = 2 * j < valid ? e[2 * j] : 0u;
+            const uint32_t hi = 2 * j + 1 < valid ? e[2 * j + 1] : 0u;
+            w[j] = lo | (hi << 16);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) r[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    }
+}
+
+__device__ __forceinline__ void unpack32(const uint4 (&r)[4], float (&v)[32]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t w[4] = {r[i].x, r[i].y, r[i].z, r[i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
+            v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
     }
 }
 
@@ -491,8 +532,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const TileCoord tc = decode_tile<G::TILE_M>(tile, p);
             const int acc = count & 1;
             const uint32_t acc_phase = (count >> 1) & 1;
-            if (!wait_bounded(&acc_full[acc], acc_phase, abort_flag, p.status)) break;
-            tc_fence_after();
 
             const int m_cta = tc.m0 + static_cast<int>(rank) * BM;  // first row of this CTA
             const int row0 = m_cta + q * 32;                           // first row of this warp
@@ -501,6 +540,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             long long grow = m, gcol0 = tc.n0;
             if (p.shard_mode == SHARD_N) gcol0 += static_cast<long long>(tc.s) * p.N;
             if (p.shard_mode == SHARD_M) grow += static_cast<long long>(tc.s) * p.M;
+            // The row operand of the fused math (Z for GeLU', the residual) does
+            // not depend on the accumulator: its first 32 columns are requested
+            // before the wait, and each 32-column block's loads are issued one
+            // block ahead of their use, so their latency overlaps TMEM reads.
+            constexpr bool kAux = EPI == EPI_DGELU || EPI == EPI_BIAS_RESIDUAL;
+            uint4 aux_cur[4], aux_nxt[4];
+            if constexpr (kAux) {
+                const int v0 = row_ok ? min(32, p.N - tc.n0) : 0;
+                load_raw32(p.aux + grow * p.ld_aux + gcol0, v0, aux_cur);
+            }
+            if (!wait_bounded(&acc_full[acc], acc_phase, abort_flag, p.status)) break;
+            tc_fence_after();
 
             if constexpr (EPI == EPI_PARTIAL) {
                 // fp32 accumulator blocks of 32 rows x 32 columns (128 B rows)
@@ -542,14 +593,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (lane == 0) bulk_wait_group_read<1>();
                 }
                 __syncwarp();  // the buffer's previous store has read it
+                // Both 32-column halves of the block are read from TMEM before
+                // one wait, so each block pays the load latency once.
+                uint32_t r2[2][32];
+                tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + c * 64, r2[0]);
+                tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + c * 64 + 32,
+                          r2[1]);
+                tmem_wait_ld();
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     const int n = n64 + half * 32;
-                    uint32_t r[32];
-                    tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + c * 64 +
-                                  half * 32,
-                              r);
-                    tmem_wait_ld();
+                    if constexpr (kAux) {
+                        if (c * 64 + half * 32 + 32 < BN) {
+                            const int vn = row_ok ? min(32, p.N - (n + 32)) : 0;
+                            load_raw32(p.aux + grow * p.ld_aux + gcol0 + c * 64 + half * 32 + 32, vn,
+                                       aux_nxt);
+                        }
+                    }
+                    const uint32_t(&r)[32] = r2[half];
                     const int cvalid = min(32, p.N - n);  // columns inside the shard
                     const int valid = row_ok ? cvalid : 0;
                     const long long gcol = gcol0 + c * 64 + half * 32;
@@ -572,7 +633,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (valid > 0) {
                             float b[32], res[32];
                             load_bf16x32(p.bias + gcol, valid, b);
-                            load_bf16x32(p.aux + grow * p.ld_aux + gcol, valid, res);
+                            unpack32(aux_cur, res);
                             if (p.drop.threshold == 0u) {
 #pragma unroll
                                 for (int i = 0; i < 32; ++i) v[i] += b[i] + res[i];
@@ -597,10 +658,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         stage_row(buf0 + my_row, half, swz, v);
                     } else if constexpr (EPI == EPI_DGELU) {
                         float z[32];
-                        load_bf16x32(p.aux + grow * p.ld_aux + gcol, valid, z);
+                        unpack32(aux_cur, z);
+                        if (valid >= 32) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            v[i] = i < valid ? v[i] * gelu_tanh_grad(z[i]) : 0.0f;
+                            for (int i = 0; i < 32; ++i) v[i] *= gelu_tanh_grad(z[i]);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                v[i] = i < valid ? v[i] * gelu_tanh_grad(z[i]) : 0.0f;
+                        }
                         stage_row(buf0 + my_row, half, swz, v);
                         // db1 partial: lane l gets column n+l summed over this warp's 32 rows;
                         // one partial row per 32-row block of the shard's rows.
@@ -610,6 +676,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                      gcol + lane] = cs;
                     } else {
                         stage_row(buf0 + my_row, half, swz, v);
+                    }
+                    if constexpr (kAux) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) aux_cur[i] = aux_nxt[i];
                     }
                 }
                 fence_proxy_async_smem();  // staged rows visible to the TMA store
