@@ -58,6 +58,10 @@ class Oracle:
         L.orc_dropout_mask.argtypes = [u64, u64, cl, ctypes.c_double, ctypes.POINTER(ctypes.c_uint8)]
         L.orc_forward_dropout.argtypes = [dp] * 6 + [cl] * 4 + [ctypes.c_double, u64, u64] + [dp] * 3
         L.orc_backward_dropout.argtypes = [dp] * 5 + [cl] * 4 + [ctypes.c_double, u64, u64] + [dp] * 5
+        L.orc_attn_forward.argtypes = [dp] * 6 + [cl] * 5 + [dp] * 3
+        L.orc_attn_backward.argtypes = [dp] * 5 + [cl] * 5 + [dp] * 5
+        L.orc_attn_head_bf16.argtypes = [up] * 3 + [cl] * 5 + [dp]
+        L.orc_attn_head_grads_bf16.argtypes = [up] * 5 + [cl] * 5 + [dp] * 3
         for name in ("orc_dropout_mask", "orc_forward_dropout", "orc_backward_dropout"):
             getattr(L, name).restype = ctypes.c_int
         for name in ("orc_ln_forward", "orc_ln_backward", "orc_forward", "orc_backward", "orc_forward_rows_bf16",
@@ -203,6 +207,52 @@ class Oracle:
                                            _dp(db2)), "backward_dropout")
         return dX, dA, dB, db1, db2
 
+    # ------------------------------------------------ attention block
+
+    def attn_forward(self, X, Wqkv, bqkv, Wo, bo, R, nb: int, nh: int, t: int):
+        """Y, QKV, O of the head-parallel attention block (nb sequences)."""
+        X, Wqkv, bqkv, Wo, bo, R = (_f64(v) for v in (X, Wqkv, bqkv, Wo, bo, R))
+        T, h = X.shape
+        s = T // nb if nb else 0
+        Y, QKV, O = np.zeros((T, h)), np.zeros((T, 3 * h)), np.zeros((T, h))
+        _check(self.L.orc_attn_forward(_dp(X), _dp(Wqkv), _dp(bqkv), _dp(Wo), _dp(bo), _dp(R),
+                                       nb, max(s, 1), h, nh, t, _dp(Y), _dp(QKV), _dp(O)),
+               "attn_forward")
+        return Y, QKV, O
+
+    def attn_backward(self, dY, X, Wqkv, bqkv, Wo, nb: int, nh: int, t: int):
+        """dX, dWqkv, dbqkv, dWo, dbo of the attention block."""
+        dY, X, Wqkv, bqkv, Wo = (_f64(v) for v in (dY, X, Wqkv, bqkv, Wo))
+        T, h = X.shape
+        s = T // nb if nb else 0
+        dX, dWqkv, dbqkv = np.zeros((T, h)), np.zeros((h, 3 * h)), np.zeros(3 * h)
+        dWo, dbo = np.zeros((h, h)), np.zeros(h)
+        _check(self.L.orc_attn_backward(_dp(dY), _dp(X), _dp(Wqkv), _dp(bqkv), _dp(Wo), nb,
+                                        max(s, 1), h, nh, t, _dp(dX), _dp(dWqkv), _dp(dbqkv),
+                                        _dp(dWo), _dp(dbo)), "attn_backward")
+        return dX, dWqkv, dbqkv, dWo, dbo
+
+    def attn_head(self, inp: dict, nb: int, nh: int, j: int) -> np.ndarray:
+        """Head j's attention output O_j [T, d] from bf16 CPU tensors."""
+        X, Wqkv, bqkv = (_u16(inp[k]) for k in ("X", "Wqkv", "bqkv"))
+        T, h = inp["X"].shape
+        d = h // nh
+        Oj = np.zeros((T, d))
+        _check(self.L.orc_attn_head_bf16(_up(X), _up(Wqkv), _up(bqkv), nb, T // nb, h, nh, j,
+                                         _dp(Oj)), "attn_head")
+        return Oj
+
+    def attn_head_grads(self, inp: dict, nb: int, nh: int, j: int):
+        """Head j's dWqkv columns [h, 3d] (Q, K, V), dbqkv [3d], dWo rows [d, h]."""
+        dY, X, Wqkv, bqkv, Wo = (_u16(inp[k]) for k in ("dY", "X", "Wqkv", "bqkv", "Wo"))
+        T, h = inp["X"].shape
+        d = h // nh
+        dW, db, dWo = np.zeros((h, 3 * d)), np.zeros(3 * d), np.zeros((d, h))
+        _check(self.L.orc_attn_head_grads_bf16(_up(dY), _up(X), _up(Wqkv), _up(bqkv), _up(Wo), nb,
+                                               T // nb, h, nh, j, _dp(dW), _dp(db), _dp(dWo)),
+               "attn_head_grads")
+        return dW, db, dWo
+
     def db2(self, dY) -> np.ndarray:
         """Column sums of dY from a bf16 CPU tensor."""
         T, h = dY.shape
@@ -299,6 +349,22 @@ def forward_dropout(*a, **k):
 
 def backward_dropout(*a, **k):
     return default().backward_dropout(*a, **k)
+
+
+def attn_forward(*a, **k):
+    return default().attn_forward(*a, **k)
+
+
+def attn_backward(*a, **k):
+    return default().attn_backward(*a, **k)
+
+
+def attn_head(*a, **k):
+    return default().attn_head(*a, **k)
+
+
+def attn_head_grads(*a, **k):
+    return default().attn_head_grads(*a, **k)
 
 
 def ln_forward(*a, **k):

@@ -602,3 +602,340 @@ int orc_backward_dropout(const double* dY, const double* X, const double* A, con
     free(dP); free(keep);
     return rc;
 }
+
+/* ------------------------------------------------------------------ */
+/* Head-parallel self-attention block                                  */
+/* ------------------------------------------------------------------ */
+/*
+ * "Megatron-LM: Tensor Model Parallel", section "Attention: split Q/K/V by
+ * head" (Figure 3b): the Q, K and V projections are split by columns so that
+ * each rank holds a subset of the heads; a head's scores, softmax and value
+ * sum are computed locally; the output projection is split by rows and its
+ * per-rank partials meet in the g-operator sum before the residual.
+ *
+ * Layout (readings; the page fixes only the split):
+ *  - X, R, Y [T, h] with T = nb sequences of s tokens (token = n s + pos);
+ *  - Wqkv [h, 3h], columns [Q | K | V], head j at columns j d .. j d + d - 1
+ *    of each part, d = h / nh; bqkv [3h] likewise; Wo [h, h] with the rows
+ *    of head j at j d ..; bo [h];
+ *  - shard i owns heads i nh/t .. (i+1) nh/t - 1: their Wqkv columns, bqkv
+ *    entries and Wo rows.
+ * Scores are scaled by 1/sqrt(d) and causal: a token attends to itself and
+ * the earlier tokens of its own sequence (the GPT models of the pages).
+ *
+ *   QKV = X Wqkv + bqkv
+ *   each sequence n, head j:  S = Q_j K_j^T / sqrt(d), masked,
+ *                             P = softmax over each row, O_j = P V_j
+ *   Y = sum_i O_i Wo_i + bo + R
+ * Backward (chain rule of the same formula, forward recomputed from X):
+ *   dbo = sum_rows dY ; dWo_i = O_i^T dY ; dO_i = dY Wo_i^T
+ *   dV = P^T dO_j ; dP = dO_j V_j^T ; dS = P * (dP - rowsum(P * dP))
+ *   dQ = dS K_j / sqrt(d) ; dK = dS^T Q_j / sqrt(d)
+ *   dWqkv = X^T dQKV ; dbqkv = sum_rows dQKV ; dX = sum_i dQKV_i Wqkv_i^T
+ */
+
+static int attn_bad(long nb, long s, long h, long nh, long t) {
+    if (nb < 0 || s < 1 || h < 1 || nh < 1 || t < 1) return 1;
+    if (h % nh != 0 || nh % t != 0) return 1;
+    return 0;
+}
+
+/* One head of one sequence.  q, k, v: s x d with row stride ld; writes the
+ * s x d output o (row stride ldo) and, when P is not NULL, the s x s
+ * probabilities (zero above the diagonal). */
+static void attn_head_forward(const double* q, const double* k, const double* v, long ld,
+                              long s, long d, double* o, long ldo, double* P) {
+    double scale = 1.0 / sqrt((double)d);
+    double* row = (double*)malloc(sizeof(double) * (size_t)s);
+    for (long r = 0; r < s; ++r) {
+        double m = -INFINITY;
+        for (long c = 0; c <= r; ++c) { /* causal: keys 0..r */
+            double acc = 0.0;
+            for (long e = 0; e < d; ++e) acc += q[r * ld + e] * k[c * ld + e];
+            row[c] = acc * scale;
+            if (row[c] > m) m = row[c];
+        }
+        double sum = 0.0;
+        for (long c = 0; c <= r; ++c) {
+            row[c] = exp(row[c] - m);
+            sum += row[c];
+        }
+        for (long c = 0; c <= r; ++c) row[c] /= sum;
+        for (long e = 0; e < d; ++e) {
+            double acc = 0.0;
+            for (long c = 0; c <= r; ++c) acc += row[c] * v[c * ld + e];
+            o[r * ldo + e] = acc;
+        }
+        if (P)
+            for (long c = 0; c < s; ++c) P[r * s + c] = c <= r ? row[c] : 0.0;
+    }
+    free(row);
+}
+
+/* Backward of one head of one sequence: given dO (s x d, stride ldo) writes
+ * dq, dk, dv (s x d, stride ldg). */
+static void attn_head_backward(const double* q, const double* k, const double* v, long ld,
+                               long s, long d, const double* dO, long ldo, double* dq,
+                               double* dk, double* dv, long ldg) {
+    double scale = 1.0 / sqrt((double)d);
+    double* P = (double*)malloc(sizeof(double) * (size_t)(s * s));
+    double* dS = (double*)malloc(sizeof(double) * (size_t)(s * s));
+    double* o = (double*)malloc(sizeof(double) * (size_t)(s * d));
+    attn_head_forward(q, k, v, ld, s, d, o, d, P);
+    for (long r = 0; r < s; ++r) {
+        double D = 0.0;
+        for (long c = 0; c <= r; ++c) {
+            double dp = 0.0;
+            for (long e = 0; e < d; ++e) dp += dO[r * ldo + e] * v[c * ld + e];
+            dS[r * s + c] = dp;
+            D += P[r * s + c] * dp;
+        }
+        for (long c = 0; c < s; ++c)
+            dS[r * s + c] = c <= r ? P[r * s + c] * (dS[r * s + c] - D) : 0.0;
+    }
+    for (long r = 0; r < s; ++r)
+        for (long e = 0; e < d; ++e) {
+            double a = 0.0;
+            for (long c = 0; c <= r; ++c) a += dS[r * s + c] * k[c * ld + e];
+            dq[r * ldg + e] = a * scale;
+        }
+    for (long c = 0; c < s; ++c)
+        for (long e = 0; e < d; ++e) {
+            double a = 0.0, b = 0.0;
+            for (long r = c; r < s; ++r) {
+                a += dS[r * s + c] * q[r * ld + e];
+                b += P[r * s + c] * dO[r * ldo + e];
+            }
+            dk[c * ldg + e] = a * scale;
+            dv[c * ldg + e] = b;
+        }
+    free(P); free(dS); free(o);
+}
+
+/* QKV columns of shard i (its Q, K and V blocks of width h/t): out = X W + b. */
+static void attn_qkv_shard(const double* X, const double* Wqkv, const double* bqkv, long T,
+                           long h, long t, long i, double* QKV) {
+    long w = h / t;
+#pragma omp parallel for schedule(static)
+    for (long r = 0; r < T; ++r)
+        for (long part = 0; part < 3; ++part)
+            for (long c = part * h + i * w; c < part * h + (i + 1) * w; ++c) {
+                double acc = bqkv[c];
+                for (long k = 0; k < h; ++k) acc += X[r * h + k] * Wqkv[k * 3 * h + c];
+                QKV[r * 3 * h + c] = acc;
+            }
+}
+
+/* Attention of shard i's heads for every sequence: O columns of shard i. */
+static void attn_shard_core(const double* QKV, long nb, long s, long h, long nh, long t, long i,
+                            double* O) {
+    long d = h / nh, hs = nh / t;
+#pragma omp parallel for collapse(2) schedule(dynamic)
+    for (long n = 0; n < nb; ++n)
+        for (long jj = 0; jj < hs; ++jj) {
+            long j = i * hs + jj;
+            const double* base = QKV + n * s * 3 * h + j * d;
+            attn_head_forward(base, base + h, base + 2 * h, 3 * h, s, d, O + n * s * h + j * d, h,
+                              NULL);
+        }
+}
+
+int orc_attn_forward(const double* X, const double* Wqkv, const double* bqkv, const double* Wo,
+                     const double* bo, const double* R, long nb, long s, long h, long nh, long t,
+                     double* Y, double* QKV, double* O) {
+    if (attn_bad(nb, s, h, nh, t)) return ORC_ERR_SHAPE;
+    long T = nb * s, w = h / t;
+    for (long e = 0; e < T * h; ++e) Y[e] = 0.0;
+    for (long i = 0; i < t; ++i) {
+        attn_qkv_shard(X, Wqkv, bqkv, T, h, t, i, QKV);
+        attn_shard_core(QKV, nb, s, h, nh, t, i, O);
+        /* the shard's partial of the row-parallel output projection, added
+         * to the running sum (the g operator) */
+#pragma omp parallel for schedule(static)
+        for (long r = 0; r < T; ++r)
+            for (long n = 0; n < h; ++n) {
+                double acc = 0.0;
+                for (long c = i * w; c < (i + 1) * w; ++c) acc += O[r * h + c] * Wo[c * h + n];
+                Y[r * h + n] += acc; /* g: sum of partials */
+            }
+    }
+#pragma omp parallel for schedule(static)
+    for (long r = 0; r < T; ++r)
+        for (long n = 0; n < h; ++n) Y[r * h + n] += bo[n] + R[r * h + n];
+    return ORC_OK;
+}
+
+int orc_attn_backward(const double* dY, const double* X, const double* Wqkv, const double* bqkv,
+                      const double* Wo, long nb, long s, long h, long nh, long t, double* dX,
+                      double* dWqkv, double* dbqkv, double* dWo, double* dbo) {
+    if (attn_bad(nb, s, h, nh, t)) return ORC_ERR_SHAPE;
+    long T = nb * s, w = h / t, d = h / nh, hs = nh / t;
+    double* QKV = (double*)calloc((size_t)(T * 3 * h + 1), sizeof(double));
+    double* O = (double*)calloc((size_t)(T * h + 1), sizeof(double));
+    double* dO = (double*)calloc((size_t)(T * h + 1), sizeof(double));
+    double* dQKV = (double*)calloc((size_t)(T * 3 * h + 1), sizeof(double));
+    if (!QKV || !O || !dO || !dQKV) {
+        free(QKV); free(O); free(dO); free(dQKV);
+        return ORC_ERR_ALLOC;
+    }
+    for (long n = 0; n < h; ++n) {
+        double acc = 0.0;
+        for (long r = 0; r < T; ++r) acc += dY[r * h + n];
+        dbo[n] = acc; /* g backward: the identity */
+    }
+    for (long e = 0; e < T * h; ++e) dX[e] = 0.0;
+    for (long i = 0; i < t; ++i) {
+        attn_qkv_shard(X, Wqkv, bqkv, T, h, t, i, QKV);
+        attn_shard_core(QKV, nb, s, h, nh, t, i, O);
+        /* dO_i = dY Wo_i^T ; dWo_i = O_i^T dY */
+#pragma omp parallel for schedule(static)
+        for (long r = 0; r < T; ++r)
+            for (long c = i * w; c < (i + 1) * w; ++c) {
+                double acc = 0.0;
+                for (long n = 0; n < h; ++n) acc += dY[r * h + n] * Wo[c * h + n];
+                dO[r * h + c] = acc;
+            }
+#pragma omp parallel for schedule(static)
+        for (long c = i * w; c < (i + 1) * w; ++c)
+            for (long n = 0; n < h; ++n) {
+                double acc = 0.0;
+                for (long r = 0; r < T; ++r) acc += O[r * h + c] * dY[r * h + n];
+                dWo[c * h + n] = acc;
+            }
+        /* local attention backward of the shard's heads */
+#pragma omp parallel for collapse(2) schedule(dynamic)
+        for (long n = 0; n < nb; ++n)
+            for (long jj = 0; jj < hs; ++jj) {
+                long j = i * hs + jj;
+                const double* base = QKV + n * s * 3 * h + j * d;
+                double* g = dQKV + n * s * 3 * h + j * d;
+                attn_head_backward(base, base + h, base + 2 * h, 3 * h, s, d,
+                                   dO + n * s * h + j * d, h, g, g + h, g + 2 * h, 3 * h);
+            }
+        /* dWqkv_i = X^T dQKV_i ; dbqkv_i = sum_rows dQKV_i */
+#pragma omp parallel for schedule(static)
+        for (long part = 0; part < 3; ++part)
+            for (long c = part * h + i * w; c < part * h + (i + 1) * w; ++c) {
+                double acc = 0.0;
+                for (long r = 0; r < T; ++r) acc += dQKV[r * 3 * h + c];
+                dbqkv[c] = acc;
+            }
+#pragma omp parallel for schedule(static)
+        for (long k = 0; k < h; ++k)
+            for (long part = 0; part < 3; ++part)
+                for (long c = part * h + i * w; c < part * h + (i + 1) * w; ++c) {
+                    double acc = 0.0;
+                    for (long r = 0; r < T; ++r) acc += X[r * h + k] * dQKV[r * 3 * h + c];
+                    dWqkv[k * 3 * h + c] = acc;
+                }
+        /* dX += dQKV_i Wqkv_i^T : the shard's partial of the f-operator sum */
+#pragma omp parallel for schedule(static)
+        for (long r = 0; r < T; ++r)
+            for (long k = 0; k < h; ++k) {
+                double acc = 0.0;
+                for (long part = 0; part < 3; ++part)
+                    for (long c = part * h + i * w; c < part * h + (i + 1) * w; ++c)
+                        acc += dQKV[r * 3 * h + c] * Wqkv[k * 3 * h + c];
+                dX[r * h + k] += acc; /* f: sum of partials */
+            }
+    }
+    free(QKV); free(O); free(dO); free(dQKV);
+    return ORC_OK;
+}
+
+/* Sampled entry points for full-size workloads: everything of one head j,
+ * from the bf16 inputs.  QKV_j [T, 3d] holds head j's Q, K, V columns. */
+static void attn_head_qkv_bf16(const uint16_t* X, const uint16_t* Wqkv, const uint16_t* bqkv,
+                               long T, long h, long d, long j, double* QKVj) {
+#pragma omp parallel for schedule(static)
+    for (long r = 0; r < T; ++r) {
+        double* out = QKVj + r * 3 * d;
+        for (long part = 0; part < 3; ++part)
+            for (long e = 0; e < d; ++e) out[part * d + e] = w16(bqkv[part * h + j * d + e]);
+        for (long k = 0; k < h; ++k) {
+            double x = w16(X[r * h + k]);
+            const uint16_t* wrow = Wqkv + k * 3 * h + j * d;
+            for (long part = 0; part < 3; ++part)
+                for (long e = 0; e < d; ++e) out[part * d + e] += x * w16(wrow[part * h + e]);
+        }
+    }
+}
+
+/* O_j [T, d]: head j's attention output for every sequence. */
+int orc_attn_head_bf16(const uint16_t* X, const uint16_t* Wqkv, const uint16_t* bqkv, long nb,
+                       long s, long h, long nh, long j, double* Oj) {
+    if (attn_bad(nb, s, h, nh, 1) || j < 0 || j >= nh) return ORC_ERR_SHAPE;
+    long T = nb * s, d = h / nh;
+    double* QKVj = (double*)malloc(sizeof(double) * (size_t)(T * 3 * d + 1));
+    if (!QKVj) return ORC_ERR_ALLOC;
+    attn_head_qkv_bf16(X, Wqkv, bqkv, T, h, d, j, QKVj);
+#pragma omp parallel for schedule(dynamic)
+    for (long n = 0; n < nb; ++n) {
+        const double* base = QKVj + n * s * 3 * d;
+        attn_head_forward(base, base + d, base + 2 * d, 3 * d, s, d, Oj + n * s * d, d, NULL);
+    }
+    free(QKVj);
+    return ORC_OK;
+}
+
+/* Head j's parameter gradients: dWqkv_j [h, 3d] (its Q, K, V columns),
+ * dbqkv_j [3d] and dWo_j [d, h] (its rows of Wo). */
+int orc_attn_head_grads_bf16(const uint16_t* dY, const uint16_t* X, const uint16_t* Wqkv,
+                             const uint16_t* bqkv, const uint16_t* Wo, long nb, long s, long h,
+                             long nh, long j, double* dWqkvj, double* dbqkvj, double* dWoj) {
+    if (attn_bad(nb, s, h, nh, 1) || j < 0 || j >= nh) return ORC_ERR_SHAPE;
+    long T = nb * s, d = h / nh;
+    double* QKVj = (double*)malloc(sizeof(double) * (size_t)(T * 3 * d + 1));
+    double* Oj = (double*)malloc(sizeof(double) * (size_t)(T * d + 1));
+    double* dOj = (double*)malloc(sizeof(double) * (size_t)(T * d + 1));
+    double* G = (double*)malloc(sizeof(double) * (size_t)(T * 3 * d + 1));
+    if (!QKVj || !Oj || !dOj || !G) {
+        free(QKVj); free(Oj); free(dOj); free(G);
+        return ORC_ERR_ALLOC;
+    }
+    attn_head_qkv_bf16(X, Wqkv, bqkv, T, h, d, j, QKVj);
+#pragma omp parallel for schedule(dynamic)
+    for (long n = 0; n < nb; ++n) {
+        const double* base = QKVj + n * s * 3 * d;
+        attn_head_forward(base, base + d, base + 2 * d, 3 * d, s, d, Oj + n * s * d, d, NULL);
+    }
+#pragma omp parallel for schedule(static)
+    for (long r = 0; r < T; ++r)
+        for (long e = 0; e < d; ++e) {
+            double acc = 0.0;
+            for (long n = 0; n < h; ++n) acc += w16(dY[r * h + n]) * w16(Wo[(j * d + e) * h + n]);
+            dOj[r * d + e] = acc;
+        }
+#pragma omp parallel for schedule(static)
+    for (long e = 0; e < d; ++e) {
+        double* out = dWoj + e * h;
+        for (long n = 0; n < h; ++n) out[n] = 0.0;
+        for (long r = 0; r < T; ++r) {
+            double o = Oj[r * d + e];
+            for (long n = 0; n < h; ++n) out[n] += o * w16(dY[r * h + n]);
+        }
+    }
+#pragma omp parallel for schedule(dynamic)
+    for (long n = 0; n < nb; ++n) {
+        const double* base = QKVj + n * s * 3 * d;
+        double* g = G + n * s * 3 * d;
+        attn_head_backward(base, base + d, base + 2 * d, 3 * d, s, d, dOj + n * s * d, d, g,
+                           g + d, g + 2 * d, 3 * d);
+    }
+    for (long c = 0; c < 3 * d; ++c) {
+        double acc = 0.0;
+        for (long r = 0; r < T; ++r) acc += G[r * 3 * d + c];
+        dbqkvj[c] = acc;
+    }
+#pragma omp parallel for schedule(static)
+    for (long k = 0; k < h; ++k) {
+        double* out = dWqkvj + k * 3 * d;
+        for (long c = 0; c < 3 * d; ++c) out[c] = 0.0;
+        for (long r = 0; r < T; ++r) {
+            double x = w16(X[r * h + k]);
+            for (long c = 0; c < 3 * d; ++c) out[c] += x * G[r * 3 * d + c];
+        }
+    }
+    free(QKVj); free(Oj); free(dOj); free(G);
+    return ORC_OK;
+}

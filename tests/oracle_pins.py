@@ -381,6 +381,153 @@ def pin_dropout_backward_fd(o) -> bool:
     return True
 
 
+# ------------------------------------------------------------ attention
+
+def _attn_inputs(nb, s, h, seed, scale_w=0.4):
+    rng = np.random.default_rng(seed)
+    return dict(X=rng.standard_normal((nb * s, h)),
+                Wqkv=scale_w * rng.standard_normal((h, 3 * h)),
+                bqkv=0.1 * rng.standard_normal(3 * h),
+                Wo=scale_w * rng.standard_normal((h, h)),
+                bo=0.1 * rng.standard_normal(h),
+                R=rng.standard_normal((nb * s, h)),
+                dY=rng.standard_normal((nb * s, h)))
+
+
+def _attn_library(p, nb, nh):
+    """The block from numpy float64 matmuls and scipy's softmax over each
+    row's causal prefix: library routines composed by the definition."""
+    from scipy.special import softmax
+
+    T, h = p["X"].shape
+    s, d = T // nb, h // nh
+    QKV = p["X"] @ p["Wqkv"] + p["bqkv"]
+    O = np.zeros((T, h))
+    for n in range(nb):
+        rows = slice(n * s, (n + 1) * s)
+        for j in range(nh):
+            q = QKV[rows, j * d:(j + 1) * d]
+            k = QKV[rows, h + j * d:h + (j + 1) * d]
+            v = QKV[rows, 2 * h + j * d:2 * h + (j + 1) * d]
+            S = q @ k.T / math.sqrt(d)
+            for r in range(s):
+                pr = softmax(S[r, :r + 1])
+                O[n * s + r, j * d:(j + 1) * d] = pr @ v[:r + 1]
+    return O @ p["Wo"] + p["bo"] + p["R"], QKV, O
+
+
+def pin_attn_vs_library(o) -> bool:
+    ok = True
+    for nb, s, h, nh, t in ((2, 5, 8, 2, 2), (1, 7, 12, 3, 3), (3, 1, 4, 1, 1), (0, 4, 8, 2, 1)):
+        p = _attn_inputs(nb, s, h, 60 + s)
+        Y, QKV, O = o.attn_forward(p["X"], p["Wqkv"], p["bqkv"], p["Wo"], p["bo"], p["R"], nb, nh, t)
+        Yl, QKVl, Ol = _attn_library(p, nb, nh) if nb else (np.zeros((0, h)),) * 3
+        ok &= _rel(Y, Yl) < 1e-12 and _rel(O, Ol) < 1e-12 and _rel(QKV, QKVl) < 1e-12
+    return bool(ok)
+
+
+def pin_attn_closed_forms(o) -> bool:
+    """One token per sequence: each row attends only to itself, so
+    O = V = X Wv + bv.  Zero query weights: every score is 0 and each row
+    averages the values of its prefix (a running mean)."""
+    nb, s, h, nh = 3, 1, 8, 2
+    p = _attn_inputs(nb, s, h, 71)
+    Y, _, O = o.attn_forward(p["X"], p["Wqkv"], p["bqkv"], p["Wo"], p["bo"], p["R"], nb, nh, 2)
+    V = p["X"] @ p["Wqkv"][:, 2 * h:] + p["bqkv"][2 * h:]
+    ok = _rel(O, V) < 1e-13 and _rel(Y, V @ p["Wo"] + p["bo"] + p["R"]) < 1e-13
+    nb, s = 2, 6
+    p = _attn_inputs(nb, s, h, 72)
+    p["Wqkv"][:, :h] = 0.0
+    p["bqkv"][:h] = 0.0
+    _, QKV, O = o.attn_forward(p["X"], p["Wqkv"], p["bqkv"], p["Wo"], p["bo"], p["R"], nb, nh, 1)
+    V = QKV[:, 2 * h:].reshape(nb, s, h)
+    mean = np.cumsum(V, axis=1) / np.arange(1, s + 1)[None, :, None]
+    return bool(ok and _rel(O, mean.reshape(nb * s, h)) < 1e-13)
+
+
+def pin_attn_invariants(o) -> bool:
+    """Causality, independence of the sequences, and the key bias: adding
+    the same vector to every key shifts each score row by a constant, which
+    softmax ignores, so Y and the other gradients do not see bk and its
+    gradient vanishes."""
+    nb, s, h, nh = 2, 5, 8, 2
+    p = _attn_inputs(nb, s, h, 73)
+    args = lambda q: (q["X"], q["Wqkv"], q["bqkv"], q["Wo"], q["bo"], q["R"], nb, nh, 2)  # noqa: E731
+    Y0, _, _ = o.attn_forward(*args(p))
+    q = {k: v.copy() for k, v in p.items()}
+    q["X"][3:5] += 1.7             # tokens 3, 4 of sequence 0 and nothing else
+    Y1, _, _ = o.attn_forward(*args(q))
+    ok = np.array_equal(Y0[:3], Y1[:3]) and np.array_equal(Y0[5:], Y1[5:]) and not np.allclose(Y0[3:5], Y1[3:5])
+    q = {k: v.copy() for k, v in p.items()}
+    q["bqkv"][h:2 * h] += 0.9      # the key bias
+    Y2, _, _ = o.attn_forward(*args(q))
+    ok &= _rel(Y2, Y0) < 1e-13
+    g = o.attn_backward(p["dY"], p["X"], p["Wqkv"], p["bqkv"], p["Wo"], nb, nh, 2)
+    ok &= float(np.max(np.abs(g[2][h:2 * h]))) < 1e-12 * max(1.0, float(np.max(np.abs(g[2]))))
+    return bool(ok)
+
+
+def pin_attn_partition_invariant(o) -> bool:
+    nb, s, h, nh = 2, 4, 16, 4
+    p = _attn_inputs(nb, s, h, 74)
+    base = None
+    for t in (1, 2, 4):
+        out = o.attn_forward(p["X"], p["Wqkv"], p["bqkv"], p["Wo"], p["bo"], p["R"], nb, nh, t)[:1] + \
+            o.attn_backward(p["dY"], p["X"], p["Wqkv"], p["bqkv"], p["Wo"], nb, nh, t)
+        if base is None:
+            base = out
+        elif not all(_rel(a, b) < 1e-12 for a, b in zip(out, base)):
+            return False
+    return True
+
+
+def pin_attn_gradients_fd(o) -> bool:
+    """dX, dWqkv, dbqkv, dWo, dbo against central differences of <dY, Y>."""
+    nb, s, h, nh, t = 2, 3, 4, 2, 2
+    p = _attn_inputs(nb, s, h, 75)
+
+    def loss(q):
+        Y, _, _ = o.attn_forward(q["X"], q["Wqkv"], q["bqkv"], q["Wo"], q["bo"], q["R"], nb, nh, t)
+        return float(np.sum(p["dY"] * Y))
+
+    grads = o.attn_backward(p["dY"], p["X"], p["Wqkv"], p["bqkv"], p["Wo"], nb, nh, t)
+    eps = 1e-6
+    for key, an in zip(("X", "Wqkv", "bqkv", "Wo", "bo"), grads):
+        fd = np.zeros_like(p[key])
+        it = np.nditer(p[key], flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            q = {k: v.copy() for k, v in p.items()}
+            q[key][idx] += eps
+            lp = loss(q)
+            q[key][idx] -= 2 * eps
+            fd[idx] = (lp - loss(q)) / (2 * eps)
+        if _rel(an, fd) > 1e-6:
+            return False
+    return True
+
+
+def pin_attn_sampled_matches_full(o) -> bool:
+    """The per-head entry points (bf16 inputs) against the full block."""
+    nb, s, h, nh, t = 2, 6, 16, 4, 2
+    rng = np.random.default_rng(76)
+    bf = lambda *sh: torch.from_numpy(0.5 * rng.standard_normal(sh)).to(torch.bfloat16)  # noqa: E731
+    inp = dict(X=bf(nb * s, h), Wqkv=bf(h, 3 * h), bqkv=bf(3 * h), Wo=bf(h, h), bo=bf(h),
+               R=bf(nb * s, h), dY=bf(nb * s, h))
+    f = {k: v.double().numpy() for k, v in inp.items()}
+    _, _, O = o.attn_forward(f["X"], f["Wqkv"], f["bqkv"], f["Wo"], f["bo"], f["R"], nb, nh, t)
+    dX, dW, db, dWo, dbo = o.attn_backward(f["dY"], f["X"], f["Wqkv"], f["bqkv"], f["Wo"], nb, nh, t)
+    d = h // nh
+    ok = True
+    for j in range(nh):
+        cols = np.r_[j * d:(j + 1) * d, h + j * d:h + (j + 1) * d, 2 * h + j * d:2 * h + (j + 1) * d]
+        ok &= _rel(o.attn_head(inp, nb, nh, j), O[:, j * d:(j + 1) * d]) < 1e-13
+        gW, gb, gWo = o.attn_head_grads(inp, nb, nh, j)
+        ok &= _rel(gW, dW[:, cols]) < 1e-12 and _rel(gb, db[cols]) < 1e-12
+        ok &= _rel(gWo, dWo[j * d:(j + 1) * d]) < 1e-12
+    return bool(ok)
+
+
 ALL_PINS = [
     pin_gelu_identities,
     pin_gelu_asymptotes,
@@ -400,6 +547,12 @@ ALL_PINS = [
     pin_dropout_mask,
     pin_dropout_forward,
     pin_dropout_backward_fd,
+    pin_attn_vs_library,
+    pin_attn_closed_forms,
+    pin_attn_invariants,
+    pin_attn_partition_invariant,
+    pin_attn_gradients_fd,
+    pin_attn_sampled_matches_full,
 ]
 
 

@@ -61,6 +61,18 @@ MUTANTS = {
     "dropout_no_rescale": ("Y[e] = R[e] + (keep[e] ? Y[e] / (1.0 - p) : 0.0);", "Y[e] = R[e] + (keep[e] ? Y[e] : 0.0);"),
     "dropout_bwd_ignores_mask": ("dP[e] = keep[e] ? dY[e] / (1.0 - p) : 0.0;", "dP[e] = dY[e] / (1.0 - p);"),
     "dropout_counter_word": ("keep[e] = w[g & 3] >= thr ? 1 : 0;", "keep[e] = w[0] >= thr ? 1 : 0;"),
+    "attn_no_score_scale": ("row[c] = acc * scale;", "row[c] = acc;"),
+    "attn_mask_open": ("c <= r; ++c) { /* causal: keys 0..r */", "c < s; ++c) { /* causal: keys 0..r */"),
+    "attn_dS_drops_rowsum": ("P[r * s + c] * (dS[r * s + c] - D)", "P[r * s + c] * dS[r * s + c]"),
+    "attn_dK_no_scale": ("dk[c * ldg + e] = a * scale;", "dk[c * ldg + e] = a;"),
+    "attn_dV_uses_dS": ("b += P[r * s + c] * dO[r * ldo + e];", "b += dS[r * s + c] * dO[r * ldo + e];"),
+    "attn_g_sum_overwrites": ("Y[r * h + n] += acc; /* g: sum of partials */", "Y[r * h + n] = acc;"),
+    "attn_f_sum_overwrites": ("dX[r * h + k] += acc; /* f: sum of partials */", "dX[r * h + k] = acc;"),
+    "attn_bo_dropped": ("Y[r * h + n] += bo[n] + R[r * h + n];", "Y[r * h + n] += R[r * h + n];"),
+    "attn_k_v_swapped": ("attn_head_forward(base, base + h, base + 2 * h, 3 * h, s, d, O + n * s * h + j * d, h,",
+                         "attn_head_forward(base, base + 2 * h, base + h, 3 * h, s, d, O + n * s * h + j * d, h,"),
+    "attn_head_wrong_part_stride": ("out[part * d + e] += x * w16(wrow[part * h + e]);",
+                                    "out[part * d + e] += x * w16(wrow[part * d + e]);"),
     "db2_drops_last_row": ("for (long r = 0; r < T; ++r) s += w16(dY[r * h + n]);",
                            "for (long r = 0; r + 1 < T; ++r) s += w16(dY[r * h + n]);"),
 }
