@@ -333,6 +333,90 @@ int tp_mlp_backward_dropout(const tpmlp_bf16* dY, const tpmlp_bf16* X, const tpm
                             float* db2, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------- */
+/* Head-parallel self-attention block                                      */
+/* ---------------------------------------------------------------------- */
+
+/* "Megatron-LM: Tensor Model Parallel" (charles2530.github.io), section
+ * "Attention: split Q/K/V by head" (Figure 3b): the Q, K and V projections
+ * are split by columns so that each rank owns nh / t of the nh heads; each
+ * head's scores, softmax and value sum are local; the output projection is
+ * split by rows, and its per-rank partials meet in the g-operator sum before
+ * the residual add:
+ *
+ *   QKV = X Wqkv + bqkv                            (column-parallel)
+ *   per sequence and head j:  S = Q_j K_j^T / sqrt(d), causal mask,
+ *                             P = softmax over each row, O_j = P V_j
+ *   Y   = sum_i O_i Wo_i + bo + residual           (row-parallel, g sum)
+ *
+ * Layout: nb sequences of s tokens, T = nb * s, token n * s + pos;
+ * X, residual, Y, O [T, h]; QKV [T, 3h] with columns [Q | K | V] and head j
+ * at columns j*d .. j*d + d - 1 of each part (d = h / nh); Wqkv [h, 3h],
+ * bqkv [3h], Wo [h, h] (head j's rows at j*d), bo [h]; lse float32 [nh, T].
+ * Shard i owns heads i*nh/t .. (i+1)*nh/t - 1: their Wqkv columns, bqkv
+ * entries and Wo rows.  The mask is causal within a sequence (a token sees
+ * itself and the earlier tokens of its sequence), as in the pages' GPT
+ * models; the page fixes only the split, the rest is the plain reading.
+ *
+ * Rules (else TPMLP_ERR_SHAPE): nb >= 0, s >= 1, h % 8 == 0, nh >= 1,
+ * h % nh == 0, d = h / nh in {64, 96, 128} (the head dims with a compiled
+ * kernel: GPT-2 355M, 2.5B and 8.3B of the page's Table 2), 1 <= t <= 64,
+ * nh % t == 0, T < 2^31.  nb == 0 is an empty batch.  Pointers, ownership,
+ * streams and status codes as for the MLP block above. */
+
+/* QKV = X Wqkv + bqkv (bf16 out, fp32 accumulation): the column-parallel
+ * projection of every shard as one GEMM (no sum crosses its columns).
+ * Rules T >= 0, h % 8 == 0, h >= 8. */
+int tp_attn_qkv(const tpmlp_bf16* X, const tpmlp_bf16* Wqkv, const tpmlp_bf16* bqkv, int T, int h,
+                tpmlp_bf16* QKV, void* stream);
+
+/* Causal attention of every (sequence, head) from QKV: O [T, h] (bf16) and
+ * lse [nh, T] (float32), lse = log2 sum_k 2^(c q.k) over the visible keys
+ * with c = log2(e) / sqrt(d), saved for the backward pass. */
+int tp_attn_core_forward(const tpmlp_bf16* QKV, int nb, int s, int h, int nh, tpmlp_bf16* O,
+                         float* lse, void* stream);
+
+/* Backward of tp_attn_core_forward given dO [T, h]: dQKV [T, 3h] (bf16;
+ * dQ, dK, dV in the layout of QKV).  delta [nh, T] float32 is scratch
+ * (rowsum(dO * O) per head).  Every gradient is written once, in a fixed
+ * summation order, with no atomics, so results are reproducible. */
+int tp_attn_core_backward(const tpmlp_bf16* QKV, const tpmlp_bf16* O, const float* lse,
+                          const tpmlp_bf16* dO, int nb, int s, int h, int nh, tpmlp_bf16* dQKV,
+                          float* delta, void* stream);
+
+/* Optional scratch of tp_attn_forward: lets the output projection split its
+ * reduction when its output tiles cannot occupy the GPU (0 if never). */
+size_t tp_attn_forward_workspace_bytes(int nb, int s, int h, int nh, int t);
+
+/* The block's forward pass: tp_attn_qkv, tp_attn_core_forward, then the
+ * row-parallel output projection (tp_mlp_row_sum with F = h: Y = sum_i O_i
+ * Wo_i + bo + residual, the g sum folded into one fp32 accumulator).  QKV, O
+ * and lse are outputs saved for the backward pass.  workspace may be NULL. */
+int tp_attn_forward(const tpmlp_bf16* X, const tpmlp_bf16* Wqkv, const tpmlp_bf16* bqkv,
+                    const tpmlp_bf16* Wo, const tpmlp_bf16* bo, const tpmlp_bf16* residual,
+                    int nb, int s, int h, int nh, int t, tpmlp_bf16* Y, tpmlp_bf16* QKV,
+                    tpmlp_bf16* O, float* lse, void* workspace, size_t workspace_bytes,
+                    void* stream);
+
+/* Bytes of scratch tp_attn_backward needs: dO [T,h] bf16, delta [nh,T] f32,
+ * dQKV [T,3h] bf16, column-sum partials, split-reduction partials. */
+size_t tp_attn_backward_workspace_bytes(int nb, int s, int h, int nh, int t);
+
+/* The block's backward pass (chain rule of the forward formula):
+ *   dbo = sum_rows dY ; dWo_i = O_i^T dY ; dO_i = dY Wo_i^T ;
+ *   attention backward -> dQKV ; dbqkv = sum_rows dQKV ;
+ *   dWqkv = X^T dQKV ; dX = sum_i dQKV_i Wqkv_i^T (the f-operator sum, one
+ *   fp32 accumulation over all 3h columns).
+ * dX is the gradient through the block; the residual's gradient is dY
+ * itself and is not written.  dX, dWqkv, dWo bf16; dbqkv, dbo float32.
+ * workspace must hold tp_attn_backward_workspace_bytes (it may be NULL when
+ * nb == 0, in which case the parameter gradients are zeroed). */
+int tp_attn_backward(const tpmlp_bf16* dY, const tpmlp_bf16* X, const tpmlp_bf16* Wqkv,
+                     const tpmlp_bf16* Wo, const tpmlp_bf16* QKV, const tpmlp_bf16* O,
+                     const float* lse, int nb, int s, int h, int nh, int t, tpmlp_bf16* dX,
+                     tpmlp_bf16* dWqkv, float* dbqkv, tpmlp_bf16* dWo, float* dbo,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------- */
 /* Status                                                                  */
 /* ---------------------------------------------------------------------- */
 
@@ -360,6 +444,13 @@ int tpmlp_last_cuda_error(void);
  * last read.  Synchronises the device. Returns TPMLP_ERR_LAUNCH if the read
  * itself fails. */
 int tpmlp_device_status(void);
+
+/* Reads and clears the site code of the first bounded wait that gave up on
+ * the current device since the last read: 0 if none; otherwise a code that
+ * names the kernel and the wait (0x1nn attention forward, 0x2nn attention dQ,
+ * 0x3nn attention dK/dV; the GEMM kernels record none).  Synchronises the
+ * device.  A failed read returns minus the status code. */
+int tpmlp_device_wait_site(void);
 
 /* Number of kernels the last successful call on the calling thread
  * launched (for launch accounting). */

@@ -75,9 +75,17 @@ _SIGNATURES = {
     "tp_ln_residual_forward": ([_P] * 4 + [_I, _I, ctypes.c_float] + [_P] * 4 + [_P], _I),
     "tp_ln_residual_backward_workspace_floats": ([_I, _I], _S),
     "tp_ln_residual_backward": ([_P] * 7 + [_I, _I] + [_P] * 4 + [_P], _I),
+    "tp_attn_qkv": ([_P] * 3 + [_I] * 2 + [_P, _P], _I),
+    "tp_attn_core_forward": ([_P] + [_I] * 4 + [_P] * 2 + [_P], _I),
+    "tp_attn_core_backward": ([_P] * 4 + [_I] * 4 + [_P] * 2 + [_P], _I),
+    "tp_attn_forward_workspace_bytes": ([_I] * 5, _S),
+    "tp_attn_forward": ([_P] * 6 + [_I] * 5 + [_P] * 4 + [_P, _S, _P], _I),
+    "tp_attn_backward_workspace_bytes": ([_I] * 5, _S),
+    "tp_attn_backward": ([_P] * 7 + [_I] * 5 + [_P] * 5 + [_P, _S, _P], _I),
     "tpmlp_status_string": ([_I], ctypes.c_char_p),
     "tpmlp_last_cuda_error": ([], _I),
     "tpmlp_device_status": ([], _I),
+    "tpmlp_device_wait_site": ([], _I),
     "tpmlp_last_launch_count": ([], _I),
     "tpmlp_selftest_bounded_wait": ([_I, _P], _I),
     "tpmlp_set_cta_pair_mode": ([_I], _I),
@@ -165,6 +173,11 @@ def set_cta_pair_mode(mode: int) -> int:
 
 def device_status() -> int:
     return int(lib().tpmlp_device_status())
+
+
+def device_wait_site() -> int:
+    """Site code of the first device wait that gave up since the last read."""
+    return int(lib().tpmlp_device_wait_site())
 
 
 def tp_mlp_column_gelu(X, A, b1, t: int, Z=None, H=None, stream=None, want_z=True):
@@ -466,3 +479,99 @@ def selftest_bounded_wait(timeout_us: int, stream=None) -> int:
     _check("tpmlp_selftest_bounded_wait",
            lib().tpmlp_selftest_bounded_wait(timeout_us, _stream(stream)))
     return device_status()
+
+
+# ------------------------------------------------------------ attention block
+
+def tp_attn_qkv(X, Wqkv, bqkv, QKV=None, stream=None):
+    """QKV = X Wqkv + bqkv: [T, 3h] with columns [Q | K | V]."""
+    T, h = X.shape
+    QKV = _out(QKV, (T, 3 * h), X)
+    _check("tp_attn_qkv", lib().tp_attn_qkv(
+        _ptr(X, "X", (T, h)) if T else None, _ptr(Wqkv, "Wqkv", (h, 3 * h)),
+        _ptr(bqkv, "bqkv", (3 * h,)), T, h, _ptr(QKV, "QKV", (T, 3 * h)) if T else None,
+        _stream(stream)))
+    return QKV
+
+
+def tp_attn_core_forward(QKV, nb: int, nh: int, O=None, lse=None, stream=None):
+    """O [T, h] (bf16) and lse [nh, T] (float32, log2 domain) of causal
+    attention over nb sequences of T / nb tokens."""
+    T, h3 = QKV.shape
+    h = h3 // 3
+    s = T // nb if nb else 1
+    O = _out(O, (T, h), QKV)
+    lse = _out(lse, (nh, T), QKV, torch.float32)
+    _check("tp_attn_core_forward", lib().tp_attn_core_forward(
+        _ptr(QKV, "QKV", (T, 3 * h)) if T else None, nb, s, h, nh,
+        _ptr(O, "O", (T, h)) if T else None, _ptr(lse, "lse", (nh, T), torch.float32) if T else None,
+        _stream(stream)))
+    return O, lse
+
+
+def tp_attn_core_backward(QKV, O, lse, dO, nb: int, nh: int, dQKV=None, delta=None, stream=None):
+    """dQKV [T, 3h] of causal attention given dO; delta [nh, T] is scratch."""
+    T, h3 = QKV.shape
+    h = h3 // 3
+    s = T // nb if nb else 1
+    dQKV = _out(dQKV, (T, 3 * h), QKV)
+    delta = _out(delta, (nh, T), QKV, torch.float32)
+    _check("tp_attn_core_backward", lib().tp_attn_core_backward(
+        _ptr(QKV, "QKV", (T, 3 * h)), _ptr(O, "O", (T, h)),
+        _ptr(lse, "lse", (nh, T), torch.float32), _ptr(dO, "dO", (T, h)), nb, s, h, nh,
+        _ptr(dQKV, "dQKV", (T, 3 * h)), _ptr(delta, "delta", (nh, T), torch.float32),
+        _stream(stream)))
+    return dQKV
+
+
+def tp_attn_forward(X, Wqkv, bqkv, Wo, bo, residual, nb: int, nh: int, t: int, Y=None, QKV=None,
+                    O=None, lse=None, workspace=None, stream=None):
+    """Y of the head-parallel attention block, with QKV, O, lse saved for the
+    backward pass."""
+    T, h = X.shape
+    s = T // nb if nb else 1
+    Y = _out(Y, (T, h), X)
+    QKV = _out(QKV, (T, 3 * h), X)
+    O = _out(O, (T, h), X)
+    lse = _out(lse, (nh, T), X, torch.float32)
+    wp, wn = _workspace(workspace, int(lib().tp_attn_forward_workspace_bytes(nb, s, h, nh, t)), X)
+    nz = T > 0
+    _check("tp_attn_forward", lib().tp_attn_forward(
+        _ptr(X, "X", (T, h)) if nz else None, _ptr(Wqkv, "Wqkv", (h, 3 * h)),
+        _ptr(bqkv, "bqkv", (3 * h,)), _ptr(Wo, "Wo", (h, h)), _ptr(bo, "bo", (h,)),
+        _ptr(residual, "residual", (T, h)) if nz else None, nb, s, h, nh, t,
+        _ptr(Y, "Y", (T, h)) if nz else None, _ptr(QKV, "QKV", (T, 3 * h)) if nz else None,
+        _ptr(O, "O", (T, h)) if nz else None,
+        _ptr(lse, "lse", (nh, T), torch.float32) if nz else None, wp, wn, _stream(stream)))
+    return Y, QKV, O, lse
+
+
+def tp_attn_backward_workspace_bytes(nb: int, s: int, h: int, nh: int, t: int) -> int:
+    return int(lib().tp_attn_backward_workspace_bytes(nb, s, h, nh, t))
+
+
+def tp_attn_backward(dY, X, Wqkv, Wo, QKV, O, lse, nb: int, nh: int, t: int, dX=None, dWqkv=None,
+                     dbqkv=None, dWo=None, dbo=None, workspace=None, stream=None):
+    """dX, dWqkv, dWo (bf16) and dbqkv, dbo (float32) of the attention block
+    (dX is the gradient through the block; the residual's is dY)."""
+    T, h = X.shape
+    s = T // nb if nb else 1
+    dX = _out(dX, (T, h), X)
+    dWqkv = _out(dWqkv, (h, 3 * h), X)
+    dbqkv = _out(dbqkv, (3 * h,), X, torch.float32)
+    dWo = _out(dWo, (h, h), X)
+    dbo = _out(dbo, (h,), X, torch.float32)
+    need = tp_attn_backward_workspace_bytes(nb, s, h, nh, t)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=X.device)
+    nz = T > 0
+    _check("tp_attn_backward", lib().tp_attn_backward(
+        _ptr(dY, "dY", (T, h)) if nz else None, _ptr(X, "X", (T, h)) if nz else None,
+        _ptr(Wqkv, "Wqkv", (h, 3 * h)), _ptr(Wo, "Wo", (h, h)),
+        _ptr(QKV, "QKV", (T, 3 * h)) if nz else None, _ptr(O, "O", (T, h)) if nz else None,
+        _ptr(lse, "lse", (nh, T), torch.float32) if nz else None, nb, s, h, nh, t,
+        _ptr(dX, "dX", (T, h)) if nz else None, _ptr(dWqkv, "dWqkv", (h, 3 * h)),
+        _ptr(dbqkv, "dbqkv", (3 * h,), torch.float32), _ptr(dWo, "dWo", (h, h)),
+        _ptr(dbo, "dbo", (h,), torch.float32),
+        _ptr(workspace, "workspace", None, torch.uint8), workspace.numel(), _stream(stream)))
+    return dX, dWqkv, dbqkv, dWo, dbo

@@ -1,0 +1,1038 @@
+// attention.cu -- the core of the head-parallel self-attention block on
+// tcgen05 tensor cores: causal softmax attention of every (sequence, head),
+// forward and backward.
+//
+// "Megatron-LM: Tensor Model Parallel" (charles2530.github.io), section
+// "Attention: split Q/K/V by head" (Figure 3b): the Q, K and V projections
+// are split by columns so that each rank owns a group of heads, and each
+// head's scores, softmax and value sum are computed where the head lives.
+// On one GPU every head of every shard is one CTA's work; the shard count
+// only decides which rank a head would belong to and changes nothing here.
+//
+// Layout: QKV [T, 3h] bf16 (row = token n*s + pos; columns [Q | K | V], head
+// j at columns j*d .. j*d+d-1 of each part), O and dO [T, h], dQKV [T, 3h],
+// lse and delta fp32 [nh, T].  Scores are scaled by 1/sqrt(d) and causal
+// (a token sees itself and the earlier tokens of its own sequence).
+//
+//   S = Q_j K_j^T / sqrt(d) (masked) ; P = softmax_rows(S) ; O_j = P V_j
+//   backward: dV = P^T dO ; dP = dO V^T ; dS = P * (dP - delta),
+//             delta = rowsum(dO * O) ; dQ = dS K / sqrt(d) ; dK = dS^T Q / sqrt(d)
+//
+// The softmax runs in the log2 domain: with c = log2(e)/sqrt(d) each score is
+// taken as u = c * (q . k), P = 2^(u - m) / l, and lse = m + log2(l) is saved
+// per (head, token) so that the backward pass rebuilds P = 2^(u - lse) without
+// a second normalisation pass.
+//
+// Kernels (warps 0-3 do the softmax, one query or key row per thread and TMEM
+// lane; warp 4 is the TMA producer; warp 5 allocates TMEM and issues the
+// MMAs from one thread):
+//   attn_fwd_kernel     one CTA per (128 queries, head, sequence); 128-key
+//                       tiles; S double-buffered in TMEM so that S of the next
+//                       tile is computed while this one is softmaxed; P goes
+//                       through shared memory (K-major, 128-byte swizzle) into
+//                       the P V product, whose fp32 result the softmax threads
+//                       fold into a register-resident output row.
+//   attn_delta_kernel   delta = rowsum(dO * O) per (token, head).
+//   attn_bwd_dq_kernel  one CTA per (128 queries, head, sequence); 64-key
+//                       tiles: S and dP (TMEM, double-buffered), dS through
+//                       shared memory, dQ accumulated in TMEM.
+//   attn_bwd_dkdv_kernel one CTA per (128 keys, head, sequence); 64-query
+//                       tiles: S^T and dP^T (TMEM, double-buffered), P^T and
+//                       dS^T through shared memory, dV and dK accumulated in
+//                       TMEM.
+// dQ and dK/dV are separate kernels so that every gradient is written once,
+// in a fixed summation order, with no atomics.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "kernels.h"
+
+namespace tpmlp {
+namespace {
+
+constexpr int kAttnThreads = 192;
+constexpr int kRowBytes = 128;  // one 64-column bf16 box row (the swizzle width)
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float lg2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Byte offset of UMMA k-step kk (16 elements) inside a K-major operand tile
+// of R rows stored as 64-column boxes (R x 128 B each): box kk/4, 32 B a step.
+template <int R>
+__device__ __forceinline__ uint32_t kmajor_step(int kk) {
+    return static_cast<uint32_t>((kk >> 2) * (R * kRowBytes) + (kk & 3) * 32);
+}
+
+// Byte offset of UMMA k-step kk of an MN-major operand whose K runs along the
+// box rows: 16 rows of 128 B.
+__device__ __forceinline__ uint32_t mnmajor_step(int kk) {
+    return static_cast<uint32_t>(kk * 16 * kRowBytes);
+}
+
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+
+// tcgen05 MMA chain D (+)= A B^T where B is MN-major along d (the value or
+// query/key tile as the N operand, N = D): the N extent is issued as a
+// multiple of 64 (whole swizzle atoms) plus a 32-wide tail, so that no MMA
+// spans part of an atom.  `box_bytes` is the stride of the 64-wide atoms.
+// A is K-major with its 64-column boxes `a_box_bytes` apart.
+template <int D, int KSTEPS>
+__device__ __forceinline__ void mma_n_is_d(uint32_t d_tmem, uint64_t a_desc, uint32_t a_box_bytes,
+                                           uint64_t b_desc, uint32_t box_bytes,
+                                           bool accumulate_first) {
+    constexpr int N1 = (D / 64) * 64;
+    constexpr int N2 = D - N1;
+    constexpr uint32_t id1 = idesc_bf16_f32(128, N1 > 0 ? N1 : 64, false, true);
+    constexpr uint32_t id2 = idesc_bf16_f32(128, N2 > 0 ? N2 : 32, false, true);
+#pragma unroll
+    for (int kk = 0; kk < KSTEPS; ++kk) {
+        const uint32_t acc = (accumulate_first || kk > 0) ? 1u : 0u;
+        const uint32_t aoff = static_cast<uint32_t>((kk >> 2) * a_box_bytes + (kk & 3) * 32);
+        const uint64_t ad = desc_add(a_desc, aoff);
+        const uint64_t bd = desc_add(b_desc, mnmajor_step(kk));
+        if constexpr (N1 > 0) tc_mma_f16(d_tmem, ad, bd, id1, acc);
+        if constexpr (N2 > 0)
+            tc_mma_f16(d_tmem + N1, ad, desc_add(bd, (N1 / 64) * box_bytes), id2, acc);
+    }
+}
+
+// ---------------------------------------------------------------- forward
+
+template <int D>
+struct FwdCfg {
+    static constexpr int NB = (D + 63) / 64;           // 64-column boxes per row
+    static constexpr int TILE = NB * 128 * kRowBytes;  // 128 rows x D (box-padded)
+    static constexpr int P_BYTES = 2 * 128 * kRowBytes;  // 128 x 128 bf16
+    static constexpr int STAGES_FIT = (225 * 1024 - TILE - P_BYTES) / TILE;
+    static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
+    static constexpr int SMEM = 1024 + TILE + P_BYTES + STAGES * TILE + 256;
+};
+
+struct AttnArgs {
+    int nb, s, h, nh;
+    long long T;
+    int q_tiles;     // tiles along the sequence of this kernel's row dimension
+    float scale2;    // log2(e) / sqrt(d)
+    float scale;     // 1 / sqrt(d)
+    __nv_bfloat16* O;        // forward output [T, h]
+    float* lse;              // forward output [nh, T]
+    const float* lse_in;     // backward input [nh, T]
+    const float* delta;      // backward input [nh, T]
+    __nv_bfloat16* dqkv;     // backward output [T, 3h]
+    int* status;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const AttnArgs a) {
+    using C = FwdCfg<D>;
+    constexpr int S = C::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    uint8_t* sQ = smem;
+    uint8_t* sP = smem + C::TILE;
+    uint8_t* ring = sP + C::P_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(ring + S * C::TILE);
+    uint64_t* q_full = bars;
+    uint64_t* kv_full = bars + 1;
+    uint64_t* kv_empty = kv_full + S;
+    uint64_t* s_full = kv_empty + S;  // 2
+    uint64_t* p_full = s_full + 2;
+    uint64_t* pv_done = p_full + 1;
+    uint64_t* drain = pv_done + 1;
+    uint32_t* misc = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile uint32_t* abort_flag = misc + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // heaviest query tiles (most key tiles) first
+    const int per_qt = a.nb * a.nh;
+    const int qt = a.q_tiles - 1 - static_cast<int>(blockIdx.x) / per_qt;
+    const int rem = static_cast<int>(blockIdx.x) % per_qt;
+    const int n = rem / a.nh, head = rem % a.nh;
+    const int q0 = qt * 128;
+    const int n_kv = qt + 1;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&kv_full[i], 1);
+            mbar_init(&kv_empty[i], 1);
+        }
+        mbar_init(&s_full[0], 1);
+        mbar_init(&s_full[1], 1);
+        mbar_init(p_full, 4);  // one arrival per softmax warp
+        mbar_init(pv_done, 1);
+        mbar_init(drain, 1);
+        misc[1] = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(&misc[0], 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+    constexpr uint32_t kS0 = 0, kPV = 256;
+
+    if (warp == 4) {
+        if (lane == 0) {
+            prefetch_tmap(&tm_qkv);
+            const int qcol = head * D, kcol = a.h + head * D, vcol = 2 * a.h + head * D;
+            mbar_arrive_expect_tx(q_full, C::TILE);
+            for (int b = 0; b < C::NB; ++b)
+                tma_load_3d(&tm_qkv, smem_u32(q_full), smem_u32(sQ) + b * 128 * kRowBytes,
+                            qcol + 64 * b, q0, n);
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, issued_phase = 0;
+            bool ok = true;
+            auto load = [&](int col, int row) {
+                if (!ok) return;
+                if (!wait_bounded(&kv_empty[stage], phase ^ 1u, abort_flag, a.status, 0x101)) {
+                    ok = false;
+                    return;
+                }
+                mbar_arrive_expect_tx(&kv_full[stage], C::TILE);
+                const uint32_t dst = smem_u32(ring) + stage * C::TILE;
+                for (int b = 0; b < C::NB; ++b)
+                    tma_load_3d(&tm_qkv, smem_u32(&kv_full[stage]), dst + b * 128 * kRowBytes,
+                                col + 64 * b, row, n);
+                issued |= 1u << stage;
+                issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            };
+            // the order the MMAs consume them: K0, K1, V0, K2, V1, ..., V_last
+            load(kcol, 0);
+            for (int j = 1; j < n_kv; ++j) {
+                load(kcol, j * 128);
+                load(vcol, (j - 1) * 128);
+            }
+            load(vcol, (n_kv - 1) * 128);
+            wait_drain(q_full, 0, a.status, 0x102);
+            for (int i = 0; i < S; ++i)
+                if (issued & (1u << i)) wait_drain(&kv_full[i], (issued_phase >> i) & 1u, a.status, 0x103);
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        if (lane == 0) {
+            constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
+            const uint64_t qdesc = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+            const uint64_t pdesc = smem_desc_sw128(smem_u32(sP), 16, 1024);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = wait_bounded(q_full, 0, abort_flag, a.status, 0x104);
+            tc_fence_after();
+            auto next = [&]() {
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            };
+            auto issue_pv = [&](int i) {
+                if (!ok) return;
+                if (!wait_bounded(p_full, static_cast<uint32_t>(i) & 1u, abort_flag, a.status, 0x105) ||
+                    !wait_bounded(&kv_full[stage], phase, abort_flag, a.status, 0x106)) {
+                    ok = false;
+                    return;
+                }
+                tc_fence_after();
+                const uint64_t vdesc =
+                    smem_desc_sw128(smem_u32(ring) + stage * C::TILE, 128 * kRowBytes, 1024);
+                // O_part = P V: A = P (K-major, keys along the 128-byte rows), B = V
+                // (MN-major: d along the rows, keys down the box)
+                mma_n_is_d<D, 128 / 16>(tmem + kPV, pdesc, 128 * kRowBytes, vdesc,
+                                        128 * kRowBytes, false);
+                tc_commit(pv_done);
+                tc_commit(&kv_empty[stage]);
+                next();
+            };
+            for (int j = 0; j < n_kv && ok; ++j) {
+                if (!wait_bounded(&kv_full[stage], phase, abort_flag, a.status, 0x107)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t kdesc = smem_desc_sw128(smem_u32(ring) + stage * C::TILE, 16, 1024);
+                const uint32_t d_s = tmem + kS0 + (j & 1) * 128;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    tc_mma_f16(d_s, desc_add(qdesc, kmajor_step<128>(kk)),
+                               desc_add(kdesc, kmajor_step<128>(kk)), id_s, kk > 0 ? 1u : 0u);
+                tc_commit(&s_full[j & 1]);
+                tc_commit(&kv_empty[stage]);
+                next();
+                if (j >= 1) issue_pv(j - 1);
+            }
+            issue_pv(n_kv - 1);
+            tc_commit(drain);
+            wait_drain(drain, 0, a.status, 0x108);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ softmax warps
+        const int r = threadIdx.x;  // row of the tile = TMEM lane
+        const int q = q0 + r;
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const uint32_t p_row = smem_u32(sP) + static_cast<uint32_t>(r) * kRowBytes;
+        const uint32_t swz = static_cast<uint32_t>(r & 7);
+        float o[D];
+#pragma unroll
+        for (int i = 0; i < D; ++i) o[i] = 0.0f;
+        float m = -INFINITY, l = 0.0f, alpha_prev = 0.0f;
+        bool ok = true;
+        auto fold = [&](float alpha) {
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(lane_addr + kPV + c * 32, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[c * 32 + i] = fmaf(o[c * 32 + i], alpha, __uint_as_float(v[i]));
+            }
+        };
+        for (int j = 0; j < n_kv; ++j) {
+            if (!warp_wait_bounded(&s_full[j & 1], static_cast<uint32_t>(j >> 1) & 1u, abort_flag,
+                                   a.status, 0x109)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t s_addr = lane_addr + kS0 + (j & 1) * 128;
+            const bool diag = j == qt;  // keys k0 + c with c > r are masked there
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                tmem_ld32(s_addr + c * 32, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (!diag || c * 32 + i <= r) mx = fmaxf(mx, __uint_as_float(v[i]));
+            }
+            const float m_new = fmaxf(m, mx * a.scale2);
+            const float alpha = ex2(m - m_new);
+            if (j >= 1) {
+                if (!warp_wait_bounded(pv_done, static_cast<uint32_t>(j - 1) & 1u, abort_flag, a.status,
+                                       0x10A)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                fold(alpha_prev);
+            }
+            float rs = 0.0f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                tmem_ld32(s_addr + c * 32, v);
+                tmem_wait_ld();
+                float p[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const bool valid = !diag || c * 32 + i <= r;
+                    p[i] = valid ? ex2(fmaf(__uint_as_float(v[i]), a.scale2, -m_new)) : 0.0f;
+                    rs += p[i];
+                }
+                stage_row(p_row + (c >> 1) * 128 * kRowBytes, c & 1, swz, p);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
+            l = fmaf(l, alpha, rs);
+            m = m_new;
+            alpha_prev = alpha;
+        }
+        if (ok && warp_wait_bounded(pv_done, static_cast<uint32_t>(n_kv - 1) & 1u, abort_flag,
+                                    a.status, 0x10B)) {
+            tc_fence_after();
+            fold(alpha_prev);
+            if (q < a.s) {
+                const float inv = 1.0f / l;
+                const long long tok = static_cast<long long>(n) * a.s + q;
+                uint4* dst = reinterpret_cast<uint4*>(a.O + tok * a.h + head * D);
+#pragma unroll
+                for (int i = 0; i < D / 8; ++i) {
+                    uint4 u;
+                    u.x = pack_bf16x2(o[8 * i] * inv, o[8 * i + 1] * inv);
+                    u.y = pack_bf16x2(o[8 * i + 2] * inv, o[8 * i + 3] * inv);
+                    u.z = pack_bf16x2(o[8 * i + 4] * inv, o[8 * i + 5] * inv);
+                    u.w = pack_bf16x2(o[8 * i + 6] * inv, o[8 * i + 7] * inv);
+                    dst[i] = u;
+                }
+                a.lse[head * a.T + tok] = m + lg2(l);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------------ delta
+
+// delta[head, tok] = sum_c dO[tok, head*d + c] * O[tok, head*d + c], fp32;
+// one thread per (token, head).
+__global__ void __launch_bounds__(256)
+    attn_delta_kernel(const __nv_bfloat16* __restrict__ dO, const __nv_bfloat16* __restrict__ O,
+                      long long T, int h, int nh, int d, float* __restrict__ delta) {
+    const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= T * nh) return;
+    const long long tok = idx / nh;
+    const int head = static_cast<int>(idx - tok * nh);
+    const uint4* g = reinterpret_cast<const uint4*>(dO + tok * h + head * d);
+    const uint4* o = reinterpret_cast<const uint4*>(O + tok * h + head * d);
+    float acc = 0.0f;
+    for (int i = 0; i < d / 8; ++i) {
+        const uint4 gu = __ldg(g + i), ou = __ldg(o + i);
+        const uint32_t gw[4] = {gu.x, gu.y, gu.z, gu.w}, ow[4] = {ou.x, ou.y, ou.z, ou.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            acc = fmaf(__uint_as_float(gw[j] << 16), __uint_as_float(ow[j] << 16), acc);
+            acc = fmaf(__uint_as_float(gw[j] & 0xFFFF0000u), __uint_as_float(ow[j] & 0xFFFF0000u), acc);
+        }
+    }
+    delta[static_cast<long long>(head) * T + tok] = acc;
+}
+
+// ------------------------------------------------------------- dQ
+
+template <int D>
+struct DqCfg {
+    static constexpr int NB = (D + 63) / 64;
+    static constexpr int ROW_TILE = NB * 128 * kRowBytes;  // Q or dO: 128 rows
+    static constexpr int KV_TILE = NB * 64 * kRowBytes;    // K or V: 64 rows
+    static constexpr int DS_BYTES = 128 * kRowBytes;       // 128 x 64 bf16
+    static constexpr int FIXED = 2 * ROW_TILE + 2 * DS_BYTES;
+    static constexpr int STAGES_FIT = (225 * 1024 - FIXED) / (2 * KV_TILE);
+    static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
+    static constexpr int SMEM = 1024 + FIXED + STAGES * 2 * KV_TILE + 256;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q128,  // QKV, 128-row boxes
+                       const __grid_constant__ CUtensorMap tm_kv64,  // QKV, 64-row boxes
+                       const __grid_constant__ CUtensorMap tm_do128, // dO, 128-row boxes
+                       const AttnArgs a) {
+    using C = DqCfg<D>;
+    constexpr int S = C::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    uint8_t* sQ = smem;
+    uint8_t* sdO = sQ + C::ROW_TILE;
+    uint8_t* sdS = sdO + C::ROW_TILE;  // 2 buffers
+    uint8_t* ring = sdS + 2 * C::DS_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(ring + S * 2 * C::KV_TILE);
+    uint64_t* q_full = bars;
+    uint64_t* kv_full = bars + 1;
+    uint64_t* kv_empty = kv_full + S;
+    uint64_t* sdp_full = kv_empty + S;  // 2
+    uint64_t* ds_full = sdp_full + 2;   // 2
+    uint64_t* ds_free = ds_full + 2;    // 2
+    uint64_t* dq_done = ds_free + 2;
+    uint64_t* drain = dq_done + 1;
+    uint32_t* misc = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile uint32_t* abort_flag = misc + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int per_qt = a.nb * a.nh;
+    const int qt = a.q_tiles - 1 - static_cast<int>(blockIdx.x) / per_qt;
+    const int rem = static_cast<int>(blockIdx.x) % per_qt;
+    const int n = rem / a.nh, head = rem % a.nh;
+    const int q0 = qt * 128;
+    // 64-key tiles holding keys <= the tile's last valid query
+    const int last_q = min(q0 + 127, a.s - 1);
+    const int n_kv = last_q / 64 + 1;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&kv_full[i], 1);
+            mbar_init(&kv_empty[i], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sdp_full[b], 1);
+            mbar_init(&ds_full[b], 4);
+            mbar_init(&ds_free[b], 1);
+        }
+        mbar_init(dq_done, 1);
+        mbar_init(drain, 1);
+        misc[1] = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(&misc[0], 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+    // TMEM columns: S[b] at 64 b, dP[b] at 128 + 64 b, dQ at 256
+    constexpr uint32_t kS = 0, kDP = 128, kDQ = 256;
+
+    if (warp == 4) {
+        if (lane == 0) {
+            prefetch_tmap(&tm_q128);
+            prefetch_tmap(&tm_kv64);
+            prefetch_tmap(&tm_do128);
+            const int qcol = head * D, kcol = a.h + head * D, vcol = 2 * a.h + head * D;
+            mbar_arrive_expect_tx(q_full, 2 * C::ROW_TILE);
+            for (int b = 0; b < C::NB; ++b) {
+                tma_load_3d(&tm_q128, smem_u32(q_full), smem_u32(sQ) + b * 128 * kRowBytes,
+                            qcol + 64 * b, q0, n);
+                tma_load_3d(&tm_do128, smem_u32(q_full), smem_u32(sdO) + b * 128 * kRowBytes,
+                            qcol + 64 * b, q0, n);
+            }
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, issued_phase = 0;
+            for (int j = 0; j < n_kv; ++j) {
+                if (!wait_bounded(&kv_empty[stage], phase ^ 1u, abort_flag, a.status, 0x201)) break;
+                mbar_arrive_expect_tx(&kv_full[stage], 2 * C::KV_TILE);
+                const uint32_t dst = smem_u32(ring) + stage * 2 * C::KV_TILE;
+                for (int b = 0; b < C::NB; ++b) {
+                    tma_load_3d(&tm_kv64, smem_u32(&kv_full[stage]), dst + b * 64 * kRowBytes,
+                                kcol + 64 * b, j * 64, n);
+                    tma_load_3d(&tm_kv64, smem_u32(&kv_full[stage]),
+                                dst + C::KV_TILE + b * 64 * kRowBytes, vcol + 64 * b, j * 64, n);
+                }
+                issued |= 1u << stage;
+                issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            wait_drain(q_full, 0, a.status, 0x202);
+            for (int i = 0; i < S; ++i)
+                if (issued & (1u << i)) wait_drain(&kv_full[i], (issued_phase >> i) & 1u, a.status, 0x203);
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        if (lane == 0) {
+            constexpr uint32_t id_s = idesc_bf16_f32(128, 64, false, false);
+            const uint64_t qdesc = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+            const uint64_t dodesc = smem_desc_sw128(smem_u32(sdO), 16, 1024);
+            int stage = 0, prev_stage = 0;
+            uint32_t phase = 0;
+            bool ok = wait_bounded(q_full, 0, abort_flag, a.status, 0x204);
+            tc_fence_after();
+            auto issue_dq = [&](int i, int st) {
+                if (!ok) return;
+                if (!wait_bounded(&ds_full[i & 1], static_cast<uint32_t>(i >> 1) & 1u, abort_flag,
+                                  a.status, 0x205)) {
+                    ok = false;
+                    return;
+                }
+                tc_fence_after();
+                // dQ += dS K: A = dS (K-major, keys along the rows), B = K
+                // (MN-major: d along the rows, keys down the 64-row box)
+                const uint64_t dsdesc =
+                    smem_desc_sw128(smem_u32(sdS) + (i & 1) * C::DS_BYTES, 16, 1024);
+                const uint64_t kdesc = smem_desc_sw128(smem_u32(ring) + st * 2 * C::KV_TILE,
+                                                       64 * kRowBytes, 1024);
+                mma_n_is_d<D, 64 / 16>(tmem + kDQ, dsdesc, 128 * kRowBytes, kdesc,
+                                       64 * kRowBytes, i > 0);
+                tc_commit(&ds_free[i & 1]);
+                tc_commit(&kv_empty[st]);
+            };
+            for (int j = 0; j < n_kv && ok; ++j) {
+                if (!wait_bounded(&kv_full[stage], phase, abort_flag, a.status, 0x206)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t kv = smem_u32(ring) + stage * 2 * C::KV_TILE;
+                const uint64_t kdesc = smem_desc_sw128(kv, 16, 1024);
+                const uint64_t vdesc = smem_desc_sw128(kv + C::KV_TILE, 16, 1024);
+                const uint32_t b = static_cast<uint32_t>(j & 1);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    tc_mma_f16(tmem + kS + 64 * b, desc_add(qdesc, kmajor_step<128>(kk)),
+                               desc_add(kdesc, kmajor_step<64>(kk)), id_s, kk > 0 ? 1u : 0u);
+                    tc_mma_f16(tmem + kDP + 64 * b, desc_add(dodesc, kmajor_step<128>(kk)),
+                               desc_add(vdesc, kmajor_step<64>(kk)), id_s, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(&sdp_full[b]);
+                if (j >= 1) issue_dq(j - 1, prev_stage);
+                prev_stage = stage;
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            issue_dq(n_kv - 1, prev_stage);
+            tc_commit(dq_done);
+            tc_commit(drain);
+            wait_drain(drain, 0, a.status, 0x207);
+        }
+        __syncwarp();
+    } else {
+        const int r = threadIdx.x;
+        const int q = q0 + r;
+        const bool q_ok = q < a.s;
+        const long long tok = static_cast<long long>(n) * a.s + q;
+        const float lse = q_ok ? __ldg(a.lse_in + head * a.T + tok) : 0.0f;
+        const float dlt = q_ok ? __ldg(a.delta + head * a.T + tok) : 0.0f;
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const uint32_t swz = static_cast<uint32_t>(r & 7);
+        bool ok = true;
+        for (int j = 0; j < n_kv; ++j) {
+            const uint32_t b = static_cast<uint32_t>(j & 1);
+            if (!warp_wait_bounded(&sdp_full[b], static_cast<uint32_t>(j >> 1) & 1u, abort_flag,
+                                   a.status, 0x208) ||
+                (j >= 2 && !warp_wait_bounded(&ds_free[b], static_cast<uint32_t>((j >> 1) - 1) & 1u,
+                                              abort_flag, a.status, 0x209))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t ds_row = smem_u32(sdS) + b * C::DS_BYTES + static_cast<uint32_t>(r) * kRowBytes;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t sv[32], pv[32];
+                tmem_ld32(lane_addr + kS + 64 * b + c * 32, sv);
+                tmem_ld32(lane_addr + kDP + 64 * b + c * 32, pv);
+                tmem_wait_ld();
+                float ds[32];
+                const int key0 = j * 64 + c * 32;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const bool valid = q_ok && key0 + i <= q;
+                    const float p = valid ? ex2(fmaf(__uint_as_float(sv[i]), a.scale2, -lse)) : 0.0f;
+                    ds[i] = p * (__uint_as_float(pv[i]) - dlt);
+                }
+                stage_row(ds_row, c, swz, ds);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ds_full[b]);
+        }
+        if (ok && warp_wait_bounded(dq_done, 0, abort_flag, a.status, 0x20A)) {
+            tc_fence_after();
+            // tcgen05.ld is warp-collective (.sync.aligned): every lane loads,
+            // only rows inside the sequence are stored
+            uint4* dst = reinterpret_cast<uint4*>(a.dqkv + tok * 3 * a.h + head * D);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(lane_addr + kDQ + c * 32, v);
+                tmem_wait_ld();
+                if (q_ok) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint4 u;
+                        u.x = pack_bf16x2(__uint_as_float(v[8 * i]) * a.scale, __uint_as_float(v[8 * i + 1]) * a.scale);
+                        u.y = pack_bf16x2(__uint_as_float(v[8 * i + 2]) * a.scale, __uint_as_float(v[8 * i + 3]) * a.scale);
+                        u.z = pack_bf16x2(__uint_as_float(v[8 * i + 4]) * a.scale, __uint_as_float(v[8 * i + 5]) * a.scale);
+                        u.w = pack_bf16x2(__uint_as_float(v[8 * i + 6]) * a.scale, __uint_as_float(v[8 * i + 7]) * a.scale);
+                        dst[c * 4 + i] = u;
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ---------------------------------------------------------- dK, dV
+
+template <int D>
+struct DkvCfg {
+    static constexpr int NB = (D + 63) / 64;
+    static constexpr int KEY_TILE = NB * 128 * kRowBytes;  // K or V: 128 rows
+    static constexpr int Q_TILE = NB * 64 * kRowBytes;     // Q or dO: 64 rows
+    static constexpr int PT_BYTES = 128 * kRowBytes;       // 128 keys x 64 queries
+    static constexpr int FIXED = 2 * KEY_TILE + 4 * PT_BYTES;  // P^T and dS^T, 2 each
+    static constexpr int STAGES_FIT = (225 * 1024 - FIXED) / (2 * Q_TILE);
+    static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
+    static constexpr int SMEM = 1024 + FIXED + STAGES * 2 * Q_TILE + 256;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k128,  // QKV, 128-row boxes
+                         const __grid_constant__ CUtensorMap tm_q64,    // QKV, 64-row boxes
+                         const __grid_constant__ CUtensorMap tm_do64,   // dO, 64-row boxes
+                         const AttnArgs a) {
+    using C = DkvCfg<D>;
+    constexpr int S = C::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    uint8_t* sK = smem;
+    uint8_t* sV = sK + C::KEY_TILE;
+    uint8_t* sPT = sV + C::KEY_TILE;       // 2 buffers
+    uint8_t* sdST = sPT + 2 * C::PT_BYTES;  // 2 buffers
+    uint8_t* ring = sdST + 2 * C::PT_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(ring + S * 2 * C::Q_TILE);
+    uint64_t* kv_full = bars;
+    uint64_t* q_full = bars + 1;
+    uint64_t* q_empty = q_full + S;
+    uint64_t* st_full = q_empty + S;  // 2
+    uint64_t* pds_full = st_full + 2;  // 2
+    uint64_t* pds_free = pds_full + 2;  // 2
+    uint64_t* grad_done = pds_free + 2;
+    uint64_t* drain = grad_done + 1;
+    uint32_t* misc = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile uint32_t* abort_flag = misc + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // key tiles with the fewest queries after them are the lightest: the
+    // first key tiles (most queries) go first
+    const int per_kt = a.nb * a.nh;
+    const int kt = static_cast<int>(blockIdx.x) / per_kt;
+    const int rem = static_cast<int>(blockIdx.x) % per_kt;
+    const int n = rem / a.nh, head = rem % a.nh;
+    const int k0 = kt * 128;
+    const int i0 = k0 / 64;                  // first 64-query tile with a query >= k0
+    const int nq = (a.s + 63) / 64 - i0;     // query tiles to visit
+
+    if (threadIdx.x == 0) {
+        mbar_init(kv_full, 1);
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&q_full[i], 1);
+            mbar_init(&q_empty[i], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&st_full[b], 1);
+            mbar_init(&pds_full[b], 4);
+            mbar_init(&pds_free[b], 1);
+        }
+        mbar_init(grad_done, 1);
+        mbar_init(drain, 1);
+        misc[1] = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(&misc[0], 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+    // TMEM columns: S^T[b] at 64 b, dP^T[b] at 128 + 64 b, dV at 256, dK at the
+    // next multiple of 64 after dV (every accumulator starts on a 64-column step)
+    constexpr uint32_t kST = 0, kDPT = 128, kDV = 256, kDK = 256 + ((D + 63) / 64) * 64;
+
+    if (warp == 4) {
+        if (lane == 0) {
+            prefetch_tmap(&tm_k128);
+            prefetch_tmap(&tm_q64);
+            prefetch_tmap(&tm_do64);
+            const int qcol = head * D, kcol = a.h + head * D, vcol = 2 * a.h + head * D;
+            mbar_arrive_expect_tx(kv_full, 2 * C::KEY_TILE);
+            for (int b = 0; b < C::NB; ++b) {
+                tma_load_3d(&tm_k128, smem_u32(kv_full), smem_u32(sK) + b * 128 * kRowBytes,
+                            kcol + 64 * b, k0, n);
+                tma_load_3d(&tm_k128, smem_u32(kv_full), smem_u32(sV) + b * 128 * kRowBytes,
+                            vcol + 64 * b, k0, n);
+            }
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, issued_phase = 0;
+            for (int i = 0; i < nq; ++i) {
+                if (!wait_bounded(&q_empty[stage], phase ^ 1u, abort_flag, a.status, 0x301)) break;
+                mbar_arrive_expect_tx(&q_full[stage], 2 * C::Q_TILE);
+                const uint32_t dst = smem_u32(ring) + stage * 2 * C::Q_TILE;
+                const int qrow = (i0 + i) * 64;
+                for (int b = 0; b < C::NB; ++b) {
+                    tma_load_3d(&tm_q64, smem_u32(&q_full[stage]), dst + b * 64 * kRowBytes,
+                                qcol + 64 * b, qrow, n);
+                    tma_load_3d(&tm_do64, smem_u32(&q_full[stage]),
+                                dst + C::Q_TILE + b * 64 * kRowBytes, qcol + 64 * b, qrow, n);
+                }
+                issued |= 1u << stage;
+                issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            wait_drain(kv_full, 0, a.status, 0x302);
+            for (int i = 0; i < S; ++i)
+                if (issued & (1u << i)) wait_drain(&q_full[i], (issued_phase >> i) & 1u, a.status, 0x303);
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        if (lane == 0) {
+            constexpr uint32_t id_st = idesc_bf16_f32(128, 64, false, false);
+            const uint64_t kdesc = smem_desc_sw128(smem_u32(sK), 16, 1024);
+            const uint64_t vdesc = smem_desc_sw128(smem_u32(sV), 16, 1024);
+            int stage = 0, prev_stage = 0;
+            uint32_t phase = 0;
+            bool ok = wait_bounded(kv_full, 0, abort_flag, a.status, 0x304);
+            tc_fence_after();
+            auto issue_grads = [&](int i, int st) {
+                if (!ok) return;
+                if (!wait_bounded(&pds_full[i & 1], static_cast<uint32_t>(i >> 1) & 1u, abort_flag,
+                                  a.status, 0x305)) {
+                    ok = false;
+                    return;
+                }
+                tc_fence_after();
+                const uint32_t qd = smem_u32(ring) + st * 2 * C::Q_TILE;
+                // dV += P^T dO and dK += dS^T Q: A = P^T / dS^T (K-major, queries
+                // along the rows), B = dO / Q (MN-major: d along the rows,
+                // queries down the 64-row box)
+                const uint64_t ptdesc = smem_desc_sw128(smem_u32(sPT) + (i & 1) * C::PT_BYTES, 16, 1024);
+                const uint64_t dstdesc = smem_desc_sw128(smem_u32(sdST) + (i & 1) * C::PT_BYTES, 16, 1024);
+                const uint64_t dodesc = smem_desc_sw128(qd + C::Q_TILE, 64 * kRowBytes, 1024);
+                const uint64_t qdesc = smem_desc_sw128(qd, 64 * kRowBytes, 1024);
+                mma_n_is_d<D, 64 / 16>(tmem + kDV, ptdesc, 128 * kRowBytes, dodesc,
+                                       64 * kRowBytes, i > 0);
+                mma_n_is_d<D, 64 / 16>(tmem + kDK, dstdesc, 128 * kRowBytes, qdesc,
+                                       64 * kRowBytes, i > 0);
+                tc_commit(&pds_free[i & 1]);
+                tc_commit(&q_empty[st]);
+            };
+            for (int i = 0; i < nq && ok; ++i) {
+                if (!wait_bounded(&q_full[stage], phase, abort_flag, a.status, 0x306)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t qd = smem_u32(ring) + stage * 2 * C::Q_TILE;
+                const uint64_t qdesc = smem_desc_sw128(qd, 16, 1024);
+                const uint64_t dodesc = smem_desc_sw128(qd + C::Q_TILE, 16, 1024);
+                const uint32_t b = static_cast<uint32_t>(i & 1);
+                // S^T = K Q^T and dP^T = V dO^T (M = 128 keys, N = 64 queries, K = d)
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    tc_mma_f16(tmem + kST + 64 * b, desc_add(kdesc, kmajor_step<128>(kk)),
+                               desc_add(qdesc, kmajor_step<64>(kk)), id_st, kk > 0 ? 1u : 0u);
+                    tc_mma_f16(tmem + kDPT + 64 * b, desc_add(vdesc, kmajor_step<128>(kk)),
+                               desc_add(dodesc, kmajor_step<64>(kk)), id_st, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(&st_full[b]);
+                if (i >= 1) issue_grads(i - 1, prev_stage);
+                prev_stage = stage;
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            issue_grads(nq - 1, prev_stage);
+            tc_commit(grad_done);
+            tc_commit(drain);
+            wait_drain(drain, 0, a.status, 0x307);
+        }
+        __syncwarp();
+    } else {
+        const int r = threadIdx.x;
+        const int key = k0 + r;
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const uint32_t swz = static_cast<uint32_t>(r & 7);
+        const float* lse_seq = a.lse_in + head * a.T + static_cast<long long>(n) * a.s;
+        const float* dlt_seq = a.delta + head * a.T + static_cast<long long>(n) * a.s;
+        const bool vec_ok = ((reinterpret_cast<uintptr_t>(lse_seq) | reinterpret_cast<uintptr_t>(dlt_seq)) & 15u) == 0;
+        bool ok = true;
+        for (int i = 0; i < nq; ++i) {
+            const uint32_t b = static_cast<uint32_t>(i & 1);
+            if (!warp_wait_bounded(&st_full[b], static_cast<uint32_t>(i >> 1) & 1u, abort_flag,
+                                   a.status, 0x308) ||
+                (i >= 2 && !warp_wait_bounded(&pds_free[b], static_cast<uint32_t>((i >> 1) - 1) & 1u,
+                                              abort_flag, a.status, 0x309))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t pt_row = smem_u32(sPT) + b * C::PT_BYTES + static_cast<uint32_t>(r) * kRowBytes;
+            const uint32_t dst_row = smem_u32(sdST) + b * C::PT_BYTES + static_cast<uint32_t>(r) * kRowBytes;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int qa = (i0 + i) * 64 + c * 32;  // first query of this chunk
+                float lse[32], dlt[32];
+                if (vec_ok && qa + 32 <= a.s) {
+                    const float4* l4 = reinterpret_cast<const float4*>(lse_seq + qa);
+                    const float4* d4 = reinterpret_cast<const float4*>(dlt_seq + qa);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        const float4 x = __ldg(l4 + v), y = __ldg(d4 + v);
+                        lse[4 * v] = x.x; lse[4 * v + 1] = x.y; lse[4 * v + 2] = x.z; lse[4 * v + 3] = x.w;
+                        dlt[4 * v] = y.x; dlt[4 * v + 1] = y.y; dlt[4 * v + 2] = y.z; dlt[4 * v + 3] = y.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int v = 0; v < 32; ++v) {
+                        const bool in = qa + v < a.s;
+                        lse[v] = in ? __ldg(lse_seq + qa + v) : INFINITY;
+                        dlt[v] = in ? __ldg(dlt_seq + qa + v) : 0.0f;
+                    }
+                }
+                uint32_t sv[32], pv[32];
+                tmem_ld32(lane_addr + kST + 64 * b + c * 32, sv);
+                tmem_ld32(lane_addr + kDPT + 64 * b + c * 32, pv);
+                tmem_wait_ld();
+                float p[32], ds[32];
+#pragma unroll
+                for (int v = 0; v < 32; ++v) {
+                    const bool valid = qa + v >= key && qa + v < a.s;
+                    p[v] = valid ? ex2(fmaf(__uint_as_float(sv[v]), a.scale2, -lse[v])) : 0.0f;
+                    ds[v] = p[v] * (__uint_as_float(pv[v]) - dlt[v]);
+                }
+                stage_row(pt_row, c, swz, p);
+                stage_row(dst_row, c, swz, ds);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pds_full[b]);
+        }
+        if (ok && warp_wait_bounded(grad_done, 0, abort_flag, a.status, 0x30A)) {
+            tc_fence_after();
+            // tcgen05.ld is warp-collective (.sync.aligned): every lane loads,
+            // only keys inside the sequence are stored
+            const bool key_ok = key < a.s;
+            const long long tok = static_cast<long long>(n) * a.s + key;
+            uint4* dk = reinterpret_cast<uint4*>(a.dqkv + tok * 3 * a.h + a.h + head * D);
+            uint4* dv = reinterpret_cast<uint4*>(a.dqkv + tok * 3 * a.h + 2 * a.h + head * D);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32], k[32];
+                tmem_ld32(lane_addr + kDV + c * 32, v);
+                tmem_ld32(lane_addr + kDK + c * 32, k);
+                tmem_wait_ld();
+                if (key_ok) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint4 u, w;
+                        u.x = pack_bf16x2(__uint_as_float(v[8 * i]), __uint_as_float(v[8 * i + 1]));
+                        u.y = pack_bf16x2(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3]));
+                        u.z = pack_bf16x2(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5]));
+                        u.w = pack_bf16x2(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7]));
+                        w.x = pack_bf16x2(__uint_as_float(k[8 * i]) * a.scale, __uint_as_float(k[8 * i + 1]) * a.scale);
+                        w.y = pack_bf16x2(__uint_as_float(k[8 * i + 2]) * a.scale, __uint_as_float(k[8 * i + 3]) * a.scale);
+                        w.z = pack_bf16x2(__uint_as_float(k[8 * i + 4]) * a.scale, __uint_as_float(k[8 * i + 5]) * a.scale);
+                        w.w = pack_bf16x2(__uint_as_float(k[8 * i + 6]) * a.scale, __uint_as_float(k[8 * i + 7]) * a.scale);
+                        dv[c * 4 + i] = u;
+                        dk[c * 4 + i] = w;
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------- launchers
+
+cudaError_t launch_attn_forward(const CUtensorMap& tm_qkv128, int d, const AttnParams& p,
+                                cudaStream_t st, int* launches) {
+    AttnArgs a{};
+    a.nb = p.nb; a.s = p.s; a.h = p.h; a.nh = p.nh;
+    a.T = static_cast<long long>(p.nb) * p.s;
+    a.q_tiles = (p.s + 127) / 128;
+    a.scale = 1.0f / sqrtf(static_cast<float>(d));
+    a.scale2 = 1.4426950408889634f * a.scale;
+    a.O = p.O;
+    a.lse = p.lse;
+    a.status = p.status;
+    const unsigned grid = static_cast<unsigned>(a.q_tiles * p.nb * p.nh);
+    cudaError_t e = cudaSuccess;
+#define TPMLP_ATTN_FWD(DD)                                                                        \
+    if (d == DD) {                                                                                \
+        auto kern = attn_fwd_kernel<DD>;                                                          \
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<DD>::SMEM); \
+        if (e == cudaSuccess) kern<<<grid, kAttnThreads, FwdCfg<DD>::SMEM, st>>>(tm_qkv128, a);   \
+    }
+    TPMLP_ATTN_FWD(64)
+    TPMLP_ATTN_FWD(96)
+    TPMLP_ATTN_FWD(128)
+#undef TPMLP_ATTN_FWD
+    if (e != cudaSuccess) return e;
+    e = cudaGetLastError();
+    if (e == cudaSuccess) ++*launches;
+    return e;
+}
+
+cudaError_t launch_attn_backward(const CUtensorMap& tm_qkv128, const CUtensorMap& tm_qkv64,
+                                 const CUtensorMap& tm_do128, const CUtensorMap& tm_do64, int d,
+                                 const AttnParams& p, cudaStream_t st, int* launches) {
+    AttnArgs a{};
+    a.nb = p.nb; a.s = p.s; a.h = p.h; a.nh = p.nh;
+    a.T = static_cast<long long>(p.nb) * p.s;
+    a.scale = 1.0f / sqrtf(static_cast<float>(d));
+    a.scale2 = 1.4426950408889634f * a.scale;
+    a.lse_in = p.lse_in;
+    a.dqkv = p.dqkv;
+    a.status = p.status;
+    // delta = rowsum(dO * O)
+    {
+        const long long items = a.T * p.nh;
+        attn_delta_kernel<<<static_cast<unsigned>((items + 255) / 256), 256, 0, st>>>(
+            p.dO, p.O_in, a.T, p.h, p.nh, d, p.delta_out);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        ++*launches;
+    }
+    a.delta = p.delta_out;
+    cudaError_t e = cudaSuccess;
+    const int q_tiles = (p.s + 127) / 128;
+    AttnArgs aq = a;
+    aq.q_tiles = q_tiles;
+    const unsigned grid = static_cast<unsigned>(q_tiles * p.nb * p.nh);
+#define TPMLP_ATTN_BWD(DD)                                                                          \
+    if (d == DD) {                                                                                  \
+        auto kq = attn_bwd_dq_kernel<DD>;                                                           \
+        e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<DD>::SMEM); \
+        if (e == cudaSuccess) {                                                                     \
+            kq<<<grid, kAttnThreads, DqCfg<DD>::SMEM, st>>>(tm_qkv128, tm_qkv64, tm_do128, aq);     \
+            e = cudaGetLastError();                                                                 \
+        }                                                                                           \
+        if (e == cudaSuccess) {                                                                     \
+            ++*launches;                                                                            \
+            auto kk = attn_bwd_dkdv_kernel<DD>;                                                     \
+            e = cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize, DkvCfg<DD>::SMEM); \
+            if (e == cudaSuccess) {                                                                 \
+                kk<<<grid, kAttnThreads, DkvCfg<DD>::SMEM, st>>>(tm_qkv128, tm_qkv64, tm_do64, a);  \
+                e = cudaGetLastError();                                                             \
+            }                                                                                       \
+            if (e == cudaSuccess) ++*launches;                                                      \
+        }                                                                                           \
+    }
+    TPMLP_ATTN_BWD(64)
+    TPMLP_ATTN_BWD(96)
+    TPMLP_ATTN_BWD(128)
+#undef TPMLP_ATTN_BWD
+    return e;
+}
+
+}  // namespace tpmlp

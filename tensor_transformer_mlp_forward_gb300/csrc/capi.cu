@@ -22,9 +22,11 @@
 
 namespace tpmlp {
 
-// Device status word: kernels write a nonzero code here when a bounded wait
-// gives up; tpmlp_device_status() reads and clears it.
-__device__ int g_status_word;
+// Device status words: [0] a kernel writes a nonzero code when a bounded
+// wait gives up (tpmlp_device_status() reads and clears it); [1] the site of
+// the first wait that gave up, where the kernel names one
+// (tpmlp_device_wait_site() reads and clears it).
+__device__ int g_status_word[2];
 
 namespace {
 
@@ -1189,6 +1191,233 @@ TPMLP_API int tp_ln_residual_backward(const tpmlp_bf16* dX, const tpmlp_bf16* dr
     return e == cudaSuccess ? TPMLP_OK : fail_cuda(e);
 }
 
+// ---------------------------------------------- head-parallel attention
+
+namespace tpmlp {
+namespace {
+
+// Head dims with a compiled attention kernel.
+bool attn_head_dim_ok(int d) { return d == 64 || d == 96 || d == 128; }
+
+int check_attn(int nb, int s, int h, int nh, int t) {
+    if (nb < 0 || s < 1 || h < 8 || h % 8 != 0 || nh < 1 || h % nh != 0 || t < 1 ||
+        t > TPMLP_MAX_SHARDS || nh % t != 0)
+        return TPMLP_ERR_SHAPE;
+    if (!attn_head_dim_ok(h / nh)) return TPMLP_ERR_SHAPE;
+    if (static_cast<long long>(nb) * s >= (1LL << 31) || 3LL * h >= (1LL << 31))
+        return TPMLP_ERR_SHAPE;
+    return TPMLP_OK;
+}
+
+// 3-D tensor map {cols, s, nb} over a row-major bf16 [nb * s, cols] matrix
+// (token n * s + pos), boxes of 64 columns x box_rows positions, so that a
+// tile never crosses into the next sequence and ragged tails read zeros.
+int make_seq_map(CUtensorMap* m, const void* ptr, int nb, int s, long long cols, int box_rows) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(s),
+                          static_cast<cuuint64_t>(nb)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2,
+                             static_cast<cuuint64_t>(cols) * 2 * static_cast<cuuint64_t>(s)};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1}, estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        t_last_cuda_error = static_cast<int>(r);
+        return TPMLP_ERR_LAUNCH;
+    }
+    return TPMLP_OK;
+}
+
+// QKV = X Wqkv + bqkv over all 3h columns: the column-parallel projection.
+// Shard i's columns are its heads' blocks of Q, K and V; with no reduction
+// across columns the t shards are one GEMM on one GPU.
+int qkv_gemm(const tpmlp_bf16* X, const tpmlp_bf16* W, const tpmlp_bf16* b, int T, int h,
+             tpmlp_bf16* QKV, cudaStream_t st, const DeviceInfo& d) {
+    GemmArgs g = blank_args();
+    const GemmShape sh{T, 3 * h, h, 1, SHARD_N, 1LL * T * h, 3LL * h * h};
+    g.a_on = ON_NONE;
+    g.b_on = ON_CONTIG;
+    g.bias = cb(b);
+    Operand a{X, T, h, ON_NONE, false};
+    Operand bb{W, h, 3LL * h, ON_CONTIG, true};
+    Output o{QKV, nullptr, T, 3LL * h, 1};
+    return run_gemm(launch_column_bias, a, bb, o, g, sh, st, d);
+}
+
+int attn_core_forward(const tpmlp_bf16* QKV, int nb, int s, int h, int nh, tpmlp_bf16* O,
+                      float* lse, cudaStream_t st, const DeviceInfo& d) {
+    CUtensorMap tm;
+    if (int rc = make_seq_map(&tm, QKV, nb, s, 3LL * h, 128)) return rc;
+    AttnParams p{};
+    p.nb = nb; p.s = s; p.h = h; p.nh = nh;
+    p.O = reinterpret_cast<__nv_bfloat16*>(O);
+    p.lse = lse;
+    p.status = d.status;
+    cudaError_t e = launch_attn_forward(tm, h / nh, p, st, &t_last_launches);
+    return e == cudaSuccess ? TPMLP_OK : fail_cuda(e);
+}
+
+int attn_core_backward(const tpmlp_bf16* QKV, const tpmlp_bf16* O, const float* lse,
+                       const tpmlp_bf16* dO, int nb, int s, int h, int nh, tpmlp_bf16* dQKV,
+                       float* delta, cudaStream_t st, const DeviceInfo& d) {
+    CUtensorMap q128, q64, do128, do64;
+    if (int rc = make_seq_map(&q128, QKV, nb, s, 3LL * h, 128)) return rc;
+    if (int rc = make_seq_map(&q64, QKV, nb, s, 3LL * h, 64)) return rc;
+    if (int rc = make_seq_map(&do128, dO, nb, s, h, 128)) return rc;
+    if (int rc = make_seq_map(&do64, dO, nb, s, h, 64)) return rc;
+    AttnParams p{};
+    p.nb = nb; p.s = s; p.h = h; p.nh = nh;
+    p.O_in = cb(O);
+    p.dO = cb(dO);
+    p.lse_in = lse;
+    p.delta_out = delta;
+    p.dqkv = reinterpret_cast<__nv_bfloat16*>(dQKV);
+    p.status = d.status;
+    cudaError_t e = launch_attn_backward(q128, q64, do128, do64, h / nh, p, st, &t_last_launches);
+    return e == cudaSuccess ? TPMLP_OK : fail_cuda(e);
+}
+
+size_t attn_colsum_floats(int T, int h) {
+    return std::max(static_cast<size_t>(colsum_chunks(T, h)) * h,
+                    static_cast<size_t>(colsum_chunks(T, 3 * h)) * 3 * h);
+}
+
+struct AttnBackwardLayout {
+    size_t dO, delta, dqkv, colsum, split, total;
+};
+
+AttnBackwardLayout attn_backward_layout(int nb, int s, int h, int nh) {
+    const long long T = 1LL * nb * s;
+    AttnBackwardLayout L;
+    L.dO = 0;
+    L.delta = align256(L.dO + sizeof(uint16_t) * static_cast<size_t>(T) * h);
+    L.dqkv = align256(L.delta + sizeof(float) * static_cast<size_t>(T) * nh);
+    L.colsum = align256(L.dqkv + sizeof(uint16_t) * static_cast<size_t>(T) * 3 * h);
+    L.split = align256(L.colsum + sizeof(float) * attn_colsum_floats(static_cast<int>(T), h));
+    const size_t sp = std::max(split_partial_floats(static_cast<int>(T), h, h, 1),
+                               split_partial_floats(static_cast<int>(T), h, 3 * h, 1));
+    L.total = align256(L.split + sizeof(float) * sp);
+    return L;
+}
+
+}  // namespace
+}  // namespace tpmlp
+
+TPMLP_API int tp_attn_qkv(const tpmlp_bf16* X, const tpmlp_bf16* Wqkv, const tpmlp_bf16* bqkv,
+                          int T, int h, tpmlp_bf16* QKV, void* stream) {
+    TPMLP_PROLOGUE((T < 0 || h < 8 || h % 8 != 0) ? TPMLP_ERR_SHAPE : TPMLP_OK);
+    if (T == 0) return TPMLP_OK;
+    if (any_null(X, Wqkv, bqkv, QKV)) return TPMLP_ERR_NULL;
+    if (!all_aligned(X, Wqkv, bqkv, QKV)) return TPMLP_ERR_ALIGN;
+    DeviceInfo d;
+    if (int rc = enter(d)) return rc;
+    return qkv_gemm(X, Wqkv, bqkv, T, h, QKV, static_cast<cudaStream_t>(stream), d);
+}
+
+TPMLP_API int tp_attn_core_forward(const tpmlp_bf16* QKV, int nb, int s, int h, int nh,
+                                   tpmlp_bf16* O, float* lse, void* stream) {
+    TPMLP_PROLOGUE(check_attn(nb, s, h, nh, 1));
+    if (nb == 0) return TPMLP_OK;
+    if (any_null(QKV, O, lse)) return TPMLP_ERR_NULL;
+    if (!all_aligned(QKV, O, lse)) return TPMLP_ERR_ALIGN;
+    DeviceInfo d;
+    if (int rc = enter(d)) return rc;
+    return attn_core_forward(QKV, nb, s, h, nh, O, lse, static_cast<cudaStream_t>(stream), d);
+}
+
+TPMLP_API int tp_attn_core_backward(const tpmlp_bf16* QKV, const tpmlp_bf16* O, const float* lse,
+                                    const tpmlp_bf16* dO, int nb, int s, int h, int nh,
+                                    tpmlp_bf16* dQKV, float* delta, void* stream) {
+    TPMLP_PROLOGUE(check_attn(nb, s, h, nh, 1));
+    if (nb == 0) return TPMLP_OK;
+    if (any_null(QKV, O, lse, dO, dQKV, delta)) return TPMLP_ERR_NULL;
+    if (!all_aligned(QKV, O, lse, dO, dQKV, delta)) return TPMLP_ERR_ALIGN;
+    DeviceInfo d;
+    if (int rc = enter(d)) return rc;
+    return attn_core_backward(QKV, O, lse, dO, nb, s, h, nh, dQKV, delta,
+                              static_cast<cudaStream_t>(stream), d);
+}
+
+TPMLP_API size_t tp_attn_forward_workspace_bytes(int nb, int s, int h, int nh, int t) {
+    if (check_attn(nb, s, h, nh, t) || nb == 0) return 0;
+    return sizeof(float) * split_partial_floats(nb * s, h, h, t);
+}
+
+TPMLP_API int tp_attn_forward(const tpmlp_bf16* X, const tpmlp_bf16* Wqkv, const tpmlp_bf16* bqkv,
+                              const tpmlp_bf16* Wo, const tpmlp_bf16* bo,
+                              const tpmlp_bf16* residual, int nb, int s, int h, int nh, int t,
+                              tpmlp_bf16* Y, tpmlp_bf16* QKV, tpmlp_bf16* O, float* lse,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+    TPMLP_PROLOGUE(check_attn(nb, s, h, nh, t));
+    if (nb == 0) return TPMLP_OK;
+    if (any_null(X, Wqkv, bqkv, Wo, bo, residual, Y, QKV, O, lse)) return TPMLP_ERR_NULL;
+    if (!all_aligned(X, Wqkv, bqkv, Wo, bo, residual, Y, QKV, O, lse, workspace))
+        return TPMLP_ERR_ALIGN;
+    DeviceInfo d;
+    if (int rc = enter(d)) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int T = nb * s;
+    if (int rc = qkv_gemm(X, Wqkv, bqkv, T, h, QKV, st, d)) return rc;
+    if (int rc = attn_core_forward(QKV, nb, s, h, nh, O, lse, st, d)) return rc;
+    // row-parallel output projection: Y = sum_i O_i Wo_i + bo + residual, the
+    // g-operator sum folded into one accumulator (the MLP's a3 GEMM with F = h)
+    return row_sum(O, Wo, bo, residual, T, h, h, t, Y, workspace, workspace_bytes, st, d);
+}
+
+TPMLP_API size_t tp_attn_backward_workspace_bytes(int nb, int s, int h, int nh, int t) {
+    if (check_attn(nb, s, h, nh, t)) return 0;
+    return attn_backward_layout(nb, s, h, nh).total;
+}
+
+TPMLP_API int tp_attn_backward(const tpmlp_bf16* dY, const tpmlp_bf16* X, const tpmlp_bf16* Wqkv,
+                               const tpmlp_bf16* Wo, const tpmlp_bf16* QKV, const tpmlp_bf16* O,
+                               const float* lse, int nb, int s, int h, int nh, int t,
+                               tpmlp_bf16* dX, tpmlp_bf16* dWqkv, float* dbqkv, tpmlp_bf16* dWo,
+                               float* dbo, void* workspace, size_t workspace_bytes, void* stream) {
+    TPMLP_PROLOGUE(check_attn(nb, s, h, nh, t));
+    if (any_null(Wqkv, Wo, dWqkv, dbqkv, dWo, dbo) ||
+        (nb > 0 && any_null(dY, X, QKV, O, lse, dX)))
+        return TPMLP_ERR_NULL;
+    if (!all_aligned(dY, X, Wqkv, Wo, QKV, O, lse, dX, dWqkv, dbqkv, dWo, dbo))
+        return TPMLP_ERR_ALIGN;
+    const AttnBackwardLayout L = attn_backward_layout(nb, s, h, nh);
+    if (nb > 0 && (workspace == nullptr || workspace_bytes < L.total)) return TPMLP_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return TPMLP_ERR_ALIGN;
+    DeviceInfo d;
+    if (int rc = enter(d)) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int T = nb * s;
+    if (T == 0) {
+        cudaError_t e;
+        if ((e = cudaMemsetAsync(dbo, 0, sizeof(float) * static_cast<size_t>(h), st)) != cudaSuccess ||
+            (e = cudaMemsetAsync(dbqkv, 0, sizeof(float) * 3 * static_cast<size_t>(h), st)) != cudaSuccess ||
+            (e = cudaMemsetAsync(dWo, 0, sizeof(uint16_t) * static_cast<size_t>(h) * h, st)) != cudaSuccess ||
+            (e = cudaMemsetAsync(dWqkv, 0, sizeof(uint16_t) * 3 * static_cast<size_t>(h) * h, st)) != cudaSuccess)
+            return fail_cuda(e);
+        return TPMLP_OK;
+    }
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    tpmlp_bf16* dO = reinterpret_cast<tpmlp_bf16*>(ws + L.dO);
+    float* delta = reinterpret_cast<float*>(ws + L.delta);
+    tpmlp_bf16* dQKV = reinterpret_cast<tpmlp_bf16*>(ws + L.dqkv);
+    float* colsum = reinterpret_cast<float*>(ws + L.colsum);
+    // dbo = sum_rows dY (g backward: the identity on every shard)
+    if (int rc = bias_grad(dY, T, h, dbo, colsum, st)) return rc;
+    // dWo_i = O_i^T dY (rows of Wo per shard)
+    if (int rc = dB_gemm(O, dY, T, h, h, t, dWo, st, d)) return rc;
+    // dO = dY Wo^T: shard i's columns of dO from its rows of Wo, no sum
+    if (int rc = dx_gemm(dY, Wo, T, h, h, 1, dO, ws + L.split, L.total - L.split, st, d)) return rc;
+    // local attention backward of every head
+    if (int rc = attn_core_backward(QKV, O, lse, dO, nb, s, h, nh, dQKV, delta, st, d)) return rc;
+    // dbqkv = sum_rows dQKV ; dWqkv = X^T dQKV (column blocks per shard)
+    if (int rc = bias_grad(dQKV, T, 3 * h, dbqkv, colsum, st)) return rc;
+    if (int rc = dA_gemm(X, dQKV, T, h, 3 * h, 1, dWqkv, st, d)) return rc;
+    // dX = sum_i dQKV_i Wqkv_i^T: the f-operator sum as one accumulation over
+    // all 3h columns
+    return dx_gemm(dQKV, Wqkv, T, h, 3 * h, 1, dX, ws + L.split, L.total - L.split, st, d);
+}
+
 TPMLP_API const char* tpmlp_status_string(int status) {
     switch (status) {
         case TPMLP_OK: return "ok";
@@ -1212,17 +1441,30 @@ TPMLP_API int tpmlp_last_cuda_error(void) { return t_last_cuda_error; }
 
 TPMLP_API int tpmlp_last_launch_count(void) { return t_last_launches; }
 
-TPMLP_API int tpmlp_device_status(void) {
+static int read_clear_status(int index, int* out) {
     DeviceInfo d;
     if (int rc = device_info(d)) return rc;
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return fail_cuda(e);
     int v = 0;
-    if ((e = cudaMemcpy(&v, d.status, sizeof v, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    if ((e = cudaMemcpy(&v, d.status + index, sizeof v, cudaMemcpyDeviceToHost)) != cudaSuccess)
         return fail_cuda(e);
     const int zero = 0;
-    if ((e = cudaMemcpy(d.status, &zero, sizeof zero, cudaMemcpyHostToDevice)) != cudaSuccess)
+    if ((e = cudaMemcpy(d.status + index, &zero, sizeof zero, cudaMemcpyHostToDevice)) != cudaSuccess)
         return fail_cuda(e);
+    *out = v;
+    return TPMLP_OK;
+}
+
+TPMLP_API int tpmlp_device_status(void) {
+    int v = 0;
+    if (int rc = read_clear_status(0, &v)) return rc;
+    return v;
+}
+
+TPMLP_API int tpmlp_device_wait_site(void) {
+    int v = 0;
+    if (int rc = read_clear_status(1, &v)) return -rc;
     return v;
 }
 

@@ -79,7 +79,15 @@ enum ShardMode { SHARD_NONE = 0, SHARD_N = 1, SHARD_M = 2, SHARD_K = 3 };
 enum ShardOn { ON_NONE = 0, ON_CONTIG = 1, ON_ROWS = 2 };
 // EPI_PARTIAL: split reduction -- the fp32 accumulator of k-range split ks is
 // stored as is into plane ks of an fp32 [splits, M, N] workspace.
-enum Epilogue { EPI_BIAS_GELU = 0, EPI_BIAS_RESIDUAL = 1, EPI_DGELU = 2, EPI_STORE = 3, EPI_PARTIAL = 4 };
+// EPI_BIAS: + bias only (the attention block's Q/K/V projection).
+enum Epilogue {
+    EPI_BIAS_GELU = 0,
+    EPI_BIAS_RESIDUAL = 1,
+    EPI_DGELU = 2,
+    EPI_STORE = 3,
+    EPI_PARTIAL = 4,
+    EPI_BIAS = 5
+};
 
 struct GemmArgs {
     int M, N;            // output extent of one shard (SHARD_M: M per shard; SHARD_N: N per shard)
@@ -550,7 +558,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int v0 = row_ok ? min(32, p.N - tc.n0) : 0;
                 load_raw32(p.aux + grow * p.ld_aux + gcol0, v0, aux_cur);
             }
-            if (!wait_bounded(&acc_full[acc], acc_phase, abort_flag, p.status)) break;
+            if (!warp_wait_bounded(&acc_full[acc], acc_phase, abort_flag, p.status)) break;
             tc_fence_after();
 
             if constexpr (EPI == EPI_PARTIAL) {
@@ -654,6 +662,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                     }
                                 }
                             }
+                        }
+                        stage_row(buf0 + my_row, half, swz, v);
+                    } else if constexpr (EPI == EPI_BIAS) {
+                        if (valid > 0) {
+                            float b[32];
+                            load_bf16x32(p.bias + gcol, valid, b);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] += b[i];
                         }
                         stage_row(buf0 + my_row, half, swz, v);
                     } else if constexpr (EPI == EPI_DGELU) {

@@ -22,6 +22,9 @@ cudaError_t launch_column_gelu(const GemmMaps& m, const GemmArgs& g,
                                int grid, bool pair, cudaStream_t st);
 cudaError_t launch_row_sum(const GemmMaps& m, const GemmArgs& g,
                            int grid, bool pair, cudaStream_t st);
+// Column GEMM with + bias only (the attention block's Q/K/V projection).
+cudaError_t launch_column_bias(const GemmMaps& m, const GemmArgs& g, int grid, bool pair,
+                               cudaStream_t st);
 // The same two GEMMs with a split reduction: fp32 partials per k-range split.
 cudaError_t launch_row_partial(const GemmMaps& m, const GemmArgs& g, int grid, bool pair,
                                cudaStream_t st);
@@ -49,6 +52,27 @@ cudaError_t launch_ln_backward(const __nv_bfloat16* dX, const __nv_bfloat16* dre
                                float* partial, cudaStream_t st, int* launches);
 // Row chunks of the dgamma / dbeta partial sums (partial = 2 * chunks * h floats).
 int ln_param_chunks(int T, int h);
+
+// Causal attention of every (sequence, head) (attention.cu).  Head dims
+// d in {64, 96, 128}.  QKV [T, 3h] is read through 3-D tensor maps
+// {3h, s, nb} with 64 x 128-row (qkv128) or 64 x 64-row (qkv64) boxes, dO
+// [T, h] likewise; T = nb * s.
+struct AttnParams {
+    int nb, s, h, nh;
+    __nv_bfloat16* O;            // forward: output [T, h]
+    float* lse;                  // forward: log2-domain log-sum-exp [nh, T]
+    const __nv_bfloat16* O_in;   // backward: the forward's O
+    const __nv_bfloat16* dO;     // backward: gradient at O [T, h]
+    const float* lse_in;         // backward: the forward's lse
+    float* delta_out;            // backward: rowsum(dO * O) scratch [nh, T]
+    __nv_bfloat16* dqkv;         // backward: output [T, 3h]
+    int* status;
+};
+cudaError_t launch_attn_forward(const CUtensorMap& tm_qkv128, int d, const AttnParams& p,
+                                cudaStream_t st, int* launches);
+cudaError_t launch_attn_backward(const CUtensorMap& tm_qkv128, const CUtensorMap& tm_qkv64,
+                                 const CUtensorMap& tm_do128, const CUtensorMap& tm_do64, int d,
+                                 const AttnParams& p, cudaStream_t st, int* launches);
 
 // `grid` is the number of work units wanted (CTAs, or CTA pairs when PAIR);
 // it is clipped to what can be resident at once, so the persistent loop never

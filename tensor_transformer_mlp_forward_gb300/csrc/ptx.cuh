@@ -56,10 +56,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Waits for the phase of `bar` with the given parity to complete.  Gives up
 // after kWaitLimitNs, or as soon as another role of the CTA has given up
-// (*abort != 0): on its own timeout it raises *abort and writes the timeout
-// code to the device status word `status`.  Returns false when it gave up.
+// (*abort != 0): on its own timeout it raises *abort, writes the timeout
+// code to the device status word status[0] and, when `site` is nonzero and
+// no earlier wait has done so, records `site` in status[1] so that the host
+// can tell which wait gave up first.  Returns false when it gave up.
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
-                                             volatile uint32_t* abort, int* status) {
+                                             volatile uint32_t* abort, int* status, int site = 0) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (true) {
@@ -70,17 +72,34 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
         if (global_ns() - t0 > kWaitLimitNs) {
             *abort = 1u;
             atomicExch(status, kStatusTimeout);
+            if (site) atomicCAS(status + 1, 0, site);
             return false;
         }
     }
 }
 
+// wait_bounded for a whole warp: lane 0 polls and the verdict is broadcast,
+// so the warp leaves its loops together (a lane-divergent exit would strand
+// the other lanes at the warp's next __syncwarp).  The closing __syncwarp
+// orders the other lanes' later reads after lane 0's observation.
+__device__ __forceinline__ bool warp_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  volatile uint32_t* abort, int* status,
+                                                  int site = 0) {
+    uint32_t ok = 1u;
+    if ((threadIdx.x & 31) == 0) ok = wait_bounded(bar, parity, abort, status, site) ? 1u : 0u;
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    __syncwarp();
+    return ok != 0u;
+}
+
 // Bounded wait used while draining after an abort: ignores the abort flag.
-__device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, int* status) {
+__device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, int* status,
+                                           int site = 0) {
     const unsigned long long t0 = global_ns();
     while (!mbar_try_wait(bar, parity)) {
         if (global_ns() - t0 > kWaitLimitNs) {
             atomicExch(status, kStatusTimeout);
+            if (site) atomicCAS(status + 1, 0, site);
             return false;
         }
     }

@@ -137,6 +137,88 @@ def make_inputs(w: Workload, keys=DRAW_ORDER) -> Dict[str, torch.Tensor]:
             for key in DRAW_ORDER if key in keys}
 
 
+# ------------------------------------------------------- attention block
+
+ATTN_DRAW_ORDER = ("X", "Wqkv", "bqkv", "Wo", "bo", "residual", "dY")
+_ATTN_KEY_BASE = 16  # generator key indices of the attention tensors (after the MLP's)
+
+
+@dataclasses.dataclass(frozen=True)
+class AttnWorkload:
+    """One head-parallel self-attention block: nb sequences of s tokens,
+    hidden h, nh heads of d = h / nh, t shards of nh / t heads."""
+
+    name: str
+    nb: int
+    s: int
+    h: int
+    nh: int
+    t: int
+    std: Dict[str, float]
+    seed: int
+
+    @property
+    def T(self) -> int:
+        return self.nb * self.s
+
+    @property
+    def d(self) -> int:
+        return self.h // self.nh
+
+    def flops_fwd_bwd(self) -> int:
+        """Algorithmic flops: the Q/K/V and output projections (2 T h 3h and
+        2 T h h forward, twice that backward) and the six products of causal
+        attention (S = Q K^T, O = P V; dP, dV, dQ, dK), 2 d flops per visible
+        (query, key) pair per head each."""
+        pairs = self.nb * self.s * (self.s + 1) // 2
+        proj = 3 * (2 * self.T * self.h * 3 * self.h + 2 * self.T * self.h * self.h)
+        return proj + 6 * 2 * pairs * self.h
+
+    def shape(self, key: str):
+        T, h = self.T, self.h
+        return {
+            "X": (T, h),
+            "Wqkv": (h, 3 * h),
+            "bqkv": (3 * h,),
+            "Wo": (h, h),
+            "bo": (h,),
+            "residual": (T, h),
+            "dY": (T, h),
+        }[key]
+
+
+def _attn_std(x=1.0, w=0.02, bqkv=0.0, wo=0.02, bo=0.0, res=1.0, dy=1.0):
+    return {"X": x, "Wqkv": w, "bqkv": bqkv, "Wo": wo, "bo": bo, "residual": res, "dY": dy}
+
+
+# Attention shapes of the pages' GPT-2 models ("Megatron-LM: Tensor Model
+# Parallel", Table 2: 355M with 16 heads of 64, 2.5B with 20 of 96, 8.3B with
+# 24 of 128; sequence length 1024), batch 8 as in the MLP workloads.  The
+# output projection sits before the residual, so the 8.3B model scales it by
+# 1/sqrt(2 * 72) like B.  The tiny case matches the tiny MLP block's tokens.
+ATTN_TINY = AttnWorkload("attn-tiny", 2, 64, 256, 4, 2, _attn_std(bqkv=0.01, bo=0.01), 1100)
+ATTN_GPT2_355M = AttnWorkload("attn-gpt2-355m", 8, 1024, 1024, 16, 2, _attn_std(), 1101)
+ATTN_GPT2_2_5B = AttnWorkload("attn-gpt2-2.5b", 8, 1024, 1920, 20, 2,
+                              _attn_std(wo=0.02 / math.sqrt(2 * 54)), 1102)
+ATTN_GPT2_8_3B = AttnWorkload("attn-gpt2-8.3b", 8, 1024, 3072, 24, 8,
+                              _attn_std(wo=0.02 / math.sqrt(2 * 72)), 1103)
+
+ATTN_WORKLOADS = {w.name: w for w in (ATTN_TINY, ATTN_GPT2_355M, ATTN_GPT2_2_5B, ATTN_GPT2_8_3B)}
+
+
+def attn_custom(nb: int, s: int, h: int, nh: int, t: int, seed: int, std=None,
+                name="attn-custom") -> AttnWorkload:
+    """An attention block of arbitrary shape with the tiny case's distributions."""
+    return AttnWorkload(name, nb, s, h, nh, t, dict(std or ATTN_TINY.std), seed)
+
+
+def make_attn_inputs(w: AttnWorkload, keys=ATTN_DRAW_ORDER) -> Dict[str, torch.Tensor]:
+    """Draw the attention block's bf16 tensors on the CPU (contiguous)."""
+    return {key: _draw(w.seed, _ATTN_KEY_BASE + ATTN_DRAW_ORDER.index(key), w.shape(key),
+                       w.std[key]).contiguous()
+            for key in ATTN_DRAW_ORDER if key in keys}
+
+
 def sample_indices(n: int, k: int, seed: int) -> torch.Tensor:
     """k distinct sorted indices in [0, n) (always includes n-1, the tail)."""
     gen = torch.Generator(device="cpu")
