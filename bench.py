@@ -60,6 +60,9 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--layernorm", action="store_true",
                    help="time the residual add + LayerNorm kernels instead (GB/s)")
+    p.add_argument("--attention", action="store_true",
+                   help="time the head-parallel attention block instead (TFLOPS fwd+bwd)")
+    p.add_argument("--attn-workload", default="attn-gpt2-8.3b")
     p.add_argument("--pair-mode", type=int, default=None,
                    help="GEMM kernel: 0 single CTA, 1 auto (default), 2 CTA pairs")
     return p.parse_args(argv)
@@ -97,13 +100,18 @@ def peaks():
         return FALLBACK_BF16_TFLOPS, FALLBACK_BF16_TFLOPS_SUSTAINED, "fallback"
 
 
+# The sources the GEMM kernels and their host-side tile schedule are built
+# from: a recorded DRAM-traffic figure holds while none of them changes.
+GEMM_SOURCES = ("capi.cu", "gemm.cuh", "gemm_backward_data.cu", "gemm_backward_weight.cu",
+                "gemm_forward.cu", "kernels.h", "philox.cuh", "ptx.cuh")
+
+
 def kernel_source_hash() -> str:
     d = os.path.join(ROOT, "tensor_transformer_mlp_forward_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(d)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(f.encode())
-            h.update(open(os.path.join(d, f), "rb").read())
+    for f in GEMM_SOURCES:
+        h.update(f.encode())
+        h.update(open(os.path.join(d, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -551,8 +559,182 @@ def run_layernorm(args, w):
     return 0
 
 
+# -------------------------------------------------------- attention block
+
+ATTN_CALLS = ("qkv", "core_fwd", "out_proj", "dbo", "dWo", "dO", "core_bwd", "dbqkv", "dWqkv",
+              "dX")
+
+
+class AttnStep:
+    """All buffers of the attention block, resident in HBM; run() issues one
+    forward + backward step as the library's calls (tp_attn_forward and
+    tp_attn_backward issue the same calls in the same order)."""
+
+    def __init__(self, w, device):
+        import torch
+
+        from tensor_transformer_mlp_forward_gb300 import binding, inputs
+
+        self.b, self.w = binding, w
+        T, h, nh = w.T, w.h, w.nh
+        self.cpu = inputs.make_attn_inputs(w)
+        self.inp = {k: v.to(device) for k, v in self.cpu.items()}
+        e = lambda *s, dt=torch.bfloat16: torch.empty(s, dtype=dt, device=device)  # noqa: E731
+        self.QKV, self.O, self.Y = e(T, 3 * h), e(T, h), e(T, h)
+        self.lse, self.delta = e(nh, T, dt=torch.float32), e(nh, T, dt=torch.float32)
+        self.dO, self.dQKV, self.dX = e(T, h), e(T, 3 * h), e(T, h)
+        self.dWqkv, self.dWo = e(h, 3 * h), e(h, h)
+        self.dbqkv, self.dbo = e(3 * h, dt=torch.float32), e(h, dt=torch.float32)
+        lib = binding.lib()
+        self.p_sum = e(max(1, int(lib.tp_mlp_bias_grad_workspace_floats(T, 3 * h)),
+                           int(lib.tp_mlp_bias_grad_workspace_floats(T, h))), dt=torch.float32)
+        self.ws = e(max(16, binding.split_workspace_bytes(T, h, 3 * h, 1),
+                        binding.split_workspace_bytes(T, h, h, w.t)), dt=torch.uint8)
+        self.launches = 0
+        self.names = ATTN_CALLS
+
+    def run(self, events=None):
+        b, i, w = self.b, self.inp, self.w
+        calls = (
+            lambda: b.tp_attn_qkv(i["X"], i["Wqkv"], i["bqkv"], QKV=self.QKV),
+            lambda: b.tp_attn_core_forward(self.QKV, w.nb, w.nh, O=self.O, lse=self.lse),
+            lambda: b.tp_mlp_row_sum(self.O, i["Wo"], i["bo"], i["residual"], w.t, Y=self.Y,
+                                     workspace=self.ws),
+            lambda: b.tp_mlp_bias_grad(i["dY"], db=self.dbo, partial=self.p_sum),
+            lambda: b.tp_mlp_dB(self.O, i["dY"], w.t, dB=self.dWo),
+            lambda: b.tp_mlp_dx(i["dY"], i["Wo"], 1, dX=self.dO, workspace=self.ws),
+            lambda: b.tp_attn_core_backward(self.QKV, self.O, self.lse, self.dO, w.nb, w.nh,
+                                            dQKV=self.dQKV, delta=self.delta),
+            lambda: b.tp_mlp_bias_grad(self.dQKV, db=self.dbqkv, partial=self.p_sum),
+            lambda: b.tp_mlp_dA(i["X"], self.dQKV, 1, dA=self.dWqkv),
+            lambda: b.tp_mlp_dx(self.dQKV, i["Wqkv"], 1, dX=self.dX, workspace=self.ws),
+        )
+        if events is not None:
+            events[0].record()
+        for k, c in enumerate(calls):
+            c()
+            self.launches += b.last_launch_count()
+            if events is not None:
+                events[k + 1].record()
+
+
+def attn_cpu_baseline(w, cpu, budget_s=20.0):
+    """The oracle's per-head entry points, as they stand, on whole heads
+    (forward output and every parameter gradient of the head)."""
+    import oracle
+
+    pairs = w.nb * w.s * (w.s + 1) // 2
+    d, T, h = w.d, w.T, w.h
+    per_head = (3 * (2 * T * h * 3 * d + 2 * T * d * h) + 12 * pairs * d)
+    done, spent = 0, 0.0
+    while done < w.nh and (done == 0 or spent < budget_s):
+        t0 = time.perf_counter()
+        oracle.attn_head(cpu, w.nb, w.nh, done)
+        oracle.attn_head_grads(cpu, w.nb, w.nh, done)
+        spent += time.perf_counter() - t0
+        done += 1
+    return {"value": per_head * done / spent / 1e12, "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{done} head(s) of the {w.name} block: O_j and dWqkv_j, dbqkv_j, dWo_j "
+                      f"(forward + backward of the head's share), fp64, {spent:.1f} s"}
+
+
+def run_attention(args):
+    import torch
+
+    from tensor_transformer_mlp_forward_gb300 import inputs
+
+    w = inputs.ATTN_WORKLOADS[args.attn_workload]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    step = AttnStep(w, dev)
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    assert step.b.device_status() == 0, "device wait timed out during warm-up"
+    step.launches = 0
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(step.names) + 1)]
+           for _ in range(args.steps)]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clocks:
+        w0 = time.time()
+        for k in range(args.steps):
+            flush.fill_(k & 0xFF)
+            step.run(evs[k])
+        torch.cuda.synchronize()
+        clocks.mark(w0, time.time())
+    assert step.b.device_status() == 0, "device wait timed out"
+    dev_s = sum(evs[k][0].elapsed_time(evs[k][-1]) for k in range(args.steps)) / 1e3
+    per_call = {n: statistics.mean(evs[k][j].elapsed_time(evs[k][j + 1]) for k in range(args.steps))
+                for j, n in enumerate(step.names)}
+    flops = w.flops_fwd_bwd()
+    value = flops * args.steps / dev_s / 1e12
+    burst, sustained, src = peaks()
+    pairs = w.nb * w.s * (w.s + 1) // 2
+    core = {"core_fwd": 4 * pairs * w.h, "core_bwd": 8 * pairs * w.h}
+    core_tf = {k: v / (per_call[k] / 1e3) / 1e12 for k, v in core.items()}
+    dominant = max(core, key=lambda k: per_call[k])
+    roofline = {"bound": "tensor", "kernel": "attn_fwd_kernel" if dominant == "core_fwd"
+                else "attn_bwd_dq_kernel + attn_bwd_dkdv_kernel",
+                "achieved": core_tf[dominant], "peak": burst, "unit": "TFLOP/s",
+                "frac": core_tf[dominant] / burst,
+                "peak_source": f"{src} bf16 burst (MEASURED_PEAKS.json)", "traffic": None,
+                "algorithmic_flops": {"core_fwd": "4 d per visible (query, key) pair per head",
+                                      "core_bwd": "8 d per visible pair per head (dP, dV, dQ, dK; "
+                                                  "the recomputed S is not counted)"}}
+    e2e = None
+    if not args.no_e2e:
+        i = step.inp
+        host_in = {k: step.cpu[k].pin_memory() for k in ("X", "residual", "dY")}
+        host_out = {k: torch.empty_like(getattr(step, k), device="cpu").pin_memory()
+                    for k in ("Y", "dX")}
+
+        def one():
+            for k, v in host_in.items():
+                i[k].copy_(v, non_blocking=True)
+            step.run()
+            for k, v in host_out.items():
+                v.copy_(getattr(step, k), non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            one()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            one()
+        b.record()
+        torch.cuda.synchronize()
+        e2e = {"value": flops * args.steps / (a.elapsed_time(b) / 1e3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in host_in.values()),
+               "d2h_bytes_per_step": sum(v.numel() * v.element_size() for v in host_out.values())}
+    line = {
+        "metric": "TFLOPS fwd+bwd of the head-parallel causal attention block on 1 GB300",
+        "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * dev_s / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{w.name} attention block (nb={w.nb}, s={w.s}, h={w.h}, nh={w.nh}, "
+                               f"d={w.d}, t={w.t}, causal)",
+                   "l2": "L2 flushed between timed steps (256 MiB write)",
+                   "flops": "projections 3 x (2 T h 3h + 2 T h h) + 12 d per visible pair per head"},
+        "pct_of_peak": {"burst": 100 * value / burst, "sustained": 100 * value / sustained,
+                        "source": src},
+        "per_call_ms": {k: round(v, 4) for k, v in per_call.items()},
+        "core_tflops": {k: round(v, 1) for k, v in core_tf.items()},
+        "roofline": roofline, "e2e": e2e, "clocks": clocks.summary(),
+        "gpu_launches": step.launches,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = attn_cpu_baseline(w, step.cpu)
+    print(json.dumps(line))
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.attention and args.impl == "ours":
+        return run_attention(args)
     if args.layernorm:
         return run_layernorm(args, workload(args))
     if args.impl == "reference":
