@@ -82,6 +82,26 @@ __device__ __forceinline__ uint32_t mnmajor_step(int kk) {
 
 __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
+// Stores 32 consecutive 32-bit TMEM columns of this thread's lane (same
+// lane quadrant rule as tmem_ld32).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0],"
+        " {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16,"
+        " %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+
 // tcgen05 MMA chain D (+)= A B^T where B is MN-major along d (the value or
 // query/key tile as the N operand, N = D): the N extent is issued as a
 // multiple of 64 (whole swizzle atoms) plus a 32-wide tail, so that no MMA
@@ -109,20 +129,10 @@ __device__ __forceinline__ void mma_n_is_d(uint32_t d_tmem, uint64_t a_desc, uin
 
 // ---------------------------------------------------------------- forward
 
-template <int D>
-struct FwdCfg {
-    static constexpr int NB = (D + 63) / 64;           // 64-column boxes per row
-    static constexpr int TILE = NB * 128 * kRowBytes;  // 128 rows x D (box-padded)
-    static constexpr int P_BYTES = 2 * 128 * kRowBytes;  // 128 x 128 bf16
-    static constexpr int STAGES_FIT = (225 * 1024 - TILE - P_BYTES) / TILE;
-    static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
-    static constexpr int SMEM = 1024 + TILE + P_BYTES + STAGES * TILE + 256;
-};
-
 struct AttnArgs {
     int nb, s, h, nh;
     long long T;
-    int q_tiles;     // tiles along the sequence of this kernel's row dimension
+    int q_tiles;     // work tiles along the sequence (forward: pairs of 128-row tiles)
     float scale2;    // log2(e) / sqrt(d)
     float scale;     // 1 / sqrt(d)
     __nv_bfloat16* O;        // forward output [T, h]
@@ -133,36 +143,59 @@ struct AttnArgs {
     int* status;
 };
 
+// The forward CTA owns two adjacent 128-query tiles of one (sequence, head),
+// A = rows q0..q0+127 and B = q0+128..q0+255, which share every K/V tile.
+// Each has its own softmax warpgroup (A: warps 0-3, B: warps 4-7), its own
+// S and O accumulators in TMEM (A at columns 0 and 128, B at 256 and 384) and
+// its own P buffer.  The MMA warp alternates between them (ping-pong): while
+// warpgroup A turns S_A into P_A, the tensor cores run B's P V and next
+// S, and the other way round.
+constexpr int kFwdThreads = 320;  // 8 softmax warps, producer, MMA
+constexpr float kRescaleLog2 = 8.0f;  // keep a stale row max while it is within 2^8
+
 template <int D>
-__global__ void __launch_bounds__(kAttnThreads, 1)
+struct FwdCfg {
+    static constexpr int NB = (D + 63) / 64;           // 64-column boxes per row
+    static constexpr int TILE = NB * 128 * kRowBytes;  // 128 rows x D (box-padded)
+    static constexpr int P_BYTES = 2 * 128 * kRowBytes;  // 128 x 128 bf16
+    static constexpr int FIXED = 2 * TILE + 2 * P_BYTES;
+    static constexpr int STAGES_FIT = (225 * 1024 - FIXED) / TILE;
+    static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
+    static constexpr int SMEM = 1024 + FIXED + STAGES * TILE + 256;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const AttnArgs a) {
     using C = FwdCfg<D>;
     constexpr int S = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-    uint8_t* sQ = smem;
-    uint8_t* sP = smem + C::TILE;
-    uint8_t* ring = sP + C::P_BYTES;
+    uint8_t* sQ = smem;                   // Q_A, Q_B
+    uint8_t* sP = smem + 2 * C::TILE;     // P_A, P_B
+    uint8_t* ring = sP + 2 * C::P_BYTES;  // K_0, V_0, K_1, V_1, ...
     uint64_t* bars = reinterpret_cast<uint64_t*>(ring + S * C::TILE);
     uint64_t* q_full = bars;
     uint64_t* kv_full = bars + 1;
     uint64_t* kv_empty = kv_full + S;
-    uint64_t* s_full = kv_empty + S;  // 2
-    uint64_t* p_full = s_full + 2;
-    uint64_t* pv_done = p_full + 1;
-    uint64_t* drain = pv_done + 1;
+    uint64_t* s_full = kv_empty + S;  // [tile]
+    uint64_t* p_full = s_full + 2;    // [tile]
+    uint64_t* pv_done = p_full + 2;   // [tile]
+    uint64_t* drain = pv_done + 2;
     uint32_t* misc = reinterpret_cast<uint32_t*>(drain + 1);
     volatile uint32_t* abort_flag = misc + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // heaviest query tiles (most key tiles) first
-    const int per_qt = a.nb * a.nh;
-    const int qt = a.q_tiles - 1 - static_cast<int>(blockIdx.x) / per_qt;
-    const int rem = static_cast<int>(blockIdx.x) % per_qt;
+    // heaviest pairs (most key tiles) first
+    const int per = a.nb * a.nh;
+    const int pair = a.q_tiles - 1 - static_cast<int>(blockIdx.x) / per;
+    const int rem = static_cast<int>(blockIdx.x) % per;
     const int n = rem / a.nh, head = rem % a.nh;
-    const int q0 = qt * 128;
-    const int n_kv = qt + 1;
+    const int q0 = pair * 256;
+    const bool has_b = q0 + 128 < a.s;
+    const int last[2] = {2 * pair, 2 * pair + 1};  // last (diagonal) key tile of A, B
+    const int n_kv = has_b ? last[1] + 1 : last[0] + 1;
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
@@ -170,15 +203,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_init(&kv_full[i], 1);
             mbar_init(&kv_empty[i], 1);
         }
-        mbar_init(&s_full[0], 1);
-        mbar_init(&s_full[1], 1);
-        mbar_init(p_full, 4);  // one arrival per softmax warp
-        mbar_init(pv_done, 1);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&s_full[x], 1);
+            mbar_init(&p_full[x], 4);  // one arrival per warp of the tile's warpgroup
+            mbar_init(&pv_done[x], 1);
+        }
         mbar_init(drain, 1);
         misc[1] = 0u;
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == 9) {
         tmem_alloc(&misc[0], 512);
         tmem_relinquish();
     }
@@ -186,204 +220,240 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
-    constexpr uint32_t kS0 = 0, kPV = 256;
+    // TMEM columns of tile x: S at 256 x, O at 256 x + 128
 
-    if (warp == 4) {
+    if (warp == 8) {
+        // ------------------------------------------------------ producer
         if (lane == 0) {
             prefetch_tmap(&tm_qkv);
             const int qcol = head * D, kcol = a.h + head * D, vcol = 2 * a.h + head * D;
-            mbar_arrive_expect_tx(q_full, C::TILE);
-            for (int b = 0; b < C::NB; ++b)
-                tma_load_3d(&tm_qkv, smem_u32(q_full), smem_u32(sQ) + b * 128 * kRowBytes,
-                            qcol + 64 * b, q0, n);
-            int stage = 0;
-            uint32_t phase = 0, issued = 0, issued_phase = 0;
-            bool ok = true;
-            auto load = [&](int col, int row) {
-                if (!ok) return;
-                if (!wait_bounded(&kv_empty[stage], phase ^ 1u, abort_flag, a.status, 0x101)) {
-                    ok = false;
-                    return;
-                }
+            mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * C::TILE);
+            for (int x = 0; x < (has_b ? 2 : 1); ++x)
+                for (int b = 0; b < C::NB; ++b)
+                    tma_load_3d(&tm_qkv, smem_u32(q_full),
+                                smem_u32(sQ) + x * C::TILE + b * 128 * kRowBytes, qcol + 64 * b,
+                                q0 + 128 * x, n);
+            uint32_t issued = 0, issued_phase = 0;
+            for (int idx = 0; idx < 2 * n_kv; ++idx) {  // K_j = 2j, V_j = 2j + 1
+                const int stage = idx % S;
+                const uint32_t phase = static_cast<uint32_t>(idx / S) & 1u;
+                if (!wait_bounded(&kv_empty[stage], phase ^ 1u, abort_flag, a.status, 0x101)) break;
                 mbar_arrive_expect_tx(&kv_full[stage], C::TILE);
                 const uint32_t dst = smem_u32(ring) + stage * C::TILE;
+                const int col = (idx & 1) ? vcol : kcol;
                 for (int b = 0; b < C::NB; ++b)
                     tma_load_3d(&tm_qkv, smem_u32(&kv_full[stage]), dst + b * 128 * kRowBytes,
-                                col + 64 * b, row, n);
+                                col + 64 * b, (idx >> 1) * 128, n);
                 issued |= 1u << stage;
                 issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-                if (++stage == S) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-            };
-            // the order the MMAs consume them: K0, K1, V0, K2, V1, ..., V_last
-            load(kcol, 0);
-            for (int j = 1; j < n_kv; ++j) {
-                load(kcol, j * 128);
-                load(vcol, (j - 1) * 128);
             }
-            load(vcol, (n_kv - 1) * 128);
             wait_drain(q_full, 0, a.status, 0x102);
             for (int i = 0; i < S; ++i)
                 if (issued & (1u << i)) wait_drain(&kv_full[i], (issued_phase >> i) & 1u, a.status, 0x103);
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == 9) {
+        // ------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
-            const uint64_t qdesc = smem_desc_sw128(smem_u32(sQ), 16, 1024);
-            const uint64_t pdesc = smem_desc_sw128(smem_u32(sP), 16, 1024);
-            int stage = 0;
-            uint32_t phase = 0;
             bool ok = wait_bounded(q_full, 0, abort_flag, a.status, 0x104);
             tc_fence_after();
-            auto next = [&]() {
-                if (++stage == S) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-            };
-            auto issue_pv = [&](int i) {
-                if (!ok) return;
-                if (!wait_bounded(p_full, static_cast<uint32_t>(i) & 1u, abort_flag, a.status, 0x105) ||
-                    !wait_bounded(&kv_full[stage], phase, abort_flag, a.status, 0x106)) {
+            // wait for ring entry idx (K_j = 2j, V_j = 2j + 1); returns its stage
+            auto acquire = [&](int idx, int site) -> int {
+                const int stage = idx % S;
+                if (ok && !wait_bounded(&kv_full[stage], static_cast<uint32_t>(idx / S) & 1u,
+                                        abort_flag, a.status, site))
                     ok = false;
-                    return;
-                }
                 tc_fence_after();
-                const uint64_t vdesc =
-                    smem_desc_sw128(smem_u32(ring) + stage * C::TILE, 128 * kRowBytes, 1024);
-                // O_part = P V: A = P (K-major, keys along the 128-byte rows), B = V
-                // (MN-major: d along the rows, keys down the box)
-                mma_n_is_d<D, 128 / 16>(tmem + kPV, pdesc, 128 * kRowBytes, vdesc,
-                                        128 * kRowBytes, false);
-                tc_commit(pv_done);
-                tc_commit(&kv_empty[stage]);
-                next();
+                return stage;
             };
-            for (int j = 0; j < n_kv && ok; ++j) {
-                if (!wait_bounded(&kv_full[stage], phase, abort_flag, a.status, 0x107)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
+            auto issue_s = [&](int x, int stage) {  // S_x = Q_x K^T
+                const uint64_t qdesc = smem_desc_sw128(smem_u32(sQ) + x * C::TILE, 16, 1024);
                 const uint64_t kdesc = smem_desc_sw128(smem_u32(ring) + stage * C::TILE, 16, 1024);
-                const uint32_t d_s = tmem + kS0 + (j & 1) * 128;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    tc_mma_f16(d_s, desc_add(qdesc, kmajor_step<128>(kk)),
+                    tc_mma_f16(tmem + 256 * x, desc_add(qdesc, kmajor_step<128>(kk)),
                                desc_add(kdesc, kmajor_step<128>(kk)), id_s, kk > 0 ? 1u : 0u);
-                tc_commit(&s_full[j & 1]);
-                tc_commit(&kv_empty[stage]);
-                next();
-                if (j >= 1) issue_pv(j - 1);
+                tc_commit(&s_full[x]);
+            };
+            auto issue_pv = [&](int x, int j, int stage) {  // O_x (+)= P_x V
+                if (ok && !wait_bounded(&p_full[x], static_cast<uint32_t>(j) & 1u, abort_flag,
+                                        a.status, 0x105 + x))
+                    ok = false;
+                if (!ok) return;
+                tc_fence_after();
+                const uint64_t pdesc = smem_desc_sw128(smem_u32(sP) + x * C::P_BYTES, 16, 1024);
+                const uint64_t vdesc =
+                    smem_desc_sw128(smem_u32(ring) + stage * C::TILE, 128 * kRowBytes, 1024);
+                mma_n_is_d<D, 128 / 16>(tmem + 256 * x + 128, pdesc, 128 * kRowBytes, vdesc,
+                                        128 * kRowBytes, j > 0);
+                tc_commit(&pv_done[x]);
+            };
+            // S of both tiles for key tile 0
+            int ks = acquire(0, 0x107);
+            if (ok) {
+                issue_s(0, ks);
+                if (has_b) issue_s(1, ks);
+                tc_commit(&kv_empty[ks]);
             }
-            issue_pv(n_kv - 1);
+            for (int j = 0; j < n_kv && ok; ++j) {
+                const int vs = acquire(2 * j + 1, 0x108);
+                const bool more = j + 1 < n_kv;
+                int kn = -1;
+                if (j <= last[0]) {
+                    issue_pv(0, j, vs);
+                    if (ok && j + 1 <= last[0]) {
+                        kn = acquire(2 * j + 2, 0x109);
+                        if (ok) issue_s(0, kn);
+                    }
+                }
+                if (has_b && ok) {
+                    issue_pv(1, j, vs);
+                    if (ok) tc_commit(&kv_empty[vs]);
+                    if (ok && more) {
+                        if (kn < 0) kn = acquire(2 * j + 2, 0x10A);
+                        if (ok) issue_s(1, kn);
+                    }
+                } else if (ok) {
+                    tc_commit(&kv_empty[vs]);
+                }
+                if (ok && kn >= 0) tc_commit(&kv_empty[kn]);
+            }
             tc_commit(drain);
-            wait_drain(drain, 0, a.status, 0x108);
+            wait_drain(drain, 0, a.status, 0x10B);
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------ softmax warps
-        const int r = threadIdx.x;  // row of the tile = TMEM lane
-        const int q = q0 + r;
-        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        const uint32_t p_row = smem_u32(sP) + static_cast<uint32_t>(r) * kRowBytes;
-        const uint32_t swz = static_cast<uint32_t>(r & 7);
-        float o[D];
-#pragma unroll
-        for (int i = 0; i < D; ++i) o[i] = 0.0f;
-        float m = -INFINITY, l = 0.0f, alpha_prev = 0.0f;
-        bool ok = true;
-        auto fold = [&](float alpha) {
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(lane_addr + kPV + c * 32, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) o[c * 32 + i] = fmaf(o[c * 32 + i], alpha, __uint_as_float(v[i]));
-            }
-        };
-        for (int j = 0; j < n_kv; ++j) {
-            if (!warp_wait_bounded(&s_full[j & 1], static_cast<uint32_t>(j >> 1) & 1u, abort_flag,
-                                   a.status, 0x109)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t s_addr = lane_addr + kS0 + (j & 1) * 128;
-            const bool diag = j == qt;  // keys k0 + c with c > r are masked there
-            float mx = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t v[32];
-                tmem_ld32(s_addr + c * 32, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (!diag || c * 32 + i <= r) mx = fmaxf(mx, __uint_as_float(v[i]));
-            }
-            const float m_new = fmaxf(m, mx * a.scale2);
-            const float alpha = ex2(m - m_new);
-            if (j >= 1) {
-                if (!warp_wait_bounded(pv_done, static_cast<uint32_t>(j - 1) & 1u, abort_flag, a.status,
-                                       0x10A)) {
+        // -------------------------------------------------- softmax warps
+        const int x = warp >> 2;               // tile: 0 = A, 1 = B
+        const int r = threadIdx.x & 127;       // row of the tile = TMEM lane
+        const int q = q0 + 128 * x + r;
+        if (x == 0 || has_b) {
+            const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + 256 * x;
+            const uint32_t p_row = smem_u32(sP) + x * C::P_BYTES + static_cast<uint32_t>(r) * kRowBytes;
+            const uint32_t swz = static_cast<uint32_t>(r & 7);
+            const int jl = last[x];
+            float m = -INFINITY, l = 0.0f;
+            bool ok = true;
+            for (int j = 0; j <= jl; ++j) {
+                if (!warp_wait_bounded(&s_full[x], static_cast<uint32_t>(j) & 1u, abort_flag,
+                                       a.status, 0x10C + x)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                fold(alpha_prev);
-            }
-            float rs = 0.0f;
+                uint32_t v[4][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t v[32];
-                tmem_ld32(s_addr + c * 32, v);
+                for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + c * 32, v[c]);
                 tmem_wait_ld();
-                float p[32];
+                const bool diag = j == jl;  // keys j*128 + c with c > r are masked there
+                if (diag) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const bool valid = !diag || c * 32 + i <= r;
-                    p[i] = valid ? ex2(fmaf(__uint_as_float(v[i]), a.scale2, -m_new)) : 0.0f;
-                    rs += p[i];
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (c * 32 + i > r) v[c][i] = __float_as_uint(-INFINITY);
                 }
-                stage_row(p_row + (c >> 1) * 128 * kRowBytes, c & 1, swz, p);
+                // eight independent max / sum chains: the row is one thread's
+                // work, so its reductions must not be one serial chain
+                float mx8[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(v[c][i]));
+                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                // the reference max only moves when the row max outgrows it by
+                // more than 2^8, so the O rescale below is rare
+                const float m_new = fmaxf(m, mx * a.scale2);
+                const bool move = j == 0 || m_new > m + kRescaleLog2;
+                const float alpha = move ? ex2(m - m_new) : 1.0f;
+                if (move) m = m_new;
+                float rs8[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) rs8[k] = 0.0f;
+                uint32_t pk[4][16];
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        // masked scores are -inf: 2^-inf = 0
+                        const float p0 = ex2(fmaf(__uint_as_float(v[c][2 * i]), a.scale2, -m));
+                        const float p1 = ex2(fmaf(__uint_as_float(v[c][2 * i + 1]), a.scale2, -m));
+                        rs8[i & 7] += p0 + p1;
+                        pk[c][i] = pack_bf16x2(p0, p1);
+                    }
+                const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+                l = fmaf(l, alpha, rs);
+                if (j >= 1) {
+                    // P V of the previous key tile has finished: P_x is free and O_x final
+                    if (!warp_wait_bounded(&pv_done[x], static_cast<uint32_t>(j - 1) & 1u, abort_flag,
+                                           a.status, 0x10E + x)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (__any_sync(0xFFFFFFFFu, move)) {
+#pragma unroll
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t o[32];
+                            tmem_ld32(lane_addr + 128 + c * 32, o);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                            tmem_st32(lane_addr + 128 + c * 32, o);
+                        }
+                        tmem_wait_st();
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t row = p_row + (c >> 1) * 128 * kRowBytes;
+                    const uint32_t half = static_cast<uint32_t>(c & 1);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        st_shared_v4(row + (((half * 4 + k) ^ swz) << 4), pk[c][4 * k], pk[c][4 * k + 1],
+                                     pk[c][4 * k + 2], pk[c][4 * k + 3]);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[x]);
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
-            l = fmaf(l, alpha, rs);
-            m = m_new;
-            alpha_prev = alpha;
-        }
-        if (ok && warp_wait_bounded(pv_done, static_cast<uint32_t>(n_kv - 1) & 1u, abort_flag,
-                                    a.status, 0x10B)) {
-            tc_fence_after();
-            fold(alpha_prev);
-            if (q < a.s) {
+            if (ok && warp_wait_bounded(&pv_done[x], static_cast<uint32_t>(jl) & 1u, abort_flag,
+                                        a.status, 0x110 + x)) {
+                tc_fence_after();
                 const float inv = 1.0f / l;
+                const bool q_ok = q < a.s;
                 const long long tok = static_cast<long long>(n) * a.s + q;
                 uint4* dst = reinterpret_cast<uint4*>(a.O + tok * a.h + head * D);
 #pragma unroll
-                for (int i = 0; i < D / 8; ++i) {
-                    uint4 u;
-                    u.x = pack_bf16x2(o[8 * i] * inv, o[8 * i + 1] * inv);
-                    u.y = pack_bf16x2(o[8 * i + 2] * inv, o[8 * i + 3] * inv);
-                    u.z = pack_bf16x2(o[8 * i + 4] * inv, o[8 * i + 5] * inv);
-                    u.w = pack_bf16x2(o[8 * i + 6] * inv, o[8 * i + 7] * inv);
-                    dst[i] = u;
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(lane_addr + 128 + c * 32, o);  // every lane: warp-collective
+                    tmem_wait_ld();
+                    if (q_ok) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            uint4 u;
+                            u.x = pack_bf16x2(__uint_as_float(o[8 * i]) * inv, __uint_as_float(o[8 * i + 1]) * inv);
+                            u.y = pack_bf16x2(__uint_as_float(o[8 * i + 2]) * inv, __uint_as_float(o[8 * i + 3]) * inv);
+                            u.z = pack_bf16x2(__uint_as_float(o[8 * i + 4]) * inv, __uint_as_float(o[8 * i + 5]) * inv);
+                            u.w = pack_bf16x2(__uint_as_float(o[8 * i + 6]) * inv, __uint_as_float(o[8 * i + 7]) * inv);
+                            dst[c * 4 + i] = u;
+                        }
+                    }
                 }
-                a.lse[head * a.T + tok] = m + lg2(l);
+                if (q_ok) a.lse[head * a.T + tok] = m + lg2(l);
             }
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -618,10 +688,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 tmem_wait_ld();
                 float ds[32];
                 const int key0 = j * 64 + c * 32;
+                // causal mask (keys after the query), only where this chunk
+                // reaches past the row's query; a masked score of -inf gives
+                // P = 0.  Rows past the sequence read zero Q and dO rows and
+                // are never stored, so they need no mask.
+                if (key0 + 31 > q) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (key0 + i > q) sv[i] = __float_as_uint(-INFINITY);
+                }
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const bool valid = q_ok && key0 + i <= q;
-                    const float p = valid ? ex2(fmaf(__uint_as_float(sv[i]), a.scale2, -lse)) : 0.0f;
+                    const float p = ex2(fmaf(__uint_as_float(sv[i]), a.scale2, -lse));
                     ds[i] = p * (__uint_as_float(pv[i]) - dlt);
                 }
                 stage_row(ds_row, c, swz, ds);
@@ -854,10 +932,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const uint32_t swz = static_cast<uint32_t>(r & 7);
         const float* lse_seq = a.lse_in + head * a.T + static_cast<long long>(n) * a.s;
         const float* dlt_seq = a.delta + head * a.T + static_cast<long long>(n) * a.s;
-        const bool vec_ok = ((reinterpret_cast<uintptr_t>(lse_seq) | reinterpret_cast<uintptr_t>(dlt_seq)) & 15u) == 0;
+        // lse and delta of a 64-query tile: lane l holds queries l and 32 + l
+        // (lse +inf and delta 0 past the sequence, so P = 0 there); the
+        // next tile's are loaded while this one is computed, and each chunk
+        // reads them by warp shuffle
+        auto fetch = [&](int i, float (&lv)[2], float (&dv)[2]) {
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int qq = (i0 + i) * 64 + 32 * h2 + lane;
+                const bool in = i < nq && qq < a.s;
+                lv[h2] = in ? __ldg(lse_seq + qq) : INFINITY;
+                dv[h2] = in ? __ldg(dlt_seq + qq) : 0.0f;
+            }
+        };
+        float lse_c[2], dlt_c[2];
+        fetch(0, lse_c, dlt_c);
         bool ok = true;
         for (int i = 0; i < nq; ++i) {
             const uint32_t b = static_cast<uint32_t>(i & 1);
+            float lse_n[2], dlt_n[2];
+            fetch(i + 1, lse_n, dlt_n);
             if (!warp_wait_bounded(&st_full[b], static_cast<uint32_t>(i >> 1) & 1u, abort_flag,
                                    a.status, 0x308) ||
                 (i >= 2 && !warp_wait_bounded(&pds_free[b], static_cast<uint32_t>((i >> 1) - 1) & 1u,
@@ -871,37 +965,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 const int qa = (i0 + i) * 64 + c * 32;  // first query of this chunk
-                float lse[32], dlt[32];
-                if (vec_ok && qa + 32 <= a.s) {
-                    const float4* l4 = reinterpret_cast<const float4*>(lse_seq + qa);
-                    const float4* d4 = reinterpret_cast<const float4*>(dlt_seq + qa);
-#pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        const float4 x = __ldg(l4 + v), y = __ldg(d4 + v);
-                        lse[4 * v] = x.x; lse[4 * v + 1] = x.y; lse[4 * v + 2] = x.z; lse[4 * v + 3] = x.w;
-                        dlt[4 * v] = y.x; dlt[4 * v + 1] = y.y; dlt[4 * v + 2] = y.z; dlt[4 * v + 3] = y.w;
-                    }
-                } else {
-#pragma unroll
-                    for (int v = 0; v < 32; ++v) {
-                        const bool in = qa + v < a.s;
-                        lse[v] = in ? __ldg(lse_seq + qa + v) : INFINITY;
-                        dlt[v] = in ? __ldg(dlt_seq + qa + v) : 0.0f;
-                    }
-                }
                 uint32_t sv[32], pv[32];
                 tmem_ld32(lane_addr + kST + 64 * b + c * 32, sv);
                 tmem_ld32(lane_addr + kDPT + 64 * b + c * 32, pv);
                 tmem_wait_ld();
+                // causal mask: queries before this row's key
+                if (qa < key) {
+#pragma unroll
+                    for (int v = 0; v < 32; ++v)
+                        if (qa + v < key) sv[v] = __float_as_uint(-INFINITY);
+                }
                 float p[32], ds[32];
 #pragma unroll
                 for (int v = 0; v < 32; ++v) {
-                    const bool valid = qa + v >= key && qa + v < a.s;
-                    p[v] = valid ? ex2(fmaf(__uint_as_float(sv[v]), a.scale2, -lse[v])) : 0.0f;
-                    ds[v] = p[v] * (__uint_as_float(pv[v]) - dlt[v]);
+                    const float lq = __shfl_sync(0xFFFFFFFFu, lse_c[c], v);
+                    const float dq = __shfl_sync(0xFFFFFFFFu, dlt_c[c], v);
+                    p[v] = ex2(fmaf(__uint_as_float(sv[v]), a.scale2, -lq));
+                    ds[v] = p[v] * (__uint_as_float(pv[v]) - dq);
                 }
                 stage_row(pt_row, c, swz, p);
                 stage_row(dst_row, c, swz, ds);
+            }
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                lse_c[h2] = lse_n[h2];
+                dlt_c[h2] = dlt_n[h2];
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -959,7 +1047,7 @@ cudaError_t launch_attn_forward(const CUtensorMap& tm_qkv128, int d, const AttnP
     AttnArgs a{};
     a.nb = p.nb; a.s = p.s; a.h = p.h; a.nh = p.nh;
     a.T = static_cast<long long>(p.nb) * p.s;
-    a.q_tiles = (p.s + 127) / 128;
+    a.q_tiles = (p.s + 255) / 256;  // pairs of 128-query tiles
     a.scale = 1.0f / sqrtf(static_cast<float>(d));
     a.scale2 = 1.4426950408889634f * a.scale;
     a.O = p.O;
@@ -971,7 +1059,7 @@ cudaError_t launch_attn_forward(const CUtensorMap& tm_qkv128, int d, const AttnP
     if (d == DD) {                                                                                \
         auto kern = attn_fwd_kernel<DD>;                                                          \
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<DD>::SMEM); \
-        if (e == cudaSuccess) kern<<<grid, kAttnThreads, FwdCfg<DD>::SMEM, st>>>(tm_qkv128, a);   \
+        if (e == cudaSuccess) kern<<<grid, kFwdThreads, FwdCfg<DD>::SMEM, st>>>(tm_qkv128, a);    \
     }
     TPMLP_ATTN_FWD(64)
     TPMLP_ATTN_FWD(96)
