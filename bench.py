@@ -601,7 +601,7 @@ class AttnStep:
             lambda: b.tp_mlp_row_sum(self.O, i["Wo"], i["bo"], i["residual"], w.t, Y=self.Y,
                                      workspace=self.ws),
             lambda: b.tp_mlp_bias_grad(i["dY"], db=self.dbo, partial=self.p_sum),
-            lambda: b.tp_mlp_dB(self.O, i["dY"], w.t, dB=self.dWo),
+            lambda: b.tp_mlp_dB(self.O, i["dY"], 1, dB=self.dWo),
             lambda: b.tp_mlp_dx(i["dY"], i["Wo"], 1, dX=self.dO, workspace=self.ws),
             lambda: b.tp_attn_core_backward(self.QKV, self.O, self.lse, self.dO, w.nb, w.nh,
                                             dQKV=self.dQKV, delta=self.delta),

@@ -1404,8 +1404,10 @@ TPMLP_API int tp_attn_backward(const tpmlp_bf16* dY, const tpmlp_bf16* X, const 
     float* colsum = reinterpret_cast<float*>(ws + L.colsum);
     // dbo = sum_rows dY (g backward: the identity on every shard)
     if (int rc = bias_grad(dY, T, h, dbo, colsum, st)) return rc;
-    // dWo_i = O_i^T dY (rows of Wo per shard)
-    if (int rc = dB_gemm(O, dY, T, h, h, t, dWo, st, d)) return rc;
+    // dWo_i = O_i^T dY: shard i's rows of dWo.  No sum crosses the shards,
+    // so all rows are one GEMM (t only labels them), free of the ragged
+    // per-shard row tiles that h / t rows would leave
+    if (int rc = dB_gemm(O, dY, T, h, h, 1, dWo, st, d)) return rc;
     // dO = dY Wo^T: shard i's columns of dO from its rows of Wo, no sum
     if (int rc = dx_gemm(dY, Wo, T, h, h, 1, dO, ws + L.split, L.total - L.split, st, d)) return rc;
     // local attention backward of every head
