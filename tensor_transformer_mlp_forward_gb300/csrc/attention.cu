@@ -462,27 +462,36 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 // ------------------------------------------------------------ delta
 
 // delta[head, tok] = sum_c dO[tok, head*d + c] * O[tok, head*d + c], fp32;
-// one thread per (token, head).
+// one thread per (token, head).  All of a thread's 16-byte loads are issued
+// before any product, so each thread keeps d/4 loads in flight.
+template <int D>
 __global__ void __launch_bounds__(256)
     attn_delta_kernel(const __nv_bfloat16* __restrict__ dO, const __nv_bfloat16* __restrict__ O,
-                      long long T, int h, int nh, int d, float* __restrict__ delta) {
+                      long long T, int h, int nh, float* __restrict__ delta) {
     const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (idx >= T * nh) return;
     const long long tok = idx / nh;
     const int head = static_cast<int>(idx - tok * nh);
-    const uint4* g = reinterpret_cast<const uint4*>(dO + tok * h + head * d);
-    const uint4* o = reinterpret_cast<const uint4*>(O + tok * h + head * d);
-    float acc = 0.0f;
-    for (int i = 0; i < d / 8; ++i) {
-        const uint4 gu = __ldg(g + i), ou = __ldg(o + i);
-        const uint32_t gw[4] = {gu.x, gu.y, gu.z, gu.w}, ow[4] = {ou.x, ou.y, ou.z, ou.w};
+    const uint4* g = reinterpret_cast<const uint4*>(dO + tok * h + head * D);
+    const uint4* o = reinterpret_cast<const uint4*>(O + tok * h + head * D);
+    uint4 gu[D / 8], ou[D / 8];
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) {
+        gu[i] = __ldg(g + i);
+        ou[i] = __ldg(o + i);
+    }
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) {
+        const uint32_t gw[4] = {gu[i].x, gu[i].y, gu[i].z, gu[i].w};
+        const uint32_t ow[4] = {ou[i].x, ou[i].y, ou[i].z, ou[i].w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            acc = fmaf(__uint_as_float(gw[j] << 16), __uint_as_float(ow[j] << 16), acc);
-            acc = fmaf(__uint_as_float(gw[j] & 0xFFFF0000u), __uint_as_float(ow[j] & 0xFFFF0000u), acc);
+            acc[j] = fmaf(__uint_as_float(gw[j] << 16), __uint_as_float(ow[j] << 16), acc[j]);
+            acc[j] = fmaf(__uint_as_float(gw[j] & 0xFFFF0000u), __uint_as_float(ow[j] & 0xFFFF0000u), acc[j]);
         }
     }
-    delta[static_cast<long long>(head) * T + tok] = acc;
+    delta[static_cast<long long>(head) * T + tok] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
 
 // ------------------------------------------------------------- dQ
@@ -1085,8 +1094,10 @@ cudaError_t launch_attn_backward(const CUtensorMap& tm_qkv128, const CUtensorMap
     // delta = rowsum(dO * O)
     {
         const long long items = a.T * p.nh;
-        attn_delta_kernel<<<static_cast<unsigned>((items + 255) / 256), 256, 0, st>>>(
-            p.dO, p.O_in, a.T, p.h, p.nh, d, p.delta_out);
+        const unsigned blocks = static_cast<unsigned>((items + 255) / 256);
+        if (d == 64) attn_delta_kernel<64><<<blocks, 256, 0, st>>>(p.dO, p.O_in, a.T, p.h, p.nh, p.delta_out);
+        if (d == 96) attn_delta_kernel<96><<<blocks, 256, 0, st>>>(p.dO, p.O_in, a.T, p.h, p.nh, p.delta_out);
+        if (d == 128) attn_delta_kernel<128><<<blocks, 256, 0, st>>>(p.dO, p.O_in, a.T, p.h, p.nh, p.delta_out);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         ++*launches;
