@@ -420,7 +420,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 int k0 = kb_in_shard * BK;
                 bool ok = true;
                 for (int kb = kb_begin; kb < kb_end; ++kb) {
-                    if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
+                    if (!wait_bounded<true>(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
@@ -471,7 +471,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int tile = unit; tile < p.num_tiles; tile += units, ++count) {
                 const int acc = count & 1;
                 const uint32_t acc_phase = (count >> 1) & 1;
-                if (!wait_bounded(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
+                if (!wait_bounded<true>(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 const int ks = p.k_splits > 1 ? tile / p.base_tiles : 0;
@@ -479,7 +479,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int kb_end = (ks + 1) * total_kb / p.k_splits;
                 bool ok = true;
                 for (int kb = kb_begin; kb < kb_end; ++kb) {
-                    if (!wait_bounded(&full[stage], phase, abort_flag, p.status)) {
+                    if (!wait_bounded<true>(&full[stage], phase, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
@@ -558,7 +558,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int v0 = row_ok ? min(32, p.N - tc.n0) : 0;
                 load_raw32(p.aux + grow * p.ld_aux + gcol0, v0, aux_cur);
             }
-            if (!warp_wait_bounded(&acc_full[acc], acc_phase, abort_flag, p.status)) break;
+            if (!warp_wait_bounded<true>(&acc_full[acc], acc_phase, abort_flag, p.status)) break;
             tc_fence_after();
 
             if constexpr (EPI == EPI_PARTIAL) {

@@ -54,12 +54,37 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread sleeps until the phase
+// completes (or the hint, in ns, runs out) instead of spinning, so a role
+// that waits for long stretches takes no issue slots or power from the
+// others.
+constexpr uint32_t kSuspendHintNs = 1000000u;
+
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
+        : "memory");
+    return ok != 0;
+}
+
+template <bool SLEEP>
+__device__ __forceinline__ bool mbar_poll(uint64_t* bar, uint32_t parity) {
+    return SLEEP ? mbar_try_wait_sleep(bar, parity) : mbar_try_wait(bar, parity);
+}
+
 // Waits for the phase of `bar` with the given parity to complete.  Gives up
 // after kWaitLimitNs, or as soon as another role of the CTA has given up
 // (*abort != 0): on its own timeout it raises *abort, writes the timeout
 // code to the device status word status[0] and, when `site` is nonzero and
 // no earlier wait has done so, records `site` in status[1] so that the host
 // can tell which wait gave up first.  Returns false when it gave up.
+// SLEEP selects the suspending try_wait (see mbar_try_wait_sleep).
+template <bool SLEEP = false>
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
                                              volatile uint32_t* abort, int* status, int site = 0) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -67,7 +92,7 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+            if (mbar_poll<SLEEP>(bar, parity)) return true;
         if (*abort) return false;
         if (global_ns() - t0 > kWaitLimitNs) {
             *abort = 1u;
@@ -82,11 +107,12 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
 // so the warp leaves its loops together (a lane-divergent exit would strand
 // the other lanes at the warp's next __syncwarp).  The closing __syncwarp
 // orders the other lanes' later reads after lane 0's observation.
+template <bool SLEEP = false>
 __device__ __forceinline__ bool warp_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   volatile uint32_t* abort, int* status,
                                                   int site = 0) {
     uint32_t ok = 1u;
-    if ((threadIdx.x & 31) == 0) ok = wait_bounded(bar, parity, abort, status, site) ? 1u : 0u;
+    if ((threadIdx.x & 31) == 0) ok = wait_bounded<SLEEP>(bar, parity, abort, status, site) ? 1u : 0u;
     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
     __syncwarp();
     return ok != 0u;
