@@ -127,6 +127,49 @@ __device__ __forceinline__ void mma_n_is_d(uint32_t d_tmem, uint64_t a_desc, uin
     }
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T, bf16 x bf16 -> f32: the A operand (128
+// rows = TMEM lanes, 16 k values packed two bf16 to a 32-bit column, low
+// half first) is read from tensor memory.
+__device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// 16 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0],"
+        " {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
+
+// The same chain as mma_n_is_d with A in tensor memory: k-step kk reads the
+// 8 columns a_tmem + 8 kk.
+template <int D, int KSTEPS>
+__device__ __forceinline__ void mma_ts_n_is_d(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t box_bytes, bool accumulate_first) {
+    constexpr int N1 = (D / 64) * 64;
+    constexpr int N2 = D - N1;
+    constexpr uint32_t id1 = idesc_bf16_f32(128, N1 > 0 ? N1 : 64, false, true);
+    constexpr uint32_t id2 = idesc_bf16_f32(128, N2 > 0 ? N2 : 32, false, true);
+#pragma unroll
+    for (int kk = 0; kk < KSTEPS; ++kk) {
+        const uint32_t acc = (accumulate_first || kk > 0) ? 1u : 0u;
+        const uint64_t bd = desc_add(b_desc, mnmajor_step(kk));
+        if constexpr (N1 > 0) tc_mma_f16_ts(d_tmem, a_tmem + 8 * kk, bd, id1, acc);
+        if constexpr (N2 > 0)
+            tc_mma_f16_ts(d_tmem + N1, a_tmem + 8 * kk, desc_add(bd, (N1 / 64) * box_bytes), id2, acc);
+    }
+}
+
 // ---------------------------------------------------------------- forward
 
 struct AttnArgs {
@@ -758,8 +801,7 @@ struct DkvCfg {
     static constexpr int NB = (D + 63) / 64;
     static constexpr int KEY_TILE = NB * 128 * kRowBytes;  // K or V: 128 rows
     static constexpr int Q_TILE = NB * 64 * kRowBytes;     // Q or dO: 64 rows
-    static constexpr int PT_BYTES = 128 * kRowBytes;       // 128 keys x 64 queries
-    static constexpr int FIXED = 2 * KEY_TILE + 4 * PT_BYTES;  // P^T and dS^T, 2 each
+    static constexpr int FIXED = 2 * KEY_TILE;
     static constexpr int STAGES_FIT = (225 * 1024 - FIXED) / (2 * Q_TILE);
     static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
     static constexpr int SMEM = 1024 + FIXED + STAGES * 2 * Q_TILE + 256;
@@ -778,17 +820,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     uint8_t* sK = smem;
     uint8_t* sV = sK + C::KEY_TILE;
-    uint8_t* sPT = sV + C::KEY_TILE;       // 2 buffers
-    uint8_t* sdST = sPT + 2 * C::PT_BYTES;  // 2 buffers
-    uint8_t* ring = sdST + 2 * C::PT_BYTES;
+    uint8_t* ring = sV + C::KEY_TILE;
     uint64_t* bars = reinterpret_cast<uint64_t*>(ring + S * 2 * C::Q_TILE);
     uint64_t* kv_full = bars;
     uint64_t* q_full = bars + 1;
     uint64_t* q_empty = q_full + S;
     uint64_t* st_full = q_empty + S;  // 2
     uint64_t* pds_full = st_full + 2;  // 2
-    uint64_t* pds_free = pds_full + 2;  // 2
-    uint64_t* grad_done = pds_free + 2;
+    uint64_t* grad_done = pds_full + 2;
     uint64_t* drain = grad_done + 1;
     uint32_t* misc = reinterpret_cast<uint32_t*>(drain + 1);
     volatile uint32_t* abort_flag = misc + 1;
@@ -813,7 +852,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(&st_full[b], 1);
             mbar_init(&pds_full[b], 4);
-            mbar_init(&pds_free[b], 1);
         }
         mbar_init(grad_done, 1);
         mbar_init(drain, 1);
@@ -888,18 +926,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t qd = smem_u32(ring) + st * 2 * C::Q_TILE;
-                // dV += P^T dO and dK += dS^T Q: A = P^T / dS^T (K-major, queries
-                // along the rows), B = dO / Q (MN-major: d along the rows,
-                // queries down the 64-row box)
-                const uint64_t ptdesc = smem_desc_sw128(smem_u32(sPT) + (i & 1) * C::PT_BYTES, 16, 1024);
-                const uint64_t dstdesc = smem_desc_sw128(smem_u32(sdST) + (i & 1) * C::PT_BYTES, 16, 1024);
+                // dV += P^T dO and dK += dS^T Q: A = P^T / dS^T from TMEM (the
+                // softmax threads wrote them, packed bf16, over the first 32
+                // columns of the S^T / dP^T buffer), B = dO / Q (MN-major: d
+                // along the rows, queries down the 64-row box)
                 const uint64_t dodesc = smem_desc_sw128(qd + C::Q_TILE, 64 * kRowBytes, 1024);
                 const uint64_t qdesc = smem_desc_sw128(qd, 64 * kRowBytes, 1024);
-                mma_n_is_d<D, 64 / 16>(tmem + kDV, ptdesc, 128 * kRowBytes, dodesc,
-                                       64 * kRowBytes, i > 0);
-                mma_n_is_d<D, 64 / 16>(tmem + kDK, dstdesc, 128 * kRowBytes, qdesc,
-                                       64 * kRowBytes, i > 0);
-                tc_commit(&pds_free[i & 1]);
+                const uint32_t b = static_cast<uint32_t>(i & 1);
+                mma_ts_n_is_d<D, 64 / 16>(tmem + kDV, tmem + kST + 64 * b, dodesc, 64 * kRowBytes, i > 0);
+                mma_ts_n_is_d<D, 64 / 16>(tmem + kDK, tmem + kDPT + 64 * b, qdesc, 64 * kRowBytes, i > 0);
                 tc_commit(&q_empty[st]);
             };
             for (int i = 0; i < nq && ok; ++i) {
@@ -938,7 +973,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int r = threadIdx.x;
         const int key = k0 + r;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        const uint32_t swz = static_cast<uint32_t>(r & 7);
         const float* lse_seq = a.lse_in + head * a.T + static_cast<long long>(n) * a.s;
         const float* dlt_seq = a.delta + head * a.T + static_cast<long long>(n) * a.s;
         // lse and delta of a 64-query tile: lane l holds queries l and 32 + l
@@ -961,16 +995,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const uint32_t b = static_cast<uint32_t>(i & 1);
             float lse_n[2], dlt_n[2];
             fetch(i + 1, lse_n, dlt_n);
+            // S^T(i) was issued after dV/dK(i-2), which read this buffer's
+            // previous P^T / dS^T, so once it is here the buffer is free
             if (!warp_wait_bounded(&st_full[b], static_cast<uint32_t>(i >> 1) & 1u, abort_flag,
-                                   a.status, 0x308) ||
-                (i >= 2 && !warp_wait_bounded(&pds_free[b], static_cast<uint32_t>((i >> 1) - 1) & 1u,
-                                              abort_flag, a.status, 0x309))) {
+                                   a.status, 0x308)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t pt_row = smem_u32(sPT) + b * C::PT_BYTES + static_cast<uint32_t>(r) * kRowBytes;
-            const uint32_t dst_row = smem_u32(sdST) + b * C::PT_BYTES + static_cast<uint32_t>(r) * kRowBytes;
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 const int qa = (i0 + i) * 64 + c * 32;  // first query of this chunk
@@ -984,23 +1016,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     for (int v = 0; v < 32; ++v)
                         if (qa + v < key) sv[v] = __float_as_uint(-INFINITY);
                 }
-                float p[32], ds[32];
+                uint32_t pp[16], dd[16];
 #pragma unroll
-                for (int v = 0; v < 32; ++v) {
-                    const float lq = __shfl_sync(0xFFFFFFFFu, lse_c[c], v);
-                    const float dq = __shfl_sync(0xFFFFFFFFu, dlt_c[c], v);
-                    p[v] = ex2(fmaf(__uint_as_float(sv[v]), a.scale2, -lq));
-                    ds[v] = p[v] * (__uint_as_float(pv[v]) - dq);
+                for (int v = 0; v < 16; ++v) {
+                    float p2[2], d2[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int u = 2 * v + e;
+                        const float lq = __shfl_sync(0xFFFFFFFFu, lse_c[c], u);
+                        const float dq = __shfl_sync(0xFFFFFFFFu, dlt_c[c], u);
+                        p2[e] = ex2(fmaf(__uint_as_float(sv[u]), a.scale2, -lq));
+                        d2[e] = p2[e] * (__uint_as_float(pv[u]) - dq);
+                    }
+                    pp[v] = pack_bf16x2(p2[0], p2[1]);
+                    dd[v] = pack_bf16x2(d2[0], d2[1]);
                 }
-                stage_row(pt_row, c, swz, p);
-                stage_row(dst_row, c, swz, ds);
+                // P^T and dS^T, packed, over the columns this thread has read
+                tmem_st16(lane_addr + kST + 64 * b + 16 * c, pp);
+                tmem_st16(lane_addr + kDPT + 64 * b + 16 * c, dd);
             }
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
                 lse_c[h2] = lse_n[h2];
                 dlt_c[h2] = dlt_n[h2];
             }
-            fence_proxy_async_smem();
+            tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&pds_full[b]);
