@@ -189,10 +189,11 @@ struct AttnArgs {
 // The forward CTA owns two adjacent 128-query tiles of one (sequence, head),
 // A = rows q0..q0+127 and B = q0+128..q0+255, which share every K/V tile.
 // Each has its own softmax warpgroup (A: warps 0-3, B: warps 4-7), its own
-// S and O accumulators in TMEM (A at columns 0 and 128, B at 256 and 384) and
-// its own P buffer.  The MMA warp alternates between them (ping-pong): while
-// warpgroup A turns S_A into P_A, the tensor cores run B's P V and next
-// S, and the other way round.
+// S and O accumulators in TMEM (A at columns 0 and 128, B at 256 and 384).
+// P goes back into TMEM, packed bf16 over the first 64 columns of S, and is
+// the A operand of P V from there.  The MMA warp alternates between the tiles
+// (ping-pong): while warpgroup A turns S_A into P_A, the tensor cores run B's
+// P V and next S, and the other way round.
 constexpr int kFwdThreads = 320;  // 8 softmax warps, producer, MMA
 constexpr float kRescaleLog2 = 8.0f;  // keep a stale row max while it is within 2^8
 
@@ -200,8 +201,7 @@ template <int D>
 struct FwdCfg {
     static constexpr int NB = (D + 63) / 64;           // 64-column boxes per row
     static constexpr int TILE = NB * 128 * kRowBytes;  // 128 rows x D (box-padded)
-    static constexpr int P_BYTES = 2 * 128 * kRowBytes;  // 128 x 128 bf16
-    static constexpr int FIXED = 2 * TILE + 2 * P_BYTES;
+    static constexpr int FIXED = 2 * TILE;
     static constexpr int STAGES_FIT = (225 * 1024 - FIXED) / TILE;
     static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
     static constexpr int SMEM = 1024 + FIXED + STAGES * TILE + 256;
@@ -215,9 +215,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-    uint8_t* sQ = smem;                   // Q_A, Q_B
-    uint8_t* sP = smem + 2 * C::TILE;     // P_A, P_B
-    uint8_t* ring = sP + 2 * C::P_BYTES;  // K_0, V_0, K_1, V_1, ...
+    uint8_t* sQ = smem;                 // Q_A, Q_B
+    uint8_t* ring = smem + 2 * C::TILE;  // K_0, V_0, K_1, V_1, ...
     uint64_t* bars = reinterpret_cast<uint64_t*>(ring + S * C::TILE);
     uint64_t* q_full = bars;
     uint64_t* kv_full = bars + 1;
@@ -325,11 +324,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     ok = false;
                 if (!ok) return;
                 tc_fence_after();
-                const uint64_t pdesc = smem_desc_sw128(smem_u32(sP) + x * C::P_BYTES, 16, 1024);
+                // O_x (+)= P_x V: A = P_x from TMEM (packed over S_x's first 64
+                // columns), B = V (MN-major: d along the rows, keys down the box)
                 const uint64_t vdesc =
                     smem_desc_sw128(smem_u32(ring) + stage * C::TILE, 128 * kRowBytes, 1024);
-                mma_n_is_d<D, 128 / 16>(tmem + 256 * x + 128, pdesc, 128 * kRowBytes, vdesc,
-                                        128 * kRowBytes, j > 0);
+                mma_ts_n_is_d<D, 128 / 16>(tmem + 256 * x + 128, tmem + 256 * x, vdesc,
+                                           128 * kRowBytes, j > 0);
                 tc_commit(&pv_done[x]);
             };
             // S of both tiles for key tile 0
@@ -373,8 +373,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int q = q0 + 128 * x + r;
         if (x == 0 || has_b) {
             const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + 256 * x;
-            const uint32_t p_row = smem_u32(sP) + x * C::P_BYTES + static_cast<uint32_t>(r) * kRowBytes;
-            const uint32_t swz = static_cast<uint32_t>(r & 7);
             const int jl = last[x];
             float m = -INFINITY, l = 0.0f;
             bool ok = true;
@@ -430,14 +428,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     }
                 const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
                 l = fmaf(l, alpha, rs);
+                // S_x(j) was issued after P_x V of the previous key tile, and the
+                // commit that signalled S_x covers every earlier MMA: that P V
+                // has finished, so O_x is final and P_x's columns are free
                 if (j >= 1) {
-                    // P V of the previous key tile has finished: P_x is free and O_x final
-                    if (!warp_wait_bounded(&pv_done[x], static_cast<uint32_t>(j - 1) & 1u, abort_flag,
-                                           a.status, 0x10E + x)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
                     if (__any_sync(0xFFFFFFFFu, move)) {
 #pragma unroll
                         for (int c = 0; c < D / 32; ++c) {
@@ -451,16 +445,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                         tmem_wait_st();
                     }
                 }
+                // P_x, packed bf16, over the first 64 columns of S_x (already read)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint32_t row = p_row + (c >> 1) * 128 * kRowBytes;
-                    const uint32_t half = static_cast<uint32_t>(c & 1);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        st_shared_v4(row + (((half * 4 + k) ^ swz) << 4), pk[c][4 * k], pk[c][4 * k + 1],
-                                     pk[c][4 * k + 2], pk[c][4 * k + 3]);
-                }
-                fence_proxy_async_smem();
+                for (int c = 0; c < 4; ++c) tmem_st16(lane_addr + 16 * c, pk[c]);
+                tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[x]);
@@ -544,8 +532,7 @@ struct DqCfg {
     static constexpr int NB = (D + 63) / 64;
     static constexpr int ROW_TILE = NB * 128 * kRowBytes;  // Q or dO: 128 rows
     static constexpr int KV_TILE = NB * 64 * kRowBytes;    // K or V: 64 rows
-    static constexpr int DS_BYTES = 128 * kRowBytes;       // 128 x 64 bf16
-    static constexpr int FIXED = 2 * ROW_TILE + 2 * DS_BYTES;
+    static constexpr int FIXED = 2 * ROW_TILE;
     static constexpr int STAGES_FIT = (225 * 1024 - FIXED) / (2 * KV_TILE);
     static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
     static constexpr int SMEM = 1024 + FIXED + STAGES * 2 * KV_TILE + 256;
@@ -564,16 +551,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     uint8_t* sQ = smem;
     uint8_t* sdO = sQ + C::ROW_TILE;
-    uint8_t* sdS = sdO + C::ROW_TILE;  // 2 buffers
-    uint8_t* ring = sdS + 2 * C::DS_BYTES;
+    uint8_t* ring = sdO + C::ROW_TILE;
     uint64_t* bars = reinterpret_cast<uint64_t*>(ring + S * 2 * C::KV_TILE);
     uint64_t* q_full = bars;
     uint64_t* kv_full = bars + 1;
     uint64_t* kv_empty = kv_full + S;
     uint64_t* sdp_full = kv_empty + S;  // 2
     uint64_t* ds_full = sdp_full + 2;   // 2
-    uint64_t* ds_free = ds_full + 2;    // 2
-    uint64_t* dq_done = ds_free + 2;
+    uint64_t* dq_done = ds_full + 2;
     uint64_t* drain = dq_done + 1;
     uint32_t* misc = reinterpret_cast<uint32_t*>(drain + 1);
     volatile uint32_t* abort_flag = misc + 1;
@@ -597,7 +582,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(&sdp_full[b], 1);
             mbar_init(&ds_full[b], 4);
-            mbar_init(&ds_free[b], 1);
         }
         mbar_init(dq_done, 1);
         mbar_init(drain, 1);
@@ -669,15 +653,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     return;
                 }
                 tc_fence_after();
-                // dQ += dS K: A = dS (K-major, keys along the rows), B = K
+                // dQ += dS K: A = dS from TMEM (the softmax threads wrote it,
+                // packed bf16, over the first 32 columns of the S buffer), B = K
                 // (MN-major: d along the rows, keys down the 64-row box)
-                const uint64_t dsdesc =
-                    smem_desc_sw128(smem_u32(sdS) + (i & 1) * C::DS_BYTES, 16, 1024);
                 const uint64_t kdesc = smem_desc_sw128(smem_u32(ring) + st * 2 * C::KV_TILE,
                                                        64 * kRowBytes, 1024);
-                mma_n_is_d<D, 64 / 16>(tmem + kDQ, dsdesc, 128 * kRowBytes, kdesc,
-                                       64 * kRowBytes, i > 0);
-                tc_commit(&ds_free[i & 1]);
+                mma_ts_n_is_d<D, 64 / 16>(tmem + kDQ, tmem + kS + 64 * (i & 1), kdesc,
+                                          64 * kRowBytes, i > 0);
                 tc_commit(&kv_empty[st]);
             };
             for (int j = 0; j < n_kv && ok; ++j) {
@@ -719,26 +701,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const float lse = q_ok ? __ldg(a.lse_in + head * a.T + tok) : 0.0f;
         const float dlt = q_ok ? __ldg(a.delta + head * a.T + tok) : 0.0f;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        const uint32_t swz = static_cast<uint32_t>(r & 7);
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
             const uint32_t b = static_cast<uint32_t>(j & 1);
+            // S(j) was issued after dQ(j-2), which read this buffer's
+            // previous dS, so once it is here the buffer is free
             if (!warp_wait_bounded(&sdp_full[b], static_cast<uint32_t>(j >> 1) & 1u, abort_flag,
-                                   a.status, 0x208) ||
-                (j >= 2 && !warp_wait_bounded(&ds_free[b], static_cast<uint32_t>((j >> 1) - 1) & 1u,
-                                              abort_flag, a.status, 0x209))) {
+                                   a.status, 0x208)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t ds_row = smem_u32(sdS) + b * C::DS_BYTES + static_cast<uint32_t>(r) * kRowBytes;
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 uint32_t sv[32], pv[32];
                 tmem_ld32(lane_addr + kS + 64 * b + c * 32, sv);
                 tmem_ld32(lane_addr + kDP + 64 * b + c * 32, pv);
                 tmem_wait_ld();
-                float ds[32];
                 const int key0 = j * 64 + c * 32;
                 // causal mask (keys after the query), only where this chunk
                 // reaches past the row's query; a masked score of -inf gives
@@ -749,14 +728,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     for (int i = 0; i < 32; ++i)
                         if (key0 + i > q) sv[i] = __float_as_uint(-INFINITY);
                 }
+                uint32_t dd[16];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float p = ex2(fmaf(__uint_as_float(sv[i]), a.scale2, -lse));
-                    ds[i] = p * (__uint_as_float(pv[i]) - dlt);
+                for (int i = 0; i < 16; ++i) {
+                    const float p0 = ex2(fmaf(__uint_as_float(sv[2 * i]), a.scale2, -lse));
+                    const float p1 = ex2(fmaf(__uint_as_float(sv[2 * i + 1]), a.scale2, -lse));
+                    dd[i] = pack_bf16x2(p0 * (__uint_as_float(pv[2 * i]) - dlt),
+                                        p1 * (__uint_as_float(pv[2 * i + 1]) - dlt));
                 }
-                stage_row(ds_row, c, swz, ds);
+                // dS, packed, over the S columns this thread has read
+                tmem_st16(lane_addr + kS + 64 * b + 16 * c, dd);
             }
-            fence_proxy_async_smem();
+            tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ds_full[b]);
