@@ -358,8 +358,9 @@ int tp_mlp_backward_dropout(const tpmlp_bf16* dY, const tpmlp_bf16* X, const tpm
  * models; the page fixes only the split, the rest is the plain reading.
  *
  * Rules (else TPMLP_ERR_SHAPE): nb >= 0, s >= 1, h % 8 == 0, nh >= 1,
- * h % nh == 0, d = h / nh in {64, 96, 128} (the head dims with a compiled
- * kernel: GPT-2 355M, 2.5B and 8.3B of the page's Table 2), 1 <= t <= 64,
+ * h % nh == 0, d = h / nh in {64, 96, 128, 160} (the head dims with a
+ * compiled kernel: GPT-2 355M, 2.5B and 8.3B of the Megatron-LM page's
+ * Table 2, and MT-NLG 530B's 20480 / 128), 1 <= t <= 64,
  * nh % t == 0, T < 2^31.  nb == 0 is an empty batch.  Pointers, ownership,
  * streams and status codes as for the MLP block above. */
 

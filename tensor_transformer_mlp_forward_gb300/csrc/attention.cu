@@ -152,10 +152,12 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 }
 
 // The same chain as mma_n_is_d with A in tensor memory: k-step kk reads the
-// 8 columns a_tmem + 8 kk.
+// 8 columns a_tmem + 8 kk.  The 32-wide tail of N = d (d % 64 == 32) goes to
+// columns d_tail (d_tmem + the whole atoms' width unless given).
 template <int D, int KSTEPS>
 __device__ __forceinline__ void mma_ts_n_is_d(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                              uint32_t box_bytes, bool accumulate_first) {
+                                              uint32_t box_bytes, bool accumulate_first,
+                                              uint32_t d_tail = 0xFFFFFFFFu) {
     constexpr int N1 = (D / 64) * 64;
     constexpr int N2 = D - N1;
     constexpr uint32_t id1 = idesc_bf16_f32(128, N1 > 0 ? N1 : 64, false, true);
@@ -166,7 +168,8 @@ __device__ __forceinline__ void mma_ts_n_is_d(uint32_t d_tmem, uint32_t a_tmem, 
         const uint64_t bd = desc_add(b_desc, mnmajor_step(kk));
         if constexpr (N1 > 0) tc_mma_f16_ts(d_tmem, a_tmem + 8 * kk, bd, id1, acc);
         if constexpr (N2 > 0)
-            tc_mma_f16_ts(d_tmem + N1, a_tmem + 8 * kk, desc_add(bd, (N1 / 64) * box_bytes), id2, acc);
+            tc_mma_f16_ts(d_tail == 0xFFFFFFFFu ? d_tmem + N1 : d_tail, a_tmem + 8 * kk,
+                          desc_add(bd, (N1 / 64) * box_bytes), id2, acc);
     }
 }
 
@@ -188,36 +191,57 @@ struct AttnArgs {
 
 // The forward CTA owns two adjacent 128-query tiles of one (sequence, head),
 // A = rows q0..q0+127 and B = q0+128..q0+255, which share every K/V tile.
-// Each has its own softmax warpgroup (A: warps 0-3, B: warps 4-7), its own
-// S and O accumulators in TMEM (A at columns 0 and 128, B at 256 and 384).
-// P goes back into TMEM, packed bf16 over the first 64 columns of S, and is
-// the A operand of P V from there.  The MMA warp alternates between the tiles
-// (ping-pong): while warpgroup A turns S_A into P_A, the tensor cores run B's
-// P V and next S, and the other way round.
+// Each has its own softmax warpgroup (A: warps 0-3, B: warps 4-7) and its own
+// S and O accumulators in TMEM.  P goes back into TMEM, packed bf16 over the
+// first columns of S, and is the A operand of P V from there.  The MMA warp
+// alternates between the tiles (ping-pong): while warpgroup A turns S_A into
+// P_A, the tensor cores run B's P V and next S, and the other way round.
+// Key tiles are 128 keys for d <= 128 and 64 keys for d = 160, whose two
+// output accumulators (2 x 160 columns) leave room for only 64 columns of S
+// per tile.
 constexpr int kFwdThreads = 320;  // 8 softmax warps, producer, MMA
 constexpr float kRescaleLog2 = 8.0f;  // keep a stale row max while it is within 2^8
 
 template <int D>
 struct FwdCfg {
-    static constexpr int NB = (D + 63) / 64;           // 64-column boxes per row
-    static constexpr int TILE = NB * 128 * kRowBytes;  // 128 rows x D (box-padded)
-    static constexpr int FIXED = 2 * TILE;
-    static constexpr int STAGES_FIT = (225 * 1024 - FIXED) / TILE;
+    static constexpr int NB = (D + 63) / 64;            // 64-column boxes per row
+    static constexpr int BKV = D <= 128 ? 128 : 64;     // keys per K/V tile
+    static constexpr int QTILE = NB * 128 * kRowBytes;  // 128 query rows x D (box-padded)
+    static constexpr int KVTILE = NB * BKV * kRowBytes;
+    static constexpr int FIXED = 2 * QTILE;
+    static constexpr int STAGES_FIT = (225 * 1024 - FIXED) / KVTILE;
     static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
-    static constexpr int SMEM = 1024 + FIXED + STAGES * TILE + 256;
+    static constexpr int SMEM = 1024 + FIXED + STAGES * KVTILE + 256;
+    // TMEM columns of tile x.  d <= 128: S at 256 x, O at 256 x + 128 (its
+    // 32-wide tail, d = 96, right after).  d = 160: S at 64 x, the 128-column
+    // part of O at 128 + 128 x and its 32-column tail at 384 + 32 x, so that
+    // every N >= 128 accumulator part starts on a multiple of 128.
+    static constexpr uint32_t s_col(int x) { return D <= 128 ? 256u * x : 64u * x; }
+    static constexpr uint32_t o_col(int x) { return D <= 128 ? 256u * x + 128u : 128u + 128u * x; }
+    static constexpr uint32_t o_tail(int x) {
+        return D <= 128 ? o_col(x) + (D / 64) * 64 : 384u + 32u * x;
+    }
+    // column of 32-column chunk c of O_x
+    static constexpr uint32_t o_chunk(int x, int c) {
+        return c < (D / 64) * 2 ? o_col(x) + 32u * c : o_tail(x) + 32u * (c - (D / 64) * 2);
+    }
 };
 
 template <int D>
 __global__ void __launch_bounds__(kFwdThreads, 1)
-    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_qkv, const AttnArgs a) {
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q128,  // QKV, 128-row boxes (Q)
+                    const __grid_constant__ CUtensorMap tm_kv,    // QKV, BKV-row boxes (K, V)
+                    const AttnArgs a) {
     using C = FwdCfg<D>;
     constexpr int S = C::STAGES;
+    constexpr int BKV = C::BKV;
+    constexpr int SCH = BKV / 32;  // 32-key chunks of S per key tile
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-    uint8_t* sQ = smem;                 // Q_A, Q_B
-    uint8_t* ring = smem + 2 * C::TILE;  // K_0, V_0, K_1, V_1, ...
-    uint64_t* bars = reinterpret_cast<uint64_t*>(ring + S * C::TILE);
+    uint8_t* sQ = smem;                   // Q_A, Q_B
+    uint8_t* ring = smem + 2 * C::QTILE;  // K_0, V_0, K_1, V_1, ...
+    uint64_t* bars = reinterpret_cast<uint64_t*>(ring + S * C::KVTILE);
     uint64_t* q_full = bars;
     uint64_t* kv_full = bars + 1;
     uint64_t* kv_empty = kv_full + S;
@@ -236,7 +260,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int n = rem / a.nh, head = rem % a.nh;
     const int q0 = pair * 256;
     const bool has_b = q0 + 128 < a.s;
-    const int last[2] = {2 * pair, 2 * pair + 1};  // last (diagonal) key tile of A, B
+    // last key tile each query tile sees (its keys reach the tile's last query)
+    const int last[2] = {(q0 + 127) / BKV, (q0 + 255) / BKV};
     const int n_kv = has_b ? last[1] + 1 : last[0] + 1;
 
     if (threadIdx.x == 0) {
@@ -262,30 +287,30 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
-    // TMEM columns of tile x: S at 256 x, O at 256 x + 128
 
     if (warp == 8) {
         // ------------------------------------------------------ producer
         if (lane == 0) {
-            prefetch_tmap(&tm_qkv);
+            prefetch_tmap(&tm_q128);
+            prefetch_tmap(&tm_kv);
             const int qcol = head * D, kcol = a.h + head * D, vcol = 2 * a.h + head * D;
-            mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * C::TILE);
+            mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * C::QTILE);
             for (int x = 0; x < (has_b ? 2 : 1); ++x)
                 for (int b = 0; b < C::NB; ++b)
-                    tma_load_3d(&tm_qkv, smem_u32(q_full),
-                                smem_u32(sQ) + x * C::TILE + b * 128 * kRowBytes, qcol + 64 * b,
+                    tma_load_3d(&tm_q128, smem_u32(q_full),
+                                smem_u32(sQ) + x * C::QTILE + b * 128 * kRowBytes, qcol + 64 * b,
                                 q0 + 128 * x, n);
             uint32_t issued = 0, issued_phase = 0;
             for (int idx = 0; idx < 2 * n_kv; ++idx) {  // K_j = 2j, V_j = 2j + 1
                 const int stage = idx % S;
                 const uint32_t phase = static_cast<uint32_t>(idx / S) & 1u;
                 if (!wait_bounded(&kv_empty[stage], phase ^ 1u, abort_flag, a.status, 0x101)) break;
-                mbar_arrive_expect_tx(&kv_full[stage], C::TILE);
-                const uint32_t dst = smem_u32(ring) + stage * C::TILE;
+                mbar_arrive_expect_tx(&kv_full[stage], C::KVTILE);
+                const uint32_t dst = smem_u32(ring) + stage * C::KVTILE;
                 const int col = (idx & 1) ? vcol : kcol;
                 for (int b = 0; b < C::NB; ++b)
-                    tma_load_3d(&tm_qkv, smem_u32(&kv_full[stage]), dst + b * 128 * kRowBytes,
-                                col + 64 * b, (idx >> 1) * 128, n);
+                    tma_load_3d(&tm_kv, smem_u32(&kv_full[stage]), dst + b * BKV * kRowBytes,
+                                col + 64 * b, (idx >> 1) * BKV, n);
                 issued |= 1u << stage;
                 issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
             }
@@ -297,7 +322,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     } else if (warp == 9) {
         // ------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
+            constexpr uint32_t id_s = idesc_bf16_f32(128, BKV, false, false);
             bool ok = wait_bounded(q_full, 0, abort_flag, a.status, 0x104);
             tc_fence_after();
             // wait for ring entry idx (K_j = 2j, V_j = 2j + 1); returns its stage
@@ -310,12 +335,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 return stage;
             };
             auto issue_s = [&](int x, int stage) {  // S_x = Q_x K^T
-                const uint64_t qdesc = smem_desc_sw128(smem_u32(sQ) + x * C::TILE, 16, 1024);
-                const uint64_t kdesc = smem_desc_sw128(smem_u32(ring) + stage * C::TILE, 16, 1024);
+                const uint64_t qdesc = smem_desc_sw128(smem_u32(sQ) + x * C::QTILE, 16, 1024);
+                const uint64_t kdesc = smem_desc_sw128(smem_u32(ring) + stage * C::KVTILE, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    tc_mma_f16(tmem + 256 * x, desc_add(qdesc, kmajor_step<128>(kk)),
-                               desc_add(kdesc, kmajor_step<128>(kk)), id_s, kk > 0 ? 1u : 0u);
+                    tc_mma_f16(tmem + C::s_col(x), desc_add(qdesc, kmajor_step<128>(kk)),
+                               desc_add(kdesc, kmajor_step<BKV>(kk)), id_s, kk > 0 ? 1u : 0u);
                 tc_commit(&s_full[x]);
             };
             auto issue_pv = [&](int x, int j, int stage) {  // O_x (+)= P_x V
@@ -324,12 +349,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     ok = false;
                 if (!ok) return;
                 tc_fence_after();
-                // O_x (+)= P_x V: A = P_x from TMEM (packed over S_x's first 64
+                // O_x (+)= P_x V: A = P_x from TMEM (packed over S_x's first
                 // columns), B = V (MN-major: d along the rows, keys down the box)
                 const uint64_t vdesc =
-                    smem_desc_sw128(smem_u32(ring) + stage * C::TILE, 128 * kRowBytes, 1024);
-                mma_ts_n_is_d<D, 128 / 16>(tmem + 256 * x + 128, tmem + 256 * x, vdesc,
-                                           128 * kRowBytes, j > 0);
+                    smem_desc_sw128(smem_u32(ring) + stage * C::KVTILE, BKV * kRowBytes, 1024);
+                mma_ts_n_is_d<D, BKV / 16>(tmem + C::o_col(x), tmem + C::s_col(x), vdesc,
+                                           BKV * kRowBytes, j > 0, tmem + C::o_tail(x));
                 tc_commit(&pv_done[x]);
             };
             // S of both tiles for key tile 0
@@ -372,7 +397,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int r = threadIdx.x & 127;       // row of the tile = TMEM lane
         const int q = q0 + 128 * x + r;
         if (x == 0 || has_b) {
-            const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + 256 * x;
+            const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+            const uint32_t s_addr = lane_addr + C::s_col(x);
             const int jl = last[x];
             float m = -INFINITY, l = 0.0f;
             bool ok = true;
@@ -383,17 +409,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                uint32_t v[4][32];
+                uint32_t v[SCH][32];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + c * 32, v[c]);
+                for (int c = 0; c < SCH; ++c) tmem_ld32(s_addr + c * 32, v[c]);
                 tmem_wait_ld();
-                const bool diag = j == jl;  // keys j*128 + c with c > r are masked there
-                if (diag) {
+                // causal mask where this key tile reaches past the row's query
+                const int k0 = j * BKV;
+                if (k0 + BKV - 1 > q) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
+                    for (int c = 0; c < SCH; ++c)
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
-                            if (c * 32 + i > r) v[c][i] = __float_as_uint(-INFINITY);
+                            if (k0 + c * 32 + i > q) v[c][i] = __float_as_uint(-INFINITY);
                 }
                 // eight independent max / sum chains: the row is one thread's
                 // work, so its reductions must not be one serial chain
@@ -401,23 +428,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
                 for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
+                for (int c = 0; c < SCH; ++c)
 #pragma unroll
                     for (int i = 0; i < 32; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(v[c][i]));
                 const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                        fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
                 // the reference max only moves when the row max outgrows it by
-                // more than 2^8, so the O rescale below is rare
+                // more than 2^8, so the O rescale below is rare.  A row whose
+                // keys in this tile are all masked (rows past the sequence end
+                // in a 64-key tile) keeps its reference.
                 const float m_new = fmaxf(m, mx * a.scale2);
-                const bool move = j == 0 || m_new > m + kRescaleLog2;
+                const bool move = (j == 0 && m_new > -INFINITY) || m_new > m + kRescaleLog2;
                 const float alpha = move ? ex2(m - m_new) : 1.0f;
                 if (move) m = m_new;
                 float rs8[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) rs8[k] = 0.0f;
-                uint32_t pk[4][16];
+                uint32_t pk[SCH][16];
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
+                for (int c = 0; c < SCH; ++c)
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         // masked scores are -inf: 2^-inf = 0
@@ -436,18 +465,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
                         for (int c = 0; c < D / 32; ++c) {
                             uint32_t o[32];
-                            tmem_ld32(lane_addr + 128 + c * 32, o);
+                            tmem_ld32(lane_addr + C::o_chunk(x, c), o);
                             tmem_wait_ld();
 #pragma unroll
                             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                            tmem_st32(lane_addr + 128 + c * 32, o);
+                            tmem_st32(lane_addr + C::o_chunk(x, c), o);
                         }
                         tmem_wait_st();
                     }
                 }
-                // P_x, packed bf16, over the first 64 columns of S_x (already read)
+                // P_x, packed bf16, over the first columns of S_x (already read)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_st16(lane_addr + 16 * c, pk[c]);
+                for (int c = 0; c < SCH; ++c) tmem_st16(s_addr + 16 * c, pk[c]);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
@@ -463,7 +492,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
-                    tmem_ld32(lane_addr + 128 + c * 32, o);  // every lane: warp-collective
+                    tmem_ld32(lane_addr + C::o_chunk(x, c), o);  // every lane: warp-collective
                     tmem_wait_ld();
                     if (q_ok) {
 #pragma unroll
@@ -849,9 +878,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
-    // TMEM columns: S^T[b] at 64 b, dP^T[b] at 128 + 64 b, dV at 256, dK at the
-    // next multiple of 64 after dV (every accumulator starts on a 64-column step)
-    constexpr uint32_t kST = 0, kDPT = 128, kDV = 256, kDK = 256 + ((D + 63) / 64) * 64;
+    // TMEM columns.  d <= 128: S^T[b] at 64 b, dP^T[b] at 128 + 64 b (two
+    // buffers, so the next tile's S^T / dP^T run during this tile's softmax),
+    // dV at 256, dK at the next multiple of 64 after dV.  d = 160: one buffer
+    // (S^T at 0, dP^T at 64), the 128-column parts of dV and dK at 128 and 256
+    // and their 32-column tails at 384 and 416.  Every N >= 128 accumulator
+    // part starts on a multiple of 128.
+    constexpr int NBUF = D <= 128 ? 2 : 1;
+    constexpr uint32_t kST = 0, kDPT = NBUF == 2 ? 128 : 64;
+    constexpr uint32_t kDV = NBUF == 2 ? 256 : 128;
+    constexpr uint32_t kDK = NBUF == 2 ? 256 + ((D + 63) / 64) * 64 : 256;
+    constexpr uint32_t kDVt = NBUF == 2 ? kDV + (D / 64) * 64 : 384;
+    constexpr uint32_t kDKt = NBUF == 2 ? kDK + (D / 64) * 64 : 416;
+    // column of 32-column chunk c of an accumulator with parts at main / tail
+    auto acc_col = [](uint32_t main, uint32_t tail, int c) -> uint32_t {
+        return c < D / 64 * 2 ? main + 32 * c : tail + 32 * (c - D / 64 * 2);
+    };
 
     if (warp == 4) {
         if (lane == 0) {
@@ -902,7 +944,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tc_fence_after();
             auto issue_grads = [&](int i, int st) {
                 if (!ok) return;
-                if (!wait_bounded(&pds_full[i & 1], static_cast<uint32_t>(i >> 1) & 1u, abort_flag,
+                if (!wait_bounded(&pds_full[NBUF == 2 ? (i & 1) : 0],
+                                  static_cast<uint32_t>(NBUF == 2 ? (i >> 1) : i) & 1u, abort_flag,
                                   a.status, 0x305)) {
                     ok = false;
                     return;
@@ -915,9 +958,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 // along the rows, queries down the 64-row box)
                 const uint64_t dodesc = smem_desc_sw128(qd + C::Q_TILE, 64 * kRowBytes, 1024);
                 const uint64_t qdesc = smem_desc_sw128(qd, 64 * kRowBytes, 1024);
-                const uint32_t b = static_cast<uint32_t>(i & 1);
-                mma_ts_n_is_d<D, 64 / 16>(tmem + kDV, tmem + kST + 64 * b, dodesc, 64 * kRowBytes, i > 0);
-                mma_ts_n_is_d<D, 64 / 16>(tmem + kDK, tmem + kDPT + 64 * b, qdesc, 64 * kRowBytes, i > 0);
+                const uint32_t b = NBUF == 2 ? static_cast<uint32_t>(i & 1) : 0u;
+                mma_ts_n_is_d<D, 64 / 16>(tmem + kDV, tmem + kST + 64 * b, dodesc, 64 * kRowBytes, i > 0,
+                                          tmem + kDVt);
+                mma_ts_n_is_d<D, 64 / 16>(tmem + kDK, tmem + kDPT + 64 * b, qdesc, 64 * kRowBytes, i > 0,
+                                          tmem + kDKt);
                 tc_commit(&q_empty[st]);
             };
             for (int i = 0; i < nq && ok; ++i) {
@@ -929,7 +974,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const uint32_t qd = smem_u32(ring) + stage * 2 * C::Q_TILE;
                 const uint64_t qdesc = smem_desc_sw128(qd, 16, 1024);
                 const uint64_t dodesc = smem_desc_sw128(qd + C::Q_TILE, 16, 1024);
-                const uint32_t b = static_cast<uint32_t>(i & 1);
+                const uint32_t b = NBUF == 2 ? static_cast<uint32_t>(i & 1) : 0u;
                 // S^T = K Q^T and dP^T = V dO^T (M = 128 keys, N = 64 queries, K = d)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -939,14 +984,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                desc_add(dodesc, kmajor_step<64>(kk)), id_st, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(&st_full[b]);
-                if (i >= 1) issue_grads(i - 1, prev_stage);
+                if constexpr (NBUF == 2) {
+                    // the previous tile's dV / dK run while this tile is softmaxed
+                    if (i >= 1) issue_grads(i - 1, prev_stage);
+                } else {
+                    // one buffer: this tile's dV / dK before the next S^T
+                    issue_grads(i, stage);
+                }
                 prev_stage = stage;
                 if (++stage == S) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
-            issue_grads(nq - 1, prev_stage);
+            if constexpr (NBUF == 2) issue_grads(nq - 1, prev_stage);
             tc_commit(grad_done);
             tc_commit(drain);
             wait_drain(drain, 0, a.status, 0x307);
@@ -975,13 +1026,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         fetch(0, lse_c, dlt_c);
         bool ok = true;
         for (int i = 0; i < nq; ++i) {
-            const uint32_t b = static_cast<uint32_t>(i & 1);
+            const uint32_t b = NBUF == 2 ? static_cast<uint32_t>(i & 1) : 0u;
             float lse_n[2], dlt_n[2];
             fetch(i + 1, lse_n, dlt_n);
-            // S^T(i) was issued after dV/dK(i-2), which read this buffer's
-            // previous P^T / dS^T, so once it is here the buffer is free
-            if (!warp_wait_bounded(&st_full[b], static_cast<uint32_t>(i >> 1) & 1u, abort_flag,
-                                   a.status, 0x308)) {
+            // S^T(i) was issued after the dV / dK that last read this buffer's
+            // P^T / dS^T, so once it is here the buffer is free
+            if (!warp_wait_bounded(&st_full[b], static_cast<uint32_t>(NBUF == 2 ? (i >> 1) : i) & 1u,
+                                   abort_flag, a.status, 0x308)) {
                 ok = false;
                 break;
             }
@@ -1039,8 +1090,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t v[32], k[32];
-                tmem_ld32(lane_addr + kDV + c * 32, v);
-                tmem_ld32(lane_addr + kDK + c * 32, k);
+                tmem_ld32(lane_addr + acc_col(kDV, kDVt, c), v);
+                tmem_ld32(lane_addr + acc_col(kDK, kDKt, c), k);
                 tmem_wait_ld();
                 if (key_ok) {
 #pragma unroll
@@ -1074,8 +1125,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
 // ------------------------------------------------------------- launchers
 
-cudaError_t launch_attn_forward(const CUtensorMap& tm_qkv128, int d, const AttnParams& p,
-                                cudaStream_t st, int* launches) {
+cudaError_t launch_attn_forward(const CUtensorMap& tm_qkv128, const CUtensorMap& tm_qkv64, int d,
+                                const AttnParams& p, cudaStream_t st, int* launches) {
     AttnArgs a{};
     a.nb = p.nb; a.s = p.s; a.h = p.h; a.nh = p.nh;
     a.T = static_cast<long long>(p.nb) * p.s;
@@ -1091,11 +1142,14 @@ cudaError_t launch_attn_forward(const CUtensorMap& tm_qkv128, int d, const AttnP
     if (d == DD) {                                                                                \
         auto kern = attn_fwd_kernel<DD>;                                                          \
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<DD>::SMEM); \
-        if (e == cudaSuccess) kern<<<grid, kFwdThreads, FwdCfg<DD>::SMEM, st>>>(tm_qkv128, a);    \
+        if (e == cudaSuccess)                                                                     \
+            kern<<<grid, kFwdThreads, FwdCfg<DD>::SMEM, st>>>(                                    \
+                tm_qkv128, FwdCfg<DD>::BKV == 128 ? tm_qkv128 : tm_qkv64, a);                     \
     }
     TPMLP_ATTN_FWD(64)
     TPMLP_ATTN_FWD(96)
     TPMLP_ATTN_FWD(128)
+    TPMLP_ATTN_FWD(160)
 #undef TPMLP_ATTN_FWD
     if (e != cudaSuccess) return e;
     e = cudaGetLastError();
@@ -1121,6 +1175,7 @@ cudaError_t launch_attn_backward(const CUtensorMap& tm_qkv128, const CUtensorMap
         if (d == 64) attn_delta_kernel<64><<<blocks, 256, 0, st>>>(p.dO, p.O_in, a.T, p.h, p.nh, p.delta_out);
         if (d == 96) attn_delta_kernel<96><<<blocks, 256, 0, st>>>(p.dO, p.O_in, a.T, p.h, p.nh, p.delta_out);
         if (d == 128) attn_delta_kernel<128><<<blocks, 256, 0, st>>>(p.dO, p.O_in, a.T, p.h, p.nh, p.delta_out);
+        if (d == 160) attn_delta_kernel<160><<<blocks, 256, 0, st>>>(p.dO, p.O_in, a.T, p.h, p.nh, p.delta_out);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         ++*launches;
@@ -1153,6 +1208,7 @@ cudaError_t launch_attn_backward(const CUtensorMap& tm_qkv128, const CUtensorMap
     TPMLP_ATTN_BWD(64)
     TPMLP_ATTN_BWD(96)
     TPMLP_ATTN_BWD(128)
+    TPMLP_ATTN_BWD(160)
 #undef TPMLP_ATTN_BWD
     return e;
 }

@@ -1197,7 +1197,7 @@ namespace tpmlp {
 namespace {
 
 // Head dims with a compiled attention kernel.
-bool attn_head_dim_ok(int d) { return d == 64 || d == 96 || d == 128; }
+bool attn_head_dim_ok(int d) { return d == 64 || d == 96 || d == 128 || d == 160; }
 
 int check_attn(int nb, int s, int h, int nh, int t) {
     if (nb < 0 || s < 1 || h < 8 || h % 8 != 0 || nh < 1 || h % nh != 0 || t < 1 ||
@@ -1247,14 +1247,15 @@ int qkv_gemm(const tpmlp_bf16* X, const tpmlp_bf16* W, const tpmlp_bf16* b, int 
 
 int attn_core_forward(const tpmlp_bf16* QKV, int nb, int s, int h, int nh, tpmlp_bf16* O,
                       float* lse, cudaStream_t st, const DeviceInfo& d) {
-    CUtensorMap tm;
+    CUtensorMap tm, tm64;
     if (int rc = make_seq_map(&tm, QKV, nb, s, 3LL * h, 128)) return rc;
+    if (int rc = make_seq_map(&tm64, QKV, nb, s, 3LL * h, 64)) return rc;
     AttnParams p{};
     p.nb = nb; p.s = s; p.h = h; p.nh = nh;
     p.O = reinterpret_cast<__nv_bfloat16*>(O);
     p.lse = lse;
     p.status = d.status;
-    cudaError_t e = launch_attn_forward(tm, h / nh, p, st, &t_last_launches);
+    cudaError_t e = launch_attn_forward(tm, tm64, h / nh, p, st, &t_last_launches);
     return e == cudaSuccess ? TPMLP_OK : fail_cuda(e);
 }
 

@@ -54,7 +54,7 @@ cudaError_t launch_ln_backward(const __nv_bfloat16* dX, const __nv_bfloat16* dre
 int ln_param_chunks(int T, int h);
 
 // Causal attention of every (sequence, head) (attention.cu).  Head dims
-// d in {64, 96, 128}.  QKV [T, 3h] is read through 3-D tensor maps
+// d in {64, 96, 128, 160}.  QKV [T, 3h] is read through 3-D tensor maps
 // {3h, s, nb} with 64 x 128-row (qkv128) or 64 x 64-row (qkv64) boxes, dO
 // [T, h] likewise; T = nb * s.
 struct AttnParams {
@@ -68,8 +68,8 @@ struct AttnParams {
     __nv_bfloat16* dqkv;         // backward: output [T, 3h]
     int* status;
 };
-cudaError_t launch_attn_forward(const CUtensorMap& tm_qkv128, int d, const AttnParams& p,
-                                cudaStream_t st, int* launches);
+cudaError_t launch_attn_forward(const CUtensorMap& tm_qkv128, const CUtensorMap& tm_qkv64, int d,
+                                const AttnParams& p, cudaStream_t st, int* launches);
 cudaError_t launch_attn_backward(const CUtensorMap& tm_qkv128, const CUtensorMap& tm_qkv64,
                                  const CUtensorMap& tm_do128, const CUtensorMap& tm_do64, int d,
                                  const AttnParams& p, cudaStream_t st, int* launches);

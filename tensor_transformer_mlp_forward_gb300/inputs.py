@@ -203,7 +203,14 @@ ATTN_GPT2_2_5B = AttnWorkload("attn-gpt2-2.5b", 8, 1024, 1920, 20, 2,
 ATTN_GPT2_8_3B = AttnWorkload("attn-gpt2-8.3b", 8, 1024, 3072, 24, 8,
                               _attn_std(wo=0.02 / math.sqrt(2 * 72)), 1103)
 
-ATTN_WORKLOADS = {w.name: w for w in (ATTN_TINY, ATTN_GPT2_355M, ATTN_GPT2_2_5B, ATTN_GPT2_8_3B)}
+# MT-NLG 530B's attention: 128 heads of 160 over h = 20480, sequence 2048,
+# 8-way tensor parallel ("MT-NLG 530B deep dive", section 4.1), one sequence
+# as in the MLP workload, weights N(0, 0.006) as the MLP's.
+ATTN_MTNLG_530B = AttnWorkload("attn-mt-nlg-530b", 1, 2048, 20480, 128, 8,
+                               _attn_std(w=0.006, wo=0.006), 1104)
+
+ATTN_WORKLOADS = {w.name: w for w in (ATTN_TINY, ATTN_GPT2_355M, ATTN_GPT2_2_5B, ATTN_GPT2_8_3B,
+                                      ATTN_MTNLG_530B)}
 
 
 def attn_custom(nb: int, s: int, h: int, nh: int, t: int, seed: int, std=None,

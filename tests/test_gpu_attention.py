@@ -4,9 +4,9 @@ oracle, through the C ABI.
 Tolerances are the block's (bf16 inputs, fp32 accumulation): max|gpu - ref|
 / max|ref| <= 1e-2 for forward outputs (Y, QKV, O) and <= 2e-2 for every
 gradient (dX, dWqkv, dbqkv, dWo, dbo).  Small cases compare every element
-with the full oracle; the full-size GPT-2 shapes compare sampled heads (their
-attention output and every parameter gradient of the head) with the oracle's
-per-head entry points.
+with the full oracle; the full-size GPT-2 and MT-NLG shapes compare sampled
+heads (their attention output and every parameter gradient of the head) with
+the oracle's per-head entry points.
 """
 
 import numpy as np
@@ -47,7 +47,7 @@ def run_gpu(w: inputs.AttnWorkload, cpu):
     return dict(Y=Y, QKV=QKV, O=O, lse=lse, dX=dX, dWqkv=dWqkv, dbqkv=dbqkv, dWo=dWo, dbo=dbo)
 
 
-# Every compiled head dim (64, 96, 128), several query/key tiles, ragged
+# Every compiled head dim (64, 96, 128, 160), several query/key tiles, ragged
 # sequence tails against the 128-row and 64-row tiles, t from 1 to nh.
 SMALL = [
     inputs.ATTN_TINY,                                              # d = 64, one tile
@@ -57,6 +57,8 @@ SMALL = [
     inputs.attn_custom(nb=3, s=72, h=384, nh=4, t=4, seed=24),     # d = 96, t = nh
     inputs.attn_custom(nb=1, s=1, h=64, nh=1, t=1, seed=25),       # one token
     inputs.attn_custom(nb=2, s=257, h=512, nh=4, t=2, seed=26),    # d = 128, 3 tiles + 1
+    inputs.attn_custom(nb=2, s=200, h=320, nh=2, t=2, seed=30),    # d = 160: 64-key tiles
+    inputs.attn_custom(nb=1, s=300, h=480, nh=3, t=3, seed=31),    # d = 160, 3 query pairs
 ]
 
 
@@ -134,7 +136,7 @@ def test_attention_shard_count_changes_nothing_but_the_sum_order():
             assert torch.equal(o[k], outs[0][k]), k
 
 
-FULL = [inputs.ATTN_GPT2_355M, inputs.ATTN_GPT2_8_3B]
+FULL = [inputs.ATTN_GPT2_355M, inputs.ATTN_GPT2_8_3B, inputs.ATTN_MTNLG_530B]
 
 
 @pytest.mark.parametrize("w", FULL, ids=lambda w: w.name)
@@ -150,10 +152,10 @@ def test_attention_full_size_sampled_heads(w):
         e = rel(np64(out["O"][:, j * d:(j + 1) * d]), Oj)
         assert e <= TOL_FWD, (j, "O", e)
         dW, db, dWo = oracle.attn_head_grads(cpu, w.nb, w.nh, j)
-        cols = np.concatenate([np.arange(p * h + j * d, p * h + (j + 1) * d) for p in range(3)])
-        got_w = np64(out["dWqkv"])[:, cols]
-        got_b = np64(out["dbqkv"])[cols]
-        got_o = np64(out["dWo"])[j * d:(j + 1) * d]
+        cols = torch.cat([torch.arange(p * h + j * d, p * h + (j + 1) * d) for p in range(3)]).cuda()
+        got_w = np64(out["dWqkv"].index_select(1, cols))  # the head's columns only
+        got_b = np64(out["dbqkv"].index_select(0, cols))
+        got_o = np64(out["dWo"][j * d:(j + 1) * d])
         for name, got, ref in (("dWqkv", got_w, dW), ("dbqkv", got_b, db), ("dWo", got_o, dWo)):
             e = rel(got, ref)
             assert e <= TOL_BWD, (j, name, e)
