@@ -102,31 +102,6 @@ __device__ __forceinline__ void tmem_wait_st() {
 }
 
 
-// tcgen05 MMA chain D (+)= A B^T where B is MN-major along d (the value or
-// query/key tile as the N operand, N = D): the N extent is issued as a
-// multiple of 64 (whole swizzle atoms) plus a 32-wide tail, so that no MMA
-// spans part of an atom.  `box_bytes` is the stride of the 64-wide atoms.
-// A is K-major with its 64-column boxes `a_box_bytes` apart.
-template <int D, int KSTEPS>
-__device__ __forceinline__ void mma_n_is_d(uint32_t d_tmem, uint64_t a_desc, uint32_t a_box_bytes,
-                                           uint64_t b_desc, uint32_t box_bytes,
-                                           bool accumulate_first) {
-    constexpr int N1 = (D / 64) * 64;
-    constexpr int N2 = D - N1;
-    constexpr uint32_t id1 = idesc_bf16_f32(128, N1 > 0 ? N1 : 64, false, true);
-    constexpr uint32_t id2 = idesc_bf16_f32(128, N2 > 0 ? N2 : 32, false, true);
-#pragma unroll
-    for (int kk = 0; kk < KSTEPS; ++kk) {
-        const uint32_t acc = (accumulate_first || kk > 0) ? 1u : 0u;
-        const uint32_t aoff = static_cast<uint32_t>((kk >> 2) * a_box_bytes + (kk & 3) * 32);
-        const uint64_t ad = desc_add(a_desc, aoff);
-        const uint64_t bd = desc_add(b_desc, mnmajor_step(kk));
-        if constexpr (N1 > 0) tc_mma_f16(d_tmem, ad, bd, id1, acc);
-        if constexpr (N2 > 0)
-            tc_mma_f16(d_tmem + N1, ad, desc_add(bd, (N1 / 64) * box_bytes), id2, acc);
-    }
-}
-
 // D[tmem] (+)= A[tmem] * B[smem]^T, bf16 x bf16 -> f32: the A operand (128
 // rows = TMEM lanes, 16 k values packed two bf16 to a 32-bit column, low
 // half first) is read from tensor memory.
@@ -151,9 +126,12 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         : "memory");
 }
 
-// The same chain as mma_n_is_d with A in tensor memory: k-step kk reads the
-// 8 columns a_tmem + 8 kk.  The 32-wide tail of N = d (d % 64 == 32) goes to
-// columns d_tail (d_tmem + the whole atoms' width unless given).
+// tcgen05 MMA chain D (+)= A B^T with A in tensor memory (k-step kk reads the
+// 8 columns a_tmem + 8 kk) and B MN-major along d in shared memory (the value
+// or query/key tile as the N operand, N = d): the N extent is issued as a
+// multiple of 64 (whole swizzle atoms, `box_bytes` apart) plus a 32-wide
+// tail, so that no MMA spans part of an atom.  The tail (d % 64 == 32) goes
+// to columns d_tail (d_tmem + the whole atoms' width unless given).
 template <int D, int KSTEPS>
 __device__ __forceinline__ void mma_ts_n_is_d(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                               uint32_t box_bytes, bool accumulate_first,
