@@ -23,23 +23,25 @@
 // per (head, token) so that the backward pass rebuilds P = 2^(u - lse) without
 // a second normalisation pass.
 //
-// Kernels (warps 0-3 do the softmax, one query or key row per thread and TMEM
-// lane; warp 4 is the TMA producer; warp 5 allocates TMEM and issues the
-// MMAs from one thread):
-//   attn_fwd_kernel     one CTA per (128 queries, head, sequence); 128-key
-//                       tiles; S double-buffered in TMEM so that S of the next
-//                       tile is computed while this one is softmaxed; P goes
-//                       through shared memory (K-major, 128-byte swizzle) into
-//                       the P V product, whose fp32 result the softmax threads
-//                       fold into a register-resident output row.
+// Kernels (softmax warps own one query or key row per thread and TMEM lane; a
+// producer warp issues the TMA loads; one thread of the MMA warp allocates
+// TMEM and issues every MMA):
+//   attn_fwd_kernel     one CTA per pair of 128-query tiles of a (sequence,
+//                       head), two softmax warpgroups in ping-pong; S and the
+//                       output O of each tile in TMEM; P written back into
+//                       TMEM over S and used there as the A operand of P V.
 //   attn_delta_kernel   delta = rowsum(dO * O) per (token, head).
 //   attn_bwd_dq_kernel  one CTA per (128 queries, head, sequence); 64-key
-//                       tiles: S and dP (TMEM, double-buffered), dS through
-//                       shared memory, dQ accumulated in TMEM.
+//                       tiles: S and dP in TMEM (double-buffered), dS written
+//                       back over S and used there as the A operand of dS K,
+//                       dQ accumulated in TMEM.
 //   attn_bwd_dkdv_kernel one CTA per (128 keys, head, sequence); 64-query
-//                       tiles: S^T and dP^T (TMEM, double-buffered), P^T and
-//                       dS^T through shared memory, dV and dK accumulated in
-//                       TMEM.
+//                       tiles: S^T and dP^T in TMEM, P^T and dS^T written back
+//                       over them and used there as the A operands of P^T dO
+//                       and dS^T Q, dV and dK accumulated in TMEM.
+// Keeping P, dS, P^T and dS^T in tensor memory keeps shared-memory traffic
+// (K, V, Q, dO operands and the TMA writes) within what shared memory
+// delivers per clock.
 // dQ and dK/dV are separate kernels so that every gradient is written once,
 // in a fixed summation order, with no atomics.
 #include <cuda_bf16.h>
