@@ -213,7 +213,10 @@ class ClockSampler:
 
 # -------------------------------------------------------------- our step
 
+# On large blocks dA and dB read K-major operands (X, dZ, H and dY
+# transposed first), as tp_mlp_backward does
 STEP_CALLS = ("column_gelu", "row_sum", "db2", "dgelu", "dx", "dA", "dB")
+KMAJOR_CALLS = ("t_X", "t_dZ", "dA", "t_H", "t_dY", "dB")
 GEMM_CALLS = ("column_gelu", "row_sum", "dx", "dA", "dB")  # one kernel each
 
 
@@ -237,6 +240,10 @@ class Step:
         self.p_db1 = e(max(1, int(binding.lib().tp_mlp_dgelu_partial_floats(T, F))), dt=torch.float32)
         self.p_db2 = e(max(1, int(binding.lib().tp_mlp_bias_grad_workspace_floats(T, h))), dt=torch.float32)
         self.ws_split = e(max(16, binding.split_workspace_bytes(T, h, F, w.t)), dt=torch.uint8)
+        self.kmajor = binding.weight_grad_kmajor(h, F)
+        if self.kmajor:
+            ldT = binding.pitch(T)
+            self.Xt, self.dYt, self.dZt, self.Ht = e(h, ldT), e(h, ldT), e(F, ldT), e(F, ldT)
         self.launches = 0
         # dropout before the residual add: a fresh pattern every step (the
         # element counter advances by T*h, rounded up to a Philox block)
@@ -246,11 +253,12 @@ class Step:
         # the backward pass rebuilds Z and H from X before a4
         self.recompute = recompute
         self.names = (("column_gelu", "row_sum") + (("dropout_grad",) if p_drop > 0 else ())
-                      + (("recompute",) if recompute else ()) + STEP_CALLS[2:])
+                      + (("recompute",) if recompute else ()) + STEP_CALLS[2:5]
+                      + (KMAJOR_CALLS if self.kmajor else STEP_CALLS[5:]))
 
     def run(self, events=None):
-        """One fwd+bwd step; if `events` (len 8) is given, records them
-        between the calls on the current stream."""
+        """One fwd+bwd step; if `events` (one more than the calls) is given,
+        records them between the calls on the current stream."""
         b, i, t = self.b, self.inp, self.w.t
         rec = self.recompute
         calls = (lambda: b.tp_mlp_column_gelu(i["X"], i["A"], i["b1"], t, Z=None if rec else self.Z,
@@ -273,9 +281,21 @@ class Step:
             lambda: b.tp_mlp_bias_grad(dP, db=self.db2, partial=self.p_db2),
             lambda: b.tp_mlp_dgelu(dP, i["B"], self.Z, t, dZ=self.dZ, db1=self.db1, partial=self.p_db1),
             lambda: b.tp_mlp_dx(self.dZ, i["A"], t, dX=self.dX, workspace=self.ws_split),
-            lambda: b.tp_mlp_dA(i["X"], self.dZ, t, dA=self.dA),
-            lambda: b.tp_mlp_dB(self.H, dP, t, dB=self.dB),
         )
+        if self.kmajor:
+            calls += (
+                lambda: b.tp_transpose(i["X"], out=self.Xt),
+                lambda: b.tp_transpose(self.dZ, out=self.dZt),
+                lambda: b.tp_mlp_dA_kmajor(self.Xt, self.dZt, self.w.T, t, dA=self.dA),
+                lambda: b.tp_transpose(self.H, out=self.Ht),
+                lambda: b.tp_transpose(dP, out=self.dYt),
+                lambda: b.tp_mlp_dB_kmajor(self.Ht, self.dYt, self.w.T, t, dB=self.dB),
+            )
+        else:
+            calls += (
+                lambda: b.tp_mlp_dA(i["X"], self.dZ, t, dA=self.dA),
+                lambda: b.tp_mlp_dB(self.H, dP, t, dB=self.dB),
+            )
         if events is not None:
             events[0].record()
         for k, c in enumerate(calls):
@@ -624,7 +644,16 @@ class AttnStep:
         self.ws = e(max(16, binding.split_workspace_bytes(T, h, 3 * h, 1),
                         binding.split_workspace_bytes(T, h, h, w.t)), dt=torch.uint8)
         self.launches = 0
-        self.names = ATTN_CALLS
+        # the weight gradients in K-major form where tp_attn_backward takes it
+        self.kmajor_o = binding.weight_grad_kmajor(h, h)
+        self.kmajor_qkv = binding.weight_grad_kmajor(h, 3 * h)
+        ldT = binding.pitch(T)
+        if self.kmajor_o:
+            self.Ot, self.dYt = e(h, ldT), e(h, ldT)
+        if self.kmajor_qkv:
+            self.Xt, self.dQKVt = e(h, ldT), e(3 * h, ldT)
+        self.names = (ATTN_CALLS[:4] + (("t_O", "t_dY") if self.kmajor_o else ()) + ATTN_CALLS[4:8]
+                      + (("t_X", "t_dQKV") if self.kmajor_qkv else ()) + ATTN_CALLS[8:])
 
     def run(self, events=None):
         b, i, w = self.b, self.inp, self.w
@@ -634,14 +663,30 @@ class AttnStep:
             lambda: b.tp_mlp_row_sum(self.O, i["Wo"], i["bo"], i["residual"], w.t, Y=self.Y,
                                      workspace=self.ws),
             lambda: b.tp_mlp_bias_grad(i["dY"], db=self.dbo, partial=self.p_sum),
-            lambda: b.tp_mlp_dB(self.O, i["dY"], 1, dB=self.dWo),
+        )
+        if self.kmajor_o:
+            calls += (
+                lambda: b.tp_transpose(self.O, out=self.Ot),
+                lambda: b.tp_transpose(i["dY"], out=self.dYt),
+                lambda: b.tp_mlp_dB_kmajor(self.Ot, self.dYt, w.T, 1, dB=self.dWo),
+            )
+        else:
+            calls += (lambda: b.tp_mlp_dB(self.O, i["dY"], 1, dB=self.dWo),)
+        calls += (
             lambda: b.tp_mlp_dx(i["dY"], i["Wo"], 1, dX=self.dO, workspace=self.ws),
             lambda: b.tp_attn_core_backward(self.QKV, self.O, self.lse, self.dO, w.nb, w.nh,
                                             dQKV=self.dQKV, delta=self.delta),
             lambda: b.tp_mlp_bias_grad(self.dQKV, db=self.dbqkv, partial=self.p_sum),
-            lambda: b.tp_mlp_dA(i["X"], self.dQKV, 1, dA=self.dWqkv),
-            lambda: b.tp_mlp_dx(self.dQKV, i["Wqkv"], 1, dX=self.dX, workspace=self.ws),
         )
+        if self.kmajor_qkv:
+            calls += (
+                lambda: b.tp_transpose(i["X"], out=self.Xt),
+                lambda: b.tp_transpose(self.dQKV, out=self.dQKVt),
+                lambda: b.tp_mlp_dA_kmajor(self.Xt, self.dQKVt, w.T, 1, dA=self.dWqkv),
+            )
+        else:
+            calls += (lambda: b.tp_mlp_dA(i["X"], self.dQKV, 1, dA=self.dWqkv),)
+        calls += (lambda: b.tp_mlp_dx(self.dQKV, i["Wqkv"], 1, dX=self.dX, workspace=self.ws),)
         if events is not None:
             events[0].record()
         for k, c in enumerate(calls):

@@ -114,7 +114,8 @@ int tp_mlp_backward(const tpmlp_bf16* dY, const tpmlp_bf16* X, const tpmlp_bf16*
 
 /* ---------------------------------------------------------------------- */
 /* The steps of the hot path, one call each.  tp_mlp_forward and          */
-/* tp_mlp_backward are exactly these calls in this order.                  */
+/* tp_mlp_backward are exactly these calls in this order (the backward     */
+/* takes a8 and a9 in their transposed-operand form, below tp_mlp_dB).     */
 /* ---------------------------------------------------------------------- */
 
 /* a2: column-parallel GEMM with fused bias and GeLU, all t shards in one
@@ -194,6 +195,39 @@ int tp_mlp_dA(const tpmlp_bf16* X, const tpmlp_bf16* dZ, int T, int h, int F, in
 /* a9: dB_i = H_i^T dY for every shard.  H [T,F], dY [T,h] -> dB [F,h]. */
 int tp_mlp_dB(const tpmlp_bf16* H, const tpmlp_bf16* dY, int T, int h, int F, int t,
               tpmlp_bf16* dB, void* stream);
+
+/* Transpose of a bf16 matrix, the layout the two calls below read:
+ * out[c * ld_out + r] = in[r * cols + c] for r < rows, c < cols, and
+ * out[c * ld_out + r] = 0 for rows <= r < (rows rounded up to 8); the rest of
+ * each output row is not touched.  in [rows, cols] row-major, out [cols,
+ * ld_out], both device memory, 16-byte aligned, not overlapping.
+ * Rules: rows >= 0, cols >= 0, cols % 8 == 0, ld_out % 8 == 0, ld_out >=
+ * rows rounded up to 8.  rows or cols 0: nothing is launched. */
+int tp_transpose(const tpmlp_bf16* in, int rows, int cols, tpmlp_bf16* out, int ld_out,
+                 void* stream);
+
+/* 1 when the composite calls (tp_mlp_backward and its variants,
+ * tp_attn_backward) compute an M x N weight gradient (dA, dB: h x F or
+ * F x h; dWqkv: h x 3h; dWo: h x h) from transposed operands with
+ * tp_transpose and the two calls below, else 0 (they call tp_mlp_dA /
+ * tp_mlp_dB).  The rule is M N / (M + N) >= 6144: there the faster K-major
+ * GEMM repays the two transposes.  No device work. */
+int tp_weight_grad_kmajor(int M, int N);
+
+/* a8 and a9 from transposed operands, so that both GEMM operands are read
+ * along their contiguous dimension (the tensor cores take this K-major form
+ * faster than the row-major X, dZ, H, dY of tp_mlp_dA / tp_mlp_dB).  Same
+ * sums, same outputs:
+ *   dA_i = X^T dZ_i   from Xt = X^T [h, ldT] and dZt = dZ^T [F, ldT]
+ *   dB_i = H_i^T dY   from Ht = H^T [F, ldT] and dYt = dY^T [h, ldT]
+ * (shard i of dZt / Ht is rows i F/t .. (i+1) F/t - 1), as tp_transpose
+ * writes them with ld_out = ldT.  Only the first T entries of each row are
+ * read.  Rules: those of tp_mlp_dA plus ldT % 8 == 0, ldT >= T rounded up
+ * to 8.  T == 0: the output is zeroed. */
+int tp_mlp_dA_kmajor(const tpmlp_bf16* Xt, const tpmlp_bf16* dZt, int T, int ldT, int h, int F,
+                     int t, tpmlp_bf16* dA, void* stream);
+int tp_mlp_dB_kmajor(const tpmlp_bf16* Ht, const tpmlp_bf16* dYt, int T, int ldT, int h, int F,
+                     int t, tpmlp_bf16* dB, void* stream);
 
 /* ---------------------------------------------------------------------- */
 /* Residual add + LayerNorm feeding the block's input X                    */

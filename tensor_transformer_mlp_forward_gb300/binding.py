@@ -61,6 +61,10 @@ _SIGNATURES = {
     "tp_mlp_dx": ([_P] * 2 + [_I] * 4 + [_P] + [_P, _S, _P], _I),
     "tp_mlp_dA": ([_P] * 2 + [_I] * 4 + [_P] + [_P], _I),
     "tp_mlp_dB": ([_P] * 2 + [_I] * 4 + [_P] + [_P], _I),
+    "tp_weight_grad_kmajor": ([_I, _I], _I),
+    "tp_transpose": ([_P, _I, _I, _P, _I, _P], _I),
+    "tp_mlp_dA_kmajor": ([_P] * 2 + [_I] * 5 + [_P] + [_P], _I),
+    "tp_mlp_dB_kmajor": ([_P] * 2 + [_I] * 5 + [_P] + [_P], _I),
     "tp_mlp_forward_recompute_workspace_bytes": ([_I] * 4, _S),
     "tp_mlp_forward_recompute": ([_P] * 6 + [_I] * 4 + [_P] + [_P, _S, _P], _I),
     "tp_mlp_backward_recompute_workspace_bytes": ([_I] * 4, _S),
@@ -434,6 +438,50 @@ def tp_mlp_dB(H, dY, t: int, dB=None, stream=None):
     _check("tp_mlp_dB", lib().tp_mlp_dB(
         _ptr(H, "H", (T, F)), _ptr(dY, "dY", (T, h)), T, h, F, t, _ptr(dB, "dB", (F, h)),
         _stream(stream)))
+    return dB
+
+
+def pitch(rows: int) -> int:
+    """Row pitch tp_transpose needs at least: rows rounded up to 8."""
+    return (rows + 7) // 8 * 8
+
+
+def weight_grad_kmajor(M: int, N: int) -> bool:
+    """Whether the composite backward calls compute an M x N weight gradient
+    from transposed operands (tp_transpose + tp_mlp_dA_kmajor/_dB_kmajor)."""
+    return bool(lib().tp_weight_grad_kmajor(M, N))
+
+
+def tp_transpose(x, ld: Optional[int] = None, out=None, stream=None):
+    """out[c, r] = x[r, c] for x [rows, cols]; out is [cols, ld] (ld defaults to
+    pitch(rows)); columns rows .. pitch(rows) - 1 of out are zeroed."""
+    rows, cols = x.shape
+    ld = pitch(rows) if ld is None else ld
+    out = _out(out, (cols, ld), x)
+    _check("tp_transpose", lib().tp_transpose(
+        _ptr(x, "x", (rows, cols)), rows, cols, _ptr(out, "out", (cols, ld)), ld, _stream(stream)))
+    return out
+
+
+def tp_mlp_dA_kmajor(Xt, dZt, T: int, t: int, dA=None, stream=None):
+    """dA from Xt = X^T [h, ldT] and dZt = dZ^T [F, ldT] (tp_transpose's output)."""
+    h, ldT = Xt.shape
+    F = dZt.shape[0]
+    dA = _out(dA, (h, F), Xt)
+    _check("tp_mlp_dA_kmajor", lib().tp_mlp_dA_kmajor(
+        _ptr(Xt, "Xt", (h, ldT)), _ptr(dZt, "dZt", (F, ldT)), T, ldT, h, F, t,
+        _ptr(dA, "dA", (h, F)), _stream(stream)))
+    return dA
+
+
+def tp_mlp_dB_kmajor(Ht, dYt, T: int, t: int, dB=None, stream=None):
+    """dB from Ht = H^T [F, ldT] and dYt = dY^T [h, ldT] (tp_transpose's output)."""
+    F, ldT = Ht.shape
+    h = dYt.shape[0]
+    dB = _out(dB, (F, h), Ht)
+    _check("tp_mlp_dB_kmajor", lib().tp_mlp_dB_kmajor(
+        _ptr(Ht, "Ht", (F, ldT)), _ptr(dYt, "dYt", (h, ldT)), T, ldT, h, F, t,
+        _ptr(dB, "dB", (F, h)), _stream(stream)))
     return dB
 
 

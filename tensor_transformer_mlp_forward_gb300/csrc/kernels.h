@@ -35,9 +35,16 @@ cudaError_t launch_dx(const GemmMaps& m, const GemmArgs& g, int grid,
                       bool pair, cudaStream_t st);
 cudaError_t launch_dx_partial(const GemmMaps& m, const GemmArgs& g, int grid, bool pair,
                               cudaStream_t st);
-// A MN-major, B MN-major: the weight gradients.
+// A MN-major, B MN-major: the weight gradients read from X, dZ, H and dY in
+// place (their K-major form from the transposes runs launch_dx).
 cudaError_t launch_weight_grad(const GemmMaps& m, const GemmArgs& g,
                                int grid, bool pair, cudaStream_t st);
+
+// out[c * ld_out + r] = in[r * cols + c], bf16, with each output row zeroed
+// from `rows` to the next multiple of 8 (transpose.cu).  cols % 8 == 0,
+// ld_out % 8 == 0, ld_out >= rows rounded up to 8, 16-byte aligned pointers.
+cudaError_t launch_transpose(const __nv_bfloat16* in, int rows, int cols, __nv_bfloat16* out,
+                             int ld_out, cudaStream_t st, int* launches);
 
 // Residual add + LayerNorm (layernorm.cu).  `launches` is incremented per
 // kernel launched.

@@ -71,6 +71,51 @@ def test_workspace_errors(L):
     assert L.tp_mlp_backward_workspace_bytes(T, h, 1000, 8) == 0
 
 
+def test_weight_grad_form_rule(L):
+    # K-major (transposed operands) where M N / (M + N) >= 6144
+    assert L.tp_weight_grad_kmajor(20480, 81920) == 1   # MT-NLG dA / dB
+    assert L.tp_weight_grad_kmajor(8192, 32768) == 1
+    assert L.tp_weight_grad_kmajor(20480, 20480) == 1   # MT-NLG dWo
+    assert L.tp_weight_grad_kmajor(4096, 16384) == 0
+    assert L.tp_weight_grad_kmajor(3072, 9216) == 0     # GPT-2 8.3B dWqkv
+    assert L.tp_weight_grad_kmajor(12288, 12288) == 1 and L.tp_weight_grad_kmajor(12286, 12288) == 0
+    assert L.tp_weight_grad_kmajor(0, 81920) == 0 and L.tp_weight_grad_kmajor(-5, 81920) == 0
+
+
+def test_backward_workspace_holds_the_transposes(L):
+    # with the K-major weight gradients: dZ, then X^T and dY^T [h, ldT] and
+    # dZ^T and H^T [F, ldT], ldT = T rounded up to 8; without them, none
+    T, h, F, t = 300, 8192, 32768, 4
+    ldT = 304
+    big = L.tp_mlp_backward_workspace_bytes(T, h, F, t)
+    assert big >= 2 * T * F + 2 * ldT * (2 * h + 2 * F)
+    T, h, F = 300, 200, 1536
+    assert L.tp_mlp_backward_workspace_bytes(T, h, F, t) < 2 * T * F + 2 * ldT * (2 * h + 2 * F)
+
+
+def test_transpose_argument_errors(L):
+    S, NU, AL = binding.TPMLP_ERR_SHAPE, binding.TPMLP_ERR_NULL, binding.TPMLP_ERR_ALIGN
+    assert L.tp_transpose(P, 130, 70, P, 136, N) == S    # cols % 8
+    assert L.tp_transpose(P, 130, 72, P, 128, N) == S    # ld_out < 136
+    assert L.tp_transpose(P, 130, 72, P, 140, N) == S    # ld_out % 8
+    assert L.tp_transpose(P, -1, 72, P, 136, N) == S
+    assert L.tp_transpose(N, 130, 72, P, 136, N) == NU
+    assert L.tp_transpose(P, 130, 72, Q, 136, N) == AL
+    assert L.tp_transpose(N, 0, 72, N, 0, N) == binding.TPMLP_OK  # nothing to do
+    assert L.tp_transpose(N, 130, 0, N, 136, N) == binding.TPMLP_OK
+
+
+def test_kmajor_weight_grad_argument_errors(L):
+    S = binding.TPMLP_ERR_SHAPE
+    for fn in (L.tp_mlp_dA_kmajor, L.tp_mlp_dB_kmajor):
+        assert fn(P, P, 130, 128, 256, 1024, 2, P, N) == S   # ldT < 136
+        assert fn(P, P, 130, 140, 256, 1024, 2, P, N) == S   # ldT % 8
+        assert fn(P, P, 130, 136, 256, 1000, 8, P, N) == S   # F / t % 8
+        assert fn(N, P, 130, 136, 256, 1024, 2, P, N) == binding.TPMLP_ERR_NULL
+        assert fn(P, P, 130, 136, 256, 1024, 2, N, N) == binding.TPMLP_ERR_NULL
+        assert fn(P, Q, 130, 136, 256, 1024, 2, P, N) == binding.TPMLP_ERR_ALIGN
+
+
 def test_split_workspace_sizes(L):
     # few output tiles (T=512, h=4096: 2 x 16 tiles of 256 x 256): the
     # row-parallel GEMMs split their reduction, and the scratch covers it
