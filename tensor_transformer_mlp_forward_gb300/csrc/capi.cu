@@ -240,6 +240,91 @@ struct Output {
     int k_splits;  // > 1: ptr0 is an fp32 [k_splits, rows, cols] partial-sum workspace
 };
 
+// ------------------------------------------------------------ tail split
+//
+// A persistent GEMM over `tiles` output tiles on `units` CTA pairs runs
+// ceil(tiles / units) rounds of tiles; when the last round is only partly
+// full the rest of the GPU idles for a whole tile's time (640 tiles on 76
+// pairs: 9 rounds for 8.42 rounds of work).  The tail split runs the first
+// `main` tiles (whole rounds) as usual, then cuts each of the last X tiles'
+// reduction into S contiguous k ranges computed by different pairs as fp32
+// partial tiles, and a reduce kernel adds the S partials of each tile in k
+// order and applies the fused epilogue (bias, residual, dropout).  Used for
+// the row-parallel GEMMs, whose epilogue the reduce kernel can apply.
+
+constexpr long long kTailTileFloats = 2LL * BM * BN;  // one 256 x 256 fp32 partial tile
+
+struct TailPlan {
+    long long main;  // tiles computed whole, a multiple of units
+    long long X;     // tail tiles
+    int S;           // k ranges per tail tile (1: no tail split)
+};
+
+// Estimated time of a plan: (main / units + ceil(X S / units) / S) rounds of
+// a whole tile, plus the partial tiles' write and read at HBM speed and two
+// more launches.  A tile's time is its 2 x 256 x 256 x K flops at a CTA
+// pair's share of the dense bf16 rate under the power cap (~1.5 PFLOP/s over
+// 76 pairs).  Among X = rem, rem + units, rem + 2 units and S = 2..8 (at
+// least 8 k-blocks per range; partials within ws_floats) the fastest plan is
+// taken when it beats the plain schedule.
+TailPlan plan_tail(long long tiles, long long total_kb, int units, long long ws_floats) {
+    constexpr double kPairFlopsPerNs = 1.5e6 / 76;   // 1.5 PFLOP/s over 76 pairs
+    constexpr double kHbmBytesPerNs = 6500.0;
+    constexpr double kLaunchNs = 4000.0;
+    TailPlan best{tiles, 0, 1};
+    if (units <= 0 || tiles <= units || tiles % units == 0) return best;
+    const double tile_ns = 2.0 * 2 * BM * BN * BK * static_cast<double>(total_kb) / kPairFlopsPerNs;
+    const double base = static_cast<double>(cdiv(tiles, units)) * tile_ns;
+    double best_t = base;
+    const long long rem = tiles % units;
+    for (long long X = rem; X <= tiles && X <= rem + 2LL * units; X += units) {
+        for (int S = 2; S <= 8 && total_kb / S >= 8; ++S) {
+            if (X * S * kTailTileFloats > ws_floats) break;
+            const double rounds = static_cast<double>((tiles - X) / units) +
+                                  static_cast<double>(cdiv(X * S, units)) / S;
+            const double t = rounds * tile_ns + 2.0 * kLaunchNs +
+                             2.0 * 4.0 * static_cast<double>(X * S * kTailTileFloats) / kHbmBytesPerNs;
+            if (t < best_t - 1e-9) {
+                best_t = t;
+                best = TailPlan{tiles - X, X, S};
+            }
+        }
+    }
+    return best;
+}
+
+// What a tail split needs besides the GEMM itself: the same GEMM with the
+// EPI_PARTIAL epilogue, a workspace for the partial tiles and the fused
+// epilogue's operands for the reduce kernel.
+struct TailSpec {
+    Launcher partial_fn;
+    void* ws;
+    size_t ws_bytes;
+    const tpmlp_bf16* bias;  // may be null (no epilogue: dX)
+    const tpmlp_bf16* res;
+    Dropout dr;
+};
+
+int launch_tail_reduce(const float* P, int S, const GemmArgs& g, long long first, long long X,
+                       const TailSpec& ts, tpmlp_bf16* out, cudaStream_t st);
+
+// fp32 map over X S compact partial tiles [X S, 256, 256]: 32 x 32 boxes.
+int make_tail_map(CUtensorMap* m, void* ptr, long long slots) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(BN), static_cast<cuuint64_t>(2 * BM),
+                          static_cast<cuuint64_t>(slots)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(BN) * 4,
+                             static_cast<cuuint64_t>(2 * BM) * BN * 4};
+    cuuint32_t box[3] = {32, 32, 1}, estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        t_last_cuda_error = static_cast<int>(r);
+        return TPMLP_ERR_LAUNCH;
+    }
+    return TPMLP_OK;
+}
+
 // One GEMM: M x N output per shard, K reduction (per shard for SHARD_K).
 struct GemmShape {
     int M, N, K, t, mode;
@@ -247,7 +332,8 @@ struct GemmShape {
 };
 
 int run_gemm(Launcher fn, const Operand& a, const Operand& b, const Output& out, GemmArgs& g,
-             const GemmShape& sh, cudaStream_t st, const DeviceInfo& dev) {
+             const GemmShape& sh, cudaStream_t st, const DeviceInfo& dev,
+             const TailSpec* tail = nullptr) {
     const int pair_mode = g_pair_mode.load(std::memory_order_relaxed);
     GemmArgs probe = g;
     tile_space(probe, sh.M, sh.N, sh.K, sh.t, sh.mode, sh.a_bytes, sh.b_bytes, 2 * BM);
@@ -303,11 +389,30 @@ int run_gemm(Launcher fn, const Operand& a, const Operand& b, const Output& out,
     if (rc) return rc;
     g.status = dev.status;
     const int units = pair ? std::max(1, dev.sms / 2) : dev.sms;
-    const int grid = std::min(g.num_tiles, units);
-    cudaError_t e = fn(maps, g, grid, pair, st);
+    TailPlan plan{g.num_tiles, 0, 1};
+    if (tail != nullptr && pair && out.k_splits <= 1 && tail->ws != nullptr)
+        plan = plan_tail(g.num_tiles, 1LL * g.k_blocks * (f.mode == SHARD_K ? f.t : 1), units,
+                         static_cast<long long>(tail->ws_bytes / sizeof(float)));
+    GemmArgs gm = g;
+    if (plan.S > 1) gm.num_tiles = gm.base_tiles = static_cast<int>(plan.main);  // whole rounds
+    cudaError_t e = fn(maps, gm, std::min(gm.num_tiles, units), pair, st);
     if (e != cudaSuccess) return fail_cuda(e);
     ++t_last_launches;
-    return TPMLP_OK;
+    if (plan.S <= 1) return TPMLP_OK;
+    // the tail: X tiles x S k ranges into compact partial tiles, then the reduce
+    GemmArgs gt = g;
+    gt.tile_offset = static_cast<int>(plan.main);
+    gt.base_tiles = static_cast<int>(plan.X);
+    gt.k_splits = plan.S;
+    gt.num_tiles = static_cast<int>(plan.X * plan.S);
+    gt.partial_compact = 1;
+    if ((rc = make_tail_map(&maps.o0, tail->ws, plan.X * plan.S))) return rc;
+    maps.o1 = maps.o0;
+    e = tail->partial_fn(maps, gt, std::min(gt.num_tiles, units), pair, st);
+    if (e != cudaSuccess) return fail_cuda(e);
+    ++t_last_launches;
+    return launch_tail_reduce(static_cast<const float*>(tail->ws), plan.S, g, plan.main, plan.X,
+                              *tail, static_cast<tpmlp_bf16*>(out.ptr0), st);
 }
 
 GemmArgs blank_args() {
@@ -364,29 +469,24 @@ constexpr int kSizingPairs = 76;
 
 long long row_total_kb(int F, int t) { return cdiv(F / t, BK) * t; }
 
-// Floats of split-reduction workspace the row-parallel GEMMs of this shape use.
+// Floats of split-reduction workspace the row-parallel GEMMs of this shape
+// use: a whole split, or else the partial tiles of a tail split.
 size_t split_partial_floats(int T, int h, int F, int t) {
-    const int sp = choose_splits(T, h, row_total_kb(F, t), kSizingPairs);
-    return sp > 1 ? static_cast<size_t>(sp) * T * h : 0;
+    const long long total_kb = row_total_kb(F, t);
+    const int sp = choose_splits(T, h, total_kb, kSizingPairs);
+    if (sp > 1) return static_cast<size_t>(sp) * T * h;
+    const long long tiles = cdiv(T, 2 * BM) * cdiv(h, BN);
+    const TailPlan p = plan_tail(tiles, total_kb, kSizingPairs, 1LL << 60);
+    return p.S > 1 ? static_cast<size_t>(p.X * p.S * kTailTileFloats) : 0;
 }
 
-// out[i] = bf16(sum_s P[s][i] (+ bias[i % n] + res[i])), 8 elements a thread;
-// with dropout, out[i] = res[i] + keep(i) * (sum_s P[s][i] + bias[i % n]) * scale.
-__global__ void __launch_bounds__(256)
-    split_reduce_kernel(const float* __restrict__ P, int splits, long long count, int n,
-                        const __nv_bfloat16* __restrict__ bias, const __nv_bfloat16* __restrict__ res,
-                        Dropout dr, __nv_bfloat16* __restrict__ out) {
-    const long long i = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
-    if (i >= count) return;
-    float a[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) a[j] = 0.0f;
-    for (int sp = 0; sp < splits; ++sp) {
-        const float4* q = reinterpret_cast<const float4*>(P + sp * count + i);
-        const float4 x = __ldg(q), y = __ldg(q + 1);
-        a[0] += x.x; a[1] += x.y; a[2] += x.z; a[3] += x.w;
-        a[4] += y.x; a[5] += y.y; a[6] += y.z; a[7] += y.w;
-    }
+// The fused epilogue of the row-parallel GEMMs on 8 fp32 sums of elements
+// i..i+7 of a row-major [., n] output: + bias[i % n] + res[i]; with dropout,
+// res[i] + keep(i) * (sum + bias[i % n]) * scale; bias null: the sums alone.
+// Returns them as bf16.
+__device__ __forceinline__ uint4 finish8(float (&a)[8], long long i, int n,
+                                         const __nv_bfloat16* __restrict__ bias,
+                                         const __nv_bfloat16* __restrict__ res, const Dropout& dr) {
     if (bias != nullptr) {
         const uint4 b = __ldg(reinterpret_cast<const uint4*>(bias + i % n));
         const uint4 r = __ldg(reinterpret_cast<const uint4*>(res + i));
@@ -414,7 +514,69 @@ __global__ void __launch_bounds__(256)
     o.y = pack_bf16x2(a[2], a[3]);
     o.z = pack_bf16x2(a[4], a[5]);
     o.w = pack_bf16x2(a[6], a[7]);
-    *reinterpret_cast<uint4*>(out + i) = o;
+    return o;
+}
+
+// out[i] = finish8(sum_s P[s][i]), 8 elements a thread, P: [splits, count].
+__global__ void __launch_bounds__(256)
+    split_reduce_kernel(const float* __restrict__ P, int splits, long long count, int n,
+                        const __nv_bfloat16* __restrict__ bias, const __nv_bfloat16* __restrict__ res,
+                        Dropout dr, __nv_bfloat16* __restrict__ out) {
+    const long long i = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
+    if (i >= count) return;
+    float a[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) a[j] = 0.0f;
+    for (int sp = 0; sp < splits; ++sp) {
+        const float4* q = reinterpret_cast<const float4*>(P + sp * count + i);
+        const float4 x = __ldg(q), y = __ldg(q + 1);
+        a[0] += x.x; a[1] += x.y; a[2] += x.z; a[3] += x.w;
+        a[4] += y.x; a[5] += y.y; a[6] += y.z; a[7] += y.w;
+    }
+    *reinterpret_cast<uint4*>(out + i) = finish8(a, i, n, bias, res, dr);
+}
+
+// The tail tiles of a tail split (plan_tail): tile `local` of X is output
+// tile first + local of the GEMM's raster order; its S partial tiles sit in
+// slots s X + local (s = 0..S-1, k order) of P, 256 x 256 fp32 each.  A
+// thread adds 8 consecutive columns of one row over s in order and applies
+// finish8; 32 CTAs cover a tile.
+__global__ void __launch_bounds__(256)
+    tail_reduce_kernel(const float* __restrict__ P, int S, GemmArgs g, int X,
+                       const __nv_bfloat16* __restrict__ bias, const __nv_bfloat16* __restrict__ res,
+                       Dropout dr, __nv_bfloat16* __restrict__ out) {
+    const int local = static_cast<int>(blockIdx.x >> 5);
+    const int e = static_cast<int>(((blockIdx.x & 31u) * blockDim.x + threadIdx.x) * 8u);
+    const int r = e / BN, c = e % BN;
+    const TileCoord tc = decode_tile<2 * BM>(local, g);
+    const int row = tc.m0 + r, col = tc.n0 + c;
+    if (row >= g.M || col >= g.N) return;
+    float a[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) a[j] = 0.0f;
+    for (int sp = 0; sp < S; ++sp) {
+        const float4* q = reinterpret_cast<const float4*>(
+            P + (static_cast<long long>(sp) * X + local) * kTailTileFloats + e);
+        const float4 x = __ldg(q), y = __ldg(q + 1);
+        a[0] += x.x; a[1] += x.y; a[2] += x.z; a[3] += x.w;
+        a[4] += y.x; a[5] += y.y; a[6] += y.z; a[7] += y.w;
+    }
+    const long long i = static_cast<long long>(row) * g.N + col;
+    *reinterpret_cast<uint4*>(out + i) = finish8(a, i, g.N, bias, res, dr);
+}
+
+int launch_tail_reduce(const float* P, int S, const GemmArgs& g, long long first, long long X,
+                       const TailSpec& ts, tpmlp_bf16* out, cudaStream_t st) {
+    GemmArgs r = g;
+    r.tile_offset = static_cast<int>(first);
+    r.base_tiles = static_cast<int>(X);
+    tail_reduce_kernel<<<static_cast<unsigned>(X * 32), 256, 0, st>>>(
+        P, S, r, static_cast<int>(X), cb(ts.bias), cb(ts.res), ts.dr,
+        reinterpret_cast<__nv_bfloat16*>(out));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail_cuda(e);
+    ++t_last_launches;
+    return TPMLP_OK;
 }
 
 int launch_split_reduce(const float* P, int splits, int T, int h, const tpmlp_bf16* bias,
@@ -454,7 +616,8 @@ int row_sum(const tpmlp_bf16* H, const tpmlp_bf16* B, const tpmlp_bf16* b2,
     const int sp = ws ? row_splits(T, h, F, t, ws_bytes, d) : 1;
     if (sp == 1) {
         Output o{Y, nullptr, T, h, 1};
-        return run_gemm(launch_row_sum, a, b, o, g, sh, st, d);
+        const TailSpec ts{launch_row_partial, ws, ws_bytes, b2, R, dr};
+        return run_gemm(launch_row_sum, a, b, o, g, sh, st, d, &ts);
     }
     Output o{ws, nullptr, T, h, sp};
     if (int rc = run_gemm(launch_row_partial, a, b, o, g, sh, st, d)) return rc;
@@ -540,7 +703,8 @@ int dx_gemm(const tpmlp_bf16* dZ, const tpmlp_bf16* A, int T, int h, int F, int 
     const int sp = ws ? row_splits(T, h, F, t, ws_bytes, d) : 1;
     if (sp == 1) {
         Output o{dX, nullptr, T, h, 1};
-        return run_gemm(launch_dx, a, b, o, g, sh, st, d);
+        const TailSpec ts{launch_dx_partial, ws, ws_bytes, nullptr, nullptr, Dropout{}};
+        return run_gemm(launch_dx, a, b, o, g, sh, st, d, &ts);
     }
     Output o{ws, nullptr, T, h, sp};
     if (int rc = run_gemm(launch_dx_partial, a, b, o, g, sh, st, d)) return rc;

@@ -112,19 +112,29 @@ struct GemmArgs {
     float* colsum;  // EPI_DGELU: column sums per 32-row block, [4 * mt_total][ld_colsum]
     long long ld_colsum;
     int* status;    // device status word
+    // This launch covers output tiles [tile_offset, tile_offset + base_tiles)
+    // of the raster order (decode_tile); 0 and all tiles by default.
+    int tile_offset;
+    // EPI_PARTIAL: 1 = the partial sums of work unit u go to slot u of a
+    // compact [units, TILE_M, BN] fp32 map (tile-local coordinates) instead
+    // of split ks of a [splits, M, N] map.
+    int partial_compact;
 };
 
 struct TileCoord {
     int m0, n0, s;
-    int ks;  // k-range split of this work unit (0 unless the reduction is split)
+    int ks;    // k-range split of this work unit (0 unless the reduction is split)
+    int slot;  // the work unit's index in this launch
 };
 
 template <int TILE_M>
 __device__ __forceinline__ TileCoord decode_tile(int tile, const GemmArgs& p) {
     // Work unit -> (split, output tile): the splits of one tile are
     // base_tiles apart, so each split sweeps the tiles in the order below.
+    const int slot = tile;
     const int ks = tile / p.base_tiles;
     tile -= ks * p.base_tiles;
+    tile += p.tile_offset;
     // Tiles are visited in bands of `band` tiles along the fast dimension:
     // inside a band the fast index cycles over the band while the slow index
     // advances, so the band's panels of the fast-dimension operand stay in L2
@@ -148,6 +158,7 @@ __device__ __forceinline__ TileCoord decode_tile(int tile, const GemmArgs& p) {
     TileCoord c;
     c.s = 0;
     c.ks = ks;
+    c.slot = slot;
     if (p.shard_mode == SHARD_N) {
         c.s = ni / p.n_tiles;
         ni -= c.s * p.n_tiles;
@@ -580,7 +591,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     __syncwarp();
                     if (row0 < p.M && n < p.N) {  // warp-uniform
                         if (lane == 0) {
-                            tma_store_3d(&tmO0, buf, n, row0, tc.ks);
+                            if (p.partial_compact)
+                                tma_store_3d(&tmO0, buf, n - tc.n0, row0 - tc.m0, tc.slot);
+                            else
+                                tma_store_3d(&tmO0, buf, n, row0, tc.ks);
                             bulk_commit_group();
                         }
                         ++seq;

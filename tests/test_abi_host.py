@@ -122,8 +122,12 @@ def test_split_workspace_sizes(L):
     n = L.tp_mlp_split_workspace_bytes(512, 4096, 16384, 8)
     assert n > 0 and n % (4 * 512 * 4096) == 0
     assert L.tp_mlp_forward_workspace_bytes(512, 4096, 16384, 8) == n
-    # many tiles (MT-NLG 530B): no split, no scratch
-    assert L.tp_mlp_split_workspace_bytes(2048, 20480, 81920, 8) == 0
+    # many tiles (MT-NLG 530B, 640 of them): no whole split, but the last
+    # round's 32 tiles are split 7 ways into 256 x 256 fp32 partial tiles
+    assert L.tp_mlp_split_workspace_bytes(2048, 20480, 81920, 8) == 32 * 7 * 256 * 256 * 4
+    # a multiple of 76 tiles, or too short a reduction to repay a split: nothing
+    assert L.tp_mlp_split_workspace_bytes(2048, 19456, 81920, 8) == 0
+    assert L.tp_mlp_split_workspace_bytes(8192, 1024, 4096, 2) == 0
     assert L.tp_mlp_split_workspace_bytes(0, 4096, 16384, 8) == 0
     # the backward workspace includes the dX split scratch
     assert (L.tp_mlp_backward_workspace_bytes(512, 4096, 16384, 8)

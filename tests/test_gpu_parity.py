@@ -121,6 +121,45 @@ def test_split_reduction_matches_unsplit():
     assert not torch.equal(dx_split, dx_one)  # the split path really ran
 
 
+def test_tail_split_matches_one_launch():
+    """384 output tiles of 256 x 256 on 76 CTA pairs (5.05 rounds): with a
+    workspace the row-parallel GEMMs (a3, also with dropout, and a7) run the
+    five whole rounds in one launch and split the last 4 tiles' reduction
+    into k ranges (fp32 partial tiles, then a reduce kernel with the fused
+    epilogue): three launches.  Without a workspace one launch computes every
+    tile.  The two agree bit for bit outside the tail tiles and within one
+    bf16 rounding inside them."""
+    T, h, F, t = 2048, 12288, 4096, 2
+    g = torch.Generator().manual_seed(31)
+    bf = lambda *s, std=1.0: (torch.randn(*s, generator=g) * std).to(torch.bfloat16).cuda()  # noqa: E731
+    H, B, b2, R = bf(T, F, std=0.5), bf(F, h, std=0.02), bf(h, std=0.02), bf(T, h)
+    dZ, A = bf(T, F, std=0.5), bf(h, F, std=0.02)
+    assert binding.split_workspace_bytes(T, h, F, t) > 0
+    empty = torch.empty(0, dtype=torch.uint8, device="cuda")
+    units = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    tiles = (T // 256) * (h // 256)
+    runs = {
+        "row_sum": lambda ws: binding.tp_mlp_row_sum(H, B, b2, R, t, workspace=ws),
+        "row_sum_dropout": lambda ws: binding.tp_mlp_row_sum_dropout(H, B, b2, R, t, 0.1, 99, 0,
+                                                                     workspace=ws),
+        "dx": lambda ws: binding.tp_mlp_dx(dZ, A, t, workspace=ws),
+    }
+    for name, fn in runs.items():
+        tail = fn(None)
+        n_tail = binding.last_launch_count()
+        one = fn(empty)
+        n_one = binding.last_launch_count()
+        torch.cuda.synchronize()
+        assert binding.device_status() == 0
+        assert n_one == 1, name
+        if tiles % units == 0 or tiles < units:
+            continue  # no partly full round on this GPU
+        assert n_tail == 3, name
+        assert rel(np64(tail), np64(one)) < TOL_FWD, name
+        differ = int((tail != one).sum())
+        assert differ <= (tiles % units + 2 * units) * 256 * 256, name
+
+
 def test_empty_batch():
     w = inputs.custom(T=0, h=64, F=256, t=2, seed=17)
     cpu = inputs.make_inputs(w)
@@ -183,6 +222,7 @@ def check_sampled(w: inputs.Workload, nrows=8, ncols=16):
 
 
 FULL = [
+    inputs.custom(T=2048, h=12288, F=4096, t=2, seed=32, name="tail-split"),  # 384 tiles, 76 pairs
     inputs.GPT2_MEDIUM.with_shape(T=8192, t=1),
     inputs.GPT2_MEDIUM.with_shape(T=8192, t=2),
     inputs.MEGATRON_8_3B,
