@@ -16,7 +16,7 @@ import json
 import sys
 
 CALLS = ("column_gelu", "column_gelu_h_only", "row_sum", "row_sum_dropout", "dgelu", "dx", "dA",
-         "dB", "dropout_grad", "ln_forward", "ln_backward")
+         "dB", "dA_kmajor", "dB_kmajor", "transpose", "dropout_grad", "ln_forward", "ln_backward")
 
 
 def parse_args(argv=None):
@@ -73,6 +73,18 @@ def main(argv=None) -> int:
     elif c == "dB":
         H, dY, dB = bf(T, F), bf(T, h), bf(F, h)
         fn = lambda: b.tp_mlp_dB(H, dY, t, dB=dB)  # noqa: E731
+    elif c == "dA_kmajor":  # from X^T [h, ldT] and dZ^T [F, ldT]
+        ld = b.pitch(T)
+        Xt, dZt, dA = bf(h, ld), bf(F, ld), bf(h, F)
+        fn = lambda: b.tp_mlp_dA_kmajor(Xt, dZt, T, t, dA=dA)  # noqa: E731
+    elif c == "dB_kmajor":  # from H^T [F, ldT] and dY^T [h, ldT]
+        ld = b.pitch(T)
+        Ht, dYt, dB = bf(F, ld), bf(h, ld), bf(F, h)
+        fn = lambda: b.tp_mlp_dB_kmajor(Ht, dYt, T, t, dB=dB)  # noqa: E731
+    elif c == "transpose":  # dZ [T, F] -> dZ^T [F, ldT]
+        dZ = bf(T, F)
+        dZt = torch.empty(F, b.pitch(T), dtype=torch.bfloat16, device=dev)
+        fn = lambda: b.tp_transpose(dZ, out=dZt)  # noqa: E731
     elif c == "dropout_grad":
         dY, dP = bf(T, h), bf(T, h)
         fn = lambda: b.tp_mlp_dropout_grad(dY, a.dropout, 7, 0, dP=dP)  # noqa: E731
