@@ -501,37 +501,66 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
 // ------------------------------------------------------------ delta
 
-// delta[head, tok] = sum_c dO[tok, head*d + c] * O[tok, head*d + c], fp32;
-// one thread per (token, head).  All of a thread's 16-byte loads are issued
-// before any product, so each thread keeps d/4 loads in flight.
+// delta[head, tok] = sum_c dO[tok, head*d + c] * O[tok, head*d + c], fp32.
+// The (token, head) segments of d elements lie end to end in dO and O, d/8
+// 16-byte chunks each.  A CTA takes kDeltaSegs(d) whole segments (at most
+// 2048 chunks): its 256 threads read the chunks coalesced (chunk base + tid +
+// 256 k, all loads issued before any product), each chunk's 8 products are
+// summed and parked in shared memory, and one thread per segment adds its
+// chunks in order.
+constexpr int kDeltaChunks = 2048;
+constexpr int kDeltaThreads = 256;
 template <int D>
-__global__ void __launch_bounds__(256)
+constexpr int delta_segs() { return kDeltaChunks / (D / 8); }
+
+template <int D>
+__global__ void __launch_bounds__(kDeltaThreads)
     attn_delta_kernel(const __nv_bfloat16* __restrict__ dO, const __nv_bfloat16* __restrict__ O,
-                      long long T, int h, int nh, float* __restrict__ delta) {
-    const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (idx >= T * nh) return;
-    const long long tok = idx / nh;
-    const int head = static_cast<int>(idx - tok * nh);
-    const uint4* g = reinterpret_cast<const uint4*>(dO + tok * h + head * D);
-    const uint4* o = reinterpret_cast<const uint4*>(O + tok * h + head * D);
-    uint4 gu[D / 8], ou[D / 8];
+                      long long T, int nh, float* __restrict__ delta) {
+    constexpr int CH = D / 8;                 // chunks per segment
+    constexpr int SEGS = delta_segs<D>();     // segments per CTA
+    constexpr int PER = (SEGS * CH + kDeltaThreads - 1) / kDeltaThreads;
+    __shared__ float part[SEGS * CH];
+    const long long seg0 = static_cast<long long>(blockIdx.x) * SEGS;
+    const long long segs_total = T * nh;
+    const int segs = static_cast<int>(segs_total - seg0 < SEGS ? segs_total - seg0 : SEGS);
+    const int chunks = segs * CH;
+    const uint4* g = reinterpret_cast<const uint4*>(dO) + seg0 * CH;
+    const uint4* o = reinterpret_cast<const uint4*>(O) + seg0 * CH;
+    uint4 gu[PER], ou[PER];
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i) {
-        gu[i] = __ldg(g + i);
-        ou[i] = __ldg(o + i);
-    }
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-    for (int i = 0; i < D / 8; ++i) {
-        const uint32_t gw[4] = {gu[i].x, gu[i].y, gu[i].z, gu[i].w};
-        const uint32_t ow[4] = {ou[i].x, ou[i].y, ou[i].z, ou[i].w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            acc[j] = fmaf(__uint_as_float(gw[j] << 16), __uint_as_float(ow[j] << 16), acc[j]);
-            acc[j] = fmaf(__uint_as_float(gw[j] & 0xFFFF0000u), __uint_as_float(ow[j] & 0xFFFF0000u), acc[j]);
+    for (int k = 0; k < PER; ++k) {
+        const int c = threadIdx.x + k * kDeltaThreads;
+        if (c < chunks) {
+            gu[k] = __ldg(g + c);
+            ou[k] = __ldg(o + c);
         }
     }
-    delta[static_cast<long long>(head) * T + tok] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        const int c = threadIdx.x + k * kDeltaThreads;
+        if (c < chunks) {
+            const uint32_t gw[4] = {gu[k].x, gu[k].y, gu[k].z, gu[k].w};
+            const uint32_t ow[4] = {ou[k].x, ou[k].y, ou[k].z, ou[k].w};
+            float acc = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                acc = fmaf(__uint_as_float(gw[j] << 16), __uint_as_float(ow[j] << 16), acc);
+                acc = fmaf(__uint_as_float(gw[j] & 0xFFFF0000u), __uint_as_float(ow[j] & 0xFFFF0000u), acc);
+            }
+            part[c] = acc;
+        }
+    }
+    __syncthreads();
+    for (int t = threadIdx.x; t < segs; t += kDeltaThreads) {
+        float sum = 0.0f;
+#pragma unroll
+        for (int i = 0; i < CH; ++i) sum += part[t * CH + i];
+        const long long sg = seg0 + t;
+        const long long tok = sg / nh;
+        const long long head = sg - tok * nh;
+        delta[head * T + tok] = sum;
+    }
 }
 
 // ------------------------------------------------------------- dQ
@@ -1150,12 +1179,20 @@ cudaError_t launch_attn_backward(const CUtensorMap& tm_qkv128, const CUtensorMap
     a.status = p.status;
     // delta = rowsum(dO * O)
     {
-        const long long items = a.T * p.nh;
-        const unsigned blocks = static_cast<unsigned>((items + 255) / 256);
-        if (d == 64) attn_delta_kernel<64><<<blocks, 256, 0, st>>>(p.dO, p.O_in, a.T, p.h, p.nh, p.delta_out);
-        if (d == 96) attn_delta_kernel<96><<<blocks, 256, 0, st>>>(p.dO, p.O_in, a.T, p.h, p.nh, p.delta_out);
-        if (d == 128) attn_delta_kernel<128><<<blocks, 256, 0, st>>>(p.dO, p.O_in, a.T, p.h, p.nh, p.delta_out);
-        if (d == 160) attn_delta_kernel<160><<<blocks, 256, 0, st>>>(p.dO, p.O_in, a.T, p.h, p.nh, p.delta_out);
+        const long long items = a.T * p.nh;  // (token, head) segments
+        auto blocks = [&](int segs) { return static_cast<unsigned>((items + segs - 1) / segs); };
+        if (d == 64)
+            attn_delta_kernel<64><<<blocks(delta_segs<64>()), kDeltaThreads, 0, st>>>(
+                p.dO, p.O_in, a.T, p.nh, p.delta_out);
+        if (d == 96)
+            attn_delta_kernel<96><<<blocks(delta_segs<96>()), kDeltaThreads, 0, st>>>(
+                p.dO, p.O_in, a.T, p.nh, p.delta_out);
+        if (d == 128)
+            attn_delta_kernel<128><<<blocks(delta_segs<128>()), kDeltaThreads, 0, st>>>(
+                p.dO, p.O_in, a.T, p.nh, p.delta_out);
+        if (d == 160)
+            attn_delta_kernel<160><<<blocks(delta_segs<160>()), kDeltaThreads, 0, st>>>(
+                p.dO, p.O_in, a.T, p.nh, p.delta_out);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         ++*launches;
