@@ -576,6 +576,14 @@ struct DqCfg {
     static constexpr int SMEM = 1024 + FIXED + STAGES * 2 * KV_TILE + 256;
 };
 
+// Work items of the dQ kernel: (128 queries, sequence, head), heaviest
+// (most key tiles) first.  CTAs take them one at a time from g_dq_work[0]
+// (atomicAdd) until it runs past the last item; the last CTA to finish
+// (counted in g_dq_work[1]) sets both counters back to zero for the next
+// launch.  Launches on different streams that overlap on the GPU would
+// share the counters: the backward runs its kernels in stream order.
+__device__ unsigned int g_dq_work[2];
+
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q128,  // QKV, 128-row boxes
@@ -591,28 +599,42 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint8_t* sdO = sQ + C::ROW_TILE;
     uint8_t* ring = sdO + C::ROW_TILE;
     uint64_t* bars = reinterpret_cast<uint64_t*>(ring + S * 2 * C::KV_TILE);
-    uint64_t* q_full = bars;
-    uint64_t* kv_full = bars + 1;
+    uint64_t* q_full = bars;             // the item's Q and dO have landed
+    uint64_t* q_empty = bars + 1;        // the item's last S and dP MMAs have read them
+    uint64_t* kv_full = bars + 2;
     uint64_t* kv_empty = kv_full + S;
-    uint64_t* sdp_full = kv_empty + S;  // 2
-    uint64_t* ds_full = sdp_full + 2;   // 2
-    uint64_t* dq_done = ds_full + 2;
-    uint64_t* drain = dq_done + 1;
-    uint32_t* misc = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* sdp_full = kv_empty + S;   // [2]
+    uint64_t* ds_full = sdp_full + 2;    // [2]
+    uint64_t* dq_done = ds_full + 2;     // the item's dQ is complete in TMEM
+    uint64_t* dq_free = dq_done + 1;     // the softmax warps have read it out
+    uint64_t* item_full = dq_free + 1;   // [2] items[slot] holds the next item
+    uint64_t* item_empty = item_full + 2;  // [2] every consumer has read it
+    uint64_t* drain = item_empty + 2;
+    int* items = reinterpret_cast<int*>(drain + 1);  // [2]
+    uint32_t* misc = reinterpret_cast<uint32_t*>(items + 2);
     volatile uint32_t* abort_flag = misc + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int per_qt = a.nb * a.nh;
-    const int qt = a.q_tiles - 1 - static_cast<int>(blockIdx.x) / per_qt;
-    const int rem = static_cast<int>(blockIdx.x) % per_qt;
-    const int n = rem / a.nh, head = rem % a.nh;
-    const int q0 = qt * 128;
-    // 64-key tiles holding keys <= the tile's last valid query
-    const int last_q = min(q0 + 127, a.s - 1);
-    const int n_kv = last_q / 64 + 1;
+    const int total = a.q_tiles * per_qt;
+    struct Item {
+        int q0, n, head, n_kv;
+    };
+    auto decode = [&](int item) {
+        Item it;
+        const int qt = a.q_tiles - 1 - item / per_qt;
+        const int rem = item - (a.q_tiles - 1 - qt) * per_qt;
+        it.n = rem / a.nh;
+        it.head = rem - it.n * a.nh;
+        it.q0 = qt * 128;
+        // 64-key tiles holding keys <= the tile's last valid query
+        it.n_kv = min(it.q0 + 127, a.s - 1) / 64 + 1;
+        return it;
+    };
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
         for (int i = 0; i < S; ++i) {
             mbar_init(&kv_full[i], 1);
             mbar_init(&kv_empty[i], 1);
@@ -620,8 +642,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(&sdp_full[b], 1);
             mbar_init(&ds_full[b], 4);
+            mbar_init(&item_full[b], 1);
+            mbar_init(&item_empty[b], 5);  // the MMA thread and the 4 softmax warps
         }
         mbar_init(dq_done, 1);
+        mbar_init(dq_free, 4);
         mbar_init(drain, 1);
         misc[1] = 0u;
         fence_mbar_init();
@@ -642,34 +667,62 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             prefetch_tmap(&tm_q128);
             prefetch_tmap(&tm_kv64);
             prefetch_tmap(&tm_do128);
-            const int qcol = head * D, kcol = a.h + head * D, vcol = 2 * a.h + head * D;
-            mbar_arrive_expect_tx(q_full, 2 * C::ROW_TILE);
-            for (int b = 0; b < C::NB; ++b) {
-                tma_load_3d(&tm_q128, smem_u32(q_full), smem_u32(sQ) + b * 128 * kRowBytes,
-                            qcol + 64 * b, q0, n);
-                tma_load_3d(&tm_do128, smem_u32(q_full), smem_u32(sdO) + b * 128 * kRowBytes,
-                            qcol + 64 * b, q0, n);
-            }
             int stage = 0;
             uint32_t phase = 0, issued = 0, issued_phase = 0;
-            for (int j = 0; j < n_kv; ++j) {
-                if (!wait_bounded(&kv_empty[stage], phase ^ 1u, abort_flag, a.status, 0x201)) break;
-                mbar_arrive_expect_tx(&kv_full[stage], 2 * C::KV_TILE);
-                const uint32_t dst = smem_u32(ring) + stage * 2 * C::KV_TILE;
+            int q_loads = 0;  // Q/dO loads issued (q_full's completed phases)
+            bool ok = true;
+            for (int k = 0;; ++k) {
+                const int slot = k & 1;
+                // the slot's item k - 2 has been read by every consumer
+                if (k >= 2 && !wait_bounded(&item_empty[slot], static_cast<uint32_t>((k - 2) >> 1) & 1u,
+                                            abort_flag, a.status, 0x20B))
+                    ok = false;
+                int item = -1;
+                if (ok) {
+                    item = static_cast<int>(atomicAdd(&g_dq_work[0], 1u));
+                    if (item >= total) item = -1;
+                }
+                items[slot] = item;
+                mbar_arrive(&item_full[slot]);
+                if (item < 0) break;
+                const Item it = decode(item);
+                const int qcol = it.head * D, kcol = a.h + it.head * D, vcol = 2 * a.h + it.head * D;
+                // Q and dO: the previous item's S and dP MMAs are done with them
+                if (k >= 1 && !wait_bounded(q_empty, static_cast<uint32_t>(k - 1) & 1u, abort_flag,
+                                            a.status, 0x20C))
+                    break;
+                mbar_arrive_expect_tx(q_full, 2 * C::ROW_TILE);
                 for (int b = 0; b < C::NB; ++b) {
-                    tma_load_3d(&tm_kv64, smem_u32(&kv_full[stage]), dst + b * 64 * kRowBytes,
-                                kcol + 64 * b, j * 64, n);
-                    tma_load_3d(&tm_kv64, smem_u32(&kv_full[stage]),
-                                dst + C::KV_TILE + b * 64 * kRowBytes, vcol + 64 * b, j * 64, n);
+                    tma_load_3d(&tm_q128, smem_u32(q_full), smem_u32(sQ) + b * 128 * kRowBytes,
+                                qcol + 64 * b, it.q0, it.n);
+                    tma_load_3d(&tm_do128, smem_u32(q_full), smem_u32(sdO) + b * 128 * kRowBytes,
+                                qcol + 64 * b, it.q0, it.n);
                 }
-                issued |= 1u << stage;
-                issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-                if (++stage == S) {
-                    stage = 0;
-                    phase ^= 1u;
+                ++q_loads;
+                for (int j = 0; j < it.n_kv && ok; ++j) {
+                    if (!wait_bounded(&kv_empty[stage], phase ^ 1u, abort_flag, a.status, 0x201)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&kv_full[stage], 2 * C::KV_TILE);
+                    const uint32_t dst = smem_u32(ring) + stage * 2 * C::KV_TILE;
+                    for (int b = 0; b < C::NB; ++b) {
+                        tma_load_3d(&tm_kv64, smem_u32(&kv_full[stage]), dst + b * 64 * kRowBytes,
+                                    kcol + 64 * b, j * 64, it.n);
+                        tma_load_3d(&tm_kv64, smem_u32(&kv_full[stage]),
+                                    dst + C::KV_TILE + b * 64 * kRowBytes, vcol + 64 * b, j * 64, it.n);
+                    }
+                    issued |= 1u << stage;
+                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
+                if (!ok) break;
             }
-            wait_drain(q_full, 0, a.status, 0x202);
+            // every copy this thread started lands before the CTA may exit
+            if (q_loads > 0) wait_drain(q_full, static_cast<uint32_t>(q_loads - 1) & 1u, a.status, 0x202);
             for (int i = 0; i < S; ++i)
                 if (issued & (1u << i)) wait_drain(&kv_full[i], (issued_phase >> i) & 1u, a.status, 0x203);
         }
@@ -679,114 +732,154 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             constexpr uint32_t id_s = idesc_bf16_f32(128, 64, false, false);
             const uint64_t qdesc = smem_desc_sw128(smem_u32(sQ), 16, 1024);
             const uint64_t dodesc = smem_desc_sw128(smem_u32(sdO), 16, 1024);
-            int stage = 0, prev_stage = 0;
+            int stage = 0, g = 0;  // g: tiles of every item so far (S/dP buffer index)
             uint32_t phase = 0;
-            bool ok = wait_bounded(q_full, 0, abort_flag, a.status, 0x204);
-            tc_fence_after();
-            auto issue_dq = [&](int i, int st) {
+            bool ok = true;
+            // dQ += dS K for tile i of item k (global tile gi), K in ring stage st
+            auto issue_dq = [&](int i, int gi, int st, int k) {
                 if (!ok) return;
-                if (!wait_bounded(&ds_full[i & 1], static_cast<uint32_t>(i >> 1) & 1u, abort_flag,
+                // the first dQ MMA of an item overwrites the previous item's dQ
+                if (i == 0 && k >= 1 &&
+                    !wait_bounded(dq_free, static_cast<uint32_t>(k - 1) & 1u, abort_flag, a.status, 0x20D)) {
+                    ok = false;
+                    return;
+                }
+                if (!wait_bounded(&ds_full[gi & 1], static_cast<uint32_t>(gi >> 1) & 1u, abort_flag,
                                   a.status, 0x205)) {
                     ok = false;
                     return;
                 }
                 tc_fence_after();
-                // dQ += dS K: A = dS from TMEM (the softmax threads wrote it,
-                // packed bf16, over the first 32 columns of the S buffer), B = K
-                // (MN-major: d along the rows, keys down the 64-row box)
+                // A = dS from TMEM (the softmax threads wrote it, packed bf16,
+                // over the first 32 columns of the S buffer), B = K (MN-major:
+                // d along the rows, keys down the 64-row box)
                 const uint64_t kdesc = smem_desc_sw128(smem_u32(ring) + st * 2 * C::KV_TILE,
                                                        64 * kRowBytes, 1024);
-                mma_ts_n_is_d<D, 64 / 16>(tmem + kDQ, tmem + kS + 64 * (i & 1), kdesc,
+                mma_ts_n_is_d<D, 64 / 16>(tmem + kDQ, tmem + kS + 64 * (gi & 1), kdesc,
                                           64 * kRowBytes, i > 0);
                 tc_commit(&kv_empty[st]);
             };
-            for (int j = 0; j < n_kv && ok; ++j) {
-                if (!wait_bounded(&kv_full[stage], phase, abort_flag, a.status, 0x206)) {
+            for (int k = 0; ok; ++k) {
+                const int slot = k & 1;
+                if (!wait_bounded(&item_full[slot], static_cast<uint32_t>(k >> 1) & 1u, abort_flag,
+                                  a.status, 0x20E))
+                    break;
+                const int item = *reinterpret_cast<volatile int*>(&items[slot]);
+                mbar_arrive(&item_empty[slot]);
+                if (item < 0) break;
+                const Item it = decode(item);
+                if (!wait_bounded(q_full, static_cast<uint32_t>(k) & 1u, abort_flag, a.status, 0x204)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t kv = smem_u32(ring) + stage * 2 * C::KV_TILE;
-                const uint64_t kdesc = smem_desc_sw128(kv, 16, 1024);
-                const uint64_t vdesc = smem_desc_sw128(kv + C::KV_TILE, 16, 1024);
-                const uint32_t b = static_cast<uint32_t>(j & 1);
+                int prev_stage = 0;
+                for (int j = 0; j < it.n_kv && ok; ++j, ++g) {
+                    if (!wait_bounded(&kv_full[stage], phase, abort_flag, a.status, 0x206)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t kv = smem_u32(ring) + stage * 2 * C::KV_TILE;
+                    const uint64_t kdesc = smem_desc_sw128(kv, 16, 1024);
+                    const uint64_t vdesc = smem_desc_sw128(kv + C::KV_TILE, 16, 1024);
+                    const uint32_t b = static_cast<uint32_t>(g & 1);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    tc_mma_f16(tmem + kS + 64 * b, desc_add(qdesc, kmajor_step<128>(kk)),
-                               desc_add(kdesc, kmajor_step<64>(kk)), id_s, kk > 0 ? 1u : 0u);
-                    tc_mma_f16(tmem + kDP + 64 * b, desc_add(dodesc, kmajor_step<128>(kk)),
-                               desc_add(vdesc, kmajor_step<64>(kk)), id_s, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        tc_mma_f16(tmem + kS + 64 * b, desc_add(qdesc, kmajor_step<128>(kk)),
+                                   desc_add(kdesc, kmajor_step<64>(kk)), id_s, kk > 0 ? 1u : 0u);
+                        tc_mma_f16(tmem + kDP + 64 * b, desc_add(dodesc, kmajor_step<128>(kk)),
+                                   desc_add(vdesc, kmajor_step<64>(kk)), id_s, kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(&sdp_full[b]);
+                    // the item's last S and dP have been issued: once they are
+                    // done, Q and dO may be replaced by the next item's
+                    if (j == it.n_kv - 1) tc_commit(q_empty);
+                    if (j >= 1) issue_dq(j - 1, g - 1, prev_stage, k);
+                    prev_stage = stage;
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
-                tc_commit(&sdp_full[b]);
-                if (j >= 1) issue_dq(j - 1, prev_stage);
-                prev_stage = stage;
-                if (++stage == S) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
+                issue_dq(it.n_kv - 1, g - 1, prev_stage, k);
+                if (ok) tc_commit(dq_done);
             }
-            issue_dq(n_kv - 1, prev_stage);
-            tc_commit(dq_done);
             tc_commit(drain);
             wait_drain(drain, 0, a.status, 0x207);
         }
         __syncwarp();
     } else {
         const int r = threadIdx.x;
-        const int q = q0 + r;
-        const bool q_ok = q < a.s;
-        const long long tok = static_cast<long long>(n) * a.s + q;
-        const float lse = q_ok ? __ldg(a.lse_in + head * a.T + tok) : 0.0f;
-        const float dlt = q_ok ? __ldg(a.delta + head * a.T + tok) : 0.0f;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
         bool ok = true;
-        for (int j = 0; j < n_kv; ++j) {
-            const uint32_t b = static_cast<uint32_t>(j & 1);
-            // S(j) was issued after dQ(j-2), which read this buffer's
-            // previous dS, so once it is here the buffer is free
-            if (!warp_wait_bounded(&sdp_full[b], static_cast<uint32_t>(j >> 1) & 1u, abort_flag,
-                                   a.status, 0x208)) {
+        int g = 0;
+        for (int k = 0; ok; ++k) {
+            const int slot = k & 1;
+            if (!warp_wait_bounded(&item_full[slot], static_cast<uint32_t>(k >> 1) & 1u, abort_flag,
+                                   a.status, 0x20F))
+                break;
+            const int item = *reinterpret_cast<volatile int*>(&items[slot]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&item_empty[slot]);
+            if (item < 0) break;
+            const Item it = decode(item);
+            const int q = it.q0 + r;
+            const bool q_ok = q < a.s;
+            const long long tok = static_cast<long long>(it.n) * a.s + q;
+            const float lse = q_ok ? __ldg(a.lse_in + it.head * a.T + tok) : 0.0f;
+            const float dlt = q_ok ? __ldg(a.delta + it.head * a.T + tok) : 0.0f;
+            for (int j = 0; j < it.n_kv; ++j, ++g) {
+                const uint32_t b = static_cast<uint32_t>(g & 1);
+                // S(g) was issued after dQ(g-2), which read this buffer's
+                // previous dS, so once it is here the buffer is free
+                if (!warp_wait_bounded(&sdp_full[b], static_cast<uint32_t>(g >> 1) & 1u, abort_flag,
+                                       a.status, 0x208)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t sv[32], pv[32];
+                    tmem_ld32(lane_addr + kS + 64 * b + c * 32, sv);
+                    tmem_ld32(lane_addr + kDP + 64 * b + c * 32, pv);
+                    tmem_wait_ld();
+                    const int key0 = j * 64 + c * 32;
+                    // causal mask (keys after the query), only where this chunk
+                    // reaches past the row's query; a masked score of -inf gives
+                    // P = 0.  Rows past the sequence read zero Q and dO rows and
+                    // are never stored, so they need no mask.
+                    if (key0 + 31 > q) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (key0 + i > q) sv[i] = __float_as_uint(-INFINITY);
+                    }
+                    uint32_t dd[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float p0 = ex2(fmaf(__uint_as_float(sv[2 * i]), a.scale2, -lse));
+                        const float p1 = ex2(fmaf(__uint_as_float(sv[2 * i + 1]), a.scale2, -lse));
+                        dd[i] = pack_bf16x2(p0 * (__uint_as_float(pv[2 * i]) - dlt),
+                                            p1 * (__uint_as_float(pv[2 * i + 1]) - dlt));
+                    }
+                    // dS, packed, over the S columns this thread has read
+                    tmem_st16(lane_addr + kS + 64 * b + 16 * c, dd);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ds_full[b]);
+            }
+            if (!ok || !warp_wait_bounded(dq_done, static_cast<uint32_t>(k) & 1u, abort_flag, a.status,
+                                          0x20A)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t sv[32], pv[32];
-                tmem_ld32(lane_addr + kS + 64 * b + c * 32, sv);
-                tmem_ld32(lane_addr + kDP + 64 * b + c * 32, pv);
-                tmem_wait_ld();
-                const int key0 = j * 64 + c * 32;
-                // causal mask (keys after the query), only where this chunk
-                // reaches past the row's query; a masked score of -inf gives
-                // P = 0.  Rows past the sequence read zero Q and dO rows and
-                // are never stored, so they need no mask.
-                if (key0 + 31 > q) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (key0 + i > q) sv[i] = __float_as_uint(-INFINITY);
-                }
-                uint32_t dd[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float p0 = ex2(fmaf(__uint_as_float(sv[2 * i]), a.scale2, -lse));
-                    const float p1 = ex2(fmaf(__uint_as_float(sv[2 * i + 1]), a.scale2, -lse));
-                    dd[i] = pack_bf16x2(p0 * (__uint_as_float(pv[2 * i]) - dlt),
-                                        p1 * (__uint_as_float(pv[2 * i + 1]) - dlt));
-                }
-                // dS, packed, over the S columns this thread has read
-                tmem_st16(lane_addr + kS + 64 * b + 16 * c, dd);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ds_full[b]);
-        }
-        if (ok && warp_wait_bounded(dq_done, 0, abort_flag, a.status, 0x20A)) {
-            tc_fence_after();
             // tcgen05.ld is warp-collective (.sync.aligned): every lane loads,
             // only rows inside the sequence are stored
-            uint4* dst = reinterpret_cast<uint4*>(a.dqkv + tok * 3 * a.h + head * D);
+            uint4* dst = reinterpret_cast<uint4*>(a.dqkv + tok * 3 * a.h + it.head * D);
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t v[32];
@@ -804,6 +897,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     }
                 }
             }
+            // dQ is in registers or on its way to memory: the MMA may reuse it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(dq_free);
         }
     }
 
@@ -812,6 +909,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (warp == 5) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
+    }
+    // the last CTA out resets the work counters for the next launch
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(&g_dq_work[1], 1u) == gridDim.x - 1) {
+            g_dq_work[0] = 0u;
+            g_dq_work[1] = 0u;
+            __threadfence();
+        }
     }
 }
 
@@ -1203,12 +1309,21 @@ cudaError_t launch_attn_backward(const CUtensorMap& tm_qkv128, const CUtensorMap
     AttnArgs aq = a;
     aq.q_tiles = q_tiles;
     const unsigned grid = static_cast<unsigned>(q_tiles * p.nb * p.nh);
+    // the dQ kernel is persistent: one CTA per SM at most, items taken in turn
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = 1;
+    }
+    const unsigned dq_grid = grid < static_cast<unsigned>(sms) ? grid : static_cast<unsigned>(sms);
 #define TPMLP_ATTN_BWD(DD)                                                                          \
     if (d == DD) {                                                                                  \
         auto kq = attn_bwd_dq_kernel<DD>;                                                           \
         e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<DD>::SMEM); \
         if (e == cudaSuccess) {                                                                     \
-            kq<<<grid, kAttnThreads, DqCfg<DD>::SMEM, st>>>(tm_qkv128, tm_qkv64, tm_do128, aq);     \
+            kq<<<dq_grid, kAttnThreads, DqCfg<DD>::SMEM, st>>>(tm_qkv128, tm_qkv64, tm_do128, aq);  \
             e = cudaGetLastError();                                                                 \
         }                                                                                           \
         if (e == cudaSuccess) {                                                                     \
