@@ -934,6 +934,11 @@ struct DkvCfg {
     static constexpr int SMEM = 1024 + FIXED + STAGES * 2 * Q_TILE + 256;
 };
 
+// Work items of the dK/dV kernel: (128 keys, sequence, head), the first key
+// tiles (most queries after them) first; taken and the counters reset as
+// for the dQ kernel.
+__device__ unsigned int g_dkdv_work[2];
+
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k128,  // QKV, 128-row boxes
@@ -949,29 +954,42 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint8_t* sV = sK + C::KEY_TILE;
     uint8_t* ring = sV + C::KEY_TILE;
     uint64_t* bars = reinterpret_cast<uint64_t*>(ring + S * 2 * C::Q_TILE);
-    uint64_t* kv_full = bars;
-    uint64_t* q_full = bars + 1;
+    uint64_t* kv_full = bars;            // the item's K and V have landed
+    uint64_t* kv_empty = bars + 1;       // the item's last S^T and dP^T MMAs have read them
+    uint64_t* q_full = bars + 2;
     uint64_t* q_empty = q_full + S;
-    uint64_t* st_full = q_empty + S;  // 2
-    uint64_t* pds_full = st_full + 2;  // 2
-    uint64_t* grad_done = pds_full + 2;
-    uint64_t* drain = grad_done + 1;
-    uint32_t* misc = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* st_full = q_empty + S;     // [2]
+    uint64_t* pds_full = st_full + 2;    // [2]
+    uint64_t* grad_done = pds_full + 2;  // the item's dV and dK are complete in TMEM
+    uint64_t* grad_free = grad_done + 1; // the softmax warps have read them out
+    uint64_t* item_full = grad_free + 1;     // [2]
+    uint64_t* item_empty = item_full + 2;    // [2]
+    uint64_t* drain = item_empty + 2;
+    int* items = reinterpret_cast<int*>(drain + 1);  // [2]
+    uint32_t* misc = reinterpret_cast<uint32_t*>(items + 2);
     volatile uint32_t* abort_flag = misc + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // key tiles with the fewest queries after them are the lightest: the
-    // first key tiles (most queries) go first
     const int per_kt = a.nb * a.nh;
-    const int kt = static_cast<int>(blockIdx.x) / per_kt;
-    const int rem = static_cast<int>(blockIdx.x) % per_kt;
-    const int n = rem / a.nh, head = rem % a.nh;
-    const int k0 = kt * 128;
-    const int i0 = k0 / 64;                  // first 64-query tile with a query >= k0
-    const int nq = (a.s + 63) / 64 - i0;     // query tiles to visit
+    const int total = ((a.s + 127) / 128) * per_kt;
+    struct Item {
+        int k0, n, head, i0, nq;
+    };
+    auto decode = [&](int item) {
+        Item it;
+        const int kt = item / per_kt;
+        const int rem = item - kt * per_kt;
+        it.n = rem / a.nh;
+        it.head = rem - it.n * a.nh;
+        it.k0 = kt * 128;
+        it.i0 = it.k0 / 64;                  // first 64-query tile with a query >= k0
+        it.nq = (a.s + 63) / 64 - it.i0;     // query tiles to visit
+        return it;
+    };
 
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
+        mbar_init(kv_empty, 1);
         for (int i = 0; i < S; ++i) {
             mbar_init(&q_full[i], 1);
             mbar_init(&q_empty[i], 1);
@@ -979,8 +997,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(&st_full[b], 1);
             mbar_init(&pds_full[b], 4);
+            mbar_init(&item_full[b], 1);
+            mbar_init(&item_empty[b], 5);  // the MMA thread and the 4 softmax warps
         }
         mbar_init(grad_done, 1);
+        mbar_init(grad_free, 4);
         mbar_init(drain, 1);
         misc[1] = 0u;
         fence_mbar_init();
@@ -1015,35 +1036,63 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             prefetch_tmap(&tm_k128);
             prefetch_tmap(&tm_q64);
             prefetch_tmap(&tm_do64);
-            const int qcol = head * D, kcol = a.h + head * D, vcol = 2 * a.h + head * D;
-            mbar_arrive_expect_tx(kv_full, 2 * C::KEY_TILE);
-            for (int b = 0; b < C::NB; ++b) {
-                tma_load_3d(&tm_k128, smem_u32(kv_full), smem_u32(sK) + b * 128 * kRowBytes,
-                            kcol + 64 * b, k0, n);
-                tma_load_3d(&tm_k128, smem_u32(kv_full), smem_u32(sV) + b * 128 * kRowBytes,
-                            vcol + 64 * b, k0, n);
-            }
             int stage = 0;
             uint32_t phase = 0, issued = 0, issued_phase = 0;
-            for (int i = 0; i < nq; ++i) {
-                if (!wait_bounded(&q_empty[stage], phase ^ 1u, abort_flag, a.status, 0x301)) break;
-                mbar_arrive_expect_tx(&q_full[stage], 2 * C::Q_TILE);
-                const uint32_t dst = smem_u32(ring) + stage * 2 * C::Q_TILE;
-                const int qrow = (i0 + i) * 64;
+            int kv_loads = 0;  // K/V loads issued (kv_full's completed phases)
+            bool ok = true;
+            for (int k = 0;; ++k) {
+                const int slot = k & 1;
+                // the slot's item k - 2 has been read by every consumer
+                if (k >= 2 && !wait_bounded(&item_empty[slot], static_cast<uint32_t>((k - 2) >> 1) & 1u,
+                                            abort_flag, a.status, 0x30B))
+                    ok = false;
+                int item = -1;
+                if (ok) {
+                    item = static_cast<int>(atomicAdd(&g_dkdv_work[0], 1u));
+                    if (item >= total) item = -1;
+                }
+                items[slot] = item;
+                mbar_arrive(&item_full[slot]);
+                if (item < 0) break;
+                const Item it = decode(item);
+                const int qcol = it.head * D, kcol = a.h + it.head * D, vcol = 2 * a.h + it.head * D;
+                // K and V: the previous item's S^T and dP^T MMAs are done with them
+                if (k >= 1 && !wait_bounded(kv_empty, static_cast<uint32_t>(k - 1) & 1u, abort_flag,
+                                            a.status, 0x30C))
+                    break;
+                mbar_arrive_expect_tx(kv_full, 2 * C::KEY_TILE);
                 for (int b = 0; b < C::NB; ++b) {
-                    tma_load_3d(&tm_q64, smem_u32(&q_full[stage]), dst + b * 64 * kRowBytes,
-                                qcol + 64 * b, qrow, n);
-                    tma_load_3d(&tm_do64, smem_u32(&q_full[stage]),
-                                dst + C::Q_TILE + b * 64 * kRowBytes, qcol + 64 * b, qrow, n);
+                    tma_load_3d(&tm_k128, smem_u32(kv_full), smem_u32(sK) + b * 128 * kRowBytes,
+                                kcol + 64 * b, it.k0, it.n);
+                    tma_load_3d(&tm_k128, smem_u32(kv_full), smem_u32(sV) + b * 128 * kRowBytes,
+                                vcol + 64 * b, it.k0, it.n);
                 }
-                issued |= 1u << stage;
-                issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-                if (++stage == S) {
-                    stage = 0;
-                    phase ^= 1u;
+                ++kv_loads;
+                for (int i = 0; i < it.nq && ok; ++i) {
+                    if (!wait_bounded(&q_empty[stage], phase ^ 1u, abort_flag, a.status, 0x301)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&q_full[stage], 2 * C::Q_TILE);
+                    const uint32_t dst = smem_u32(ring) + stage * 2 * C::Q_TILE;
+                    const int qrow = (it.i0 + i) * 64;
+                    for (int b = 0; b < C::NB; ++b) {
+                        tma_load_3d(&tm_q64, smem_u32(&q_full[stage]), dst + b * 64 * kRowBytes,
+                                    qcol + 64 * b, qrow, it.n);
+                        tma_load_3d(&tm_do64, smem_u32(&q_full[stage]),
+                                    dst + C::Q_TILE + b * 64 * kRowBytes, qcol + 64 * b, qrow, it.n);
+                    }
+                    issued |= 1u << stage;
+                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
+                if (!ok) break;
             }
-            wait_drain(kv_full, 0, a.status, 0x302);
+            // every copy this thread started lands before the CTA may exit
+            if (kv_loads > 0) wait_drain(kv_full, static_cast<uint32_t>(kv_loads - 1) & 1u, a.status, 0x302);
             for (int i = 0; i < S; ++i)
                 if (issued & (1u << i)) wait_drain(&q_full[i], (issued_phase >> i) & 1u, a.status, 0x303);
         }
@@ -1053,14 +1102,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             constexpr uint32_t id_st = idesc_bf16_f32(128, 64, false, false);
             const uint64_t kdesc = smem_desc_sw128(smem_u32(sK), 16, 1024);
             const uint64_t vdesc = smem_desc_sw128(smem_u32(sV), 16, 1024);
-            int stage = 0, prev_stage = 0;
+            int stage = 0, g = 0;  // g: query tiles of every item so far
             uint32_t phase = 0;
-            bool ok = wait_bounded(kv_full, 0, abort_flag, a.status, 0x304);
-            tc_fence_after();
-            auto issue_grads = [&](int i, int st) {
+            bool ok = true;
+            // dV / dK of tile i of item k (global tile gi), Q/dO in ring stage st
+            auto issue_grads = [&](int i, int gi, int st, int k) {
                 if (!ok) return;
-                if (!wait_bounded(&pds_full[NBUF == 2 ? (i & 1) : 0],
-                                  static_cast<uint32_t>(NBUF == 2 ? (i >> 1) : i) & 1u, abort_flag,
+                // the first dV / dK MMAs of an item overwrite the previous item's
+                if (i == 0 && k >= 1 &&
+                    !wait_bounded(grad_free, static_cast<uint32_t>(k - 1) & 1u, abort_flag, a.status, 0x30D)) {
+                    ok = false;
+                    return;
+                }
+                if (!wait_bounded(&pds_full[NBUF == 2 ? (gi & 1) : 0],
+                                  static_cast<uint32_t>(NBUF == 2 ? (gi >> 1) : gi) & 1u, abort_flag,
                                   a.status, 0x305)) {
                     ok = false;
                     return;
@@ -1073,14 +1128,29 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 // along the rows, queries down the 64-row box)
                 const uint64_t dodesc = smem_desc_sw128(qd + C::Q_TILE, 64 * kRowBytes, 1024);
                 const uint64_t qdesc = smem_desc_sw128(qd, 64 * kRowBytes, 1024);
-                const uint32_t b = NBUF == 2 ? static_cast<uint32_t>(i & 1) : 0u;
+                const uint32_t b = NBUF == 2 ? static_cast<uint32_t>(gi & 1) : 0u;
                 mma_ts_n_is_d<D, 64 / 16>(tmem + kDV, tmem + kST + 64 * b, dodesc, 64 * kRowBytes, i > 0,
                                           tmem + kDVt);
                 mma_ts_n_is_d<D, 64 / 16>(tmem + kDK, tmem + kDPT + 64 * b, qdesc, 64 * kRowBytes, i > 0,
                                           tmem + kDKt);
                 tc_commit(&q_empty[st]);
             };
-            for (int i = 0; i < nq && ok; ++i) {
+            for (int k = 0; ok; ++k) {
+                const int slot = k & 1;
+                if (!wait_bounded(&item_full[slot], static_cast<uint32_t>(k >> 1) & 1u, abort_flag,
+                                  a.status, 0x30E))
+                    break;
+                const int item = *reinterpret_cast<volatile int*>(&items[slot]);
+                mbar_arrive(&item_empty[slot]);
+                if (item < 0) break;
+                const Item it = decode(item);
+                if (!wait_bounded(kv_full, static_cast<uint32_t>(k) & 1u, abort_flag, a.status, 0x304)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                int prev_stage = 0;
+            for (int i = 0; i < it.nq && ok; ++i, ++g) {
                 if (!wait_bounded(&q_full[stage], phase, abort_flag, a.status, 0x306)) {
                     ok = false;
                     break;
@@ -1089,7 +1159,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const uint32_t qd = smem_u32(ring) + stage * 2 * C::Q_TILE;
                 const uint64_t qdesc = smem_desc_sw128(qd, 16, 1024);
                 const uint64_t dodesc = smem_desc_sw128(qd + C::Q_TILE, 16, 1024);
-                const uint32_t b = NBUF == 2 ? static_cast<uint32_t>(i & 1) : 0u;
+                const uint32_t b = NBUF == 2 ? static_cast<uint32_t>(g & 1) : 0u;
                 // S^T = K Q^T and dP^T = V dO^T (M = 128 keys, N = 64 queries, K = d)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
@@ -1099,12 +1169,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                desc_add(dodesc, kmajor_step<64>(kk)), id_st, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(&st_full[b]);
+                // the item's last S^T and dP^T have been issued: once they are
+                // done, K and V may be replaced by the next item's
+                if (i == it.nq - 1) tc_commit(kv_empty);
                 if constexpr (NBUF == 2) {
                     // the previous tile's dV / dK run while this tile is softmaxed
-                    if (i >= 1) issue_grads(i - 1, prev_stage);
+                    if (i >= 1) issue_grads(i - 1, g - 1, prev_stage, k);
                 } else {
                     // one buffer: this tile's dV / dK before the next S^T
-                    issue_grads(i, stage);
+                    issue_grads(i, g, stage, k);
                 }
                 prev_stage = stage;
                 if (++stage == S) {
@@ -1112,16 +1185,30 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     phase ^= 1u;
                 }
             }
-            if constexpr (NBUF == 2) issue_grads(nq - 1, prev_stage);
-            tc_commit(grad_done);
+                if constexpr (NBUF == 2) issue_grads(it.nq - 1, g - 1, prev_stage, k);
+                if (ok) tc_commit(grad_done);
+            }
             tc_commit(drain);
             wait_drain(drain, 0, a.status, 0x307);
         }
         __syncwarp();
     } else {
         const int r = threadIdx.x;
-        const int key = k0 + r;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        bool ok = true;
+        int g = 0;
+        for (int k = 0; ok; ++k) {
+        const int slot = k & 1;
+        if (!warp_wait_bounded(&item_full[slot], static_cast<uint32_t>(k >> 1) & 1u, abort_flag,
+                               a.status, 0x30F))
+            break;
+        const int item = *reinterpret_cast<volatile int*>(&items[slot]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&item_empty[slot]);
+        if (item < 0) break;
+        const Item it = decode(item);
+        const int i0 = it.i0, nq = it.nq, n = it.n, head = it.head;
+        const int key = it.k0 + r;
         const float* lse_seq = a.lse_in + head * a.T + static_cast<long long>(n) * a.s;
         const float* dlt_seq = a.delta + head * a.T + static_cast<long long>(n) * a.s;
         // lse and delta of a 64-query tile: lane l holds queries l and 32 + l
@@ -1139,14 +1226,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         };
         float lse_c[2], dlt_c[2];
         fetch(0, lse_c, dlt_c);
-        bool ok = true;
-        for (int i = 0; i < nq; ++i) {
-            const uint32_t b = NBUF == 2 ? static_cast<uint32_t>(i & 1) : 0u;
+        for (int i = 0; i < nq; ++i, ++g) {
+            const uint32_t b = NBUF == 2 ? static_cast<uint32_t>(g & 1) : 0u;
             float lse_n[2], dlt_n[2];
             fetch(i + 1, lse_n, dlt_n);
-            // S^T(i) was issued after the dV / dK that last read this buffer's
+            // S^T(g) was issued after the dV / dK that last read this buffer's
             // P^T / dS^T, so once it is here the buffer is free
-            if (!warp_wait_bounded(&st_full[b], static_cast<uint32_t>(NBUF == 2 ? (i >> 1) : i) & 1u,
+            if (!warp_wait_bounded(&st_full[b], static_cast<uint32_t>(NBUF == 2 ? (g >> 1) : g) & 1u,
                                    abort_flag, a.status, 0x308)) {
                 ok = false;
                 break;
@@ -1194,7 +1280,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&pds_full[b]);
         }
-        if (ok && warp_wait_bounded(grad_done, 0, abort_flag, a.status, 0x30A)) {
+        if (!ok || !warp_wait_bounded(grad_done, static_cast<uint32_t>(k) & 1u, abort_flag, a.status,
+                                      0x30A)) {
+            ok = false;
+            break;
+        }
+        {
             tc_fence_after();
             // tcgen05.ld is warp-collective (.sync.aligned): every lane loads,
             // only keys inside the sequence are stored
@@ -1226,6 +1317,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
             }
         }
+        // dV and dK are in registers or on their way to memory: the MMA may reuse them
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(grad_free);
+        }
     }
 
     tc_fence_before();
@@ -1233,6 +1329,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (warp == 5) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
+    }
+    // the last CTA out resets the work counters for the next launch
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(&g_dkdv_work[1], 1u) == gridDim.x - 1) {
+            g_dkdv_work[0] = 0u;
+            g_dkdv_work[1] = 0u;
+            __threadfence();
+        }
     }
 }
 
@@ -1309,7 +1414,8 @@ cudaError_t launch_attn_backward(const CUtensorMap& tm_qkv128, const CUtensorMap
     AttnArgs aq = a;
     aq.q_tiles = q_tiles;
     const unsigned grid = static_cast<unsigned>(q_tiles * p.nb * p.nh);
-    // the dQ kernel is persistent: one CTA per SM at most, items taken in turn
+    // the dQ and dK/dV kernels are persistent: one CTA per SM at most, items
+    // taken in turn (both have q_tiles x nb x nh items)
     static int sms = 0;
     if (sms == 0) {
         int dev = 0;
@@ -1331,7 +1437,7 @@ cudaError_t launch_attn_backward(const CUtensorMap& tm_qkv128, const CUtensorMap
             auto kk = attn_bwd_dkdv_kernel<DD>;                                                     \
             e = cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize, DkvCfg<DD>::SMEM); \
             if (e == cudaSuccess) {                                                                 \
-                kk<<<grid, kAttnThreads, DkvCfg<DD>::SMEM, st>>>(tm_qkv128, tm_qkv64, tm_do64, a);  \
+                kk<<<dq_grid, kAttnThreads, DkvCfg<DD>::SMEM, st>>>(tm_qkv128, tm_qkv64, tm_do64, a); \
                 e = cudaGetLastError();                                                             \
             }                                                                                       \
             if (e == cudaSuccess) ++*launches;                                                      \
