@@ -207,6 +207,11 @@ struct FwdCfg {
     }
 };
 
+// Work items of the forward kernel: (pair of 128-query tiles, sequence,
+// head), heaviest (most key tiles) first; taken and the counters reset as
+// for the backward kernels.
+__device__ unsigned int g_fwd_work[2];
+
 template <int D>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q128,  // QKV, 128-row boxes (Q)
@@ -220,32 +225,48 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     uint8_t* sQ = smem;                   // Q_A, Q_B
-    uint8_t* ring = smem + 2 * C::QTILE;  // K_0, V_0, K_1, V_1, ...
+    uint8_t* ring = smem + 2 * C::QTILE;  // K_0, V_0, K_1, V_1, ... of every item in turn
     uint64_t* bars = reinterpret_cast<uint64_t*>(ring + S * C::KVTILE);
-    uint64_t* q_full = bars;
-    uint64_t* kv_full = bars + 1;
+    uint64_t* q_full = bars;              // the item's Q tiles have landed
+    uint64_t* q_empty = bars + 1;         // the item's last S MMAs have read them
+    uint64_t* kv_full = bars + 2;
     uint64_t* kv_empty = kv_full + S;
-    uint64_t* s_full = kv_empty + S;  // [tile]
-    uint64_t* p_full = s_full + 2;    // [tile]
-    uint64_t* pv_done = p_full + 2;   // [tile]
-    uint64_t* drain = pv_done + 2;
-    uint32_t* misc = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* s_full = kv_empty + S;      // [tile]
+    uint64_t* p_full = s_full + 2;        // [tile]
+    uint64_t* pv_done = p_full + 2;       // [tile]
+    uint64_t* o_free = pv_done + 2;       // [tile] the softmax warps have read O_x out
+    uint64_t* item_full = o_free + 2;     // [2]
+    uint64_t* item_empty = item_full + 2; // [2]
+    uint64_t* drain = item_empty + 2;
+    int* items = reinterpret_cast<int*>(drain + 1);  // [2]
+    uint32_t* misc = reinterpret_cast<uint32_t*>(items + 2);
     volatile uint32_t* abort_flag = misc + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // heaviest pairs (most key tiles) first
     const int per = a.nb * a.nh;
-    const int pair = a.q_tiles - 1 - static_cast<int>(blockIdx.x) / per;
-    const int rem = static_cast<int>(blockIdx.x) % per;
-    const int n = rem / a.nh, head = rem % a.nh;
-    const int q0 = pair * 256;
-    const bool has_b = q0 + 128 < a.s;
-    // last key tile each query tile sees (its keys reach the tile's last query)
-    const int last[2] = {(q0 + 127) / BKV, (q0 + 255) / BKV};
-    const int n_kv = has_b ? last[1] + 1 : last[0] + 1;
+    const int total = a.q_tiles * per;
+    struct Item {
+        int q0, n, head, n_kv;
+        bool has_b;
+        int last[2];  // last key tile each query tile sees
+    };
+    auto decode = [&](int item) {
+        Item it;
+        const int g = item / per;
+        const int rem = item - g * per;
+        it.n = rem / a.nh;
+        it.head = rem - it.n * a.nh;
+        it.q0 = (a.q_tiles - 1 - g) * 256;
+        it.has_b = it.q0 + 128 < a.s;
+        it.last[0] = (it.q0 + 127) / BKV;
+        it.last[1] = (it.q0 + 255) / BKV;
+        it.n_kv = it.has_b ? it.last[1] + 1 : it.last[0] + 1;
+        return it;
+    };
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
         for (int i = 0; i < S; ++i) {
             mbar_init(&kv_full[i], 1);
             mbar_init(&kv_empty[i], 1);
@@ -254,6 +275,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             mbar_init(&s_full[x], 1);
             mbar_init(&p_full[x], 4);  // one arrival per warp of the tile's warpgroup
             mbar_init(&pv_done[x], 1);
+            mbar_init(&o_free[x], 4);
+            mbar_init(&item_full[x], 1);
+            mbar_init(&item_empty[x], 9);  // the MMA thread and the 8 softmax warps
         }
         mbar_init(drain, 1);
         misc[1] = 0u;
@@ -273,28 +297,57 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (lane == 0) {
             prefetch_tmap(&tm_q128);
             prefetch_tmap(&tm_kv);
-            const int qcol = head * D, kcol = a.h + head * D, vcol = 2 * a.h + head * D;
-            mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * C::QTILE);
-            for (int x = 0; x < (has_b ? 2 : 1); ++x)
-                for (int b = 0; b < C::NB; ++b)
-                    tma_load_3d(&tm_q128, smem_u32(q_full),
-                                smem_u32(sQ) + x * C::QTILE + b * 128 * kRowBytes, qcol + 64 * b,
-                                q0 + 128 * x, n);
-            uint32_t issued = 0, issued_phase = 0;
-            for (int idx = 0; idx < 2 * n_kv; ++idx) {  // K_j = 2j, V_j = 2j + 1
-                const int stage = idx % S;
-                const uint32_t phase = static_cast<uint32_t>(idx / S) & 1u;
-                if (!wait_bounded(&kv_empty[stage], phase ^ 1u, abort_flag, a.status, 0x101)) break;
-                mbar_arrive_expect_tx(&kv_full[stage], C::KVTILE);
-                const uint32_t dst = smem_u32(ring) + stage * C::KVTILE;
-                const int col = (idx & 1) ? vcol : kcol;
-                for (int b = 0; b < C::NB; ++b)
-                    tma_load_3d(&tm_kv, smem_u32(&kv_full[stage]), dst + b * BKV * kRowBytes,
-                                col + 64 * b, (idx >> 1) * BKV, n);
-                issued |= 1u << stage;
-                issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, issued_phase = 0;
+            int q_loads = 0;
+            bool ok = true;
+            for (int k = 0;; ++k) {
+                const int slot = k & 1;
+                if (k >= 2 && !wait_bounded(&item_empty[slot], static_cast<uint32_t>((k - 2) >> 1) & 1u,
+                                            abort_flag, a.status, 0x111))
+                    ok = false;
+                int item = -1;
+                if (ok) {
+                    item = static_cast<int>(atomicAdd(&g_fwd_work[0], 1u));
+                    if (item >= total) item = -1;
+                }
+                items[slot] = item;
+                mbar_arrive(&item_full[slot]);
+                if (item < 0) break;
+                const Item it = decode(item);
+                const int qcol = it.head * D, kcol = a.h + it.head * D, vcol = 2 * a.h + it.head * D;
+                // the previous item's S MMAs are done with the Q tiles
+                if (k >= 1 && !wait_bounded(q_empty, static_cast<uint32_t>(k - 1) & 1u, abort_flag,
+                                            a.status, 0x112))
+                    break;
+                mbar_arrive_expect_tx(q_full, (it.has_b ? 2 : 1) * C::QTILE);
+                for (int x = 0; x < (it.has_b ? 2 : 1); ++x)
+                    for (int b = 0; b < C::NB; ++b)
+                        tma_load_3d(&tm_q128, smem_u32(q_full),
+                                    smem_u32(sQ) + x * C::QTILE + b * 128 * kRowBytes, qcol + 64 * b,
+                                    it.q0 + 128 * x, it.n);
+                ++q_loads;
+                for (int idx = 0; idx < 2 * it.n_kv; ++idx) {  // K_j = 2j, V_j = 2j + 1
+                    if (!wait_bounded(&kv_empty[stage], phase ^ 1u, abort_flag, a.status, 0x101)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&kv_full[stage], C::KVTILE);
+                    const uint32_t dst = smem_u32(ring) + stage * C::KVTILE;
+                    const int col = (idx & 1) ? vcol : kcol;
+                    for (int b = 0; b < C::NB; ++b)
+                        tma_load_3d(&tm_kv, smem_u32(&kv_full[stage]), dst + b * BKV * kRowBytes,
+                                    col + 64 * b, (idx >> 1) * BKV, it.n);
+                    issued |= 1u << stage;
+                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
             }
-            wait_drain(q_full, 0, a.status, 0x102);
+            if (q_loads > 0) wait_drain(q_full, static_cast<uint32_t>(q_loads - 1) & 1u, a.status, 0x102);
             for (int i = 0; i < S; ++i)
                 if (issued & (1u << i)) wait_drain(&kv_full[i], (issued_phase >> i) & 1u, a.status, 0x103);
         }
@@ -303,17 +356,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // ------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t id_s = idesc_bf16_f32(128, BKV, false, false);
-            bool ok = wait_bounded(q_full, 0, abort_flag, a.status, 0x104);
-            tc_fence_after();
-            // wait for ring entry idx (K_j = 2j, V_j = 2j + 1); returns its stage
-            auto acquire = [&](int idx, int site) -> int {
-                const int stage = idx % S;
-                if (ok && !wait_bounded(&kv_full[stage], static_cast<uint32_t>(idx / S) & 1u,
-                                        abort_flag, a.status, site))
-                    ok = false;
+            bool ok = true;
+            int rstage = 0;  // ring entries are taken in order, across items
+            uint32_t rphase = 0;
+            int gx[2] = {0, 0};  // S / P V MMAs of each tile over the items so far
+            int cx[2] = {0, 0};  // items each tile has taken part in
+            // wait for the next ring entry; returns its stage
+            auto acquire = [&](int site) -> int {
+                const int stage = rstage;
+                if (ok && !wait_bounded(&kv_full[stage], rphase, abort_flag, a.status, site)) ok = false;
                 tc_fence_after();
+                if (++rstage == S) {
+                    rstage = 0;
+                    rphase ^= 1u;
+                }
                 return stage;
             };
+            int s_left = 0;  // S MMAs of the item still to issue
             auto issue_s = [&](int x, int stage) {  // S_x = Q_x K^T
                 const uint64_t qdesc = smem_desc_sw128(smem_u32(sQ) + x * C::QTILE, 16, 1024);
                 const uint64_t kdesc = smem_desc_sw128(smem_u32(ring) + stage * C::KVTILE, 16, 1024);
@@ -322,9 +381,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     tc_mma_f16(tmem + C::s_col(x), desc_add(qdesc, kmajor_step<128>(kk)),
                                desc_add(kdesc, kmajor_step<BKV>(kk)), id_s, kk > 0 ? 1u : 0u);
                 tc_commit(&s_full[x]);
+                // the item's last S: once done, the Q tiles may be replaced
+                if (--s_left == 0) tc_commit(q_empty);
             };
             auto issue_pv = [&](int x, int j, int stage) {  // O_x (+)= P_x V
-                if (ok && !wait_bounded(&p_full[x], static_cast<uint32_t>(j) & 1u, abort_flag,
+                // the first P V of an item overwrites the previous item's O_x
+                if (ok && j == 0 && cx[x] >= 1 &&
+                    !wait_bounded(&o_free[x], static_cast<uint32_t>(cx[x] - 1) & 1u, abort_flag, a.status,
+                                  0x113 + x))
+                    ok = false;
+                if (ok && !wait_bounded(&p_full[x], static_cast<uint32_t>(gx[x] + j) & 1u, abort_flag,
                                         a.status, 0x105 + x))
                     ok = false;
                 if (!ok) return;
@@ -337,35 +403,57 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                                            BKV * kRowBytes, j > 0, tmem + C::o_tail(x));
                 tc_commit(&pv_done[x]);
             };
-            // S of both tiles for key tile 0
-            int ks = acquire(0, 0x107);
-            if (ok) {
-                issue_s(0, ks);
-                if (has_b) issue_s(1, ks);
-                tc_commit(&kv_empty[ks]);
-            }
-            for (int j = 0; j < n_kv && ok; ++j) {
-                const int vs = acquire(2 * j + 1, 0x108);
-                const bool more = j + 1 < n_kv;
-                int kn = -1;
-                if (j <= last[0]) {
-                    issue_pv(0, j, vs);
-                    if (ok && j + 1 <= last[0]) {
-                        kn = acquire(2 * j + 2, 0x109);
-                        if (ok) issue_s(0, kn);
-                    }
+            for (int k = 0; ok; ++k) {
+                const int slot = k & 1;
+                if (!wait_bounded(&item_full[slot], static_cast<uint32_t>(k >> 1) & 1u, abort_flag,
+                                  a.status, 0x115))
+                    break;
+                const int item = *reinterpret_cast<volatile int*>(&items[slot]);
+                mbar_arrive(&item_empty[slot]);
+                if (item < 0) break;
+                const Item it = decode(item);
+                if (!wait_bounded(q_full, static_cast<uint32_t>(k) & 1u, abort_flag, a.status, 0x104)) {
+                    ok = false;
+                    break;
                 }
-                if (has_b && ok) {
-                    issue_pv(1, j, vs);
-                    if (ok) tc_commit(&kv_empty[vs]);
-                    if (ok && more) {
-                        if (kn < 0) kn = acquire(2 * j + 2, 0x10A);
-                        if (ok) issue_s(1, kn);
-                    }
-                } else if (ok) {
-                    tc_commit(&kv_empty[vs]);
+                tc_fence_after();
+                s_left = it.last[0] + 1 + (it.has_b ? it.last[1] + 1 : 0);
+                // S of both tiles for key tile 0
+                int ks = acquire(0x107);
+                if (ok) {
+                    issue_s(0, ks);
+                    if (it.has_b) issue_s(1, ks);
+                    tc_commit(&kv_empty[ks]);
                 }
-                if (ok && kn >= 0) tc_commit(&kv_empty[kn]);
+                for (int j = 0; j < it.n_kv && ok; ++j) {
+                    const int vs = acquire(0x108);
+                    const bool more = j + 1 < it.n_kv;
+                    int kn = -1;
+                    if (j <= it.last[0]) {
+                        issue_pv(0, j, vs);
+                        if (ok && j + 1 <= it.last[0]) {
+                            kn = acquire(0x109);
+                            if (ok) issue_s(0, kn);
+                        }
+                    }
+                    if (it.has_b && ok) {
+                        issue_pv(1, j, vs);
+                        if (ok) tc_commit(&kv_empty[vs]);
+                        if (ok && more) {
+                            if (kn < 0) kn = acquire(0x10A);
+                            if (ok) issue_s(1, kn);
+                        }
+                    } else if (ok) {
+                        tc_commit(&kv_empty[vs]);
+                    }
+                    if (ok && kn >= 0) tc_commit(&kv_empty[kn]);
+                }
+                gx[0] += it.last[0] + 1;
+                cx[0] += 1;
+                if (it.has_b) {
+                    gx[1] += it.last[1] + 1;
+                    cx[1] += 1;
+                }
             }
             tc_commit(drain);
             wait_drain(drain, 0, a.status, 0x10B);
@@ -375,15 +463,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // -------------------------------------------------- softmax warps
         const int x = warp >> 2;               // tile: 0 = A, 1 = B
         const int r = threadIdx.x & 127;       // row of the tile = TMEM lane
-        const int q = q0 + 128 * x + r;
-        if (x == 0 || has_b) {
-            const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-            const uint32_t s_addr = lane_addr + C::s_col(x);
-            const int jl = last[x];
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        const uint32_t s_addr = lane_addr + C::s_col(x);
+        int gxl = 0;  // this tile's S / P V MMAs over the items so far
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            const int slot = k & 1;
+            if (!warp_wait_bounded(&item_full[slot], static_cast<uint32_t>(k >> 1) & 1u, abort_flag,
+                                   a.status, 0x116))
+                break;
+            const int item = *reinterpret_cast<volatile int*>(&items[slot]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&item_empty[slot]);
+            if (item < 0) break;
+            const Item it = decode(item);
+            if (x == 1 && !it.has_b) continue;  // no B tile in this item
+            const int q = it.q0 + 128 * x + r;
+            const int jl = it.last[x];
             float m = -INFINITY, l = 0.0f;
-            bool ok = true;
             for (int j = 0; j <= jl; ++j) {
-                if (!warp_wait_bounded(&s_full[x], static_cast<uint32_t>(j) & 1u, abort_flag,
+                if (!warp_wait_bounded(&s_full[x], static_cast<uint32_t>(gxl + j) & 1u, abort_flag,
                                        a.status, 0x10C + x)) {
                     ok = false;
                     break;
@@ -406,7 +505,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 // work, so its reductions must not be one serial chain
                 float mx8[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
+                for (int kk = 0; kk < 8; ++kk) mx8[kk] = -INFINITY;
 #pragma unroll
                 for (int c = 0; c < SCH; ++c)
 #pragma unroll
@@ -423,7 +522,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 if (move) m = m_new;
                 float rs8[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) rs8[k] = 0.0f;
+                for (int kk = 0; kk < 8; ++kk) rs8[kk] = 0.0f;
                 uint32_t pk[SCH][16];
 #pragma unroll
                 for (int c = 0; c < SCH; ++c)
@@ -462,32 +561,39 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[x]);
             }
-            if (ok && warp_wait_bounded(&pv_done[x], static_cast<uint32_t>(jl) & 1u, abort_flag,
-                                        a.status, 0x110 + x)) {
-                tc_fence_after();
-                const float inv = 1.0f / l;
-                const bool q_ok = q < a.s;
-                const long long tok = static_cast<long long>(n) * a.s + q;
-                uint4* dst = reinterpret_cast<uint4*>(a.O + tok * a.h + head * D);
+            if (!ok || !warp_wait_bounded(&pv_done[x], static_cast<uint32_t>(gxl + jl) & 1u, abort_flag,
+                                          a.status, 0x110 + x)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const float inv = 1.0f / l;
+            const bool q_ok = q < a.s;
+            const long long tok = static_cast<long long>(it.n) * a.s + q;
+            uint4* dst = reinterpret_cast<uint4*>(a.O + tok * a.h + it.head * D);
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(lane_addr + C::o_chunk(x, c), o);  // every lane: warp-collective
-                    tmem_wait_ld();
-                    if (q_ok) {
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(lane_addr + C::o_chunk(x, c), o);  // every lane: warp-collective
+                tmem_wait_ld();
+                if (q_ok) {
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            uint4 u;
-                            u.x = pack_bf16x2(__uint_as_float(o[8 * i]) * inv, __uint_as_float(o[8 * i + 1]) * inv);
-                            u.y = pack_bf16x2(__uint_as_float(o[8 * i + 2]) * inv, __uint_as_float(o[8 * i + 3]) * inv);
-                            u.z = pack_bf16x2(__uint_as_float(o[8 * i + 4]) * inv, __uint_as_float(o[8 * i + 5]) * inv);
-                            u.w = pack_bf16x2(__uint_as_float(o[8 * i + 6]) * inv, __uint_as_float(o[8 * i + 7]) * inv);
-                            dst[c * 4 + i] = u;
-                        }
+                    for (int i = 0; i < 4; ++i) {
+                        uint4 u;
+                        u.x = pack_bf16x2(__uint_as_float(o[8 * i]) * inv, __uint_as_float(o[8 * i + 1]) * inv);
+                        u.y = pack_bf16x2(__uint_as_float(o[8 * i + 2]) * inv, __uint_as_float(o[8 * i + 3]) * inv);
+                        u.z = pack_bf16x2(__uint_as_float(o[8 * i + 4]) * inv, __uint_as_float(o[8 * i + 5]) * inv);
+                        u.w = pack_bf16x2(__uint_as_float(o[8 * i + 6]) * inv, __uint_as_float(o[8 * i + 7]) * inv);
+                        dst[c * 4 + i] = u;
                     }
                 }
-                if (q_ok) a.lse[head * a.T + tok] = m + lg2(l);
             }
+            if (q_ok) a.lse[it.head * a.T + tok] = m + lg2(l);
+            // O_x is in registers or on its way to memory: the MMA may reuse it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&o_free[x]);
+            gxl += jl + 1;
         }
     }
 
@@ -496,6 +602,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
+    }
+    // the last CTA out resets the work counters for the next launch
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(&g_fwd_work[1], 1u) == gridDim.x - 1) {
+            g_fwd_work[0] = 0u;
+            g_fwd_work[1] = 0u;
+            __threadfence();
+        }
     }
 }
 
@@ -1345,6 +1460,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
 // ------------------------------------------------------------- launchers
 
+namespace {
+// CTAs of a persistent attention kernel: one per SM at most.
+unsigned persistent_grid(unsigned items) {
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = 1;
+    }
+    return items < static_cast<unsigned>(sms) ? items : static_cast<unsigned>(sms);
+}
+}  // namespace
+
 cudaError_t launch_attn_forward(const CUtensorMap& tm_qkv128, const CUtensorMap& tm_qkv64, int d,
                                 const AttnParams& p, cudaStream_t st, int* launches) {
     AttnArgs a{};
@@ -1356,7 +1485,8 @@ cudaError_t launch_attn_forward(const CUtensorMap& tm_qkv128, const CUtensorMap&
     a.O = p.O;
     a.lse = p.lse;
     a.status = p.status;
-    const unsigned grid = static_cast<unsigned>(a.q_tiles * p.nb * p.nh);
+    // persistent: items (query-tile pairs x sequences x heads) taken in turn
+    const unsigned grid = persistent_grid(static_cast<unsigned>(a.q_tiles * p.nb * p.nh));
     cudaError_t e = cudaSuccess;
 #define TPMLP_ATTN_FWD(DD)                                                                        \
     if (d == DD) {                                                                                \
@@ -1413,17 +1543,9 @@ cudaError_t launch_attn_backward(const CUtensorMap& tm_qkv128, const CUtensorMap
     const int q_tiles = (p.s + 127) / 128;
     AttnArgs aq = a;
     aq.q_tiles = q_tiles;
-    const unsigned grid = static_cast<unsigned>(q_tiles * p.nb * p.nh);
     // the dQ and dK/dV kernels are persistent: one CTA per SM at most, items
     // taken in turn (both have q_tiles x nb x nh items)
-    static int sms = 0;
-    if (sms == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (sms <= 0) sms = 1;
-    }
-    const unsigned dq_grid = grid < static_cast<unsigned>(sms) ? grid : static_cast<unsigned>(sms);
+    const unsigned dq_grid = persistent_grid(static_cast<unsigned>(q_tiles * p.nb * p.nh));
 #define TPMLP_ATTN_BWD(DD)                                                                          \
     if (d == DD) {                                                                                  \
         auto kq = attn_bwd_dq_kernel<DD>;                                                           \
