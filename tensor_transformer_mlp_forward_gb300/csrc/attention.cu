@@ -6,8 +6,9 @@
 // "Attention: split Q/K/V by head" (Figure 3b): the Q, K and V projections
 // are split by columns so that each rank owns a group of heads, and each
 // head's scores, softmax and value sum are computed where the head lives.
-// On one GPU every head of every shard is one CTA's work; the shard count
-// only decides which rank a head would belong to and changes nothing here.
+// On one GPU the heads of every shard are work items of the same kernels;
+// the shard count only decides which rank a head would belong to and
+// changes nothing here.
 //
 // Layout: QKV [T, 3h] bf16 (row = token n*s + pos; columns [Q | K | V], head
 // j at columns j*d .. j*d+d-1 of each part), O and dO [T, h], dQKV [T, 3h],
@@ -25,20 +26,22 @@
 //
 // Kernels (softmax warps own one query or key row per thread and TMEM lane; a
 // producer warp issues the TMA loads; one thread of the MMA warp allocates
-// TMEM and issues every MMA):
-//   attn_fwd_kernel     one CTA per pair of 128-query tiles of a (sequence,
-//                       head), two softmax warpgroups in ping-pong; S and the
-//                       output O of each tile in TMEM; P written back into
-//                       TMEM over S and used there as the A operand of P V.
+// TMEM and issues every MMA).  The three tensor-core kernels are persistent:
+// one CTA per SM takes work items in turn from an atomic counter, heaviest
+// first, so that one item's loads and read-out overlap its neighbours' MMAs.
+//   attn_fwd_kernel     items: pairs of 128-query tiles of a (sequence, head);
+//                       two softmax warpgroups in ping-pong; S and the output
+//                       O of each tile in TMEM; P written back into TMEM over
+//                       S and used there as the A operand of P V.
 //   attn_delta_kernel   delta = rowsum(dO * O) per (token, head).
-//   attn_bwd_dq_kernel  one CTA per (128 queries, head, sequence); 64-key
-//                       tiles: S and dP in TMEM (double-buffered), dS written
-//                       back over S and used there as the A operand of dS K,
-//                       dQ accumulated in TMEM.
-//   attn_bwd_dkdv_kernel one CTA per (128 keys, head, sequence); 64-query
-//                       tiles: S^T and dP^T in TMEM, P^T and dS^T written back
-//                       over them and used there as the A operands of P^T dO
-//                       and dS^T Q, dV and dK accumulated in TMEM.
+//   attn_bwd_dq_kernel  items: (128 queries, head, sequence); 64-key tiles:
+//                       S and dP in TMEM (double-buffered), dS written back
+//                       over S and used there as the A operand of dS K, dQ
+//                       accumulated in TMEM.
+//   attn_bwd_dkdv_kernel items: (128 keys, head, sequence); 64-query tiles:
+//                       S^T and dP^T in TMEM, P^T and dS^T written back over
+//                       them and used there as the A operands of P^T dO and
+//                       dS^T Q, dV and dK accumulated in TMEM.
 // Keeping P, dS, P^T and dS^T in tensor memory keeps shared-memory traffic
 // (K, V, Q, dO operands and the TMA writes) within what shared memory
 // delivers per clock.
