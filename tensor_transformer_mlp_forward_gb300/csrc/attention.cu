@@ -1268,41 +1268,41 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
                 tc_fence_after();
                 int prev_stage = 0;
-            for (int i = 0; i < it.nq && ok; ++i, ++g) {
-                if (!wait_bounded(&q_full[stage], phase, abort_flag, a.status, 0x306)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t qd = smem_u32(ring) + stage * 2 * C::Q_TILE;
-                const uint64_t qdesc = smem_desc_sw128(qd, 16, 1024);
-                const uint64_t dodesc = smem_desc_sw128(qd + C::Q_TILE, 16, 1024);
-                const uint32_t b = NBUF == 2 ? static_cast<uint32_t>(g & 1) : 0u;
-                // S^T = K Q^T and dP^T = V dO^T (M = 128 keys, N = 64 queries, K = d)
+                for (int i = 0; i < it.nq && ok; ++i, ++g) {
+                    if (!wait_bounded(&q_full[stage], phase, abort_flag, a.status, 0x306)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t qd = smem_u32(ring) + stage * 2 * C::Q_TILE;
+                    const uint64_t qdesc = smem_desc_sw128(qd, 16, 1024);
+                    const uint64_t dodesc = smem_desc_sw128(qd + C::Q_TILE, 16, 1024);
+                    const uint32_t b = NBUF == 2 ? static_cast<uint32_t>(g & 1) : 0u;
+                    // S^T = K Q^T and dP^T = V dO^T (M = 128 keys, N = 64 queries, K = d)
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    tc_mma_f16(tmem + kST + 64 * b, desc_add(kdesc, kmajor_step<128>(kk)),
-                               desc_add(qdesc, kmajor_step<64>(kk)), id_st, kk > 0 ? 1u : 0u);
-                    tc_mma_f16(tmem + kDPT + 64 * b, desc_add(vdesc, kmajor_step<128>(kk)),
-                               desc_add(dodesc, kmajor_step<64>(kk)), id_st, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        tc_mma_f16(tmem + kST + 64 * b, desc_add(kdesc, kmajor_step<128>(kk)),
+                                   desc_add(qdesc, kmajor_step<64>(kk)), id_st, kk > 0 ? 1u : 0u);
+                        tc_mma_f16(tmem + kDPT + 64 * b, desc_add(vdesc, kmajor_step<128>(kk)),
+                                   desc_add(dodesc, kmajor_step<64>(kk)), id_st, kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(&st_full[b]);
+                    // the item's last S^T and dP^T have been issued: once they are
+                    // done, K and V may be replaced by the next item's
+                    if (i == it.nq - 1) tc_commit(kv_empty);
+                    if constexpr (NBUF == 2) {
+                        // the previous tile's dV / dK run while this tile is softmaxed
+                        if (i >= 1) issue_grads(i - 1, g - 1, prev_stage, k);
+                    } else {
+                        // one buffer: this tile's dV / dK before the next S^T
+                        issue_grads(i, g, stage, k);
+                    }
+                    prev_stage = stage;
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
-                tc_commit(&st_full[b]);
-                // the item's last S^T and dP^T have been issued: once they are
-                // done, K and V may be replaced by the next item's
-                if (i == it.nq - 1) tc_commit(kv_empty);
-                if constexpr (NBUF == 2) {
-                    // the previous tile's dV / dK run while this tile is softmaxed
-                    if (i >= 1) issue_grads(i - 1, g - 1, prev_stage, k);
-                } else {
-                    // one buffer: this tile's dV / dK before the next S^T
-                    issue_grads(i, g, stage, k);
-                }
-                prev_stage = stage;
-                if (++stage == S) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-            }
                 if constexpr (NBUF == 2) issue_grads(it.nq - 1, g - 1, prev_stage, k);
                 if (ok) tc_commit(grad_done);
             }
@@ -1316,129 +1316,129 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         bool ok = true;
         int g = 0;
         for (int k = 0; ok; ++k) {
-        const int slot = k & 1;
-        if (!warp_wait_bounded(&item_full[slot], static_cast<uint32_t>(k >> 1) & 1u, abort_flag,
-                               a.status, 0x30F))
-            break;
-        const int item = *reinterpret_cast<volatile int*>(&items[slot]);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&item_empty[slot]);
-        if (item < 0) break;
-        const Item it = decode(item);
-        const int i0 = it.i0, nq = it.nq, n = it.n, head = it.head;
-        const int key = it.k0 + r;
-        const float* lse_seq = a.lse_in + head * a.T + static_cast<long long>(n) * a.s;
-        const float* dlt_seq = a.delta + head * a.T + static_cast<long long>(n) * a.s;
-        // lse and delta of a 64-query tile: lane l holds queries l and 32 + l
-        // (lse +inf and delta 0 past the sequence, so P = 0 there); the
-        // next tile's are loaded while this one is computed, and each chunk
-        // reads them by warp shuffle
-        auto fetch = [&](int i, float (&lv)[2], float (&dv)[2]) {
+            const int slot = k & 1;
+            if (!warp_wait_bounded(&item_full[slot], static_cast<uint32_t>(k >> 1) & 1u, abort_flag,
+                                   a.status, 0x30F))
+                break;
+            const int item = *reinterpret_cast<volatile int*>(&items[slot]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&item_empty[slot]);
+            if (item < 0) break;
+            const Item it = decode(item);
+            const int i0 = it.i0, nq = it.nq, n = it.n, head = it.head;
+            const int key = it.k0 + r;
+            const float* lse_seq = a.lse_in + head * a.T + static_cast<long long>(n) * a.s;
+            const float* dlt_seq = a.delta + head * a.T + static_cast<long long>(n) * a.s;
+            // lse and delta of a 64-query tile: lane l holds queries l and 32 + l
+            // (lse +inf and delta 0 past the sequence, so P = 0 there); the
+            // next tile's are loaded while this one is computed, and each chunk
+            // reads them by warp shuffle
+            auto fetch = [&](int i, float (&lv)[2], float (&dv)[2]) {
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                const int qq = (i0 + i) * 64 + 32 * h2 + lane;
-                const bool in = i < nq && qq < a.s;
-                lv[h2] = in ? __ldg(lse_seq + qq) : INFINITY;
-                dv[h2] = in ? __ldg(dlt_seq + qq) : 0.0f;
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int qq = (i0 + i) * 64 + 32 * h2 + lane;
+                    const bool in = i < nq && qq < a.s;
+                    lv[h2] = in ? __ldg(lse_seq + qq) : INFINITY;
+                    dv[h2] = in ? __ldg(dlt_seq + qq) : 0.0f;
+                }
+            };
+            float lse_c[2], dlt_c[2];
+            fetch(0, lse_c, dlt_c);
+            for (int i = 0; i < nq; ++i, ++g) {
+                const uint32_t b = NBUF == 2 ? static_cast<uint32_t>(g & 1) : 0u;
+                float lse_n[2], dlt_n[2];
+                fetch(i + 1, lse_n, dlt_n);
+                // S^T(g) was issued after the dV / dK that last read this buffer's
+                // P^T / dS^T, so once it is here the buffer is free
+                if (!warp_wait_bounded(&st_full[b], static_cast<uint32_t>(NBUF == 2 ? (g >> 1) : g) & 1u,
+                                       abort_flag, a.status, 0x308)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int qa = (i0 + i) * 64 + c * 32;  // first query of this chunk
+                    uint32_t sv[32], pv[32];
+                    tmem_ld32(lane_addr + kST + 64 * b + c * 32, sv);
+                    tmem_ld32(lane_addr + kDPT + 64 * b + c * 32, pv);
+                    tmem_wait_ld();
+                    // causal mask: queries before this row's key
+                    if (qa < key) {
+#pragma unroll
+                        for (int v = 0; v < 32; ++v)
+                            if (qa + v < key) sv[v] = __float_as_uint(-INFINITY);
+                    }
+                    uint32_t pp[16], dd[16];
+#pragma unroll
+                    for (int v = 0; v < 16; ++v) {
+                        float p2[2], d2[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int u = 2 * v + e;
+                            const float lq = __shfl_sync(0xFFFFFFFFu, lse_c[c], u);
+                            const float dq = __shfl_sync(0xFFFFFFFFu, dlt_c[c], u);
+                            p2[e] = ex2(fmaf(__uint_as_float(sv[u]), a.scale2, -lq));
+                            d2[e] = p2[e] * (__uint_as_float(pv[u]) - dq);
+                        }
+                        pp[v] = pack_bf16x2(p2[0], p2[1]);
+                        dd[v] = pack_bf16x2(d2[0], d2[1]);
+                    }
+                    // P^T and dS^T, packed, over the columns this thread has read
+                    tmem_st16(lane_addr + kST + 64 * b + 16 * c, pp);
+                    tmem_st16(lane_addr + kDPT + 64 * b + 16 * c, dd);
+                }
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    lse_c[h2] = lse_n[h2];
+                    dlt_c[h2] = dlt_n[h2];
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&pds_full[b]);
             }
-        };
-        float lse_c[2], dlt_c[2];
-        fetch(0, lse_c, dlt_c);
-        for (int i = 0; i < nq; ++i, ++g) {
-            const uint32_t b = NBUF == 2 ? static_cast<uint32_t>(g & 1) : 0u;
-            float lse_n[2], dlt_n[2];
-            fetch(i + 1, lse_n, dlt_n);
-            // S^T(g) was issued after the dV / dK that last read this buffer's
-            // P^T / dS^T, so once it is here the buffer is free
-            if (!warp_wait_bounded(&st_full[b], static_cast<uint32_t>(NBUF == 2 ? (g >> 1) : g) & 1u,
-                                   abort_flag, a.status, 0x308)) {
+            if (!ok || !warp_wait_bounded(grad_done, static_cast<uint32_t>(k) & 1u, abort_flag, a.status,
+                                          0x30A)) {
                 ok = false;
                 break;
             }
-            tc_fence_after();
+            {
+                tc_fence_after();
+                // tcgen05.ld is warp-collective (.sync.aligned): every lane loads,
+                // only keys inside the sequence are stored
+                const bool key_ok = key < a.s;
+                const long long tok = static_cast<long long>(n) * a.s + key;
+                uint4* dk = reinterpret_cast<uint4*>(a.dqkv + tok * 3 * a.h + a.h + head * D);
+                uint4* dv = reinterpret_cast<uint4*>(a.dqkv + tok * 3 * a.h + 2 * a.h + head * D);
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int qa = (i0 + i) * 64 + c * 32;  // first query of this chunk
-                uint32_t sv[32], pv[32];
-                tmem_ld32(lane_addr + kST + 64 * b + c * 32, sv);
-                tmem_ld32(lane_addr + kDPT + 64 * b + c * 32, pv);
-                tmem_wait_ld();
-                // causal mask: queries before this row's key
-                if (qa < key) {
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t v[32], k[32];
+                    tmem_ld32(lane_addr + acc_col(kDV, kDVt, c), v);
+                    tmem_ld32(lane_addr + acc_col(kDK, kDKt, c), k);
+                    tmem_wait_ld();
+                    if (key_ok) {
 #pragma unroll
-                    for (int v = 0; v < 32; ++v)
-                        if (qa + v < key) sv[v] = __float_as_uint(-INFINITY);
-                }
-                uint32_t pp[16], dd[16];
-#pragma unroll
-                for (int v = 0; v < 16; ++v) {
-                    float p2[2], d2[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int u = 2 * v + e;
-                        const float lq = __shfl_sync(0xFFFFFFFFu, lse_c[c], u);
-                        const float dq = __shfl_sync(0xFFFFFFFFu, dlt_c[c], u);
-                        p2[e] = ex2(fmaf(__uint_as_float(sv[u]), a.scale2, -lq));
-                        d2[e] = p2[e] * (__uint_as_float(pv[u]) - dq);
+                        for (int i = 0; i < 4; ++i) {
+                            uint4 u, w;
+                            u.x = pack_bf16x2(__uint_as_float(v[8 * i]), __uint_as_float(v[8 * i + 1]));
+                            u.y = pack_bf16x2(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3]));
+                            u.z = pack_bf16x2(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5]));
+                            u.w = pack_bf16x2(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7]));
+                            w.x = pack_bf16x2(__uint_as_float(k[8 * i]) * a.scale, __uint_as_float(k[8 * i + 1]) * a.scale);
+                            w.y = pack_bf16x2(__uint_as_float(k[8 * i + 2]) * a.scale, __uint_as_float(k[8 * i + 3]) * a.scale);
+                            w.z = pack_bf16x2(__uint_as_float(k[8 * i + 4]) * a.scale, __uint_as_float(k[8 * i + 5]) * a.scale);
+                            w.w = pack_bf16x2(__uint_as_float(k[8 * i + 6]) * a.scale, __uint_as_float(k[8 * i + 7]) * a.scale);
+                            dv[c * 4 + i] = u;
+                            dk[c * 4 + i] = w;
+                        }
                     }
-                    pp[v] = pack_bf16x2(p2[0], p2[1]);
-                    dd[v] = pack_bf16x2(d2[0], d2[1]);
                 }
-                // P^T and dS^T, packed, over the columns this thread has read
-                tmem_st16(lane_addr + kST + 64 * b + 16 * c, pp);
-                tmem_st16(lane_addr + kDPT + 64 * b + 16 * c, dd);
             }
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                lse_c[h2] = lse_n[h2];
-                dlt_c[h2] = dlt_n[h2];
-            }
-            tmem_wait_st();
+            // dV and dK are in registers or on their way to memory: the MMA may reuse them
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&pds_full[b]);
-        }
-        if (!ok || !warp_wait_bounded(grad_done, static_cast<uint32_t>(k) & 1u, abort_flag, a.status,
-                                      0x30A)) {
-            ok = false;
-            break;
-        }
-        {
-            tc_fence_after();
-            // tcgen05.ld is warp-collective (.sync.aligned): every lane loads,
-            // only keys inside the sequence are stored
-            const bool key_ok = key < a.s;
-            const long long tok = static_cast<long long>(n) * a.s + key;
-            uint4* dk = reinterpret_cast<uint4*>(a.dqkv + tok * 3 * a.h + a.h + head * D);
-            uint4* dv = reinterpret_cast<uint4*>(a.dqkv + tok * 3 * a.h + 2 * a.h + head * D);
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t v[32], k[32];
-                tmem_ld32(lane_addr + acc_col(kDV, kDVt, c), v);
-                tmem_ld32(lane_addr + acc_col(kDK, kDKt, c), k);
-                tmem_wait_ld();
-                if (key_ok) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        uint4 u, w;
-                        u.x = pack_bf16x2(__uint_as_float(v[8 * i]), __uint_as_float(v[8 * i + 1]));
-                        u.y = pack_bf16x2(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3]));
-                        u.z = pack_bf16x2(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5]));
-                        u.w = pack_bf16x2(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7]));
-                        w.x = pack_bf16x2(__uint_as_float(k[8 * i]) * a.scale, __uint_as_float(k[8 * i + 1]) * a.scale);
-                        w.y = pack_bf16x2(__uint_as_float(k[8 * i + 2]) * a.scale, __uint_as_float(k[8 * i + 3]) * a.scale);
-                        w.z = pack_bf16x2(__uint_as_float(k[8 * i + 4]) * a.scale, __uint_as_float(k[8 * i + 5]) * a.scale);
-                        w.w = pack_bf16x2(__uint_as_float(k[8 * i + 6]) * a.scale, __uint_as_float(k[8 * i + 7]) * a.scale);
-                        dv[c * 4 + i] = u;
-                        dk[c * 4 + i] = w;
-                    }
-                }
-            }
-        }
-        // dV and dK are in registers or on their way to memory: the MMA may reuse them
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(grad_free);
+            if (lane == 0) mbar_arrive(grad_free);
         }
     }
 
