@@ -622,6 +622,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + c * 64 + 32,
                           r2[1]);
                 tmem_wait_ld();
+                if (c == BN / 64 - 1) {
+                    // every column of this accumulator is in registers: the MMA
+                    // may start the tile after next on it while the last block
+                    // is staged and stored
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (PAIR)
+                            mbar_arrive_cluster(release_bar + acc * 8);
+                        else
+                            mbar_arrive(&acc_empty[acc]);
+                    }
+                }
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     const int n = n64 + half * 32;
@@ -730,14 +743,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             }
-            // TMEM of this accumulator may be overwritten from here on.
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                if constexpr (PAIR)
-                    mbar_arrive_cluster(release_bar + acc * 8);
-                else
-                    mbar_arrive(&acc_empty[acc]);
+            if constexpr (EPI == EPI_PARTIAL) {
+                // TMEM of this accumulator may be overwritten from here on (the
+                // other epilogues release it after their last TMEM read)
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (PAIR)
+                        mbar_arrive_cluster(release_bar + acc * 8);
+                    else
+                        mbar_arrive(&acc_empty[acc]);
+                }
             }
         }
         if (lane == 0) bulk_wait_group<0>();  // every output store has completed
