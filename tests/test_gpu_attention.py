@@ -136,7 +136,11 @@ def test_attention_shard_count_changes_nothing_but_the_sum_order():
             assert torch.equal(o[k], outs[0][k]), k
 
 
-FULL = [inputs.ATTN_GPT2_355M, inputs.ATTN_GPT2_8_3B, inputs.ATTN_MTNLG_530B]
+FULL = [inputs.ATTN_GPT2_355M, inputs.ATTN_GPT2_8_3B, inputs.ATTN_MTNLG_530B,
+        # h = 12288: dWo and dWqkv from transposed operands, T = 130 ragged
+        # (weights drawn as for the MT-NLG block, which has h of this order)
+        inputs.attn_custom(nb=1, s=130, h=12288, nh=96, t=8, seed=34,
+                           std=inputs.ATTN_MTNLG_530B.std, name="attn-kmajor-ragged")]
 
 
 @pytest.mark.parametrize("w", FULL, ids=lambda w: w.name)

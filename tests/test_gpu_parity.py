@@ -223,6 +223,9 @@ def check_sampled(w: inputs.Workload, nrows=8, ncols=16):
 
 FULL = [
     inputs.custom(T=2048, h=12288, F=4096, t=2, seed=32, name="tail-split"),  # 384 tiles, 76 pairs
+    # h >= 8192: dA and dB from transposed operands inside tp_mlp_backward,
+    # T = 130 padded to a 136-element row pitch
+    inputs.custom(T=130, h=8192, F=32768, t=4, seed=33, name="kmajor-ragged"),
     inputs.GPT2_MEDIUM.with_shape(T=8192, t=1),
     inputs.GPT2_MEDIUM.with_shape(T=8192, t=2),
     inputs.MEGATRON_8_3B,
