@@ -50,6 +50,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "kernels.h"
@@ -162,6 +163,7 @@ struct AttnArgs {
     int nb, s, h, nh;
     long long T;
     int q_tiles;     // work tiles along the sequence (forward: pairs of 128-row tiles)
+    int work_slot;   // this launch's counters in g_work
     float scale2;    // log2(e) / sqrt(d)
     float scale;     // 1 / sqrt(d)
     __nv_bfloat16* O;        // forward output [T, h]
@@ -210,10 +212,17 @@ struct FwdCfg {
     }
 };
 
+// Work counters of the persistent kernels.  Each launch gets its own slot
+// (next_work_slot, round robin): CTAs take work items one at a time from
+// g_work[slot][0] (atomicAdd) until it runs past the last item, and the last
+// CTA to finish (counted in g_work[slot][1]) sets both back to zero.  So
+// launches that overlap on the GPU (other streams) do not share counters,
+// as long as fewer than kWorkSlots of them are in flight at once.
+constexpr int kWorkSlots = 256;
+__device__ unsigned int g_work[kWorkSlots][2];
+
 // Work items of the forward kernel: (pair of 128-query tiles, sequence,
-// head), heaviest (most key tiles) first; taken and the counters reset as
-// for the backward kernels.
-__device__ unsigned int g_fwd_work[2];
+// head), heaviest (most key tiles) first.
 
 template <int D>
 __global__ void __launch_bounds__(kFwdThreads, 1)
@@ -311,7 +320,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     ok = false;
                 int item = -1;
                 if (ok) {
-                    item = static_cast<int>(atomicAdd(&g_fwd_work[0], 1u));
+                    item = static_cast<int>(atomicAdd(&g_work[a.work_slot][0], 1u));
                     if (item >= total) item = -1;
                 }
                 items[slot] = item;
@@ -609,9 +618,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // the last CTA out resets the work counters for the next launch
     if (threadIdx.x == 0) {
         __threadfence();
-        if (atomicAdd(&g_fwd_work[1], 1u) == gridDim.x - 1) {
-            g_fwd_work[0] = 0u;
-            g_fwd_work[1] = 0u;
+        if (atomicAdd(&g_work[a.work_slot][1], 1u) == gridDim.x - 1) {
+            g_work[a.work_slot][0] = 0u;
+            g_work[a.work_slot][1] = 0u;
             __threadfence();
         }
     }
@@ -695,12 +704,7 @@ struct DqCfg {
 };
 
 // Work items of the dQ kernel: (128 queries, sequence, head), heaviest
-// (most key tiles) first.  CTAs take them one at a time from g_dq_work[0]
-// (atomicAdd) until it runs past the last item; the last CTA to finish
-// (counted in g_dq_work[1]) sets both counters back to zero for the next
-// launch.  Launches on different streams that overlap on the GPU would
-// share the counters: the backward runs its kernels in stream order.
-__device__ unsigned int g_dq_work[2];
+// (most key tiles) first, taken from the launch's g_work slot.
 
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
@@ -797,7 +801,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     ok = false;
                 int item = -1;
                 if (ok) {
-                    item = static_cast<int>(atomicAdd(&g_dq_work[0], 1u));
+                    item = static_cast<int>(atomicAdd(&g_work[a.work_slot][0], 1u));
                     if (item >= total) item = -1;
                 }
                 items[slot] = item;
@@ -1031,9 +1035,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // the last CTA out resets the work counters for the next launch
     if (threadIdx.x == 0) {
         __threadfence();
-        if (atomicAdd(&g_dq_work[1], 1u) == gridDim.x - 1) {
-            g_dq_work[0] = 0u;
-            g_dq_work[1] = 0u;
+        if (atomicAdd(&g_work[a.work_slot][1], 1u) == gridDim.x - 1) {
+            g_work[a.work_slot][0] = 0u;
+            g_work[a.work_slot][1] = 0u;
             __threadfence();
         }
     }
@@ -1053,9 +1057,7 @@ struct DkvCfg {
 };
 
 // Work items of the dK/dV kernel: (128 keys, sequence, head), the first key
-// tiles (most queries after them) first; taken and the counters reset as
-// for the dQ kernel.
-__device__ unsigned int g_dkdv_work[2];
+// tiles (most queries after them) first, taken from the launch's g_work slot.
 
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
@@ -1166,7 +1168,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     ok = false;
                 int item = -1;
                 if (ok) {
-                    item = static_cast<int>(atomicAdd(&g_dkdv_work[0], 1u));
+                    item = static_cast<int>(atomicAdd(&g_work[a.work_slot][0], 1u));
                     if (item >= total) item = -1;
                 }
                 items[slot] = item;
@@ -1451,9 +1453,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // the last CTA out resets the work counters for the next launch
     if (threadIdx.x == 0) {
         __threadfence();
-        if (atomicAdd(&g_dkdv_work[1], 1u) == gridDim.x - 1) {
-            g_dkdv_work[0] = 0u;
-            g_dkdv_work[1] = 0u;
+        if (atomicAdd(&g_work[a.work_slot][1], 1u) == gridDim.x - 1) {
+            g_work[a.work_slot][0] = 0u;
+            g_work[a.work_slot][1] = 0u;
             __threadfence();
         }
     }
@@ -1464,6 +1466,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 // ------------------------------------------------------------- launchers
 
 namespace {
+// The g_work slot of the next persistent launch (round robin).
+int next_work_slot() {
+    static std::atomic<unsigned> seq{0};
+    return static_cast<int>(seq.fetch_add(1u, std::memory_order_relaxed) % kWorkSlots);
+}
+
 // CTAs of a persistent attention kernel: one per SM at most.
 unsigned persistent_grid(unsigned items) {
     static int sms = 0;
@@ -1490,6 +1498,7 @@ cudaError_t launch_attn_forward(const CUtensorMap& tm_qkv128, const CUtensorMap&
     a.status = p.status;
     // persistent: items (query-tile pairs x sequences x heads) taken in turn
     const unsigned grid = persistent_grid(static_cast<unsigned>(a.q_tiles * p.nb * p.nh));
+    a.work_slot = next_work_slot();
     cudaError_t e = cudaSuccess;
 #define TPMLP_ATTN_FWD(DD)                                                                        \
     if (d == DD) {                                                                                \
@@ -1546,6 +1555,8 @@ cudaError_t launch_attn_backward(const CUtensorMap& tm_qkv128, const CUtensorMap
     const int q_tiles = (p.s + 127) / 128;
     AttnArgs aq = a;
     aq.q_tiles = q_tiles;
+    aq.work_slot = next_work_slot();
+    a.work_slot = next_work_slot();
     // the dQ and dK/dV kernels are persistent: one CTA per SM at most, items
     // taken in turn (both have q_tiles x nb x nh items)
     const unsigned dq_grid = persistent_grid(static_cast<unsigned>(q_tiles * p.nb * p.nh));

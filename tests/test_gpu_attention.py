@@ -136,6 +136,38 @@ def test_attention_shard_count_changes_nothing_but_the_sum_order():
             assert torch.equal(o[k], outs[0][k]), k
 
 
+def test_attention_kernels_on_two_streams():
+    """The persistent attention kernels take their work items from counters
+    of their own launch: attention on two streams at once gives the same
+    bits as one call after the other on one stream."""
+    shapes = [(2, 384, 512, 4), (3, 256, 640, 5)]  # nb, s, h, nh
+    g = torch.Generator(device="cuda").manual_seed(42)
+    data = []
+    for nb, s, h, nh in shapes:
+        T = nb * s
+        QKV = (torch.randn(T, 3 * h, generator=g, device="cuda") * 0.5).to(torch.bfloat16)
+        dO = torch.randn(T, h, generator=g, device="cuda").to(torch.bfloat16)
+        data.append((QKV, dO, nb, nh))
+    ref = []
+    for QKV, dO, nb, nh in data:
+        O, lse = binding.tp_attn_core_forward(QKV, nb, nh)
+        ref.append((O, lse, binding.tp_attn_core_backward(QKV, O, lse, dO, nb, nh)))
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    got = [[], []]
+    for _ in range(4):
+        for i, (QKV, dO, nb, nh) in enumerate(data):
+            with torch.cuda.stream(streams[i]):
+                O, lse = binding.tp_attn_core_forward(QKV, nb, nh)
+                got[i].append((O, lse, binding.tp_attn_core_backward(QKV, O, lse, dO, nb, nh)))
+    torch.cuda.synchronize()
+    assert binding.device_status() == 0
+    for i in range(2):
+        for O, lse, dQKV in got[i]:
+            assert torch.equal(O, ref[i][0]) and torch.equal(lse, ref[i][1])
+            assert torch.equal(dQKV, ref[i][2])
+
+
 FULL = [inputs.ATTN_GPT2_355M, inputs.ATTN_GPT2_8_3B, inputs.ATTN_MTNLG_530B,
         # h = 12288: dWo and dWqkv from transposed operands, T = 130 ragged
         # (weights drawn as for the MT-NLG block, which has h of this order)
