@@ -786,6 +786,7 @@ bool kmajor_weight_grad(long long M, long long N) { return M * N >= 6144LL * (M 
 
 constexpr int kColBlock = 64;   // columns per CTA: 8 lanes x 8 bf16 (16 B each)
 constexpr int kSumThreads = 256;
+constexpr int kSumBatch = 8;    // 16-byte loads a thread keeps in flight
 constexpr int kTargetCtas = 640;
 
 int colsum_chunks(int T, int n) {
@@ -796,9 +797,12 @@ int colsum_chunks(int T, int n) {
 }
 
 // Partial column sums of G [T, n] over one chunk of rows.  A warp covers
-// 64 columns and 4 rows per step (lanes 8j..8j+7 read row 4k+j, 16 B each);
-// the 4 row phases meet by warp shuffle, the 8 warps in shared memory, in a
-// fixed order.  Writes out[blockIdx.y * n + col].
+// 64 columns and 4 rows per step (lanes 8j..8j+7 read row 4k+j, 16 B each),
+// the CTA 32 rows per step.  Each thread issues the loads of kSumBatch steps
+// before it adds any of them (rows past the chunk read as zero), so that
+// 32 KiB per CTA are in flight; the adds stay in row order.  The 4 row
+// phases meet by warp shuffle, the 8 warps in shared memory, in a fixed
+// order.  Writes out[blockIdx.y * n + col].
 __global__ void __launch_bounds__(kSumThreads)
     colsum_partial_kernel(const __nv_bfloat16* __restrict__ G, int T, int n, int rows_per_chunk,
                           float* __restrict__ out) {
@@ -810,18 +814,33 @@ __global__ void __launch_bounds__(kSumThreads)
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-    const bool full_vec = col0 + 8 <= n;
-    for (int r = r0 + warp * 4 + (lane >> 3); r < r1; r += 32) {
-        const __nv_bfloat16* row = G + static_cast<long long>(r) * n + col0;
-        if (full_vec) {
-            const uint4 u = __ldg(reinterpret_cast<const uint4*>(row));
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    const int rt = r0 + warp * 4 + (lane >> 3);  // this thread's first row
+    if (col0 + 8 <= n) {
+        const __nv_bfloat16* base = G + col0;
+        for (int r = rt; r < r1; r += 32 * kSumBatch) {
+            // every load is issued (a row past the chunk re-reads its last
+            // row) and its words are zeroed afterwards: no branch between
+            // the loads
+            uint4 u[kSumBatch];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                acc[2 * j] += __uint_as_float(w[j] << 16);
-                acc[2 * j + 1] += __uint_as_float(w[j] & 0xFFFF0000u);
+            for (int k = 0; k < kSumBatch; ++k) {
+                const int rk = min(r + 32 * k, r1 - 1);
+                u[k] = __ldg(reinterpret_cast<const uint4*>(base + static_cast<long long>(rk) * n));
             }
-        } else {
+#pragma unroll
+            for (int k = 0; k < kSumBatch; ++k) {
+                const uint32_t keep = r + 32 * k < r1 ? 0xFFFFFFFFu : 0u;
+                const uint32_t w[4] = {u[k].x & keep, u[k].y & keep, u[k].z & keep, u[k].w & keep};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    acc[2 * j] += __uint_as_float(w[j] << 16);
+                    acc[2 * j + 1] += __uint_as_float(w[j] & 0xFFFF0000u);
+                }
+            }
+        }
+    } else {
+        for (int r = rt; r < r1; r += 32) {
+            const __nv_bfloat16* row = G + static_cast<long long>(r) * n + col0;
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 if (col0 + i < n) acc[i] += __bfloat162float(row[i]);
@@ -846,18 +865,35 @@ __global__ void __launch_bounds__(kSumThreads)
     }
 }
 
-// out[j] = sum_{i < rows} P[i * n + j], summed in row order.
-__global__ void __launch_bounds__(256)
+// out[j] = sum_{i < rows} P[i * n + j].  A 256-thread CTA covers 32 columns:
+// the warp g sums rows g, g + 8, g + 16, ... in order (4 loads in flight a
+// thread), then thread j of warp 0 adds the 8 warps' sums in warp order.
+constexpr int kRowsumCols = 32;
+constexpr int kRowsumGroups = 8;
+
+__global__ void __launch_bounds__(kRowsumCols * kRowsumGroups)
     rowsum_kernel(const float* __restrict__ P, int rows, int n, float* __restrict__ out) {
-    const int j = blockIdx.x * blockDim.x + threadIdx.x;
-    if (j >= n) return;
+    __shared__ float part[kRowsumGroups][kRowsumCols];
+    const int g = threadIdx.x / kRowsumCols, c = threadIdx.x % kRowsumCols;
+    const int j = blockIdx.x * kRowsumCols + c;
     float s = 0.0f;
-    for (int i = 0; i < rows; ++i) s += P[static_cast<long long>(i) * n + j];
-    out[j] = s;
+    if (j < n) {
+#pragma unroll 4
+        for (int i = g; i < rows; i += kRowsumGroups) s += __ldg(P + static_cast<long long>(i) * n + j);
+    }
+    part[g][c] = s;
+    __syncthreads();
+    if (g == 0 && j < n) {
+        float t = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kRowsumGroups; ++w) t += part[w][c];
+        out[j] = t;
+    }
 }
 
 int launch_rowsum(const float* P, int rows, int n, float* out, cudaStream_t st) {
-    rowsum_kernel<<<static_cast<unsigned>(cdiv(n, 256)), 256, 0, st>>>(P, rows, n, out);
+    rowsum_kernel<<<static_cast<unsigned>(cdiv(n, kRowsumCols)), kRowsumCols * kRowsumGroups, 0, st>>>(
+        P, rows, n, out);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail_cuda(e);
     ++t_last_launches;
