@@ -46,6 +46,17 @@ cudaError_t launch_weight_grad(const GemmMaps& m, const GemmArgs& g,
 cudaError_t launch_transpose(const __nv_bfloat16* in, int rows, int cols, __nv_bfloat16* out,
                              int ld_out, cudaStream_t st, int* launches);
 
+// Column sums db[j] = sum_{r < T} G[r * n + j] of a bf16 [T, n] matrix in
+// fp32 (colsum.cu).  With colsum_chunks(T, n) > 1 row chunks the chunks'
+// partial rows go to `partial` (colsum_chunks(T, n) * n floats) and a second
+// launch adds them in chunk order; with one chunk db is written directly.
+int colsum_chunks(int T, int n);
+cudaError_t launch_colsum(const __nv_bfloat16* G, int T, int n, float* db, float* partial,
+                          cudaStream_t st, int* launches);
+// out[j] = sum_{i < rows} P[i * n + j] for an fp32 [rows, n] matrix (colsum.cu).
+cudaError_t launch_rowsum_f32(const float* P, int rows, int n, float* out, cudaStream_t st,
+                              int* launches);
+
 // Residual add + LayerNorm (layernorm.cu).  `launches` is incremented per
 // kernel launched.
 cudaError_t launch_ln_forward(const __nv_bfloat16* a, const __nv_bfloat16* r,
