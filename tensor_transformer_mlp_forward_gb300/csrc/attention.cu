@@ -67,6 +67,31 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Two fp32 values in one 64-bit register, for the paired fp32 instructions
+// (one issue slot for two FMAs or two adds).
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f32x2_split(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
 __device__ __forceinline__ float lg2(float x) {
     float y;
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -532,21 +557,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 const bool move = (j == 0 && m_new > -INFINITY) || m_new > m + kRescaleLog2;
                 const float alpha = move ? ex2(m - m_new) : 1.0f;
                 if (move) m = m_new;
-                float rs8[8];
+                uint64_t rs2[4];
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) rs8[kk] = 0.0f;
+                for (int kk = 0; kk < 4; ++kk) rs2[kk] = 0ull;  // (0.0f, 0.0f)
+                const uint64_t scale2 = f32x2(a.scale2, a.scale2), neg_m = f32x2(-m, -m);
                 uint32_t pk[SCH][16];
 #pragma unroll
                 for (int c = 0; c < SCH; ++c)
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         // masked scores are -inf: 2^-inf = 0
-                        const float p0 = ex2(fmaf(__uint_as_float(v[c][2 * i]), a.scale2, -m));
-                        const float p1 = ex2(fmaf(__uint_as_float(v[c][2 * i + 1]), a.scale2, -m));
-                        rs8[i & 7] += p0 + p1;
+                        float x0, x1;
+                        f32x2_split(fma_f32x2(f32x2(__uint_as_float(v[c][2 * i]), __uint_as_float(v[c][2 * i + 1])),
+                                              scale2, neg_m), x0, x1);
+                        const float p0 = ex2(x0), p1 = ex2(x1);
+                        rs2[i & 3] = add_f32x2(rs2[i & 3], f32x2(p0, p1));
                         pk[c][i] = pack_bf16x2(p0, p1);
                     }
-                const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+                float rsv[8];
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) f32x2_split(rs2[kk], rsv[2 * kk], rsv[2 * kk + 1]);
+                const float rs = ((rsv[0] + rsv[1]) + (rsv[2] + rsv[3])) + ((rsv[4] + rsv[5]) + (rsv[6] + rsv[7]));
                 l = fmaf(l, alpha, rs);
                 // S_x(j) was issued after P_x V of the previous key tile, and the
                 // commit that signalled S_x covers every earlier MMA: that P V
@@ -978,12 +1009,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             if (key0 + i > q) sv[i] = __float_as_uint(-INFINITY);
                     }
                     uint32_t dd[16];
+                    const uint64_t scale2 = f32x2(a.scale2, a.scale2), neg_lse = f32x2(-lse, -lse),
+                                   neg_dlt = f32x2(-dlt, -dlt);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const float p0 = ex2(fmaf(__uint_as_float(sv[2 * i]), a.scale2, -lse));
-                        const float p1 = ex2(fmaf(__uint_as_float(sv[2 * i + 1]), a.scale2, -lse));
-                        dd[i] = pack_bf16x2(p0 * (__uint_as_float(pv[2 * i]) - dlt),
-                                            p1 * (__uint_as_float(pv[2 * i + 1]) - dlt));
+                        float x0, x1, d0, d1;
+                        f32x2_split(fma_f32x2(f32x2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])),
+                                              scale2, neg_lse), x0, x1);
+                        const float p0 = ex2(x0), p1 = ex2(x1);
+                        f32x2_split(mul_f32x2(f32x2(p0, p1),
+                                              add_f32x2(f32x2(__uint_as_float(pv[2 * i]),
+                                                              __uint_as_float(pv[2 * i + 1])), neg_dlt)), d0, d1);
+                        dd[i] = pack_bf16x2(d0, d1);
                     }
                     // dS, packed, over the S columns this thread has read
                     tmem_st16(lane_addr + kS + 64 * b + 16 * c, dd);
@@ -1340,8 +1377,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 for (int h2 = 0; h2 < 2; ++h2) {
                     const int qq = (i0 + i) * 64 + 32 * h2 + lane;
                     const bool in = i < nq && qq < a.s;
-                    lv[h2] = in ? __ldg(lse_seq + qq) : INFINITY;
-                    dv[h2] = in ? __ldg(dlt_seq + qq) : 0.0f;
+                    lv[h2] = in ? -__ldg(lse_seq + qq) : -INFINITY;  // held negated
+                    dv[h2] = in ? -__ldg(dlt_seq + qq) : -0.0f;
                 }
             };
             float lse_c[2], dlt_c[2];
@@ -1372,19 +1409,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             if (qa + v < key) sv[v] = __float_as_uint(-INFINITY);
                     }
                     uint32_t pp[16], dd[16];
+                    const uint64_t scale2 = f32x2(a.scale2, a.scale2);
 #pragma unroll
                     for (int v = 0; v < 16; ++v) {
-                        float p2[2], d2[2];
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int u = 2 * v + e;
-                            const float lq = __shfl_sync(0xFFFFFFFFu, lse_c[c], u);
-                            const float dq = __shfl_sync(0xFFFFFFFFu, dlt_c[c], u);
-                            p2[e] = ex2(fmaf(__uint_as_float(sv[u]), a.scale2, -lq));
-                            d2[e] = p2[e] * (__uint_as_float(pv[u]) - dq);
-                        }
-                        pp[v] = pack_bf16x2(p2[0], p2[1]);
-                        dd[v] = pack_bf16x2(d2[0], d2[1]);
+                        const uint64_t neg_lq = f32x2(__shfl_sync(0xFFFFFFFFu, lse_c[c], 2 * v),
+                                                      __shfl_sync(0xFFFFFFFFu, lse_c[c], 2 * v + 1));
+                        const uint64_t neg_dq = f32x2(__shfl_sync(0xFFFFFFFFu, dlt_c[c], 2 * v),
+                                                      __shfl_sync(0xFFFFFFFFu, dlt_c[c], 2 * v + 1));
+                        float x0, x1, d0, d1;
+                        f32x2_split(fma_f32x2(f32x2(__uint_as_float(sv[2 * v]), __uint_as_float(sv[2 * v + 1])),
+                                              scale2, neg_lq), x0, x1);
+                        const float p0 = ex2(x0), p1 = ex2(x1);
+                        f32x2_split(mul_f32x2(f32x2(p0, p1),
+                                              add_f32x2(f32x2(__uint_as_float(pv[2 * v]),
+                                                              __uint_as_float(pv[2 * v + 1])), neg_dq)), d0, d1);
+                        pp[v] = pack_bf16x2(p0, p1);
+                        dd[v] = pack_bf16x2(d0, d1);
                     }
                     // P^T and dS^T, packed, over the columns this thread has read
                     tmem_st16(lane_addr + kST + 64 * b + 16 * c, pp);
