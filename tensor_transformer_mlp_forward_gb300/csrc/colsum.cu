@@ -142,6 +142,7 @@ cudaError_t launch_rowsum_f32(const float* P, int rows, int n, float* out, cudaS
     return cudaGetLastError();
 }
 
+// T == 0 or n == 0 launches nothing and leaves db as it was.
 cudaError_t launch_colsum(const __nv_bfloat16* G, int T, int n, float* db, float* partial,
                           cudaStream_t st, int* launches) {
     if (T == 0 || n == 0) return cudaSuccess;
