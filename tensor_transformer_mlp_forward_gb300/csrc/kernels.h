@@ -50,7 +50,6 @@ cudaError_t launch_transpose(const __nv_bfloat16* in, int rows, int cols, __nv_b
 // fp32 (colsum.cu).  With colsum_chunks(T, n) > 1 row chunks the chunks'
 // partial rows go to `partial` (colsum_chunks(T, n) * n floats) and a second
 // launch adds them in chunk order; with one chunk db is written directly.
-// T == 0 or n == 0 launches nothing and leaves db as it was.
 int colsum_chunks(int T, int n);
 cudaError_t launch_colsum(const __nv_bfloat16* G, int T, int n, float* db, float* partial,
                           cudaStream_t st, int* launches);
