@@ -641,12 +641,17 @@ class AttnStep:
         lib = binding.lib()
         self.p_sum = e(max(1, int(lib.tp_mlp_bias_grad_workspace_floats(T, 3 * h)),
                            int(lib.tp_mlp_bias_grad_workspace_floats(T, h))), dt=torch.float32)
-        self.ws = e(max(16, binding.split_workspace_bytes(T, h, 3 * h, 1),
-                        binding.split_workspace_bytes(T, h, h, w.t)), dt=torch.uint8)
-        self.launches = 0
         # the weight gradients in K-major form where tp_attn_backward takes it
         self.kmajor_o = binding.weight_grad_kmajor(h, h)
         self.kmajor_qkv = binding.weight_grad_kmajor(h, 3 * h)
+        # split reductions: the row-parallel GEMMs', and the MN-major weight
+        # gradients' where their few output tiles leave SM pairs idle
+        self.ws = e(max(16, binding.split_workspace_bytes(T, h, 3 * h, 1),
+                        binding.split_workspace_bytes(T, h, h, w.t),
+                        0 if self.kmajor_o else binding.weight_grad_workspace_bytes(T, h, h),
+                        0 if self.kmajor_qkv else binding.weight_grad_workspace_bytes(T, h, 3 * h)),
+                    dt=torch.uint8)
+        self.launches = 0
         ldT = binding.pitch(T)
         if self.kmajor_o:
             self.Ot, self.dYt = e(h, ldT), e(h, ldT)
@@ -671,7 +676,7 @@ class AttnStep:
                 lambda: b.tp_mlp_dB_kmajor(self.Ot, self.dYt, w.T, 1, dB=self.dWo),
             )
         else:
-            calls += (lambda: b.tp_mlp_dB(self.O, i["dY"], 1, dB=self.dWo),)
+            calls += (lambda: b.tp_mlp_dB_ws(self.O, i["dY"], 1, dB=self.dWo, workspace=self.ws),)
         calls += (
             lambda: b.tp_mlp_dx(i["dY"], i["Wo"], 1, dX=self.dO, workspace=self.ws),
             lambda: b.tp_attn_core_backward(self.QKV, self.O, self.lse, self.dO, w.nb, w.nh,
@@ -685,7 +690,7 @@ class AttnStep:
                 lambda: b.tp_mlp_dA_kmajor(self.Xt, self.dQKVt, w.T, 1, dA=self.dWqkv),
             )
         else:
-            calls += (lambda: b.tp_mlp_dA(i["X"], self.dQKV, 1, dA=self.dWqkv),)
+            calls += (lambda: b.tp_mlp_dA_ws(i["X"], self.dQKV, 1, dA=self.dWqkv, workspace=self.ws),)
         calls += (lambda: b.tp_mlp_dx(self.dQKV, i["Wqkv"], 1, dX=self.dX, workspace=self.ws),)
         if events is not None:
             events[0].record()

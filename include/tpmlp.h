@@ -196,6 +196,24 @@ int tp_mlp_dA(const tpmlp_bf16* X, const tpmlp_bf16* dZ, int T, int h, int F, in
 int tp_mlp_dB(const tpmlp_bf16* H, const tpmlp_bf16* dY, int T, int h, int F, int t,
               tpmlp_bf16* dB, void* stream);
 
+/* a8 and a9 as above, with a caller workspace (device memory, 16-byte
+ * aligned, owned by the caller, not read before it is written).  With t == 1
+ * and an output of few 256 x 256 tiles -- the attention block's dWo (h x h)
+ * and dWqkv (h x 3h) at small h -- the token reduction is cut into k ranges
+ * that run on otherwise idle SM pairs as fp32 partial outputs in the
+ * workspace, added in range order by a second kernel (deterministic; the
+ * sum order differs from tp_mlp_dA / tp_mlp_dB by that split).  Otherwise,
+ * or with a NULL or smaller workspace (fewer ranges), the result is that of
+ * tp_mlp_dA / tp_mlp_dB.  tp_weight_grad_workspace_bytes(T, M, N) is the
+ * workspace that allows every split for an M x N gradient (0: none is
+ * taken).  Errors: those of tp_mlp_dA / tp_mlp_dB, ERR_ALIGN for a
+ * misaligned workspace.  tp_attn_backward computes dWo and dWqkv this way. */
+size_t tp_weight_grad_workspace_bytes(int T, int M, int N);
+int tp_mlp_dA_ws(const tpmlp_bf16* X, const tpmlp_bf16* dZ, int T, int h, int F, int t,
+                 tpmlp_bf16* dA, void* workspace, size_t workspace_bytes, void* stream);
+int tp_mlp_dB_ws(const tpmlp_bf16* H, const tpmlp_bf16* dY, int T, int h, int F, int t,
+                 tpmlp_bf16* dB, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Transpose of a bf16 matrix, the layout the two calls below read:
  * out[c * ld_out + r] = in[r * cols + c] for r < rows, c < cols, and
  * out[c * ld_out + r] = 0 for rows <= r < (rows rounded up to 8); the rest of

@@ -62,6 +62,9 @@ _SIGNATURES = {
     "tp_mlp_dA": ([_P] * 2 + [_I] * 4 + [_P] + [_P], _I),
     "tp_mlp_dB": ([_P] * 2 + [_I] * 4 + [_P] + [_P], _I),
     "tp_weight_grad_kmajor": ([_I, _I], _I),
+    "tp_weight_grad_workspace_bytes": ([_I, _I, _I], _S),
+    "tp_mlp_dA_ws": ([_P] * 2 + [_I] * 4 + [_P] + [_P, _S, _P], _I),
+    "tp_mlp_dB_ws": ([_P] * 2 + [_I] * 4 + [_P] + [_P, _S, _P], _I),
     "tp_transpose": ([_P, _I, _I, _P, _I, _P], _I),
     "tp_mlp_dA_kmajor": ([_P] * 2 + [_I] * 5 + [_P] + [_P], _I),
     "tp_mlp_dB_kmajor": ([_P] * 2 + [_I] * 5 + [_P] + [_P], _I),
@@ -438,6 +441,38 @@ def tp_mlp_dB(H, dY, t: int, dB=None, stream=None):
     _check("tp_mlp_dB", lib().tp_mlp_dB(
         _ptr(H, "H", (T, F)), _ptr(dY, "dY", (T, h)), T, h, F, t, _ptr(dB, "dB", (F, h)),
         _stream(stream)))
+    return dB
+
+
+def weight_grad_workspace_bytes(T: int, M: int, N: int) -> int:
+    """Workspace that lets an M x N weight gradient split its T-token
+    reduction over idle SM pairs (0: it is computed whole)."""
+    return int(lib().tp_weight_grad_workspace_bytes(T, M, N))
+
+
+def tp_mlp_dA_ws(X, dZ, t: int, dA=None, workspace=None, stream=None):
+    """tp_mlp_dA with a workspace for the split reduction (allocated here
+    when None and the shape takes a split)."""
+    T, h = X.shape
+    F = dZ.shape[1]
+    dA = _out(dA, (h, F), X)
+    wp, wn = _workspace(workspace, weight_grad_workspace_bytes(T, h, F) if t == 1 else 0, X)
+    _check("tp_mlp_dA_ws", lib().tp_mlp_dA_ws(
+        _ptr(X, "X", (T, h)), _ptr(dZ, "dZ", (T, F)), T, h, F, t, _ptr(dA, "dA", (h, F)),
+        wp, wn, _stream(stream)))
+    return dA
+
+
+def tp_mlp_dB_ws(H, dY, t: int, dB=None, workspace=None, stream=None):
+    """tp_mlp_dB with a workspace for the split reduction (allocated here
+    when None and the shape takes a split)."""
+    T, F = H.shape
+    h = dY.shape[1]
+    dB = _out(dB, (F, h), H)
+    wp, wn = _workspace(workspace, weight_grad_workspace_bytes(T, F, h) if t == 1 else 0, H)
+    _check("tp_mlp_dB_ws", lib().tp_mlp_dB_ws(
+        _ptr(H, "H", (T, F)), _ptr(dY, "dY", (T, h)), T, h, F, t, _ptr(dB, "dB", (F, h)),
+        wp, wn, _stream(stream)))
     return dB
 
 

@@ -599,6 +599,23 @@ int row_splits(int T, int h, int F, int t, size_t ws_bytes, const DeviceInfo& d)
     return sp;
 }
 
+// Splits of a weight gradient's token reduction (cdiv(T, BK) k-blocks) when
+// its M x N output tiles leave CTA pairs idle (a small hidden size: dWo of
+// h x h at h = 1024 has 16 tiles of 256 x 256), limited by the caller's
+// workspace, which holds the splits' fp32 partial outputs.
+int weight_splits(int T, long long M, long long N, size_t ws_bytes, const DeviceInfo& d) {
+    int sp = choose_splits(M, N, cdiv(T, BK), d.sms / 2);
+    const size_t per = sizeof(float) * static_cast<size_t>(M) * static_cast<size_t>(N);
+    while (sp > 1 && static_cast<size_t>(sp) * per > ws_bytes) --sp;
+    return sp;
+}
+
+// Floats of partial outputs a split weight gradient of this shape uses.
+size_t weight_split_floats(int T, long long M, long long N) {
+    const int sp = choose_splits(M, N, cdiv(T, BK), kSizingPairs);
+    return sp > 1 ? static_cast<size_t>(sp) * static_cast<size_t>(M) * static_cast<size_t>(N) : 0;
+}
+
 int row_sum(const tpmlp_bf16* H, const tpmlp_bf16* B, const tpmlp_bf16* b2,
             const tpmlp_bf16* R, int T, int h, int F, int t, tpmlp_bf16* Y, void* ws,
             size_t ws_bytes, cudaStream_t st, const DeviceInfo& d, const Dropout& dr = Dropout{}) {
@@ -711,8 +728,26 @@ int dx_gemm(const tpmlp_bf16* dZ, const tpmlp_bf16* A, int T, int h, int F, int 
     return launch_split_reduce(static_cast<const float*>(ws), sp, T, h, nullptr, nullptr, Dropout{}, dX, st);
 }
 
+// A weight gradient whole, or -- one shard (t = 1) and a workspace given --
+// as k-range splits of fp32 partial outputs (weight_splits) added in split
+// order by split_reduce_kernel.
+int weight_grad(const Operand& a, const Operand& b, long long M, long long N, int T,
+                GemmArgs& g, const GemmShape& sh, tpmlp_bf16* out, void* ws, size_t ws_bytes,
+                cudaStream_t st, const DeviceInfo& d) {
+    const int sp = (ws != nullptr && sh.t == 1) ? weight_splits(T, M, N, ws_bytes, d) : 1;
+    if (sp == 1) {
+        Output o{out, nullptr, M, N, 1};
+        return run_gemm(launch_weight_grad, a, b, o, g, sh, st, d);
+    }
+    Output o{ws, nullptr, M, N, sp};
+    if (int rc = run_gemm(launch_weight_grad_partial, a, b, o, g, sh, st, d)) return rc;
+    return launch_split_reduce(static_cast<const float*>(ws), sp, static_cast<int>(M),
+                               static_cast<int>(N), nullptr, nullptr, Dropout{}, out, st);
+}
+
 int dA_gemm(const tpmlp_bf16* X, const tpmlp_bf16* dZ, int T, int h, int F, int t,
-            tpmlp_bf16* dA, cudaStream_t st, const DeviceInfo& d) {
+            tpmlp_bf16* dA, cudaStream_t st, const DeviceInfo& d, void* ws = nullptr,
+            size_t ws_bytes = 0) {
     const int f = F / t;
     GemmArgs g = blank_args();
     const GemmShape sh{h, f, T, t, SHARD_N, 1LL * T * h, 1LL * T * F};
@@ -720,12 +755,12 @@ int dA_gemm(const tpmlp_bf16* X, const tpmlp_bf16* dZ, int T, int h, int F, int 
     g.b_on = ON_CONTIG;
     Operand a{X, T, h, ON_NONE, true};
     Operand b{dZ, T, F, ON_CONTIG, true};
-    Output o{dA, nullptr, h, F};
-    return run_gemm(launch_weight_grad, a, b, o, g, sh, st, d);
+    return weight_grad(a, b, h, F, T, g, sh, dA, ws, ws_bytes, st, d);
 }
 
 int dB_gemm(const tpmlp_bf16* H, const tpmlp_bf16* dY, int T, int h, int F, int t,
-            tpmlp_bf16* dB, cudaStream_t st, const DeviceInfo& d) {
+            tpmlp_bf16* dB, cudaStream_t st, const DeviceInfo& d, void* ws = nullptr,
+            size_t ws_bytes = 0) {
     const int f = F / t;
     GemmArgs g = blank_args();
     const GemmShape sh{f, h, T, t, SHARD_M, 1LL * T * F, 1LL * T * h};
@@ -733,8 +768,7 @@ int dB_gemm(const tpmlp_bf16* H, const tpmlp_bf16* dY, int T, int h, int F, int 
     g.b_on = ON_NONE;
     Operand a{H, T, F, ON_CONTIG, true};
     Operand b{dY, T, h, ON_NONE, true};
-    Output o{dB, nullptr, F, h};
-    return run_gemm(launch_weight_grad, a, b, o, g, sh, st, d);
+    return weight_grad(a, b, F, h, T, g, sh, dB, ws, ws_bytes, st, d);
 }
 
 // a8 and a9 from the transposed operands, both K-major: Xt = X^T [h, ldT],
@@ -1021,11 +1055,11 @@ TPMLP_API int tp_mlp_dx(const tpmlp_bf16* dZ, const tpmlp_bf16* A, int T, int h,
                    static_cast<cudaStream_t>(stream), d);
 }
 
-TPMLP_API int tp_mlp_dA(const tpmlp_bf16* X, const tpmlp_bf16* dZ, int T, int h, int F, int t,
-                        tpmlp_bf16* dA, void* stream) {
+TPMLP_API int tp_mlp_dA_ws(const tpmlp_bf16* X, const tpmlp_bf16* dZ, int T, int h, int F, int t,
+                           tpmlp_bf16* dA, void* workspace, size_t workspace_bytes, void* stream) {
     TPMLP_PROLOGUE(check_dims(T, h, F, t));
     if (any_null(dA) || (T > 0 && any_null(X, dZ))) return TPMLP_ERR_NULL;
-    if (!all_aligned(X, dZ, dA)) return TPMLP_ERR_ALIGN;
+    if (!all_aligned(X, dZ, dA) || !aligned16(workspace)) return TPMLP_ERR_ALIGN;
     DeviceInfo d;
     if (int rc = enter(d)) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -1033,14 +1067,19 @@ TPMLP_API int tp_mlp_dA(const tpmlp_bf16* X, const tpmlp_bf16* dZ, int T, int h,
         cudaError_t e = cudaMemsetAsync(dA, 0, sizeof(uint16_t) * static_cast<size_t>(h) * F, st);
         return e == cudaSuccess ? TPMLP_OK : fail_cuda(e);
     }
-    return dA_gemm(X, dZ, T, h, F, t, dA, st, d);
+    return dA_gemm(X, dZ, T, h, F, t, dA, st, d, workspace, workspace ? workspace_bytes : 0);
 }
 
-TPMLP_API int tp_mlp_dB(const tpmlp_bf16* H, const tpmlp_bf16* dY, int T, int h, int F, int t,
-                        tpmlp_bf16* dB, void* stream) {
+TPMLP_API int tp_mlp_dA(const tpmlp_bf16* X, const tpmlp_bf16* dZ, int T, int h, int F, int t,
+                        tpmlp_bf16* dA, void* stream) {
+    return tp_mlp_dA_ws(X, dZ, T, h, F, t, dA, nullptr, 0, stream);
+}
+
+TPMLP_API int tp_mlp_dB_ws(const tpmlp_bf16* H, const tpmlp_bf16* dY, int T, int h, int F, int t,
+                           tpmlp_bf16* dB, void* workspace, size_t workspace_bytes, void* stream) {
     TPMLP_PROLOGUE(check_dims(T, h, F, t));
     if (any_null(dB) || (T > 0 && any_null(H, dY))) return TPMLP_ERR_NULL;
-    if (!all_aligned(H, dY, dB)) return TPMLP_ERR_ALIGN;
+    if (!all_aligned(H, dY, dB) || !aligned16(workspace)) return TPMLP_ERR_ALIGN;
     DeviceInfo d;
     if (int rc = enter(d)) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -1048,7 +1087,17 @@ TPMLP_API int tp_mlp_dB(const tpmlp_bf16* H, const tpmlp_bf16* dY, int T, int h,
         cudaError_t e = cudaMemsetAsync(dB, 0, sizeof(uint16_t) * static_cast<size_t>(F) * h, st);
         return e == cudaSuccess ? TPMLP_OK : fail_cuda(e);
     }
-    return dB_gemm(H, dY, T, h, F, t, dB, st, d);
+    return dB_gemm(H, dY, T, h, F, t, dB, st, d, workspace, workspace ? workspace_bytes : 0);
+}
+
+TPMLP_API int tp_mlp_dB(const tpmlp_bf16* H, const tpmlp_bf16* dY, int T, int h, int F, int t,
+                        tpmlp_bf16* dB, void* stream) {
+    return tp_mlp_dB_ws(H, dY, T, h, F, t, dB, nullptr, 0, stream);
+}
+
+TPMLP_API size_t tp_weight_grad_workspace_bytes(int T, int M, int N) {
+    if (T <= 0 || M <= 0 || N <= 0) return 0;
+    return sizeof(float) * weight_split_floats(T, M, N);
 }
 
 TPMLP_API int tp_weight_grad_kmajor(int M, int N) {
@@ -1492,7 +1541,8 @@ size_t attn_colsum_floats(int T, int h) {
 
 // Attention backward workspace: dO, delta, dQKV, the column-sum partials,
 // the transposed operands of dWo (O^T, dY^T) and dWqkv (X^T, dQKV^T) where
-// those take the K-major form, and the split-reduction scratch.
+// those take the K-major form, and the split-reduction scratch (the
+// row-parallel GEMMs' and, where dWo or dWqkv is split, its partials).
 struct AttnBackwardLayout {
     size_t dO, delta, dqkv, colsum, ot, dyt, xt, dqkvt, split, total;
 };
@@ -1512,8 +1562,10 @@ AttnBackwardLayout attn_backward_layout(int nb, int s, int h, int nh) {
     L.xt = align256(L.dyt + sizeof(uint16_t) * lo * h);
     L.dqkvt = align256(L.xt + sizeof(uint16_t) * lq * h);
     L.split = align256(L.dqkvt + sizeof(uint16_t) * lq * 3 * h);
-    const size_t sp = std::max(split_partial_floats(static_cast<int>(T), h, h, 1),
-                               split_partial_floats(static_cast<int>(T), h, 3 * h, 1));
+    size_t sp = std::max(split_partial_floats(static_cast<int>(T), h, h, 1),
+                         split_partial_floats(static_cast<int>(T), h, 3 * h, 1));
+    if (!lo) sp = std::max(sp, weight_split_floats(static_cast<int>(T), h, h));
+    if (!lq) sp = std::max(sp, weight_split_floats(static_cast<int>(T), h, 3LL * h));
     L.total = align256(L.split + sizeof(float) * sp);
     return L;
 }
@@ -1631,7 +1683,8 @@ TPMLP_API int tp_attn_backward(const tpmlp_bf16* dY, const tpmlp_bf16* X, const 
         if (int rc = transpose(O, T, h, Ot, ldT, st)) return rc;
         if (int rc = transpose(dY, T, h, dYt, ldT, st)) return rc;
         if (int rc = dB_kmajor_gemm(Ot, dYt, T, ldT, h, h, 1, dWo, st, d)) return rc;
-    } else if (int rc = dB_gemm(O, dY, T, h, h, 1, dWo, st, d)) {
+    } else if (int rc = dB_gemm(O, dY, T, h, h, 1, dWo, st, d, ws + L.split,
+                                L.total - L.split)) {
         return rc;
     }
     // dO = dY Wo^T: shard i's columns of dO from its rows of Wo, no sum
@@ -1646,7 +1699,8 @@ TPMLP_API int tp_attn_backward(const tpmlp_bf16* dY, const tpmlp_bf16* X, const 
         if (int rc = transpose(X, T, h, Xt, ldT, st)) return rc;
         if (int rc = transpose(dQKV, T, 3 * h, dQKVt, ldT, st)) return rc;
         if (int rc = dA_kmajor_gemm(Xt, dQKVt, T, ldT, h, 3 * h, 1, dWqkv, st, d)) return rc;
-    } else if (int rc = dA_gemm(X, dQKV, T, h, 3 * h, 1, dWqkv, st, d)) {
+    } else if (int rc = dA_gemm(X, dQKV, T, h, 3 * h, 1, dWqkv, st, d, ws + L.split,
+                                L.total - L.split)) {
         return rc;
     }
     // dX = sum_i dQKV_i Wqkv_i^T: the f-operator sum as one accumulation over

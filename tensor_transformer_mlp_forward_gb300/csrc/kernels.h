@@ -39,6 +39,9 @@ cudaError_t launch_dx_partial(const GemmMaps& m, const GemmArgs& g, int grid, bo
 // place (their K-major form from the transposes runs launch_dx).
 cudaError_t launch_weight_grad(const GemmMaps& m, const GemmArgs& g,
                                int grid, bool pair, cudaStream_t st);
+// The same with a split reduction: fp32 partials per k-range split.
+cudaError_t launch_weight_grad_partial(const GemmMaps& m, const GemmArgs& g, int grid, bool pair,
+                                       cudaStream_t st);
 
 // out[c * ld_out + r] = in[r * cols + c], bf16, with each output row zeroed
 // from `rows` to the next multiple of 8 (transpose.cu).  cols % 8 == 0,

@@ -134,6 +134,25 @@ def test_split_workspace_sizes(L):
             >= n + 2 * 512 * 16384)
 
 
+def test_weight_grad_split_workspace(L):
+    # 256 x 256 output tiles of an M x N weight gradient against 76 SM pairs:
+    # dWo at h = 1024 has 16 tiles -> 4 k ranges; dWqkv (1024 x 3072) 48 ->
+    # 3; 64 tiles (h = 1920) or a 2048-token MT-NLG gradient: none
+    assert L.tp_weight_grad_workspace_bytes(8192, 1024, 1024) == 4 * 1024 * 1024 * 4
+    assert L.tp_weight_grad_workspace_bytes(8192, 1024, 3072) == 3 * 1024 * 3072 * 4
+    assert L.tp_weight_grad_workspace_bytes(8192, 1920, 1920) == 0
+    assert L.tp_weight_grad_workspace_bytes(2048, 20480, 81920) == 0
+    assert L.tp_weight_grad_workspace_bytes(256, 1024, 1024) == 0  # 4 k-blocks: too short
+    assert L.tp_weight_grad_workspace_bytes(0, 1024, 1024) == 0
+    # the attention backward workspace holds dWo's and dWqkv's partials
+    assert (L.tp_attn_backward_workspace_bytes(8, 1024, 1024, 16, 2)
+            >= 3 * 1024 * 3072 * 4)
+    assert L.tp_mlp_dA_ws(P, P, 128, 256, 1024, 1, P, Q, 1 << 20, N) == binding.TPMLP_ERR_ALIGN
+    assert L.tp_mlp_dB_ws(P, P, 128, 256, 1024, 1, P, Q, 1 << 20, N) == binding.TPMLP_ERR_ALIGN
+    assert L.tp_mlp_dA_ws(P, P, 128, 256, 1024, 1, N, P, 1 << 20, N) == binding.TPMLP_ERR_NULL
+    assert L.tp_mlp_dB_ws(P, P, 128, 12, 1024, 1, P, P, 1 << 20, N) == binding.TPMLP_ERR_SHAPE
+
+
 def test_scratch_sizes(L):
     assert L.tp_mlp_dgelu_partial_floats(300, 1536) == 4 * 3 * 1536
     assert L.tp_mlp_dgelu_partial_floats(0, 1536) == 0
