@@ -101,9 +101,35 @@ def peaks():
 
 
 # The sources the GEMM kernels and their host-side tile schedule are built
-# from: a recorded DRAM-traffic figure holds while none of them changes.
+# from: a recorded DRAM-traffic figure holds while none of their code
+# changes (comments and blank lines do not count).
 GEMM_SOURCES = ("capi.cu", "gemm.cuh", "gemm_backward_data.cu", "gemm_backward_weight.cu",
                 "gemm_forward.cu", "kernels.h", "philox.cuh", "ptx.cuh")
+
+
+def code_only(text: str) -> str:
+    """C/C++ source without its comments, trailing blanks and blank lines
+    (string and character literals are kept as they are)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = (line.rstrip() for line in "".join(out).split("\n"))
+    return "\n".join(line for line in lines if line)
 
 
 def kernel_source_hash() -> str:
@@ -111,7 +137,7 @@ def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for f in GEMM_SOURCES:
         h.update(f.encode())
-        h.update(open(os.path.join(d, f), "rb").read())
+        h.update(code_only(open(os.path.join(d, f), encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -8,13 +8,15 @@
 //   db[j] = sum_{r < T} G[r * n + j]
 //
 // HBM-bound: 2 bytes read per element.  A 2-D grid of 64-column blocks x
-// row chunks (about 640 CTAs) writes one fp32 partial row per chunk; a
-// second kernel adds the chunks' rows in a fixed order, so the result does
-// not depend on scheduling.
+// row chunks (about 640 CTAs) writes one fp32 partial row per chunk; the
+// last CTA of each column block to finish (counted per launch) adds that
+// block's chunk partials in chunk order, so the result does not depend on
+// which CTA comes last.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 
 #include "kernels.h"
@@ -36,9 +38,10 @@ constexpr int kTargetCtas = 640;
 // 32 KiB per CTA are in flight; the adds stay in row order.  The 4 row
 // phases meet by warp shuffle, the 8 warps in shared memory, in a fixed
 // order.  Writes out[blockIdx.y * n + col].
+template <bool kFinish>
 __global__ void __launch_bounds__(kSumThreads)
     colsum_partial_kernel(const __nv_bfloat16* __restrict__ G, int T, int n, int rows_per_chunk,
-                          float* __restrict__ out) {
+                          float* __restrict__ out, float* __restrict__ db, unsigned int* counts) {
     __shared__ float part[kSumThreads / 32][kColBlock];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int col0 = blockIdx.x * kColBlock + (lane & 7) * 8;
@@ -96,6 +99,64 @@ __global__ void __launch_bounds__(kSumThreads)
         for (int w = 0; w < kSumThreads / 32; ++w) s += part[w][threadIdx.x];
         if (col < n) out[static_cast<long long>(blockIdx.y) * n + col] = s;
     }
+    if constexpr (kFinish) {
+        // the last of the column block's gridDim.y CTAs adds their partial
+        // rows: 4 groups of 64 threads take chunks g, g + 4, ... in order,
+        // then the 4 group sums are added in group order
+        __shared__ bool last;
+        __threadfence();  // this CTA's partial row is visible before it is counted
+        __syncthreads();
+        if (threadIdx.x == 0) last = atomicAdd(&counts[blockIdx.x], 1u) == gridDim.y - 1;
+        __syncthreads();
+        if (!last) return;
+        __threadfence();
+        const int g = threadIdx.x / kColBlock, c = threadIdx.x % kColBlock;
+        const int col = blockIdx.x * kColBlock + c;
+        float s = 0.0f;
+        if (col < n) {
+#pragma unroll 4
+            for (int i = g; i < static_cast<int>(gridDim.y); i += kSumThreads / kColBlock)
+                s += __ldcg(out + static_cast<long long>(i) * n + col);
+        }
+        part[g][c] = s;
+        __syncthreads();
+        if (g == 0 && col < n)
+            db[col] = ((part[0][c] + part[1][c]) + part[2][c]) + part[3][c];
+        if (threadIdx.x == 0) counts[blockIdx.x] = 0u;  // ready for the slot's next launch
+    }
+}
+
+// Completion counts of the one-launch form, one row per launch slot (taken
+// round robin, so launches overlapping on other streams do not share a
+// row while fewer than kCountSlots are in flight); the last CTA of each
+// column block sets its count back to zero.
+constexpr int kCountSlots = 32;
+constexpr int kCountBlocks = 2048;  // column blocks: n <= 131072
+__device__ unsigned int g_colsum_count[kCountSlots][kCountBlocks];
+
+// This launch's row of counts on the current device (the array's address is
+// looked up once per device), or null where that fails: the caller then
+// takes the two-launch form.
+unsigned int* next_count_slot() {
+    constexpr int kMaxDevices = 64;
+    static std::atomic<unsigned int*> base[kMaxDevices];
+    static std::atomic<unsigned> seq{0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    unsigned int* p = base[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        void* q = nullptr;
+        if (cudaGetSymbolAddress(&q, g_colsum_count) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
+        p = static_cast<unsigned int*>(q);
+        base[dev].store(p, std::memory_order_release);
+    }
+    return p + static_cast<size_t>(seq.fetch_add(1u) % kCountSlots) * kCountBlocks;
 }
 
 // out[j] = sum_{i < rows} P[i * n + j].  A 256-thread CTA covers 32 columns:
@@ -149,11 +210,24 @@ cudaError_t launch_colsum(const __nv_bfloat16* G, int T, int n, float* db, float
     const int chunks = colsum_chunks(T, n);
     const int rows_per_chunk = static_cast<int>(cdiv_ll(T, chunks));
     const dim3 grid(static_cast<unsigned>(cdiv_ll(n, kColBlock)), static_cast<unsigned>(chunks));
-    float* out = chunks == 1 ? db : partial;
-    colsum_partial_kernel<<<grid, kSumThreads, 0, st>>>(G, T, n, rows_per_chunk, out);
+    if (chunks == 1) {  // one chunk: its partial row is the result
+        colsum_partial_kernel<false><<<grid, kSumThreads, 0, st>>>(G, T, n, rows_per_chunk, db,
+                                                                  nullptr, nullptr);
+        if (launches) ++*launches;
+        return cudaGetLastError();
+    }
+    unsigned int* counts = grid.x <= static_cast<unsigned>(kCountBlocks) ? next_count_slot() : nullptr;
+    if (counts != nullptr) {
+        colsum_partial_kernel<true><<<grid, kSumThreads, 0, st>>>(G, T, n, rows_per_chunk, partial,
+                                                                 db, counts);
+        if (launches) ++*launches;
+        return cudaGetLastError();
+    }
+    colsum_partial_kernel<false><<<grid, kSumThreads, 0, st>>>(G, T, n, rows_per_chunk, partial,
+                                                              nullptr, nullptr);
     if (launches) ++*launches;
     const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess || chunks == 1) return e;
+    if (e != cudaSuccess) return e;
     return launch_rowsum_f32(partial, chunks, n, db, st, launches);
 }
 

@@ -51,8 +51,10 @@ cudaError_t launch_transpose(const __nv_bfloat16* in, int rows, int cols, __nv_b
 
 // Column sums db[j] = sum_{r < T} G[r * n + j] of a bf16 [T, n] matrix in
 // fp32 (colsum.cu).  With colsum_chunks(T, n) > 1 row chunks the chunks'
-// partial rows go to `partial` (colsum_chunks(T, n) * n floats) and a second
-// launch adds them in chunk order; with one chunk db is written directly.
+// partial rows go to `partial` (colsum_chunks(T, n) * n floats) and are
+// added in chunk order by the last CTA of each column block (by a second
+// launch where n exceeds the completion counters); with one chunk db is
+// written directly.  T == 0 or n == 0 launches nothing.
 int colsum_chunks(int T, int n);
 cudaError_t launch_colsum(const __nv_bfloat16* G, int T, int n, float* db, float* partial,
                           cudaStream_t st, int* launches);
