@@ -146,7 +146,13 @@ size_t tp_mlp_bias_grad_workspace_floats(int T, int n);
 /* a4 (and the reduction of a6): column sums of a [T, n] bf16 matrix,
  * db[j] = sum_r G[r, j], in float32, deterministic.  Used for db2 = sum_rows
  * dY (the g operator is the identity backward, so dY reaches b2 whole).
- * `partial` must hold tp_mlp_bias_grad_workspace_floats(T, n) floats. */
+ * `partial` must hold tp_mlp_bias_grad_workspace_floats(T, n) floats.
+ * One launch: the last CTA of each column block adds the row chunks'
+ * partials, counted in a small array inside the library (32 rows, taken
+ * round robin per call, so up to 32 calls may overlap on other streams).
+ * The first call on each device looks up that array's address: make it
+ * before any stream capture (where the lookup fails, and for n > 131072,
+ * a second kernel adds the partials instead). */
 int tp_mlp_bias_grad(const tpmlp_bf16* G, int T, int n, float* db, float* partial,
                      void* stream);
 
