@@ -12,6 +12,8 @@ also given as % of the measured dense bf16 peak.
     python bench.py [--gpus N --steps K --warmup W] [--workload NAME]
     python bench.py --impl reference ...   # the fp64 CPU oracle, timed on host cores
     python bench.py --sweep                 # one line per sweep point (not the headline)
+    python bench.py --all-configs           # one line per workload family and shard count
+    python bench.py --call dB --shape T,h,F,t [--repeat N] [--vs-cublas]   # one entry point alone
 
 Under torchrun (N > 1) every rank runs an independent replica of the step on
 its own GPU (weak scaling, no collective on the data path); rank 0 prints
@@ -42,6 +44,10 @@ FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
 
 
+CALLS = ("column_gelu", "column_gelu_h_only", "row_sum", "row_sum_dropout", "dgelu", "dx", "dA",
+         "dB", "dA_kmajor", "dB_kmajor", "transpose", "dropout_grad", "ln_forward", "ln_backward")
+
+
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -52,6 +58,9 @@ def parse_args(argv=None):
     p.add_argument("--tokens", type=int, default=None)
     p.add_argument("--shards", type=int, default=None)
     p.add_argument("--sweep", action="store_true")
+    p.add_argument("--all-configs", action="store_true",
+                   help="one line per workload family x shard count (tiny, GPT-2-medium, 8.3B, "
+                        "MT-NLG, every sweep point)")
     p.add_argument("--recompute", action="store_true",
                    help="activation recompute: save only X, rebuild Z and H in the backward pass")
     p.add_argument("--dropout", type=float, default=0.0,
@@ -65,6 +74,15 @@ def parse_args(argv=None):
     p.add_argument("--attn-workload", default="attn-gpt2-8.3b")
     p.add_argument("--pair-mode", type=int, default=None,
                    help="GEMM kernel: 0 single CTA, 1 auto (default), 2 CTA pairs")
+    p.add_argument("--call", choices=CALLS, default=None,
+                   help="run ONE entry point --repeat times at --shape, holding only its operands "
+                        "on the device (the command a profiler wraps to capture one kernel)")
+    p.add_argument("--shape", default="2048,4096,16384,8",
+                   help="T,h,F,t of --call (default: a sweep point under 1 GB on the device)")
+    p.add_argument("--repeat", type=int, default=4)
+    p.add_argument("--vs-cublas", action="store_true",
+                   help="with --call: alternate the call with torch.matmul of the same shapes")
+    p.add_argument("--rounds", type=int, default=8)
     return p.parse_args(argv)
 
 
@@ -399,7 +417,10 @@ def time_ours(w, steps, warmup, local, p_drop=0.0, recompute=False):
     dev_ms = sum(evs[k][0].elapsed_time(evs[k][-1]) for k in range(steps))
     per_call = {name: [evs[k][j].elapsed_time(evs[k][j + 1]) for k in range(steps)]
                 for j, name in enumerate(step.names)}
-    return step, dev_ms / 1e3, wall, per_call, clocks.summary(), launches
+    # the forward pass is a2 + a3 (events 0..2), the backward pass the rest
+    split = {"fwd_ms": statistics.mean(evs[k][0].elapsed_time(evs[k][2]) for k in range(steps)),
+             "bwd_ms": statistics.mean(evs[k][2].elapsed_time(evs[k][-1]) for k in range(steps))}
+    return step, dev_ms / 1e3, wall, per_call, clocks.summary(), launches, split
 
 
 def time_e2e(step, steps, warmup):
@@ -534,8 +555,8 @@ def run_ours(args, w):
     if args.pair_mode is not None:
         binding.set_cta_pair_mode(args.pair_mode)
     rank, world, local = init_distributed(args.gpus)
-    step, dev_s, wall, per_call, clocks, launches = time_ours(w, args.steps, args.warmup, local,
-                                                              args.dropout, args.recompute)
+    step, dev_s, wall, per_call, clocks, launches, split = time_ours(
+        w, args.steps, args.warmup, local, args.dropout, args.recompute)
     flops = w.flops_fwd_bwd()
     max_s, units = reduce_max_sum(dev_s, flops * args.steps)
     value = units / max_s / 1e12
@@ -568,7 +589,10 @@ def run_ours(args, w):
                            "value counts the 12*T*h*F model flops only"} if args.recompute else {})),
         "pct_of_peak": {"burst": 100 * value / world / burst, "sustained": 100 * value / world / sustained,
                         "source": src},
+        "fwd_ms": round(split["fwd_ms"], 4), "bwd_ms": round(split["bwd_ms"], 4),
         "per_call_ms": {k: round(v, 4) for k, v in avg_ms.items()},
+        # db2: the column sums of dY, HBM-bound: 2 T h bytes read, 4 h written
+        "db2_gbs": round((2 * w.T * w.h + 4 * w.h) / (avg_ms["db2"] / 1e3) / 1e9, 1),
         "roofline": roofline,
         "e2e": e2e,
         "clocks": clocks,
@@ -677,6 +701,8 @@ class AttnStep:
                         0 if self.kmajor_o else binding.weight_grad_workspace_bytes(T, h, h),
                         0 if self.kmajor_qkv else binding.weight_grad_workspace_bytes(T, h, 3 * h)),
                     dt=torch.uint8)
+        self.ws_core = e(max(16, int(lib.tp_attn_core_workspace_bytes(w.nb, w.s, h, nh))),
+                         dt=torch.uint8)
         self.launches = 0
         ldT = binding.pitch(T)
         if self.kmajor_o:
@@ -690,7 +716,8 @@ class AttnStep:
         b, i, w = self.b, self.inp, self.w
         calls = (
             lambda: b.tp_attn_qkv(i["X"], i["Wqkv"], i["bqkv"], QKV=self.QKV),
-            lambda: b.tp_attn_core_forward(self.QKV, w.nb, w.nh, O=self.O, lse=self.lse),
+            lambda: b.tp_attn_core_forward(self.QKV, w.nb, w.nh, O=self.O, lse=self.lse,
+                                           workspace=self.ws_core),
             lambda: b.tp_mlp_row_sum(self.O, i["Wo"], i["bo"], i["residual"], w.t, Y=self.Y,
                                      workspace=self.ws),
             lambda: b.tp_mlp_bias_grad(i["dY"], db=self.dbo, partial=self.p_sum),
@@ -706,7 +733,8 @@ class AttnStep:
         calls += (
             lambda: b.tp_mlp_dx(i["dY"], i["Wo"], 1, dX=self.dO, workspace=self.ws),
             lambda: b.tp_attn_core_backward(self.QKV, self.O, self.lse, self.dO, w.nb, w.nh,
-                                            dQKV=self.dQKV, delta=self.delta),
+                                            dQKV=self.dQKV, delta=self.delta,
+                                            workspace=self.ws_core),
             lambda: b.tp_mlp_bias_grad(self.dQKV, db=self.dbqkv, partial=self.p_sum),
         )
         if self.kmajor_qkv:
@@ -819,23 +847,168 @@ def run_attention(args):
     return 0
 
 
+# ----------------------------------------------------------- one call
+
+def run_call(a) -> int:
+    """One entry point of the library, --repeat times at --shape, with only
+    that call's operands on the device (seeded device-side normals: a profile
+    depends on the shapes, not the values).  Prints one JSON line with the
+    CUDA-event time of each call.  With --vs-cublas (column_gelu, dx,
+    dA_kmajor, dB_kmajor) the call and the plain cuBLAS product of the same
+    shapes (torch.matmul, bf16, no epilogue) alternate in rounds of 5 calls,
+    and the line gives both medians."""
+    import torch
+
+    from tensor_transformer_mlp_forward_gb300 import binding as b
+
+    T, h, F, t = (int(v) for v in a.shape.split(","))
+    p_drop = a.dropout if a.dropout > 0 else 0.1
+    dev = torch.device("cuda", 0)
+    gen = torch.Generator(device=dev).manual_seed(1234)
+
+    def bf(*shape, std=1.0):
+        return (torch.randn(*shape, generator=gen, device=dev) * std).to(torch.bfloat16)
+
+    c = a.call
+    ref = None  # the plain cuBLAS product of the call's shapes (--vs-cublas)
+    if c in ("column_gelu", "column_gelu_h_only"):
+        X, A, b1 = bf(T, h), bf(h, F, std=0.02), bf(F, std=0.02)
+        Z = None if c == "column_gelu_h_only" else bf(T, F)
+        H = bf(T, F)
+        fn = lambda: b.tp_mlp_column_gelu(X, A, b1, t, Z=Z, H=H, want_z=Z is not None)  # noqa: E731
+        C = torch.empty(T, F, dtype=torch.bfloat16, device=dev)
+        ref = lambda: torch.matmul(X, A, out=C)  # noqa: E731
+    elif c in ("row_sum", "row_sum_dropout"):
+        H, B, b2, R, Y = bf(T, F), bf(F, h, std=0.02), bf(h, std=0.02), bf(T, h), bf(T, h)
+        ws = torch.empty(max(16, b.split_workspace_bytes(T, h, F, t)), dtype=torch.uint8, device=dev)
+        if c == "row_sum":
+            fn = lambda: b.tp_mlp_row_sum(H, B, b2, R, t, Y=Y, workspace=ws)  # noqa: E731
+        else:
+            fn = lambda: b.tp_mlp_row_sum_dropout(H, B, b2, R, t, p_drop, 7, 0, Y=Y,  # noqa: E731
+                                                  workspace=ws)
+    elif c == "dgelu":
+        dY, B, Z, dZ = bf(T, h), bf(F, h, std=0.02), bf(T, F), bf(T, F)
+        db1 = torch.empty(F, device=dev)
+        part = torch.empty(max(1, int(b.lib().tp_mlp_dgelu_partial_floats(T, F))), device=dev)
+        fn = lambda: b.tp_mlp_dgelu(dY, B, Z, t, dZ=dZ, db1=db1, partial=part)  # noqa: E731
+    elif c == "dx":
+        dZ, A, dX = bf(T, F), bf(h, F, std=0.02), bf(T, h)
+        ws = torch.empty(max(16, b.split_workspace_bytes(T, h, F, t)), dtype=torch.uint8, device=dev)
+        fn = lambda: b.tp_mlp_dx(dZ, A, t, dX=dX, workspace=ws)  # noqa: E731
+        C = torch.empty(T, h, dtype=torch.bfloat16, device=dev)
+        ref = lambda: torch.matmul(dZ, A.t(), out=C)  # noqa: E731
+    elif c == "dA":
+        X, dZ, dA = bf(T, h), bf(T, F), bf(h, F)
+        fn = lambda: b.tp_mlp_dA(X, dZ, t, dA=dA)  # noqa: E731
+    elif c == "dB":
+        H, dY, dB = bf(T, F), bf(T, h), bf(F, h)
+        fn = lambda: b.tp_mlp_dB(H, dY, t, dB=dB)  # noqa: E731
+    elif c == "dA_kmajor":  # from X^T [h, ldT] and dZ^T [F, ldT]
+        ld = b.pitch(T)
+        Xt, dZt, dA = bf(h, ld), bf(F, ld), bf(h, F)
+        fn = lambda: b.tp_mlp_dA_kmajor(Xt, dZt, T, t, dA=dA)  # noqa: E731
+        C = torch.empty(h, F, dtype=torch.bfloat16, device=dev)
+        ref = lambda: torch.matmul(Xt[:, :T], dZt[:, :T].t(), out=C)  # noqa: E731
+    elif c == "dB_kmajor":  # from H^T [F, ldT] and dY^T [h, ldT]
+        ld = b.pitch(T)
+        Ht, dYt, dB = bf(F, ld), bf(h, ld), bf(F, h)
+        fn = lambda: b.tp_mlp_dB_kmajor(Ht, dYt, T, t, dB=dB)  # noqa: E731
+        C = torch.empty(F, h, dtype=torch.bfloat16, device=dev)
+        ref = lambda: torch.matmul(Ht[:, :T], dYt[:, :T].t(), out=C)  # noqa: E731
+    elif c == "transpose":  # dZ [T, F] -> dZ^T [F, ldT]
+        dZ = bf(T, F)
+        dZt = torch.empty(F, b.pitch(T), dtype=torch.bfloat16, device=dev)
+        fn = lambda: b.tp_transpose(dZ, out=dZt)  # noqa: E731
+    elif c == "dropout_grad":
+        dY, dP = bf(T, h), bf(T, h)
+        fn = lambda: b.tp_mlp_dropout_grad(dY, p_drop, 7, 0, dP=dP)  # noqa: E731
+    else:
+        x, r, gam, bet = bf(T, h), bf(T, h), bf(h, std=0.1), bf(h, std=0.1)
+        X, s = torch.empty_like(x), torch.empty_like(x)
+        mean, rstd = torch.empty(T, device=dev), torch.empty(T, device=dev)
+        b.tp_ln_residual_forward(x, r, gam, bet, 1e-5, X=X, s=s, mean=mean, rstd=rstd)
+        if c == "ln_forward":
+            fn = lambda: b.tp_ln_residual_forward(x, r, gam, bet, 1e-5, X=X, s=s,  # noqa: E731
+                                                  mean=mean, rstd=rstd)
+        else:
+            dX, dres, ds = bf(T, h), bf(T, h), torch.empty_like(x)
+            dg, dbt = torch.empty(h, device=dev), torch.empty(h, device=dev)
+            part = torch.empty(max(1, int(b.lib().tp_ln_residual_backward_workspace_floats(T, h))),
+                               device=dev)
+            fn = lambda: b.tp_ln_residual_backward(dX, dres, x, r, gam, mean, rstd, ds=ds,  # noqa: E731
+                                                   dgamma=dg, dbeta=dbt, partial=part)
+    if a.vs_cublas:
+        if ref is None:
+            raise SystemExit(f"--vs-cublas is not defined for {c}")
+        return compare_cublas(c, fn, ref, a, 2.0 * T * h * F)
+    ms = []
+    for _ in range(a.repeat):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    status = b.device_status()
+    print(json.dumps({"call": c, "T": T, "h": h, "F": F, "t": t, "repeat": a.repeat,
+                      "launches_per_call": b.last_launch_count(),
+                      "ms_mean_after_first": sum(ms[1:]) / max(1, len(ms) - 1), "ms": ms,
+                      "device_status": status}))
+    return 0 if status == 0 else 1
+
+
+def compare_cublas(call, fn, ref, a, flops) -> int:
+    """The call and cuBLAS alternating in rounds (the order flips each round),
+    5 calls a round, the first of each round dropped; medians of the rest."""
+    import torch
+
+    from tensor_transformer_mlp_forward_gb300 import binding as b
+
+    for f in (fn, ref, fn, ref):
+        f()
+    torch.cuda.synchronize()
+    res = {"ours": [], "cublas": []}
+    for rnd in range(a.rounds):
+        order = (("ours", fn), ("cublas", ref)) if rnd % 2 == 0 else (("cublas", ref), ("ours", fn))
+        for tag, f in order:
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+            ev[0].record()
+            for k in range(5):
+                f()
+                ev[k + 1].record()
+            torch.cuda.synchronize()
+            res[tag] += [ev[k].elapsed_time(ev[k + 1]) for k in range(1, 5)]
+    mo, mc = statistics.median(res["ours"]), statistics.median(res["cublas"])
+    status = b.device_status()
+    print(json.dumps({"call": call, "ours_ms": mo, "cublas_ms": mc, "ours_over_cublas": mo / mc,
+                      "ours_tflops": flops / mo / 1e9, "cublas_tflops": flops / mc / 1e9,
+                      "samples": len(res["ours"]), "device_status": status}))
+    return 0 if status == 0 else 1
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.call:
+        return run_call(args)
     if args.attention and args.impl == "ours":
         return run_attention(args)
     if args.layernorm:
         return run_layernorm(args, workload(args))
     if args.impl == "reference":
         return run_reference(args)
-    if args.sweep:
+    if args.sweep or args.all_configs:
         from tensor_transformer_mlp_forward_gb300 import inputs
 
-        for T in inputs.SWEEP_TOKENS:
-            for t in inputs.SWEEP_SHARDS:
-                a = parse_args(["--workload", "sweep-h4096", "--tokens", str(T), "--shards", str(t),
-                                "--steps", str(args.steps), "--warmup", str(args.warmup),
-                                "--no-cpu-baseline", "--no-e2e"])
-                run_ours(a, workload(a))
+        points = [("sweep-h4096", T, t) for T in inputs.SWEEP_TOKENS for t in inputs.SWEEP_SHARDS]
+        if args.all_configs:
+            points = [("tiny", 128, 2), ("gpt2-medium", 8192, 1), ("gpt2-medium", 8192, 2)] + [
+                ("megatron-8.3b", 8192, t) for t in (8, 1, 2, 4)] + [
+                ("mt-nlg-530b", 2048, 8)] + points
+        for name, T, t in points:
+            a = parse_args(["--workload", name, "--tokens", str(T), "--shards", str(t),
+                            "--steps", str(args.steps), "--warmup", str(args.warmup),
+                            "--no-cpu-baseline", "--no-e2e"])
+            run_ours(a, workload(a))
         return 0
     return run_ours(args, workload(args))
 

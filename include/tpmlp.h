@@ -38,9 +38,20 @@
  *    CUDA error.  Device-side waits are bounded: a kernel whose wait gives up
  *    records TPMLP_ERR_DEVICE_TIMEOUT in a device status word, which
  *    tpmlp_device_status() reads (synchronously) and clears.
- *  - Thread safety: entry points hold no mutable host state except a
- *    once-per-process lookup of the driver's tensor-map encoder and a
- *    once-per-device kernel attribute setup, both guarded.
+ *  - Thread safety and shared state.  Every scratch word a kernel counts
+ *    or accumulates in is caller memory passed with the call (a workspace,
+ *    cleared on the stream where it must start at zero), so calls on
+ *    different streams or threads, and calls captured into CUDA graphs and
+ *    replayed beside eager calls, share no device state -- except the
+ *    array of tp_mlp_bias_grad_noalloc, which its calls share (see there).
+ *    Process-wide host state: the GEMM kernel mode of
+ *    tpmlp_set_cta_pair_mode (an atomic, read at each launch: change it only
+ *    while no other thread launches, or results stay equal but the launch
+ *    shape may differ between two calls), a once-per-process lookup of the
+ *    driver's tensor-map encoder, once-per-device kernel attributes and
+ *    device addresses (the status word, the no-allocation array), all
+ *    guarded.  The device status word is per device: a timeout recorded by
+ *    one call is read by whichever thread calls tpmlp_device_status next.
  */
 #ifndef TPMLP_H
 #define TPMLP_H
@@ -140,19 +151,17 @@ int tp_mlp_row_sum(const tpmlp_bf16* H, const tpmlp_bf16* B, const tpmlp_bf16* b
                    const tpmlp_bf16* residual, int T, int h, int F, int t, tpmlp_bf16* Y,
                    void* workspace, size_t workspace_bytes, void* stream);
 
-/* Float32 elements of partial-sum scratch tp_mlp_bias_grad needs. */
+/* Float32 elements of scratch tp_mlp_bias_grad needs: the row chunks'
+ * partial sums and one completion count per 64-column block. */
 size_t tp_mlp_bias_grad_workspace_floats(int T, int n);
 
 /* a4 (and the reduction of a6): column sums of a [T, n] bf16 matrix,
  * db[j] = sum_r G[r, j], in float32, deterministic.  Used for db2 = sum_rows
  * dY (the g operator is the identity backward, so dY reaches b2 whole).
- * `partial` must hold tp_mlp_bias_grad_workspace_floats(T, n) floats.
- * One launch: the last CTA of each column block adds the row chunks'
- * partials, counted in a small array inside the library (32 rows, taken
- * round robin per call, so up to 32 calls may overlap on other streams).
- * The first call on each device looks up that array's address: make it
- * before any stream capture (where the lookup fails, and for n > 131072,
- * a second kernel adds the partials instead). */
+ * `partial` must hold tp_mlp_bias_grad_workspace_floats(T, n) floats, any
+ * contents.  One kernel launch (after a small memset of the counts on the
+ * stream): the last CTA of each column block, counted in `partial`, adds the
+ * row chunks' partials in chunk order. */
 int tp_mlp_bias_grad(const tpmlp_bf16* G, int T, int n, float* db, float* partial,
                      void* stream);
 
@@ -164,13 +173,15 @@ int tp_mlp_bias_grad(const tpmlp_bf16* G, int T, int n, float* db, float* partia
  * library (tp_mlp_bias_grad_noalloc_max_floats() floats), so this call
  * allocates nothing; every GPU that loads the library holds that array
  * until the process exits.  Arguments as tp_mlp_bias_grad minus `partial`.
- * Limit: the row-chunk partials, chunks(T, n) * n floats, must fit the
- * array; every n <= 24576 fits at any T, larger shapes may return
+ * Limit: what tp_mlp_bias_grad_workspace_floats(T, n) asks for must fit
+ * the array; every n <= 24576 fits at any T, larger shapes may return
  * TPMLP_ERR_WORKSPACE (nothing launched).  The first call on each device
  * looks up the array's device address: make it before any stream capture.
- * All calls on a device share the array and every call overwrites the part
- * it uses before reading it, so no clearing is needed; calls whose kernels
- * overlap on the GPU (different streams, no ordering) race on it. */
+ * All calls on a device share the array, which keeps what the last call
+ * left there: each call clears the completion counts it needs on its
+ * stream and overwrites the partial rows before reading them, so no result
+ * depends on an earlier call; calls whose kernels overlap on the GPU
+ * (different streams, no ordering) race on it. */
 int tp_mlp_bias_grad_noalloc(const tpmlp_bf16* G, int T, int n, float* db, void* stream);
 
 /* Capacity, in floats, of the array tp_mlp_bias_grad_noalloc uses. */
@@ -428,28 +439,40 @@ int tp_mlp_backward_dropout(const tpmlp_bf16* dY, const tpmlp_bf16* X, const tpm
 int tp_attn_qkv(const tpmlp_bf16* X, const tpmlp_bf16* Wqkv, const tpmlp_bf16* bqkv, int T, int h,
                 tpmlp_bf16* QKV, void* stream);
 
+/* Bytes of scratch the two core calls below need (0 when nb == 0): the
+ * item counters of their persistent kernels, which each call clears on its
+ * stream before its kernels run (contents on entry do not matter). */
+size_t tp_attn_core_workspace_bytes(int nb, int s, int h, int nh);
+
 /* Causal attention of every (sequence, head) from QKV: O [T, h] (bf16) and
  * lse [nh, T] (float32), lse = log2 sum_k 2^(c q.k) over the visible keys
- * with c = log2(e) / sqrt(d), saved for the backward pass. */
+ * with c = log2(e) / sqrt(d), saved for the backward pass.  `workspace`:
+ * device memory of tp_attn_core_workspace_bytes bytes, 16-byte aligned
+ * (TPMLP_ERR_WORKSPACE if NULL or smaller when nb > 0). */
 int tp_attn_core_forward(const tpmlp_bf16* QKV, int nb, int s, int h, int nh, tpmlp_bf16* O,
-                         float* lse, void* stream);
+                         float* lse, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Backward of tp_attn_core_forward given dO [T, h]: dQKV [T, 3h] (bf16;
  * dQ, dK, dV in the layout of QKV).  delta [nh, T] float32 is scratch
- * (rowsum(dO * O) per head).  Every gradient is written once, in a fixed
- * summation order, with no atomics, so results are reproducible. */
+ * (rowsum(dO * O) per head); `workspace` as for tp_attn_core_forward.  Every
+ * gradient is written once, in a fixed summation order, with no atomics, so
+ * results are reproducible. */
 int tp_attn_core_backward(const tpmlp_bf16* QKV, const tpmlp_bf16* O, const float* lse,
                           const tpmlp_bf16* dO, int nb, int s, int h, int nh, tpmlp_bf16* dQKV,
-                          float* delta, void* stream);
+                          float* delta, void* workspace, size_t workspace_bytes, void* stream);
 
-/* Optional scratch of tp_attn_forward: lets the output projection split its
- * reduction when its output tiles cannot occupy the GPU (0 if never). */
+/* Scratch of tp_attn_forward: the core call's counters (required), then
+ * room that lets the output projection split its reduction when its output
+ * tiles cannot occupy the GPU (optional: with fewer bytes it splits less or
+ * not at all).  0 when nb == 0. */
 size_t tp_attn_forward_workspace_bytes(int nb, int s, int h, int nh, int t);
 
 /* The block's forward pass: tp_attn_qkv, tp_attn_core_forward, then the
  * row-parallel output projection (tp_mlp_row_sum with F = h: Y = sum_i O_i
  * Wo_i + bo + residual, the g sum folded into one fp32 accumulator).  QKV, O
- * and lse are outputs saved for the backward pass.  workspace may be NULL. */
+ * and lse are outputs saved for the backward pass.  workspace: at least
+ * tp_attn_core_workspace_bytes bytes when nb > 0 (16-byte aligned), up to
+ * tp_attn_forward_workspace_bytes. */
 int tp_attn_forward(const tpmlp_bf16* X, const tpmlp_bf16* Wqkv, const tpmlp_bf16* bqkv,
                     const tpmlp_bf16* Wo, const tpmlp_bf16* bo, const tpmlp_bf16* residual,
                     int nb, int s, int h, int nh, int t, tpmlp_bf16* Y, tpmlp_bf16* QKV,
@@ -492,6 +515,9 @@ int tp_attn_backward(const tpmlp_bf16* dY, const tpmlp_bf16* X, const tpmlp_bf16
 int tpmlp_set_cta_pair_mode(int mode);
 
 /* Static text for a status code. */
+const char* tp_mlp_status_string(int status);
+
+/* The same function under its earlier name. */
 const char* tpmlp_status_string(int status);
 
 /* The CUDA error code (cudaError_t) behind the last TPMLP_ERR_LAUNCH on the

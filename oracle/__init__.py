@@ -27,13 +27,15 @@ import os
 import numpy as np
 import torch
 
+from . import attn_rows as _attn_rows
 from . import build as _build
 
 class Oracle:
     """Calls into one build of the oracle library (the default one, or a
     mutated copy that the tests compile to check that the pins bite)."""
 
-    def __init__(self, path: str | None = None):
+    def __init__(self, path: str | None = None, attn_rows_impl=None):
+        self._attn_rows = attn_rows_impl or _attn_rows.attn_rows
         L = ctypes.CDLL(path or _build.build())
         dp = ctypes.POINTER(ctypes.c_double)
         up = ctypes.POINTER(ctypes.c_uint16)
@@ -253,6 +255,11 @@ class Oracle:
                "attn_head_grads")
         return dW, db, dWo
 
+    def attn_rows(self, inp: dict, nb: int, nh: int, t: int, rows):
+        """Y[rows] and dX[rows] of the attention block from bf16 CPU tensors
+        (the sampled-row evaluation in attn_rows.py)."""
+        return self._attn_rows(inp, nb, nh, t, rows)
+
     def db2(self, dY) -> np.ndarray:
         """Column sums of dY from a bf16 CPU tensor."""
         T, h = dY.shape
@@ -365,6 +372,10 @@ def attn_head(*a, **k):
 
 def attn_head_grads(*a, **k):
     return default().attn_head_grads(*a, **k)
+
+
+def attn_rows(*a, **k):
+    return default().attn_rows(*a, **k)
 
 
 def ln_forward(*a, **k):

@@ -83,12 +83,14 @@ _SIGNATURES = {
     "tp_ln_residual_backward_workspace_floats": ([_I, _I], _S),
     "tp_ln_residual_backward": ([_P] * 7 + [_I, _I] + [_P] * 4 + [_P], _I),
     "tp_attn_qkv": ([_P] * 3 + [_I] * 2 + [_P, _P], _I),
-    "tp_attn_core_forward": ([_P] + [_I] * 4 + [_P] * 2 + [_P], _I),
-    "tp_attn_core_backward": ([_P] * 4 + [_I] * 4 + [_P] * 2 + [_P], _I),
+    "tp_attn_core_workspace_bytes": ([_I] * 4, _S),
+    "tp_attn_core_forward": ([_P] + [_I] * 4 + [_P] * 2 + [_P, _S, _P], _I),
+    "tp_attn_core_backward": ([_P] * 4 + [_I] * 4 + [_P] * 2 + [_P, _S, _P], _I),
     "tp_attn_forward_workspace_bytes": ([_I] * 5, _S),
     "tp_attn_forward": ([_P] * 6 + [_I] * 5 + [_P] * 4 + [_P, _S, _P], _I),
     "tp_attn_backward_workspace_bytes": ([_I] * 5, _S),
     "tp_attn_backward": ([_P] * 7 + [_I] * 5 + [_P] * 5 + [_P, _S, _P], _I),
+    "tp_mlp_status_string": ([_I], ctypes.c_char_p),
     "tpmlp_status_string": ([_I], ctypes.c_char_p),
     "tpmlp_last_cuda_error": ([], _I),
     "tpmlp_device_status": ([], _I),
@@ -126,7 +128,7 @@ def lib(path: str = LIB_PATH):
 
 
 def status_string(status: int) -> str:
-    return lib().tpmlp_status_string(status).decode()
+    return lib().tp_mlp_status_string(status).decode()
 
 
 def _check(fn: str, status: int):
@@ -377,9 +379,11 @@ def tp_mlp_backward_dropout(dY, X, A, B, Z, H, t: int, p: float, seed: int, offs
 def tp_mlp_bias_grad(G, db=None, partial=None, stream=None):
     T, n = G.shape
     db = _out(db, (n,), G, torch.float32)
+    need = max(1, int(lib().tp_mlp_bias_grad_workspace_floats(T, n)))
     if partial is None:
-        partial = torch.empty(max(1, int(lib().tp_mlp_bias_grad_workspace_floats(T, n))),
-                              dtype=torch.float32, device=G.device)
+        partial = torch.empty(need, dtype=torch.float32, device=G.device)
+    if partial.numel() < need:
+        raise ValueError(f"partial holds {partial.numel()} floats, {need} needed")
     _check("tp_mlp_bias_grad", lib().tp_mlp_bias_grad(
         _ptr(G, "G", (T, n)), T, n, _ptr(db, "db", (n,), torch.float32),
         _ptr(partial, "partial", None, torch.float32), _stream(stream)))
@@ -577,7 +581,7 @@ def tp_attn_qkv(X, Wqkv, bqkv, QKV=None, stream=None):
     return QKV
 
 
-def tp_attn_core_forward(QKV, nb: int, nh: int, O=None, lse=None, stream=None):
+def tp_attn_core_forward(QKV, nb: int, nh: int, O=None, lse=None, workspace=None, stream=None):
     """O [T, h] (bf16) and lse [nh, T] (float32, log2 domain) of causal
     attention over nb sequences of T / nb tokens."""
     T, h3 = QKV.shape
@@ -585,25 +589,28 @@ def tp_attn_core_forward(QKV, nb: int, nh: int, O=None, lse=None, stream=None):
     s = T // nb if nb else 1
     O = _out(O, (T, h), QKV)
     lse = _out(lse, (nh, T), QKV, torch.float32)
+    wp, wn = _workspace(workspace, int(lib().tp_attn_core_workspace_bytes(nb, s, h, nh)), QKV)
     _check("tp_attn_core_forward", lib().tp_attn_core_forward(
         _ptr(QKV, "QKV", (T, 3 * h)) if T else None, nb, s, h, nh,
         _ptr(O, "O", (T, h)) if T else None, _ptr(lse, "lse", (nh, T), torch.float32) if T else None,
-        _stream(stream)))
+        wp, wn, _stream(stream)))
     return O, lse
 
 
-def tp_attn_core_backward(QKV, O, lse, dO, nb: int, nh: int, dQKV=None, delta=None, stream=None):
+def tp_attn_core_backward(QKV, O, lse, dO, nb: int, nh: int, dQKV=None, delta=None,
+                          workspace=None, stream=None):
     """dQKV [T, 3h] of causal attention given dO; delta [nh, T] is scratch."""
     T, h3 = QKV.shape
     h = h3 // 3
     s = T // nb if nb else 1
     dQKV = _out(dQKV, (T, 3 * h), QKV)
     delta = _out(delta, (nh, T), QKV, torch.float32)
+    wp, wn = _workspace(workspace, int(lib().tp_attn_core_workspace_bytes(nb, s, h, nh)), QKV)
     _check("tp_attn_core_backward", lib().tp_attn_core_backward(
         _ptr(QKV, "QKV", (T, 3 * h)), _ptr(O, "O", (T, h)),
         _ptr(lse, "lse", (nh, T), torch.float32), _ptr(dO, "dO", (T, h)), nb, s, h, nh,
         _ptr(dQKV, "dQKV", (T, 3 * h)), _ptr(delta, "delta", (nh, T), torch.float32),
-        _stream(stream)))
+        wp, wn, _stream(stream)))
     return dQKV
 
 

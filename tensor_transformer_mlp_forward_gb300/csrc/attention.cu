@@ -50,7 +50,6 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
-#include <atomic>
 #include <cstdint>
 
 #include "kernels.h"
@@ -188,7 +187,7 @@ struct AttnArgs {
     int nb, s, h, nh;
     long long T;
     int q_tiles;     // work tiles along the sequence (forward: pairs of 128-row tiles)
-    int work_slot;   // this launch's counters in g_work
+    unsigned int* work;  // this launch's item counter, zero at launch (caller memory)
     float scale2;    // log2(e) / sqrt(d)
     float scale;     // 1 / sqrt(d)
     __nv_bfloat16* O;        // forward output [T, h]
@@ -237,14 +236,10 @@ struct FwdCfg {
     }
 };
 
-// Work counters of the persistent kernels.  Each launch gets its own slot
-// (next_work_slot, round robin): CTAs take work items one at a time from
-// g_work[slot][0] (atomicAdd) until it runs past the last item, and the last
-// CTA to finish (counted in g_work[slot][1]) sets both back to zero.  So
-// launches that overlap on the GPU (other streams) do not share counters,
-// as long as fewer than kWorkSlots of them are in flight at once.
-constexpr int kWorkSlots = 256;
-__device__ unsigned int g_work[kWorkSlots][2];
+// Work counters of the persistent kernels: CTAs take work items one at a
+// time from the launch's counter (atomicAdd) until it runs past the last
+// item.  The counter is a word of the caller's workspace that the launcher
+// clears on the stream first, so no two calls share one.
 
 // Work items of the forward kernel: (pair of 128-query tiles, sequence,
 // head), heaviest (most key tiles) first.
@@ -345,7 +340,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     ok = false;
                 int item = -1;
                 if (ok) {
-                    item = static_cast<int>(atomicAdd(&g_work[a.work_slot][0], 1u));
+                    item = static_cast<int>(atomicAdd(a.work, 1u));
                     if (item >= total) item = -1;
                 }
                 items[slot] = item;
@@ -646,15 +641,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
-    // the last CTA out resets the work counters for the next launch
-    if (threadIdx.x == 0) {
-        __threadfence();
-        if (atomicAdd(&g_work[a.work_slot][1], 1u) == gridDim.x - 1) {
-            g_work[a.work_slot][0] = 0u;
-            g_work[a.work_slot][1] = 0u;
-            __threadfence();
-        }
-    }
 }
 
 // ------------------------------------------------------------ delta
@@ -735,7 +721,7 @@ struct DqCfg {
 };
 
 // Work items of the dQ kernel: (128 queries, sequence, head), heaviest
-// (most key tiles) first, taken from the launch's g_work slot.
+// (most key tiles) first, taken in turn from the launch's item counter.
 
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
@@ -832,7 +818,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     ok = false;
                 int item = -1;
                 if (ok) {
-                    item = static_cast<int>(atomicAdd(&g_work[a.work_slot][0], 1u));
+                    item = static_cast<int>(atomicAdd(a.work, 1u));
                     if (item >= total) item = -1;
                 }
                 items[slot] = item;
@@ -1069,15 +1055,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
-    // the last CTA out resets the work counters for the next launch
-    if (threadIdx.x == 0) {
-        __threadfence();
-        if (atomicAdd(&g_work[a.work_slot][1], 1u) == gridDim.x - 1) {
-            g_work[a.work_slot][0] = 0u;
-            g_work[a.work_slot][1] = 0u;
-            __threadfence();
-        }
-    }
 }
 
 // ---------------------------------------------------------- dK, dV
@@ -1094,7 +1071,7 @@ struct DkvCfg {
 };
 
 // Work items of the dK/dV kernel: (128 keys, sequence, head), the first key
-// tiles (most queries after them) first, taken from the launch's g_work slot.
+// tiles (most queries after them) first, taken in turn from the launch's item counter.
 
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
@@ -1205,7 +1182,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     ok = false;
                 int item = -1;
                 if (ok) {
-                    item = static_cast<int>(atomicAdd(&g_work[a.work_slot][0], 1u));
+                    item = static_cast<int>(atomicAdd(a.work, 1u));
                     if (item >= total) item = -1;
                 }
                 items[slot] = item;
@@ -1490,15 +1467,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
-    // the last CTA out resets the work counters for the next launch
-    if (threadIdx.x == 0) {
-        __threadfence();
-        if (atomicAdd(&g_work[a.work_slot][1], 1u) == gridDim.x - 1) {
-            g_work[a.work_slot][0] = 0u;
-            g_work[a.work_slot][1] = 0u;
-            __threadfence();
-        }
-    }
 }
 
 }  // namespace
@@ -1506,12 +1474,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 // ------------------------------------------------------------- launchers
 
 namespace {
-// The g_work slot of the next persistent launch (round robin).
-int next_work_slot() {
-    static std::atomic<unsigned> seq{0};
-    return static_cast<int>(seq.fetch_add(1u, std::memory_order_relaxed) % kWorkSlots);
-}
-
 // CTAs of a persistent attention kernel: one per SM at most.
 unsigned persistent_grid(unsigned items) {
     static int sms = 0;
@@ -1538,8 +1500,9 @@ cudaError_t launch_attn_forward(const CUtensorMap& tm_qkv128, const CUtensorMap&
     a.status = p.status;
     // persistent: items (query-tile pairs x sequences x heads) taken in turn
     const unsigned grid = persistent_grid(static_cast<unsigned>(a.q_tiles * p.nb * p.nh));
-    a.work_slot = next_work_slot();
-    cudaError_t e = cudaSuccess;
+    a.work = p.work;
+    cudaError_t e = cudaMemsetAsync(p.work, 0, sizeof(unsigned int), st);
+    if (e != cudaSuccess) return e;
 #define TPMLP_ATTN_FWD(DD)                                                                        \
     if (d == DD) {                                                                                \
         auto kern = attn_fwd_kernel<DD>;                                                          \
@@ -1595,8 +1558,10 @@ cudaError_t launch_attn_backward(const CUtensorMap& tm_qkv128, const CUtensorMap
     const int q_tiles = (p.s + 127) / 128;
     AttnArgs aq = a;
     aq.q_tiles = q_tiles;
-    aq.work_slot = next_work_slot();
-    a.work_slot = next_work_slot();
+    aq.work = p.work;      // the dQ kernel's item counter
+    a.work = p.work + 1;   // the dK/dV kernel's
+    e = cudaMemsetAsync(p.work, 0, 2 * sizeof(unsigned int), st);
+    if (e != cudaSuccess) return e;
     // the dQ and dK/dV kernels are persistent: one CTA per SM at most, items
     // taken in turn (both have q_tiles x nb x nh items)
     const unsigned dq_grid = persistent_grid(static_cast<unsigned>(q_tiles * p.nb * p.nh));

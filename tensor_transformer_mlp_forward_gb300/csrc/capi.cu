@@ -871,7 +871,7 @@ BackwardLayout backward_layout(int T, int h, int F, int t) {
     L.dz = 0;
     L.colsum = align256(L.dz + sizeof(uint16_t) * static_cast<size_t>(T) * F);
     L.db2 = align256(L.colsum + sizeof(float) * dgelu_partial_floats(T, F));
-    const size_t db2_floats = static_cast<size_t>(colsum_chunks(T, h)) * h;
+    const size_t db2_floats = colsum_workspace_floats(T, h);
     // the transposes only where a8 and a9 take the K-major form
     const size_t ldT = kmajor_weight_grad(h, F) ? static_cast<size_t>(pitch_of(T)) : 0;
     L.xt = align256(L.db2 + sizeof(float) * db2_floats);
@@ -948,7 +948,7 @@ TPMLP_API int tp_mlp_forward(const tpmlp_bf16* X, const tpmlp_bf16* A, const tpm
 
 TPMLP_API size_t tp_mlp_bias_grad_workspace_floats(int T, int n) {
     if (T < 0 || n < 1) return 0;
-    return static_cast<size_t>(colsum_chunks(T, n)) * static_cast<size_t>(n);
+    return colsum_workspace_floats(T, n);
 }
 
 TPMLP_API int tp_mlp_bias_grad(const tpmlp_bf16* G, int T, int n, float* db, float* partial,
@@ -1011,8 +1011,10 @@ TPMLP_API int tp_mlp_bias_grad_noalloc(const tpmlp_bf16* G, int T, int n, float*
     if (any_null(db) || (T > 0 && any_null(G))) return TPMLP_ERR_NULL;
     if (!all_aligned(G, db)) return TPMLP_ERR_ALIGN;
     // Same row chunks as tp_mlp_bias_grad; one chunk needs no partials.
-    const int chunks = T == 0 ? 1 : colsum_chunks(T, n);
-    if (chunks > 1 && static_cast<long long>(chunks) * n > kNoAllocScratchFloats)
+    // The completion counts inside the array are cleared on the stream
+    // before each use, so nothing carries over from an earlier call.
+    if (T > 0 && colsum_chunks(T, n) > 1 &&
+        colsum_workspace_floats(T, n) > static_cast<size_t>(kNoAllocScratchFloats))
         return TPMLP_ERR_WORKSPACE;
     DeviceInfo d;
     if (int rc = enter(d)) return rc;
@@ -1500,8 +1502,12 @@ int qkv_gemm(const tpmlp_bf16* X, const tpmlp_bf16* W, const tpmlp_bf16* b, int 
     return run_gemm(launch_column_bias, a, bb, o, g, sh, st, d);
 }
 
+// Bytes of caller memory that hold the persistent attention kernels' item
+// counters (cleared on the stream by each call, so calls share nothing).
+constexpr size_t kAttnCoreWorkBytes = 256;
+
 int attn_core_forward(const tpmlp_bf16* QKV, int nb, int s, int h, int nh, tpmlp_bf16* O,
-                      float* lse, cudaStream_t st, const DeviceInfo& d) {
+                      float* lse, void* work, cudaStream_t st, const DeviceInfo& d) {
     CUtensorMap tm, tm64;
     if (int rc = make_seq_map(&tm, QKV, nb, s, 3LL * h, 128)) return rc;
     if (int rc = make_seq_map(&tm64, QKV, nb, s, 3LL * h, 64)) return rc;
@@ -1509,6 +1515,7 @@ int attn_core_forward(const tpmlp_bf16* QKV, int nb, int s, int h, int nh, tpmlp
     p.nb = nb; p.s = s; p.h = h; p.nh = nh;
     p.O = reinterpret_cast<__nv_bfloat16*>(O);
     p.lse = lse;
+    p.work = static_cast<unsigned int*>(work);
     p.status = d.status;
     cudaError_t e = launch_attn_forward(tm, tm64, h / nh, p, st, &t_last_launches);
     return e == cudaSuccess ? TPMLP_OK : fail_cuda(e);
@@ -1516,7 +1523,7 @@ int attn_core_forward(const tpmlp_bf16* QKV, int nb, int s, int h, int nh, tpmlp
 
 int attn_core_backward(const tpmlp_bf16* QKV, const tpmlp_bf16* O, const float* lse,
                        const tpmlp_bf16* dO, int nb, int s, int h, int nh, tpmlp_bf16* dQKV,
-                       float* delta, cudaStream_t st, const DeviceInfo& d) {
+                       float* delta, void* work, cudaStream_t st, const DeviceInfo& d) {
     CUtensorMap q128, q64, do128, do64;
     if (int rc = make_seq_map(&q128, QKV, nb, s, 3LL * h, 128)) return rc;
     if (int rc = make_seq_map(&q64, QKV, nb, s, 3LL * h, 64)) return rc;
@@ -1529,14 +1536,14 @@ int attn_core_backward(const tpmlp_bf16* QKV, const tpmlp_bf16* O, const float* 
     p.lse_in = lse;
     p.delta_out = delta;
     p.dqkv = reinterpret_cast<__nv_bfloat16*>(dQKV);
+    p.work = static_cast<unsigned int*>(work);
     p.status = d.status;
     cudaError_t e = launch_attn_backward(q128, q64, do128, do64, h / nh, p, st, &t_last_launches);
     return e == cudaSuccess ? TPMLP_OK : fail_cuda(e);
 }
 
 size_t attn_colsum_floats(int T, int h) {
-    return std::max(static_cast<size_t>(colsum_chunks(T, h)) * h,
-                    static_cast<size_t>(colsum_chunks(T, 3 * h)) * 3 * h);
+    return std::max(colsum_workspace_floats(T, h), colsum_workspace_floats(T, 3 * h));
 }
 
 // Attention backward workspace: dO, delta, dQKV, the column-sum partials,
@@ -1544,13 +1551,14 @@ size_t attn_colsum_floats(int T, int h) {
 // those take the K-major form, and the split-reduction scratch (the
 // row-parallel GEMMs' and, where dWo or dWqkv is split, its partials).
 struct AttnBackwardLayout {
-    size_t dO, delta, dqkv, colsum, ot, dyt, xt, dqkvt, split, total;
+    size_t work, dO, delta, dqkv, colsum, ot, dyt, xt, dqkvt, split, total;
 };
 
 AttnBackwardLayout attn_backward_layout(int nb, int s, int h, int nh) {
     const long long T = 1LL * nb * s;
     AttnBackwardLayout L;
-    L.dO = 0;
+    L.work = 0;
+    L.dO = kAttnCoreWorkBytes;
     L.delta = align256(L.dO + sizeof(uint16_t) * static_cast<size_t>(T) * h);
     L.dqkv = align256(L.delta + sizeof(float) * static_cast<size_t>(T) * nh);
     L.colsum = align256(L.dqkv + sizeof(uint16_t) * static_cast<size_t>(T) * 3 * h);
@@ -1584,33 +1592,45 @@ TPMLP_API int tp_attn_qkv(const tpmlp_bf16* X, const tpmlp_bf16* Wqkv, const tpm
     return qkv_gemm(X, Wqkv, bqkv, T, h, QKV, static_cast<cudaStream_t>(stream), d);
 }
 
+TPMLP_API size_t tp_attn_core_workspace_bytes(int nb, int s, int h, int nh) {
+    if (check_attn(nb, s, h, nh, 1) || nb == 0) return 0;
+    return kAttnCoreWorkBytes;
+}
+
 TPMLP_API int tp_attn_core_forward(const tpmlp_bf16* QKV, int nb, int s, int h, int nh,
-                                   tpmlp_bf16* O, float* lse, void* stream) {
+                                   tpmlp_bf16* O, float* lse, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
     TPMLP_PROLOGUE(check_attn(nb, s, h, nh, 1));
     if (nb == 0) return TPMLP_OK;
     if (any_null(QKV, O, lse)) return TPMLP_ERR_NULL;
-    if (!all_aligned(QKV, O, lse)) return TPMLP_ERR_ALIGN;
+    if (workspace == nullptr || workspace_bytes < kAttnCoreWorkBytes) return TPMLP_ERR_WORKSPACE;
+    if (!all_aligned(QKV, O, lse, workspace)) return TPMLP_ERR_ALIGN;
     DeviceInfo d;
     if (int rc = enter(d)) return rc;
-    return attn_core_forward(QKV, nb, s, h, nh, O, lse, static_cast<cudaStream_t>(stream), d);
+    return attn_core_forward(QKV, nb, s, h, nh, O, lse, workspace,
+                             static_cast<cudaStream_t>(stream), d);
 }
 
 TPMLP_API int tp_attn_core_backward(const tpmlp_bf16* QKV, const tpmlp_bf16* O, const float* lse,
                                     const tpmlp_bf16* dO, int nb, int s, int h, int nh,
-                                    tpmlp_bf16* dQKV, float* delta, void* stream) {
+                                    tpmlp_bf16* dQKV, float* delta, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
     TPMLP_PROLOGUE(check_attn(nb, s, h, nh, 1));
     if (nb == 0) return TPMLP_OK;
     if (any_null(QKV, O, lse, dO, dQKV, delta)) return TPMLP_ERR_NULL;
-    if (!all_aligned(QKV, O, lse, dO, dQKV, delta)) return TPMLP_ERR_ALIGN;
+    if (workspace == nullptr || workspace_bytes < kAttnCoreWorkBytes) return TPMLP_ERR_WORKSPACE;
+    if (!all_aligned(QKV, O, lse, dO, dQKV, delta, workspace)) return TPMLP_ERR_ALIGN;
     DeviceInfo d;
     if (int rc = enter(d)) return rc;
-    return attn_core_backward(QKV, O, lse, dO, nb, s, h, nh, dQKV, delta,
+    return attn_core_backward(QKV, O, lse, dO, nb, s, h, nh, dQKV, delta, workspace,
                               static_cast<cudaStream_t>(stream), d);
 }
 
+// tp_attn_forward's workspace: the core kernel's item counter, then the
+// output projection's split-reduction scratch.
 TPMLP_API size_t tp_attn_forward_workspace_bytes(int nb, int s, int h, int nh, int t) {
     if (check_attn(nb, s, h, nh, t) || nb == 0) return 0;
-    return sizeof(float) * split_partial_floats(nb * s, h, h, t);
+    return kAttnCoreWorkBytes + sizeof(float) * split_partial_floats(nb * s, h, h, t);
 }
 
 TPMLP_API int tp_attn_forward(const tpmlp_bf16* X, const tpmlp_bf16* Wqkv, const tpmlp_bf16* bqkv,
@@ -1621,17 +1641,20 @@ TPMLP_API int tp_attn_forward(const tpmlp_bf16* X, const tpmlp_bf16* Wqkv, const
     TPMLP_PROLOGUE(check_attn(nb, s, h, nh, t));
     if (nb == 0) return TPMLP_OK;
     if (any_null(X, Wqkv, bqkv, Wo, bo, residual, Y, QKV, O, lse)) return TPMLP_ERR_NULL;
+    if (workspace == nullptr || workspace_bytes < kAttnCoreWorkBytes) return TPMLP_ERR_WORKSPACE;
     if (!all_aligned(X, Wqkv, bqkv, Wo, bo, residual, Y, QKV, O, lse, workspace))
         return TPMLP_ERR_ALIGN;
     DeviceInfo d;
     if (int rc = enter(d)) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int T = nb * s;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
     if (int rc = qkv_gemm(X, Wqkv, bqkv, T, h, QKV, st, d)) return rc;
-    if (int rc = attn_core_forward(QKV, nb, s, h, nh, O, lse, st, d)) return rc;
+    if (int rc = attn_core_forward(QKV, nb, s, h, nh, O, lse, ws, st, d)) return rc;
     // row-parallel output projection: Y = sum_i O_i Wo_i + bo + residual, the
     // g-operator sum folded into one accumulator (the MLP's a3 GEMM with F = h)
-    return row_sum(O, Wo, bo, residual, T, h, h, t, Y, workspace, workspace_bytes, st, d);
+    return row_sum(O, Wo, bo, residual, T, h, h, t, Y, ws + kAttnCoreWorkBytes,
+                   workspace_bytes - kAttnCoreWorkBytes, st, d);
 }
 
 TPMLP_API size_t tp_attn_backward_workspace_bytes(int nb, int s, int h, int nh, int t) {
@@ -1690,7 +1713,8 @@ TPMLP_API int tp_attn_backward(const tpmlp_bf16* dY, const tpmlp_bf16* X, const 
     // dO = dY Wo^T: shard i's columns of dO from its rows of Wo, no sum
     if (int rc = dx_gemm(dY, Wo, T, h, h, 1, dO, ws + L.split, L.total - L.split, st, d)) return rc;
     // local attention backward of every head
-    if (int rc = attn_core_backward(QKV, O, lse, dO, nb, s, h, nh, dQKV, delta, st, d)) return rc;
+    if (int rc = attn_core_backward(QKV, O, lse, dO, nb, s, h, nh, dQKV, delta, ws + L.work, st, d))
+        return rc;
     // dbqkv = sum_rows dQKV ; dWqkv = X^T dQKV (column blocks per shard)
     if (int rc = bias_grad(dQKV, T, 3 * h, dbqkv, colsum, st)) return rc;
     if (kmajor_weight_grad(h, 3LL * h)) {
@@ -1708,7 +1732,7 @@ TPMLP_API int tp_attn_backward(const tpmlp_bf16* dY, const tpmlp_bf16* X, const 
     return dx_gemm(dQKV, Wqkv, T, h, 3 * h, 1, dX, ws + L.split, L.total - L.split, st, d);
 }
 
-TPMLP_API const char* tpmlp_status_string(int status) {
+TPMLP_API const char* tp_mlp_status_string(int status) {
     switch (status) {
         case TPMLP_OK: return "ok";
         case TPMLP_ERR_NULL: return "a required pointer is NULL";
@@ -1721,6 +1745,8 @@ TPMLP_API const char* tpmlp_status_string(int status) {
         default: return "unknown status";
     }
 }
+
+TPMLP_API const char* tpmlp_status_string(int status) { return tp_mlp_status_string(status); }
 
 TPMLP_API int tpmlp_set_cta_pair_mode(int mode) {
     if (mode < 0 || mode > 2) return -1;

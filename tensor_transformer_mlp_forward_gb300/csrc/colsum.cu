@@ -9,14 +9,13 @@
 //
 // HBM-bound: 2 bytes read per element.  A 2-D grid of 64-column blocks x
 // row chunks (about 640 CTAs) writes one fp32 partial row per chunk; the
-// last CTA of each column block to finish (counted per launch) adds that
-// block's chunk partials in chunk order, so the result does not depend on
-// which CTA comes last.
+// last CTA of each column block to finish (counted in the caller's
+// workspace, cleared before the launch) adds that block's chunk partials in
+// chunk order, so the result does not depend on which CTA comes last.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <atomic>
 #include <cstdint>
 
 #include "kernels.h"
@@ -122,41 +121,7 @@ __global__ void __launch_bounds__(kSumThreads)
         __syncthreads();
         if (g == 0 && col < n)
             db[col] = ((part[0][c] + part[1][c]) + part[2][c]) + part[3][c];
-        if (threadIdx.x == 0) counts[blockIdx.x] = 0u;  // ready for the slot's next launch
     }
-}
-
-// Completion counts of the one-launch form, one row per launch slot (taken
-// round robin, so launches overlapping on other streams do not share a
-// row while fewer than kCountSlots are in flight); the last CTA of each
-// column block sets its count back to zero.
-constexpr int kCountSlots = 32;
-constexpr int kCountBlocks = 2048;  // column blocks: n <= 131072
-__device__ unsigned int g_colsum_count[kCountSlots][kCountBlocks];
-
-// This launch's row of counts on the current device (the array's address is
-// looked up once per device), or null where that fails: the caller then
-// takes the two-launch form.
-unsigned int* next_count_slot() {
-    constexpr int kMaxDevices = 64;
-    static std::atomic<unsigned int*> base[kMaxDevices];
-    static std::atomic<unsigned> seq{0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-        (void)cudaGetLastError();
-        return nullptr;
-    }
-    unsigned int* p = base[dev].load(std::memory_order_acquire);
-    if (p == nullptr) {
-        void* q = nullptr;
-        if (cudaGetSymbolAddress(&q, g_colsum_count) != cudaSuccess) {
-            (void)cudaGetLastError();
-            return nullptr;
-        }
-        p = static_cast<unsigned int*>(q);
-        base[dev].store(p, std::memory_order_release);
-    }
-    return p + static_cast<size_t>(seq.fetch_add(1u) % kCountSlots) * kCountBlocks;
 }
 
 // out[j] = sum_{i < rows} P[i * n + j].  A 256-thread CTA covers 32 columns:
@@ -194,6 +159,15 @@ int colsum_chunks(int T, int n) {
     return static_cast<int>(std::max<long long>(1, r));
 }
 
+size_t colsum_workspace_floats(int T, int n) {
+    const int chunks = colsum_chunks(T, n);
+    const size_t rows = static_cast<size_t>(chunks) * static_cast<size_t>(n);
+    if (chunks == 1) return rows;
+    // the completion counts (one 32-bit word per column block) follow the
+    // partial rows, padded to 16 bytes
+    return rows + ((static_cast<size_t>(cdiv_ll(n, kColBlock)) + 3) & ~static_cast<size_t>(3));
+}
+
 cudaError_t launch_rowsum_f32(const float* P, int rows, int n, float* out, cudaStream_t st,
                               int* launches) {
     if (n == 0) return cudaSuccess;
@@ -203,7 +177,11 @@ cudaError_t launch_rowsum_f32(const float* P, int rows, int n, float* out, cudaS
     return cudaGetLastError();
 }
 
-// T == 0 or n == 0 launches nothing and leaves db as it was.
+// T == 0 or n == 0 launches nothing and leaves db as it was.  With more than
+// one row chunk, `partial` holds colsum_workspace_floats(T, n) floats: the
+// chunks' partial rows, then the column blocks' completion counts, which are
+// cleared on the stream before the kernel runs, so the workspace may hold
+// anything on entry and no state is shared between calls.
 cudaError_t launch_colsum(const __nv_bfloat16* G, int T, int n, float* db, float* partial,
                           cudaStream_t st, int* launches) {
     if (T == 0 || n == 0) return cudaSuccess;
@@ -216,19 +194,14 @@ cudaError_t launch_colsum(const __nv_bfloat16* G, int T, int n, float* db, float
         if (launches) ++*launches;
         return cudaGetLastError();
     }
-    unsigned int* counts = grid.x <= static_cast<unsigned>(kCountBlocks) ? next_count_slot() : nullptr;
-    if (counts != nullptr) {
-        colsum_partial_kernel<true><<<grid, kSumThreads, 0, st>>>(G, T, n, rows_per_chunk, partial,
-                                                                 db, counts);
-        if (launches) ++*launches;
-        return cudaGetLastError();
-    }
-    colsum_partial_kernel<false><<<grid, kSumThreads, 0, st>>>(G, T, n, rows_per_chunk, partial,
-                                                              nullptr, nullptr);
-    if (launches) ++*launches;
-    const cudaError_t e = cudaGetLastError();
+    unsigned int* counts =
+        reinterpret_cast<unsigned int*>(partial + static_cast<size_t>(chunks) * static_cast<size_t>(n));
+    cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(unsigned int) * grid.x, st);
     if (e != cudaSuccess) return e;
-    return launch_rowsum_f32(partial, chunks, n, db, st, launches);
+    colsum_partial_kernel<true><<<grid, kSumThreads, 0, st>>>(G, T, n, rows_per_chunk, partial, db,
+                                                             counts);
+    if (launches) ++*launches;
+    return cudaGetLastError();
 }
 
 }  // namespace tpmlp

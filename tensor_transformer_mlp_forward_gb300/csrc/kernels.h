@@ -50,12 +50,14 @@ cudaError_t launch_transpose(const __nv_bfloat16* in, int rows, int cols, __nv_b
                              int ld_out, cudaStream_t st, int* launches);
 
 // Column sums db[j] = sum_{r < T} G[r * n + j] of a bf16 [T, n] matrix in
-// fp32 (colsum.cu).  With colsum_chunks(T, n) > 1 row chunks the chunks'
-// partial rows go to `partial` (colsum_chunks(T, n) * n floats) and are
-// added in chunk order by the last CTA of each column block (by a second
-// launch where n exceeds the completion counters); with one chunk db is
-// written directly.  T == 0 or n == 0 launches nothing.
+// fp32 (colsum.cu), one kernel launch.  With colsum_chunks(T, n) > 1 row
+// chunks the chunks' partial rows go to `partial` and are added in chunk
+// order by the last CTA of each column block, counted in words of `partial`
+// after the rows that a memset on the stream clears first; `partial` holds
+// colsum_workspace_floats(T, n) floats, 16-byte aligned, any contents.  With
+// one chunk db is written directly.  T == 0 or n == 0 launches nothing.
 int colsum_chunks(int T, int n);
+size_t colsum_workspace_floats(int T, int n);
 cudaError_t launch_colsum(const __nv_bfloat16* G, int T, int n, float* db, float* partial,
                           cudaStream_t st, int* launches);
 // out[j] = sum_{i < rows} P[i * n + j] for an fp32 [rows, n] matrix (colsum.cu).
@@ -89,6 +91,8 @@ struct AttnParams {
     const float* lse_in;         // backward: the forward's lse
     float* delta_out;            // backward: rowsum(dO * O) scratch [nh, T]
     __nv_bfloat16* dqkv;         // backward: output [T, 3h]
+    unsigned int* work;          // item counters of the persistent kernels (forward 1 word,
+                                 // backward 2), caller memory, cleared by the launcher
     int* status;
 };
 cudaError_t launch_attn_forward(const CUtensorMap& tm_qkv128, const CUtensorMap& tm_qkv64, int d,

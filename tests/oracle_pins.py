@@ -528,6 +528,27 @@ def pin_attn_sampled_matches_full(o) -> bool:
     return bool(ok)
 
 
+def pin_attn_rows_match_full(o) -> bool:
+    """Sampled rows of Y and dX (bf16 inputs, several sequences, shards and
+    heads, rows early and late in their sequences) against the full block."""
+    rng = np.random.default_rng(77)
+    ok = True
+    for nb, s, h, nh, t, rows in ((2, 6, 16, 4, 2, [0, 5, 6, 11]), (3, 9, 24, 6, 3, [4, 17, 26]),
+                                  (1, 7, 8, 1, 1, [6]), (2, 5, 12, 3, 1, [])):
+        bf = lambda *sh: torch.from_numpy(0.5 * rng.standard_normal(sh)).to(torch.bfloat16)  # noqa: E731
+        inp = dict(X=bf(nb * s, h), Wqkv=bf(h, 3 * h), bqkv=bf(3 * h), Wo=bf(h, h), bo=bf(h),
+                   residual=bf(nb * s, h), dY=bf(nb * s, h))
+        f = {k: v.double().numpy() for k, v in inp.items()}
+        Y, _, _ = o.attn_forward(f["X"], f["Wqkv"], f["bqkv"], f["Wo"], f["bo"], f["residual"],
+                                 nb, nh, t)
+        dX = o.attn_backward(f["dY"], f["X"], f["Wqkv"], f["bqkv"], f["Wo"], nb, nh, t)[0]
+        Yr, dXr = o.attn_rows(inp, nb, nh, t, rows)
+        ok &= Yr.shape == (len(rows), h) and dXr.shape == (len(rows), h)
+        if rows:
+            ok &= _rel(Yr, Y[rows]) < 1e-12 and _rel(dXr, dX[rows]) < 1e-12
+    return bool(ok)
+
+
 ALL_PINS = [
     pin_gelu_identities,
     pin_gelu_asymptotes,
@@ -553,6 +574,7 @@ ALL_PINS = [
     pin_attn_partition_invariant,
     pin_attn_gradients_fd,
     pin_attn_sampled_matches_full,
+    pin_attn_rows_match_full,
 ]
 
 

@@ -168,6 +168,41 @@ def test_attention_kernels_on_two_streams():
             assert torch.equal(dQKV, ref[i][2])
 
 
+def test_attention_graph_replays_beside_eager_calls():
+    """A CUDA graph of the core forward and backward, replayed while the same
+    calls run eagerly on another stream: each call takes its work items from
+    the counters of its own workspace, so every result is the lone call's."""
+    nb, s, h, nh = 2, 384, 512, 4
+    g = torch.Generator(device="cuda").manual_seed(43)
+    QKV = (torch.randn(nb * s, 3 * h, generator=g, device="cuda") * 0.5).to(torch.bfloat16)
+    dO = torch.randn(nb * s, h, generator=g, device="cuda").to(torch.bfloat16)
+    O_ref, lse_ref = binding.tp_attn_core_forward(QKV, nb, nh)
+    dQKV_ref = binding.tp_attn_core_backward(QKV, O_ref, lse_ref, dO, nb, nh)
+    O_g, lse_g = torch.empty_like(O_ref), torch.empty_like(lse_ref)
+    dQKV_g, delta_g = torch.empty_like(dQKV_ref), torch.empty_like(lse_ref)
+    ws_g = torch.empty(int(binding.lib().tp_attn_core_workspace_bytes(nb, s, h, nh)),
+                       dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        binding.tp_attn_core_forward(QKV, nb, nh, O=O_g, lse=lse_g, workspace=ws_g)
+        binding.tp_attn_core_backward(QKV, O_g, lse_g, dO, nb, nh, dQKV=dQKV_g, delta=delta_g,
+                                      workspace=ws_g)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    eager = []
+    for _ in range(4):
+        graph.replay()
+        with torch.cuda.stream(side):
+            O, lse = binding.tp_attn_core_forward(QKV, nb, nh)
+            eager.append((O, binding.tp_attn_core_backward(QKV, O, lse, dO, nb, nh)))
+        torch.cuda.synchronize()
+        assert torch.equal(O_g, O_ref) and torch.equal(dQKV_g, dQKV_ref)
+    assert binding.device_status() == 0
+    for O, dQKV in eager:
+        assert torch.equal(O, O_ref) and torch.equal(dQKV, dQKV_ref)
+
+
 FULL = [inputs.ATTN_GPT2_355M, inputs.ATTN_GPT2_8_3B, inputs.ATTN_MTNLG_530B,
         # h = 12288: dWo and dWqkv from transposed operands, T = 130 ragged
         # (weights drawn as for the MT-NLG block, which has h of this order)
@@ -175,13 +210,42 @@ FULL = [inputs.ATTN_GPT2_355M, inputs.ATTN_GPT2_8_3B, inputs.ATTN_MTNLG_530B,
                            std=inputs.ATTN_MTNLG_530B.std, name="attn-kmajor-ragged")]
 
 
+def attn_sample_rows(w: inputs.AttnWorkload, total: int = 36) -> np.ndarray:
+    """Token rows for the Y / dX comparison: in the first, a middle and the
+    last sequence, the first and the last position, one position in each of
+    evenly spread 128-token bands (the query and key tiles of the attention
+    kernels), and random positions, about `total` rows in all."""
+    g = np.random.default_rng(w.seed + 5)
+    seqs = sorted({0, w.nb // 2, w.nb - 1})
+    per_seq = min(w.s, max(3, total // len(seqs)))
+    bands = (w.s + 127) // 128
+    rows = set()
+    for n in seqs:
+        pick = np.unique(np.linspace(0, bands - 1, min(bands, per_seq - 2)).round().astype(int))
+        pos = {0, w.s - 1} | {int(g.integers(128 * b, min(w.s, 128 * b + 128))) for b in pick}
+        while len(pos) < per_seq:
+            pos.add(int(g.integers(0, w.s)))
+        rows |= {n * w.s + p for p in pos}
+    return np.array(sorted(rows), dtype=np.int64)
+
+
 @pytest.mark.parametrize("w", FULL, ids=lambda w: w.name)
 def test_attention_full_size_sampled_heads(w):
-    """Full-size block in the bench's configuration; the oracle recomputes
-    two heads (the first and the last) from the bf16 inputs: their O columns
-    and their dWqkv columns, dbqkv entries and dWo rows."""
+    """Full-size block in the bench's configuration.  The oracle recomputes
+    sampled token rows of Y (the g sum over every head's output plus bo and
+    the residual) and of dX (the f sum over the Q, K and V shards of every
+    head), evaluating the whole block on each sequence that holds a sampled
+    row; and two heads (the first and the last) from the bf16 inputs: their O
+    columns and their dWqkv columns, dbqkv entries and dWo rows."""
     cpu = inputs.make_attn_inputs(w)
     out = run_gpu(w, cpu)
+    rows = attn_sample_rows(w)
+    Yr, dXr = oracle.attn_rows(cpu, w.nb, w.nh, w.t, rows)
+    ri = torch.as_tensor(rows, device="cuda")
+    e = rel(np64(out["Y"][ri]), Yr)
+    assert e <= TOL_FWD, ("Y", e)
+    e = rel(np64(out["dX"][ri]), dXr)
+    assert e <= TOL_BWD, ("dX", e)
     d, h = w.d, w.h
     for j in (0, w.nh - 1):
         Oj = oracle.attn_head(cpu, w.nb, w.nh, j)

@@ -5,6 +5,9 @@ accumulation): max|gpu - ref| / max|ref| <= 1e-2 for the forward outputs
 (Y, and the saved Z and H) and <= 2e-2 for every gradient.
 """
 
+import json
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -51,6 +54,8 @@ def check_full(w: inputs.Workload):
                            ("dX", dX, TOL_BWD), ("dA", dA, TOL_BWD), ("dB", dB, TOL_BWD),
                            ("db1", db1, TOL_BWD), ("db2", db2, TOL_BWD)):
         errs[name] = (rel(np64(out[name]), ref), tol)
+    log_errors({"workload": w.name, "T": w.T, "h": w.h, "F": w.F, "t": w.t, "rows": w.T,
+                "cols": w.F, "max_rel_err": {k: v[0] for k, v in errs.items()}})
     bad = {k: v for k, v in errs.items() if not v[0] <= v[1]}
     assert not bad, f"{w}: {errs}"
     return out
@@ -196,29 +201,96 @@ def test_partition_invariant_on_gpu():
 
 # ---------------------------------------------------------------- full sizes
 
-def check_sampled(w: inputs.Workload, nrows=8, ncols=16):
+# Sampled outputs at full size.  The oracle recomputes whole token rows (Y,
+# Z, H and dX over every column: every column tile of every shard, the
+# row-parallel GEMMs' tail-split tiles among them) and whole FFN columns (dA
+# over every row of A, the matching row of dB, db1).  The rows are picked one
+# per 128-row tile band (spread evenly when there are more bands than rows),
+# plus the first and the last token; the columns are the first and the last
+# of every shard, of the first and last 256-column tile of each shard, plus
+# random ones.  Sample sizes follow a fixed fp64 budget per case.
+ROW_FLOPS_BUDGET = 6e11  # one token row of Y and dX costs 10 h F flops
+
+
+def sample_rows(T: int, want: int, seed: int) -> np.ndarray:
+    g = np.random.default_rng(seed)
+    bands = (T + 127) // 128
+    pick = np.arange(bands) if bands <= want else np.unique(
+        np.linspace(0, bands - 1, want).round().astype(np.int64))
+    rows = {0, T - 1}
+    for b in pick:
+        lo, hi = 128 * b, min(T, 128 * b + 128)
+        rows.add(int(g.integers(lo, hi)))
+    while len(rows) < min(T, want):
+        rows.add(int(g.integers(0, T)))
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def sample_cols(F: int, t: int, want: int, seed: int) -> np.ndarray:
+    g = np.random.default_rng(seed)
+    f = F // t
+    cols = set()
+    for i in range(t):
+        a, b = i * f, (i + 1) * f - 1
+        cols.update((a, b, min(b, a + 255), max(a, b - 255)))
+    while len(cols) < min(F, max(want, len(cols))):
+        cols.add(int(g.integers(0, F)))
+    return np.array(sorted(cols), dtype=np.int64)
+
+
+def sample_sizes(w: inputs.Workload):
+    nrows = int(min(96, max(32, ROW_FLOPS_BUDGET // (10 * w.h * w.F))))
+    return nrows, 64
+
+
+def log_errors(record: dict):
+    """Appends one JSON line of measured errors to the file named by
+    TPMLP_PARITY_LOG, if set (the per-configuration table of errors)."""
+    path = os.environ.get("TPMLP_PARITY_LOG")
+    if path:
+        with open(path, "a") as fh:
+            fh.write(json.dumps(record) + "\n")
+
+
+def check_sampled(w: inputs.Workload):
+    nrows, ncols = sample_sizes(w)
     cpu = inputs.make_inputs(w)
     out = run_gpu(cpu, w.t)
-    rows = inputs.sample_indices(w.T, nrows, w.seed + 1).numpy()
-    cols = inputs.sample_indices(w.F, ncols, w.seed + 2).numpy()
+    rows = sample_rows(w.T, nrows, w.seed + 1)
+    cols = sample_cols(w.F, w.t, ncols, w.seed + 2)
+    ri = torch.as_tensor(rows, device="cuda")
+    ci = torch.as_tensor(cols, device="cuda")
     Yr, Zr, Hr = oracle.forward_rows(cpu, w.t, rows)
     dXr = oracle.backward_rows(cpu, w.t, rows)
     dAc, dBr, db1c = oracle.backward_cols(cpu, w.t, cols)
     db2 = oracle.db2(cpu["dY"])
-    ri = torch.as_tensor(rows)
-    ci = torch.as_tensor(cols)
     errs = {
-        "Y": (rel(np64(out["Y"].cpu()[ri]), Yr), TOL_FWD),
-        "Z": (rel(np64(out["Z"].cpu()[ri]), Zr), TOL_FWD),
-        "H": (rel(np64(out["H"].cpu()[ri]), Hr), TOL_FWD),
-        "dX": (rel(np64(out["dX"].cpu()[ri]), dXr), TOL_BWD),
-        "dA": (rel(np64(out["dA"].cpu()[:, ci]), dAc), TOL_BWD),
-        "dB": (rel(np64(out["dB"].cpu()[ci]), dBr), TOL_BWD),
-        "db1": (rel(np64(out["db1"].cpu()[ci]), db1c), TOL_BWD),
-        "db2": (rel(np64(out["db2"].cpu()), db2), TOL_BWD),
+        "Y": (rel(np64(out["Y"][ri]), Yr), TOL_FWD),
+        "Z": (rel(np64(out["Z"][ri]), Zr), TOL_FWD),
+        "H": (rel(np64(out["H"][ri]), Hr), TOL_FWD),
+        "dX": (rel(np64(out["dX"][ri]), dXr), TOL_BWD),
+        "dA": (rel(np64(out["dA"][:, ci]), dAc), TOL_BWD),
+        "dB": (rel(np64(out["dB"][ci]), dBr), TOL_BWD),
+        "db1": (rel(np64(out["db1"][ci]), db1c), TOL_BWD),
+        "db2": (rel(np64(out["db2"]), db2), TOL_BWD),
     }
+    log_errors({"workload": w.name, "T": w.T, "h": w.h, "F": w.F, "t": w.t, "rows": len(rows),
+                "cols": len(cols), "max_rel_err": {k: v[0] for k, v in errs.items()}})
     bad = {k: v for k, v in errs.items() if not v[0] <= v[1]}
     assert not bad, f"{w.name} t={w.t}: {errs}"
+
+
+def test_samples_cover_every_band_and_shard_edge():
+    rows = sample_rows(16384, 96, 5)
+    assert rows[0] == 0 and rows[-1] == 16383 and len(rows) >= 96
+    assert len(np.unique(rows // 128)) >= 95  # spread over the 128 bands
+    rows = sample_rows(2048, 36, 5)
+    assert set(range(16)) <= set((rows // 128).tolist())  # every band of a short batch
+    cols = sample_cols(81920, 8, 64, 6)
+    f = 81920 // 8
+    for i in range(8):
+        assert {i * f, (i + 1) * f - 1} <= set(cols.tolist())
+    assert len(cols) >= 64
 
 
 FULL = [
@@ -228,11 +300,9 @@ FULL = [
     inputs.custom(T=130, h=8192, F=32768, t=4, seed=33, name="kmajor-ragged"),
     inputs.GPT2_MEDIUM.with_shape(T=8192, t=1),
     inputs.GPT2_MEDIUM.with_shape(T=8192, t=2),
-    inputs.MEGATRON_8_3B,
+] + [inputs.MEGATRON_8_3B.with_shape(T=8192, t=t) for t in (1, 2, 4, 8)] + [
     inputs.MTNLG_530B,
-    inputs.SWEEP.with_shape(T=512, t=1),
-    inputs.SWEEP.with_shape(T=16384, t=8),
-]
+] + [inputs.SWEEP.with_shape(T=T, t=t) for T in inputs.SWEEP_TOKENS for t in inputs.SWEEP_SHARDS]
 
 
 @pytest.mark.parametrize("w", FULL, ids=lambda w: f"{w.name}_T{w.T}_t{w.t}")

@@ -91,3 +91,38 @@ def test_pins_catch_mutant(name, tmp_path):
     assert r.returncode == 0, r.stderr
     failed = P.failing_pins(Oracle(str(so)))
     assert failed, f"no pin caught the planted mistake {name}"
+
+
+# Planted mistakes in the sampled-row attention oracle (numpy), each loaded
+# from an edited copy of its source.
+ATTN_ROWS_SRC = os.path.join(os.path.dirname(oracle.__file__), "attn_rows.py")
+ROWS_MUTANTS = {
+    "rows_mask_open": ("S = np.where(causal, Q @ K.T * scale, -np.inf)", "S = Q @ K.T * scale"),
+    "rows_no_score_scale": ("S = np.where(causal, Q @ K.T * scale, -np.inf)",
+                            "S = np.where(causal, Q @ K.T, -np.inf)"),
+    "rows_dS_drops_rowsum": ("dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))", "dS = P * dP"),
+    "rows_dQ_no_scale": ("dqkv[:, c] = dS[pos] @ K * scale", "dqkv[:, c] = dS[pos] @ K"),
+    "rows_dK_transposed": ("dqkv[:, ck] = dS[:, pos].T @ Q * scale", "dqkv[:, ck] = dS[pos] @ Q * scale"),
+    "rows_dV_uses_dS": ("dqkv[:, cv] = P[:, pos].T @ dOj", "dqkv[:, cv] = dS[:, pos].T @ dOj"),
+    "rows_k_v_swapped": ("Q, K, V = qkv[:, c], qkv[:, ck], qkv[:, cv]",
+                         "Q, K, V = qkv[:, c], qkv[:, cv], qkv[:, ck]"),
+    "rows_g_sum_overwrites": ("Y[sel] += O[pos] @ Woi", "Y[sel] = O[pos] @ Woi"),
+    "rows_f_sum_overwrites": ("dX[sel] += dqkv @ Wi.T", "dX[sel] = dqkv @ Wi.T"),
+    "rows_bo_dropped": ('Y += _f64(inp["bo"]) + _f64(inp["residual"][torch.as_tensor(rows)])',
+                        'Y += _f64(inp["residual"][torch.as_tensor(rows)])'),
+    "rows_wrong_shard_columns": ("np.arange(p * h + i * w, p * h + (i + 1) * w)",
+                                 "np.arange(p * w + i * w, p * w + (i + 1) * w)"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(ROWS_MUTANTS))
+def test_pins_catch_attn_rows_mutant(name):
+    import types
+
+    old, new = ROWS_MUTANTS[name]
+    src = open(ATTN_ROWS_SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} must occur exactly once"
+    mod = types.ModuleType("attn_rows_mutant")
+    exec(compile(src.replace(old, new), "attn_rows_mutant.py", "exec"), mod.__dict__)
+    failed = P.failing_pins(Oracle(attn_rows_impl=mod.attn_rows))
+    assert failed, f"no pin caught the planted mistake {name}"

@@ -60,7 +60,11 @@ def test_matches_allocating_entry_point_twice(T, n, seed):
     assert binding.device_status() == binding.TPMLP_OK
     assert _rel(first, ref) <= TOL
     assert _rel(second, ref) <= TOL
-    assert torch.equal(first, second)
+    # the same kernels add in the same order whichever memory holds the
+    # partial sums, so the results agree bit for bit: a partial row or a
+    # completion count left over from an earlier call would show here
+    assert torch.equal(first, ref)
+    assert torch.equal(second, ref)
 
 
 @pytest.mark.gpu
