@@ -45,7 +45,8 @@ FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
 
 
 CALLS = ("column_gelu", "column_gelu_h_only", "row_sum", "row_sum_dropout", "dgelu", "dx", "dA",
-         "dB", "dA_kmajor", "dB_kmajor", "transpose", "dropout_grad", "ln_forward", "ln_backward")
+         "dB", "dA_kmajor", "dB_kmajor", "transpose", "dropout_grad", "bias_grad", "ln_forward",
+         "ln_backward")
 
 
 def parse_args(argv=None):
@@ -301,8 +302,10 @@ class Step:
                       + (KMAJOR_CALLS if self.kmajor else STEP_CALLS[5:]))
 
     def run(self, events=None):
-        """One fwd+bwd step; if `events` (one more than the calls) is given,
-        records them between the calls on the current stream."""
+        """One fwd+bwd step.  `events`: a list of one more event than the
+        calls, recorded between every two calls on the current stream, or a
+        dict {boundary: event} recorded at those boundaries only (boundary k
+        is just before call k; len(calls) is after the last)."""
         b, i, t = self.b, self.inp, self.w.t
         rec = self.recompute
         calls = (lambda: b.tp_mlp_column_gelu(i["X"], i["A"], i["b1"], t, Z=None if rec else self.Z,
@@ -340,13 +343,14 @@ class Step:
                 lambda: b.tp_mlp_dA(i["X"], self.dZ, t, dA=self.dA),
                 lambda: b.tp_mlp_dB(self.H, dP, t, dB=self.dB),
             )
-        if events is not None:
-            events[0].record()
+        marks = events if isinstance(events, dict) else dict(enumerate(events or ()))
+        if 0 in marks:
+            marks[0].record()
         for k, c in enumerate(calls):
             c()
             self.launches += b.last_launch_count()
-            if events is not None:
-                events[k + 1].record()
+            if k + 1 in marks:
+                marks[k + 1].record()
 
 
 def init_distributed(n_gpus):
@@ -387,6 +391,13 @@ def barrier():
 
 
 def time_ours(w, steps, warmup, local, p_drop=0.0, recompute=False):
+    """Two timed passes of `steps` steps each, L2 flushed between steps
+    outside the events.  The headline pass records events only at the step's
+    start, between the forward and the backward pass and at its end, so that
+    a kernel may begin its launch while the one before it finishes, as in a
+    training step; it gives the step time, the forward / backward split and
+    the launch count.  The breakdown pass records an event between every two
+    calls; it gives each call's time (the roofline's kernel duration)."""
     import torch
 
     dev = torch.device("cuda", local)
@@ -398,7 +409,10 @@ def time_ours(w, steps, warmup, local, p_drop=0.0, recompute=False):
     assert step.b.device_status() == 0, "device wait timed out during warm-up"
     step.launches = 0
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(step.names) + 1)] for _ in range(steps)]
+    ncalls = len(step.names)
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    head = [{0: ev(), 2: ev(), ncalls: ev()} for _ in range(steps)]
+    evs = [[ev() for _ in range(ncalls + 1)] for _ in range(steps)]
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     barrier()
     torch.cuda.synchronize()
@@ -407,20 +421,54 @@ def time_ours(w, steps, warmup, local, p_drop=0.0, recompute=False):
         w0 = time.time()
         for k in range(steps):
             flush.fill_(k & 0xFF)  # evict L2 between steps (outside the events)
-            step.run(evs[k])
+            step.run(head[k])
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
+        launches = step.launches
+        for k in range(steps):
+            flush.fill_(k & 0xFF)
+            step.run(evs[k])
+        torch.cuda.synchronize()
         clocks.mark(w0, time.time())
     barrier()
     assert step.b.device_status() == 0, "device wait timed out"
-    launches = step.launches
-    dev_ms = sum(evs[k][0].elapsed_time(evs[k][-1]) for k in range(steps))
+    dev_ms = sum(head[k][0].elapsed_time(head[k][ncalls]) for k in range(steps))
     per_call = {name: [evs[k][j].elapsed_time(evs[k][j + 1]) for k in range(steps)]
                 for j, name in enumerate(step.names)}
-    # the forward pass is a2 + a3 (events 0..2), the backward pass the rest
-    split = {"fwd_ms": statistics.mean(evs[k][0].elapsed_time(evs[k][2]) for k in range(steps)),
-             "bwd_ms": statistics.mean(evs[k][2].elapsed_time(evs[k][-1]) for k in range(steps))}
+    # the forward pass is a2 + a3 (calls 0 and 1), the backward pass the rest
+    split = {"fwd_ms": statistics.mean(head[k][0].elapsed_time(head[k][2]) for k in range(steps)),
+             "bwd_ms": statistics.mean(head[k][2].elapsed_time(head[k][ncalls]) for k in range(steps)),
+             "breakdown_ms_per_step": statistics.mean(evs[k][0].elapsed_time(evs[k][ncalls])
+                                                      for k in range(steps))}
     return step, dev_ms / 1e3, wall, per_call, clocks.summary(), launches, split
+
+
+def time_graph(step, steps, warmup):
+    """Seconds of `steps` replays of one step captured as a CUDA graph (the
+    library's calls on the capturing stream, workspaces and outputs fixed),
+    L2 flushed between replays outside the events."""
+    import torch
+
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step.run()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=torch.cuda.current_device())
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    total = 0.0
+    for k in range(steps):
+        flush.fill_(k & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        total += e0.elapsed_time(e1) / 1e3
+    assert step.b.device_status() == 0, "device wait timed out in a graph replay"
+    del graph
+    return total
 
 
 def time_e2e(step, steps, warmup):
@@ -567,6 +615,7 @@ def run_ours(args, w):
         e_max, e_units = reduce_max_sum(e_s, flops * args.steps)
         e2e = {"value": e_units / e_max / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h}
+    graph_s = time_graph(step, args.steps, args.warmup)
 
     burst, sustained, src = peaks()
     gemm_flops = 2 * w.T * w.h * w.F
@@ -590,11 +639,17 @@ def run_ours(args, w):
         "pct_of_peak": {"burst": 100 * value / world / burst, "sustained": 100 * value / world / sustained,
                         "source": src},
         "fwd_ms": round(split["fwd_ms"], 4), "bwd_ms": round(split["bwd_ms"], 4),
+        # the per-call pass (an event between every two calls) takes this long a step
+        "breakdown_ms_per_step": round(split["breakdown_ms_per_step"], 4),
         "per_call_ms": {k: round(v, 4) for k, v in avg_ms.items()},
         # db2: the column sums of dY, HBM-bound: 2 T h bytes read, 4 h written
         "db2_gbs": round((2 * w.T * w.h + 4 * w.h) / (avg_ms["db2"] / 1e3) / 1e9, 1),
         "roofline": roofline,
         "e2e": e2e,
+        # the same step captured once as a CUDA graph and replayed: the device
+        # time without the host's per-call launch work between kernels
+        "graph": {"ms_per_step": 1e3 * graph_s / args.steps,
+                  "value": flops * args.steps / graph_s / 1e12},
         "clocks": clocks,
         "gpu_launches": launches,
         "gemm_kernel": {0: "single CTA", 1: "auto", 2: "CTA pairs"}[
@@ -922,6 +977,10 @@ def run_call(a) -> int:
     elif c == "dropout_grad":
         dY, dP = bf(T, h), bf(T, h)
         fn = lambda: b.tp_mlp_dropout_grad(dY, p_drop, 7, 0, dP=dP)  # noqa: E731
+    elif c == "bias_grad":  # db2 = column sums of dY [T, h]
+        dY, db = bf(T, h), torch.empty(h, device=dev)
+        part = torch.empty(max(1, int(b.lib().tp_mlp_bias_grad_workspace_floats(T, h))), device=dev)
+        fn = lambda: b.tp_mlp_bias_grad(dY, db=db, partial=part)  # noqa: E731
     else:
         x, r, gam, bet = bf(T, h), bf(T, h), bf(h, std=0.1), bf(h, std=0.1)
         X, s = torch.empty_like(x), torch.empty_like(x)

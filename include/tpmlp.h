@@ -44,8 +44,10 @@
  *    different streams or threads, and calls captured into CUDA graphs and
  *    replayed beside eager calls, share no device state -- except the
  *    array of tp_mlp_bias_grad_noalloc, which its calls share (see there).
- *    Process-wide host state: the GEMM kernel mode of
- *    tpmlp_set_cta_pair_mode (an atomic, read at each launch: change it only
+ *    Process-wide host state: the GEMM launch modes of
+ *    tpmlp_set_cta_pair_mode, tpmlp_set_epilogue_warps and
+ *    tpmlp_set_dependent_launch (atomics, read at
+ *    each launch: change them only
  *    while no other thread launches, or results stay equal but the launch
  *    shape may differ between two calls), a once-per-process lookup of the
  *    driver's tensor-map encoder, once-per-device kernel attributes and
@@ -513,6 +515,25 @@ int tp_attn_backward(const tpmlp_bf16* dY, const tpmlp_bf16* X, const tpmlp_bf16
  * reduction does not depend on the mode), so results are bitwise identical
  * across modes. */
 int tpmlp_set_cta_pair_mode(int mode);
+
+/* How many epilogue warps the dZ GEMM (step a5, the one GEMM kernel with
+ * both forms) launches with (process-wide; returns the previous mode, or -1
+ * for an invalid mode):
+ *   0  default: eight for reductions of at most 16 k-blocks of 64 (K <=
+ *      1024), where a tile's mainloop is too short to hide four warps'
+ *      epilogue, else four;
+ *   4  four warps always;  8  eight warps always.
+ * Each output element gets the same arithmetic in either form, so results
+ * are bitwise identical across modes. */
+int tpmlp_set_epilogue_warps(int mode);
+
+/* Whether GEMM kernels are launched as programmatic dependents of the
+ * kernel before them on the stream (process-wide; returns the previous
+ * setting, or -1 for a value other than 0 or 1).  1 (default): a GEMM's CTAs
+ * may start, and set up their barriers and tensor memory, while that kernel
+ * finishes; they read and write global memory only after it has completed,
+ * so results are identical either way.  0: plain stream order. */
+int tpmlp_set_dependent_launch(int on);
 
 /* Static text for a status code. */
 const char* tp_mlp_status_string(int status);

@@ -98,6 +98,8 @@ _SIGNATURES = {
     "tpmlp_last_launch_count": ([], _I),
     "tpmlp_selftest_bounded_wait": ([_I, _P], _I),
     "tpmlp_set_cta_pair_mode": ([_I], _I),
+    "tpmlp_set_epilogue_warps": ([_I], _I),
+    "tpmlp_set_dependent_launch": ([_I], _I),
 }
 
 
@@ -177,6 +179,24 @@ def set_cta_pair_mode(mode: int) -> int:
     prev = int(lib().tpmlp_set_cta_pair_mode(mode))
     if prev < 0:
         raise ValueError(f"invalid mode {mode}")
+    return prev
+
+
+def set_epilogue_warps(mode: int) -> int:
+    """0 by the reduction's length (default), 4 or 8 epilogue warps always.
+    Returns the previous mode."""
+    prev = int(lib().tpmlp_set_epilogue_warps(mode))
+    if prev < 0:
+        raise ValueError(f"invalid mode {mode}")
+    return prev
+
+
+def set_dependent_launch(on: int) -> int:
+    """1 (default): GEMMs start as programmatic dependents of the kernel
+    before them; 0: plain stream order.  Returns the previous setting."""
+    prev = int(lib().tpmlp_set_dependent_launch(on))
+    if prev < 0:
+        raise ValueError(f"invalid setting {on}")
     return prev
 
 

@@ -249,6 +249,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q128,  // QKV, 128-row boxes (Q)
                     const __grid_constant__ CUtensorMap tm_kv,    // QKV, BKV-row boxes (K, V)
                     const AttnArgs a) {
+    pdl_launch_dependents();  // the next kernel may begin its launch
     using C = FwdCfg<D>;
     constexpr int S = C::STAGES;
     constexpr int BKV = C::BKV;
@@ -661,6 +662,7 @@ template <int D>
 __global__ void __launch_bounds__(kDeltaThreads)
     attn_delta_kernel(const __nv_bfloat16* __restrict__ dO, const __nv_bfloat16* __restrict__ O,
                       long long T, int nh, float* __restrict__ delta) {
+    pdl_launch_dependents();  // the next kernel may begin its launch
     constexpr int CH = D / 8;                 // chunks per segment
     constexpr int SEGS = delta_segs<D>();     // segments per CTA
     constexpr int PER = (SEGS * CH + kDeltaThreads - 1) / kDeltaThreads;
@@ -729,6 +731,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                        const __grid_constant__ CUtensorMap tm_kv64,  // QKV, 64-row boxes
                        const __grid_constant__ CUtensorMap tm_do128, // dO, 128-row boxes
                        const AttnArgs a) {
+    pdl_launch_dependents();  // the next kernel may begin its launch
     using C = DqCfg<D>;
     constexpr int S = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -1079,6 +1082,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                          const __grid_constant__ CUtensorMap tm_q64,    // QKV, 64-row boxes
                          const __grid_constant__ CUtensorMap tm_do64,   // dO, 64-row boxes
                          const AttnArgs a) {
+    pdl_launch_dependents();  // the next kernel may begin its launch
     using C = DkvCfg<D>;
     constexpr int S = C::STAGES;
     extern __shared__ uint8_t smem_raw[];

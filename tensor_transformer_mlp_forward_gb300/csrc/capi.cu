@@ -188,6 +188,23 @@ int operand_map(CUtensorMap* m, const Operand& o, int t, int tile_rows) {
 
 // 0: single-CTA kernel only, 1: CTA pairs when the problem fills them, 2: pairs always.
 std::atomic<int> g_pair_mode{1};
+// Epilogue warps of the GEMMs that have both forms: 0 = by the reduction's
+// length (epi_warps_for), 4 or 8 = always that form.
+std::atomic<int> g_epi_mode{0};
+
+// A tile's mainloop lasts its reduction's k-blocks (512 clocks each for a
+// CTA pair at the full MMA rate); its epilogue does not shrink with it.  Up
+// to 32 k-blocks (K <= 2048) the epilogue of four warps is what bounds the
+// tile, and eight warps, two per scheduler, hide each other's latencies.
+// 1: GEMMs are launched as programmatic dependents of the kernel before
+// them on the stream (their set-up overlaps its end), 0: plain stream order.
+std::atomic<int> g_dependent_launch{1};
+
+int epi_warps_for(long long total_kb) {
+    const int mode = g_epi_mode.load(std::memory_order_relaxed);
+    if (mode == 4 || mode == 8) return mode;
+    return total_kb <= 32 ? 8 : 4;
+}
 
 #ifndef TPMLP_BAND_BUDGET_MB
 #define TPMLP_BAND_BUDGET_MB 16
@@ -371,6 +388,8 @@ int run_gemm(Launcher fn, const Operand& a, const Operand& b, const Output& out,
     }
     tile_space(g, f.M, f.N, f.K, f.t, f.mode, f.a_bytes, f.b_bytes, tile_m);
     if (g.num_tiles == 0) return TPMLP_OK;
+    g.epi_warps = epi_warps_for(1LL * g.k_blocks * (f.mode == SHARD_K ? f.t : 1));
+    g.dependent_launch = g_dependent_launch.load(std::memory_order_relaxed);
     if (out.k_splits > 1) {
         g.k_splits = out.k_splits;
         g.num_tiles = g.base_tiles * out.k_splits;
@@ -522,6 +541,7 @@ __global__ void __launch_bounds__(256)
     split_reduce_kernel(const float* __restrict__ P, int splits, long long count, int n,
                         const __nv_bfloat16* __restrict__ bias, const __nv_bfloat16* __restrict__ res,
                         Dropout dr, __nv_bfloat16* __restrict__ out) {
+    pdl_launch_dependents();  // the next kernel may begin its launch
     const long long i = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
     if (i >= count) return;
     float a[8];
@@ -545,6 +565,7 @@ __global__ void __launch_bounds__(256)
     tail_reduce_kernel(const float* __restrict__ P, int S, GemmArgs g, int X,
                        const __nv_bfloat16* __restrict__ bias, const __nv_bfloat16* __restrict__ res,
                        Dropout dr, __nv_bfloat16* __restrict__ out) {
+    pdl_launch_dependents();  // the next kernel may begin its launch
     const int local = static_cast<int>(blockIdx.x >> 5);
     const int e = static_cast<int>(((blockIdx.x & 31u) * blockDim.x + threadIdx.x) * 8u);
     const int r = e / BN, c = e % BN;
@@ -641,37 +662,56 @@ int row_sum(const tpmlp_bf16* H, const tpmlp_bf16* B, const tpmlp_bf16* b2,
     return launch_split_reduce(static_cast<const float*>(ws), sp, T, h, b2, R, dr, Y, st);
 }
 
-// dP = keep * dY * scale (bf16), 8 elements a thread: the gradient that
-// reaches the MLP's output through the dropout.
-__global__ void __launch_bounds__(256)
+// dP = keep * dY * scale (bf16): the gradient that reaches the MLP's output
+// through the dropout.  HBM-bound (4 bytes of traffic per element) with a
+// Philox block per four elements of integer work beside it.  A thread owns
+// kDropVec 16-byte pieces (8 elements each) spaced a CTA-width apart (so a
+// warp's loads and stores stay coalesced), issues all their loads before
+// any Philox block, and stores after: the loads' latency overlaps the
+// arithmetic.  The tail (count not a multiple of the CTA's span) is masked.
+constexpr int kDropThreads = 256;
+constexpr int kDropVec = 4;
+
+__global__ void __launch_bounds__(kDropThreads)
     dropout_grad_kernel(const __nv_bfloat16* __restrict__ dY, long long count, Dropout dr,
                         __nv_bfloat16* __restrict__ dP) {
-    const long long i = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
-    if (i >= count) return;
-    const uint4 g = __ldg(reinterpret_cast<const uint4*>(dY + i));
-    const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
-    const uint32_t keep = dropout_keep4(dr.seed, dr.offset + i, dr.threshold) |
-                          (dropout_keep4(dr.seed, dr.offset + i + 4, dr.threshold) << 4);
-    float a[8];
+    pdl_launch_dependents();  // the next kernel may begin its launch
+    const long long base = static_cast<long long>(blockIdx.x) * kDropThreads * kDropVec * 8;
+    uint4 g[kDropVec];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const uint32_t gg = (j & 1) ? (gw[j >> 1] & 0xFFFF0000u) : (gw[j >> 1] << 16);
-        a[j] = ((keep >> j) & 1u) ? __uint_as_float(gg) * dr.scale : 0.0f;
+    for (int v = 0; v < kDropVec; ++v) {
+        const long long i = base + (static_cast<long long>(v) * kDropThreads + threadIdx.x) * 8;
+        g[v] = i < count ? __ldg(reinterpret_cast<const uint4*>(dY + i)) : make_uint4(0, 0, 0, 0);
     }
-    uint4 o;
-    o.x = pack_bf16x2(a[0], a[1]);
-    o.y = pack_bf16x2(a[2], a[3]);
-    o.z = pack_bf16x2(a[4], a[5]);
-    o.w = pack_bf16x2(a[6], a[7]);
-    *reinterpret_cast<uint4*>(dP + i) = o;
+#pragma unroll
+    for (int v = 0; v < kDropVec; ++v) {
+        const long long i = base + (static_cast<long long>(v) * kDropThreads + threadIdx.x) * 8;
+        if (i >= count) continue;
+        const uint32_t gw[4] = {g[v].x, g[v].y, g[v].z, g[v].w};
+        const uint32_t keep = dropout_keep4(dr.seed, dr.offset + i, dr.threshold) |
+                              (dropout_keep4(dr.seed, dr.offset + i + 4, dr.threshold) << 4);
+        float a[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t gg = (j & 1) ? (gw[j >> 1] & 0xFFFF0000u) : (gw[j >> 1] << 16);
+            a[j] = ((keep >> j) & 1u) ? __uint_as_float(gg) * dr.scale : 0.0f;
+        }
+        uint4 o;
+        o.x = pack_bf16x2(a[0], a[1]);
+        o.y = pack_bf16x2(a[2], a[3]);
+        o.z = pack_bf16x2(a[4], a[5]);
+        o.w = pack_bf16x2(a[6], a[7]);
+        *reinterpret_cast<uint4*>(dP + i) = o;
+    }
 }
 
 int dropout_grad(const tpmlp_bf16* dY, int T, int h, const Dropout& dr, tpmlp_bf16* dP,
                  cudaStream_t st) {
     const long long count = 1LL * T * h;
     if (count == 0) return TPMLP_OK;
-    dropout_grad_kernel<<<static_cast<unsigned>(cdiv(count / 8, 256)), 256, 0, st>>>(
-        cb(dY), count, dr, reinterpret_cast<__nv_bfloat16*>(dP));
+    dropout_grad_kernel<<<static_cast<unsigned>(cdiv(count, 8LL * kDropThreads * kDropVec)),
+                          kDropThreads, 0, st>>>(cb(dY), count, dr,
+                                                 reinterpret_cast<__nv_bfloat16*>(dP));
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail_cuda(e);
     ++t_last_launches;
@@ -1751,6 +1791,16 @@ TPMLP_API const char* tpmlp_status_string(int status) { return tp_mlp_status_str
 TPMLP_API int tpmlp_set_cta_pair_mode(int mode) {
     if (mode < 0 || mode > 2) return -1;
     return g_pair_mode.exchange(mode);
+}
+
+TPMLP_API int tpmlp_set_dependent_launch(int on) {
+    if (on != 0 && on != 1) return -1;
+    return g_dependent_launch.exchange(on);
+}
+
+TPMLP_API int tpmlp_set_epilogue_warps(int mode) {
+    if (mode != 0 && mode != 4 && mode != 8) return -1;
+    return g_epi_mode.exchange(mode);
 }
 
 TPMLP_API int tpmlp_last_cuda_error(void) { return t_last_cuda_error; }

@@ -41,6 +41,7 @@ template <bool kFinish>
 __global__ void __launch_bounds__(kSumThreads)
     colsum_partial_kernel(const __nv_bfloat16* __restrict__ G, int T, int n, int rows_per_chunk,
                           float* __restrict__ out, float* __restrict__ db, unsigned int* counts) {
+    pdl_launch_dependents();  // the next kernel may begin its launch
     __shared__ float part[kSumThreads / 32][kColBlock];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int col0 = blockIdx.x * kColBlock + (lane & 7) * 8;
@@ -132,6 +133,7 @@ constexpr int kRowsumGroups = 8;
 
 __global__ void __launch_bounds__(kRowsumCols * kRowsumGroups)
     rowsum_kernel(const float* __restrict__ P, int rows, int n, float* __restrict__ out) {
+    pdl_launch_dependents();  // the next kernel may begin its launch
     __shared__ float part[kRowsumGroups][kRowsumCols];
     const int g = threadIdx.x / kRowsumCols, c = threadIdx.x % kRowsumCols;
     const int j = blockIdx.x * kRowsumCols + c;

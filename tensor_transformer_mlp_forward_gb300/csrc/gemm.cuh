@@ -20,13 +20,20 @@
 //            shard 0's K range, then shard 1's, ..., accumulating into the
 //            same TMEM accumulator -- the in-device g / f operator sum.
 //
-// CTA layout (192 threads, one CTA per SM, persistent over tiles):
-//   warps 0-3  epilogue: TMEM -> registers -> fused math -> global memory,
-//              warp w owns accumulator rows 32w..32w+31;
-//   warp 4     TMA producer (one thread) feeding a STAGES-deep smem ring;
-//   warp 5     TMEM owner and MMA issuer (one thread).
+// CTA layout (32 (EW + 2) threads, one CTA per SM, persistent over tiles):
+//   warps 0..EW-1  epilogue: TMEM -> registers -> fused math -> global
+//                  memory; warp w reads TMEM lane quadrant w % 4
+//                  (accumulator rows 32 (w % 4) ..) and, with EW = 8, the
+//                  half w / 4 of the 256 columns;
+//   warp EW        TMA producer (one thread) feeding a STAGES-deep smem ring;
+//   warp EW + 1    TMEM owner and MMA issuer (one thread).
 // Two 128x256 fp32 accumulators (all 512 TMEM columns) let the epilogue of
-// tile i overlap the mainloop of tile i+1.
+// tile i overlap the mainloop of tile i+1.  With a short reduction a tile's
+// mainloop is short too (16 k-blocks at K = 1024), and four epilogue warps,
+// one per scheduler, may not hide their own load and store latencies behind
+// it; EW = 8 puts two epilogue warps on every scheduler, each with half of
+// the columns, at the price of one pipeline stage (its staging buffers).
+// The dZ GEMM, whose epilogue is the heaviest, is built in both forms.
 //
 // PAIR variant (cluster of 2 CTAs on neighbouring SMs, tcgen05 cta_group::2):
 // the pair computes a 256 x 256 tile.  Each CTA loads its own 128 rows of A
@@ -51,27 +58,30 @@ constexpr int BN = 256;  // accumulator columns (one TMEM accumulator)
 constexpr int BK = 64;   // 64 bf16 = one 128-byte swizzle row
 constexpr int UMMA_K = 16;
 constexpr int MN_ATOM_BYTES = 64 * BK * 2;  // one 64-wide MN-major box: 8 KiB
-constexpr int NUM_THREADS = 192;
-constexpr int EPI_THREADS = 128;
 constexpr int TMEM_COLS = 512;
 constexpr int BAR_BYTES = 256;
 // Epilogue staging: per epilogue warp two buffers, each a 32-row x 64-column
 // bf16 block (rows 128 B apart, 128-byte swizzle) stored by one TMA store.
 constexpr int EPI_BUF_BYTES = 32 * 128;
-constexpr int EPI_STAGING_BYTES = 4 * 2 * EPI_BUF_BYTES;
 
-// Per-variant geometry.  Single CTA: a 128 x 256 tile, 4 stages of
-// A 128x64 + B 256x64.  CTA pair (cluster of 2, cta_group::2): a 256 x 256
-// tile, each CTA holding 128 rows of A and 128 rows of B per stage, 7 stages.
-template <bool PAIR>
+// Per-variant geometry.  Single CTA: a 128 x 256 tile, stages of
+// A 128x64 + B 256x64 (48 KiB).  CTA pair (cluster of 2, cta_group::2): a
+// 256 x 256 tile, each CTA holding 128 rows of A and 128 rows of B per stage
+// (32 KiB).  EW epilogue warps with two staging buffers each; the stages
+// fill what is left of the 227 KiB of shared memory.
+template <bool PAIR, int EW = 4>
 struct Geometry {
     static constexpr int TILE_M = PAIR ? 2 * BM : BM;
     static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // B rows in this CTA's smem
-    static constexpr int STAGES = PAIR ? 6 : 4;
+    static constexpr int STAGES = PAIR ? (EW == 8 ? 5 : 6) : (EW == 8 ? 3 : 4);
+    static constexpr int THREADS = 32 * (EW + 2);
     static constexpr int A_STAGE_BYTES = BM * BK * 2;
     static constexpr int B_STAGE_BYTES = B_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_STAGING_BYTES + BAR_BYTES;
+    static constexpr int STAGING_BYTES = EW * 2 * EPI_BUF_BYTES;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STAGING_BYTES + BAR_BYTES;
+    static_assert(EW == 4 || EW == 8, "four or eight epilogue warps");
+    static_assert(SMEM_BYTES <= 232448, "shared memory of one CTA");
 };
 
 enum ShardMode { SHARD_NONE = 0, SHARD_N = 1, SHARD_M = 2, SHARD_K = 3 };
@@ -119,6 +129,8 @@ struct GemmArgs {
     // compact [units, TILE_M, BN] fp32 map (tile-local coordinates) instead
     // of split ks of a [splits, M, N] map.
     int partial_compact;
+    int epi_warps;  // host side: 4 or 8 epilogue warps (the kernel variant launched)
+    int dependent_launch;  // host side: launched with programmatic stream serialization
 };
 
 struct TileCoord {
@@ -337,14 +349,19 @@ __device__ __forceinline__ float warp_column_sums(float (&v)[32], int lane) {
 
 // --------------------------------------------------------------- the kernel
 
-template <bool A_MN, bool B_MN, int EPI, bool PAIR>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+template <bool A_MN, bool B_MN, int EPI, bool PAIR, int EW>
+__global__ void __launch_bounds__(32 * (EW + 2), 1)
     tcgen05_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmO0,  // output (Z for EPI_BIAS_GELU)
                         const __grid_constant__ CUtensorMap tmO1,  // H for EPI_BIAS_GELU
                         const GemmArgs p) {
-    using G = Geometry<PAIR>;
+    using G = Geometry<PAIR, EW>;
+    constexpr int PRODUCER_WARP = EW, MMA_WARP = EW + 1;
+    // Every CTA of this persistent grid is resident from the start, so the
+    // next kernel on the stream may begin launching at once: its CTAs take
+    // SMs as ours leave and run their set-up while our last tiles finish.
+    pdl_launch_dependents();
     extern __shared__ uint8_t smem_raw[];
     // 128-byte swizzle atoms repeat every 1024 B: align the ring to 1 KiB.
     const uint32_t raw = smem_u32(smem_raw);
@@ -352,7 +369,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t* ring_a = smem;
     uint8_t* ring_b = smem + G::STAGES * G::A_STAGE_BYTES;
     uint8_t* staging = smem + G::STAGES * G::STAGE_BYTES;  // 1 KiB aligned
-    uint64_t* bars = reinterpret_cast<uint64_t*>(staging + EPI_STAGING_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(staging + G::STAGING_BYTES);
     uint64_t* full = bars;                      // stage loaded  (STAGES)
     uint64_t* empty = bars + G::STAGES;         // stage drained (STAGES)
     uint64_t* acc_full = bars + 2 * G::STAGES;  // accumulator ready (2)
@@ -376,13 +393,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&acc_full[a], 1);
-            mbar_init(&acc_empty[a], PAIR ? 8 : 4);  // one arrival per epilogue warp
+            mbar_init(&acc_empty[a], PAIR ? 2 * EW : EW);  // one arrival per epilogue warp
         }
         mbar_init(drain, 1);
         misc[1] = 0u;
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == MMA_WARP) {
         if constexpr (PAIR) {
             tmem_alloc_pair(&misc[0], TMEM_COLS);
             tmem_relinquish_pair();
@@ -391,7 +408,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tmem_relinquish();
         }
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == PRODUCER_WARP && lane == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
         prefetch_tmap(&tmO0);
@@ -403,10 +420,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     else
         __syncthreads();
     tc_fence_after();
+    // Set-up (barriers, TMEM, descriptor prefetch) touched no global memory;
+    // from here on this kernel reads what the previous kernel wrote and
+    // writes what it may still read, so it waits for that kernel to finish.
+    pdl_wait();
     const uint32_t tmem_base = misc[0];
     const int total_kb = p.shard_mode == SHARD_K ? p.k_blocks * p.shards : p.k_blocks;
 
-    if (warp == 4) {
+    if (warp == PRODUCER_WARP) {
         // ---------------------------------------------------- TMA producer
         if (lane == 0) {
             int stage = 0;
@@ -470,7 +491,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == MMA_WARP) {
         // ------------------------------------------------------ MMA issuer
         if (lane == 0 && rank == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(G::TILE_M, BN, A_MN, B_MN);
@@ -533,16 +554,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
     } else {
         // -------------------------------------------------------- epilogue
-        // Warp q owns accumulator rows 32q..32q+31 (its TMEM lane quadrant).
+        // Warp w owns accumulator rows 32q..32q+31 (q = w % 4, its TMEM lane
+        // quadrant) and the NBLK 64-column blocks from column 64 cb0 on.
         // Per 64-column block: TMEM -> registers -> fused math -> bf16 rows
         // in a swizzled staging buffer -> one TMA store of the 32 x 64 block
         // (full lines; the tensor map clips rows and columns outside the
         // shard).  Two buffers per warp let a block be written while the
         // previous one is still being stored.
-        const int q = warp;
+        const int q = warp & 3;
+        constexpr int NBLK = BN / 64 / (EW / 4);
+        const int cb0 = (warp >> 2) * NBLK;
         const uint32_t release_bar =
             PAIR ? map_to_cta(smem_u32(&acc_empty[0]), 0) : smem_u32(&acc_empty[0]);
-        const uint32_t buf_base = smem_u32(staging) + static_cast<uint32_t>(q) * 2u * EPI_BUF_BYTES;
+        const uint32_t buf_base = smem_u32(staging) + static_cast<uint32_t>(warp) * 2u * EPI_BUF_BYTES;
         const uint32_t my_row = static_cast<uint32_t>(lane) * 128u;
         const uint32_t swz = static_cast<uint32_t>(lane & 7);
         uint32_t seq = 0;  // stores committed so far: selects the buffer
@@ -559,23 +583,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             long long grow = m, gcol0 = tc.n0;
             if (p.shard_mode == SHARD_N) gcol0 += static_cast<long long>(tc.s) * p.N;
             if (p.shard_mode == SHARD_M) grow += static_cast<long long>(tc.s) * p.M;
-            // The row operand of the fused math (Z for GeLU', the residual) does
-            // not depend on the accumulator: its first 32 columns are requested
-            // before the wait, and each 32-column block's loads are issued one
-            // block ahead of their use, so their latency overlaps TMEM reads.
+            // The row operand of the fused math (Z for GeLU', the residual) and
+            // the bias do not depend on the accumulator: their first 32
+            // columns are requested before the wait, and each 32-column
+            // block's loads are issued one block ahead of their use, so their
+            // latency overlaps TMEM reads and the previous block's math.
             constexpr bool kAux = EPI == EPI_DGELU || EPI == EPI_BIAS_RESIDUAL;
-            uint4 aux_cur[4], aux_nxt[4];
+            constexpr bool kBias = EPI == EPI_BIAS_GELU || EPI == EPI_BIAS_RESIDUAL || EPI == EPI_BIAS;
+            uint4 aux_cur[4], aux_nxt[4], bias_cur[4], bias_nxt[4];
             if constexpr (kAux) {
-                const int v0 = row_ok ? min(32, p.N - tc.n0) : 0;
-                load_raw32(p.aux + grow * p.ld_aux + gcol0, v0, aux_cur);
+                const int v0 = row_ok ? min(32, p.N - (tc.n0 + cb0 * 64)) : 0;
+                load_raw32(p.aux + grow * p.ld_aux + gcol0 + cb0 * 64, v0, aux_cur);
             }
+            if constexpr (kBias)  // the same 32 values for every lane (broadcast)
+                load_raw32(p.bias + gcol0 + cb0 * 64, min(32, p.N - (tc.n0 + cb0 * 64)), bias_cur);
             if (!warp_wait_bounded<true>(&acc_full[acc], acc_phase, abort_flag, p.status)) break;
             tc_fence_after();
 
             if constexpr (EPI == EPI_PARTIAL) {
                 // fp32 accumulator blocks of 32 rows x 32 columns (128 B rows)
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int cc = 0; cc < 2 * NBLK; ++cc) {
+                    const int c = 2 * cb0 + cc;
                     const int n = tc.n0 + c * 32;
                     const uint32_t buf = buf_base + (seq & 1u) * EPI_BUF_BYTES;
                     if (lane == 0) bulk_wait_group_read<1>();
@@ -602,7 +631,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             } else {
 #pragma unroll 1
-            for (int c = 0; c < BN / 64; ++c) {
+            for (int cc = 0; cc < NBLK; ++cc) {
+                const int c = cb0 + cc;
                 const int n64 = tc.n0 + c * 64;
                 uint32_t buf0, buf1;
                 if constexpr (EPI == EPI_BIAS_GELU) {  // Z and H: both buffers
@@ -622,10 +652,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + c * 64 + 32,
                           r2[1]);
                 tmem_wait_ld();
-                if (c == BN / 64 - 1) {
-                    // every column of this accumulator is in registers: the MMA
-                    // may start the tile after next on it while the last block
-                    // is staged and stored
+                if (cc == NBLK - 1) {
+                    // every column of this warp's part of the accumulator is in
+                    // registers: once all epilogue warps are here the MMA may
+                    // start the tile after next on it while the last block is
+                    // staged and stored
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) {
@@ -638,12 +669,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     const int n = n64 + half * 32;
+                    const bool more = cc * 64 + half * 32 + 32 < NBLK * 64;  // another block follows
                     if constexpr (kAux) {
-                        if (c * 64 + half * 32 + 32 < BN) {
+                        if (more) {
                             const int vn = row_ok ? min(32, p.N - (n + 32)) : 0;
                             load_raw32(p.aux + grow * p.ld_aux + gcol0 + c * 64 + half * 32 + 32, vn,
                                        aux_nxt);
                         }
+                    }
+                    if constexpr (kBias) {
+                        if (more)
+                            load_raw32(p.bias + gcol0 + c * 64 + half * 32 + 32, min(32, p.N - (n + 32)),
+                                       bias_nxt);
                     }
                     const uint32_t(&r)[32] = r2[half];
                     const int cvalid = min(32, p.N - n);  // columns inside the shard
@@ -654,9 +691,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 
                     if constexpr (EPI == EPI_BIAS_GELU) {
-                        if (valid > 0) {
+                        {
                             float b[32];
-                            load_bf16x32(p.bias + gcol, valid, b);
+                            unpack32(bias_cur, b);
 #pragma unroll
                             for (int i = 0; i < 32; ++i) v[i] += b[i];
                         }
@@ -667,7 +704,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     } else if constexpr (EPI == EPI_BIAS_RESIDUAL) {
                         if (valid > 0) {
                             float b[32], res[32];
-                            load_bf16x32(p.bias + gcol, valid, b);
+                            unpack32(bias_cur, b);
                             unpack32(aux_cur, res);
                             if (p.drop.threshold == 0u) {
 #pragma unroll
@@ -692,9 +729,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                         stage_row(buf0 + my_row, half, swz, v);
                     } else if constexpr (EPI == EPI_BIAS) {
-                        if (valid > 0) {
+                        {
                             float b[32];
-                            load_bf16x32(p.bias + gcol, valid, b);
+                            unpack32(bias_cur, b);
 #pragma unroll
                             for (int i = 0; i < 32; ++i) v[i] += b[i];
                         }
@@ -723,6 +760,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if constexpr (kAux) {
 #pragma unroll
                         for (int i = 0; i < 4; ++i) aux_cur[i] = aux_nxt[i];
+                    }
+                    if constexpr (kBias) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) bias_cur[i] = bias_nxt[i];
                     }
                 }
                 fence_proxy_async_smem();  // staged rows visible to the TMA store
@@ -763,14 +804,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_before();
     if constexpr (PAIR) {
         cluster_sync();  // every remote arrive and multicast commit has landed
-        if (warp == 5) {
+        if (warp == MMA_WARP) {
             tc_fence_after();
             tmem_dealloc_pair(tmem_base, TMEM_COLS);
         }
         cluster_sync();
     } else {
         __syncthreads();
-        if (warp == 5) {
+        if (warp == MMA_WARP) {
             tc_fence_after();
             tmem_dealloc(tmem_base, TMEM_COLS);
         }

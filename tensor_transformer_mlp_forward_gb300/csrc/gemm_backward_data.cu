@@ -6,6 +6,10 @@ namespace tpmlp {
 
 cudaError_t launch_dgelu(const GemmMaps& m, const GemmArgs& g, int grid,
                         bool pair, cudaStream_t st) {
+    if (g.epi_warps == 8) {
+        if (pair) return launch_gemm<false, false, EPI_DGELU, true, 8>(m, g, grid, st);
+        return launch_gemm<false, false, EPI_DGELU, false, 8>(m, g, grid, st);
+    }
     if (pair) return launch_gemm<false, false, EPI_DGELU, true>(m, g, grid, st);
     return launch_gemm<false, false, EPI_DGELU, false>(m, g, grid, st);
 }

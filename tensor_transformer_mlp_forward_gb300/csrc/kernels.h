@@ -16,7 +16,8 @@ struct GemmMaps {
 };
 
 // Each launcher runs the CTA-pair kernel when `pair` is set (grid even,
-// launched as clusters of 2), else the single-CTA kernel.
+// launched as clusters of 2), else the single-CTA kernel; where the
+// epilogue has an eight-warp form, g.epi_warps (4 or 8) picks it.
 // A K-major, B MN-major: the forward GEMMs.
 cudaError_t launch_column_gelu(const GemmMaps& m, const GemmArgs& g,
                                int grid, bool pair, cudaStream_t st);
@@ -104,11 +105,12 @@ cudaError_t launch_attn_backward(const CUtensorMap& tm_qkv128, const CUtensorMap
 // `grid` is the number of work units wanted (CTAs, or CTA pairs when PAIR);
 // it is clipped to what can be resident at once, so the persistent loop never
 // waits for a second wave of CTAs.
-template <bool A_MN, bool B_MN, int EPI, bool PAIR>
+template <bool A_MN, bool B_MN, int EPI, bool PAIR, int EW = 4>
 cudaError_t launch_gemm(const GemmMaps& m, const GemmArgs& g, int grid,
                         cudaStream_t st) {
-    auto kern = tcgen05_gemm_kernel<A_MN, B_MN, EPI, PAIR>;
-    constexpr int smem = Geometry<PAIR>::SMEM_BYTES;
+    auto kern = tcgen05_gemm_kernel<A_MN, B_MN, EPI, PAIR, EW>;
+    constexpr int smem = Geometry<PAIR, EW>::SMEM_BYTES;
+    constexpr int threads = Geometry<PAIR, EW>::THREADS;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -117,7 +119,7 @@ cudaError_t launch_gemm(const GemmMaps& m, const GemmArgs& g, int grid,
         if (resident_clusters == 0) {
             cudaLaunchConfig_t q = {};
             q.gridDim = dim3(2 * static_cast<unsigned>(grid));
-            q.blockDim = dim3(NUM_THREADS);
+            q.blockDim = dim3(threads);
             q.dynamicSmemBytes = smem;
             cudaLaunchAttribute qa[1];
             qa[0].id = cudaLaunchAttributeClusterDimension;
@@ -134,18 +136,25 @@ cudaError_t launch_gemm(const GemmMaps& m, const GemmArgs& g, int grid,
         grid = 2 * (grid < resident_clusters ? grid : resident_clusters);
     }
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    unsigned na = 0;
     if (PAIR) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 2;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
     }
+    if (g.dependent_launch) {  // may begin before the previous kernel ends (pdl_wait inside)
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = na ? attr : nullptr;
+    cfg.numAttrs = na;
     e = cudaLaunchKernelEx(&cfg, kern, m.a, m.b, m.o0, m.o1, g);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

@@ -63,6 +63,7 @@ __global__ void __launch_bounds__(512)
                       int h, float eps, __nv_bfloat16* __restrict__ X,
                       __nv_bfloat16* __restrict__ s_out, float* __restrict__ mean,
                       float* __restrict__ rstd) {
+    pdl_launch_dependents();  // the next kernel may begin its launch
     extern __shared__ float srow[];
     __shared__ float scratch[32];
     const long long base = static_cast<long long>(blockIdx.x) * h;
@@ -109,6 +110,7 @@ __global__ void __launch_bounds__(512)
                             const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __restrict__ r,
                             const __nv_bfloat16* __restrict__ gamma, const float* __restrict__ mean,
                             const float* __restrict__ rstd, int h, __nv_bfloat16* __restrict__ ds) {
+    pdl_launch_dependents();  // the next kernel may begin its launch
     __shared__ float scratch[32];
     const long long base = static_cast<long long>(blockIdx.x) * h;
     const int nvec = h >> 3;
@@ -159,6 +161,7 @@ __global__ void __launch_bounds__(256)
                          const __nv_bfloat16* __restrict__ r, const float* __restrict__ mean,
                          const float* __restrict__ rstd, int T, int h, int rows_per_chunk,
                          float* __restrict__ pg, float* __restrict__ pb) {
+    pdl_launch_dependents();  // the next kernel may begin its launch
     __shared__ float part[2][8][64];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int col0 = blockIdx.x * 64 + (lane & 7) * 8;
@@ -221,6 +224,7 @@ __global__ void __launch_bounds__(LN_THREADS)
                           const __nv_bfloat16* __restrict__ beta, int h, float eps,
                           __nv_bfloat16* __restrict__ X, __nv_bfloat16* __restrict__ s_out,
                           float* __restrict__ mean, float* __restrict__ rstd) {
+    pdl_launch_dependents();  // the next kernel may begin its launch
     __shared__ float scratch[32];
     const long long base = static_cast<long long>(blockIdx.x) * h;
     const int nvec = h >> 3;
@@ -272,6 +276,7 @@ __global__ void __launch_bounds__(LN_THREADS)
 // out[j] = sum_{i < rows} P[i * n + j], in row order.
 __global__ void __launch_bounds__(256)
     ln_rowsum_kernel(const float* __restrict__ P, int rows, int n, float* __restrict__ out) {
+    pdl_launch_dependents();  // the next kernel may begin its launch
     const int j = blockIdx.x * blockDim.x + threadIdx.x;
     if (j >= n) return;
     float s = 0.0f;

@@ -288,6 +288,19 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Programmatic dependent launch.  A kernel launched with the programmatic
+// stream serialization attribute may begin (its CTAs scheduled, its
+// prologue run) while the kernel before it on the stream is still running;
+// pdl_wait() returns once that kernel has completed and its memory
+// operations are visible, and is a no-op for a kernel launched without the
+// attribute.  pdl_launch_dependents() signals that the next such kernel may
+// begin launching: once every CTA of this grid has signalled (or exited).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ float tanh_approx(float x) {
     float y;
     asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));

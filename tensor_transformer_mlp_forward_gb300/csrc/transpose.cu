@@ -36,6 +36,7 @@ constexpr int kTransposeThreads = 256;
 __global__ void __launch_bounds__(kTransposeThreads)
     transpose_bf16_kernel(const uint16_t* __restrict__ in, int rows, int cols,
                           uint16_t* __restrict__ out, int ld_out, int col_tiles) {
+    pdl_launch_dependents();  // the next kernel may begin its launch
     __shared__ __align__(16) uint32_t sT[kTile * kTile / 2];  // [output row c][word]
     const int tid = threadIdx.x;
     const int tr = static_cast<int>(blockIdx.x / col_tiles);

@@ -104,6 +104,73 @@ def test_pairs_and_single_cta_agree_bitwise():
         assert torch.equal(single[k], pairs[k]), k
 
 
+@pytest.mark.parametrize("w", [
+    inputs.custom(T=300, h=200, F=1536, t=4, seed=21),     # ragged rows and columns
+    inputs.custom(T=257, h=520, F=1600, t=8, seed=22),     # f = 200: ragged shard tails
+    inputs.custom(T=1100, h=1024, F=4096, t=2, seed=23),   # K = 1024: the short-reduction form
+    inputs.custom(T=640, h=2176, F=8704, t=1, seed=24),    # K-major weight gradients off, long K
+], ids=lambda w: f"T{w.T}_h{w.h}_F{w.F}_t{w.t}")
+@pytest.mark.parametrize("pair", [0, 2], ids=["single_cta", "cta_pairs"])
+def test_epilogue_warp_forms_agree_bitwise(w, pair):
+    """Four and eight epilogue warps (the dZ GEMM's two forms) give every
+    output element the same arithmetic: the whole block is bit for bit the
+    same in both forms."""
+    cpu = inputs.make_inputs(w)
+    prev_pair = binding.set_cta_pair_mode(pair)
+    prev = binding.set_epilogue_warps(4)
+    try:
+        four = run_gpu(cpu, w.t)
+        binding.set_epilogue_warps(8)
+        eight = run_gpu(cpu, w.t)
+    finally:
+        binding.set_epilogue_warps(prev)
+        binding.set_cta_pair_mode(prev_pair)
+    for k in four:
+        assert torch.equal(four[k], eight[k]), k
+
+
+def test_dependent_launch_changes_nothing():
+    """GEMMs launched as programmatic dependents wait for the kernel before
+    them before touching global memory: the block's outputs are the same
+    bits with the launch mode on and off, eagerly and replayed from a CUDA
+    graph (where the dependencies become programmatic graph edges)."""
+    w = inputs.custom(T=1100, h=1024, F=4096, t=2, seed=25)
+    cpu = inputs.make_inputs(w)
+    prev = binding.set_dependent_launch(0)
+    try:
+        plain = run_gpu(cpu, w.t)
+        binding.set_dependent_launch(1)
+        dep = run_gpu(cpu, w.t)
+        g = {k: v.cuda() for k, v in cpu.items()}
+        outs = {k: torch.empty_like(v) for k, v in dep.items()}
+        ws_f = torch.empty(max(16, binding.split_workspace_bytes(w.T, w.h, w.F, w.t)),
+                           dtype=torch.uint8, device="cuda")
+        ws_b = torch.empty(binding.tp_mlp_backward_workspace_bytes(w.T, w.h, w.F, w.t),
+                           dtype=torch.uint8, device="cuda")
+
+        def block():
+            binding.tp_mlp_forward(g["X"], g["A"], g["b1"], g["B"], g["b2"], g["residual"], w.t,
+                                   Y=outs["Y"], Z=outs["Z"], H=outs["H"], workspace=ws_f)
+            binding.tp_mlp_backward(g["dY"], g["X"], g["A"], g["B"], outs["Z"], outs["H"], w.t,
+                                    dX=outs["dX"], dA=outs["dA"], dB=outs["dB"], db1=outs["db1"],
+                                    db2=outs["db2"], workspace=ws_b)
+        block()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            block()
+        for v in outs.values():
+            v.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+    finally:
+        binding.set_dependent_launch(prev)
+    assert binding.device_status() == 0
+    for k in plain:
+        assert torch.equal(plain[k], dep[k]), k
+        assert torch.equal(plain[k], outs[k]), k
+
+
 def test_split_reduction_matches_unsplit():
     """The row-parallel GEMMs with and without a split reduction (few output
     tiles: T=512, h=4096 gives 2 x 16 tiles) agree up to the bf16 rounding of
