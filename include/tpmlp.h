@@ -154,16 +154,15 @@ int tp_mlp_row_sum(const tpmlp_bf16* H, const tpmlp_bf16* B, const tpmlp_bf16* b
                    void* workspace, size_t workspace_bytes, void* stream);
 
 /* Float32 elements of scratch tp_mlp_bias_grad needs: the row chunks'
- * partial sums and one completion count per 64-column block. */
+ * partial sums. */
 size_t tp_mlp_bias_grad_workspace_floats(int T, int n);
 
 /* a4 (and the reduction of a6): column sums of a [T, n] bf16 matrix,
  * db[j] = sum_r G[r, j], in float32, deterministic.  Used for db2 = sum_rows
  * dY (the g operator is the identity backward, so dY reaches b2 whole).
  * `partial` must hold tp_mlp_bias_grad_workspace_floats(T, n) floats, any
- * contents.  One kernel launch (after a small memset of the counts on the
- * stream): the last CTA of each column block, counted in `partial`, adds the
- * row chunks' partials in chunk order. */
+ * contents.  One kernel writes the row chunks' partial sums, a second adds
+ * them in chunk order (one kernel when T is small enough for one chunk). */
 int tp_mlp_bias_grad(const tpmlp_bf16* G, int T, int n, float* db, float* partial,
                      void* stream);
 
@@ -180,10 +179,10 @@ int tp_mlp_bias_grad(const tpmlp_bf16* G, int T, int n, float* db, float* partia
  * TPMLP_ERR_WORKSPACE (nothing launched).  The first call on each device
  * looks up the array's device address: make it before any stream capture.
  * All calls on a device share the array, which keeps what the last call
- * left there: each call clears the completion counts it needs on its
- * stream and overwrites the partial rows before reading them, so no result
- * depends on an earlier call; calls whose kernels overlap on the GPU
- * (different streams, no ordering) race on it. */
+ * left there: each call overwrites the partial rows it uses before reading
+ * them, so no result depends on an earlier call and nothing needs clearing;
+ * calls whose kernels overlap on the GPU (different streams, no ordering)
+ * race on it. */
 int tp_mlp_bias_grad_noalloc(const tpmlp_bf16* G, int T, int n, float* db, void* stream);
 
 /* Capacity, in floats, of the array tp_mlp_bias_grad_noalloc uses. */
@@ -527,13 +526,15 @@ int tpmlp_set_cta_pair_mode(int mode);
  * are bitwise identical across modes. */
 int tpmlp_set_epilogue_warps(int mode);
 
-/* Whether GEMM kernels are launched as programmatic dependents of the
- * kernel before them on the stream (process-wide; returns the previous
- * setting, or -1 for a value other than 0 or 1).  1 (default): a GEMM's CTAs
- * may start, and set up their barriers and tensor memory, while that kernel
- * finishes; they read and write global memory only after it has completed,
- * so results are identical either way.  0: plain stream order. */
-int tpmlp_set_dependent_launch(int on);
+/* Which of the library's kernels are launched as programmatic dependents of
+ * the kernel before them on the stream (process-wide; returns the previous
+ * mode, or -1 for a mode outside 0..3): bit 0 the GEMMs, bit 1 the
+ * column-sum, reduction, transpose and dropout kernels.  A dependent's CTAs
+ * may start, and set up their barriers and tensor memory, while the kernel
+ * before it finishes; they read and write global memory only after it has
+ * completed, so results are identical in every mode.  0: plain stream
+ * order; 3 (both) is the default. */
+int tpmlp_set_dependent_launch(int mode);
 
 /* Static text for a status code. */
 const char* tp_mlp_status_string(int status);

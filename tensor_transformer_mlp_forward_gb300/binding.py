@@ -191,12 +191,13 @@ def set_epilogue_warps(mode: int) -> int:
     return prev
 
 
-def set_dependent_launch(on: int) -> int:
-    """1 (default): GEMMs start as programmatic dependents of the kernel
-    before them; 0: plain stream order.  Returns the previous setting."""
-    prev = int(lib().tpmlp_set_dependent_launch(on))
+def set_dependent_launch(mode: int) -> int:
+    """Which kernels start as programmatic dependents of the kernel before
+    them: bit 0 the GEMMs, bit 1 the others (3, the default: both; 0: plain
+    stream order).  Returns the previous mode."""
+    prev = int(lib().tpmlp_set_dependent_launch(mode))
     if prev < 0:
-        raise ValueError(f"invalid setting {on}")
+        raise ValueError(f"invalid mode {mode}")
     return prev
 
 

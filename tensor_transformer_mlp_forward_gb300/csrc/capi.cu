@@ -188,22 +188,33 @@ int operand_map(CUtensorMap* m, const Operand& o, int t, int tile_rows) {
 
 // 0: single-CTA kernel only, 1: CTA pairs when the problem fills them, 2: pairs always.
 std::atomic<int> g_pair_mode{1};
-// Epilogue warps of the GEMMs that have both forms: 0 = by the reduction's
-// length (epi_warps_for), 4 or 8 = always that form.
+// Epilogue warps of the dZ GEMM (the one GEMM with both forms): 0 = by the
+// reduction's length (epi_warps_for), 4 or 8 = always that form.
 std::atomic<int> g_epi_mode{0};
 
+// Which of the library's kernels are launched as programmatic dependents of
+// the kernel before them on the stream (their set-up overlaps its end): bit 0
+// the GEMMs, bit 1 the other kernels; 0: plain stream order.
+std::atomic<int> g_dependent_launch{3};
+
 // A tile's mainloop lasts its reduction's k-blocks (512 clocks each for a
-// CTA pair at the full MMA rate); its epilogue does not shrink with it.  Up
-// to 32 k-blocks (K <= 2048) the epilogue of four warps is what bounds the
-// tile, and eight warps, two per scheduler, hide each other's latencies.
-// 1: GEMMs are launched as programmatic dependents of the kernel before
-// them on the stream (their set-up overlaps its end), 0: plain stream order.
-std::atomic<int> g_dependent_launch{1};
+// CTA pair at the full MMA rate); its epilogue does not shrink with it.  The
+// dZ GEMM's epilogue (a read of Z, GeLU', the db1 column sums) is the
+// heaviest: with 16 k-blocks or fewer (K <= 1024) four warps bound the tile
+// and eight, two per scheduler, hide each other's latencies (dZ of the
+// GPT-2-medium block, K = 1024: 81.9 -> 73.7 us).  Elsewhere the stage the
+// eight warps' staging buffers take costs more than they gain (measured 2-17 %
+// slower on the other GEMMs and at longer K), so only that kernel has the form.
+}  // namespace
+
+bool dependent_launch() { return (g_dependent_launch.load(std::memory_order_relaxed) & 2) != 0; }
+
+namespace {
 
 int epi_warps_for(long long total_kb) {
     const int mode = g_epi_mode.load(std::memory_order_relaxed);
     if (mode == 4 || mode == 8) return mode;
-    return total_kb <= 32 ? 8 : 4;
+    return total_kb <= 16 ? 8 : 4;
 }
 
 #ifndef TPMLP_BAND_BUDGET_MB
@@ -389,7 +400,7 @@ int run_gemm(Launcher fn, const Operand& a, const Operand& b, const Output& out,
     tile_space(g, f.M, f.N, f.K, f.t, f.mode, f.a_bytes, f.b_bytes, tile_m);
     if (g.num_tiles == 0) return TPMLP_OK;
     g.epi_warps = epi_warps_for(1LL * g.k_blocks * (f.mode == SHARD_K ? f.t : 1));
-    g.dependent_launch = g_dependent_launch.load(std::memory_order_relaxed);
+    g.dependent_launch = g_dependent_launch.load(std::memory_order_relaxed) & 1;
     if (out.k_splits > 1) {
         g.k_splits = out.k_splits;
         g.num_tiles = g.base_tiles * out.k_splits;
@@ -542,6 +553,7 @@ __global__ void __launch_bounds__(256)
                         const __nv_bfloat16* __restrict__ bias, const __nv_bfloat16* __restrict__ res,
                         Dropout dr, __nv_bfloat16* __restrict__ out) {
     pdl_launch_dependents();  // the next kernel may begin its launch
+    pdl_wait();               // its inputs come from the kernel before it
     const long long i = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
     if (i >= count) return;
     float a[8];
@@ -566,6 +578,7 @@ __global__ void __launch_bounds__(256)
                        const __nv_bfloat16* __restrict__ bias, const __nv_bfloat16* __restrict__ res,
                        Dropout dr, __nv_bfloat16* __restrict__ out) {
     pdl_launch_dependents();  // the next kernel may begin its launch
+    pdl_wait();               // its inputs come from the kernel before it
     const int local = static_cast<int>(blockIdx.x >> 5);
     const int e = static_cast<int>(((blockIdx.x & 31u) * blockDim.x + threadIdx.x) * 8u);
     const int r = e / BN, c = e % BN;
@@ -591,10 +604,9 @@ int launch_tail_reduce(const float* P, int S, const GemmArgs& g, long long first
     GemmArgs r = g;
     r.tile_offset = static_cast<int>(first);
     r.base_tiles = static_cast<int>(X);
-    tail_reduce_kernel<<<static_cast<unsigned>(X * 32), 256, 0, st>>>(
-        P, S, r, static_cast<int>(X), cb(ts.bias), cb(ts.res), ts.dr,
-        reinterpret_cast<__nv_bfloat16*>(out));
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_dependent(tail_reduce_kernel, dim3(static_cast<unsigned>(X * 32)),
+                                     dim3(256), 0, st, P, S, r, static_cast<int>(X), cb(ts.bias),
+                                     cb(ts.res), ts.dr, reinterpret_cast<__nv_bfloat16*>(out));
     if (e != cudaSuccess) return fail_cuda(e);
     ++t_last_launches;
     return TPMLP_OK;
@@ -604,9 +616,10 @@ int launch_split_reduce(const float* P, int splits, int T, int h, const tpmlp_bf
                         const tpmlp_bf16* res, const Dropout& dr, tpmlp_bf16* out,
                         cudaStream_t st) {
     const long long count = 1LL * T * h;
-    split_reduce_kernel<<<static_cast<unsigned>(cdiv(count / 8, 256)), 256, 0, st>>>(
-        P, splits, count, h, cb(bias), cb(res), dr, reinterpret_cast<__nv_bfloat16*>(out));
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_dependent(split_reduce_kernel,
+                                     dim3(static_cast<unsigned>(cdiv(count / 8, 256))), dim3(256), 0,
+                                     st, P, splits, count, h, cb(bias), cb(res), dr,
+                                     reinterpret_cast<__nv_bfloat16*>(out));
     if (e != cudaSuccess) return fail_cuda(e);
     ++t_last_launches;
     return TPMLP_OK;
@@ -676,6 +689,7 @@ __global__ void __launch_bounds__(kDropThreads)
     dropout_grad_kernel(const __nv_bfloat16* __restrict__ dY, long long count, Dropout dr,
                         __nv_bfloat16* __restrict__ dP) {
     pdl_launch_dependents();  // the next kernel may begin its launch
+    pdl_wait();               // its inputs come from the kernel before it
     const long long base = static_cast<long long>(blockIdx.x) * kDropThreads * kDropVec * 8;
     uint4 g[kDropVec];
 #pragma unroll
@@ -709,10 +723,9 @@ int dropout_grad(const tpmlp_bf16* dY, int T, int h, const Dropout& dr, tpmlp_bf
                  cudaStream_t st) {
     const long long count = 1LL * T * h;
     if (count == 0) return TPMLP_OK;
-    dropout_grad_kernel<<<static_cast<unsigned>(cdiv(count, 8LL * kDropThreads * kDropVec)),
-                          kDropThreads, 0, st>>>(cb(dY), count, dr,
-                                                 reinterpret_cast<__nv_bfloat16*>(dP));
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_dependent(
+        dropout_grad_kernel, dim3(static_cast<unsigned>(cdiv(count, 8LL * kDropThreads * kDropVec))),
+        dim3(kDropThreads), 0, st, cb(dY), count, dr, reinterpret_cast<__nv_bfloat16*>(dP));
     if (e != cudaSuccess) return fail_cuda(e);
     ++t_last_launches;
     return TPMLP_OK;
@@ -1051,8 +1064,8 @@ TPMLP_API int tp_mlp_bias_grad_noalloc(const tpmlp_bf16* G, int T, int n, float*
     if (any_null(db) || (T > 0 && any_null(G))) return TPMLP_ERR_NULL;
     if (!all_aligned(G, db)) return TPMLP_ERR_ALIGN;
     // Same row chunks as tp_mlp_bias_grad; one chunk needs no partials.
-    // The completion counts inside the array are cleared on the stream
-    // before each use, so nothing carries over from an earlier call.
+    // Every partial row is written before it is read, so nothing carries
+    // over from an earlier call.
     if (T > 0 && colsum_chunks(T, n) > 1 &&
         colsum_workspace_floats(T, n) > static_cast<size_t>(kNoAllocScratchFloats))
         return TPMLP_ERR_WORKSPACE;
@@ -1793,9 +1806,9 @@ TPMLP_API int tpmlp_set_cta_pair_mode(int mode) {
     return g_pair_mode.exchange(mode);
 }
 
-TPMLP_API int tpmlp_set_dependent_launch(int on) {
-    if (on != 0 && on != 1) return -1;
-    return g_dependent_launch.exchange(on);
+TPMLP_API int tpmlp_set_dependent_launch(int mode) {
+    if (mode < 0 || mode > 3) return -1;
+    return g_dependent_launch.exchange(mode);
 }
 
 TPMLP_API int tpmlp_set_epilogue_warps(int mode) {

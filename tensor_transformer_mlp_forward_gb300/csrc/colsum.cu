@@ -8,10 +8,12 @@
 //   db[j] = sum_{r < T} G[r * n + j]
 //
 // HBM-bound: 2 bytes read per element.  A 2-D grid of 64-column blocks x
-// row chunks (about 640 CTAs) writes one fp32 partial row per chunk; the
-// last CTA of each column block to finish (counted in the caller's
-// workspace, cleared before the launch) adds that block's chunk partials in
-// chunk order, so the result does not depend on which CTA comes last.
+// row chunks (about 640 CTAs) writes one fp32 partial row per chunk; a
+// second kernel adds the chunks' rows in chunk order, so the result does not
+// depend on which CTA runs when.  Both are launched as programmatic
+// dependents: each may be scheduled while the kernel before it finishes, so
+// the second launch costs no gap, and no counter or cleared scratch word is
+// needed.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -37,11 +39,11 @@ constexpr int kTargetCtas = 640;
 // 32 KiB per CTA are in flight; the adds stay in row order.  The 4 row
 // phases meet by warp shuffle, the 8 warps in shared memory, in a fixed
 // order.  Writes out[blockIdx.y * n + col].
-template <bool kFinish>
 __global__ void __launch_bounds__(kSumThreads)
     colsum_partial_kernel(const __nv_bfloat16* __restrict__ G, int T, int n, int rows_per_chunk,
-                          float* __restrict__ out, float* __restrict__ db, unsigned int* counts) {
+                          float* __restrict__ out) {
     pdl_launch_dependents();  // the next kernel may begin its launch
+    pdl_wait();               // G is written by the kernel before this one
     __shared__ float part[kSumThreads / 32][kColBlock];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int col0 = blockIdx.x * kColBlock + (lane & 7) * 8;
@@ -99,30 +101,6 @@ __global__ void __launch_bounds__(kSumThreads)
         for (int w = 0; w < kSumThreads / 32; ++w) s += part[w][threadIdx.x];
         if (col < n) out[static_cast<long long>(blockIdx.y) * n + col] = s;
     }
-    if constexpr (kFinish) {
-        // the last of the column block's gridDim.y CTAs adds their partial
-        // rows: 4 groups of 64 threads take chunks g, g + 4, ... in order,
-        // then the 4 group sums are added in group order
-        __shared__ bool last;
-        __threadfence();  // this CTA's partial row is visible before it is counted
-        __syncthreads();
-        if (threadIdx.x == 0) last = atomicAdd(&counts[blockIdx.x], 1u) == gridDim.y - 1;
-        __syncthreads();
-        if (!last) return;
-        __threadfence();
-        const int g = threadIdx.x / kColBlock, c = threadIdx.x % kColBlock;
-        const int col = blockIdx.x * kColBlock + c;
-        float s = 0.0f;
-        if (col < n) {
-#pragma unroll 4
-            for (int i = g; i < static_cast<int>(gridDim.y); i += kSumThreads / kColBlock)
-                s += __ldcg(out + static_cast<long long>(i) * n + col);
-        }
-        part[g][c] = s;
-        __syncthreads();
-        if (g == 0 && col < n)
-            db[col] = ((part[0][c] + part[1][c]) + part[2][c]) + part[3][c];
-    }
 }
 
 // out[j] = sum_{i < rows} P[i * n + j].  A 256-thread CTA covers 32 columns:
@@ -134,6 +112,7 @@ constexpr int kRowsumGroups = 8;
 __global__ void __launch_bounds__(kRowsumCols * kRowsumGroups)
     rowsum_kernel(const float* __restrict__ P, int rows, int n, float* __restrict__ out) {
     pdl_launch_dependents();  // the next kernel may begin its launch
+    pdl_wait();               // P is written by the kernel before this one
     __shared__ float part[kRowsumGroups][kRowsumCols];
     const int g = threadIdx.x / kRowsumCols, c = threadIdx.x % kRowsumCols;
     const int j = blockIdx.x * kRowsumCols + c;
@@ -162,48 +141,32 @@ int colsum_chunks(int T, int n) {
 }
 
 size_t colsum_workspace_floats(int T, int n) {
-    const int chunks = colsum_chunks(T, n);
-    const size_t rows = static_cast<size_t>(chunks) * static_cast<size_t>(n);
-    if (chunks == 1) return rows;
-    // the completion counts (one 32-bit word per column block) follow the
-    // partial rows, padded to 16 bytes
-    return rows + ((static_cast<size_t>(cdiv_ll(n, kColBlock)) + 3) & ~static_cast<size_t>(3));
+    return static_cast<size_t>(colsum_chunks(T, n)) * static_cast<size_t>(n);
 }
 
 cudaError_t launch_rowsum_f32(const float* P, int rows, int n, float* out, cudaStream_t st,
                               int* launches) {
     if (n == 0) return cudaSuccess;
-    rowsum_kernel<<<static_cast<unsigned>(cdiv_ll(n, kRowsumCols)), kRowsumCols * kRowsumGroups, 0,
-                    st>>>(P, rows, n, out);
+    cudaError_t e = launch_dependent(rowsum_kernel,
+                                     dim3(static_cast<unsigned>(cdiv_ll(n, kRowsumCols))),
+                                     dim3(kRowsumCols * kRowsumGroups), 0, st, P, rows, n, out);
     if (launches) ++*launches;
-    return cudaGetLastError();
+    return e;
 }
 
-// T == 0 or n == 0 launches nothing and leaves db as it was.  With more than
-// one row chunk, `partial` holds colsum_workspace_floats(T, n) floats: the
-// chunks' partial rows, then the column blocks' completion counts, which are
-// cleared on the stream before the kernel runs, so the workspace may hold
-// anything on entry and no state is shared between calls.
+// T == 0 or n == 0 launches nothing and leaves db as it was.
 cudaError_t launch_colsum(const __nv_bfloat16* G, int T, int n, float* db, float* partial,
                           cudaStream_t st, int* launches) {
     if (T == 0 || n == 0) return cudaSuccess;
     const int chunks = colsum_chunks(T, n);
     const int rows_per_chunk = static_cast<int>(cdiv_ll(T, chunks));
     const dim3 grid(static_cast<unsigned>(cdiv_ll(n, kColBlock)), static_cast<unsigned>(chunks));
-    if (chunks == 1) {  // one chunk: its partial row is the result
-        colsum_partial_kernel<false><<<grid, kSumThreads, 0, st>>>(G, T, n, rows_per_chunk, db,
-                                                                  nullptr, nullptr);
-        if (launches) ++*launches;
-        return cudaGetLastError();
-    }
-    unsigned int* counts =
-        reinterpret_cast<unsigned int*>(partial + static_cast<size_t>(chunks) * static_cast<size_t>(n));
-    cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(unsigned int) * grid.x, st);
-    if (e != cudaSuccess) return e;
-    colsum_partial_kernel<true><<<grid, kSumThreads, 0, st>>>(G, T, n, rows_per_chunk, partial, db,
-                                                             counts);
+    // one chunk: its partial row is the result
+    cudaError_t e = launch_dependent(colsum_partial_kernel, grid, dim3(kSumThreads), 0, st, G, T, n,
+                                     rows_per_chunk, chunks == 1 ? db : partial);
     if (launches) ++*launches;
-    return cudaGetLastError();
+    if (e != cudaSuccess || chunks == 1) return e;
+    return launch_rowsum_f32(partial, chunks, n, db, st, launches);
 }
 
 }  // namespace tpmlp

@@ -7,7 +7,37 @@
 
 #include "gemm.cuh"
 
+#include <utility>
+
 namespace tpmlp {
+
+// Whether the library's kernels are launched as programmatic dependents of
+// the kernel before them on the stream (tpmlp_set_dependent_launch).
+bool dependent_launch();
+
+// Launches `kern` with the programmatic stream serialization attribute when
+// dependent launch is on, else as a plain launch.  Every kernel launched
+// this way calls pdl_wait() before its first global memory access, so it may
+// be scheduled (and run its set-up) while the previous kernel finishes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t st, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    if (dependent_launch()) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
 
 // The four tensor maps of one GEMM: operands A and B, output o0 (and o1, the
 // second output of the bias + GeLU epilogue; a copy of o0 otherwise).
@@ -51,12 +81,11 @@ cudaError_t launch_transpose(const __nv_bfloat16* in, int rows, int cols, __nv_b
                              int ld_out, cudaStream_t st, int* launches);
 
 // Column sums db[j] = sum_{r < T} G[r * n + j] of a bf16 [T, n] matrix in
-// fp32 (colsum.cu), one kernel launch.  With colsum_chunks(T, n) > 1 row
-// chunks the chunks' partial rows go to `partial` and are added in chunk
-// order by the last CTA of each column block, counted in words of `partial`
-// after the rows that a memset on the stream clears first; `partial` holds
-// colsum_workspace_floats(T, n) floats, 16-byte aligned, any contents.  With
-// one chunk db is written directly.  T == 0 or n == 0 launches nothing.
+// fp32 (colsum.cu).  With colsum_chunks(T, n) > 1 row chunks the chunks'
+// partial rows go to `partial` (colsum_workspace_floats(T, n) floats,
+// 16-byte aligned, any contents) and a second kernel adds them in chunk
+// order; with one chunk db is written directly.  T == 0 or n == 0 launches
+// nothing.
 int colsum_chunks(int T, int n);
 size_t colsum_workspace_floats(int T, int n);
 cudaError_t launch_colsum(const __nv_bfloat16* G, int T, int n, float* db, float* partial,

@@ -37,6 +37,7 @@ __global__ void __launch_bounds__(kTransposeThreads)
     transpose_bf16_kernel(const uint16_t* __restrict__ in, int rows, int cols,
                           uint16_t* __restrict__ out, int ld_out, int col_tiles) {
     pdl_launch_dependents();  // the next kernel may begin its launch
+    pdl_wait();               // `in` comes from the kernel before this one
     __shared__ __align__(16) uint32_t sT[kTile * kTile / 2];  // [output row c][word]
     const int tid = threadIdx.x;
     const int tr = static_cast<int>(blockIdx.x / col_tiles);
@@ -85,11 +86,12 @@ cudaError_t launch_transpose(const __nv_bfloat16* in, int rows, int cols, __nv_b
     const int col_tiles = (cols + kTile - 1) / kTile;
     const long long tiles = static_cast<long long>((rows + kTile - 1) / kTile) * col_tiles;
     if (tiles > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-    transpose_bf16_kernel<<<static_cast<unsigned>(tiles), kTransposeThreads, 0, st>>>(
-        reinterpret_cast<const uint16_t*>(in), rows, cols, reinterpret_cast<uint16_t*>(out),
-        ld_out, col_tiles);
+    cudaError_t e = launch_dependent(transpose_bf16_kernel, dim3(static_cast<unsigned>(tiles)),
+                                     dim3(kTransposeThreads), 0, st,
+                                     reinterpret_cast<const uint16_t*>(in), rows, cols,
+                                     reinterpret_cast<uint16_t*>(out), ld_out, col_tiles);
     if (launches) ++*launches;
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace tpmlp

@@ -139,7 +139,7 @@ def test_dependent_launch_changes_nothing():
     prev = binding.set_dependent_launch(0)
     try:
         plain = run_gpu(cpu, w.t)
-        binding.set_dependent_launch(1)
+        binding.set_dependent_launch(3)
         dep = run_gpu(cpu, w.t)
         g = {k: v.cuda() for k, v in cpu.items()}
         outs = {k: torch.empty_like(v) for k, v in dep.items()}
