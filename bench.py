@@ -75,6 +75,8 @@ def parse_args(argv=None):
     p.add_argument("--attn-workload", default="attn-gpt2-8.3b")
     p.add_argument("--pair-mode", type=int, default=None,
                    help="GEMM kernel: 0 single CTA, 1 auto (default), 2 CTA pairs")
+    p.add_argument("--tile-scheduler", type=int, default=None,
+                   help="GEMM tile assignment: 0 static persistent, 1 dynamic (cluster launch control)")
     p.add_argument("--call", choices=CALLS, default=None,
                    help="run ONE entry point --repeat times at --shape, holding only its operands "
                         "on the device (the command a profiler wraps to capture one kernel)")
@@ -602,6 +604,8 @@ def run_ours(args, w):
 
     if args.pair_mode is not None:
         binding.set_cta_pair_mode(args.pair_mode)
+    if args.tile_scheduler is not None:
+        binding.set_tile_scheduler(args.tile_scheduler)
     rank, world, local = init_distributed(args.gpus)
     step, dev_s, wall, per_call, clocks, launches, split = time_ours(
         w, args.steps, args.warmup, local, args.dropout, args.recompute)
@@ -918,6 +922,8 @@ def run_call(a) -> int:
 
     T, h, F, t = (int(v) for v in a.shape.split(","))
     p_drop = a.dropout if a.dropout > 0 else 0.1
+    if a.tile_scheduler is not None:
+        b.set_tile_scheduler(a.tile_scheduler)
     dev = torch.device("cuda", 0)
     gen = torch.Generator(device=dev).manual_seed(1234)
 

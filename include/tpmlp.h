@@ -45,8 +45,8 @@
  *    replayed beside eager calls, share no device state -- except the
  *    array of tp_mlp_bias_grad_noalloc, which its calls share (see there).
  *    Process-wide host state: the GEMM launch modes of
- *    tpmlp_set_cta_pair_mode, tpmlp_set_epilogue_warps and
- *    tpmlp_set_dependent_launch (atomics, read at
+ *    tpmlp_set_cta_pair_mode, tpmlp_set_epilogue_warps,
+ *    tpmlp_set_dependent_launch and tpmlp_set_tile_scheduler (atomics, read at
  *    each launch: change them only
  *    while no other thread launches, or results stay equal but the launch
  *    shape may differ between two calls), a once-per-process lookup of the
@@ -535,6 +535,19 @@ int tpmlp_set_epilogue_warps(int mode);
  * completed, so results are identical in every mode.  0: plain stream
  * order; 3 (both) is the default. */
 int tpmlp_set_dependent_launch(int mode);
+
+/* How the GEMM kernels assign output tiles (work units) to CTA pairs
+ * (process-wide; returns the previous mode, or -1 for a mode other than 0
+ * or 1):
+ *   0  default: a persistent grid of as many pairs as fit, pair u taking
+ *      units u, u + pairs, ... in the tile raster order;
+ *   1  one pair per unit in the grid; a running pair takes the next unit by
+ *      cancelling the launch of a pair that has not started (cluster launch
+ *      control), so the units in flight are always a contiguous run of the
+ *      raster order however unevenly the pairs progress.
+ * Both compute every unit with the same sums: results are bitwise identical
+ * across modes. */
+int tpmlp_set_tile_scheduler(int mode);
 
 /* Static text for a status code. */
 const char* tp_mlp_status_string(int status);

@@ -100,6 +100,7 @@ _SIGNATURES = {
     "tpmlp_set_cta_pair_mode": ([_I], _I),
     "tpmlp_set_epilogue_warps": ([_I], _I),
     "tpmlp_set_dependent_launch": ([_I], _I),
+    "tpmlp_set_tile_scheduler": ([_I], _I),
 }
 
 
@@ -196,6 +197,16 @@ def set_dependent_launch(mode: int) -> int:
     them: bit 0 the GEMMs, bit 1 the others (3, the default: both; 0: plain
     stream order).  Returns the previous mode."""
     prev = int(lib().tpmlp_set_dependent_launch(mode))
+    if prev < 0:
+        raise ValueError(f"invalid mode {mode}")
+    return prev
+
+
+def set_tile_scheduler(mode: int) -> int:
+    """0: persistent GEMM grids with a static tile assignment (default);
+    1: dynamic tiles through cluster launch control.  Returns the previous
+    mode."""
+    prev = int(lib().tpmlp_set_tile_scheduler(mode))
     if prev < 0:
         raise ValueError(f"invalid mode {mode}")
     return prev

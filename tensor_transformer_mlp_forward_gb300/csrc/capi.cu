@@ -197,6 +197,10 @@ std::atomic<int> g_epi_mode{0};
 // the GEMMs, bit 1 the other kernels; 0: plain stream order.
 std::atomic<int> g_dependent_launch{3};
 
+// 0: persistent GEMM grids with a static assignment of units to CTA pairs;
+// 1: dynamic units through cluster launch control.
+std::atomic<int> g_tile_scheduler{0};
+
 // A tile's mainloop lasts its reduction's k-blocks (512 clocks each for a
 // CTA pair at the full MMA rate); its epilogue does not shrink with it.  The
 // dZ GEMM's epilogue (a read of Z, GeLU', the db1 column sums) is the
@@ -401,6 +405,7 @@ int run_gemm(Launcher fn, const Operand& a, const Operand& b, const Output& out,
     if (g.num_tiles == 0) return TPMLP_OK;
     g.epi_warps = epi_warps_for(1LL * g.k_blocks * (f.mode == SHARD_K ? f.t : 1));
     g.dependent_launch = g_dependent_launch.load(std::memory_order_relaxed) & 1;
+    g.dynamic_tiles = g_tile_scheduler.load(std::memory_order_relaxed);
     if (out.k_splits > 1) {
         g.k_splits = out.k_splits;
         g.num_tiles = g.base_tiles * out.k_splits;
@@ -425,7 +430,8 @@ int run_gemm(Launcher fn, const Operand& a, const Operand& b, const Output& out,
                          static_cast<long long>(tail->ws_bytes / sizeof(float)));
     GemmArgs gm = g;
     if (plan.S > 1) gm.num_tiles = gm.base_tiles = static_cast<int>(plan.main);  // whole rounds
-    cudaError_t e = fn(maps, gm, std::min(gm.num_tiles, units), pair, st);
+    cudaError_t e = fn(maps, gm, gm.dynamic_tiles ? gm.num_tiles : std::min(gm.num_tiles, units),
+                       pair, st);
     if (e != cudaSuccess) return fail_cuda(e);
     ++t_last_launches;
     if (plan.S <= 1) return TPMLP_OK;
@@ -438,7 +444,8 @@ int run_gemm(Launcher fn, const Operand& a, const Operand& b, const Output& out,
     gt.partial_compact = 1;
     if ((rc = make_tail_map(&maps.o0, tail->ws, plan.X * plan.S))) return rc;
     maps.o1 = maps.o0;
-    e = tail->partial_fn(maps, gt, std::min(gt.num_tiles, units), pair, st);
+    e = tail->partial_fn(maps, gt, gt.dynamic_tiles ? gt.num_tiles : std::min(gt.num_tiles, units),
+                         pair, st);
     if (e != cudaSuccess) return fail_cuda(e);
     ++t_last_launches;
     return launch_tail_reduce(static_cast<const float*>(tail->ws), plan.S, g, plan.main, plan.X,
@@ -1809,6 +1816,11 @@ TPMLP_API int tpmlp_set_cta_pair_mode(int mode) {
 TPMLP_API int tpmlp_set_dependent_launch(int mode) {
     if (mode < 0 || mode > 3) return -1;
     return g_dependent_launch.exchange(mode);
+}
+
+TPMLP_API int tpmlp_set_tile_scheduler(int mode) {
+    if (mode != 0 && mode != 1) return -1;
+    return g_tile_scheduler.exchange(mode);
 }
 
 TPMLP_API int tpmlp_set_epilogue_warps(int mode) {

@@ -59,7 +59,8 @@ constexpr int BK = 64;   // 64 bf16 = one 128-byte swizzle row
 constexpr int UMMA_K = 16;
 constexpr int MN_ATOM_BYTES = 64 * BK * 2;  // one 64-wide MN-major box: 8 KiB
 constexpr int TMEM_COLS = 512;
-constexpr int BAR_BYTES = 256;
+constexpr int BAR_BYTES = 512;
+constexpr int kTileSlots = 4;  // responses of the dynamic tile scheduler in flight
 // Epilogue staging: per epilogue warp two buffers, each a 32-row x 64-column
 // bf16 block (rows 128 B apart, 128-byte swizzle) stored by one TMA store.
 constexpr int EPI_BUF_BYTES = 32 * 128;
@@ -131,6 +132,12 @@ struct GemmArgs {
     int partial_compact;
     int epi_warps;  // host side: 4 or 8 epilogue warps (the kernel variant launched)
     int dependent_launch;  // host side: launched with programmatic stream serialization
+    // 1: the grid holds one CTA (pair) per work unit and a running CTA (pair)
+    // takes the next unit by cancelling the launch of a pending one (cluster
+    // launch control), so the units in flight are always a contiguous run of
+    // the raster order; 0: a persistent grid, CTA (pair) u takes units
+    // u, u + units, ...
+    int dynamic_tiles;
 };
 
 struct TileCoord {
@@ -369,13 +376,17 @@ __global__ void __launch_bounds__(32 * (EW + 2), 1)
     uint8_t* ring_a = smem;
     uint8_t* ring_b = smem + G::STAGES * G::A_STAGE_BYTES;
     uint8_t* staging = smem + G::STAGES * G::STAGE_BYTES;  // 1 KiB aligned
-    uint64_t* bars = reinterpret_cast<uint64_t*>(staging + G::STAGING_BYTES);
+    uint8_t* bar_area = staging + G::STAGING_BYTES;
+    const uint32_t tile_resp = smem_u32(bar_area);  // [kTileSlots] 16-byte scheduler responses
+    uint64_t* bars = reinterpret_cast<uint64_t*>(bar_area + 16 * kTileSlots);
     uint64_t* full = bars;                      // stage loaded  (STAGES)
     uint64_t* empty = bars + G::STAGES;         // stage drained (STAGES)
     uint64_t* acc_full = bars + 2 * G::STAGES;  // accumulator ready (2)
     uint64_t* acc_empty = acc_full + 2;         // accumulator read  (2)
     uint64_t* drain = acc_empty + 2;            // teardown          (1)
-    uint32_t* misc = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* tile_full = drain + 1;            // scheduler response landed (kTileSlots)
+    uint64_t* tile_empty = tile_full + kTileSlots;  // every reader has read it (kTileSlots)
+    uint32_t* misc = reinterpret_cast<uint32_t*>(tile_empty + kTileSlots);
     volatile uint32_t* abort_flag = misc + 1;
 
     const int warp = threadIdx.x >> 5;
@@ -396,6 +407,11 @@ __global__ void __launch_bounds__(32 * (EW + 2), 1)
             mbar_init(&acc_empty[a], PAIR ? 2 * EW : EW);  // one arrival per epilogue warp
         }
         mbar_init(drain, 1);
+        for (int s = 0; s < kTileSlots; ++s) {
+            mbar_init(&tile_full[s], 1);  // this CTA's producer expects the 16 bytes
+            // readers of a response: each CTA's producer and epilogue warps, the MMA thread
+            mbar_init(&tile_empty[s], PAIR ? 2 * (1 + EW) + 1 : (1 + EW) + 1);
+        }
         misc[1] = 0u;
         fence_mbar_init();
     }
@@ -427,6 +443,32 @@ __global__ void __launch_bounds__(32 * (EW + 2), 1)
     const uint32_t tmem_base = misc[0];
     const int total_kb = p.shard_mode == SHARD_K ? p.k_blocks * p.shards : p.k_blocks;
 
+    // The work units of this CTA (pair), in order.  Static: unit, unit +
+    // units, ...  Dynamic: unit (its own launch), then for i = 0, 1, ...
+    // the unit whose launch the leader's producer cancelled with request i,
+    // answered in slot i % kTileSlots of every CTA of the pair; readers
+    // release the slot on the leader's tile_empty.  -1: no more units.
+    constexpr int kCluster = PAIR ? 2 : 1;
+    const bool dyn = p.dynamic_tiles != 0;
+    const uint32_t tile_empty_leader =
+        PAIR ? map_to_cta(smem_u32(tile_empty), 0) : smem_u32(tile_empty);
+    // the unit after the one finished with response i (one thread reads)
+    auto next_unit = [&](int tile, int i, bool& ok) -> int {
+        if (!dyn) return tile + units < p.num_tiles ? tile + units : -1;
+        const int slot = i % kTileSlots;
+        if (!wait_bounded<true>(&tile_full[slot], static_cast<uint32_t>(i / kTileSlots) & 1u,
+                                abort_flag, p.status)) {
+            ok = false;
+            return -1;
+        }
+        const int x = clc_response_ctaid_x(tile_resp + 16u * slot);
+        if constexpr (PAIR)
+            mbar_arrive_cluster(tile_empty_leader + 8u * slot);
+        else
+            mbar_arrive(&tile_empty[slot]);
+        return x < 0 ? -1 : x / kCluster;
+    };
+
     if (warp == PRODUCER_WARP) {
         // ---------------------------------------------------- TMA producer
         if (lane == 0) {
@@ -437,7 +479,30 @@ __global__ void __launch_bounds__(32 * (EW + 2), 1)
             // stage barriers as seen by the TMA: the leader's in a pair
             const uint32_t full_u = PAIR ? map_to_cta(smem_u32(full), 0) : smem_u32(full);
             const bool split_k = p.shard_mode == SHARD_K;
-            for (int tile = unit; tile < p.num_tiles; tile += units) {
+            bool run = true;
+            int pending = -1;  // a scheduler request whose answer this thread has not read
+            for (int tile = unit, i = 0; tile >= 0 && run; ++i) {
+                if (dyn) {
+                    // ask for the unit after this one now; the answer is read
+                    // once this unit's loads are issued
+                    const int slot = i % kTileSlots;
+                    if (rank == 0) {
+                        if (i >= kTileSlots &&
+                            !wait_bounded<true>(&tile_empty[slot],
+                                                static_cast<uint32_t>(i / kTileSlots - 1) & 1u,
+                                                abort_flag, p.status))
+                            break;
+                        fence_proxy_async_smem();  // earlier reads of the slot come first
+                        mbar_arrive_expect_tx(&tile_full[slot], 16);
+                        if constexpr (PAIR)
+                            clc_try_cancel_multicast(tile_resp + 16u * slot, smem_u32(&tile_full[slot]));
+                        else
+                            clc_try_cancel(tile_resp + 16u * slot, smem_u32(&tile_full[slot]));
+                    } else {
+                        mbar_arrive_expect_tx(&tile_full[slot], 16);  // the leader's answer lands here too
+                    }
+                    pending = i;
+                }
                 const TileCoord tc = decode_tile<G::TILE_M>(tile, p);
                 const int a_row0 = tc.m0 + static_cast<int>(rank) * BM;
                 const int b_row0 = tc.n0 + static_cast<int>(rank) * G::B_ROWS;
@@ -478,7 +543,13 @@ __global__ void __launch_bounds__(32 * (EW + 2), 1)
                     }
                 }
                 if (!ok) break;
+                tile = next_unit(tile, i, run);
+                if (run) pending = -1;
             }
+            // A scheduler answer still on its way lands before the CTA may exit.
+            if (pending >= 0)
+                wait_drain(&tile_full[pending % kTileSlots],
+                           static_cast<uint32_t>(pending / kTileSlots) & 1u, p.status);
             // Every copy this thread started lands before the CTA may exit.  A
             // pair's copies complete on the leader's barriers, so there the
             // stage's release by the MMA (which waited for them) is awaited.
@@ -500,7 +571,7 @@ __global__ void __launch_bounds__(32 * (EW + 2), 1)
             int stage = 0;
             uint32_t phase = 0;
             int count = 0;
-            for (int tile = unit; tile < p.num_tiles; tile += units, ++count) {
+            for (int tile = unit; tile >= 0; ++count) {
                 const int acc = count & 1;
                 const uint32_t acc_phase = (count >> 1) & 1;
                 if (!wait_bounded<true>(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
@@ -543,6 +614,9 @@ __global__ void __launch_bounds__(32 * (EW + 2), 1)
                     tc_commit_pair_multicast(&acc_full[acc], 0x3);
                 else
                     tc_commit(&acc_full[acc]);
+                bool run = true;
+                tile = next_unit(tile, count, run);
+                if (!run) break;
             }
             // No MMA may still be writing TMEM when it is released.
             if constexpr (PAIR)
@@ -571,7 +645,7 @@ __global__ void __launch_bounds__(32 * (EW + 2), 1)
         const uint32_t swz = static_cast<uint32_t>(lane & 7);
         uint32_t seq = 0;  // stores committed so far: selects the buffer
         int count = 0;
-        for (int tile = unit; tile < p.num_tiles; tile += units, ++count) {
+        for (int tile = unit; tile >= 0; ++count) {
             const TileCoord tc = decode_tile<G::TILE_M>(tile, p);
             const int acc = count & 1;
             const uint32_t acc_phase = (count >> 1) & 1;
@@ -796,6 +870,15 @@ __global__ void __launch_bounds__(32 * (EW + 2), 1)
                         mbar_arrive(&acc_empty[acc]);
                 }
             }
+            // the next unit: lane 0 reads it, the warp follows
+            bool run = true;
+            int nxt = -1;
+            if (lane == 0) nxt = next_unit(tile, count, run);
+            nxt = __shfl_sync(0xFFFFFFFFu, nxt, 0);
+            const uint32_t go = __shfl_sync(0xFFFFFFFFu, run ? 1u : 0u, 0);
+            __syncwarp();
+            if (!go) break;
+            tile = nxt;
         }
         if (lane == 0) bulk_wait_group<0>();  // every output store has completed
         __syncwarp();

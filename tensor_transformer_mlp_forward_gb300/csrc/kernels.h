@@ -131,9 +131,11 @@ cudaError_t launch_attn_backward(const CUtensorMap& tm_qkv128, const CUtensorMap
                                  const CUtensorMap& tm_do128, const CUtensorMap& tm_do64, int d,
                                  const AttnParams& p, cudaStream_t st, int* launches);
 
-// `grid` is the number of work units wanted (CTAs, or CTA pairs when PAIR);
-// it is clipped to what can be resident at once, so the persistent loop never
-// waits for a second wave of CTAs.
+// `grid` is the number of work units wanted (CTAs, or CTA pairs when PAIR).
+// With static units it is clipped to what can be resident at once, so the
+// persistent loop never waits for a second wave of CTAs; with dynamic units
+// (g.dynamic_tiles) it is one CTA (pair) per unit and the running ones take
+// over the launches of the others.
 template <bool A_MN, bool B_MN, int EPI, bool PAIR, int EW = 4>
 cudaError_t launch_gemm(const GemmMaps& m, const GemmArgs& g, int grid,
                         cudaStream_t st) {
@@ -162,7 +164,9 @@ cudaError_t launch_gemm(const GemmMaps& m, const GemmArgs& g, int grid,
             if (e != cudaSuccess) return e;
             resident_clusters = n > 0 ? n : 1;
         }
-        grid = 2 * (grid < resident_clusters ? grid : resident_clusters);
+        // persistent: no more pairs than can be resident; with dynamic units
+        // one pair per unit, the ones that do not fit wait to be cancelled
+        grid = 2 * (g.dynamic_tiles || grid < resident_clusters ? grid : resident_clusters);
     }
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(threads);

@@ -333,6 +333,45 @@ __device__ __forceinline__ uint32_t map_to_cta(uint32_t saddr, uint32_t rank) {
     return r;
 }
 
+// ------------------------------------------------ cluster launch control
+// A running CTA may cancel the launch of a cluster of its own grid that has
+// not started yet and do that cluster's work instead.  The request is
+// answered asynchronously: a 16-byte response is written to shared memory
+// at `resp` (16-byte aligned) -- in every CTA of the cluster, at the same
+// offset, with the multicast form -- and 16 bytes of transaction complete
+// on the mbarrier at `bar` (in each CTA that receives it).  After an
+// unsuccessful response (no cluster left to cancel) no further request may
+// be made.  Before a response buffer is reused, every read of the previous
+// response must be ordered before the request (fence.proxy.async).
+
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];"
+        ::"r"(resp), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void clc_try_cancel_multicast(uint32_t resp, uint32_t bar) {
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes"
+        ".multicast::cluster::all.b128 [%0], [%1];" ::"r"(resp), "r"(bar) : "memory");
+}
+
+// The x index of the first CTA of the cluster a response cancelled, or -1
+// when the request was unsuccessful.
+__device__ __forceinline__ int clc_response_ctaid_x(uint32_t resp) {
+    uint32_t ok = 0, x = 0;
+    asm volatile(
+        "{\n\t.reg .b128 q;\n\t.reg .pred p;\n\t"
+        "ld.shared.b128 q, [%2];\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, q;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t"
+        "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, q;\n\t}"
+        : "+r"(ok), "+r"(x)
+        : "r"(resp)
+        : "memory");
+    return ok ? static_cast<int>(x) : -1;
+}
+
 // Arrive on an mbarrier given by its shared::cluster address (possibly in
 // the peer CTA).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {

@@ -168,6 +168,23 @@ def test_attention_kernels_on_two_streams():
             assert torch.equal(dQKV, ref[i][2])
 
 
+def test_attention_tile_scheduler_forms_agree_bitwise():
+    """The attention block's GEMMs (QKV, output projection with the g sum,
+    the weight gradients, dO and dX) give the same bits with static and
+    dynamic tile assignment."""
+    w = inputs.attn_custom(nb=2, s=257, h=512, nh=4, t=2, seed=31)
+    cpu = inputs.make_attn_inputs(w)
+    prev = binding.set_tile_scheduler(0)
+    try:
+        static = run_gpu(w, cpu)
+        binding.set_tile_scheduler(1)
+        dynamic = run_gpu(w, cpu)
+    finally:
+        binding.set_tile_scheduler(prev)
+    for k in static:
+        assert torch.equal(static[k], dynamic[k]), k
+
+
 def test_attention_graph_replays_beside_eager_calls():
     """A CUDA graph of the core forward and backward, replayed while the same
     calls run eagerly on another stream: each call takes its work items from

@@ -171,6 +171,33 @@ def test_dependent_launch_changes_nothing():
         assert torch.equal(plain[k], outs[k]), k
 
 
+@pytest.mark.parametrize("w,pair", [
+    (inputs.custom(T=300, h=200, F=1536, t=4, seed=26), 2),       # ragged, CTA pairs
+    (inputs.custom(T=300, h=200, F=1536, t=4, seed=26), 0),       # ragged, single CTAs
+    (inputs.custom(T=2048, h=12288, F=4096, t=2, seed=27), 1),    # tail split of a3 and a7
+    (inputs.custom(T=512, h=4096, F=16384, t=4, seed=28), 1),     # split reduction of a3 and a7
+    (inputs.custom(T=1100, h=1024, F=4096, t=2, seed=29), 1),     # dZ with eight epilogue warps
+], ids=["pairs", "single_cta", "tail_split", "split_k", "short_k"])
+def test_tile_scheduler_forms_agree_bitwise(w, pair):
+    """Static and dynamic (cluster launch control) assignment of output
+    tiles compute every tile with the same sums: the block's outputs are the
+    same bits under both."""
+    cpu = inputs.make_inputs(w)
+    prev_pair = binding.set_cta_pair_mode(pair)
+    prev = binding.set_tile_scheduler(0)
+    try:
+        static = run_gpu(cpu, w.t)
+        binding.set_tile_scheduler(1)
+        dynamic = run_gpu(cpu, w.t)
+        again = run_gpu(cpu, w.t)
+    finally:
+        binding.set_tile_scheduler(prev)
+        binding.set_cta_pair_mode(prev_pair)
+    for k in static:
+        assert torch.equal(static[k], dynamic[k]), k
+        assert torch.equal(static[k], again[k]), k
+
+
 def test_split_reduction_matches_unsplit():
     """The row-parallel GEMMs with and without a split reduction (few output
     tiles: T=512, h=4096 gives 2 x 16 tiles) agree up to the bf16 rounding of
