@@ -537,16 +537,19 @@ int tpmlp_set_epilogue_warps(int mode);
 int tpmlp_set_dependent_launch(int mode);
 
 /* How the GEMM kernels assign output tiles (work units) to CTA pairs
- * (process-wide; returns the previous mode, or -1 for a mode other than 0
- * or 1):
- *   0  default: a persistent grid of as many pairs as fit, pair u taking
- *      units u, u + pairs, ... in the tile raster order;
+ * (process-wide; returns the previous mode, or -1 for a mode outside 0..2):
+ *   0  a persistent grid of as many pairs as fit, pair u taking units u,
+ *      u + pairs, ... in the tile raster order;
  *   1  one pair per unit in the grid; a running pair takes the next unit by
  *      cancelling the launch of a pair that has not started (cluster launch
  *      control), so the units in flight are always a contiguous run of the
- *      raster order however unevenly the pairs progress.
- * Both compute every unit with the same sums: results are bitwise identical
- * across modes. */
+ *      raster order however unevenly the pairs progress;
+ *   2  default: 1 for GEMMs whose tiles reduce over 192 or more k-blocks
+ *      of 64 (K >= 12288), where pairs sharing an operand panel otherwise
+ *      drift apart, 0 for the rest, whose short tiles would wait on the next
+ *      unit (MT-NLG 530B step 3.8 % faster than with 0).
+ * Every mode computes every unit with the same sums: results are bitwise
+ * identical across modes. */
 int tpmlp_set_tile_scheduler(int mode);
 
 /* Static text for a status code. */

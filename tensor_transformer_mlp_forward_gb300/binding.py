@@ -203,9 +203,9 @@ def set_dependent_launch(mode: int) -> int:
 
 
 def set_tile_scheduler(mode: int) -> int:
-    """0: persistent GEMM grids with a static tile assignment (default);
-    1: dynamic tiles through cluster launch control.  Returns the previous
-    mode."""
+    """0: persistent GEMM grids with a static tile assignment; 1: dynamic
+    tiles through cluster launch control; 2 (default): dynamic for long
+    reductions only.  Returns the previous mode."""
     prev = int(lib().tpmlp_set_tile_scheduler(mode))
     if prev < 0:
         raise ValueError(f"invalid mode {mode}")

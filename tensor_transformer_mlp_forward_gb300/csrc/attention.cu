@@ -747,9 +747,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint64_t* kv_empty = kv_full + S;
     uint64_t* sdp_full = kv_empty + S;   // [2]
     uint64_t* ds_full = sdp_full + 2;    // [2]
-    uint64_t* dq_done = ds_full + 2;     // the item's dQ is complete in TMEM
-    uint64_t* dq_free = dq_done + 1;     // the softmax warps have read it out
-    uint64_t* item_full = dq_free + 1;   // [2] items[slot] holds the next item
+    // dQ accumulators: two for d <= 128 (TMEM columns 256 and 384), so that
+    // item k's dQ is read out while item k + 1's MMAs run; one for d = 160
+    constexpr int NDQ = D <= 128 ? 2 : 1;
+    uint64_t* dq_done = ds_full + 2;     // [NDQ] the item's dQ is complete in TMEM
+    uint64_t* dq_free = dq_done + NDQ;   // [NDQ] the softmax warps have read it out
+    uint64_t* item_full = dq_free + NDQ; // [2] items[slot] holds the next item
     uint64_t* item_empty = item_full + 2;  // [2] every consumer has read it
     uint64_t* drain = item_empty + 2;
     int* items = reinterpret_cast<int*>(drain + 1);  // [2]
@@ -787,8 +790,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_init(&item_full[b], 1);
             mbar_init(&item_empty[b], 5);  // the MMA thread and the 4 softmax warps
         }
-        mbar_init(dq_done, 1);
-        mbar_init(dq_free, 4);
+        for (int b = 0; b < NDQ; ++b) {
+            mbar_init(&dq_done[b], 1);
+            mbar_init(&dq_free[b], 4);
+        }
         mbar_init(drain, 1);
         misc[1] = 0u;
         fence_mbar_init();
@@ -801,7 +806,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
-    // TMEM columns: S[b] at 64 b, dP[b] at 128 + 64 b, dQ at 256
+    // TMEM columns: S[b] at 64 b, dP[b] at 128 + 64 b, dQ[x] at 256 + 128 x
     constexpr uint32_t kS = 0, kDP = 128, kDQ = 256;
 
     if (warp == 4) {
@@ -880,9 +885,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             // dQ += dS K for tile i of item k (global tile gi), K in ring stage st
             auto issue_dq = [&](int i, int gi, int st, int k) {
                 if (!ok) return;
-                // the first dQ MMA of an item overwrites the previous item's dQ
-                if (i == 0 && k >= 1 &&
-                    !wait_bounded(dq_free, static_cast<uint32_t>(k - 1) & 1u, abort_flag, a.status, 0x20D)) {
+                // the first dQ MMA of an item overwrites the dQ of item k - NDQ
+                if (i == 0 && k >= NDQ &&
+                    !wait_bounded(&dq_free[k % NDQ], static_cast<uint32_t>((k - NDQ) / NDQ) & 1u,
+                                  abort_flag, a.status, 0x20D)) {
                     ok = false;
                     return;
                 }
@@ -897,8 +903,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 // d along the rows, keys down the 64-row box)
                 const uint64_t kdesc = smem_desc_sw128(smem_u32(ring) + st * 2 * C::KV_TILE,
                                                        64 * kRowBytes, 1024);
-                mma_ts_n_is_d<D, 64 / 16>(tmem + kDQ, tmem + kS + 64 * (gi & 1), kdesc,
-                                          64 * kRowBytes, i > 0);
+                mma_ts_n_is_d<D, 64 / 16>(tmem + kDQ + 128u * static_cast<uint32_t>(k % NDQ),
+                                          tmem + kS + 64 * (gi & 1), kdesc, 64 * kRowBytes, i > 0);
                 tc_commit(&kv_empty[st]);
             };
             for (int k = 0; ok; ++k) {
@@ -945,7 +951,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     }
                 }
                 issue_dq(it.n_kv - 1, g - 1, prev_stage, k);
-                if (ok) tc_commit(dq_done);
+                if (ok) tc_commit(&dq_done[k % NDQ]);
             }
             tc_commit(drain);
             wait_drain(drain, 0, a.status, 0x207);
@@ -956,6 +962,49 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
         bool ok = true;
         int g = 0;
+        // An item whose dQ is complete but not yet read out: with two dQ
+        // accumulators, item k's is read out after item k + 1's second key
+        // tile (its first, when it has one), while the MMA works on item
+        // k + 1; with one, at the end of item k.
+        struct Pending {
+            int k;
+            long long tok;
+            bool q_ok;
+            int head;
+        };
+        Pending pend{-1, 0, false, 0};
+        auto readout = [&](const Pending& pd) -> bool {
+            if (!warp_wait_bounded(&dq_done[pd.k % NDQ], static_cast<uint32_t>(pd.k / NDQ) & 1u,
+                                   abort_flag, a.status, 0x20A))
+                return false;
+            tc_fence_after();
+            // tcgen05.ld is warp-collective (.sync.aligned): every lane loads,
+            // only rows inside the sequence are stored
+            uint4* dst = reinterpret_cast<uint4*>(a.dqkv + pd.tok * 3 * a.h + pd.head * D);
+            const uint32_t col = kDQ + 128u * static_cast<uint32_t>(pd.k % NDQ);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(lane_addr + col + c * 32, v);
+                tmem_wait_ld();
+                if (pd.q_ok) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint4 u;
+                        u.x = pack_bf16x2(__uint_as_float(v[8 * i]) * a.scale, __uint_as_float(v[8 * i + 1]) * a.scale);
+                        u.y = pack_bf16x2(__uint_as_float(v[8 * i + 2]) * a.scale, __uint_as_float(v[8 * i + 3]) * a.scale);
+                        u.z = pack_bf16x2(__uint_as_float(v[8 * i + 4]) * a.scale, __uint_as_float(v[8 * i + 5]) * a.scale);
+                        u.w = pack_bf16x2(__uint_as_float(v[8 * i + 6]) * a.scale, __uint_as_float(v[8 * i + 7]) * a.scale);
+                        dst[c * 4 + i] = u;
+                    }
+                }
+            }
+            // dQ is in registers or on its way to memory: the MMA may reuse it
+            tc_fence_before();
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) mbar_arrive(&dq_free[pd.k % NDQ]);
+            return true;
+        };
         for (int k = 0; ok; ++k) {
             const int slot = k & 1;
             if (!warp_wait_bounded(&item_full[slot], static_cast<uint32_t>(k >> 1) & 1u, abort_flag,
@@ -1018,38 +1067,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ds_full[b]);
-            }
-            if (!ok || !warp_wait_bounded(dq_done, static_cast<uint32_t>(k) & 1u, abort_flag, a.status,
-                                          0x20A)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            // tcgen05.ld is warp-collective (.sync.aligned): every lane loads,
-            // only rows inside the sequence are stored
-            uint4* dst = reinterpret_cast<uint4*>(a.dqkv + tok * 3 * a.h + it.head * D);
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(lane_addr + kDQ + c * 32, v);
-                tmem_wait_ld();
-                if (q_ok) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        uint4 u;
-                        u.x = pack_bf16x2(__uint_as_float(v[8 * i]) * a.scale, __uint_as_float(v[8 * i + 1]) * a.scale);
-                        u.y = pack_bf16x2(__uint_as_float(v[8 * i + 2]) * a.scale, __uint_as_float(v[8 * i + 3]) * a.scale);
-                        u.z = pack_bf16x2(__uint_as_float(v[8 * i + 4]) * a.scale, __uint_as_float(v[8 * i + 5]) * a.scale);
-                        u.w = pack_bf16x2(__uint_as_float(v[8 * i + 6]) * a.scale, __uint_as_float(v[8 * i + 7]) * a.scale);
-                        dst[c * 4 + i] = u;
+                if (NDQ == 2 && pend.k >= 0 && j == (it.n_kv > 1 ? 1 : 0)) {
+                    if (!readout(pend)) {
+                        ok = false;
+                        break;
                     }
+                    pend.k = -1;
                 }
             }
-            // dQ is in registers or on its way to memory: the MMA may reuse it
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(dq_free);
+            if (!ok) break;
+            if constexpr (NDQ == 1) {
+                if (!readout(Pending{k, tok, q_ok, it.head})) {
+                    ok = false;
+                    break;
+                }
+            } else {
+                pend = Pending{k, tok, q_ok, it.head};
+            }
         }
+        if (ok && pend.k >= 0) readout(pend);
     }
 
     tc_fence_before();
