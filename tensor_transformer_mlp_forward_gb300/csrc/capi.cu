@@ -54,7 +54,21 @@ struct DeviceInfo {
     int sms = 0;
     int* status = nullptr;
     bool ok = false;
+    // The tail-split cost model's rates, from the device's attributes:
+    // a CTA pair's dense bf16 flops per ns and the DRAM bytes per ns.
+    double pair_flops_per_ns = 0.0;
+    double dram_bytes_per_ns = 0.0;
 };
+
+// A CTA pair's tensor cores do 2 x 4096 bf16 multiply-adds a clock.  The
+// planner takes 0.58 of that at the peak clock as a pair's sustained rate
+// inside a long GEMM step (1.5 PFLOP/s over GB300's 76 pairs at 2.07 GHz:
+// the clock settles near 1.5 GHz under the 1.4 kW cap, and a tile's fill
+// and epilogue cost the rest), and 0.8 of the DRAM's nominal rate (a copy
+// reaches 6.77 of 8.2 TB/s).  The ratios were calibrated on GB300; the
+// attributes carry the SM count, clock and memory of whatever device runs.
+constexpr double kSustainedRateRatio = 0.58;
+constexpr double kDramEfficiency = 0.8;
 
 constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
@@ -81,6 +95,14 @@ int device_info(DeviceInfo& out) {
             (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
             return fail_cuda(e);
         d.ok = (major == 10 && minor == 3);
+        int clock_khz = 0, mem_khz = 0, bus_bits = 0;
+        if ((e = cudaDeviceGetAttribute(&clock_khz, cudaDevAttrClockRate, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&mem_khz, cudaDevAttrMemoryClockRate, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&bus_bits, cudaDevAttrGlobalMemoryBusWidth, dev)) != cudaSuccess)
+            return fail_cuda(e);
+        // flops per ns = 2 SMs x 8192 flops a clock x GHz; DRAM: double data rate
+        d.pair_flops_per_ns = 2.0 * 8192.0 * (clock_khz * 1e-6) * kSustainedRateRatio;
+        d.dram_bytes_per_ns = 2.0 * (mem_khz * 1e-6) * (bus_bits / 8.0) * kDramEfficiency;
         if (d.ok) {
             e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status_word);
             if (e != cudaSuccess) return fail_cuda(e);
@@ -307,15 +329,19 @@ struct TailPlan {
 };
 
 // Estimated time of a plan: (main / units + ceil(X S / units) / S) rounds of
-// a whole tile, plus the partial tiles' write and read at HBM speed and two
+// a whole tile, plus the partial tiles' write and read at DRAM speed and two
 // more launches.  A tile's time is its 2 x 256 x 256 x K flops at a CTA
-// pair's share of the dense bf16 rate under the power cap (~1.5 PFLOP/s over
-// 76 pairs).  Among X = rem, rem + units, rem + 2 units and S = 2..8 (at
-// least 8 k-blocks per range; partials within ws_floats) the fastest plan is
-// taken when it beats the plain schedule.
-TailPlan plan_tail(long long tiles, long long total_kb, int units, long long ws_floats) {
-    constexpr double kPairFlopsPerNs = 1.5e6 / 76;   // 1.5 PFLOP/s over 76 pairs
-    constexpr double kHbmBytesPerNs = 6500.0;
+// pair's rate under the power cap (pair_flops_per_ns; on GB300 ~19.7
+// TFLOP/s a pair, 1.5 PFLOP/s over 76 pairs), the partial tiles' traffic at
+// dram_bytes_per_ns (~6.5 TB/s).  Among X = rem, rem + units, rem + 2 units
+// and S = 2..8 (at least 8 k-blocks per range; partials within ws_floats)
+// the fastest plan is taken when it beats the plain schedule.  Rates of 0
+// (no device) fall back to GB300's.
+TailPlan plan_tail(long long tiles, long long total_kb, int units, long long ws_floats,
+                   double pair_flops_per_ns = 0.0, double dram_bytes_per_ns = 0.0) {
+    const double kPairFlopsPerNs =
+        pair_flops_per_ns > 0.0 ? pair_flops_per_ns : 2.0 * 8192.0 * 2.07 * kSustainedRateRatio;
+    const double kHbmBytesPerNs = dram_bytes_per_ns > 0.0 ? dram_bytes_per_ns : 6500.0;
     constexpr double kLaunchNs = 4000.0;
     TailPlan best{tiles, 0, 1};
     if (units <= 0 || tiles <= units || tiles % units == 0) return best;
@@ -441,7 +467,8 @@ int run_gemm(Launcher fn, const Operand& a, const Operand& b, const Output& out,
     TailPlan plan{g.num_tiles, 0, 1};
     if (tail != nullptr && pair && out.k_splits <= 1 && tail->ws != nullptr)
         plan = plan_tail(g.num_tiles, 1LL * g.k_blocks * (f.mode == SHARD_K ? f.t : 1), units,
-                         static_cast<long long>(tail->ws_bytes / sizeof(float)));
+                         static_cast<long long>(tail->ws_bytes / sizeof(float)), dev.pair_flops_per_ns,
+                         dev.dram_bytes_per_ns);
     GemmArgs gm = g;
     if (plan.S > 1) gm.num_tiles = gm.base_tiles = static_cast<int>(plan.main);  // whole rounds
     cudaError_t e = fn(maps, gm, gm.dynamic_tiles ? gm.num_tiles : std::min(gm.num_tiles, units),

@@ -259,6 +259,39 @@ def test_tail_split_matches_one_launch():
         assert differ <= (tiles % units + 2 * units) * 256 * 256, name
 
 
+def test_tail_split_never_slower_than_one_launch():
+    """The tail split's plan is an estimate (a pair's rate under the power
+    cap, DRAM speed, launch cost).  At the MT-NLG row-parallel GEMM, where it
+    is taken, the split schedule must not be slower than the one-launch
+    schedule: medians of interleaved calls, 5 % margin for noise."""
+    import statistics
+
+    T, h, F, t = 2048, 20480, 81920, 8
+    g = torch.Generator(device="cuda").manual_seed(33)
+    bf = lambda *s, std=1.0: (torch.randn(*s, generator=g, device="cuda") * std).to(torch.bfloat16)  # noqa: E731
+    H, B, b2, R = bf(T, F, std=0.5), bf(F, h, std=0.006), bf(h, std=0.01), bf(T, h)
+    Y = torch.empty(T, h, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(binding.split_workspace_bytes(T, h, F, t), dtype=torch.uint8, device="cuda")
+    empty = torch.empty(0, dtype=torch.uint8, device="cuda")
+    runs = {"split": lambda: binding.tp_mlp_row_sum(H, B, b2, R, t, Y=Y, workspace=ws),
+            "one": lambda: binding.tp_mlp_row_sum(H, B, b2, R, t, Y=Y, workspace=empty)}
+    runs["split"]()
+    assert binding.last_launch_count() == 3  # the plan splits this shape
+    times = {k: [] for k in runs}
+    for rnd in range(6):
+        for k in (("split", "one") if rnd % 2 == 0 else ("one", "split")):
+            for _ in range(2):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                runs[k]()
+                e1.record()
+                torch.cuda.synchronize()
+                times[k].append(e0.elapsed_time(e1))
+    assert binding.device_status() == 0
+    split, one = statistics.median(times["split"]), statistics.median(times["one"])
+    assert split <= 1.05 * one, (split, one)
+
+
 def test_empty_batch():
     w = inputs.custom(T=0, h=64, F=256, t=2, seed=17)
     cpu = inputs.make_inputs(w)
