@@ -35,7 +35,11 @@ def ln_inputs(T, h, seed):
                 dX=bf(T, h), dres=bf(T, h))
 
 
-@pytest.mark.parametrize("T,h", [(1, 8), (5, 24), (37, 200), (300, 1024), (64, 20480), (3, 49152)])
+# Long rows (4096 .. 32768 columns), ragged row counts and fewer rows than
+# SMs as well as the short shapes.
+@pytest.mark.parametrize("T,h", [(1, 8), (5, 24), (37, 200), (300, 1024), (64, 20480), (3, 49152),
+                                 (130, 4096), (257, 8192), (100, 12288), (33, 16384), (5, 32768),
+                                 (3, 20480), (1, 4096)])
 @pytest.mark.parametrize("with_dres", [True, False])
 def test_layernorm_against_oracle(T, h, with_dres):
     c = ln_inputs(T, h, 100 + T + h)
@@ -71,6 +75,23 @@ def test_layernorm_full_size_and_no_s_output():
     assert rel(np64(ds), dsr) <= TOL_BWD
     assert rel(np64(dgam), dgr) <= TOL_BWD
     assert rel(np64(dbet), dbr) <= TOL_BWD
+
+
+@pytest.mark.parametrize("T,h", [(2048, 20480), (700, 8192)])
+def test_layernorm_backward_deterministic(T, h):
+    """Every sum of the backward (the row sums in the CTA, the column partials
+    over row chunks and their total) runs in a fixed order: repeated calls
+    agree bit for bit."""
+    c = ln_inputs(T, h, 11)
+    g = {k: v.cuda() for k, v in c.items()}
+    _, _, mean, rstd = binding.tp_ln_residual_forward(g["a"], g["r"], g["gamma"], g["beta"], EPS)
+    first = binding.tp_ln_residual_backward(g["dX"], g["dres"], g["a"], g["r"], g["gamma"], mean, rstd)
+    for _ in range(3):
+        again = binding.tp_ln_residual_backward(g["dX"], g["dres"], g["a"], g["r"], g["gamma"], mean,
+                                                rstd)
+        for x, y in zip(first, again):
+            assert torch.equal(x, y)
+    assert binding.device_status() == 0
 
 
 def test_empty_batch_layernorm():
