@@ -287,7 +287,7 @@ class Step:
         self.p_db1 = e(max(1, int(binding.lib().tp_mlp_dgelu_partial_floats(T, F))), dt=torch.float32)
         self.p_db2 = e(max(1, int(binding.lib().tp_mlp_bias_grad_workspace_floats(T, h))), dt=torch.float32)
         self.ws_split = e(max(16, binding.split_workspace_bytes(T, h, F, w.t)), dt=torch.uint8)
-        self.kmajor = binding.weight_grad_kmajor(h, F)
+        self.kmajor = binding.weight_grad_kmajor(h, F // w.t)
         if self.kmajor:
             ldT = binding.pitch(T)
             self.Xt, self.dYt, self.dZt, self.Ht = e(h, ldT), e(h, ldT), e(F, ldT), e(F, ldT)

@@ -243,11 +243,13 @@ int tp_transpose(const tpmlp_bf16* in, int rows, int cols, tpmlp_bf16* out, int 
                  void* stream);
 
 /* 1 when the composite calls (tp_mlp_backward and its variants,
- * tp_attn_backward) compute an M x N weight gradient (dA, dB: h x F or
- * F x h; dWqkv: h x 3h; dWo: h x h) from transposed operands with
- * tp_transpose and the two calls below, else 0 (they call tp_mlp_dA /
- * tp_mlp_dB).  The rule is M N / (M + N) >= 6144: there the faster K-major
- * GEMM repays the two transposes.  No device work. */
+ * tp_attn_backward) compute an M x N weight gradient (per shard: dA_i,
+ * dB_i: h x F/t or F/t x h; dWqkv: h x 3h; dWo: h x h) from transposed
+ * operands with tp_transpose and the two calls below, else 0 (they call
+ * tp_mlp_dA / tp_mlp_dB).  The rule: 0 when M and N are both multiples of
+ * 64 (the row-major operands are then read in one box per stage, as fast
+ * as the transposed ones); otherwise 1 when M N / (M + N) >= 6144, where
+ * the K-major GEMM repays the two transposes.  No device work. */
 int tp_weight_grad_kmajor(int M, int N);
 
 /* a8 and a9 from transposed operands, so that both GEMM operands are read

@@ -204,7 +204,53 @@ struct Operand {
     long long ld = 0;
 };
 
-int operand_map(CUtensorMap* m, const Operand& o, int t, int tile_rows) {
+// 4-D view of an MN-major operand, [rows = k, cols = mn] row-major with the
+// shard index on `on` as in make_map: dims {64, k rows, mn / 64, shards},
+// so that one box {64, BK, atoms, 1} holds `atoms` 64-wide MN atoms of a
+// k-block, each 64 rows of 128 bytes, one after another (the layout the
+// MN-major UMMA descriptor reads).  Only for MN extents (per shard) that are
+// multiples of 64, so that no atom reaches past its shard or row.
+int make_map_mn4(CUtensorMap* m, const void* ptr, long long rows, long long cols, int t, int on,
+                 int atoms, long long ld) {
+    cuuint64_t dims[4], strides[3];
+    cuuint32_t box[4] = {64, static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(atoms), 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    const cuuint64_t row_bytes = static_cast<cuuint64_t>(ld > 0 ? ld : cols) * 2;
+    if (on == ON_CONTIG) {  // shards split the MN columns
+        const long long cs = cols / t;
+        dims[0] = 64; dims[1] = rows; dims[2] = cs / 64; dims[3] = t;
+        strides[0] = row_bytes; strides[1] = 128; strides[2] = static_cast<cuuint64_t>(cs) * 2;
+    } else if (on == ON_ROWS) {  // shards split the k rows
+        const long long rs = rows / t;
+        dims[0] = 64; dims[1] = rs; dims[2] = cols / 64; dims[3] = t;
+        strides[0] = row_bytes; strides[1] = 128; strides[2] = static_cast<cuuint64_t>(rs) * row_bytes;
+    } else {
+        dims[0] = 64; dims[1] = rows; dims[2] = cols / 64; dims[3] = 1;
+        strides[0] = row_bytes; strides[1] = 128; strides[2] = static_cast<cuuint64_t>(rows) * row_bytes;
+    }
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides,
+                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        t_last_cuda_error = static_cast<int>(r);
+        return TPMLP_ERR_LAUNCH;
+    }
+    return TPMLP_OK;
+}
+
+// The operand's tensor map: K-major operands and MN-major ones of ragged
+// MN extent as 3-D maps with one box per 64 rows (MN-major: per 64-wide
+// atom); other MN-major operands as the 4-D view, one box per stage
+// (*mn4 = 1).
+int operand_map(CUtensorMap* m, const Operand& o, int t, int tile_rows, int* mn4) {
+    *mn4 = 0;
+    if (o.mn_major) {
+        const long long mn = o.on == ON_CONTIG ? o.cols / t : o.cols;
+        if (mn % 64 == 0 && tile_rows % 64 == 0 && (o.on != ON_ROWS || o.rows % t == 0)) {
+            *mn4 = 1;
+            return make_map_mn4(m, o.ptr, o.rows, o.cols, t, o.on, tile_rows / 64, o.ld);
+        }
+    }
     return make_map(m, o.ptr, o.rows, o.cols, t, o.on, o.mn_major ? BK : tile_rows, o.ld);
 }
 
@@ -451,9 +497,9 @@ int run_gemm(Launcher fn, const Operand& a, const Operand& b, const Output& out,
         g.num_tiles = g.base_tiles * out.k_splits;
     }
     alignas(64) GemmMaps maps;
-    int rc = operand_map(&maps.a, fa, f.t, BM);
+    int rc = operand_map(&maps.a, fa, f.t, BM, &g.a_mn4);
     if (rc) return rc;
-    rc = operand_map(&maps.b, fb, f.t, pair ? BN / 2 : BN);
+    rc = operand_map(&maps.b, fb, f.t, pair ? BN / 2 : BN, &g.b_mn4);
     if (rc) return rc;
     if (out.k_splits > 1)
         rc = make_partial_map(&maps.o0, out.ptr0, out.rows, out.cols, out.k_splits);
@@ -908,14 +954,20 @@ int transpose(const tpmlp_bf16* in, int rows, int cols, tpmlp_bf16* out, int ld_
 // Row pitch of a transposed [., T] operand: T rounded up to 8 elements (16 B).
 int pitch_of(int T) { return (T + 7) & ~7; }
 
-// Whether an M x N weight gradient (reduction over the T tokens) is computed
-// from transposed, K-major operands.  The K-major GEMM runs 8-20 % faster
-// than the MN-major one on the row-major operands, and the two transposes
-// cost 4 T (M + N) bytes of HBM traffic, so it pays when the GEMM's work
-// per transposed element, M N / (M + N), is large: measured on GB300 with
-// F = 4h, the MLP's dA + dB gained with h >= 8192 and lost with h <= 4096
-// at every T from 1024 to 16384.
-bool kmajor_weight_grad(long long M, long long N) { return M * N >= 6144LL * (M + N); }
+// Whether an M x N weight gradient (reduction over the T tokens; N the
+// extent of one shard) is computed from transposed, K-major operands.  With
+// both extents multiples of 64 the MN-major GEMM reads each operand's part
+// of a stage as one box (the 4-D view of make_map_mn4) and runs within 1.3 %
+// of the K-major one, which is less than the two transposes cost (4 T (M +
+// N) bytes of HBM traffic; MT-NLG dA: 3.62 ms MN-major against 3.57 + 0.15
+// ms).  With a ragged extent the MN-major operand takes two boxes per stage
+// and runs 8-20 % slower; there the transposes pay when the GEMM's work per
+// transposed element, M N / (M + N), is large (measured with F = 4h: gained
+// with h >= 8192, lost with h <= 4096, at every T from 1024 to 16384).
+bool kmajor_weight_grad(long long M, long long N) {
+    if (M % 64 == 0 && N % 64 == 0) return false;
+    return M * N >= 6144LL * (M + N);
+}
 
 // -------------------------------------------------- column sums (bias grads)
 
@@ -974,7 +1026,7 @@ BackwardLayout backward_layout(int T, int h, int F, int t) {
     L.db2 = align256(L.colsum + sizeof(float) * dgelu_partial_floats(T, F));
     const size_t db2_floats = colsum_workspace_floats(T, h);
     // the transposes only where a8 and a9 take the K-major form
-    const size_t ldT = kmajor_weight_grad(h, F) ? static_cast<size_t>(pitch_of(T)) : 0;
+    const size_t ldT = kmajor_weight_grad(h, F / t) ? static_cast<size_t>(pitch_of(T)) : 0;
     L.xt = align256(L.db2 + sizeof(float) * db2_floats);
     L.dyt = align256(L.xt + sizeof(uint16_t) * ldT * h);
     L.dzt = align256(L.dyt + sizeof(uint16_t) * ldT * h);
@@ -1296,9 +1348,9 @@ static int backward_steps(const tpmlp_bf16* dY, const tpmlp_bf16* X, const tpmlp
     if (int rc = launch_rowsum(colsum, static_cast<int>(4 * cdiv(T, BM)), F, db1, st)) return rc;
     // a7: dX = sum_i dZ_i A_i^T (the f-operator sum inside the accumulator)
     if (int rc = dx_gemm(dZ, A, T, h, F, t, dX, ws + L.split, L.total - L.split, st, d)) return rc;
-    // a8, a9: weight gradients of every shard; on large blocks both operands
-    // K-major after transposing X, dZ, H and dY
-    if (!kmajor_weight_grad(h, F)) {
+    // a8, a9: weight gradients of every shard; on large blocks of ragged
+    // shard width both operands K-major after transposing X, dZ, H and dY
+    if (!kmajor_weight_grad(h, F / t)) {
         if (int rc = dA_gemm(X, dZ, T, h, F, t, dA, st, d)) return rc;
         return dB_gemm(H, dY, T, h, F, t, dB, st, d);
     }

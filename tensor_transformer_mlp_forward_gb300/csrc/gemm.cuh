@@ -138,6 +138,10 @@ struct GemmArgs {
     // the raster order; 0: a persistent grid, CTA (pair) u takes units
     // u, u + units, ...
     int dynamic_tiles;
+    // MN-major operands whose tensor map is the 4-D view {64, k, mn / 64,
+    // shard} (a_mn4 for A, b_mn4 for B): the operand's whole part of a
+    // stage (ROWS / 64 atoms of 64 x BK) is one box.
+    int a_mn4, b_mn4;
 };
 
 struct TileCoord {
@@ -210,7 +214,15 @@ __device__ __forceinline__ void tma_coords(int on, int contig, int row, int s, i
 //  MN-major: ROWS/64 boxes of 64 (m or n) x BK (k), each 8 KiB.
 template <bool MN, int ROWS, bool PAIR>
 __device__ __forceinline__ void load_operand(const CUtensorMap* map, uint32_t bar, uint32_t dst,
-                                             int on, int mn0, int k0, int s) {
+                                             int on, int mn0, int k0, int s, int mn4) {
+    if (MN && mn4) {  // one box: the ROWS / 64 atoms land MN_ATOM_BYTES apart
+        const int sh = on == ON_NONE ? 0 : s;
+        if constexpr (PAIR)
+            tma_load_4d_pair(map, bar, dst, 0, k0, mn0 >> 6, sh);
+        else
+            tma_load_4d(map, bar, dst, 0, k0, mn0 >> 6, sh);
+        return;
+    }
     int c0, c1, c2;
 #pragma unroll
     for (int j = 0; j < (MN ? ROWS / 64 : 1); ++j) {
@@ -526,9 +538,9 @@ __global__ void __launch_bounds__(32 * (EW + 2), 1)
                         mbar_arrive_expect_tx(&full[stage], PAIR ? 2 * G::STAGE_BYTES : G::STAGE_BYTES);
                     const uint32_t bar = full_u + stage * 8;
                     load_operand<A_MN, BM, PAIR>(&tmA, bar, ring_a_u + stage * G::A_STAGE_BYTES,
-                                                 p.a_on, a_row0, k0, s);
+                                                 p.a_on, a_row0, k0, s, p.a_mn4);
                     load_operand<B_MN, G::B_ROWS, PAIR>(&tmB, bar, ring_b_u + stage * G::B_STAGE_BYTES,
-                                                        p.b_on, b_row0, k0, s);
+                                                        p.b_on, b_row0, k0, s, p.b_mn4);
                     issued |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                     k0 += BK;

@@ -72,24 +72,34 @@ def test_workspace_errors(L):
 
 
 def test_weight_grad_form_rule(L):
-    # K-major (transposed operands) where M N / (M + N) >= 6144
-    assert L.tp_weight_grad_kmajor(20480, 81920) == 1   # MT-NLG dA / dB
-    assert L.tp_weight_grad_kmajor(8192, 32768) == 1
-    assert L.tp_weight_grad_kmajor(20480, 20480) == 1   # MT-NLG dWo
+    # extents that are multiples of 64: the row-major (MN-major) operands
+    # are read in one box per stage, no transposes
+    assert L.tp_weight_grad_kmajor(20480, 10240) == 0   # MT-NLG dA_i / dB_i (F/t = 10240)
+    assert L.tp_weight_grad_kmajor(20480, 81920) == 0
+    assert L.tp_weight_grad_kmajor(20480, 20480) == 0   # MT-NLG dWo
     assert L.tp_weight_grad_kmajor(4096, 16384) == 0
     assert L.tp_weight_grad_kmajor(3072, 9216) == 0     # GPT-2 8.3B dWqkv
-    assert L.tp_weight_grad_kmajor(12288, 12288) == 1 and L.tp_weight_grad_kmajor(12286, 12288) == 0
+    # a ragged extent: K-major (transposed operands) where M N / (M + N) >= 6144
+    assert L.tp_weight_grad_kmajor(12320, 12288) == 1 and L.tp_weight_grad_kmajor(12296, 12288) == 1
+    assert L.tp_weight_grad_kmajor(20480, 20488) == 1 and L.tp_weight_grad_kmajor(4104, 16384) == 0
     assert L.tp_weight_grad_kmajor(0, 81920) == 0 and L.tp_weight_grad_kmajor(-5, 81920) == 0
 
 
 def test_backward_workspace_holds_the_transposes(L):
-    # with the K-major weight gradients: dZ, then X^T and dY^T [h, ldT] and
-    # dZ^T and H^T [F, ldT], ldT = T rounded up to 8; without them, none
-    T, h, F, t = 300, 8192, 32768, 4
-    ldT = 304
+    # with the K-major weight gradients (a large block of ragged width): dZ,
+    # then X^T and dY^T [h, ldT] and dZ^T and H^T [F, ldT], ldT = T rounded
+    # up to 8; without them (extents multiples of 64, or small), none
+    T, ldT = 300, 304
+    h, F, t = 20488, 81920, 8
+    assert L.tp_weight_grad_kmajor(h, F // t) == 1
     big = L.tp_mlp_backward_workspace_bytes(T, h, F, t)
     assert big >= 2 * T * F + 2 * ldT * (2 * h + 2 * F)
-    T, h, F = 300, 200, 1536
+    # the same block at h = 20480 (multiples of 64) holds no transposed
+    # buffers (its split partials differ a little from the ragged block's)
+    assert L.tp_weight_grad_kmajor(20480, F // t) == 0
+    assert big - L.tp_mlp_backward_workspace_bytes(T, 20480, F, t) >= 0.5 * 2 * ldT * (2 * h + 2 * F)
+    h, F, t = 200, 1536, 4
+    assert L.tp_weight_grad_kmajor(h, F // t) == 0
     assert L.tp_mlp_backward_workspace_bytes(T, h, F, t) < 2 * T * F + 2 * ldT * (2 * h + 2 * F)
 
 
