@@ -211,7 +211,11 @@ __device__ __forceinline__ void tma_coords(int on, int contig, int row, int s, i
 // shared address `dst`; completion counts on the mbarrier at `bar` (in a
 // pair: the leader's barrier, a shared::cluster address).
 //  K-major:  one box of 64 (k) x ROWS (m or n), rows 128 B apart.
-//  MN-major: ROWS/64 boxes of 64 (m or n) x BK (k), each 8 KiB.
+//  MN-major: with mn4 (the 4-D map {64, k, mn / 64, shard}), one box of
+//            64 x BK x ROWS/64 whose atoms land 8 KiB apart; otherwise
+//            (a ragged MN extent) ROWS/64 boxes of 64 (m or n) x BK (k),
+//            each 8 KiB.  The producer's issue per box sets the pace of a
+//            stage, so fewer boxes is faster.
 template <bool MN, int ROWS, bool PAIR>
 __device__ __forceinline__ void load_operand(const CUtensorMap* map, uint32_t bar, uint32_t dst,
                                              int on, int mn0, int k0, int s, int mn4) {
