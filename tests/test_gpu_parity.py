@@ -74,6 +74,11 @@ SMALL = [
     inputs.custom(T=77, h=64, F=512, t=64, seed=14),       # f = 8: one sliver per shard
     inputs.custom(T=1, h=8, F=8, t=1, seed=15),            # smallest legal block
     inputs.custom(T=64, h=8, F=16, t=2, seed=16),          # boxes wider than the tensor
+    # f = 200 with h a multiple of 64: the row-parallel GEMM's weight operand
+    # is read through the one-box (4-D) MN-major view with the shards on k,
+    # the weight gradients' X and dY likewise, dZ and H through two boxes
+    inputs.custom(T=300, h=256, F=1600, t=8, seed=17),
+    inputs.custom(T=200, h=384, F=3072, t=3, seed=18),     # f = 1024: every MN operand one box
 ]
 
 
