@@ -128,7 +128,8 @@ int tp_mlp_backward(const tpmlp_bf16* dY, const tpmlp_bf16* X, const tpmlp_bf16*
 /* ---------------------------------------------------------------------- */
 /* The steps of the hot path, one call each.  tp_mlp_forward and          */
 /* tp_mlp_backward are exactly these calls in this order (the backward     */
-/* takes a8 and a9 in their transposed-operand form, below tp_mlp_dB).     */
+/* takes a8 and a9 in their transposed-operand form, below tp_mlp_dB,      */
+/* where tp_weight_grad_kmajor says so).                                   */
 /* ---------------------------------------------------------------------- */
 
 /* a2: column-parallel GEMM with fused bias and GeLU, all t shards in one
@@ -253,9 +254,10 @@ int tp_transpose(const tpmlp_bf16* in, int rows, int cols, tpmlp_bf16* out, int 
 int tp_weight_grad_kmajor(int M, int N);
 
 /* a8 and a9 from transposed operands, so that both GEMM operands are read
- * along their contiguous dimension (the tensor cores take this K-major form
- * faster than the row-major X, dZ, H, dY of tp_mlp_dA / tp_mlp_dB).  Same
- * sums, same outputs:
+ * along their contiguous dimension (K-major).  Faster than the row-major X,
+ * dZ, H, dY of tp_mlp_dA / tp_mlp_dB where a shard's width is not a
+ * multiple of 64 (those operands then take two boxes a pipeline stage);
+ * level with them otherwise.  Same sums, same outputs:
  *   dA_i = X^T dZ_i   from Xt = X^T [h, ldT] and dZt = dZ^T [F, ldT]
  *   dB_i = H_i^T dY   from Ht = H^T [F, ldT] and dYt = dY^T [h, ldT]
  * (shard i of dZt / Ht is rows i F/t .. (i+1) F/t - 1), as tp_transpose
