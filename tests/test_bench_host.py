@@ -26,3 +26,46 @@ def test_comment_edits_keep_the_hash_and_code_edits_change_it():
     assert bench.code_only(a) == bench.code_only(b)
     assert bench.code_only(a) != bench.code_only(c)
 
+
+
+def test_recorded_traffic_is_keyed_by_kernel_workload_and_source(tmp_path, monkeypatch):
+    f = tmp_path / "traffic.md"
+    f.write_text("notes\n"
+                 "traffic: kernel=dB workload=mt-nlg-530b src_sha=aaaa bytes_per_launch=111\n"
+                 "traffic: kernel=dB workload=mt-nlg-530b src_sha=bbbb bytes_per_launch=222\n"
+                 "traffic: kernel=dA workload=mt-nlg-530b src_sha=bbbb bytes_per_launch=333\n")
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "bbbb")
+    assert bench.recorded_traffic("dB", "mt-nlg-530b") == 222
+    assert bench.recorded_traffic("dA", "mt-nlg-530b") == 333
+    assert bench.recorded_traffic("dB", "megatron-8.3b") is None
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "cccc")  # a changed kernel: no figure
+    assert bench.recorded_traffic("dB", "mt-nlg-530b") is None
+
+
+def test_reference_arm_prints_one_contract_line():
+    """`bench.py --impl reference` (the fp64 oracle on the host cores, a
+    bounded sample of the MT-NLG block) needs no GPU: one JSON line with the
+    contract's keys, its cpu_baseline and an e2e equal to its own value."""
+    import json
+    import os
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "1"],
+                       cwd=root, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] == 1
+    assert d["value"] > 0 and d["higher_is_better"] is True and d["dtype"] == "f64"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["value"] == d["value"] and d["e2e"]["unit"] == d["unit"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert "workload" in d["config"]
