@@ -588,6 +588,34 @@ int choose_splits(long long M, long long N, long long total_kb, int units) {
     return best <= 0.8 * base ? best_s : 1;
 }
 
+// The row-parallel GEMMs' split, with the partial outputs counted: among 1..8
+// splits, the one with the least estimated time -- rounds of a 1/sp tile at
+// a pair's rate plus, for sp > 1, the fp32 partials' write and read (2 x 4
+// sp M N bytes at DRAM speed) and the reduce launch -- when it beats the
+// unsplit time by 5 % or more.  The rates are plan_tail's.
+int choose_row_splits(long long M, long long N, long long total_kb, int units,
+                      double pair_flops_per_ns = 0.0, double dram_bytes_per_ns = 0.0) {
+    const long long tiles = cdiv(M, 2 * BM) * cdiv(N, BN);
+    if (units <= 0 || tiles <= 0) return 1;
+    const double flops_ns =
+        pair_flops_per_ns > 0.0 ? pair_flops_per_ns : 2.0 * 8192.0 * 2.07 * kSustainedRateRatio;
+    const double dram_ns = dram_bytes_per_ns > 0.0 ? dram_bytes_per_ns : 6500.0;
+    constexpr double kLaunchNs = 4000.0;
+    const double tile_ns = 2.0 * 2 * BM * BN * BK * static_cast<double>(total_kb) / flops_ns;
+    const double base = static_cast<double>(cdiv(tiles, units)) * tile_ns;
+    double best = base;
+    int best_s = 1;
+    for (int sp = 2; sp <= 8 && total_kb / sp >= 8; ++sp) {
+        const double c = static_cast<double>(cdiv(tiles * sp, units)) * tile_ns / sp + kLaunchNs +
+                         8.0 * sp * static_cast<double>(M) * static_cast<double>(N) / dram_ns;
+        if (c < best - 1e-9) {
+            best = c;
+            best_s = sp;
+        }
+    }
+    return best <= 0.95 * base ? best_s : 1;
+}
+
 // CTA pairs the split heuristic assumes when sizing workspaces (GB300: 152 SMs).
 constexpr int kSizingPairs = 76;
 
@@ -597,7 +625,7 @@ long long row_total_kb(int F, int t) { return cdiv(F / t, BK) * t; }
 // use: a whole split, or else the partial tiles of a tail split.
 size_t split_partial_floats(int T, int h, int F, int t) {
     const long long total_kb = row_total_kb(F, t);
-    const int sp = choose_splits(T, h, total_kb, kSizingPairs);
+    const int sp = choose_row_splits(T, h, total_kb, kSizingPairs);
     if (sp > 1) return static_cast<size_t>(sp) * T * h;
     const long long tiles = cdiv(T, 2 * BM) * cdiv(h, BN);
     const TailPlan p = plan_tail(tiles, total_kb, kSizingPairs, 1LL << 60);
@@ -721,7 +749,8 @@ int launch_split_reduce(const float* P, int splits, int T, int h, const tpmlp_bf
 
 // Splits to use for a row-parallel GEMM given the caller's workspace.
 int row_splits(int T, int h, int F, int t, size_t ws_bytes, const DeviceInfo& d) {
-    int sp = choose_splits(T, h, row_total_kb(F, t), d.sms / 2);
+    int sp = choose_row_splits(T, h, row_total_kb(F, t), d.sms / 2, d.pair_flops_per_ns,
+                               d.dram_bytes_per_ns);
     const size_t per = sizeof(float) * static_cast<size_t>(T) * h;
     while (sp > 1 && static_cast<size_t>(sp) * per > ws_bytes) --sp;
     return sp;
