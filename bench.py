@@ -560,9 +560,13 @@ def oracle_sample(w, cpu, budget_s=20.0, max_rows=64, first=0):
 
 def cpu_baseline(w, cpu, budget_s=20.0):
     flops, secs, rows, threads = oracle_sample(w, cpu, budget_s)
-    return {"value": flops / secs / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+    rate = flops / secs
+    return {"value": rate / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"{rows} token row(s) of Y and dX (forward + backward, 10*h*F flops each) "
-                      f"of the {w.name} block, fp64, {secs:.1f} s"}
+                      f"of the {w.name} block, fp64, {secs:.1f} s",
+            # an extrapolation, not a measurement: the whole step's 12*T*h*F
+            # flops at the sample's fp64 rate
+            "extrapolated_full_step_s": round(w.flops_fwd_bwd() / rate, 1)}
 
 
 # ------------------------------------------------------------------ main

@@ -69,3 +69,16 @@ def test_reference_arm_prints_one_contract_line():
     assert d["e2e"]["value"] == d["value"] and d["e2e"]["unit"] == d["unit"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert "workload" in d["config"]
+
+
+def test_cpu_baseline_states_its_extrapolation():
+    """The oracle's timed sample is a few token rows; the whole step's time
+    it implies is reported beside it, labelled as an extrapolation."""
+    import bench
+    from tensor_transformer_mlp_forward_gb300 import inputs
+
+    w = inputs.WORKLOADS["tiny"]
+    cb = bench.cpu_baseline(w, inputs.make_inputs(w), budget_s=0.0)
+    assert cb["kind"] == "oracle" and cb["value"] > 0
+    want = w.flops_fwd_bwd() / (cb["value"] * 1e12)
+    assert abs(cb["extrapolated_full_step_s"] - want) <= 0.05 + 1e-3 * want
