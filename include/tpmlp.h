@@ -149,7 +149,10 @@ int tp_mlp_column_gelu(const tpmlp_bf16* X, const tpmlp_bf16* A, const tpmlp_bf1
  * aligned, tp_mlp_split_workspace_bytes bytes; may be NULL) allows, each
  * tile's k range -- the shards in order -- is cut into contiguous runs whose
  * fp32 partial sums go to the workspace, and a second kernel adds them in
- * run order with b2 and the residual (two launches instead of one). */
+ * run order with b2 and the residual (two launches instead of one).  When
+ * the tiles fill more than one round of the CTA pairs but the last round
+ * only partly (CTA pairs only; the tail split), the whole rounds run as
+ * usual and only the last round's tiles are cut that way (three launches). */
 int tp_mlp_row_sum(const tpmlp_bf16* H, const tpmlp_bf16* B, const tpmlp_bf16* b2,
                    const tpmlp_bf16* residual, int T, int h, int F, int t, tpmlp_bf16* Y,
                    void* workspace, size_t workspace_bytes, void* stream);
@@ -511,12 +514,14 @@ int tp_attn_backward(const tpmlp_bf16* dY, const tpmlp_bf16* X, const tpmlp_bf16
  * previous mode, or -1 for an invalid mode):
  *   0  single-CTA kernel (128 x 256 output tiles, one SM each);
  *   1  default: CTA pairs (cluster of 2, 256 x 256 tiles shared by two SMs
- *      through tcgen05 cta_group::2) when the problem has at least as many
- *      256 x 256 tiles as the GPU has SM pairs, else single CTAs;
+ *      through tcgen05 cta_group::2) when the problem has at least 32
+ *      256 x 256 tiles, else single CTAs;
  *   2  CTA pairs always.
  * Both kernels compute the same sums in the same order (the split of a
  * reduction does not depend on the mode), so results are bitwise identical
- * across modes. */
+ * across modes -- except where a row-parallel GEMM takes the tail split,
+ * which only CTA pairs do: the tiles of its last partly full round are
+ * summed in k ranges (see tp_mlp_row_sum). */
 int tpmlp_set_cta_pair_mode(int mode);
 
 /* How many epilogue warps the dZ GEMM (step a5, the one GEMM kernel with

@@ -254,8 +254,18 @@ int operand_map(CUtensorMap* m, const Operand& o, int t, int tile_rows, int* mn4
     return make_map(m, o.ptr, o.rows, o.cols, t, o.on, o.mn_major ? BK : tile_rows, o.ld);
 }
 
-// 0: single-CTA kernel only, 1: CTA pairs when the problem fills them, 2: pairs always.
+// 0: single-CTA kernel only, 1: CTA pairs unless the problem has very few
+// tiles, 2: pairs always.
 std::atomic<int> g_pair_mode{1};
+
+// A pair loads half of each B tile per SM and keeps six stages in flight
+// against a single CTA's four, which pays even when the pairs are fewer than
+// the GPU's SM pairs: the row-parallel GEMMs of 64 tiles at T = 1024,
+// h = 4096 ran 11-16 % faster on 64 pairs than on 128 single CTAs, and the
+// 64-tile weight gradients of the GPT-2-medium block 6-11 %.  Below this
+// many 256 x 256 tiles the single CTA's 128-row tiles occupy twice as many
+// SMs, which the launch-bound calls of small blocks prefer.
+constexpr int kPairMinTiles = 32;
 // Epilogue warps of the dZ GEMM (the one GEMM with both forms): 0 = by the
 // reduction's length (epi_warps_for), 4 or 8 = always that form.
 std::atomic<int> g_epi_mode{0};
@@ -455,7 +465,7 @@ int run_gemm(Launcher fn, const Operand& a, const Operand& b, const Output& out,
     const int pair_mode = g_pair_mode.load(std::memory_order_relaxed);
     GemmArgs probe = g;
     tile_space(probe, sh.M, sh.N, sh.K, sh.t, sh.mode, sh.a_bytes, sh.b_bytes, 2 * BM);
-    const bool pair = pair_mode == 2 || (pair_mode == 1 && probe.num_tiles >= dev.sms / 2);
+    const bool pair = pair_mode == 2 || (pair_mode == 1 && probe.num_tiles >= kPairMinTiles);
     const int tile_m = pair ? 2 * BM : BM;
     // When every shard boundary falls on a tile boundary (SHARD_N, SHARD_M)
     // or a k-block boundary (SHARD_K), the shards are runs of whole tiles of
