@@ -725,10 +725,14 @@ __global__ void __launch_bounds__(32 * (EW + 2), 1)
                 const int c = cb0 + cc;
                 const int n64 = tc.n0 + c * 64;
                 uint32_t buf0, buf1;
-                if constexpr (EPI == EPI_BIAS_GELU) {  // Z and H: both buffers
+                if constexpr (EPI == EPI_BIAS_GELU) {
+                    // Z in buffer 0, H in buffer 1, each block's two stores
+                    // committed as two groups (Z first): here only Z's store
+                    // must have read its buffer; H's may still be reading
+                    // until the first H row of this block is staged
                     buf0 = buf_base;
                     buf1 = buf_base + EPI_BUF_BYTES;
-                    if (lane == 0) bulk_wait_group_read<0>();
+                    if (lane == 0) bulk_wait_group_read<1>();
                 } else {
                     buf0 = buf_base + (seq & 1u) * EPI_BUF_BYTES;
                     buf1 = buf0;
@@ -790,6 +794,10 @@ __global__ void __launch_bounds__(32 * (EW + 2), 1)
                         if (!p.skip_o0) stage_row(buf0 + my_row, half, swz, v);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = gelu_tanh(v[i]);
+                        if (half == 0) {
+                            if (lane == 0) bulk_wait_group_read<0>();  // the previous H store
+                            __syncwarp();
+                        }
                         stage_row(buf1 + my_row, half, swz, v);
                     } else if constexpr (EPI == EPI_BIAS_RESIDUAL) {
                         if (valid > 0) {
@@ -866,9 +874,14 @@ __global__ void __launch_bounds__(32 * (EW + 2), 1)
                     if (lane == 0) {
                         int c0, c1, c2;
                         tma_coords(p.o_on, n64, row0, tc.s, c0, c1, c2);
-                        if (EPI != EPI_BIAS_GELU || !p.skip_o0) tma_store_3d(&tmO0, buf0, c0, c1, c2);
-                        if constexpr (EPI == EPI_BIAS_GELU) tma_store_3d(&tmO1, buf1, c0, c1, c2);
-                        bulk_commit_group();
+                        if (EPI != EPI_BIAS_GELU || !p.skip_o0) {
+                            tma_store_3d(&tmO0, buf0, c0, c1, c2);
+                            bulk_commit_group();
+                        }
+                        if constexpr (EPI == EPI_BIAS_GELU) {
+                            tma_store_3d(&tmO1, buf1, c0, c1, c2);
+                            bulk_commit_group();
+                        }
                     }
                     ++seq;
                 }
