@@ -103,7 +103,7 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
     }
 }
 
-// wait_bounded for a whole warp: lane 0 polls and the verdict is broadcast,
+// wait_bounded for a whole warp: lane 0 polls and the outcome is broadcast,
 // so the warp leaves its loops together (a lane-divergent exit would strand
 // the other lanes at the warp's next __syncwarp).  The closing __syncwarp
 // orders the other lanes' later reads after lane 0's observation.
