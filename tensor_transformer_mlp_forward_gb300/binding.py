@@ -175,8 +175,8 @@ def last_launch_count() -> int:
 
 
 def set_cta_pair_mode(mode: int) -> int:
-    """0 single-CTA GEMMs, 1 CTA pairs when the problem fills them (default),
-    2 CTA pairs always.  Returns the previous mode."""
+    """0 single-CTA GEMMs, 1 CTA pairs from 32 output tiles of 256 x 256 up
+    (default), 2 CTA pairs always.  Returns the previous mode."""
     prev = int(lib().tpmlp_set_cta_pair_mode(mode))
     if prev < 0:
         raise ValueError(f"invalid mode {mode}")
