@@ -45,7 +45,7 @@
  *    replayed beside eager calls, share no device state -- except the
  *    array of tp_mlp_bias_grad_noalloc, which its calls share (see there).
  *    Process-wide host state: the GEMM launch modes of
- *    tpmlp_set_cta_pair_mode, tpmlp_set_epilogue_warps,
+ *    tpmlp_set_cta_pair_mode, tpmlp_set_epilogue_warps, tpmlp_set_wide_tiles,
  *    tpmlp_set_dependent_launch and tpmlp_set_tile_scheduler (atomics, read at
  *    each launch: change them only
  *    while no other thread launches, or results stay equal but the launch
@@ -560,6 +560,18 @@ int tpmlp_set_dependent_launch(int mode);
  * Every mode computes every unit with the same sums: results are bitwise
  * identical across modes. */
 int tpmlp_set_tile_scheduler(int mode);
+
+/* Output tile of the GEMMs with K-major operands and a plain store (dX, and
+ * the weight gradients from transposed operands), process-wide; returns the
+ * previous mode, or -1 for a mode outside 0..1:
+ *   0  default: 256 x 256 per CTA pair;
+ *   1  256 x 512 per CTA pair where the reduction is not split: two N = 256
+ *      MMAs share each A stage, a quarter fewer operand bytes from L2 per
+ *      flop; TMEM holds one accumulator, so a tile's epilogue does not
+ *      overlap the next tile's MMAs.
+ * Each output element gets the same sums in the same order: results are
+ * bitwise identical across modes. */
+int tpmlp_set_wide_tiles(int mode);
 
 /* Static text for a status code. */
 const char* tp_mlp_status_string(int status);

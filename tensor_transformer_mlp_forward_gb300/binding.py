@@ -101,6 +101,7 @@ _SIGNATURES = {
     "tpmlp_set_epilogue_warps": ([_I], _I),
     "tpmlp_set_dependent_launch": ([_I], _I),
     "tpmlp_set_tile_scheduler": ([_I], _I),
+    "tpmlp_set_wide_tiles": ([_I], _I),
 }
 
 
@@ -197,6 +198,16 @@ def set_dependent_launch(mode: int) -> int:
     them: bit 0 the GEMMs, bit 1 the others (3, the default: both; 0: plain
     stream order).  Returns the previous mode."""
     prev = int(lib().tpmlp_set_dependent_launch(mode))
+    if prev < 0:
+        raise ValueError(f"invalid mode {mode}")
+    return prev
+
+
+def set_wide_tiles(mode: int) -> int:
+    """0: 256 x 256 GEMM tiles per CTA pair (default); 1: 256 x 512 for the
+    K-major plain-store GEMMs whose reduction is not split.  Returns the
+    previous mode."""
+    prev = int(lib().tpmlp_set_wide_tiles(mode))
     if prev < 0:
         raise ValueError(f"invalid mode {mode}")
     return prev

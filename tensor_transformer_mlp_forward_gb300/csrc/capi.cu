@@ -280,6 +280,10 @@ std::atomic<int> g_dependent_launch{3};
 // long reductions only (dynamic_units_for).
 std::atomic<int> g_tile_scheduler{2};
 
+// 0: 256 x 256 tiles per CTA pair; 1: 256 x 512 tiles for the K-major
+// plain-store GEMMs (dX) where no split of the reduction applies.
+std::atomic<int> g_wide_tiles{0};
+
 // A pair that has to wait for the answer to its request for the next unit
 // loses that time on every tile; over a long reduction (a tile of 192 or
 // more k-blocks, 100 us and up) it is nothing, while keeping the tiles in
@@ -326,13 +330,14 @@ long long K_total_of(const GemmArgs&, int K, int t, int mode) {
 
 // Fills the tile space of a GEMM with output extent M x N per shard.
 void tile_space(GemmArgs& g, int M, int N, int K, int t, int mode, long long a_bytes,
-                long long b_bytes, int tile_m) {
+                long long b_bytes, int tile_m, int tile_n = BN) {
     g.M = M;
     g.N = N;
     g.shards = t;
     g.shard_mode = mode;
     g.m_tiles = static_cast<int>(cdiv(M, tile_m));
-    g.n_tiles = static_cast<int>(cdiv(N, BN));
+    g.n_tiles = static_cast<int>(cdiv(N, tile_n));
+    g.tile_n = tile_n;
     g.mt_total = g.m_tiles * (mode == SHARD_M ? t : 1);
     g.nt_total = g.n_tiles * (mode == SHARD_N ? t : 1);
     g.k_blocks = static_cast<int>(cdiv(K, BK));
@@ -347,7 +352,7 @@ void tile_space(GemmArgs& g, int M, int N, int K, int t, int mode, long long a_b
     // an L2-sized working set.  With a long reduction the concurrent tiles
     // walk K together and share each k-slab, so one band spans everything.
     const int fast_tiles = g.raster_m_fastest ? g.mt_total : g.nt_total;
-    const long long panel = 2LL * (g.raster_m_fastest ? tile_m : BN) * K_total_of(g, K, t, mode);
+    const long long panel = 2LL * (g.raster_m_fastest ? tile_m : tile_n) * K_total_of(g, K, t, mode);
     g.band = fast_tiles;
     if (panel <= kBandMaxPanelBytes && panel * fast_tiles > kBandBudgetBytes)
         g.band = static_cast<int>(std::max<long long>(1, kBandBudgetBytes / panel));
@@ -467,13 +472,16 @@ int run_gemm(Launcher fn, const Operand& a, const Operand& b, const Output& out,
     tile_space(probe, sh.M, sh.N, sh.K, sh.t, sh.mode, sh.a_bytes, sh.b_bytes, 2 * BM);
     const bool pair = pair_mode == 2 || (pair_mode == 1 && probe.num_tiles >= kPairMinTiles);
     const int tile_m = pair ? 2 * BM : BM;
+    const bool wide = pair && fn == launch_dx && out.k_splits <= 1 &&
+                      g_wide_tiles.load(std::memory_order_relaxed) == 1;
+    const int tile_n = wide ? 2 * BN : BN;
     // When every shard boundary falls on a tile boundary (SHARD_N, SHARD_M)
     // or a k-block boundary (SHARD_K), the shards are runs of whole tiles of
     // the unsharded problem, visited in the same order: run it unsharded.
     GemmShape f = sh;
     Operand fa = a, fb = b;
     if (sh.t > 1 && ((sh.mode == SHARD_K && sh.K % BK == 0) ||
-                     (sh.mode == SHARD_N && sh.N % BN == 0) ||
+                     (sh.mode == SHARD_N && sh.N % tile_n == 0) ||
                      (sh.mode == SHARD_M && sh.M % tile_m == 0))) {
         if (sh.mode == SHARD_K) f.K = sh.K * sh.t;
         if (sh.mode == SHARD_N) f.N = sh.N * sh.t;
@@ -497,7 +505,7 @@ int run_gemm(Launcher fn, const Operand& a, const Operand& b, const Output& out,
         o_t = f.t;
         g.o_on = f.mode == SHARD_N ? ON_CONTIG : ON_ROWS;
     }
-    tile_space(g, f.M, f.N, f.K, f.t, f.mode, f.a_bytes, f.b_bytes, tile_m);
+    tile_space(g, f.M, f.N, f.K, f.t, f.mode, f.a_bytes, f.b_bytes, tile_m, tile_n);
     if (g.num_tiles == 0) return TPMLP_OK;
     g.epi_warps = epi_warps_for(1LL * g.k_blocks * (f.mode == SHARD_K ? f.t : 1));
     g.dependent_launch = g_dependent_launch.load(std::memory_order_relaxed) & 1;
@@ -509,7 +517,7 @@ int run_gemm(Launcher fn, const Operand& a, const Operand& b, const Output& out,
     alignas(64) GemmMaps maps;
     int rc = operand_map(&maps.a, fa, f.t, BM, &g.a_mn4);
     if (rc) return rc;
-    rc = operand_map(&maps.b, fb, f.t, pair ? BN / 2 : BN, &g.b_mn4);
+    rc = operand_map(&maps.b, fb, f.t, pair ? tile_n / 2 : BN, &g.b_mn4);
     if (rc) return rc;
     if (out.k_splits > 1)
         rc = make_partial_map(&maps.o0, out.ptr0, out.rows, out.cols, out.k_splits);
@@ -521,7 +529,7 @@ int run_gemm(Launcher fn, const Operand& a, const Operand& b, const Output& out,
     g.status = dev.status;
     const int units = pair ? std::max(1, dev.sms / 2) : dev.sms;
     TailPlan plan{g.num_tiles, 0, 1};
-    if (tail != nullptr && pair && out.k_splits <= 1 && tail->ws != nullptr)
+    if (tail != nullptr && pair && !wide && out.k_splits <= 1 && tail->ws != nullptr)
         plan = plan_tail(g.num_tiles, 1LL * g.k_blocks * (f.mode == SHARD_K ? f.t : 1), units,
                          static_cast<long long>(tail->ws_bytes / sizeof(float)), dev.pair_flops_per_ns,
                          dev.dram_bytes_per_ns);
@@ -1953,6 +1961,11 @@ TPMLP_API int tpmlp_set_dependent_launch(int mode) {
 TPMLP_API int tpmlp_set_tile_scheduler(int mode) {
     if (mode < 0 || mode > 2) return -1;
     return g_tile_scheduler.exchange(mode);
+}
+
+TPMLP_API int tpmlp_set_wide_tiles(int mode) {
+    if (mode < 0 || mode > 1) return -1;
+    return g_wide_tiles.exchange(mode);
 }
 
 TPMLP_API int tpmlp_set_epilogue_warps(int mode) {

@@ -68,13 +68,21 @@ constexpr int EPI_BUF_BYTES = 32 * 128;
 // Per-variant geometry.  Single CTA: a 128 x 256 tile, stages of
 // A 128x64 + B 256x64 (48 KiB).  CTA pair (cluster of 2, cta_group::2): a
 // 256 x 256 tile, each CTA holding 128 rows of A and 128 rows of B per stage
-// (32 KiB).  EW epilogue warps with two staging buffers each; the stages
-// fill what is left of the 227 KiB of shared memory.
-template <bool PAIR, int EW = 4>
+// (32 KiB).  Wide pair (TN = 512): a 256 x 512 tile computed as two N = 256
+// MMAs that share the A stage, each CTA holding 128 rows of A and 256 of B
+// (48 KiB, four stages), the whole of TMEM one accumulator: a quarter fewer
+// operand bytes from L2 per flop, no second accumulator for the epilogue to
+// drain while the next tile runs.  EW epilogue warps with two staging
+// buffers each; the stages fill what is left of the 227 KiB of shared
+// memory.
+template <bool PAIR, int EW = 4, int TN = BN>
 struct Geometry {
+    static constexpr bool WIDE = TN == 2 * BN;
     static constexpr int TILE_M = PAIR ? 2 * BM : BM;
-    static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // B rows in this CTA's smem
-    static constexpr int STAGES = PAIR ? (EW == 8 ? 5 : 6) : (EW == 8 ? 3 : 4);
+    static constexpr int TILE_N = TN;
+    static constexpr int ACCS = WIDE ? 1 : 2;             // TMEM accumulators
+    static constexpr int B_ROWS = PAIR ? TN / 2 : BN;  // B rows in this CTA's smem
+    static constexpr int STAGES = WIDE ? 4 : PAIR ? (EW == 8 ? 5 : 6) : (EW == 8 ? 3 : 4);
     static constexpr int THREADS = 32 * (EW + 2);
     static constexpr int A_STAGE_BYTES = BM * BK * 2;
     static constexpr int B_STAGE_BYTES = B_ROWS * BK * 2;
@@ -82,6 +90,7 @@ struct Geometry {
     static constexpr int STAGING_BYTES = EW * 2 * EPI_BUF_BYTES;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STAGING_BYTES + BAR_BYTES;
     static_assert(EW == 4 || EW == 8, "four or eight epilogue warps");
+    static_assert(TN == BN || (PAIR && EW == 4 && TN == 2 * BN), "wide tiles: CTA pairs, 4 warps");
     static_assert(SMEM_BYTES <= 232448, "shared memory of one CTA");
 };
 
@@ -142,6 +151,7 @@ struct GemmArgs {
     // shard} (a_mn4 for A, b_mn4 for B): the operand's whole part of a
     // stage (ROWS / 64 atoms of 64 x BK) is one box.
     int a_mn4, b_mn4;
+    int tile_n;  // host side: output columns of a CTA pair's tile, BN or 2 BN (wide)
 };
 
 struct TileCoord {
@@ -150,7 +160,7 @@ struct TileCoord {
     int slot;  // the work unit's index in this launch
 };
 
-template <int TILE_M>
+template <int TILE_M, int TILE_N = BN>
 __device__ __forceinline__ TileCoord decode_tile(int tile, const GemmArgs& p) {
     // Work unit -> (split, output tile): the splits of one tile are
     // base_tiles apart, so each split sweeps the tiles in the order below.
@@ -190,7 +200,7 @@ __device__ __forceinline__ TileCoord decode_tile(int tile, const GemmArgs& p) {
         mi -= c.s * p.m_tiles;
     }
     c.m0 = mi * TILE_M;
-    c.n0 = ni * BN;
+    c.n0 = ni * TILE_N;
     return c;
 }
 
@@ -372,14 +382,15 @@ __device__ __forceinline__ float warp_column_sums(float (&v)[32], int lane) {
 
 // --------------------------------------------------------------- the kernel
 
-template <bool A_MN, bool B_MN, int EPI, bool PAIR, int EW>
+template <bool A_MN, bool B_MN, int EPI, bool PAIR, int EW, int TN>
 __global__ void __launch_bounds__(32 * (EW + 2), 1)
     tcgen05_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmO0,  // output (Z for EPI_BIAS_GELU)
                         const __grid_constant__ CUtensorMap tmO1,  // H for EPI_BIAS_GELU
                         const GemmArgs p) {
-    using G = Geometry<PAIR, EW>;
+    using G = Geometry<PAIR, EW, TN>;
+    static_assert(!(G::WIDE && EPI == EPI_PARTIAL), "wide tiles store whole sums");
     constexpr int PRODUCER_WARP = EW, MMA_WARP = EW + 1;
     // Every CTA of this persistent grid is resident from the start, so the
     // next kernel on the stream may begin launching at once: its CTAs take
@@ -519,7 +530,7 @@ __global__ void __launch_bounds__(32 * (EW + 2), 1)
                     }
                     pending = i;
                 }
-                const TileCoord tc = decode_tile<G::TILE_M>(tile, p);
+                const TileCoord tc = decode_tile<G::TILE_M, G::TILE_N>(tile, p);
                 const int a_row0 = tc.m0 + static_cast<int>(rank) * BM;
                 const int b_row0 = tc.n0 + static_cast<int>(rank) * G::B_ROWS;
                 // this unit's k-blocks [kb_begin, kb_end) and where they start
@@ -588,8 +599,8 @@ __global__ void __launch_bounds__(32 * (EW + 2), 1)
             uint32_t phase = 0;
             int count = 0;
             for (int tile = unit; tile >= 0; ++count) {
-                const int acc = count & 1;
-                const uint32_t acc_phase = (count >> 1) & 1;
+                const int acc = G::ACCS == 2 ? (count & 1) : 0;
+                const uint32_t acc_phase = G::ACCS == 2 ? (count >> 1) & 1 : count & 1;
                 if (!wait_bounded<true>(&acc_empty[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
@@ -608,10 +619,16 @@ __global__ void __launch_bounds__(32 * (EW + 2), 1)
 #pragma unroll
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                         const uint32_t accum = (kb != kb_begin || kk != 0) ? 1u : 0u;
-                        if constexpr (PAIR)
+                        if constexpr (PAIR) {
                             tc_mma_f16_pair(d_tmem, ad + kk * desc_k_step<A_MN>(),
                                             bd + kk * desc_k_step<B_MN>(), idesc, accum);
-                        else
+                            // the second half of each CTA's B rows into
+                            // accumulator columns BN..2BN-1 (same A)
+                            if constexpr (G::WIDE)
+                                tc_mma_f16_pair(d_tmem + BN, ad + kk * desc_k_step<A_MN>(),
+                                                bd + (((BN / 2) * BK * 2) >> 4) + kk * desc_k_step<B_MN>(),
+                                                idesc, accum);
+                        } else
                             tc_mma_f16(d_tmem, ad + kk * desc_k_step<A_MN>(),
                                        bd + kk * desc_k_step<B_MN>(), idesc, accum);
                     }
@@ -652,8 +669,15 @@ __global__ void __launch_bounds__(32 * (EW + 2), 1)
         // shard).  Two buffers per warp let a block be written while the
         // previous one is still being stored.
         const int q = warp & 3;
-        constexpr int NBLK = BN / 64 / (EW / 4);
+        constexpr int NBLK = G::TILE_N / 64 / (EW / 4);
         const int cb0 = (warp >> 2) * NBLK;
+        // Output 64-column block of accumulator block c.  Wide tiles: MMA h
+        // (columns 256h..256h+255) reads B rows 128h..128h+127 of each CTA,
+        // and CTA r holds the tile's B rows 256r..256r+255, so accumulator
+        // blocks 2, 3 hold output blocks 4, 5 and 4, 5 hold 2, 3.
+        auto out_blk = [](int c) -> int {
+            return G::WIDE ? ((c & 1) | (((c >> 1) & 1) << 2) | (((c >> 2) & 1) << 1)) : c;
+        };
         const uint32_t release_bar =
             PAIR ? map_to_cta(smem_u32(&acc_empty[0]), 0) : smem_u32(&acc_empty[0]);
         const uint32_t buf_base = smem_u32(staging) + static_cast<uint32_t>(warp) * 2u * EPI_BUF_BYTES;
@@ -662,9 +686,9 @@ __global__ void __launch_bounds__(32 * (EW + 2), 1)
         uint32_t seq = 0;  // stores committed so far: selects the buffer
         int count = 0;
         for (int tile = unit; tile >= 0; ++count) {
-            const TileCoord tc = decode_tile<G::TILE_M>(tile, p);
-            const int acc = count & 1;
-            const uint32_t acc_phase = (count >> 1) & 1;
+            const TileCoord tc = decode_tile<G::TILE_M, G::TILE_N>(tile, p);
+            const int acc = G::ACCS == 2 ? (count & 1) : 0;
+            const uint32_t acc_phase = G::ACCS == 2 ? (count >> 1) & 1 : count & 1;
 
             const int m_cta = tc.m0 + static_cast<int>(rank) * BM;  // first row of this CTA
             const int row0 = m_cta + q * 32;                           // first row of this warp
@@ -682,11 +706,12 @@ __global__ void __launch_bounds__(32 * (EW + 2), 1)
             constexpr bool kBias = EPI == EPI_BIAS_GELU || EPI == EPI_BIAS_RESIDUAL || EPI == EPI_BIAS;
             uint4 aux_cur[4], aux_nxt[4], bias_cur[4], bias_nxt[4];
             if constexpr (kAux) {
-                const int v0 = row_ok ? min(32, p.N - (tc.n0 + cb0 * 64)) : 0;
-                load_raw32(p.aux + grow * p.ld_aux + gcol0 + cb0 * 64, v0, aux_cur);
+                const int v0 = row_ok ? min(32, p.N - (tc.n0 + out_blk(cb0) * 64)) : 0;
+                load_raw32(p.aux + grow * p.ld_aux + gcol0 + out_blk(cb0) * 64, v0, aux_cur);
             }
             if constexpr (kBias)  // the same 32 values for every lane (broadcast)
-                load_raw32(p.bias + gcol0 + cb0 * 64, min(32, p.N - (tc.n0 + cb0 * 64)), bias_cur);
+                load_raw32(p.bias + gcol0 + out_blk(cb0) * 64, min(32, p.N - (tc.n0 + out_blk(cb0) * 64)),
+                           bias_cur);
             if (!warp_wait_bounded<true>(&acc_full[acc], acc_phase, abort_flag, p.status)) break;
             tc_fence_after();
 
@@ -723,7 +748,7 @@ __global__ void __launch_bounds__(32 * (EW + 2), 1)
 #pragma unroll 1
             for (int cc = 0; cc < NBLK; ++cc) {
                 const int c = cb0 + cc;
-                const int n64 = tc.n0 + c * 64;
+                const int n64 = tc.n0 + out_blk(c) * 64;
                 uint32_t buf0, buf1;
                 if constexpr (EPI == EPI_BIAS_GELU) {
                     // Z in buffer 0, H in buffer 1, each block's two stores
@@ -764,22 +789,22 @@ __global__ void __launch_bounds__(32 * (EW + 2), 1)
                 for (int half = 0; half < 2; ++half) {
                     const int n = n64 + half * 32;
                     const bool more = cc * 64 + half * 32 + 32 < NBLK * 64;  // another block follows
+                    // tile column of the next 32-column chunk
+                    const int nxt = half == 0 ? out_blk(c) * 64 + 32 : (more ? out_blk(c + 1) * 64 : 0);
                     if constexpr (kAux) {
                         if (more) {
-                            const int vn = row_ok ? min(32, p.N - (n + 32)) : 0;
-                            load_raw32(p.aux + grow * p.ld_aux + gcol0 + c * 64 + half * 32 + 32, vn,
-                                       aux_nxt);
+                            const int vn = row_ok ? min(32, p.N - (tc.n0 + nxt)) : 0;
+                            load_raw32(p.aux + grow * p.ld_aux + gcol0 + nxt, vn, aux_nxt);
                         }
                     }
                     if constexpr (kBias) {
                         if (more)
-                            load_raw32(p.bias + gcol0 + c * 64 + half * 32 + 32, min(32, p.N - (n + 32)),
-                                       bias_nxt);
+                            load_raw32(p.bias + gcol0 + nxt, min(32, p.N - (tc.n0 + nxt)), bias_nxt);
                     }
                     const uint32_t(&r)[32] = r2[half];
                     const int cvalid = min(32, p.N - n);  // columns inside the shard
                     const int valid = row_ok ? cvalid : 0;
-                    const long long gcol = gcol0 + c * 64 + half * 32;
+                    const long long gcol = gcol0 + out_blk(c) * 64 + half * 32;
                     float v[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);

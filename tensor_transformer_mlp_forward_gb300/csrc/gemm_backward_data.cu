@@ -16,6 +16,8 @@ cudaError_t launch_dgelu(const GemmMaps& m, const GemmArgs& g, int grid,
 
 cudaError_t launch_dx(const GemmMaps& m, const GemmArgs& g, int grid,
                         bool pair, cudaStream_t st) {
+    if (pair && g.tile_n == 2 * BN)
+        return launch_gemm<false, false, EPI_STORE, true, 4, 2 * BN>(m, g, grid, st);
     if (pair) return launch_gemm<false, false, EPI_STORE, true>(m, g, grid, st);
     return launch_gemm<false, false, EPI_STORE, false>(m, g, grid, st);
 }

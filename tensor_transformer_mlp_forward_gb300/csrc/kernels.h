@@ -136,12 +136,12 @@ cudaError_t launch_attn_backward(const CUtensorMap& tm_qkv128, const CUtensorMap
 // persistent loop never waits for a second wave of CTAs; with dynamic units
 // (g.dynamic_tiles) it is one CTA (pair) per unit and the running ones take
 // over the launches of the others.
-template <bool A_MN, bool B_MN, int EPI, bool PAIR, int EW = 4>
+template <bool A_MN, bool B_MN, int EPI, bool PAIR, int EW = 4, int TN = BN>
 cudaError_t launch_gemm(const GemmMaps& m, const GemmArgs& g, int grid,
                         cudaStream_t st) {
-    auto kern = tcgen05_gemm_kernel<A_MN, B_MN, EPI, PAIR, EW>;
-    constexpr int smem = Geometry<PAIR, EW>::SMEM_BYTES;
-    constexpr int threads = Geometry<PAIR, EW>::THREADS;
+    auto kern = tcgen05_gemm_kernel<A_MN, B_MN, EPI, PAIR, EW, TN>;
+    constexpr int smem = Geometry<PAIR, EW, TN>::SMEM_BYTES;
+    constexpr int threads = Geometry<PAIR, EW, TN>::THREADS;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};

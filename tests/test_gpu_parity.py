@@ -203,6 +203,35 @@ def test_tile_scheduler_forms_agree_bitwise(w, pair):
         assert torch.equal(static[k], again[k]), k
 
 
+@pytest.mark.parametrize("T,h,F,t", [
+    (4096, 3072, 4096, 2),    # whole 256 x 512 tiles, shards folded into one k range
+    (1000, 1320, 2048, 8),    # ragged rows and columns (1320 = 2.6 wide tiles)
+    (2048, 2048, 16384, 4),   # a long reduction: dynamic tile assignment
+], ids=["whole", "ragged", "dynamic"])
+def test_wide_tiles_agree_bitwise(T, h, F, t):
+    """dX on 256 x 512 tiles per CTA pair (two N = 256 MMAs sharing each A
+    stage) gives the bits of the 256 x 256 form: every output element is the
+    same k-ordered sum, only the columns a pair covers change."""
+    w = inputs.custom(T=T, h=h, F=F, t=t, seed=33)
+    cpu = inputs.make_inputs(w, keys=("X", "A"))
+    A = cpu["A"].cuda()
+    dZ = torch.randn(T, F, device="cuda").mul_(0.5).to(torch.bfloat16)
+    empty = torch.empty(0, dtype=torch.uint8, device="cuda")  # no split, no tail split
+    prev = binding.set_wide_tiles(0)
+    try:
+        plain = binding.tp_mlp_dx(dZ, A, t, workspace=empty)
+        binding.set_wide_tiles(1)
+        wide = binding.tp_mlp_dx(dZ, A, t, workspace=empty)
+        assert binding.last_launch_count() == 1
+        again = binding.tp_mlp_dx(dZ, A, t, workspace=empty)
+    finally:
+        binding.set_wide_tiles(prev)
+    torch.cuda.synchronize()
+    assert binding.device_status() == 0
+    assert torch.equal(plain, wide)
+    assert torch.equal(plain, again)
+
+
 def test_split_reduction_matches_unsplit():
     """The row-parallel GEMMs with and without a split reduction (few output
     tiles: T=512, h=4096 gives 2 x 16 tiles) agree up to the bf16 rounding of
