@@ -224,3 +224,28 @@ def test_recompute_workspace(L):
     assert L.tp_mlp_backward_recompute(*bargs_nob1, P, bwd_need, N) == binding.TPMLP_ERR_NULL
     # Z may be NULL in a2 (H only), H may not
     assert L.tp_mlp_column_gelu(P, P, P, T, h, F, t, N, N, N) == binding.TPMLP_ERR_NULL
+
+
+def test_launch_mode_setters(L):
+    """The process-wide GEMM launch modes: each setter returns the previous
+    mode, rejects a mode outside its range with -1 (leaving the mode as it
+    was), and touches no device."""
+    cases = [  # setter, default, valid modes, invalid modes
+        (L.tpmlp_set_cta_pair_mode, 1, (0, 1, 2), (-1, 3)),
+        (L.tpmlp_set_epilogue_warps, 0, (0, 4, 8), (2, 16)),
+        (L.tpmlp_set_dependent_launch, 3, (0, 1, 2, 3), (-1, 4)),
+        (L.tpmlp_set_tile_scheduler, 2, (0, 1, 2), (-1, 3)),
+        (L.tpmlp_set_wide_tiles, 0, (0, 1), (-1, 2)),
+    ]
+    for setter, default, valid, invalid in cases:
+        prev = setter(default)
+        try:
+            for bad in invalid:
+                assert setter(bad) == -1
+            assert setter(default) == default  # unchanged by the rejected calls
+            last = default
+            for m in valid:
+                assert setter(m) == last
+                last = m
+        finally:
+            setter(prev)
