@@ -77,6 +77,8 @@ def parse_args(argv=None):
                    help="GEMM kernel: 0 single CTA, 1 auto (default), 2 CTA pairs")
     p.add_argument("--tile-scheduler", type=int, default=None,
                    help="GEMM tile assignment: 0 static persistent, 1 dynamic (cluster launch control)")
+    p.add_argument("--wide-tiles", type=int, default=None,
+                   help="1: 256 x 512 tiles per CTA pair for the K-major plain-store GEMMs (default 0)")
     p.add_argument("--call", choices=CALLS, default=None,
                    help="run ONE entry point --repeat times at --shape, holding only its operands "
                         "on the device (the command a profiler wraps to capture one kernel)")
@@ -610,6 +612,8 @@ def run_ours(args, w):
         binding.set_cta_pair_mode(args.pair_mode)
     if args.tile_scheduler is not None:
         binding.set_tile_scheduler(args.tile_scheduler)
+    if args.wide_tiles is not None:
+        binding.set_wide_tiles(args.wide_tiles)
     rank, world, local = init_distributed(args.gpus)
     step, dev_s, wall, per_call, clocks, launches, split = time_ours(
         w, args.steps, args.warmup, local, args.dropout, args.recompute)
@@ -663,6 +667,8 @@ def run_ours(args, w):
         "gemm_kernel": {0: "single CTA", 1: "auto", 2: "CTA pairs"}[
             args.pair_mode if args.pair_mode is not None else 1],
     }
+    if args.wide_tiles:
+        line["gemm_kernel"] += ", 256 x 512 tiles for dX"
     if args.recompute:  # the rebuilt a2 is a seventh GEMM of 2*T*h*F flops
         line["hardware_tflops"] = value * 14 / 12
     if not args.no_cpu_baseline and world == 1:
@@ -928,6 +934,8 @@ def run_call(a) -> int:
     p_drop = a.dropout if a.dropout > 0 else 0.1
     if a.tile_scheduler is not None:
         b.set_tile_scheduler(a.tile_scheduler)
+    if a.wide_tiles is not None:
+        b.set_wide_tiles(a.wide_tiles)
     dev = torch.device("cuda", 0)
     gen = torch.Generator(device=dev).manual_seed(1234)
 
